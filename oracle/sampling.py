@@ -1,0 +1,150 @@
+"""Oracle for the rejection-sampling half of the verify step (fp64).
+
+Follows quant67 "speculative decoding" section 3.1 (accept x_i with
+probability min(1, p_i(x_i)/q_i(x_i)); at the first rejection n resample from
+max(0, p_n - q_n) / sum(max(0, p_n - q_n)); if all K are accepted draw a bonus
+token from p_{K+1}) and "KV Cache + Speculative Decoding" sections 7.1-7.3
+and 7.6 (p = target, q = draft, per-position softmax with temperature, the
+bonus row is the last target row).
+
+Readings adopted where the pages leave a step open:
+  * p = softmax(target_logits / T) and q = softmax(draft_logits / T), or q as
+    given when the draft is passed as probabilities.
+  * Accept test in multiplicative form: accept x_i iff u_i * q_i(x_i) <
+    p_i(x_i). For q_i(x_i) > 0 this is u_i < min(1, p/q) (strict, as in the
+    demo's `rand < r`); for q_i(x_i) = 0 it accepts iff p_i(x_i) > 0. The
+    1e-9 guards of the demo code are numerical guards, not the definition.
+  * Each position carries two uniforms [u_i, v_i]; v_n drives the residual
+    draw at the first rejection n, v_{K+1} the bonus draw. u_{K+1} is unused.
+  * Inverse CDF in ascending token id with a strict test: y = min{y : C(y) >
+    v * C(V-1)}, C the running sum of the weights. Zero-weight tokens can never
+    be drawn. If rounding leaves no such y, the largest y with nonzero weight
+    is taken. If the residual mass is exactly 0 (impossible in exact
+    arithmetic, since a rejection has probability Z), the draw falls back to p_n.
+  * Output tokens: x_1 .. x_{n-1}, y, then -1 padding; num_accepted = n - 1
+    (0-based: n_rej accepted drafts precede the drawn token).
+"""
+import numpy as np
+
+
+def _np64(x):
+    import torch
+    if isinstance(x, torch.Tensor):
+        return x.detach().cpu().to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def softmax(logits, temperature=1.0):
+    """softmax(logits / T) over the last axis, fp64, max-subtracted."""
+    x = _np64(logits) / float(temperature)
+    x = x - x.max(axis=-1, keepdims=True)
+    e = np.exp(x)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def inverse_cdf(weights, v):
+    """Row-wise y = min{y : C(y) > v*Z} with C = running sum in ascending id.
+
+    weights: [N, V] nonnegative fp64; v: [N]. Returns (y, margin, Z) where
+    margin is the distance of v from the nearest edge of y's CDF interval,
+    as a fraction of Z (the ``CDF boundary'' distance).
+    """
+    C = np.cumsum(weights, axis=1)
+    Z = C[:, -1]
+    thr = np.asarray(v, dtype=np.float64) * Z
+    above = C > thr[:, None]
+    y = np.argmax(above, axis=1)
+    none = ~above.any(axis=1)
+    if none.any():   # rounding pushed v*Z to the top: largest y with weight
+        rev = np.argmax(weights[:, ::-1] > 0, axis=1)
+        y = np.where(none, weights.shape[1] - 1 - rev, y)
+    rows = np.arange(weights.shape[0])
+    c_hi = C[rows, y]
+    c_lo = np.where(y > 0, C[rows, np.maximum(y - 1, 0)], 0.0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        margin = np.minimum(thr - c_lo, c_hi - thr) / Z
+    return y, np.abs(margin), Z
+
+
+def rejection_sample(target_logits, draft, draft_tokens, uniforms,
+                     draft_is_probs=False, temperature=1.0):
+    """Verify one round for every sequence of the batch.
+
+    target_logits [B, K+1, V]; draft [B, K, V] (logits, or probabilities when
+    draft_is_probs); draft_tokens [B, K]; uniforms [B, K+1, 2].
+    Returns a dict with out_tokens [B, K+1] (-1 padded), num_accepted [B] and
+    diagnostics (p/q at the draft tokens, accept margins |u - p/q|, CDF margin,
+    per-row alpha, the sampled row index and its mass).
+    """
+    p = softmax(target_logits, temperature)                      # [B, K+1, V]
+    q = _np64(draft) if draft_is_probs else softmax(draft, temperature)
+    return verify_from_probs(p, q, draft_tokens, uniforms)
+
+
+def verify_from_probs(p, q, draft_tokens, uniforms):
+    """The accept / resample / bonus logic on given distributions.
+
+    p [B, K+1, V] target distributions, q [B, K, V] draft distributions.
+    """
+    p = _np64(p)
+    q = _np64(q)
+    x = _np64(draft_tokens).astype(np.int64)
+    uv = _np64(uniforms)
+    B, K1, V = p.shape
+    K = K1 - 1
+    bi = np.arange(B)
+
+    p_x = np.empty((B, K))
+    q_x = np.empty((B, K))
+    acc_margin = np.empty((B, K))
+    alive = np.ones(B, dtype=bool)
+    n_rej = np.full(B, K, dtype=np.int64)        # K means "all accepted"
+    for i in range(K):
+        p_x[:, i] = p[bi, i, x[:, i]]
+        q_x[:, i] = q[bi, i, x[:, i]]
+        u = uv[:, i, 0]
+        accept = u * q_x[:, i] < p_x[:, i]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ratio = np.where(q_x[:, i] > 0, p_x[:, i] / q_x[:, i], np.inf)
+        acc_margin[:, i] = np.abs(u - ratio)
+        newly = alive & ~accept
+        n_rej[newly] = i
+        alive &= accept
+
+    # weights of the row that is sampled: the residual max(0, p_n - q_n) at
+    # the first rejection n, the target row K+1 (index K) when all accepted
+    p_n = p[bi, n_rej]                                          # [B, V]
+    if K > 0:
+        q_n = q[bi, np.minimum(n_rej, K - 1)]
+        residual = np.maximum(0.0, p_n - q_n)
+        use_residual = (n_rej < K) & (residual.sum(axis=1) > 0.0)
+        w = np.where(use_residual[:, None], residual, p_n)
+    else:
+        w = p_n
+    v = uv[bi, n_rej, 1]
+    y, cdf_margin, Z = inverse_cdf(w, v)
+
+    col = np.arange(K + 1)[None, :]
+    x_pad = np.concatenate([x, np.zeros((B, 1), dtype=np.int64)], axis=1)
+    out = np.where(col < n_rej[:, None], x_pad, -1)
+    out = np.where(col == n_rej[:, None], y[:, None], out)
+    alpha = np.minimum(p[:, :K, :], q).sum(axis=2)
+    return {"out_tokens": out, "num_accepted": n_rej, "p_at_draft": p_x,
+            "q_at_draft": q_x, "accept_margin": acc_margin,
+            "cdf_margin": cdf_margin, "sampled_row": n_rej, "sampled_mass": Z,
+            "alpha": alpha}
+
+
+def rejection_sample_chunked(target_logits, draft, draft_tokens, uniforms,
+                             draft_is_probs=False, temperature=1.0, chunk=8,
+                             batch_indices=None):
+    """rejection_sample over groups of sequences (bounded host memory)."""
+    B = target_logits.shape[0]
+    idx = list(range(B)) if batch_indices is None else list(batch_indices)
+    parts = []
+    for s in range(0, len(idx), chunk):
+        sel = idx[s:s + chunk]
+        parts.append(rejection_sample(target_logits[sel], draft[sel],
+                                      draft_tokens[sel], uniforms[sel],
+                                      draft_is_probs, temperature))
+    return {k: np.concatenate([r[k] for r in parts]) for k in parts[0]}
