@@ -1,0 +1,256 @@
+"""Python binding of libspecverify (ctypes): argument marshalling only.
+
+Every operation runs in the library's CUDA kernels; this module checks that
+tensors are CUDA, contiguous and of the expected dtype, passes their device
+pointers and the current torch stream, allocates outputs / workspaces with
+torch when the caller gives none, and raises on a non-zero status. There is no
+CPU fallback: if the library is missing or CUDA is unavailable, calls raise.
+
+Entry points (names follow the C ABI in include/specverify.h):
+  kv_block_append     paged write of the K+1 new K/V rows
+  spec_verify_attn    paged GQA verify attention over the K+1 queries
+  spec_verify_sample  fused rejection sampling (accept / residual / bonus)
+  verify_step         the three in stream order (one verify round of one layer)
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SV_F32, SV_BF16, SV_F16, SV_FP8_E4M3 = 0, 1, 2, 3
+SV_SAMPLE_FORCE_EXACT = 1
+DEV_STATUS_BITS = {1: "BAD_SEQ_LEN", 2: "BAD_BLOCK", 4: "BAD_TOKEN", 8: "TIMEOUT", 16: "NONFINITE"}
+_STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
+           4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT"}
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("%s: %s" % (_STATUS.get(status, status), msg))
+        self.status = status
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("block_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64),
+                ("slot_stride", ctypes.c_int64)]
+
+
+def load_library(path: str = LIB_PATH):
+    """Load (not build) the shared library and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libspecverify.so is not built (%s): call "
+                           "speculative_verify_paged_gb300.build.build() first" % path)
+    lib = ctypes.CDLL(path)
+    P, I, Z, F, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_uint
+    LP = ctypes.POINTER(_Layout)
+    lib.sv_last_error_string.restype = ctypes.c_char_p
+    lib.sv_last_error_string.argtypes = []
+    lib.kv_block_append.restype = I
+    lib.kv_block_append.argtypes = [P, P, I, P, P, I, LP, P, P, P, I, P, I, I, I, I, I, I, P, P]
+    lib.spec_verify_attn_workspace_size.restype = Z
+    lib.spec_verify_attn_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.spec_verify_attn_workspace_size_ex.restype = Z
+    lib.spec_verify_attn_workspace_size_ex.argtypes = [I, I, I, I, I, I, I, I]
+    attn_args = [P, I, P, P, I, LP, P, P, P, I, P, I, I, I, I, I, I, I, F, P, I, P, Z, P]
+    lib.spec_verify_attn.restype = I
+    lib.spec_verify_attn.argtypes = attn_args + [P]
+    lib.spec_verify_attn_ex.restype = I
+    lib.spec_verify_attn_ex.argtypes = attn_args + [I, P]
+    lib.spec_verify_sample_workspace_size.restype = Z
+    lib.spec_verify_sample_workspace_size.argtypes = [I, I, I]
+    samp_args = [P, I, P, I, I, P, P, I, I, I, F, P, P, P, P, P, Z, P]
+    lib.spec_verify_sample.restype = I
+    lib.spec_verify_sample.argtypes = samp_args + [P]
+    lib.spec_verify_sample_ex.restype = I
+    lib.spec_verify_sample_ex.argtypes = samp_args + [U, P]
+    _lib = lib
+    return lib
+
+
+def _check(rc):
+    if rc != 0:
+        raise SpecVerifyError(rc, load_library().sv_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor, fp8: bool = False) -> int:
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float16:
+        return SV_F16
+    if t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return SV_FP8_E4M3
+    raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensor arguments must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+
+
+def _layout_arg(layout):
+    if layout is None:
+        return None
+    return ctypes.byref(_Layout(*[int(x) for x in layout]))
+
+
+# --------------------------------------------------------------- append ---
+
+def kv_block_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_scale=None,
+                    v_scale=None, block_size=16, layout=None, status=None):
+    """Write k_new/v_new [B, n_new, H_kv, d] at positions seq_lens-n_new .. seq_lens-1."""
+    lib = load_library()
+    _cuda(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, status)
+    B, n_new, H_kv, d = k_new.shape
+    num_blocks = k_cache.shape[0]
+    _check(lib.kv_block_append(_ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(k_cache),
+                               _ptr(v_cache), _dtype_code(k_cache), _layout_arg(layout),
+                               _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+                               block_table.shape[1], _ptr(seq_lens), B, n_new, H_kv, d, block_size,
+                               num_blocks, _ptr(status), _stream()))
+
+
+# ------------------------------------------------------------ attention ---
+
+def attn_workspace_size(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size=16,
+                        blocks_per_split=None):
+    lib = load_library()
+    if blocks_per_split is None:
+        return lib.spec_verify_attn_workspace_size(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq,
+                                                   block_size)
+    return lib.spec_verify_attn_workspace_size_ex(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq,
+                                                  block_size, blocks_per_split)
+
+
+def alloc_workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=None, k_scale=None,
+                     v_scale=None, block_size=16, out=None, workspace=None, status=None,
+                     blocks_per_split=None, layout=None, num_blocks=None, H_kv=None):
+    """Paged GQA verify attention. q [B, n_new, H_q, d]; caches [num_blocks, H_kv, bs, d],
+    or, with `layout` = (block, head, slot) strides in elements, flat views whose first
+    element is (block 0, head 0, slot 0) plus explicit num_blocks and H_kv."""
+    lib = load_library()
+    _cuda(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, out, workspace, status)
+    B, n_new, H_q, d = q.shape
+    if layout is None:
+        num_blocks_, H_kv = k_cache.shape[0], k_cache.shape[1]
+    else:
+        if H_kv is None or num_blocks is None:
+            raise ValueError("with an explicit layout pass num_blocks and H_kv")
+        num_blocks_ = num_blocks
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    max_blocks = block_table.shape[1]
+    need = attn_workspace_size(B, n_new, H_q, H_kv, d, max_blocks, block_size, blocks_per_split)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    args = [_ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache), _dtype_code(k_cache, True),
+            _layout_arg(layout), _ptr(k_scale), _ptr(v_scale), _ptr(block_table), max_blocks,
+            _ptr(seq_lens), B, n_new, H_q, H_kv, d, block_size, num_blocks_, float(softmax_scale),
+            _ptr(out), _dtype_code(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(status)]
+    if blocks_per_split is None:
+        _check(lib.spec_verify_attn(*args, _stream()))
+    else:
+        _check(lib.spec_verify_attn_ex(*args, int(blocks_per_split), _stream()))
+    return out
+
+
+# ------------------------------------------------------------- sampling ---
+
+def sample_workspace_size(B, K, V):
+    return load_library().spec_verify_sample_workspace_size(B, K, V)
+
+
+def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_probs=False,
+                       temperature=1.0, out_tokens=None, num_accepted=None, p_at_draft=None,
+                       q_at_draft=None, workspace=None, status=None, force_exact=False,
+                       want_probs=True):
+    """Rejection sampling of one verify round.
+
+    target_logits [B, K+1, V]; draft [B, K, V] logits (same dtype) or f32
+    probabilities; draft_tokens int32 [B, K]; uniforms f32 [B, K+1, 2].
+    Returns (out_tokens [B, K+1], num_accepted [B], p_at_draft, q_at_draft).
+    """
+    lib = load_library()
+    _cuda(target_logits, draft, draft_tokens, uniforms, out_tokens, num_accepted, p_at_draft,
+          q_at_draft, workspace, status)
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if want_probs and p_at_draft is None:
+        p_at_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if want_probs and q_at_draft is None:
+        q_at_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(sample_workspace_size(B, K, V), dev)
+    ddt = _dtype_code(draft) if draft is not None else SV_F32
+    args = [_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt, int(bool(draft_is_probs)),
+            _ptr(draft_tokens), _ptr(uniforms), B, K, V, float(temperature), _ptr(out_tokens),
+            _ptr(num_accepted), _ptr(p_at_draft), _ptr(q_at_draft), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(status)]
+    if force_exact:
+        _check(lib.spec_verify_sample_ex(*args, SV_SAMPLE_FORCE_EXACT, _stream()))
+    else:
+        _check(lib.spec_verify_sample(*args, _stream()))
+    return out_tokens, num_accepted, p_at_draft, q_at_draft
+
+
+# ----------------------------------------------------------- verify step ---
+
+def verify_step(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, target_logits, draft,
+                draft_tokens, uniforms, k_scale=None, v_scale=None, draft_is_probs=False,
+                temperature=1.0, softmax_scale=None, attn_out=None, attn_workspace=None,
+                sample_workspace=None, status=None):
+    """One verify round of one layer: append the K+1 new K/V rows, attend, sample.
+
+    Returns (attn_out, out_tokens, num_accepted). Rolling the cache back is the
+    caller's job: next round's length is seq_lens - (K+1) + num_accepted + 1.
+    """
+    kv_block_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale,
+                    status=status)
+    out = spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale, k_scale,
+                           v_scale, out=attn_out, workspace=attn_workspace, status=status)
+    toks, nacc, _, _ = spec_verify_sample(target_logits, draft, draft_tokens, uniforms,
+                                          draft_is_probs, temperature, workspace=sample_workspace,
+                                          status=status, want_probs=False)
+    return out, toks, nacc
+
+
+def build(verbose=False, force=False):
+    """Compile the CUDA library in-tree (sm_103a)."""
+    return _build.build(verbose=verbose, force=force)

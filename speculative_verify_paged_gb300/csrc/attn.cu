@@ -1,0 +1,868 @@
+// spec_verify_attn: paged GQA attention of the K+1 verify queries.
+//
+// What is computed ("KV Cache + Speculative Decoding" sections 5.2-5.3 and
+// 6.3): for sequence b, kv head g and query row r = j*G + hh (query position
+// j, head h = g*G + hh), out = softmax_t(scale * q . K_t) V_t over keys
+// t <= L_b - n_new + j, K_t / V_t read through the block table.
+//
+// Design (flash-decoding style split-KV, CS336 lecture 10 section 9.2):
+//   * one CTA per (split of the sequence's blocks, kv head, sequence); all
+//     (K+1)*G query rows of the GQA group are packed into 16-row tiles, so
+//     every K/V byte is read from HBM once per step;
+//   * a producer warp streams (block, head) K and V tiles with 4-D TMA
+//     tensor copies (128-byte swizzle) through a ring of shared-memory
+//     stages guarded by mbarriers; the block table is read by the producer;
+//   * consumer warps own (16-row tile, key group) pairs: QK^T and PV on the
+//     tensor cores (mma.sync m16n8k16, fp32 accumulate), online softmax in
+//     the log2 domain with quad shuffles, causal / length masking only on the
+//     tail blocks; fp8 e4m3 tiles are widened to f16 in shared memory by the
+//     warps that share them, k_scale folded into the score scale and v_scale
+//     into the output;
+//   * every (split, key group) writes an unnormalised partial (acc, m, l) and
+//     attn_merge_kernel combines them with the log-sum-exp rule
+//     m = max m_s, l = sum l_s 2^(m_s - m), O = sum acc_s 2^(m_s - m) / l.
+// A plain CUDA-core kernel covers fp32 caches and shapes outside the
+// tensor-core path (any d_head <= 256, any block size).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "sv_common.cuh"
+
+namespace sv {
+namespace {
+
+// ------------------------------------------------------------ constants ---
+constexpr int kD = 128;           // head dim of the tensor-core path
+constexpr int kBS = 16;           // block size of the tensor-core path
+constexpr int kNWK = 2;           // key groups = blocks per pipeline stage
+constexpr int kStages = 6;
+constexpr int kMaxRT = 4;         // up to 64 packed query rows
+constexpr int kQStride = kD * 2 + 16;   // bytes per staged Q row (padded)
+constexpr int kTcAutoBps = 64;
+constexpr int kGenAutoBps = 8;
+constexpr int kGenThreads = 128;
+constexpr int kGenKeys = 32;
+
+// ------------------------------------------------------ PTX: tensor core ---
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+// two e4m3 codes (low byte first) -> f16x2
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t out;
+  asm volatile("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(v));
+  return out;
+}
+
+// 4-D TMA tile copy into shared memory, completion on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Byte address of element (row, col) of a 16 x 128 16-bit tile stored as two
+// 16 x 64 boxes with the 128-byte swizzle (16-byte chunk ^= row % 8).
+__device__ __forceinline__ uint32_t swz16(uint32_t tile, int row, int col) {
+  const int box = col >> 6, c = col & 63;
+  return tile + box * 2048 + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + ((c & 7) << 1);
+}
+
+// ------------------------------------------------- tensor-core kernel -----
+struct TcParams {   // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tmk;
+  CUtensorMap tmv;
+  const void *q;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  float *ws_acc;   // [B][H_kv][S*kNWK][R][kD]
+  float *ws_ml;    // [B][H_kv][S*kNWK][R][2]
+  int32_t *status;
+  int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
+  int role[3];        // tensor-map dims 1..3 hold (0 = slot, 1 = kv head, 2 = block)
+  float scale_log2;   // softmax_scale * log2(e)
+};
+
+// TMA coordinates {d, dim1, dim2, dim3} of tile (kv head g, physical block)
+__device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, int (&c)[3]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) c[k] = P.role[k] == 0 ? 0 : (P.role[k] == 1 ? g : phys);
+}
+
+template <int RT, bool FP8>
+struct TcCfg {
+  static constexpr int kCompute = RT * kNWK;              // consumer warps
+  static constexpr int kThreads = 32 * (kCompute + 1);     // + producer warp
+  static constexpr int kTile = FP8 ? kBS * kD : kBS * kD * 2;   // one K or V tile in bytes
+  static constexpr int kStageBytes = kNWK * 2 * kTile;
+  static constexpr int kStageArea = kStages * kStageBytes;
+  static constexpr int kConvBytes = FP8 ? kNWK * 2 * 2 * (kBS * kD * 2) : 0;  // K,V f16 double-buffered
+  static constexpr int kQBytes = RT * 16 * kQStride;
+  static constexpr int kSmem = 1024 + kStageArea + kConvBytes + kQBytes;
+};
+
+template <int RT, bool FP8>
+__global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ TcParams P) {
+  using Cfg = TcCfg<RT, FP8>;
+  constexpr bool F16 = FP8;   // fp8 tiles are widened to f16; bf16 stays bf16
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_base = smem_u32(smem);
+  const uint32_t conv_base = stage_base + Cfg::kStageArea;
+  uint8_t *q_smem = smem + Cfg::kStageArea + Cfg::kConvBytes;
+
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * kBS) {
+    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int nblk = (L + kBS - 1) / kBS;
+  const int blk0 = s * P.bps;
+  if (blk0 >= nblk) return;                       // the merge never reads this split
+  const int blk1 = min(nblk, blk0 + P.bps);
+  const int n_iter = (blk1 - blk0 + kNWK - 1) / kNWK;
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(&full_bar[k], 1);
+      mbar_init(&empty_bar[k], Cfg::kCompute);
+    }
+    fence_mbarrier_init();
+  }
+  // stage Q rows of this GQA group (zero rows past R); fp8 path widens to f16
+  {
+    const int R = P.R;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(P.q);
+    for (int idx = tid; idx < RT * 16 * (kD / 8); idx += blockDim.x) {
+      const int r = idx / (kD / 8), c8 = idx % (kD / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const int j = r / P.G, hh = r % P.G;
+        const int64_t off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD + c8 * 8;
+        v = *reinterpret_cast<const uint4 *>(q + off);
+        if (F16) {
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
+            __half2 h = __floats2half2_rn(lo, hi);
+            w[k] = *reinterpret_cast<uint32_t *>(&h);
+          }
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      *reinterpret_cast<uint4 *>(q_smem + r * kQStride + c8 * 16) = v;
+    }
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer ---
+  if (warp == 0) {
+    if (lane == 0) {
+      const int32_t *table = P.block_table + (int64_t)b * P.max_blocks;
+      bool ok_wait = true;
+      for (int it = 0; it < n_iter; ++it) {
+        const int st = it % kStages;
+        if (it >= kStages && !mbar_wait(&empty_bar[st], ((it / kStages) & 1) ^ 1)) {
+          ok_wait = false;   // consumers stopped: issue nothing more
+          break;
+        }
+        const int nvalid = min(kNWK, blk1 - (blk0 + it * kNWK));
+        mbar_arrive_expect_tx(&full_bar[st], (uint32_t)(nvalid * 2 * Cfg::kTile));
+        for (int kk = 0; kk < nvalid; ++kk) {
+          int phys = table[blk0 + it * kNWK + kk];
+          if (phys < 0 || phys >= P.num_blocks) {
+            atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+            phys = 0;   // stay in bounds; the output of this sequence is flagged
+          }
+          const uint32_t kt = stage_base + st * Cfg::kStageBytes + kk * 2 * Cfg::kTile;
+          const uint32_t vt = kt + Cfg::kTile;
+          int c[3];
+          tile_coords(P, g, phys, c);
+          if (FP8) {
+            tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
+            tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
+          } else {
+            tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
+            tma_load_4d(kt + 2048, &P.tmk, 64, c[0], c[1], c[2], &full_bar[st]);
+            tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
+            tma_load_4d(vt + 2048, &P.tmv, 64, c[0], c[1], c[2], &full_bar[st]);
+          }
+        }
+      }
+      if (!ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers ---
+  const int cw = warp - 1;
+  const int rt = cw % RT, kg = cw / RT;
+  const int gq = lane >> 2, tq = lane & 3;
+
+  // Q A-fragments for the 8 k-steps of d = 128
+  uint32_t qa[8][4];
+  {
+    const uint32_t qb = smem_u32(q_smem);
+    const int mi = lane >> 3;
+    const int row = rt * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int col = ks * 16 + (mi >> 1) * 8;
+      ldsm_x4(qb + row * kQStride + col * 2, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+    }
+  }
+  float scale_log2 = P.scale_log2;
+  if (FP8) scale_log2 *= P.k_scale[g];
+  const int r_lo = rt * 16 + gq, r_hi = r_lo + 8;
+  // last visible absolute key position of the two rows of this thread
+  const int lim_lo = L - P.n_new + min(r_lo, P.R - 1) / P.G;
+  const int lim_hi = L - P.n_new + min(r_hi, P.R - 1) / P.G;
+
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  bool ok_wait = true;
+
+  for (int it = 0; it < n_iter; ++it) {
+    const int st = it % kStages;
+    // after a timed-out wait this warp stops waiting but keeps its place in
+    // every named barrier (it then computes on stale tiles; status reports it)
+    if (ok_wait && !mbar_wait(&full_bar[st], (it / kStages) & 1)) ok_wait = false;
+    const int lb = blk0 + it * kNWK + kg;           // logical block of this warp
+    const int nvalid_stage = min(kNWK, blk1 - (blk0 + it * kNWK));
+    uint32_t kt = stage_base + st * Cfg::kStageBytes + kg * 2 * Cfg::kTile;
+    uint32_t vt = kt + Cfg::kTile;
+    if (FP8) {
+      // widen this key group's K and V tiles to f16 (same swizzled layout);
+      // the RT warps of the key group share the work, then sync by name.
+      const uint32_t ck = conv_base + (kg * 2 + (it & 1)) * 2 * 4096;
+      const uint32_t cv = ck + 4096;
+      if (kg < nvalid_stage) {
+        for (int idx = rt * 32 + lane; idx < 2 * kBS * (kD / 16); idx += RT * 32) {
+          const int which = idx / (kBS * (kD / 16));
+          const int rem = idx % (kBS * (kD / 16));
+          const int row = rem / (kD / 16), ch = rem % (kD / 16);   // 16-byte chunk of 16 codes
+          const uint32_t src = (which ? vt : kt) + row * 128 + ((ch ^ (row & 7)) << 4);
+          uint4 raw;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                       : "r"(src));
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffff));
+            h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+          }
+          const uint32_t dst0 = swz16(which ? cv : ck, row, ch * 16);
+          const uint32_t dst1 = swz16(which ? cv : ck, row, ch * 16 + 8);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                       "r"(h[3]));
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst1), "r"(h[4]), "r"(h[5]), "r"(h[6]),
+                       "r"(h[7]));
+        }
+      }
+      named_bar_sync(1 + kg, RT * 32);
+      kt = ck;
+      vt = cv;
+      // the fp8 stage is no longer needed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+    if (lb < blk1) {
+      // ---- S = Q K^T for the 16 keys of block lb -------------------------
+      float sacc[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+      {
+        const int mi = lane >> 3;
+        const int key = (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(swz16(kt, key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+          mma16816<F16>(sacc[0], qa[ks], b0, b1);
+          mma16816<F16>(sacc[1], qa[ks], b2, b3);
+        }
+      }
+      // ---- masking (tail blocks only) and online softmax -------------------
+      const int t0 = lb * kBS;
+      const bool tail = t0 + kBS - 1 > L - P.n_new;
+      float x[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = t0 + n * 8 + 2 * tq + (e & 1);
+          const int lim = (e < 2) ? lim_lo : lim_hi;
+          const float v = sacc[n][e] * scale_log2;
+          x[n][e] = (!tail || t <= lim) ? v : -INFINITY;
+        }
+      }
+      float mx_lo = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx_hi = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+      const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+      const float a_lo = exp2f(m_lo - base_lo), a_hi = exp2f(m_hi - base_hi);
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      float p[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        p[n][0] = exp2f(x[n][0] - base_lo);
+        p[n][1] = exp2f(x[n][1] - base_lo);
+        p[n][2] = exp2f(x[n][2] - base_hi);
+        p[n][3] = exp2f(x[n][3] - base_hi);
+      }
+      l_lo = l_lo * a_lo + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+      l_hi = l_hi * a_hi + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= a_lo; o[n][1] *= a_lo;
+        o[n][2] *= a_hi; o[n][3] *= a_hi;
+      }
+      uint32_t pa[4];
+      pa[0] = pack2<F16>(p[0][0], p[0][1]);
+      pa[1] = pack2<F16>(p[0][2], p[0][3]);
+      pa[2] = pack2<F16>(p[1][0], p[1][1]);
+      pa[3] = pack2<F16>(p[1][2], p[1][3]);
+      // ---- O += P V ---------------------------------------------------------
+      // keys at or past L in the tail block may hold anything: zero them
+      const int nvk = L - t0;   // valid keys in this block (>= 16 unless tail)
+      const int k0 = 2 * tq;    // keys k0, k0+1 (b0) and k0+8, k0+9 (b1)
+      const uint32_t m0 = (k0 < nvk ? 0x0000ffffu : 0u) | (k0 + 1 < nvk ? 0xffff0000u : 0u);
+      const uint32_t m1 = (k0 + 8 < nvk ? 0x0000ffffu : 0u) | (k0 + 9 < nvk ? 0xffff0000u : 0u);
+      {
+        const int mi = lane >> 3;
+        const int key = (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(swz16(vt, key, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
+          if (nvk < kBS) {
+            b0 &= m0; b1 &= m1; b2 &= m0; b3 &= m1;
+          }
+          mma16816<F16>(o[2 * np], pa, b0, b1);
+          mma16816<F16>(o[2 * np + 1], pa, b2, b3);
+        }
+      }
+    }
+    if (!FP8) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+  }
+  if (!ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+
+  // ---- write this (split, key group) partial --------------------------------
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  const float vs = FP8 ? P.v_scale[g] : 1.f;
+  const int S2 = P.S * kNWK;
+  const int64_t ent = ((int64_t)b * P.H_kv + g) * S2 + (int64_t)s * kNWK + kg;
+  float *acc = P.ws_acc + ent * P.R * kD;
+  float *ml = P.ws_ml + ent * P.R * 2;
+#pragma unroll
+  for (int n = 0; n < 16; ++n) {
+    const int c = n * 8 + 2 * tq;
+    if (r_lo < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_lo * kD + c) = make_float2(o[n][0] * vs, o[n][1] * vs);
+    if (r_hi < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_hi * kD + c) = make_float2(o[n][2] * vs, o[n][3] * vs);
+  }
+  if (tq == 0) {
+    if (r_lo < P.R) { ml[r_lo * 2] = m_lo; ml[r_lo * 2 + 1] = l_lo; }
+    if (r_hi < P.R) { ml[r_hi * 2] = m_hi; ml[r_hi * 2 + 1] = l_hi; }
+  }
+}
+
+// ----------------------------------------------------- CUDA-core kernel ---
+struct GenParams {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  float *ws_acc;   // [B][H_kv][S][R][d]
+  float *ws_ml;    // [B][H_kv][S][R][2]
+  int32_t *status;
+  int B, n_new, H_q, H_kv, G, R, d, bs, max_blocks, num_blocks, bps, S;
+  int64_t block_stride, head_stride, slot_stride;
+  float scale_log2;
+};
+
+template <typename T>
+__device__ __forceinline__ float kv_value(const void *pool, int64_t off, float scale);
+template <>
+__device__ __forceinline__ float kv_value<float>(const void *pool, int64_t off, float) {
+  return static_cast<const float *>(pool)[off];
+}
+template <>
+__device__ __forceinline__ float kv_value<__nv_bfloat16>(const void *pool, int64_t off, float) {
+  return __bfloat162float(static_cast<const __nv_bfloat16 *>(pool)[off]);
+}
+template <>
+__device__ __forceinline__ float kv_value<uint8_t>(const void *pool, int64_t off, float scale) {
+  const uint8_t code = static_cast<const uint8_t *>(pool)[off];
+  const uint32_t h = e4m3x2_to_f16x2((uint16_t)code);
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffff))) * scale;
+}
+
+template <typename TKV, typename TQ>
+__global__ void __launch_bounds__(kGenThreads) attn_generic_kernel(const __grid_constant__ GenParams P) {
+  extern __shared__ float gsm[];
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = P.R, d = P.d;
+  float *q_s = gsm;                       // [R][d]
+  float *o_s = q_s + R * d;               // [R][d]
+  float *k_s = o_s + R * d;               // [kGenKeys][d]
+  float *v_s = k_s + kGenKeys * d;        // [kGenKeys][d]
+  float *p_s = v_s + kGenKeys * d;        // [R][kGenKeys]
+  float *m_s = p_s + R * kGenKeys;        // [R]
+  float *l_s = m_s + R;                   // [R]
+  float *c_s = l_s + R;                   // [R]
+
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * P.bs) {
+    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int nblk = (L + P.bs - 1) / P.bs;
+  const int blk0 = s * P.bps;
+  if (blk0 >= nblk) return;
+  const int t_begin = blk0 * P.bs, t_end = min(L, min(nblk, blk0 + P.bps) * P.bs);
+  const float ks = std::is_same<TKV, uint8_t>::value ? P.k_scale[g] : 1.f;
+  const float vsc = std::is_same<TKV, uint8_t>::value ? P.v_scale[g] : 1.f;
+
+  for (int idx = tid; idx < R * d; idx += blockDim.x) {
+    const int r = idx / d, c = idx % d;
+    const int j = r / P.G, hh = r % P.G;
+    const int64_t off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * d + c;
+    q_s[idx] = to_f32(static_cast<const TQ *>(P.q)[off]);
+    o_s[idx] = 0.f;
+  }
+  for (int r = tid; r < R; r += blockDim.x) { m_s[r] = -INFINITY; l_s[r] = 0.f; }
+  __syncthreads();
+  const int32_t *table = P.block_table + (int64_t)b * P.max_blocks;
+
+  for (int t0 = t_begin; t0 < t_end; t0 += kGenKeys) {
+    for (int idx = tid; idx < kGenKeys * d; idx += blockDim.x) {
+      const int kk = idx / d, c = idx % d;
+      const int t = t0 + kk;
+      float kv = 0.f, vv = 0.f;
+      if (t < t_end) {
+        int phys = table[t / P.bs];
+        if (phys < 0 || phys >= P.num_blocks) {
+          atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+        } else {
+          const int64_t off = (int64_t)phys * P.block_stride + (int64_t)g * P.head_stride +
+                              (int64_t)(t % P.bs) * P.slot_stride + c;
+          kv = kv_value<TKV>(P.k_cache, off, ks);
+          vv = kv_value<TKV>(P.v_cache, off, vsc);
+        }
+      }
+      k_s[idx] = kv;
+      v_s[idx] = vv;
+    }
+    __syncthreads();
+    for (int r = warp; r < R; r += blockDim.x / 32) {
+      const int t = t0 + lane;
+      const int lim = L - P.n_new + r / P.G;
+      float sc = -INFINITY;
+      if (t < t_end && t <= lim) {
+        float acc = 0.f;
+        for (int c = 0; c < d; ++c) acc = fmaf(q_s[r * d + c], k_s[lane * d + c], acc);
+        sc = acc * P.scale_log2;
+      }
+      const float mx = warp_max(sc);
+      const float m_old = m_s[r];
+      const float m_new = fmaxf(m_old, mx);
+      const float base = m_new == -INFINITY ? 0.f : m_new;
+      const float p = exp2f(sc - base);
+      const float sum = warp_sum(p);
+      p_s[r * kGenKeys + lane] = p;
+      __syncwarp();
+      if (lane == 0) {
+        const float a = exp2f(m_old - base);
+        c_s[r] = a;
+        l_s[r] = l_s[r] * a + sum;
+        m_s[r] = m_new;
+      }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < R * d; idx += blockDim.x) {
+      const int r = idx / d, c = idx % d;
+      float acc = o_s[idx] * c_s[r];
+      for (int kk = 0; kk < kGenKeys; ++kk) acc = fmaf(p_s[r * kGenKeys + kk], v_s[kk * d + c], acc);
+      o_s[idx] = acc;
+    }
+    __syncthreads();
+  }
+  const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
+  for (int idx = tid; idx < R * d; idx += blockDim.x) P.ws_acc[ent * R * d + idx] = o_s[idx];
+  for (int r = tid; r < R; r += blockDim.x) {
+    P.ws_ml[(ent * R + r) * 2] = m_s[r];
+    P.ws_ml[(ent * R + r) * 2 + 1] = l_s[r];
+  }
+}
+
+// ------------------------------------------------------------ LSE merge ---
+struct MergeParams {
+  const float *ws_acc;
+  const float *ws_ml;
+  const int32_t *seq_lens;
+  void *out;
+  int B, n_new, H_q, H_kv, G, R, d, bs, max_blocks, bps, S, per_split;
+};
+
+template <typename TO>
+__global__ void attn_merge_kernel(const __grid_constant__ MergeParams P) {
+  const int r = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * P.bs) return;
+  const int nblk = (L + P.bs - 1) / P.bs;
+  const int nsplit = (nblk + P.bps - 1) / P.bps;
+  const int S2 = P.S * P.per_split;
+  const int n_ent = nsplit * P.per_split;
+  const int64_t ent0 = ((int64_t)b * P.H_kv + g) * S2;
+  float m = -INFINITY;
+  for (int e = 0; e < n_ent; ++e) m = fmaxf(m, P.ws_ml[((ent0 + e) * P.R + r) * 2]);
+  const float base = m == -INFINITY ? 0.f : m;
+  float lsum = 0.f;
+  for (int e = 0; e < n_ent; ++e) {
+    const float me = P.ws_ml[((ent0 + e) * P.R + r) * 2];
+    lsum += P.ws_ml[((ent0 + e) * P.R + r) * 2 + 1] * exp2f(me - base);
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const int j = r / P.G, hh = r % P.G;
+  const int64_t out_off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * P.d;
+  for (int c = threadIdx.x; c < P.d; c += blockDim.x) {
+    float acc = 0.f;
+    for (int e = 0; e < n_ent; ++e) {
+      const float me = P.ws_ml[((ent0 + e) * P.R + r) * 2];
+      acc += P.ws_acc[((ent0 + e) * P.R + r) * P.d + c] * exp2f(me - base);
+    }
+    const float v = acc * inv;
+    if constexpr (std::is_same<TO, float>::value) static_cast<float *>(P.out)[out_off + c] = v;
+    else static_cast<__nv_bfloat16 *>(P.out)[out_off + c] = __float2bfloat16_rn(v);
+  }
+}
+
+// ------------------------------------------------------------------ host ---
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct Plan {
+  bool tc;
+  int R, S, bps, per_split, d;
+};
+
+Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int bs, sv_dtype kv, sv_dtype qd,
+               const sv_kv_layout *lay, int bps_req) {
+  Plan p;
+  p.R = n_new * (H_q / H_kv);
+  p.d = d;
+  const int es = dtype_bytes(kv);
+  bool strides_ok = true;
+  if (lay)
+    strides_ok = (lay->block_stride * es) % 16 == 0 && (lay->head_stride * es) % 16 == 0 &&
+                 (lay->slot_stride * es) % 16 == 0;
+  p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS && p.R <= 16 * kMaxRT &&
+         strides_ok;
+  p.bps = bps_req > 0 ? bps_req : (p.tc ? kTcAutoBps : kGenAutoBps);
+  p.S = (max_blocks + p.bps - 1) / p.bps;
+  p.per_split = p.tc ? kNWK : 1;
+  (void)B;
+  return p;
+}
+
+size_t ws_bytes(const Plan &p, int B, int H_kv) {
+  const size_t ent = (size_t)B * H_kv * p.S * p.per_split * p.R;
+  return align_up(ent * p.d * sizeof(float), 256) + align_up(ent * 2 * sizeof(float), 256);
+}
+
+template <int RT, bool FP8>
+sv_status launch_tc(const TcParams &P, cudaStream_t st) {
+  using Cfg = TcCfg<RT, FP8>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_tc_kernel<RT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::kSmem);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  dim3 grid(P.S, P.H_kv, P.B);
+  attn_tc_kernel<RT, FP8><<<grid, Cfg::kThreads, Cfg::kSmem, st>>>(P);
+  return check_launch("spec_verify_attn tensor-core launch");
+}
+
+template <typename TKV, typename TQ>
+sv_status launch_gen(const GenParams &P, cudaStream_t st) {
+  const size_t smem = sizeof(float) * ((size_t)2 * P.R * P.d + 2 * kGenKeys * P.d + (size_t)P.R * kGenKeys + 3 * P.R);
+  if (smem > 200 * 1024) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: (K+1)*G*d_head too large for the fp32 path");
+  cudaError_t e = cudaFuncSetAttribute(attn_generic_kernel<TKV, TQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  dim3 grid(P.S, P.H_kv, P.B);
+  attn_generic_kernel<TKV, TQ><<<grid, kGenThreads, smem, st>>>(P);
+  return check_launch("spec_verify_attn fp32 launch");
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache, const void *v_cache,
+                           sv_dtype kv_dtype, const sv_kv_layout *layout, const float *k_scale,
+                           const float *v_scale, const int32_t *block_table, int max_blocks_per_seq,
+                           const int32_t *seq_lens, int B, int n_new, int H_q, int H_kv, int d_head,
+                           int block_size, int num_blocks, float softmax_scale, void *out, sv_dtype out_dtype,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status, int bps_req,
+                           sv_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: null pointer argument");
+  if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || d_head < 1 || block_size < 1 || num_blocks < 1 ||
+      max_blocks_per_seq < 1)
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: bad sizes");
+  if (H_q % H_kv != 0) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: H_q %% H_kv != 0");
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: softmax_scale must be finite and > 0");
+  if (q_dtype != out_dtype) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: q and out dtypes must match");
+  if (kv_dtype == SV_F32 && q_dtype != SV_F32)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: fp32 caches take fp32 queries");
+  if ((kv_dtype == SV_BF16 || kv_dtype == SV_FP8_E4M3) && q_dtype != SV_BF16)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: bf16 / fp8 caches take bf16 queries");
+  if (kv_dtype == SV_F16) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: f16 caches are not supported");
+  if (kv_dtype == SV_FP8_E4M3 && (!k_scale || !v_scale))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: fp8 caches need k_scale and v_scale");
+  if (d_head > 256) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: d_head > 256");
+  if (B > 65535 || H_kv > 65535) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: B or H_kv too large");
+  if (layout && (layout->slot_stride < d_head || layout->head_stride < d_head || layout->block_stride < d_head))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: layout strides smaller than d_head");
+  const Plan plan = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, kv_dtype, q_dtype,
+                              layout, bps_req);
+  if (plan.R > 65535) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: too many query rows per kv head");
+  const size_t need = ws_bytes(plan, B, H_kv);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "spec_verify_attn: workspace needs %zu bytes", need);
+  if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_attn: workspace not 256-byte aligned");
+  if (B == 0) return ok();
+
+  const size_t ent = (size_t)B * H_kv * plan.S * plan.per_split * plan.R;
+  float *ws_acc = static_cast<float *>(workspace);
+  float *ws_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                           align_up(ent * d_head * sizeof(float), 256));
+  const int G = H_q / H_kv;
+  int64_t slot_stride = d_head, head_stride = (int64_t)block_size * d_head,
+          block_stride = (int64_t)H_kv * block_size * d_head;
+  if (layout) {
+    slot_stride = layout->slot_stride;
+    head_stride = layout->head_stride;
+    block_stride = layout->block_stride;
+  }
+  const float scale_log2 = (float)((double)softmax_scale * 1.4426950408889634074);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  sv_status rc;
+  if (plan.tc) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return fail(SV_ERR_CUDA, "spec_verify_attn: cuTensorMapEncodeTiled unavailable");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
+      return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cache pointers must be 16-byte aligned");
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    const bool fp8 = kv_dtype == SV_FP8_E4M3;
+    const int es = fp8 ? 1 : 2;
+    // outer dims ordered by increasing stride; the box is 16 slots x 1 x 1,
+    // so a tile always lands as 16 rows of d_head elements
+    const int64_t st_of[3] = {slot_stride, head_stride, block_stride};
+    const int64_t ext_of[3] = {block_size, H_kv, num_blocks};
+    int order[3] = {0, 1, 2};
+    std::sort(order, order + 3, [&](int x, int y) { return st_of[x] < st_of[y]; });
+    cuuint64_t dims[4] = {(cuuint64_t)d_head, 0, 0, 0};
+    cuuint64_t strides[3];
+    cuuint32_t box[4] = {(cuuint32_t)(fp8 ? 128 : 64), 1, 1, 1};
+    for (int k = 0; k < 3; ++k) {
+      dims[k + 1] = (cuuint64_t)ext_of[order[k]];
+      strides[k] = (cuuint64_t)(st_of[order[k]] * es);
+      box[k + 1] = order[k] == 0 ? (cuuint32_t)block_size : 1u;
+      P.role[k] = order[k];
+    }
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    for (int w = 0; w < 2; ++w) {
+      CUresult r = enc(w ? &P.tmv : &P.tmk, dt, 4, const_cast<void *>(w ? v_cache : k_cache), dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+    P.q = q; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
+    P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
+    P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
+    P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
+    P.scale_log2 = scale_log2;
+    const int RT = (plan.R + 15) / 16;
+    switch (RT * 2 + (fp8 ? 1 : 0)) {
+      case 2: rc = launch_tc<1, false>(P, st); break;
+      case 3: rc = launch_tc<1, true>(P, st); break;
+      case 4: rc = launch_tc<2, false>(P, st); break;
+      case 5: rc = launch_tc<2, true>(P, st); break;
+      case 6: rc = launch_tc<3, false>(P, st); break;
+      case 7: rc = launch_tc<3, true>(P, st); break;
+      case 8: rc = launch_tc<4, false>(P, st); break;
+      default: rc = launch_tc<4, true>(P, st); break;
+    }
+  } else {
+    GenParams P;
+    P.q = q; P.k_cache = k_cache; P.v_cache = v_cache; P.k_scale = k_scale; P.v_scale = v_scale;
+    P.block_table = block_table; P.seq_lens = seq_lens; P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
+    P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R; P.d = d_head; P.bs = block_size;
+    P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
+    P.block_stride = block_stride; P.head_stride = head_stride; P.slot_stride = slot_stride;
+    P.scale_log2 = scale_log2;
+    if (kv_dtype == SV_F32) rc = launch_gen<float, float>(P, st);
+    else if (kv_dtype == SV_BF16) rc = launch_gen<__nv_bfloat16, __nv_bfloat16>(P, st);
+    else rc = launch_gen<uint8_t, __nv_bfloat16>(P, st);
+  }
+  if (rc != SV_OK) return rc;
+  MergeParams M;
+  M.ws_acc = ws_acc; M.ws_ml = ws_ml; M.seq_lens = seq_lens; M.out = out;
+  M.B = B; M.n_new = n_new; M.H_q = H_q; M.H_kv = H_kv; M.G = G; M.R = plan.R; M.d = d_head; M.bs = block_size;
+  M.max_blocks = max_blocks_per_seq; M.bps = plan.bps; M.S = plan.S; M.per_split = plan.per_split;
+  dim3 grid(plan.R, H_kv, B);
+  if (out_dtype == SV_F32) attn_merge_kernel<float><<<grid, 128, 0, st>>>(M);
+  else attn_merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(M);
+  return check_launch("spec_verify_attn merge launch");
+}
+
+extern "C" size_t spec_verify_attn_workspace_size(int B, int n_new, int H_q, int H_kv, int d_head,
+                                                  int max_blocks_per_seq, int block_size) {
+  if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_head < 1 || max_blocks_per_seq < 1)
+    return 0;
+  // the tensor-core plan needs the most entries per split; size for it
+  Plan p = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_BF16, SV_BF16, nullptr, 0);
+  Plan g = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_F32, SV_F32, nullptr, 0);
+  return std::max(ws_bytes(p, B, H_kv), ws_bytes(g, B, H_kv));
+}
+
+extern "C" size_t spec_verify_attn_workspace_size_ex(int B, int n_new, int H_q, int H_kv, int d_head,
+                                                     int max_blocks_per_seq, int block_size,
+                                                     int blocks_per_split) {
+  if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_head < 1 || max_blocks_per_seq < 1)
+    return 0;
+  Plan p = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_BF16, SV_BF16, nullptr,
+                     blocks_per_split);
+  Plan g = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_F32, SV_F32, nullptr,
+                     blocks_per_split);
+  return std::max(ws_bytes(p, B, H_kv), ws_bytes(g, B, H_kv));
+}
+
+extern "C" sv_status spec_verify_attn(const void *q, sv_dtype q_dtype, const void *k_cache, const void *v_cache,
+                                      sv_dtype kv_dtype, const sv_kv_layout *layout, const float *k_scale,
+                                      const float *v_scale, const int32_t *block_table, int max_blocks_per_seq,
+                                      const int32_t *seq_lens, int B, int n_new, int H_q, int H_kv, int d_head,
+                                      int block_size, int num_blocks, float softmax_scale, void *out,
+                                      sv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, sv_stream_t stream) {
+  return attn_impl(q, q_dtype, k_cache, v_cache, kv_dtype, layout, k_scale, v_scale, block_table,
+                   max_blocks_per_seq, seq_lens, B, n_new, H_q, H_kv, d_head, block_size, num_blocks,
+                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, 0, stream);
+}
+
+extern "C" sv_status spec_verify_attn_ex(const void *q, sv_dtype q_dtype, const void *k_cache,
+                                         const void *v_cache, sv_dtype kv_dtype, const sv_kv_layout *layout,
+                                         const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                         int max_blocks_per_seq, const int32_t *seq_lens, int B, int n_new,
+                                         int H_q, int H_kv, int d_head, int block_size, int num_blocks,
+                                         float softmax_scale, void *out, sv_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_status, int blocks_per_split,
+                                         sv_stream_t stream) {
+  if (blocks_per_split < 1) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn_ex: blocks_per_split < 1");
+  return attn_impl(q, q_dtype, k_cache, v_cache, kv_dtype, layout, k_scale, v_scale, block_table,
+                   max_blocks_per_seq, seq_lens, B, n_new, H_q, H_kv, d_head, block_size, num_blocks,
+                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, blocks_per_split,
+                   stream);
+}

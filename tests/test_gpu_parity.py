@@ -1,0 +1,334 @@
+"""GPU vs oracle parity through the C ABI (the Python binding passes pointers).
+
+Small cases run the oracle on every output; the full-size workloads (the
+LLaMA-3-8B / 70B layer shapes, the 128K context, the high-batch fp8 shape)
+run in the launch configuration the benchmark times and compare sampled
+sequences with the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as oatt
+from oracle import kv_append as oapp
+from oracle import sampling as osamp
+from parity_utils import attn_tolerance, compare_sampling
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def to_dev(d):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def run_attention(lib, cfg, a, **kw):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = lib.spec_verify_attn(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"],
+                               1 / math.sqrt(cfg.d_head), a["k_scale"], a["v_scale"],
+                               block_size=cfg.block_size, status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+def oracle_attention(cfg, a, batch_indices=None):
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
+    return oatt.verify_attention(cpu["q"], cpu["k_cache"], cpu["v_cache"], cpu["block_table"],
+                                 cpu["seq_lens"], 1 / math.sqrt(cfg.d_head), cfg.block_size,
+                                 cfg.kv_dtype, cpu["k_scale"], cpu["v_scale"], batch_indices)
+
+
+def check_attention(out, ref, cfg, batch_indices=None):
+    idx = list(range(cfg.B)) if batch_indices is None else list(batch_indices)
+    got = out.float().cpu().numpy()[idx]
+    exp = ref[idx]
+    err = np.abs(got - exp).max()
+    assert np.isfinite(got).all()
+    assert err <= attn_tolerance(cfg.kv_dtype), "max abs error %.3g" % err
+    return err
+
+
+# ------------------------------------------------------------------ append ---
+
+@pytest.mark.parametrize("kv_dtype,new_dtype", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32"),
+                                               ("fp8_e4m3", "bf16"), ("fp8_e4m3", "f32")])
+def test_append_bit_exact(lib, kv_dtype, new_dtype):
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype=kv_dtype, q_dtype=new_dtype, B=5,
+                                          ctx=("fixed", (16, 17, 33, 64, 100)))
+    a = workloads.make_attention_inputs(cfg, seed=1)
+    n = workloads.make_append_inputs(cfg, seed=1)
+    g = to_dev({**a, **n})
+    kc, vc = g["k_cache"].clone(), g["v_cache"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.kv_block_append(g["k_new"], g["v_new"], kc, vc, g["block_table"], g["seq_lens"],
+                        g["k_scale"], g["v_scale"], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rk, rv = oapp.kv_block_append(a["k_cache"], a["v_cache"], n["k_new"], n["v_new"], a["block_table"],
+                                  a["seq_lens"], 16, kv_dtype, a["k_scale"], a["v_scale"])
+    assert torch.equal(kc.cpu(), rk)
+    assert torch.equal(vc.cpu(), rv)
+
+
+def test_append_full_size_70b(lib):
+    cfg = workloads.CONFIGS["llama3_70b"]
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=0, device=DEV))
+    n = workloads.make_append_inputs(cfg, seed=0, device=DEV)
+    kc, vc = a["k_cache"].clone(), a["v_cache"].clone()
+    lib.kv_block_append(n["k_new"], n["v_new"], kc, vc, a["block_table"], a["seq_lens"])
+    torch.cuda.synchronize()
+    lens = a["seq_lens"].cpu().tolist()
+    table = a["block_table"].cpu()
+    for b in (0, 17, 63):
+        for j in range(cfg.n_new):
+            pos = lens[b] - cfg.n_new + j
+            blk = int(table[b, pos // 16])
+            assert torch.equal(kc[blk, :, pos % 16], n["k_new"][b, j])
+            assert torch.equal(vc[blk, :, pos % 16], n["v_new"][b, j])
+
+
+# --------------------------------------------------------------- attention ---
+
+SMALL_ATTN = [
+    # name, overrides
+    ("tiny_f32", {}),
+    ("tiny_f32_mqa", {"H_q": 4, "H_kv": 1}),
+    ("tiny_f32_mha_long", {"H_q": 2, "H_kv": 2, "ctx": ("fixed", (300, 17))}),
+    ("tc_bf16", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128}),
+    ("tc_bf16_g8", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 16, "H_kv": 2,
+                    "ctx": ("fixed", (5, 700))}),
+    ("tc_bf16_rows64", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 16, "H_kv": 2,
+                        "K": 7, "ctx": ("fixed", (1000, 33))}),
+    ("tc_bf16_n1", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "K": 0,
+                    "ctx": ("fixed", (1, 250))}),
+    ("tc_fp8", {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 128, "H_q": 8, "H_kv": 2,
+                "K": 8, "ctx": ("fixed", (9, 517))}),
+    ("gen_bf16_d64", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 64}),
+    ("gen_fp8_d64", {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 64}),
+]
+
+
+@pytest.mark.parametrize("name,over", SMALL_ATTN, ids=[x[0] for x in SMALL_ATTN])
+def test_attention_small(lib, name, over):
+    cfg = workloads.CONFIGS["tiny"].with_(**over)
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=3))
+    out = run_attention(lib, cfg, a)
+    ref = oracle_attention(cfg, a)
+    check_attention(out, ref, cfg)
+
+
+@pytest.mark.parametrize("bps", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("kv", ["f32", "bf16", "fp8_e4m3"])
+def test_attention_split_count_invariance(lib, bps, kv):
+    q = "f32" if kv == "f32" else "bf16"
+    d = 64 if kv == "f32" else 128
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype=kv, q_dtype=q, d_head=d, ctx=("fixed", (77, 250)))
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=5))
+    base = run_attention(lib, cfg, a)
+    out = run_attention(lib, cfg, a, blocks_per_split=bps)
+    ref = oracle_attention(cfg, a)
+    check_attention(out, ref, cfg)
+    tol = {"f32": 1e-5, "bf16": 1e-2, "fp8_e4m3": 2e-2}[kv]
+    assert (out.float() - base.float()).abs().max().item() <= tol
+
+
+def test_attention_block_permutation_and_garbage_invariance(lib):
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128,
+                                          ctx=("fixed", (45, 130)), spare_blocks=6)
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=7))
+    out1 = run_attention(lib, cfg, a)
+    # move every block to a new physical slot and fill the freed ones with garbage
+    nb = a["num_blocks"]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(0)).to(DEV)
+    k2 = torch.empty_like(a["k_cache"])
+    v2 = torch.empty_like(a["v_cache"])
+    k2[perm] = a["k_cache"]
+    v2[perm] = a["v_cache"]
+    table2 = a["block_table"].clone()
+    m = table2 >= 0
+    table2[m] = perm[table2[m].long()].to(torch.int32)
+    a2 = dict(a, k_cache=k2, v_cache=v2, block_table=table2)
+    out2 = run_attention(lib, cfg, a2)
+    assert torch.equal(out1, out2)
+    # slots past each sequence's end (in its last block) hold NaN: no effect
+    k3, v3 = a["k_cache"].clone(), a["v_cache"].clone()
+    for b, L in enumerate(a["seq_lens"].tolist()):
+        if L % 16:
+            blk = int(a["block_table"][b, L // 16])
+            k3[blk, :, L % 16:] = float("nan")
+            v3[blk, :, L % 16:] = float("nan")
+    out3 = run_attention(lib, cfg, dict(a, k_cache=k3, v_cache=v3))
+    assert torch.equal(out1, out3)
+
+
+def test_attention_strided_pool_layout(lib):
+    """A per-layer slice of a [pages, 16, layers, 2, H_kv, d] pool, as the pages lay it out."""
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128)
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=9))
+    nb, H_kv, bs, d = a["k_cache"].shape
+    layers, layer = 3, 1
+    big = torch.randn(nb, bs, layers, 2, H_kv, d, device=DEV).to(torch.bfloat16)
+    big[:, :, layer, 0] = a["k_cache"].permute(0, 2, 1, 3)
+    big[:, :, layer, 1] = a["v_cache"].permute(0, 2, 1, 3)
+    kview = big[:, :, layer, 0]
+    vview = big[:, :, layer, 1]
+    strides = (bs * layers * 2 * H_kv * d, d, layers * 2 * H_kv * d)   # block, head, slot
+    k_base = big.view(-1)[kview.storage_offset():]
+    v_base = big.view(-1)[vview.storage_offset():]
+    out = lib.spec_verify_attn(a["q"], k_base, v_base, a["block_table"], a["seq_lens"],
+                               layout=strides, num_blocks=nb, H_kv=H_kv)
+    ref = run_attention(lib, cfg, a)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+FULL = ["llama3_8b", "llama3_70b", "long", "fp8"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_attention_full_size(lib, name):
+    cfg = workloads.CONFIGS[name]
+    a = workloads.make_attention_inputs(cfg, seed=0, device=DEV)
+    out = run_attention(lib, cfg, a)
+    B = cfg.B
+    sample = sorted(set([0, B - 1, B // 2, (7 * B) // 13]))
+    ref = oracle_attention(cfg, a, batch_indices=sample)
+    check_attention(out, ref, cfg, sample)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_attention_device_checks(lib):
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128)
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=1))
+    bad = a["block_table"].clone()
+    bad[0, 0] = 10_000
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.spec_verify_attn(a["q"], a["k_cache"], a["v_cache"], bad, a["seq_lens"], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+    status.zero_()
+    lens = a["seq_lens"].clone()
+    lens[1] = 10_000
+    lib.spec_verify_attn(a["q"], a["k_cache"], a["v_cache"], a["block_table"], lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1
+
+
+# ---------------------------------------------------------------- sampling ---
+
+def run_sampling(lib, s, force=False, probs=None, T=1.0):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    draft = s["draft_logits"] if probs is None else probs
+    res = lib.spec_verify_sample(s["target_logits"], draft, s["draft_tokens"], s["uniforms"],
+                                 draft_is_probs=probs is not None, temperature=T, status=status,
+                                 force_exact=force)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return [r.cpu().numpy() for r in res]
+
+
+def oracle_sampling(s, probs=None, T=1.0, batch_indices=None):
+    cpu = {k: v.cpu() for k, v in s.items()}
+    draft = cpu["draft_logits"] if probs is None else probs.cpu()
+    return osamp.rejection_sample_chunked(cpu["target_logits"], draft, cpu["draft_tokens"],
+                                          cpu["uniforms"], probs is not None, T,
+                                          batch_indices=batch_indices)
+
+
+def restrict(res, idx):
+    return [r[idx] for r in res]
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("logit_dtype", ["f32", "bf16"])
+def test_sampling_tiny(lib, seed, logit_dtype):
+    cfg = workloads.CONFIGS["tiny"].with_(B=64, ctx=("fixed", (64,) * 64), logit_dtype=logit_dtype)
+    s = to_dev(workloads.make_sampling_inputs(cfg, seed=seed))
+    tok, nac, p, q = run_sampling(lib, s)
+    ref = oracle_sampling(s)
+    compare_sampling(tok, nac, ref, p, q)
+    tok2, nac2, _, _ = run_sampling(lib, s, force=True)
+    compare_sampling(tok2, nac2, ref)
+
+
+@pytest.mark.parametrize("V", [1, 7, 33, 1001, 4099])
+@pytest.mark.parametrize("K", [0, 1, 3])
+def test_sampling_ragged_vocab_and_k(lib, V, K):
+    cfg = workloads.CONFIGS["tiny"].with_(B=16, ctx=("fixed", (64,) * 16), V=V, K=K, logit_dtype="bf16")
+    s = to_dev(workloads.make_sampling_inputs(cfg, seed=V + K))
+    ref = oracle_sampling(s)
+    for force in (False, True):
+        tok, nac, p, q = run_sampling(lib, s, force=force)
+        compare_sampling(tok, nac, ref, p if K else None, q if K else None)
+
+
+def test_sampling_draft_probs_and_temperature(lib):
+    cfg = workloads.CONFIGS["tiny"].with_(B=32, ctx=("fixed", (64,) * 32), V=5000)
+    s = to_dev(workloads.make_sampling_inputs(cfg, seed=11))
+    probs = torch.from_numpy(osamp.softmax(s["draft_logits"].cpu())).float().to(DEV)
+    tok, nac, p, q = run_sampling(lib, s, probs=probs)
+    compare_sampling(tok, nac, oracle_sampling(s, probs=probs), p, q)
+    for T in (0.7, 1.6):
+        tok, nac, p, q = run_sampling(lib, s, T=T)
+        compare_sampling(tok, nac, oracle_sampling(s, T=T), p, q)
+
+
+def test_sampling_q_equals_p_accepts_everything(lib):
+    cfg = workloads.CONFIGS["tiny"].with_(B=16, ctx=("fixed", (64,) * 16), V=3000, logit_dtype="bf16")
+    s = to_dev(workloads.make_sampling_inputs(cfg, seed=2))
+    s["draft_logits"] = s["target_logits"][:, :cfg.K].contiguous()
+    tok, nac, _, _ = run_sampling(lib, s)
+    assert (nac == cfg.K).all()
+    compare_sampling(tok, nac, oracle_sampling(s))
+
+
+def test_sampling_bad_token_flagged(lib):
+    cfg = workloads.CONFIGS["tiny"].with_(B=4, ctx=("fixed", (64,) * 4))
+    s = to_dev(workloads.make_sampling_inputs(cfg, seed=0))
+    s["draft_tokens"][1, 0] = cfg.V + 5
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.spec_verify_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"],
+                           status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 4
+
+
+SAMPLING_FULL = [("llama3_8b", None), ("llama3_70b", 0.5), ("llama3_70b", 1.5), ("llama3_70b", 3.0),
+                 ("long", None), ("fp8", None)]
+
+
+@pytest.mark.parametrize("name,sigma", SAMPLING_FULL)
+def test_sampling_full_size(lib, name, sigma):
+    cfg = workloads.CONFIGS[name]
+    s = workloads.make_sampling_inputs(cfg, seed=0, device=DEV, sigma=sigma)
+    tok, nac, p, q = run_sampling(lib, s)
+    idx = list(range(cfg.B)) if cfg.B <= 64 else list(range(0, cfg.B, 4))
+    ref = oracle_sampling(s, batch_indices=idx)
+    compare_sampling(tok[idx], nac[idx], ref, p[idx], q[idx])
+    # the exact-arithmetic resolution gives the same tokens
+    tok2, nac2, _, _ = run_sampling(lib, s, force=True)
+    compare_sampling(tok2[idx], nac2[idx], ref)
+
+
+def test_verify_step_end_to_end(lib):
+    import speculative_verify_paged_gb300 as sv
+    cfg = workloads.CONFIGS["llama3_8b"].with_(B=4, ctx=("fixed", (300, 4096, 77, 1000)), V=32000)
+    a = workloads.make_attention_inputs(cfg, seed=4)
+    n = workloads.make_append_inputs(cfg, seed=4)
+    s = workloads.make_sampling_inputs(cfg, seed=4)
+    g = to_dev({**a, **n, **s})
+    kc, vc = g["k_cache"].clone(), g["v_cache"].clone()
+    out, tok, nac = sv.verify_step(g["q"], g["k_new"], g["v_new"], kc, vc, g["block_table"],
+                                   g["seq_lens"], g["target_logits"], g["draft_logits"],
+                                   g["draft_tokens"], g["uniforms"])
+    torch.cuda.synchronize()
+    rk, rv = oapp.kv_block_append(a["k_cache"], a["v_cache"], n["k_new"], n["v_new"], a["block_table"],
+                                  a["seq_lens"], 16, "bf16")
+    ref = oatt.verify_attention(a["q"], rk, rv, a["block_table"], a["seq_lens"], 1 / math.sqrt(128))
+    assert np.abs(out.float().cpu().numpy() - ref).max() <= 2e-2
+    r = osamp.rejection_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"])
+    compare_sampling(tok.cpu().numpy(), nac.cpu().numpy(), r)

@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the
+header declares, sizes workspaces, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import speculative_verify_paged_gb300 as sv
+    sv.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^(?:const\s+)?(?:sv_status|size_t|char|void)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("kv_block_append", "spec_verify_attn", "spec_verify_sample", "sv_last_error_string",
+              "spec_verify_attn_workspace_size", "spec_verify_sample_workspace_size"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_workspace_sizes(lib):
+    # sampling: one 48-byte record per (sequence, position), 256-byte rounded
+    assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == 64 * 5 * 48 // 256 * 256 + (256 if 64 * 5 * 48 % 256 else 0)
+    assert lib.spec_verify_sample_workspace_size(0, 4, 10) == 0
+    s = lib.spec_verify_attn_workspace_size(64, 5, 64, 8, 128, 512, 16)
+    # (acc d + m + l) floats per (sequence, kv head, split entry, row)
+    entries = 64 * 8 * 8 * 2 * 40
+    assert s >= entries * (128 + 2) * 4
+    assert lib.spec_verify_attn_workspace_size(1, 5, 6, 4, 128, 8, 16) == 0   # H_q % H_kv
+
+
+def test_host_validation_errors(lib):
+    import speculative_verify_paged_gb300 as sv
+    NULL = None
+    # kv_block_append: null pointers
+    rc = lib.kv_block_append(NULL, NULL, 1, NULL, NULL, 1, None, NULL, NULL, NULL, 4, NULL,
+                             2, 5, 2, 128, 16, 10, NULL, NULL)
+    assert rc == 1
+    assert b"null" in lib.sv_last_error_string()
+    # attention: H_q not a multiple of H_kv (pointers are never dereferenced)
+    fake = ctypes.c_void_p(0x1000)
+    rc = lib.spec_verify_attn(fake, 1, fake, fake, 1, None, NULL, NULL, fake, 4, fake,
+                              2, 5, 6, 4, 128, 16, 10, 0.1, fake, 1, fake, 1 << 30, NULL, NULL)
+    assert rc == 1 and b"H_q" in lib.sv_last_error_string()
+    # attention: workspace too small
+    rc = lib.spec_verify_attn(fake, 1, fake, fake, 1, None, NULL, NULL, fake, 4, fake,
+                              2, 5, 8, 2, 128, 16, 10, 0.1, fake, 1, fake, 16, NULL, NULL)
+    assert rc == 3
+    # attention: unsupported dtype pairing
+    rc = lib.spec_verify_attn(fake, 0, fake, fake, 1, None, NULL, NULL, fake, 4, fake,
+                              2, 5, 8, 2, 128, 16, 10, 0.1, fake, 0, fake, 1 << 30, NULL, NULL)
+    assert rc == 2
+    # sampling: bad temperature, bad sizes, draft dtype mismatch, small workspace
+    args = lambda T, B, K, V, ddt, ws: (fake, 1, fake, ddt, 0, fake, fake, B, K, V, T, fake, fake,
+                                        NULL, NULL, fake, ws, NULL, NULL)
+    assert lib.spec_verify_sample(*args(0.0, 2, 4, 100, 1, 1 << 20)) == 1
+    assert lib.spec_verify_sample(*args(1.0, 2, 4, 0, 1, 1 << 20)) == 1
+    assert lib.spec_verify_sample(*args(1.0, 2, 4, 100, 0, 1 << 20)) == 2
+    assert lib.spec_verify_sample(*args(1.0, 2, 4, 100, 1, 16)) == 3
+    # a good call leaves the error string empty only after success; the
+    # message of the last failure is kept
+    assert len(lib.sv_last_error_string()) > 0
+    assert sv.SpecVerifyError(3, "x").status == 3
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding raises when tensors are not on a CUDA device."""
+    import torch
+
+    import speculative_verify_paged_gb300 as sv
+    x = torch.zeros(2, 5, 8, 16)
+    with pytest.raises((ValueError, RuntimeError)):
+        sv.spec_verify_sample(torch.zeros(2, 5, 100), torch.zeros(2, 4, 100),
+                              torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, 5, 2))
+    with pytest.raises((ValueError, RuntimeError)):
+        sv.spec_verify_attn(x, x, x, torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32))
