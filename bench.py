@@ -1,0 +1,411 @@
+"""Benchmark of one verify step (paged KV append + paged GQA verify attention +
+fused rejection sampling) on the LLaMA-3-70B layer-shaped workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3_70b] [--sigma 1.5]
+
+Prints ONE JSON line on rank 0. `value` is verify steps/s of the whole job
+(inputs resident in HBM); `e2e` is the same metric through the public API with
+the step's inputs copied from pinned host memory and the outputs read back
+inside the timed region. The reference arm (`--impl reference`) times the CPU
+oracle on a bounded sample of the same workload and scales it to steps/s.
+Multi-GPU runs are independent replicas (one batch per GPU, no collective).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify steps/sec & tokens/sec; HBM GB/s vs 8 TB/s roofline (1×GB300)"
+UNIT = "verify steps/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3_70b")
+    ap.add_argument("--sigma", type=float, default=None)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def attn_traffic_from_profile():
+    """DRAM bytes per attention launch from the committed ncu summary, if the
+    kernel source is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "attn_tc_llama3_70b.md")
+    src = os.path.join(ROOT, "speculative_verify_paged_gb300", "csrc", "attn.cu")
+    if not (os.path.exists(p) and os.path.exists(src)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    text = open(p).read()
+    src_line = [l for l in text.splitlines() if l.startswith("source_sha256_16:")]
+    val_line = [l for l in text.splitlines() if l.startswith("dram_bytes_per_launch_full_workload:")]
+    if not src_line or not val_line or src_line[0].split(":", 1)[1].strip() != digest:
+        return None
+    return int(float(val_line[0].split(":", 1)[1].strip()))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm -----
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    import speculative_verify_paged_gb300 as sv
+    import workloads
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.build()
+    cfg = workloads.CONFIGS[args.workload]
+    sigma = cfg.sigma if args.sigma is None else args.sigma
+    seed = args.seed + rank
+    a = workloads.make_attention_inputs(cfg, seed=seed, device=dev)
+    n = workloads.make_append_inputs(cfg, seed=seed, device=dev)
+    s = workloads.make_sampling_inputs(cfg, seed=seed, device=dev, sigma=sigma)
+    lens = a["seq_lens"].tolist()
+    attn_bytes = workloads.attention_bytes(cfg, lens)
+    samp_bytes = workloads.sampling_bytes(cfg)
+    app_bytes = workloads.append_bytes(cfg)
+    step_bytes = attn_bytes + samp_bytes + app_bytes
+
+    k_cache, v_cache = a["k_cache"], a["v_cache"]
+    out = torch.empty_like(a["q"])
+    attn_ws = sv.alloc_workspace(sv.attn_workspace_size(cfg.B, cfg.n_new, cfg.H_q, cfg.H_kv, cfg.d_head,
+                                                        a["block_table"].shape[1]), dev)
+    samp_ws = sv.alloc_workspace(sv.sample_workspace_size(cfg.B, cfg.K, cfg.V), dev)
+    toks = torch.empty((cfg.B, cfg.K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((cfg.B,), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sv.kv_block_append(n["k_new"], n["v_new"], k_cache, v_cache, a["block_table"], a["seq_lens"],
+                           a["k_scale"], a["v_scale"], status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        sv.spec_verify_attn(a["q"], k_cache, v_cache, a["block_table"], a["seq_lens"], None,
+                            a["k_scale"], a["v_scale"], out=out, workspace=attn_ws, status=status)
+        if ev is not None:
+            ev[2].record(stream)
+        sv.spec_verify_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"],
+                              out_tokens=toks, num_accepted=nacc, workspace=samp_ws, status=status,
+                              want_probs=False)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %d" % int(status.item())
+    emitted_per_step = int((nacc.long() + 1).sum().item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    app_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    samp_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers -------------
+    host = {k: v.cpu().pin_memory() for k, v in
+            {"q": a["q"], "k_new": n["k_new"], "v_new": n["v_new"], "target_logits": s["target_logits"],
+             "draft_logits": s["draft_logits"], "draft_tokens": s["draft_tokens"],
+             "uniforms": s["uniforms"], "seq_lens": a["seq_lens"], "block_table": a["block_table"]}.items()}
+    devbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    toks_h = torch.empty(toks.shape, dtype=toks.dtype).pin_memory()
+    nacc_h = torch.empty(nacc.shape, dtype=nacc.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(x.numel() * x.element_size() for x in (out_h, toks_h, nacc_h))
+
+    def e2e_step():
+        for k, v in host.items():
+            devbuf[k].copy_(v, non_blocking=True)
+        o, tk, na = sv.verify_step(devbuf["q"], devbuf["k_new"], devbuf["v_new"], k_cache, v_cache,
+                                   devbuf["block_table"], devbuf["seq_lens"], devbuf["target_logits"],
+                                   devbuf["draft_logits"], devbuf["draft_tokens"], devbuf["uniforms"],
+                                   a["k_scale"], a["v_scale"], attn_out=out, attn_workspace=attn_ws,
+                                   sample_workspace=samp_ws, status=status)
+        out_h.copy_(o, non_blocking=True)
+        toks_h.copy_(tk, non_blocking=True)
+        nacc_h.copy_(na, non_blocking=True)
+
+    e2e_steps = 0 if args.no_e2e else max(5, args.steps // 2)
+    for _ in range(3 if e2e_steps else 0):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        dist.barrier()
+    assert int(status.item()) == 0
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    ms_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+    attn_us = 1e3 * statistics.mean(attn_ms)
+    samp_us = 1e3 * statistics.mean(samp_ms)
+    app_us = 1e3 * statistics.mean(app_ms)
+    peak, peak_kind = measured_peaks()
+    attn_gbs = attn_bytes / (attn_us * 1e-6) / 1e9
+    samp_gbs = samp_bytes / (samp_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s: B=%d H_q=%d H_kv=%d d_head=%d %s KV, ctx %s, block 16, K=%d, V=%d %s logits, "
+                               "draft sigma %.2g" % (cfg.name, cfg.B, cfg.H_q, cfg.H_kv, cfg.d_head,
+                                                    cfg.kv_dtype, cfg.ctx, cfg.K, cfg.V, cfg.logit_dtype, sigma),
+                   "global_batch": cfg.B * world, "seq_len": int(sum(lens) / len(lens)),
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (%.2f GB touched per step)" % (step_bytes / 1e9)},
+        "tokens_per_sec": world * emitted_per_step * args.steps / (total_ms / 1e3),
+        "hbm_gbs_step": step_bytes / (ms_step * 1e-3) / 1e9,
+        "frac_of_8tbs_step": step_bytes / (ms_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+        "ops": {"append_us": app_us, "attn_us": attn_us, "sample_us": samp_us,
+                "attn_bytes": attn_bytes, "sample_bytes": samp_bytes, "append_bytes": app_bytes,
+                "attn_gbs": attn_gbs, "sample_gbs": samp_gbs,
+                "attn_frac_of_8tbs": attn_gbs / NOMINAL_HBM_GBS, "sample_frac_of_8tbs": samp_gbs / NOMINAL_HBM_GBS,
+                "emitted_tokens_per_step": emitted_per_step},
+        "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (attn_tc_kernel + attn_merge_kernel)",
+                     "achieved": attn_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": attn_gbs / peak, "traffic": attn_traffic_from_profile()},
+        "roofline_sample": {"bound": "hbm", "kernel": "spec_verify_sample (rows + resolve)",
+                            "achieved": samp_gbs, "peak": peak, "unit": "GB/s", "frac": samp_gbs / peak},
+        "e2e": ({"value": world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, a, n, s, sigma)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- oracle -----
+
+def oracle_sample_time(cfg, a, n, s, n_attn, n_samp):
+    """Seconds the oracle takes for the append + attention of sequences
+    [0, n_attn) and the sampling of sequences [0, n_samp); returns the time
+    scaled to one full step and a description of the sample."""
+    import numpy as np
+
+    from oracle import attention as oatt
+    from oracle import kv_append as oapp
+    from oracle import sampling as osamp
+    cpu = lambda d: {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in d.items()}
+    a, n, s = cpu(a), cpu(n), cpu(s)
+    lens = a["seq_lens"].tolist()
+    idx = list(range(n_attn))
+    t0 = time.perf_counter()
+    sub_lens = a["seq_lens"][idx]
+    oapp.kv_block_append(a["k_cache"], a["v_cache"], n["k_new"][idx], n["v_new"][idx],
+                         a["block_table"][idx], sub_lens, cfg.block_size, cfg.kv_dtype,
+                         a["k_scale"], a["v_scale"])
+    t1 = time.perf_counter()
+    oatt.verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"],
+                          1 / math.sqrt(cfg.d_head), cfg.block_size, cfg.kv_dtype, a["k_scale"],
+                          a["v_scale"], batch_indices=idx)
+    t2 = time.perf_counter()
+    osamp.rejection_sample_chunked(s["target_logits"], s["draft_logits"], s["draft_tokens"],
+                                   s["uniforms"], batch_indices=list(range(n_samp)))
+    t3 = time.perf_counter()
+    key_frac = sum(lens[:n_attn]) / sum(lens)
+    full = (t1 - t0) * cfg.B / n_attn + (t2 - t1) / key_frac + (t3 - t2) * cfg.B / n_samp
+    desc = ("oracle append+attention on sequences 0..%d (%d of %d keys) and sampling on sequences "
+            "0..%d of %d, scaled to the full batch" % (n_attn - 1, sum(lens[:n_attn]), sum(lens),
+                                                      n_samp - 1, cfg.B))
+    return full, t3 - t0, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(cfg, a, n, s, sigma):
+    n_attn = min(cfg.B, 6)
+    n_samp = min(cfg.B, 8)
+    full, spent, desc = oracle_sample_time(cfg, a, n, s, n_attn, n_samp)
+    return {"value": 1.0 / full, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": desc + "; %.1f s of CPU work; numpy fp64 (BLAS threads = cores)" % spent}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import torch
+
+    import workloads
+    cfg = workloads.CONFIGS[args.workload]
+    sigma = cfg.sigma if args.sigma is None else args.sigma
+    a = workloads.make_attention_inputs(cfg, seed=args.seed)
+    n = workloads.make_append_inputs(cfg, seed=args.seed)
+    s = workloads.make_sampling_inputs(cfg, seed=args.seed, sigma=sigma)
+    n_attn, n_samp = 1, 1
+    for _ in range(args.warmup):
+        oracle_sample_time(cfg, a, n, s, n_attn, n_samp)
+    fulls = []
+    desc = ""
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        full, _, desc = oracle_sample_time(cfg, a, n, s, n_attn, n_samp)
+        fulls.append(full)
+    wall = time.perf_counter() - t0
+    value = 1.0 / statistics.mean(fulls)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(fulls),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "global_batch": cfg.B, "parallelism": "cpu"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": desc + "; each step is this sample (%.1f s wall for %d steps)"
+                             % (wall, args.steps)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    del torch
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()
