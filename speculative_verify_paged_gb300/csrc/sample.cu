@@ -11,18 +11,21 @@
 //   * sample_rows_kernel: one thread-block cluster per (sequence, position)
 //     row. Each CTA of the cluster pulls its slice of the target row and of
 //     the draft row into shared memory with 1-D bulk (TMA) copies, so every
-//     logit crosses HBM once. Max and sum-of-exp are reduced across the
-//     cluster through distributed shared memory. The accept test and a
-//     speculative "if rejected here" inverse-CDF draw (the bonus draw for row
-//     K) are evaluated in fp32 together with a bound on their rounding error;
-//     the result is one 48-byte record per row.
-//   * sample_resolve_kernel: one cluster per sequence walks the K records in
-//     order, stops at the first rejection and writes the emitted tokens. A
-//     decision whose fp32 margin is inside the rounding bound is recomputed
-//     from the logits in float-float arithmetic (about 2^-44 relative error),
-//     so emitted tokens agree with exact arithmetic except on a set of
-//     uniforms of measure ~1e-12.
+//     logit crosses HBM once. One online pass gives each CTA its (max, sum of
+//     exp) pair; pairs are combined across the cluster through distributed
+//     shared memory. The accept test and a speculative "if rejected here"
+//     inverse-CDF draw (the bonus draw for row K) are evaluated in fp32,
+//     each with a certificate that it lies outside its rounding bound. The
+//     result is one 48-byte record per row.
+//   * sample_finish_kernel: a few clusters walk each sequence's records in
+//     order, stop at the first rejection and write the emitted tokens; no
+//     host round-trip between positions. The rare decision that is not
+//     certified (a few percent of sequences) is re-evaluated from that row's
+//     logits in float-float arithmetic (~1e-9 relative error per term), so
+//     emitted tokens are those of exact arithmetic except for uniforms within
+//     ~1e-10 of a boundary.
 #include <cmath>
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -33,25 +36,30 @@ namespace {
 
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kResThreads = 512;
+constexpr int kResThreads = 512;   // finish kernel
 constexpr int kResWarps = kResThreads / 32;
-constexpr int kResCluster = 8;
 constexpr uint32_t kChunkBytes = 16384;
 constexpr int kMaxChunks = 32;              // per CTA, target + draft
 constexpr size_t kMaxSliceSmem = 200 * 1024;
 constexpr size_t kTargetSliceSmem = 64 * 1024;
+constexpr int kFinishClusters = 16;
 
-enum : uint32_t { REC_ACCEPT = 1u, REC_ACC_CERTAIN = 2u };
-enum : uint32_t { SMP_FOUND = 1u, SMP_CERTAIN = 2u };
+enum : uint32_t {
+  REC_ACCEPT = 1u,       // fp32 accept decision of the draft at this position
+  REC_ACC_CERT = 2u,     // ... certified: outside the rounding bound
+  REC_DRAW_CERT = 4u,    // the fp32 draw was found and certified
+  REC_EXACT_ACC = 8u,    // set by the finish kernel: accept re-evaluated in float-float
+  REC_EXACT_DRAW = 16u,  // set by the finish kernel: draw re-evaluated in float-float
+};
 
 struct RowRec {
-  float m_p, s_p, m_q, s_q;  // fast-path row max and sum of exp2((l - m) c)
+  float m_p, s_p, m_q, s_q;  // row max and sum of exp2((l - m) c) (fp32)
   float p_x, q_x;            // p_i(x_i), q_i(x_i) in fp32
-  float gap, z;              // margin of the fp32 draw and its total mass
-  int32_t y;                 // fp32 inverse-CDF draw
-  uint32_t acc_flags;        // REC_*
-  uint32_t smp_flags;        // SMP_*
-  float e_abs;               // rounding bound the margin was compared with
+  float gap, z;              // margin of the fp32 draw and the mass it was drawn from
+  int32_t y;                 // fp32 draw of this row (-1 if not found)
+  uint32_t flags;            // REC_*
+  int32_t y_exact;           // float-float draw (finish kernel; -1 if not evaluated)
+  float e_abs;               // rounding bound the fp32 margin was compared with
 };
 static_assert(sizeof(RowRec) == 48, "record layout");
 
@@ -67,7 +75,8 @@ struct SampleParams {
   RowRec *recs;
   int32_t *status;
   int B, K, V;
-  int ns;        // elements per CTA slice in the rows kernel (multiple of 8)
+  int ns;        // elements per CTA slice (multiple of 8)
+  int ns_x;      // elements per CTA slice in the finish kernel
   int aligned;   // rows are 16-byte aligned: bulk copies usable
   unsigned flags;
   float c;       // log2(e) / T
@@ -77,7 +86,71 @@ struct SampleParams {
   float2 tbl[64];  // 2^(j/64) split into (hi, lo)
 };
 
+// ------------------------------------------------- float-float arithmetic ---
+// A value is hi + lo with |lo| <= ulp(hi)/2; error-free transformations
+// (Knuth two-sum, fma-based two-product) give ~2^-44 relative accuracy.
+
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  const float e = (a - (s - bb)) + (b - bb);
+  return {s, e};
+}
+
+__device__ __forceinline__ ff quick_two_sum(float a, float b) {
+  const float s = a + b;
+  return {s, b - (s - a)};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  const ff t = two_sum(a.lo, b.lo);
+  s.lo += t.hi;
+  s = quick_two_sum(s.hi, s.lo);
+  s.lo += t.lo;
+  return quick_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return quick_two_sum(p, e);
+}
+
+__device__ __forceinline__ bool ff_pos(ff a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+
+__device__ __forceinline__ bool ff_gt(ff a, ff b) { return ff_pos(ff_add(a, ff_neg(b))); }
+
+__device__ __forceinline__ ff ff_max0(ff a) { return ff_pos(a) ? a : ff{0.f, 0.f}; }
+
+
+__device__ __forceinline__ ff scan32_ff(ff v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff t{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if (lane >= o) v = ff_add(t, v);
+  }
+  return v;
+}
+
 // ------------------------------------------------------------ fp32 path ---
+
+// 2^x on the SFU (flushes results below 2^-126, i.e. weights < 1e-38 of the
+// row maximum, to zero). Its relative error on [-30, 0] measured on GB300 is
+// below 1.5e-7.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <typename T>
 __device__ __forceinline__ void load8(const T *s, int g, float (&x)[8]);
@@ -120,45 +193,98 @@ __device__ __forceinline__ T pad_value(bool is_prob) {
   return T(-INFINITY);
 }
 
-// Block-wide reduction of one float (all threads get the result).
-template <bool MAX>
-__device__ __forceinline__ float block_reduce(float v, float *red) {
+// (m, s) pairs of an online softmax: s = sum 2^(fl(x c - fl(m c))). Every
+// exponent is taken against the rounded reference fl(m c), the same one the
+// weights of pass B use, so sums and weights share one scale. Commutative,
+// so butterfly reductions leave the same bits in every lane.
+__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2, float c) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) { m = mn; s = 0.f; return; }
+  // __fmul_rn: the references must be the rounded products, never fused
+  // into an fma (a fused m c - fl(m c) would rescale the leading partial by
+  // its rounding residual at every reduction level)
+  const float rc = __fmul_rn(mn, c);
+  s = s * ex2(__fmul_rn(m, c) - rc) + s2 * ex2(__fmul_rn(m2, c) - rc);
+  m = mn;
+}
+
+__device__ __forceinline__ void warp_ms(float &m, float &s, float c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    ms_combine(m, s, m2, s2, c);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void online8(const T *buf, int g, float c, float &m, float &s) {
+  float x[8];
+  load8(buf, g, x);
+  float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  if (mx > m) {
+    s = (m == -INFINITY) ? 0.f : s * ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+    m = mx;
+  }
+  if (m == -INFINITY) return;
+  const float mc = __fmul_rn(m, c);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += ex2(fmaf(x[j], c, -mc));
+}
+
+// Block sum of a float-float value (result in every thread).
+__device__ __forceinline__ ff block_sum_ff(ff v, ff *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = MAX ? warp_max(v) : warp_sum(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff{__shfl_xor_sync(0xffffffffu, v.hi, o),
+                                                     __shfl_xor_sync(0xffffffffu, v.lo, o)});
   __syncthreads();
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  const int nw = blockDim.x >> 5;
-  float r = lane < nw ? red[lane] : (MAX ? -INFINITY : 0.f);
-  r = MAX ? warp_max(r) : warp_sum(r);
+  ff r{0.f, 0.f};
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = ff_add(r, red[w]);
   return r;
 }
 
-// Reduce a published per-CTA float across the cluster (same result and
-// same order of operations in every CTA). `pub` is this CTA's shared copy.
-template <bool MAX>
-__device__ __forceinline__ float cluster_reduce(const float *pub, int cs) {
-  const int lane = threadIdx.x & 31;
-  float v = MAX ? -INFINITY : 0.f;
-  if (lane < cs) v = ld_dsmem_f32(mapa(pub, lane));
-  return MAX ? warp_max(v) : warp_sum(v);
+__device__ __forceinline__ ff ld_dsmem_ff(const ff *p, int rank) {
+  const uint32_t a = mapa(p, rank);
+  return ff{ld_dsmem_f32(a), ld_dsmem_f32(a + 4)};
 }
 
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+constexpr int kMaxSteps = 16;   // 32-group steps per warp range
+
+struct RowShared {
+  uint64_t bars[kMaxChunks];
+  float red_m[32], red_s[32], red_m2[32], red_s2[32];
+  float pub_mp, pub_sp, pub_mq, pub_sq;   // this CTA's (max, sum) pairs
+  float pub_lp, pub_lq;                   // logits at the draft token (its owner CTA)
+  float pub_tot;                          // this CTA's draw mass
+  float wsum[kRowWarps];
+  float stepsum[kRowWarps][kMaxSteps];
+};
+
+// One cluster per (sequence, position) row; fp32 fast path only. Writes the
+// row's record: stats, accept test, speculative draw and their certificates.
 template <typename TT, int DK>
 __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_constant__ SampleParams P) {
   using TD = typename std::conditional<DK == 0, TT, float>::type;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kMaxChunks];
-  __shared__ float red[32];
-  __shared__ float pub_max_p, pub_max_q, pub_sum_p, pub_sum_q, pub_tot, pub_q2;
-  __shared__ float wsum[kRowWarps];
+  __shared__ RowShared sh;
 
   const int cs = gridDim.x;
   const int rank = (int)cluster_ctarank();
   const int i = blockIdx.y, b = blockIdx.z;
   const int K = P.K, V = P.V;
   const bool has_draft = i < K;
+  const bool q_logits = has_draft && DK == 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float c = P.c;
 
   const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
   const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
@@ -173,33 +299,30 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   const uint32_t nb_d = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
   const int nch_t = P.aligned ? (int)((nb_t + kChunkBytes - 1) / kChunkBytes) : 0;
   const int nch_d = P.aligned ? (int)((nb_d + kChunkBytes - 1) / kChunkBytes) : 0;
-  // padding of the last group: -inf logits / zero probabilities
-  for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {
+  for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {   // pad the last group
     st[e] = pad_value<TT>(false);
     if (has_draft) sd[e] = pad_value<TD>(DK == 1);
   }
   if (P.aligned) {
     if (tid == 0) {
-      for (int k = 0; k < nch_t + nch_d; ++k) mbar_init(&bars[k], 1);
+      for (int k = 0; k < nch_t + nch_d; ++k) mbar_init(&sh.bars[k], 1);
       fence_mbarrier_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
       const uint8_t *gt = reinterpret_cast<const uint8_t *>(trow + e0);
       for (int k = 0; k < nch_t; ++k) {
         const uint32_t off = k * kChunkBytes, nb = min(kChunkBytes, nb_t - off);
-        mbar_arrive_expect_tx(&bars[k], nb);
-        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, nb, &bars[k]);
+        mbar_arrive_expect_tx(&sh.bars[k], nb);
+        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, nb, &sh.bars[k]);
       }
       if (has_draft) {
         const uint8_t *gd = reinterpret_cast<const uint8_t *>(drow + e0);
         for (int k = 0; k < nch_d; ++k) {
           const uint32_t off = k * kChunkBytes, nb = min(kChunkBytes, nb_d - off);
-          mbar_arrive_expect_tx(&bars[nch_t + k], nb);
-          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, nb, &bars[nch_t + k]);
+          mbar_arrive_expect_tx(&sh.bars[nch_t + k], nb);
+          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, nb, &sh.bars[nch_t + k]);
         }
       }
     }
+    __syncthreads();   // barriers initialised before anyone waits on them
   } else {
     for (int e = tid; e < n_loc; e += blockDim.x) {
       st[e] = trow[e0 + e];
@@ -208,105 +331,95 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
     __syncthreads();
   }
 
-  // ---- pass 1: row maxima (overlapped with the arriving chunks) ----------
+  // ---- pass A: online (max, sum of exp) as the chunks land ---------------
   bool timed_out = false;
-  float mt = -INFINITY, md = -INFINITY;
+  float mt = -INFINITY, stt = 0.f, md = -INFINITY, sdd = 0.f;
   {
-    constexpr int gpc_t = kChunkBytes / (8 * sizeof(TT));  // groups per chunk
+    constexpr int gpc_t = kChunkBytes / (8 * sizeof(TT));   // 8-element groups per chunk
     const int nchunks = P.aligned ? nch_t : 1;
     for (int k = 0; k < nchunks; ++k) {
-      if (P.aligned && !timed_out && !mbar_wait(&bars[k], 0)) timed_out = true;
+      if (P.aligned && !timed_out && !mbar_wait(&sh.bars[k], 0)) timed_out = true;
       const int g_end = P.aligned ? min(n_grp, (k + 1) * gpc_t) : n_grp;
-      for (int g = (P.aligned ? k * gpc_t : 0) + tid; g < g_end; g += blockDim.x) {
-        float x[8];
-        load8(st, g, x);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mt = fmaxf(mt, x[j]);
-      }
+      for (int g = (P.aligned ? k * gpc_t : 0) + tid; g < g_end; g += blockDim.x) online8(st, g, c, mt, stt);
     }
   }
   if (has_draft) {
     constexpr int gpc_d = kChunkBytes / (8 * sizeof(TD));
     const int nchunks = P.aligned ? nch_d : 1;
     for (int k = 0; k < nchunks; ++k) {
-      if (P.aligned && !timed_out && !mbar_wait(&bars[nch_t + k], 0)) timed_out = true;
+      if (P.aligned && !timed_out && !mbar_wait(&sh.bars[nch_t + k], 0)) timed_out = true;
       if (DK == 0) {
         const int g_end = P.aligned ? min(n_grp, (k + 1) * gpc_d) : n_grp;
-        for (int g = (P.aligned ? k * gpc_d : 0) + tid; g < g_end; g += blockDim.x) {
-          float x[8];
-          load8(sd, g, x);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) md = fmaxf(md, x[j]);
-        }
+        for (int g = (P.aligned ? k * gpc_d : 0) + tid; g < g_end; g += blockDim.x) online8(sd, g, c, md, sdd);
       }
     }
   }
   if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-  mt = block_reduce<true>(mt, red);
-  if (has_draft && DK == 0) md = block_reduce<true>(md, red);
-  if (tid == 0) { pub_max_p = mt; pub_max_q = md; }
-  cluster_sync();
-  const float m_p = cluster_reduce<true>(&pub_max_p, cs);
-  const float m_q = (has_draft && DK == 0) ? cluster_reduce<true>(&pub_max_q, cs) : 0.f;
-
-  // ---- pass 2: sums of exp2((l - m) c) ------------------------------------
-  const float c = P.c;
-  const float mcp = m_p * c, mcq = m_q * c;
-  float sp = 0.f, sq = 0.f;
-  for (int g = tid; g < n_grp; g += blockDim.x) {
-    float x[8];
-    load8(st, g, x);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sp += exp2f(fmaf(x[j], c, -mcp));
-    if (has_draft && DK == 0) {
-      load8(sd, g, x);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sq += exp2f(fmaf(x[j], c, -mcq));
+  int x_tok = 0;
+  if (has_draft) {
+    x_tok = P.tokens[(int64_t)b * K + i];
+    if (x_tok < 0 || x_tok >= V) {
+      if (rank == 0 && tid == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+      x_tok = min(max(x_tok, 0), V - 1);
     }
   }
-  sp = block_reduce<false>(sp, red);
-  if (has_draft && DK == 0) sq = block_reduce<false>(sq, red);
-  if (tid == 0) { pub_sum_p = sp; pub_sum_q = sq; }
-  cluster_sync();
-  const float S_p = cluster_reduce<false>(&pub_sum_p, cs);
-  const float S_q = (has_draft && DK == 0) ? cluster_reduce<false>(&pub_sum_q, cs) : 1.f;
-  const float inv_sp = 1.f / S_p, inv_sq = 1.f / S_q;
-
-  RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
-  const float *uv = P.uniforms + ((int64_t)b * (K + 1) + i) * 2;
-  if (!(fabsf(m_p) <= 3.0e38f) || (has_draft && DK == 0 && !(fabsf(m_q) <= 3.0e38f))) {
-    if (tid == 0 && rank == 0) atomic_or_status(P.status, SV_DEV_NONFINITE);
-  }
-
-  // ---- accept test (rank 0) ----------------------------------------------
-  if (rank == 0 && tid == 0) {
-    rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
-    uint32_t af = 0;
-    float p_x = 0.f, q_x = 0.f;
-    if (has_draft) {
-      int x = P.tokens[(int64_t)b * K + i];
-      if (x < 0 || x >= V) {
-        atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
-        x = min(max(x, 0), V - 1);
+  const int x_rank = x_tok / P.ns;
+  warp_ms(mt, stt, c);
+  if (q_logits) warp_ms(md, sdd, c);
+  if (lane == 0) { sh.red_m[warp] = mt; sh.red_s[warp] = stt; sh.red_m2[warp] = md; sh.red_s2[warp] = sdd; }
+  __syncthreads();
+  if (warp == 0) {
+    float m1 = lane < kRowWarps ? sh.red_m[lane] : -INFINITY, s1 = lane < kRowWarps ? sh.red_s[lane] : 0.f;
+    float m2 = lane < kRowWarps ? sh.red_m2[lane] : -INFINITY, s2 = lane < kRowWarps ? sh.red_s2[lane] : 0.f;
+    warp_ms(m1, s1, c);
+    if (q_logits) warp_ms(m2, s2, c);
+    if (lane == 0) {
+      sh.pub_mp = m1; sh.pub_sp = s1; sh.pub_mq = m2; sh.pub_sq = s2;
+      if (has_draft && rank == x_rank) {   // the slice holding x_i publishes its logits
+        sh.pub_lp = to_f32(st[x_tok - e0]);
+        sh.pub_lq = to_f32(sd[x_tok - e0]);
       }
-      p_x = exp2f(fmaf(to_f32(trow[x]), c, -mcp)) * inv_sp;
-      if (DK == 0) q_x = exp2f(fmaf(to_f32(drow[x]), c, -mcq)) * inv_sq;
-      else q_x = to_f32(drow[x]);
-      const float lhs = uv[0] * q_x;
-      if (lhs < p_x) af |= REC_ACCEPT;
-      // relative rounding bound of p_x and u q_x (exp2, argument rounding,
-      // row sums): a decision this far from the boundary is exact.
-      if (fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f) af |= REC_ACC_CERTAIN;
-      if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
-      if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
     }
-    rec->p_x = p_x; rec->q_x = q_x;
-    rec->acc_flags = af;
+  }
+  cluster_sync();   // #1: (max, sum) pairs and the draft token's logits published
+  float m_p = -INFINITY, S_p = 0.f, m_q = -INFINITY, S_q = 0.f;
+  if (lane < cs) {
+    m_p = ld_dsmem_f32(mapa(&sh.pub_mp, lane)); S_p = ld_dsmem_f32(mapa(&sh.pub_sp, lane));
+    m_q = ld_dsmem_f32(mapa(&sh.pub_mq, lane)); S_q = ld_dsmem_f32(mapa(&sh.pub_sq, lane));
+  }
+  warp_ms(m_p, S_p, c);
+  if (q_logits) warp_ms(m_q, S_q, c);
+  else { m_q = 0.f; S_q = 1.f; }
+  float lp_x = 0.f, lq_x = 0.f;
+  if (has_draft) {
+    lp_x = ld_dsmem_f32(mapa(&sh.pub_lp, x_rank));
+    lq_x = ld_dsmem_f32(mapa(&sh.pub_lq, x_rank));
+  }
+  const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
+  // e_p(y) = 2^(fl(l(y) c - fl(m_p c))), p = e_p / S_p. The draw works on the
+  // unnormalised weights w'(y) = S_p w(y) = max(0, e_p(y) - r e_q(y)),
+  // r = S_p / S_q (or S_p for given probabilities): the inverse CDF is
+  // invariant to the common scale.
+  const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
+  const float r_pq = q_logits ? S_p / S_q : S_p;
+  const float *uv = P.uniforms + ((int64_t)b * (K + 1) + i) * 2;
+  const float u = uv[0], v_u = uv[1];
+
+  // ---- accept test in fp32 ------------------------------------------------
+  bool accept = false, acc_cert = true;
+  float p_x = 0.f, q_x = 0.f;
+  if (has_draft) {
+    p_x = ex2(fmaf(lp_x, c, -mcp)) / S_p;
+    q_x = DK == 0 ? ex2(fmaf(lq_x, c, -mcq)) / S_q : lq_x;
+    const float lhs = u * q_x;
+    accept = lhs < p_x;
+    // p_x and u q_x each carry < 2e-6 relative rounding (exp2, argument
+    // rounding, row sums): a decision this far from the boundary is exact
+    acc_cert = fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f && finite;
   }
 
-  // ---- pass 3: weights of the speculative draw, per-warp range sums -------
-  // weight w(y) = max(0, p(y) - q(y)) for a draft row, p(y) for the bonus row.
-  auto weight8 = [&](int g, float (&w)[8], float &q2) {
+  // ---- pass B: fp32 weights of the speculative draw ----------------------
+  auto weight8 = [&](int g, float (&w)[8]) {
     float xp[8];
     load8(st, g, xp);
     if (has_draft) {
@@ -314,82 +427,94 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
       load8(sd, g, xq);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float p = exp2f(fmaf(xp[j], c, -mcp)) * inv_sp;
-        const float q = DK == 0 ? exp2f(fmaf(xq[j], c, -mcq)) * inv_sq : xq[j];
-        w[j] = fmaxf(p - q, 0.f);
-        q2 = fmaf(p, p, fmaf(q, q, q2));
+        const float ep = ex2(fmaf(xp[j], c, -mcp));
+        const float eq = DK == 0 ? ex2(fmaf(xq[j], c, -mcq)) : xq[j];
+        w[j] = fmaxf(fmaf(-r_pq, eq, ep), 0.f);
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float p = exp2f(fmaf(xp[j], c, -mcp)) * inv_sp;
-        w[j] = p;
-        q2 = fmaf(p, p, q2);
-      }
+      for (int j = 0; j < 8; ++j) w[j] = ex2(fmaf(xp[j], c, -mcp));
     }
   };
-  const int gpw = (n_grp + kRowWarps - 1) / kRowWarps;  // groups per warp range
-  const int g_lo = warp * gpw, g_hi = min(n_grp, g_lo + gpw);
-  float run = 0.f, q2 = 0.f;
-  for (int s0 = g_lo; s0 < g_hi; s0 += 32) {
+  const int gpw = (n_grp + kRowWarps - 1) / kRowWarps;   // groups per warp range
+  const int g_lo = min(n_grp, warp * gpw), g_hi = min(n_grp, g_lo + gpw);
+  float run = 0.f;
+  for (int s0 = g_lo, sidx = 0; s0 < g_hi; s0 += 32, ++sidx) {
     const int g = s0 + lane;
     float v = 0.f;
     if (g < g_hi) {
       float w[8];
-      weight8(g, w, q2);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v += w[j];
+      weight8(g, w);
+      v = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
     }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
-    }
-    run += __shfl_sync(0xffffffffu, v, 31);
+    v = warp_sum(v);
+    if (lane == 0) sh.stepsum[warp][sidx] = v;
+    run += v;
   }
-  if (lane == 0) wsum[warp] = run;
-  q2 = block_reduce<false>(q2, red);   // contains __syncthreads: wsum visible
+  if (lane == 0) sh.wsum[warp] = run;
+  __syncthreads();
   float tot_cta = 0.f;
-  for (int w = 0; w < kRowWarps; ++w) tot_cta += wsum[w];
-  if (tid == 0) { pub_tot = tot_cta; pub_q2 = q2; }
-  cluster_sync();
-  // exclusive prefix over ranks (same chain in every CTA)
+  for (int w = 0; w < kRowWarps; ++w) tot_cta += sh.wsum[w];
+  if (tid == 0) sh.pub_tot = tot_cta;
+  cluster_sync();   // #2: masses published
   float off_c = 0.f, Z = 0.f;
-  for (int r = 0; r < cs; ++r) {
-    const float t = ld_dsmem_f32(mapa(&pub_tot, r));
-    if (r == rank) off_c = Z;
+  for (int rr = 0; rr < cs; ++rr) {
+    const float t = ld_dsmem_f32(mapa(&sh.pub_tot, rr));
+    if (rr == rank) off_c = Z;
     Z += t;
   }
-  const float Q2 = cluster_reduce<false>(&pub_q2, cs);
-  const float v = uv[1];
-  const float thr = v * Z;
-  const float e_abs = 1.9073486e-06f * sqrtf(Q2) + 4.7683716e-07f * (Z + 1.f);  // 2^-19, 2^-21
-  const bool draw_ok = Z > 0.f && thr < Z && fabsf(m_p) <= 3.0e38f;
+  // the last distributed read of this launch is done: arrive now, wait at exit
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  const float thr = v_u * Z;
+  // rounding bound of the fp32 CDF near thr, in units of w' = S_p w:
+  // per-element exp / argument / ratio errors (~2^-22 relative, random:
+  // sqrt(sum p^2) <= sqrt(max p) = sqrt(1/S)), and the rounding of the
+  // running sums (~2^-24 per addition)
+  const float e_abs = 9.5367432e-07f * S_p * sqrtf(1.f / S_p + (q_logits ? 1.f / S_q : 0.f)) +
+                      2.3841858e-07f * (Z + S_p);   // 2^-20, 2^-22
+  const bool draw_ok = finite && Z > 0.f && thr < Z;
+  RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
   if (rank == 0 && tid == 0) {
-    rec->z = Z;
-    rec->e_abs = e_abs;
-    if (!draw_ok) { rec->y = -1; rec->smp_flags = 0; rec->gap = 0.f; }
+    if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
+    rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
+    rec->p_x = p_x; rec->q_x = q_x;
+    rec->z = Z; rec->e_abs = e_abs;
+    rec->y_exact = -1;
+    if (has_draft) {
+      if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
+      if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
+    }
+    if (!draw_ok) {   // no owner: the finish kernel evaluates the draw exactly
+      rec->y = -1; rec->gap = 0.f;
+      rec->flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u);
+    }
   }
   if (draw_ok && off_c <= thr && thr < off_c + tot_cta) {
-    // owner warp: A_w <= thr < A_{w+1}
-    float woff = 0.f;
+    float woff = 0.f, a_w = off_c;
     int owner = kRowWarps - 1;
-    float a_w = off_c;
     for (int w = 0; w < kRowWarps; ++w) {
-      const float a_next = off_c + (woff + wsum[w]);
-      if (thr < a_next || w == kRowWarps - 1) { owner = w; a_w = off_c + woff; break; }
-      woff += wsum[w];
+      const float nxt = woff + sh.wsum[w];
+      if (thr < off_c + nxt || w == kRowWarps - 1) { owner = w; a_w = off_c + woff; break; }
+      woff = nxt;
     }
     if (warp == owner) {
+      // the step of this warp's range that holds thr, then one rescan
+      const int nsteps = (g_hi - g_lo + 31) / 32;
       float base = a_w;
+      int sel = -1;
+      for (int sidx = 0; sidx < nsteps; ++sidx) {
+        const float nxt = base + sh.stepsum[warp][sidx];
+        if (thr < nxt) { sel = sidx; break; }
+        base = nxt;
+      }
       int y = -1;
       float c_lo = 0.f, c_hi = 0.f;
-      for (int s0 = g_lo; s0 < g_hi && y < 0; s0 += 32) {
-        const int g = s0 + lane;
-        float w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        float dummy = 0.f, vsum = 0.f;
+      if (sel >= 0) {
+        const int g = g_lo + sel * 32 + lane;
+        float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float vsum = 0.f;
         if (g < g_hi) {
-          weight8(g, w, dummy);
+          weight8(g, w);
 #pragma unroll
           for (int j = 0; j < 8; ++j) vsum += w[j];
         }
@@ -404,295 +529,246 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
           const int L = __ffs(hit) - 1;
           if (lane == L) {
             float run_c = base + (incl - vsum);
+#pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float nxt = run_c + w[j];
-              if (nxt > thr) { y = (e0 + 8 * g + j); c_lo = run_c; c_hi = nxt; break; }
+              if (y < 0 && nxt > thr) { y = e0 + 8 * g + j; c_lo = run_c; c_hi = nxt; }
               run_c = nxt;
             }
-            if (y < 0) y = -2;   // rounding moved the crossing: not found
           }
           y = __shfl_sync(0xffffffffu, y, L);
           c_lo = __shfl_sync(0xffffffffu, c_lo, L);
           c_hi = __shfl_sync(0xffffffffu, c_hi, L);
-          if (y < 0) break;
         }
-        base += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) {
-        if (y >= 0 && y < V) {
-          const float gap = fminf(thr - c_lo, c_hi - thr);
-          rec->y = y;
-          rec->gap = gap;
-          rec->smp_flags = SMP_FOUND | (gap > e_abs ? SMP_CERTAIN : 0u);
-        } else {
-          rec->y = -1;
-          rec->gap = 0.f;
-          rec->smp_flags = 0;
-        }
+        const bool found = y >= 0 && y < V;   // else: rounding moved the crossing
+        const float gap = found ? fminf(thr - c_lo, c_hi - thr) : 0.f;
+        rec->y = found ? y : -1;
+        rec->gap = gap;
+        rec->flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u) |
+                     ((found && gap > e_abs) ? REC_DRAW_CERT : 0u);
       }
     }
   }
-  // the accept test and the draw of an out-of-range draft row are resolved
-  // exactly by the resolve kernel (flags left uncertain)
-  cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// ------------------------------------------------- float-float arithmetic ---
-// A value is hi + lo with |lo| <= ulp(hi)/2; error-free transformations
-// (Knuth two-sum, fma-based two-product) give ~2^-44 relative accuracy.
-
-struct ff {
-  float hi, lo;
-};
-
-__device__ __forceinline__ ff two_sum(float a, float b) {
-  const float s = a + b;
-  const float bb = s - a;
-  const float e = (a - (s - bb)) + (b - bb);
-  return {s, e};
-}
-
-__device__ __forceinline__ ff quick_two_sum(float a, float b) {
-  const float s = a + b;
-  return {s, b - (s - a)};
-}
-
-__device__ __forceinline__ ff ff_add(ff a, ff b) {
-  ff s = two_sum(a.hi, b.hi);
-  const ff t = two_sum(a.lo, b.lo);
-  s.lo += t.hi;
-  s = quick_two_sum(s.hi, s.lo);
-  s.lo += t.lo;
-  return quick_two_sum(s.hi, s.lo);
-}
-
-__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
-
-__device__ __forceinline__ ff ff_mul(ff a, ff b) {
-  const float p = a.hi * b.hi;
-  float e = fmaf(a.hi, b.hi, -p);
-  e = fmaf(a.hi, b.lo, e);
-  e = fmaf(a.lo, b.hi, e);
-  return quick_two_sum(p, e);
-}
-
-__device__ __forceinline__ bool ff_gt(ff a, ff b) {  // a > b
-  const ff d = ff_add(a, ff_neg(b));
-  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
-}
-
-__device__ __forceinline__ ff ff_max0(ff a) {
-  return (a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f)) ? a : ff{0.f, 0.f};
-}
-
-__device__ __forceinline__ ff shfl_ff(ff v, int src) {
-  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
-}
-
-// exp((l - m) / T) for l <= m in float-float: reduce t = x log2(e) to
-// n/64 + r with |r| <= 1/128, 2^r = e^(r ln2) by its Taylor series to the
-// 5th power (truncation < 1e-14), 2^(j/64) from a float-float table.
-__device__ __forceinline__ ff ff_exp(float l, float m, const SampleParams &P, const float2 *tbl) {
+// ------------------------------------------- float-float re-evaluation ---
+// Lean float-float exp: exp((l - m)/T) for l <= m as an unevaluated pair
+// hi + lo with ~1e-9 relative error: t = (l - m) log2(e) split into
+// n/64 + r (|r| <= 1/128), 2^r - 1 by its Taylor series to r^5, 2^(j/64)
+// from the (hi, lo) table, 2^k by exponent construction. Values below e^-87
+// relative to the row maximum are returned as 0.
+__device__ __forceinline__ ff ffx_exp(float l, float m, const SampleParams &P, const float2 *tbl) {
+  if (!(l > -INFINITY)) return ff{0.f, 0.f};
   ff x = two_sum(l, -m);
   if (!P.unitT) x = ff_mul(x, ff{P.invT_hi, P.invT_lo});
-  if (!(x.hi > -87.f)) return ff{0.f, 0.f};   // below the fp32 normal range: negligible
-  const ff t = ff_mul(x, ff{P.log2e_hi, P.log2e_lo});
-  const float n = rintf(t.hi * 64.f);
-  const float rh = fmaf(-n, 0.015625f, t.hi);  // exact
-  const ff r = two_sum(rh, t.lo);
-  const ff y = ff_mul(r, ff{P.ln2_hi, P.ln2_lo});  // |y| <= 0.0055
-  const float yh = y.hi;
-  const float poly = yh * yh * (0.5f + yh * (0.16666667f + yh * (0.041666668f + yh * 0.0083333338f)));
-  const ff s = two_sum(yh, y.lo + (poly + yh * y.lo));  // e^y - 1
+  if (!(x.hi > -87.f)) return ff{0.f, 0.f};
+  const float t_hi = x.hi * P.log2e_hi;
+  const float t_lo = fmaf(x.hi, P.log2e_hi, -t_hi) + fmaf(x.hi, P.log2e_lo, x.lo * P.log2e_hi);
+  const float n = rintf(t_hi * 64.f);
+  const float r = fmaf(-n, 0.015625f, t_hi) + t_lo;
+  const float y = r * 0.69314718f;
+  const float s = fmaf(y * y, 0.5f + y * (0.16666667f + y * (0.041666668f + y * 0.0083333338f)), y);
   const int ni = (int)n;
   const float2 T = tbl[ni & 63];
-  const ff Tf{T.x, T.y};
-  ff res = ff_add(Tf, ff_mul(Tf, s));
-  const int k = ni >> 6;                           // floor(n / 64)
-  res.hi = ldexpf(res.hi, k);
-  res.lo = ldexpf(res.lo, k);
-  return res;
+  const float scale = __int_as_float(((ni >> 6) + 127) << 23);
+  return ff{T.x * scale, fmaf(T.x, s, T.y) * scale};
 }
 
-// Block reduction of a float-float sum (result in all threads).
-__device__ __forceinline__ ff block_reduce_ff(ff v, ff *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff{__shfl_xor_sync(0xffffffffu, v.hi, o),
-                                                     __shfl_xor_sync(0xffffffffu, v.lo, o)});
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  ff r = ff{0.f, 0.f};
-  const int nw = blockDim.x >> 5;
-  for (int w = 0; w < nw; ++w) r = ff_add(r, red[w]);
-  return r;
+// sum of nonnegative pairs: two-sum on the high parts, low parts added
+__device__ __forceinline__ void acc_add(ff &a, ff v) {
+  const ff s = two_sum(a.hi, v.hi);
+  a.hi = s.hi;
+  a.lo += s.lo + v.lo;
 }
+
+__device__ __forceinline__ ff ff_norm(ff a) { return quick_two_sum(a.hi, a.lo); }
 
 struct ExactShared {
   ff red[32];
   ff wsum[kResWarps];
+  ff stepsum[kResWarps][kMaxSteps];
   ff pub_sp, pub_sq, pub_tot;
   int pub_y, pub_last;
   float2 tbl[64];
 };
 
-// Exact-arithmetic evaluation of row i of sequence b by the whole cluster
-// (every thread of every CTA calls it with the same arguments). Returns the
-// accept decision when need_accept (and stops there if accepted); otherwise
-// *y_out receives the inverse-CDF draw of the row.
+// Exact-arithmetic (float-float) evaluation of row i of sequence b: the
+// accept test (when need_acc) and, unless accepted, the inverse-CDF draw.
+// Called by every thread of every CTA of the cluster; st / sd hold this CTA's
+// slice [e0, e0 + n_grp*8) of the row (padded like the rows kernel does).
 template <typename TT, int DK>
-__device__ bool exact_row(const SampleParams &P, int b, int i, const RowRec &rec, bool need_accept,
-                          int *y_out, ExactShared &sh) {
-  using TD = typename std::conditional<DK == 0, TT, float>::type;
-  const int K = P.K, V = P.V;
-  const int cs = gridDim.x;
-  const int rank = (int)cluster_ctarank();
+__device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
+                          const typename std::conditional<DK == 0, TT, float>::type *sd, int n_grp, int e0,
+                          bool has_draft, bool need_acc, float m_p, float m_q, float lp_x, float lq_x,
+                          float u, float v_u, int *y_out) {
+  const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool has_draft = i < K;
-  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
-  const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
-  const float m_p = rec.m_p, m_q = rec.m_q;
-  const int nsp = ((V + cs - 1) / cs + 31) / 32 * 32;
-  const int e0 = min(V, rank * nsp), e1 = min(V, e0 + nsp);
-
-  // pass A: float-float row sums of exp((l - m) / T)
+  const bool q_logits = has_draft && DK == 0;
   ff sp{0.f, 0.f}, sq{0.f, 0.f};
-  for (int e = e0 + tid; e < e1; e += blockDim.x) {
-    sp = ff_add(sp, ff_exp(to_f32(trow[e]), m_p, P, sh.tbl));
-    if (has_draft && DK == 0) sq = ff_add(sq, ff_exp(to_f32(drow[e]), m_q, P, sh.tbl));
+  for (int g = tid; g < n_grp; g += blockDim.x) {
+    float x[8];
+    load8(st, g, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc_add(sp, ffx_exp(x[j], m_p, P, sh.tbl));
+    if (q_logits) {
+      load8(sd, g, x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc_add(sq, ffx_exp(x[j], m_q, P, sh.tbl));
+    }
   }
-  sp = block_reduce_ff(sp, sh.red);
-  sq = block_reduce_ff(sq, sh.red);
+  sp = block_sum_ff(ff_norm(sp), sh.red);
+  sq = block_sum_ff(ff_norm(sq), sh.red);
   if (tid == 0) { sh.pub_sp = sp; sh.pub_sq = sq; }
   cluster_sync();
   ff Sp{0.f, 0.f}, Sq{0.f, 0.f};
   for (int r = 0; r < cs; ++r) {
-    const uint32_t a = mapa(&sh.pub_sp, r), q = mapa(&sh.pub_sq, r);
-    Sp = ff_add(Sp, ff{ld_dsmem_f32(a), ld_dsmem_f32(a + 4)});
-    Sq = ff_add(Sq, ff{ld_dsmem_f32(q), ld_dsmem_f32(q + 4)});
+    Sp = ff_add(Sp, ld_dsmem_ff(&sh.pub_sp, r));
+    Sq = ff_add(Sq, ld_dsmem_ff(&sh.pub_sq, r));
   }
-  cluster_sync();   // every peer has read the published sums
-  if (DK == 1 || !has_draft) Sq = ff{1.f, 0.f};
-  const float *uv = P.uniforms + ((int64_t)b * (K + 1) + i) * 2;
-
-  if (need_accept && has_draft) {
-    int x = P.tokens[(int64_t)b * K + i];
-    x = min(max(x, 0), V - 1);
-    const ff epx = ff_exp(to_f32(trow[x]), m_p, P, sh.tbl);
+  cluster_sync();   // peers have read the published sums
+  if (!q_logits) Sq = ff{1.f, 0.f};
+  if (need_acc && has_draft) {
     // u q(x) < p(x)  <=>  u e_q(x) S_p < e_p(x) S_q   (draft logits)
     //                <=>  u q(x) S_p < e_p(x)         (draft probabilities)
+    const ff epx = ff_norm(ffx_exp(lp_x, m_p, P, sh.tbl));
     ff lhs, rhs;
     if (DK == 0) {
-      const ff eqx = ff_exp(to_f32(drow[x]), m_q, P, sh.tbl);
-      lhs = ff_mul(ff_mul(ff{uv[0], 0.f}, eqx), Sp);
+      lhs = ff_mul(ff_mul(ff{u, 0.f}, ff_norm(ffx_exp(lq_x, m_q, P, sh.tbl))), Sp);
       rhs = ff_mul(epx, Sq);
     } else {
-      lhs = ff_mul(ff{uv[0], 0.f}, ff_mul(ff{to_f32(drow[x]), 0.f}, Sp));
+      lhs = ff_mul(ff{u, 0.f}, ff_mul(ff{lq_x, 0.f}, Sp));
       rhs = epx;
     }
     if (ff_gt(rhs, lhs)) return true;
   }
-
-  // pass B: scaled weights w'(y) = S_p S_q w(y) and the inverse CDF.
-  // mode 0: target row (bonus, or the zero-mass fallback), 1: residual of
-  // two softmaxes, 2: residual against given draft probabilities.
+  // scaled weights w'(y) = S_p S_q w(y); mode 0: target row (bonus, or the
+  // zero-mass fallback), 1: two softmaxes, 2: given probabilities
   int mode = !has_draft ? 0 : (DK == 0 ? 1 : 2);
-  const int wr = ((nsp + kResWarps - 1) / kResWarps + 31) / 32 * 32;
-  const int w_lo = min(e1, e0 + warp * wr), w_hi = min(e1, w_lo + wr);
-  auto weight = [&](int e) -> ff {
-    const ff ep = ff_exp(to_f32(trow[e]), m_p, P, sh.tbl);
-    if (mode == 0) return ep;
-    if (mode == 1) {
-      const ff eq = ff_exp(to_f32(drow[e]), m_q, P, sh.tbl);
-      return ff_max0(ff_add(ff_mul(ep, Sq), ff_neg(ff_mul(eq, Sp))));
-    }
-    return ff_max0(ff_add(ep, ff_neg(ff_mul(ff{to_f32(drow[e]), 0.f}, Sp))));
-  };
-  auto scan32 = [&](ff v) {
+  auto wx8 = [&](int g, ff (&w)[8]) {
+    float xp[8], xq[8];
+    load8(st, g, xp);
+    if (has_draft) load8(sd, g, xq);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const ff t{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
-      if (lane >= o) v = ff_add(t, v);
+    for (int j = 0; j < 8; ++j) {
+      const ff ep = ffx_exp(xp[j], m_p, P, sh.tbl);
+      if (mode == 0) w[j] = ep;
+      else if (mode == 1) w[j] = ff_max0(ff_add(ff_mul(ep, Sq), ff_neg(ff_mul(ffx_exp(xq[j], m_q, P, sh.tbl), Sp))));
+      else w[j] = ff_max0(ff_add(ep, ff_neg(ff_mul(ff{xq[j], 0.f}, Sp))));
     }
-    return v;
   };
-
+  const int gpw = (n_grp + kResWarps - 1) / kResWarps;
+  const int g_lo = min(n_grp, warp * gpw), g_hi = min(n_grp, g_lo + gpw);
   int y = -1;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    // per-warp totals over contiguous ranges, and the last positive index
-    ff run{0.f, 0.f};
+    ff wrun{0.f, 0.f};
     int last_pos = -1;
-    for (int s0 = w_lo; s0 < w_hi; s0 += 32) {
-      const int e = s0 + lane;
-      const ff w = e < w_hi ? weight(e) : ff{0.f, 0.f};
-      const unsigned pos = __ballot_sync(0xffffffffu, w.hi > 0.f);
-      if (pos) last_pos = s0 + 31 - __clz(pos);
-      run = ff_add(run, shfl_ff(scan32(w), 31));
+    for (int s0 = g_lo, sidx = 0; s0 < g_hi; s0 += 32, ++sidx) {
+      const int g = s0 + lane;
+      ff gs{0.f, 0.f};
+      if (g < g_hi) {
+        ff w[8];
+        wx8(g, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc_add(gs, w[j]);
+          if (w[j].hi > 0.f) last_pos = e0 + 8 * g + j;
+        }
+      }
+      gs = ff_norm(gs);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gs = ff_add(gs, ff{__shfl_xor_sync(0xffffffffu, gs.hi, o),
+                                                         __shfl_xor_sync(0xffffffffu, gs.lo, o)});
+      if (lane == 0) sh.stepsum[warp][sidx] = gs;
+      wrun = ff_add(wrun, gs);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
     if (lane == 0) {
-      sh.wsum[warp] = run;
+      sh.wsum[warp] = wrun;
       if (last_pos >= 0) atomicMax(&sh.pub_last, last_pos);
     }
     __syncthreads();
     ff tot{0.f, 0.f};
     for (int w = 0; w < kResWarps; ++w) tot = ff_add(tot, sh.wsum[w]);
     if (tid == 0) sh.pub_tot = tot;
-    cluster_sync();
-    ff off_c{0.f, 0.f}, Z{0.f, 0.f};
+    cluster_sync();   // totals published
+    ff xoff{0.f, 0.f}, XZ{0.f, 0.f};
     int last_all = -1;
     for (int r = 0; r < cs; ++r) {
-      const uint32_t a = mapa(&sh.pub_tot, r);
-      const ff t{ld_dsmem_f32(a), ld_dsmem_f32(a + 4)};
-      if (r == rank) off_c = Z;
-      Z = ff_add(Z, t);
+      const ff t = ld_dsmem_ff(&sh.pub_tot, r);
+      if (r == rank) xoff = XZ;
+      XZ = ff_add(XZ, t);
       last_all = max(last_all, ld_dsmem_s32(mapa(&sh.pub_last, r)));
     }
-    cluster_sync();   // peers have read pub_tot / pub_last
+    cluster_sync();   // peers have read the totals
     if (tid == 0) sh.pub_last = -1;
-    if (!(Z.hi > 0.f)) {   // zero residual mass: draw from p_n instead
+    if (!ff_pos(XZ)) {   // zero residual mass: draw from p_n instead
       __syncthreads();
       if (mode == 0) break;
       mode = 0;
       continue;
     }
-    const ff thr = ff_mul(ff{uv[1], 0.f}, Z);
-    const ff end_c = ff_add(off_c, tot);
-    if (!ff_gt(off_c, thr) && ff_gt(end_c, thr)) {
-      ff woff{0.f, 0.f};
+    const ff xthr = ff_mul(ff{v_u, 0.f}, XZ);
+    if (!ff_gt(xoff, xthr) && ff_gt(ff_add(xoff, tot), xthr)) {
+      ff woff{0.f, 0.f}, a_w = xoff;
       int owner = kResWarps - 1;
-      ff a_w = off_c;
       for (int w = 0; w < kResWarps; ++w) {
         const ff nxt = ff_add(woff, sh.wsum[w]);
-        if (ff_gt(ff_add(off_c, nxt), thr) || w == kResWarps - 1) {
+        if (ff_gt(ff_add(xoff, nxt), xthr) || w == kResWarps - 1) {
           owner = w;
-          a_w = ff_add(off_c, woff);
+          a_w = ff_add(xoff, woff);
           break;
         }
         woff = nxt;
       }
       if (warp == owner) {
+        const int nsteps = (g_hi - g_lo + 31) / 32;
         ff base = a_w;
-        int found = -1, last_p = -1;
-        for (int s0 = w_lo; s0 < w_hi && found < 0; s0 += 32) {
-          const int e = s0 + lane;
-          const ff w = e < w_hi ? weight(e) : ff{0.f, 0.f};
-          const unsigned pos = __ballot_sync(0xffffffffu, w.hi > 0.f);
-          if (pos) last_p = s0 + 31 - __clz(pos);
-          const ff incl = scan32(w);
-          const unsigned hit =
-              __ballot_sync(0xffffffffu, w.hi > 0.f && ff_gt(ff_add(base, incl), thr));
-          if (hit) found = s0 + __ffs(hit) - 1;
-          base = ff_add(base, shfl_ff(incl, 31));
+        int sel = nsteps - 1;
+        for (int sidx = 0; sidx < nsteps; ++sidx) {
+          const ff nxt = ff_add(base, sh.stepsum[warp][sidx]);
+          if (ff_gt(nxt, xthr) || sidx == nsteps - 1) { sel = sidx; break; }
+          base = nxt;
         }
-        if (found < 0) found = last_p;   // crossing within rounding of the range end
+        int found = -1, last_p = -1;
+        if (nsteps > 0) {
+          const int g = g_lo + sel * 32 + lane;
+          ff w[8];
+          ff gs{0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[j] = ff{0.f, 0.f};
+          if (g < g_hi) {
+            wx8(g, w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc_add(gs, w[j]);
+          }
+          gs = ff_norm(gs);
+          const ff incl = scan32_ff(gs, lane);
+          int cand = -1;
+          ff run_c = ff_add(base, ff_add(incl, ff_neg(gs)));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const ff nxt = ff_add(run_c, w[j]);
+            if (cand < 0 && w[j].hi > 0.f && ff_gt(nxt, xthr)) cand = e0 + 8 * g + j;
+            if (w[j].hi > 0.f) last_p = max(last_p, e0 + 8 * g + j);
+            run_c = nxt;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
+          if (hit) found = __shfl_sync(0xffffffffu, cand, __ffs(hit) - 1);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) last_p = max(last_p, __shfl_xor_sync(0xffffffffu, last_p, o));
+        }
+        if (found < 0) found = last_p;   // crossing within rounding of the step end
         if (lane == 0) sh.pub_y = found;
       }
     }
-    cluster_sync();
+    cluster_sync();   // the draw is published
     for (int r = 0; r < cs; ++r) y = max(y, ld_dsmem_s32(mapa(&sh.pub_y, r)));
     if (y < 0) y = last_all;   // v Z at the very top of the range (rounding)
-    cluster_sync();            // peers have read pub_y
+    cluster_sync();   // peers have read pub_y
     if (tid == 0) sh.pub_y = -1;
     __syncthreads();
     break;
@@ -701,41 +777,163 @@ __device__ bool exact_row(const SampleParams &P, int b, int i, const RowRec &rec
   return false;
 }
 
+// One cluster per group of sequences. Every thread walks one sequence's
+// records (certified accepts, then the first rejection or the bonus row) and
+// the tokens of fully certified sequences are written at once. The few
+// sequences whose next needed decision is not certified are then processed
+// one by one by the whole cluster: the row's slices are copied into shared
+// memory and re-evaluated in float-float arithmetic, continuing the walk.
+constexpr int kFinishMaxSeq = kResThreads;   // sequences per cluster
+
 template <typename TT, int DK>
-__global__ void __launch_bounds__(kResThreads) sample_resolve_kernel(const __grid_constant__ SampleParams P) {
+__global__ void __launch_bounds__(kResThreads) sample_finish_kernel(const __grid_constant__ SampleParams P) {
+  using TD = typename std::conditional<DK == 0, TT, float>::type;
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ExactShared sh;
-  const int b = blockIdx.y;
-  const int K = P.K;
-  const int tid = threadIdx.x;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int list_n;
+  __shared__ int list_b[kFinishMaxSeq], list_i[kFinishMaxSeq];
+  __shared__ int warp_cnt[kResWarps];
+  const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+  const int cid = blockIdx.x / cs, ncl = gridDim.x / cs;
+  const int K = P.K, V = P.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
+  const int chunk = (P.B + ncl - 1) / ncl;
+  const int b0 = cid * chunk, b1 = min(P.B, b0 + chunk);
+  const int ns = P.ns_x;
+  const int e0 = min(V, rank * ns);
+  const int n_loc = max(0, min(V, e0 + ns) - e0);
+  const int n_grp = (n_loc + 7) >> 3;
+  TT *st = reinterpret_cast<TT *>(smem);
+  TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)ns * sizeof(TT), 128));
   if (tid < 64) sh.tbl[tid] = P.tbl[tid];
-  if (tid == 0) { sh.pub_y = -1; sh.pub_last = -1; }
+  if (tid == 0) {
+    sh.pub_y = -1; sh.pub_last = -1;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+
+  // ---- parallel walk: one thread per sequence -----------------------------
+  const int b = b0 + tid;
+  int start = -1;   // first position whose decision needs the float-float pass
+  if (b < b1) {
+    const RowRec *recs = P.recs + (int64_t)b * (K + 1);
+    int n = K;
+    for (int i = 0; i < K; ++i) {
+      const uint32_t f = recs[i].flags;
+      if (force || !(f & REC_ACC_CERT)) { start = i; break; }
+      if (!(f & REC_ACCEPT)) { n = i; break; }
+    }
+    if (start < 0) {
+      if (!force && (recs[n].flags & REC_DRAW_CERT)) {
+        if (rank == 0) {
+          const int y = recs[n].y;
+          for (int j = 0; j <= K; ++j)
+            P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? y : -1);
+          P.num_acc[b] = n;
+        }
+      } else {
+        start = n;
+      }
+    }
+  }
+  // deterministic compaction (same order in every CTA of the cluster)
+  const unsigned vote = __ballot_sync(0xffffffffu, start >= 0);
+  if (lane == 0) warp_cnt[warp] = __popc(vote);
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int w = 0; w < kResWarps; ++w) { const int t = warp_cnt[w]; warp_cnt[w] = acc; acc += t; }
+    list_n = acc;
+  }
+  __syncthreads();
+  if (start >= 0) {
+    const int pos = warp_cnt[warp] + __popc(vote & ((1u << lane) - 1u));
+    list_b[pos] = b;
+    list_i[pos] = start;
+  }
   __syncthreads();
   cluster_sync();   // peers initialised before any distributed read
-  const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
-  int n = K, y = -1;
-  bool have_y = false;
-  for (int i = 0; i < K; ++i) {
-    const RowRec rec = P.recs[(int64_t)b * (K + 1) + i];
-    bool acc;
-    if (!force && (rec.acc_flags & REC_ACC_CERTAIN)) {
-      acc = (rec.acc_flags & REC_ACCEPT) != 0;
-    } else {
+
+  // ---- float-float re-evaluation of the listed sequences ------------------
+  uint32_t phase = 0;
+  const bool vec = P.aligned != 0;
+  for (int li = 0; li < list_n; ++li) {
+    const int bb = list_b[li];
+    const RowRec *recs = P.recs + (int64_t)bb * (K + 1);
+    const int32_t *toks = P.tokens + (int64_t)bb * K;
+    int i = list_i[li], n = K, y = -1;
+    for (;;) {
+      // next position needing evaluation from i on (certified accepts skipped)
+      int need = -1;
+      bool need_acc = false;
+      for (; i < K; ++i) {
+        const uint32_t f = recs[i].flags;
+        if (force || !(f & REC_ACC_CERT)) { need = i; need_acc = true; break; }
+        if (!(f & REC_ACCEPT)) break;
+      }
+      n = min(i, K);
+      if (need < 0) {
+        if (!force && (recs[n].flags & REC_DRAW_CERT)) { y = recs[n].y; break; }
+        need = n;
+      }
+      const bool has_draft = need < K;
+      const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + need) * V;
+      const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + need) * V : nullptr;
+      // slice -> shared memory (bulk copy when rows are 16-byte aligned)
+      for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {
+        st[e] = pad_value<TT>(false);
+        if (has_draft) sd[e] = pad_value<TD>(DK == 1);
+      }
+      if (vec) {
+        if (tid == 0 && n_loc > 0) {
+          const uint32_t nbt = (uint32_t)n_loc * sizeof(TT), nbd = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
+          fence_proxy_async_shared();
+          mbar_arrive_expect_tx(&bar, nbt + nbd);
+          bulk_g2s(st, trow + e0, nbt, &bar);
+          if (has_draft) bulk_g2s(sd, drow + e0, nbd, &bar);
+        }
+        if (n_loc > 0) {
+          if (!mbar_wait(&bar, phase) && tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+          phase ^= 1u;
+        }
+      } else {
+        for (int e = tid; e < n_loc; e += blockDim.x) {
+          st[e] = trow[e0 + e];
+          if (has_draft) sd[e] = drow[e0 + e];
+        }
+      }
+      __syncthreads();
+      const RowRec rr = recs[need];
+      const float *uv = P.uniforms + ((int64_t)bb * (K + 1) + need) * 2;
+      float lp_x = 0.f, lq_x = 0.f;
+      if (has_draft) {
+        const int x = min(max(toks[need], 0), V - 1);
+        lp_x = to_f32(trow[x]);
+        lq_x = to_f32(drow[x]);
+      }
       int yy = -1;
-      acc = exact_row<TT, DK>(P, b, i, rec, true, &yy, sh);
-      if (!acc) { y = yy; have_y = true; }
+      const bool acc = exact_row<TT, DK>(P, sh, st, sd, n_grp, e0, has_draft, need_acc, rr.m_p, rr.m_q,
+                                         lp_x, lq_x, uv[0], uv[1], &yy);
+      if (rank == 0 && tid == 0) {
+        RowRec *w = P.recs + (int64_t)bb * (K + 1) + need;
+        w->flags = rr.flags | (need_acc ? REC_EXACT_ACC : 0u) | (acc ? 0u : REC_EXACT_DRAW);
+        if (!acc) w->y_exact = yy;
+      }
+      __syncthreads();   // the slice buffers are rewritten next
+      if (need_acc && acc) { i = need + 1; continue; }   // accepted: continue the walk
+      n = need;
+      y = yy;
+      break;
     }
-    if (!acc) { n = i; break; }
+    if (rank == 0) {
+      for (int j = tid; j <= K; j += blockDim.x)
+        P.out_tokens[(int64_t)bb * (K + 1) + j] = j < n ? toks[j] : (j == n ? y : -1);
+      if (tid == 0) P.num_acc[bb] = n;
+    }
   }
-  if (!have_y) {
-    const RowRec rec = P.recs[(int64_t)b * (K + 1) + n];
-    if (!force && (rec.smp_flags & SMP_CERTAIN)) y = rec.y;
-    else exact_row<TT, DK>(P, b, n, rec, false, &y, sh);
-  }
-  if (cluster_ctarank() == 0) {
-    for (int j = tid; j < K + 1; j += blockDim.x)
-      P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? y : -1);
-    if (tid == 0) P.num_acc[b] = n;
-  }
+  cluster_sync();   // no CTA leaves while a peer may still read its shared memory
 }
 
 // ------------------------------------------------------------------ host ---
@@ -747,40 +945,45 @@ void split_ff(double d, float &hi, float &lo) {
   lo = (float)(d - (double)hi);
 }
 
-template <typename TT, int DK>
-sv_status launch_sample(const SampleParams &P, int cs, size_t smem, cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(sample_rows_kernel<TT, DK>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(kMaxSliceSmem + 1024));
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(sample_rows_kernel<TT, DK>,
-                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  });
-  if (attr_err != cudaSuccess)
-    return fail(SV_ERR_CUDA, "spec_verify_sample: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+template <typename KernelT>
+cudaError_t launch_cluster(KernelT kernel, dim3 grid, int threads, size_t smem, int cs, cudaStream_t s,
+                           const SampleParams &P) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs, P.K + 1, P.B);
-  cfg.blockDim = dim3(kRowThreads);
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, sample_rows_kernel<TT, DK>, P);
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+template <typename TT, int DK>
+sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, size_t smem_x, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    const int lim = (int)(kMaxSliceSmem + 1024);
+    attr_err = cudaFuncSetAttribute(sample_rows_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(sample_rows_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(sample_finish_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(sample_finish_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(SV_ERR_CUDA, "spec_verify_sample: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  cudaError_t e = launch_cluster(sample_rows_kernel<TT, DK>, dim3(cs, P.K + 1, P.B), kRowThreads, smem, cs, s, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample rows launch: %s", cudaGetErrorString(e));
-  attr[0].val.clusterDim.x = kResCluster;
-  cfg.gridDim = dim3(kResCluster, P.B);
-  cfg.blockDim = dim3(kResThreads);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, sample_resolve_kernel<TT, DK>, P);
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample resolve launch: %s", cudaGetErrorString(e));
+  const int ncl = std::max(std::min(P.B, kFinishClusters), (P.B + kFinishMaxSeq - 1) / kFinishMaxSeq);
+  e = launch_cluster(sample_finish_kernel<TT, DK>, dim3(cs_x * ncl), kResThreads, smem_x, cs_x, s, P);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -825,35 +1028,35 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   if (B == 0) return ok();
 
   const int es_t = dtype_bytes(logit_dtype);
-  const int es_d = K > 0 ? (draft_is_probs ? 4 : es_t) : 0;
   int cs = 0;
   int ns = 0;
   size_t smem = 0;
-  auto smem_for = [&](int c, int &ns_out) {
-    ns_out = (int)align_up((size_t)((V + c - 1) / c), 8);
-    return align_up((size_t)ns_out * es_t, 128) + (size_t)ns_out * es_d;
+  // rows kernel: the smallest cluster whose slices take <= 64 KB (three CTAs
+  // per SM), else the smallest that fits at all
+  const int es_buf_d = (draft_is_probs && K > 0) ? 4 : es_t;
+  auto slice_smem = [&](int c, int &n) {
+    n = (int)align_up((size_t)((V + c - 1) / c), 8);
+    return align_up((size_t)n * es_t, 128) + align_up((size_t)n * es_buf_d, 128);
   };
-  for (int c = 1; c <= 16; c *= 2) {
-    int n;
-    const size_t sm = smem_for(c, n);
-    if (sm <= kTargetSliceSmem) { cs = c; ns = n; smem = sm; break; }
-  }
-  if (!cs) {
+  for (int pass = 0; pass < 2 && !cs; ++pass)
     for (int c = 1; c <= 16; c *= 2) {
       int n;
-      const size_t sm = smem_for(c, n);
-      if (sm <= kMaxSliceSmem) { cs = c; ns = n; smem = sm; break; }
+      const size_t sm = slice_smem(c, n);
+      if (sm <= (pass == 0 ? kTargetSliceSmem : kMaxSliceSmem)) { cs = c; ns = n; smem = sm; break; }
     }
-  }
+  // finish kernel: 16-CTA clusters (8 for small vocabularies)
+  const int cs_x = V >= 65536 ? 16 : 8;
+  int ns_x = 0;
+  const size_t smem_x = slice_smem(cs_x, ns_x);
   if (!cs) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large", V);
 
   SampleParams P = {};
   P.target = target_logits; P.draft = draft; P.tokens = draft_tokens; P.uniforms = uniforms;
   P.p_at = p_at_draft; P.q_at = q_at_draft; P.out_tokens = out_tokens; P.num_acc = num_accepted;
   P.recs = static_cast<RowRec *>(workspace); P.status = dev_status;
-  P.B = B; P.K = K; P.V = V; P.ns = ns; P.flags = flags;
+  P.B = B; P.K = K; P.V = V; P.ns = ns; P.ns_x = ns_x; P.flags = flags;
   P.aligned = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0 &&
-              (K == 0 || (aligned(draft, 16) && ((size_t)V * es_d) % 16 == 0));
+              (K == 0 || (aligned(draft, 16) && ((size_t)V * es_buf_d) % 16 == 0));
   const double log2e = 1.4426950408889634074, ln2 = 0.69314718055994530942;
   P.c = (float)(log2e / (double)temperature);
   P.unitT = temperature == 1.0f;
@@ -865,12 +1068,12 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool probs = draft_is_probs && K > 0;
   switch (logit_dtype) {
-    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, smem, s) : launch_sample<float, 0>(P, cs, smem, s);
+    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, smem, cs_x, smem_x, s) : launch_sample<float, 0>(P, cs, smem, cs_x, smem_x, s);
     case SV_BF16:
-      return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, smem, s)
-                   : launch_sample<__nv_bfloat16, 0>(P, cs, smem, s);
+      return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, smem, cs_x, smem_x, s)
+                   : launch_sample<__nv_bfloat16, 0>(P, cs, smem, cs_x, smem_x, s);
     default:
-      return probs ? launch_sample<__half, 1>(P, cs, smem, s) : launch_sample<__half, 0>(P, cs, smem, s);
+      return probs ? launch_sample<__half, 1>(P, cs, smem, cs_x, smem_x, s) : launch_sample<__half, 0>(P, cs, smem, cs_x, smem_x, s);
   }
 }
 

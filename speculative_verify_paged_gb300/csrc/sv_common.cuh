@@ -120,14 +120,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
   return done != 0;
 }
 
+// try_wait that lets the hardware suspend the thread (up to ~65 us) until
+// the phase completes, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t phase) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(phase), "r"(0x10000u)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait: returns false (and the caller reports SV_DEV_TIMEOUT) if the
 // phase did not complete within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase) {
   if (mbar_try_wait(bar, phase)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, phase)) return true;
-    if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, phase)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 
