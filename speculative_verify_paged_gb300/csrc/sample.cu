@@ -34,7 +34,7 @@
 namespace sv {
 namespace {
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kResThreads = 512;   // finish kernel
 constexpr int kResWarps = kResThreads / 32;
@@ -208,13 +208,15 @@ __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s
   m = mn;
 }
 
-__device__ __forceinline__ void warp_ms(float &m, float &s, float c) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    ms_combine(m, s, m2, s2, c);
-  }
+
+// Warp-wide combination of (m, s) pairs: the maximum first, then every lane
+// rescales its own sum to it (one ex2), then a plain sum. Butterfly
+// reductions leave identical bits in every lane.
+__device__ __forceinline__ void warp_ms_fast(float &m, float &s, float c) {
+  const float mx = warp_max(m);
+  s = (m == -INFINITY) ? 0.f : s * ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+  s = warp_sum(s);
+  m = mx;
 }
 
 template <typename T>
@@ -257,7 +259,7 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return r;
 }
 
-constexpr int kMaxSteps = 16;   // 32-group steps per warp range
+constexpr int kMaxSteps = 32;   // 32-group steps per warp range
 
 struct RowShared {
   uint64_t bars[kMaxChunks];
@@ -295,31 +297,28 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)P.ns * sizeof(TT), 128));
 
   // ---- stage the slice into shared memory --------------------------------
+  // target slice completes on bars[0], draft slice on bars[1]; each is cut
+  // into 16 KB bulk copies
   const uint32_t nb_t = (uint32_t)n_loc * sizeof(TT);
   const uint32_t nb_d = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
-  const int nch_t = P.aligned ? (int)((nb_t + kChunkBytes - 1) / kChunkBytes) : 0;
-  const int nch_d = P.aligned ? (int)((nb_d + kChunkBytes - 1) / kChunkBytes) : 0;
   for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {   // pad the last group
     st[e] = pad_value<TT>(false);
     if (has_draft) sd[e] = pad_value<TD>(DK == 1);
   }
   if (P.aligned) {
     if (tid == 0) {
-      for (int k = 0; k < nch_t + nch_d; ++k) mbar_init(&sh.bars[k], 1);
+      mbar_init(&sh.bars[0], 1);
+      mbar_init(&sh.bars[1], 1);
       fence_mbarrier_init();
       const uint8_t *gt = reinterpret_cast<const uint8_t *>(trow + e0);
-      for (int k = 0; k < nch_t; ++k) {
-        const uint32_t off = k * kChunkBytes, nb = min(kChunkBytes, nb_t - off);
-        mbar_arrive_expect_tx(&sh.bars[k], nb);
-        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, nb, &sh.bars[k]);
-      }
+      mbar_arrive_expect_tx(&sh.bars[0], nb_t);
+      for (uint32_t off = 0; off < nb_t; off += kChunkBytes)
+        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, min(kChunkBytes, nb_t - off), &sh.bars[0]);
       if (has_draft) {
         const uint8_t *gd = reinterpret_cast<const uint8_t *>(drow + e0);
-        for (int k = 0; k < nch_d; ++k) {
-          const uint32_t off = k * kChunkBytes, nb = min(kChunkBytes, nb_d - off);
-          mbar_arrive_expect_tx(&sh.bars[nch_t + k], nb);
-          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, nb, &sh.bars[nch_t + k]);
-        }
+        mbar_arrive_expect_tx(&sh.bars[1], nb_d);
+        for (uint32_t off = 0; off < nb_d; off += kChunkBytes)
+          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, min(kChunkBytes, nb_d - off), &sh.bars[1]);
       }
     }
     __syncthreads();   // barriers initialised before anyone waits on them
@@ -331,28 +330,15 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
     __syncthreads();
   }
 
-  // ---- pass A: online (max, sum of exp) as the chunks land ---------------
+  // ---- pass A: online (max, sum of exp) per thread ------------------------
   bool timed_out = false;
   float mt = -INFINITY, stt = 0.f, md = -INFINITY, sdd = 0.f;
-  {
-    constexpr int gpc_t = kChunkBytes / (8 * sizeof(TT));   // 8-element groups per chunk
-    const int nchunks = P.aligned ? nch_t : 1;
-    for (int k = 0; k < nchunks; ++k) {
-      if (P.aligned && !timed_out && !mbar_wait(&sh.bars[k], 0)) timed_out = true;
-      const int g_end = P.aligned ? min(n_grp, (k + 1) * gpc_t) : n_grp;
-      for (int g = (P.aligned ? k * gpc_t : 0) + tid; g < g_end; g += blockDim.x) online8(st, g, c, mt, stt);
-    }
-  }
+  if (P.aligned && n_loc > 0 && !mbar_wait(&sh.bars[0], 0)) timed_out = true;
+  for (int g = tid; g < n_grp; g += blockDim.x) online8(st, g, c, mt, stt);
   if (has_draft) {
-    constexpr int gpc_d = kChunkBytes / (8 * sizeof(TD));
-    const int nchunks = P.aligned ? nch_d : 1;
-    for (int k = 0; k < nchunks; ++k) {
-      if (P.aligned && !timed_out && !mbar_wait(&sh.bars[nch_t + k], 0)) timed_out = true;
-      if (DK == 0) {
-        const int g_end = P.aligned ? min(n_grp, (k + 1) * gpc_d) : n_grp;
-        for (int g = (P.aligned ? k * gpc_d : 0) + tid; g < g_end; g += blockDim.x) online8(sd, g, c, md, sdd);
-      }
-    }
+    if (P.aligned && n_loc > 0 && !timed_out && !mbar_wait(&sh.bars[1], 0)) timed_out = true;
+    if (DK == 0)
+      for (int g = tid; g < n_grp; g += blockDim.x) online8(sd, g, c, md, sdd);
   }
   if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
   int x_tok = 0;
@@ -364,15 +350,15 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
     }
   }
   const int x_rank = x_tok / P.ns;
-  warp_ms(mt, stt, c);
-  if (q_logits) warp_ms(md, sdd, c);
+  warp_ms_fast(mt, stt, c);
+  if (q_logits) warp_ms_fast(md, sdd, c);
   if (lane == 0) { sh.red_m[warp] = mt; sh.red_s[warp] = stt; sh.red_m2[warp] = md; sh.red_s2[warp] = sdd; }
   __syncthreads();
   if (warp == 0) {
     float m1 = lane < kRowWarps ? sh.red_m[lane] : -INFINITY, s1 = lane < kRowWarps ? sh.red_s[lane] : 0.f;
     float m2 = lane < kRowWarps ? sh.red_m2[lane] : -INFINITY, s2 = lane < kRowWarps ? sh.red_s2[lane] : 0.f;
-    warp_ms(m1, s1, c);
-    if (q_logits) warp_ms(m2, s2, c);
+    warp_ms_fast(m1, s1, c);
+    if (q_logits) warp_ms_fast(m2, s2, c);
     if (lane == 0) {
       sh.pub_mp = m1; sh.pub_sp = s1; sh.pub_mq = m2; sh.pub_sq = s2;
       if (has_draft && rank == x_rank) {   // the slice holding x_i publishes its logits
@@ -387,8 +373,8 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
     m_p = ld_dsmem_f32(mapa(&sh.pub_mp, lane)); S_p = ld_dsmem_f32(mapa(&sh.pub_sp, lane));
     m_q = ld_dsmem_f32(mapa(&sh.pub_mq, lane)); S_q = ld_dsmem_f32(mapa(&sh.pub_sq, lane));
   }
-  warp_ms(m_p, S_p, c);
-  if (q_logits) warp_ms(m_q, S_q, c);
+  warp_ms_fast(m_p, S_p, c);
+  if (q_logits) warp_ms_fast(m_q, S_q, c);
   else { m_q = 0.f; S_q = 1.f; }
   float lp_x = 0.f, lq_x = 0.f;
   if (has_draft) {
@@ -470,8 +456,8 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   // per-element exp / argument / ratio errors (~2^-22 relative, random:
   // sqrt(sum p^2) <= sqrt(max p) = sqrt(1/S)), and the rounding of the
   // running sums (~2^-24 per addition)
-  const float e_abs = 9.5367432e-07f * S_p * sqrtf(1.f / S_p + (q_logits ? 1.f / S_q : 0.f)) +
-                      2.3841858e-07f * (Z + S_p);   // 2^-20, 2^-22
+  const float e_abs = 4.7683716e-07f * S_p * sqrtf(1.f / S_p + (q_logits ? 1.f / S_q : 0.f)) +
+                      1.1920929e-07f * (Z + S_p);   // 2^-21, 2^-23
   const bool draw_ok = finite && Z > 0.f && thr < Z;
   RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
   if (rank == 0 && tid == 0) {
@@ -1038,16 +1024,26 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
     n = (int)align_up((size_t)((V + c - 1) / c), 8);
     return align_up((size_t)n * es_t, 128) + align_up((size_t)n * es_buf_d, 128);
   };
-  for (int pass = 0; pass < 2 && !cs; ++pass)
-    for (int c = 1; c <= 16; c *= 2) {
-      int n;
-      const size_t sm = slice_smem(c, n);
-      if (sm <= (pass == 0 ? kTargetSliceSmem : kMaxSliceSmem)) { cs = c; ns = n; smem = sm; break; }
-    }
+  for (int c = 1; c <= 16 && !cs; c *= 2) {
+    int n;
+    const size_t sm = slice_smem(c, n);
+    if (sm <= kTargetSliceSmem) { cs = c; ns = n; smem = sm; }
+  }
+  if (!cs) {
+    int n;
+    const size_t sm = slice_smem(16, n);
+    if (sm <= kMaxSliceSmem) { cs = 16; ns = n; smem = sm; }
+  }
+  // per-warp ranges of 32-group steps must fit the step tables
+  auto steps_ok = [&](int n_elems, int warps) {
+    const int grp = (n_elems + 7) / 8, gpw = (grp + warps - 1) / warps;
+    return (gpw + 31) / 32 <= kMaxSteps;
+  };
   // finish kernel: 16-CTA clusters (8 for small vocabularies)
   const int cs_x = V >= 65536 ? 16 : 8;
   int ns_x = 0;
   const size_t smem_x = slice_smem(cs_x, ns_x);
+  if (cs && (!steps_ok(ns, kRowWarps) || !steps_ok(ns_x, kResWarps) || smem_x > kMaxSliceSmem)) cs = 0;
   if (!cs) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large", V);
 
   SampleParams P = {};
