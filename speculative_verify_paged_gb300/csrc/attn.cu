@@ -41,11 +41,10 @@ namespace {
 constexpr int kD = 128;           // head dim of the tensor-core path
 constexpr int kBS = 16;           // block size of the tensor-core path
 constexpr int kNWK = 2;           // key groups = blocks per pipeline stage
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kMaxRT = 4;         // up to 64 packed query rows
 constexpr int kQStride = kD * 2 + 16;   // bytes per staged Q row (padded)
 constexpr int kTcAutoBps = 64;
-constexpr int kGenAutoBps = 8;
 constexpr int kGenThreads = 128;
 constexpr int kGenKeys = 32;
 
@@ -125,12 +124,13 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmk;
   CUtensorMap tmv;
   const void *q;
+  void *out;       // [B][n_new][H_q][kD] bf16, written directly when a sequence has one split
   const float *k_scale;
   const float *v_scale;
   const int32_t *block_table;
   const int32_t *seq_lens;
-  float *ws_acc;   // [B][H_kv][S*kNWK][R][kD]
-  float *ws_ml;    // [B][H_kv][S*kNWK][R][2]
+  float *ws_acc;   // [B][H_kv][S][R][kD]
+  float *ws_ml;    // [B][H_kv][S][R][2]
   int32_t *status;
   int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
   int role[3];        // tensor-map dims 1..3 hold (0 = slot, 1 = kv head, 2 = block)
@@ -153,10 +153,11 @@ struct TcCfg {
   static constexpr int kConvBytes = FP8 ? kNWK * 2 * 2 * (kBS * kD * 2) : 0;  // K,V f16 double-buffered
   static constexpr int kQBytes = RT * 16 * kQStride;
   static constexpr int kSmem = 1024 + kStageArea + kConvBytes + kQBytes;
+  static constexpr int kMinBlocks = RT <= 2 ? 3 : (RT == 3 ? 2 : 1);   // resident CTAs per SM the registers allow
 };
 
 template <int RT, bool FP8>
-__global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMinBlocks)
     attn_tc_kernel(const __grid_constant__ TcParams P) {
   using Cfg = TcCfg<RT, FP8>;
   constexpr bool F16 = FP8;   // fp8 tiles are widened to f16; bf16 stays bf16
@@ -217,41 +218,58 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
   __syncthreads();
 
   // ------------------------------------------------------------ producer ---
+  // The whole warp reads the block table 32 entries at a time (the next 32
+  // are prefetched); lane 0 waits for free stages and issues the copies.
   if (warp == 0) {
-    if (lane == 0) {
-      const int32_t *table = P.block_table + (int64_t)b * P.max_blocks;
-      bool ok_wait = true;
-      for (int it = 0; it < n_iter; ++it) {
+    const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
+    const int nblocks = blk1 - blk0;
+    int cur = lane < nblocks ? table[lane] : 0;
+    int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
+    int chunk = 0;
+    bool ok_wait = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int first = it * kNWK;
+      if ((first >> 5) != chunk) {
+        chunk = first >> 5;
+        cur = nxt;
+        const int rel = (chunk + 1) * 32 + lane;
+        nxt = rel < nblocks ? table[rel] : 0;
+      }
+      int phys[kNWK];
+#pragma unroll
+      for (int kk = 0; kk < kNWK; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
+      if (lane == 0) {
         const int st = it % kStages;
         if (it >= kStages && !mbar_wait(&empty_bar[st], ((it / kStages) & 1) ^ 1)) {
           ok_wait = false;   // consumers stopped: issue nothing more
-          break;
-        }
-        const int nvalid = min(kNWK, blk1 - (blk0 + it * kNWK));
-        mbar_arrive_expect_tx(&full_bar[st], (uint32_t)(nvalid * 2 * Cfg::kTile));
-        for (int kk = 0; kk < nvalid; ++kk) {
-          int phys = table[blk0 + it * kNWK + kk];
-          if (phys < 0 || phys >= P.num_blocks) {
-            atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
-            phys = 0;   // stay in bounds; the output of this sequence is flagged
-          }
-          const uint32_t kt = stage_base + st * Cfg::kStageBytes + kk * 2 * Cfg::kTile;
-          const uint32_t vt = kt + Cfg::kTile;
-          int c[3];
-          tile_coords(P, g, phys, c);
-          if (FP8) {
-            tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
-            tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
-          } else {
-            tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
-            tma_load_4d(kt + 2048, &P.tmk, 64, c[0], c[1], c[2], &full_bar[st]);
-            tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
-            tma_load_4d(vt + 2048, &P.tmv, 64, c[0], c[1], c[2], &full_bar[st]);
+        } else {
+          const int nvalid = min(kNWK, nblocks - first);
+          mbar_arrive_expect_tx(&full_bar[st], (uint32_t)(nvalid * 2 * Cfg::kTile));
+          for (int kk = 0; kk < nvalid; ++kk) {
+            int ph = phys[kk];
+            if (ph < 0 || ph >= P.num_blocks) {
+              atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+              ph = 0;   // stay in bounds; the output of this sequence is flagged
+            }
+            const uint32_t kt = stage_base + st * Cfg::kStageBytes + kk * 2 * Cfg::kTile;
+            const uint32_t vt = kt + Cfg::kTile;
+            int c[3];
+            tile_coords(P, g, ph, c);
+            if (FP8) {
+              tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
+              tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
+            } else {
+              tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
+              tma_load_4d(kt + 2048, &P.tmk, 64, c[0], c[1], c[2], &full_bar[st]);
+              tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
+              tma_load_4d(vt + 2048, &P.tmv, 64, c[0], c[1], c[2], &full_bar[st]);
+            }
           }
         }
       }
-      if (!ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      if (!__shfl_sync(0xffffffffu, (int)ok_wait, 0)) break;
     }
+    if (lane == 0 && !ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
     return;
   }
 
@@ -261,17 +279,10 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
   const int gq = lane >> 2, tq = lane & 3;
 
   // Q A-fragments for the 8 k-steps of d = 128
-  uint32_t qa[8][4];
-  {
-    const uint32_t qb = smem_u32(q_smem);
-    const int mi = lane >> 3;
-    const int row = rt * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int col = ks * 16 + (mi >> 1) * 8;
-      ldsm_x4(qb + row * kQStride + col * 2, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-    }
-  }
+  // Q A-fragments are re-read from shared memory for every block (keeps 32
+  // registers free for more resident warps)
+  const uint32_t q_addr = smem_u32(q_smem) + (rt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7)) * kQStride +
+                          ((lane >> 4) * 8) * 2;
   float scale_log2 = P.scale_log2;
   if (FP8) scale_log2 *= P.k_scale[g];
   const int r_lo = rt * 16 + gq, r_hi = r_lo + 8;
@@ -333,19 +344,33 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
     }
     if (lb < blk1) {
       // ---- S = Q K^T for the 16 keys of block lb -------------------------
-      float sacc[2][4];
+      // two independent accumulator chains (even / odd k-steps) halve the
+      // dependent MMA latency
+      float sacc[2][4], sacc2[2][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[n][e] = sacc2[n][e] = 0.f;
       {
         const int mi = lane >> 3;
         const int key = (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          uint32_t b0, b1, b2, b3;
+          uint32_t qa[4], b0, b1, b2, b3;
+          ldsm_x4(q_addr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
           ldsm_x4(swz16(kt, key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
-          mma16816<F16>(sacc[0], qa[ks], b0, b1);
-          mma16816<F16>(sacc[1], qa[ks], b2, b3);
+          if (ks & 1) {
+            mma16816<F16>(sacc2[0], qa, b0, b1);
+            mma16816<F16>(sacc2[1], qa, b2, b3);
+          } else {
+            mma16816<F16>(sacc[0], qa, b0, b1);
+            mma16816<F16>(sacc[1], qa, b2, b3);
+          }
         }
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[n][e] += sacc2[n][e];
       }
       // ---- masking (tail blocks only) and online softmax -------------------
       const int t0 = lb * kBS;
@@ -421,16 +446,62 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
   }
   if (!ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
 
-  // ---- write this (split, key group) partial --------------------------------
+  // ---- combine the two key groups of each row tile, then write -------------
+  static_assert(kNWK == 2, "the epilogue merges two key groups");
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  named_bar_sync(3, Cfg::kCompute * 32);   // every stage consumed: the ring is free
+  float *xbuf = reinterpret_cast<float *>(smem) + (rt * 32 + lane) * 68;
+  if (kg == 1) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+      *reinterpret_cast<float4 *>(xbuf + 4 * n) = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+    *reinterpret_cast<float4 *>(xbuf + 64) = make_float4(m_lo, m_hi, l_lo, l_hi);
+  }
+  named_bar_sync(3, Cfg::kCompute * 32);
+  if (kg != 0) return;
+  {
+    const float4 ml = *reinterpret_cast<const float4 *>(xbuf + 64);
+    const float mn_lo = fmaxf(m_lo, ml.x), mn_hi = fmaxf(m_hi, ml.y);
+    const float b_lo = mn_lo == -INFINITY ? 0.f : mn_lo, b_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+    const float a0l = exp2f(m_lo - b_lo), a1l = exp2f(ml.x - b_lo);
+    const float a0h = exp2f(m_hi - b_hi), a1h = exp2f(ml.y - b_hi);
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const float4 v = *reinterpret_cast<const float4 *>(xbuf + 4 * n);
+      o[n][0] = o[n][0] * a0l + v.x * a1l;
+      o[n][1] = o[n][1] * a0l + v.y * a1l;
+      o[n][2] = o[n][2] * a0h + v.z * a1h;
+      o[n][3] = o[n][3] * a0h + v.w * a1h;
+    }
+    l_lo = l_lo * a0l + ml.z * a1l;
+    l_hi = l_hi * a0h + ml.w * a1h;
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+  }
   const float vs = FP8 ? P.v_scale[g] : 1.f;
-  const int S2 = P.S * kNWK;
-  const int64_t ent = ((int64_t)b * P.H_kv + g) * S2 + (int64_t)s * kNWK + kg;
+  const int nsplit = (nblk + P.bps - 1) / P.bps;
+  if (nsplit == 1) {
+    // the whole sequence was this split: write the normalised output
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P.out);
+    const float il = l_lo > 0.f ? vs / l_lo : 0.f, ih = l_hi > 0.f ? vs / l_hi : 0.f;
+    auto orow = [&](int r) {
+      const int j = r / P.G, hh = r % P.G;
+      return out + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
+    };
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const int c = n * 8 + 2 * tq;
+      if (r_lo < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_lo) + c) = __floats2bfloat162_rn(o[n][0] * il, o[n][1] * il);
+      if (r_hi < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_hi) + c) = __floats2bfloat162_rn(o[n][2] * ih, o[n][3] * ih);
+    }
+    return;
+  }
+  const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
   float *acc = P.ws_acc + ent * P.R * kD;
-  float *ml = P.ws_ml + ent * P.R * 2;
+  float *mlp = P.ws_ml + ent * P.R * 2;
 #pragma unroll
   for (int n = 0; n < 16; ++n) {
     const int c = n * 8 + 2 * tq;
@@ -438,14 +509,15 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, 1)
     if (r_hi < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_hi * kD + c) = make_float2(o[n][2] * vs, o[n][3] * vs);
   }
   if (tq == 0) {
-    if (r_lo < P.R) { ml[r_lo * 2] = m_lo; ml[r_lo * 2 + 1] = l_lo; }
-    if (r_hi < P.R) { ml[r_hi * 2] = m_hi; ml[r_hi * 2 + 1] = l_hi; }
+    if (r_lo < P.R) { mlp[r_lo * 2] = m_lo; mlp[r_lo * 2 + 1] = l_lo; }
+    if (r_hi < P.R) { mlp[r_hi * 2] = m_hi; mlp[r_hi * 2 + 1] = l_hi; }
   }
 }
 
 // ----------------------------------------------------- CUDA-core kernel ---
 struct GenParams {
   const void *q;
+  void *out;
   const void *k_cache;
   const void *v_cache;
   const float *k_scale;
@@ -568,6 +640,17 @@ __global__ void __launch_bounds__(kGenThreads) attn_generic_kernel(const __grid_
     }
     __syncthreads();
   }
+  if ((nblk + P.bps - 1) / P.bps == 1) {   // single split: write the normalised output
+    for (int idx = tid; idx < R * d; idx += blockDim.x) {
+      const int r = idx / d, cc = idx % d;
+      const int j = r / P.G, hh = r % P.G;
+      const int64_t off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * d + cc;
+      const float v = l_s[r] > 0.f ? o_s[idx] / l_s[r] : 0.f;
+      if (std::is_same<TQ, float>::value) static_cast<float *>(P.out)[off] = v;
+      else static_cast<__nv_bfloat16 *>(P.out)[off] = __float2bfloat16_rn(v);
+    }
+    return;
+  }
   const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
   for (int idx = tid; idx < R * d; idx += blockDim.x) P.ws_acc[ent * R * d + idx] = o_s[idx];
   for (int r = tid; r < R; r += blockDim.x) {
@@ -592,6 +675,7 @@ __global__ void attn_merge_kernel(const __grid_constant__ MergeParams P) {
   if (L < P.n_new || L > P.max_blocks * P.bs) return;
   const int nblk = (L + P.bs - 1) / P.bs;
   const int nsplit = (nblk + P.bps - 1) / P.bps;
+  if (nsplit == 1) return;   // written directly by the attention kernel
   const int S2 = P.S * P.per_split;
   const int n_ent = nsplit * P.per_split;
   const int64_t ent0 = ((int64_t)b * P.H_kv + g) * S2;
@@ -639,6 +723,26 @@ struct Plan {
   int R, S, bps, per_split, d;
 };
 
+int num_sms() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+  });
+  return n;
+}
+
+int pow2_floor(int64_t x) {
+  int p = 1;
+  while ((int64_t)p * 2 <= x) p *= 2;
+  return p;
+}
+
+// Split size (blocks per CTA): large enough that the fp32 partials a split
+// writes stay within ~4 % of the KV bytes it reads, small enough that there
+// are at least four waves of CTAs when the batch allows it.
 Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int bs, sv_dtype kv, sv_dtype qd,
                const sv_kv_layout *lay, int bps_req) {
   Plan p;
@@ -651,10 +755,19 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
                  (lay->slot_stride * es) % 16 == 0;
   p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS && p.R <= 16 * kMaxRT &&
          strides_ok;
-  p.bps = bps_req > 0 ? bps_req : (p.tc ? kTcAutoBps : kGenAutoBps);
+  if (bps_req > 0) {
+    p.bps = bps_req;
+  } else {
+    // fp32 caches are planned like bf16 ones so every dtype fits the same
+    // workspace
+    const double kv_per_block = 2.0 * bs * d * (kv == SV_FP8_E4M3 ? 1 : 2);
+    const double partial = (double)p.R * (d + 2) * 4;
+    const int min_bps = std::min(512, std::max(16, 2 * pow2_floor((int64_t)(partial / (0.04 * kv_per_block)))));
+    const int max_bps = std::max(16, pow2_floor((int64_t)max_blocks * B * H_kv / (4 * num_sms())));
+    p.bps = std::min(min_bps, max_bps);
+  }
   p.S = (max_blocks + p.bps - 1) / p.bps;
-  p.per_split = p.tc ? kNWK : 1;
-  (void)B;
+  p.per_split = 1;
   return p;
 }
 
@@ -779,7 +892,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
-    P.q = q; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
+    P.q = q; P.out = out; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
     P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
@@ -797,7 +910,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     }
   } else {
     GenParams P;
-    P.q = q; P.k_cache = k_cache; P.v_cache = v_cache; P.k_scale = k_scale; P.v_scale = v_scale;
+    P.q = q; P.out = out; P.k_cache = k_cache; P.v_cache = v_cache; P.k_scale = k_scale; P.v_scale = v_scale;
     P.block_table = block_table; P.seq_lens = seq_lens; P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R; P.d = d_head; P.bs = block_size;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
@@ -818,14 +931,24 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
   return check_launch("spec_verify_attn merge launch");
 }
 
+// The plan depends on the cache dtype; size for the largest of them.
+static size_t ws_bytes_any(int B, int n_new, int H_q, int H_kv, int d_head, int max_blocks_per_seq,
+                           int block_size, int bps) {
+  size_t best = 0;
+  const sv_dtype kvs[3] = {SV_BF16, SV_FP8_E4M3, SV_F32};
+  for (sv_dtype kv : kvs) {
+    const sv_dtype qd = kv == SV_F32 ? SV_F32 : SV_BF16;
+    Plan p = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, kv, qd, nullptr, bps);
+    best = std::max(best, ws_bytes(p, B, H_kv));
+  }
+  return best;
+}
+
 extern "C" size_t spec_verify_attn_workspace_size(int B, int n_new, int H_q, int H_kv, int d_head,
                                                   int max_blocks_per_seq, int block_size) {
   if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_head < 1 || max_blocks_per_seq < 1)
     return 0;
-  // the tensor-core plan needs the most entries per split; size for it
-  Plan p = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_BF16, SV_BF16, nullptr, 0);
-  Plan g = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_F32, SV_F32, nullptr, 0);
-  return std::max(ws_bytes(p, B, H_kv), ws_bytes(g, B, H_kv));
+  return ws_bytes_any(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, 0);
 }
 
 extern "C" size_t spec_verify_attn_workspace_size_ex(int B, int n_new, int H_q, int H_kv, int d_head,
@@ -833,11 +956,7 @@ extern "C" size_t spec_verify_attn_workspace_size_ex(int B, int n_new, int H_q, 
                                                      int blocks_per_split) {
   if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_head < 1 || max_blocks_per_seq < 1)
     return 0;
-  Plan p = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_BF16, SV_BF16, nullptr,
-                     blocks_per_split);
-  Plan g = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, SV_F32, SV_F32, nullptr,
-                     blocks_per_split);
-  return std::max(ws_bytes(p, B, H_kv), ws_bytes(g, B, H_kv));
+  return ws_bytes_any(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, blocks_per_split);
 }
 
 extern "C" sv_status spec_verify_attn(const void *q, sv_dtype q_dtype, const void *k_cache, const void *v_cache,

@@ -42,9 +42,13 @@ def test_workspace_sizes(lib):
     assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == 64 * 5 * 48 // 256 * 256 + (256 if 64 * 5 * 48 % 256 else 0)
     assert lib.spec_verify_sample_workspace_size(0, 4, 10) == 0
     s = lib.spec_verify_attn_workspace_size(64, 5, 64, 8, 128, 512, 16)
-    # (acc d + m + l) floats per (sequence, kv head, split entry, row)
-    entries = 64 * 8 * 8 * 2 * 40
-    assert s >= entries * (128 + 2) * 4
+    # (acc d + m + l) floats per (sequence, kv head, split, row); splits of at
+    # least 16 blocks
+    assert s >= 64 * 8 * 1 * 40 * (128 + 2) * 4
+    assert s <= 64 * 8 * (512 // 16) * 40 * (128 + 2) * 4 + 4096
+    # an explicit split size: ceil(512 / 7) splits
+    s7 = lib.spec_verify_attn_workspace_size_ex(64, 5, 64, 8, 128, 512, 16, 7)
+    assert s7 >= 64 * 8 * 74 * 40 * (128 + 2) * 4
     assert lib.spec_verify_attn_workspace_size(1, 5, 6, 4, 128, 8, 16) == 0   # H_q % H_kv
 
 
