@@ -40,8 +40,8 @@ namespace {
 // ------------------------------------------------------------ constants ---
 constexpr int kD = 128;           // head dim of the tensor-core path
 constexpr int kBS = 16;           // block size of the tensor-core path
-constexpr int kNWK = 2;           // key groups = blocks per pipeline stage
-constexpr int kStages = 4;
+constexpr int kNWK = 2;           // key groups (consumer warps per row tile)
+constexpr int kMaxStages = 6;
 constexpr int kMaxRT = 4;         // up to 64 packed query rows
 constexpr int kQStride = kD * 2 + 16;   // bytes per staged Q row (padded)
 constexpr int kTcAutoBps = 64;
@@ -146,9 +146,14 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 template <int RT, bool FP8>
 struct TcCfg {
   static constexpr int kCompute = RT * kNWK;              // consumer warps
+  // blocks a consumer warp takes per pipeline step (two give it four
+  // independent MMA chains); fp8 tiles are widened one block at a time
+  static constexpr int kBPW = FP8 ? 1 : 2;
+  static constexpr int kBlocksPerStage = kNWK * kBPW;
+  static constexpr int kStages = FP8 ? 6 : (RT <= 2 ? 2 : 3);
   static constexpr int kThreads = 32 * (kCompute + 1);     // + producer warp
   static constexpr int kTile = FP8 ? kBS * kD : kBS * kD * 2;   // one K or V tile in bytes
-  static constexpr int kStageBytes = kNWK * 2 * kTile;
+  static constexpr int kStageBytes = kBlocksPerStage * 2 * kTile;
   static constexpr int kStageArea = kStages * kStageBytes;
   static constexpr int kConvBytes = FP8 ? kNWK * 2 * 2 * (kBS * kD * 2) : 0;  // K,V f16 double-buffered
   static constexpr int kQBytes = RT * 16 * kQStride;
@@ -162,8 +167,9 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
   using Cfg = TcCfg<RT, FP8>;
   constexpr bool F16 = FP8;   // fp8 tiles are widened to f16; bf16 stays bf16
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  constexpr int kStages = Cfg::kStages, kBPW = Cfg::kBPW, kBPS = Cfg::kBlocksPerStage;
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
   const int blk0 = s * P.bps;
   if (blk0 >= nblk) return;                       // the merge never reads this split
   const int blk1 = min(nblk, blk0 + P.bps);
-  const int n_iter = (blk1 - blk0 + kNWK - 1) / kNWK;
+  const int n_iter = (blk1 - blk0 + kBPS - 1) / kBPS;
 
   if (tid == 0) {
     for (int k = 0; k < kStages; ++k) {
@@ -228,22 +234,22 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
     int chunk = 0;
     bool ok_wait = true;
     for (int it = 0; it < n_iter; ++it) {
-      const int first = it * kNWK;
+      const int first = it * kBPS;
       if ((first >> 5) != chunk) {
         chunk = first >> 5;
         cur = nxt;
         const int rel = (chunk + 1) * 32 + lane;
         nxt = rel < nblocks ? table[rel] : 0;
       }
-      int phys[kNWK];
+      int phys[kBPS];
 #pragma unroll
-      for (int kk = 0; kk < kNWK; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
+      for (int kk = 0; kk < kBPS; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
       if (lane == 0) {
         const int st = it % kStages;
         if (it >= kStages && !mbar_wait(&empty_bar[st], ((it / kStages) & 1) ^ 1)) {
           ok_wait = false;   // consumers stopped: issue nothing more
         } else {
-          const int nvalid = min(kNWK, nblocks - first);
+          const int nvalid = min(kBPS, nblocks - first);
           mbar_arrive_expect_tx(&full_bar[st], (uint32_t)(nvalid * 2 * Cfg::kTile));
           for (int kk = 0; kk < nvalid; ++kk) {
             int ph = phys[kk];
@@ -301,11 +307,15 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
     // after a timed-out wait this warp stops waiting but keeps its place in
     // every named barrier (it then computes on stale tiles; status reports it)
     if (ok_wait && !mbar_wait(&full_bar[st], (it / kStages) & 1)) ok_wait = false;
-    const int lb = blk0 + it * kNWK + kg;           // logical block of this warp
-    const int nvalid_stage = min(kNWK, blk1 - (blk0 + it * kNWK));
-    uint32_t kt = stage_base + st * Cfg::kStageBytes + kg * 2 * Cfg::kTile;
-    uint32_t vt = kt + Cfg::kTile;
-    if (FP8) {
+    const int lbase = blk0 + it * kBPS + kg * kBPW;     // first logical block of this warp
+    const int nvalid_stage = min(kBPS, blk1 - (blk0 + it * kBPS));
+    uint32_t kt[kBPW], vt[kBPW];
+#pragma unroll
+    for (int j = 0; j < kBPW; ++j) {
+      kt[j] = stage_base + st * Cfg::kStageBytes + (kg * kBPW + j) * 2 * Cfg::kTile;
+      vt[j] = kt[j] + Cfg::kTile;
+    }
+    if constexpr (FP8) {
       // widen this key group's K and V tiles to f16 (same swizzled layout);
       // the RT warps of the key group share the work, then sync by name.
       const uint32_t ck = conv_base + (kg * 2 + (it & 1)) * 2 * 4096;
@@ -315,7 +325,7 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
           const int which = idx / (kBS * (kD / 16));
           const int rem = idx % (kBS * (kD / 16));
           const int row = rem / (kD / 16), ch = rem % (kD / 16);   // 16-byte chunk of 16 codes
-          const uint32_t src = (which ? vt : kt) + row * 128 + ((ch ^ (row & 7)) << 4);
+          const uint32_t src = (which ? vt[0] : kt[0]) + row * 128 + ((ch ^ (row & 7)) << 4);
           uint4 raw;
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
@@ -336,58 +346,85 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
         }
       }
       named_bar_sync(1 + kg, RT * 32);
-      kt = ck;
-      vt = cv;
+      kt[0] = ck;
+      vt[0] = cv;
       // the fp8 stage is no longer needed
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
-    if (lb < blk1) {
-      // ---- S = Q K^T for the 16 keys of block lb -------------------------
-      // two independent accumulator chains (even / odd k-steps) halve the
-      // dependent MMA latency
-      float sacc[2][4], sacc2[2][4];
+    if (lbase < blk1) {
+      // ---- S = Q K^T for the 16 * kBPW keys of this warp ---------------------
+      constexpr int NT = 2 * kBPW;   // n8 key tiles
+      float sacc[NT][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[n][e] = sacc2[n][e] = 0.f;
+      for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
       {
         const int mi = lane >> 3;
         const int key = (mi >> 1) * 8 + (lane & 7);
+        if constexpr (kBPW == 1) {
+          // two independent chains (even / odd k-steps) for a single block
+          float sacc2[2][4];
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t qa[4], b0, b1, b2, b3;
-          ldsm_x4(q_addr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
-          ldsm_x4(swz16(kt, key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
-          if (ks & 1) {
-            mma16816<F16>(sacc2[0], qa, b0, b1);
-            mma16816<F16>(sacc2[1], qa, b2, b3);
-          } else {
-            mma16816<F16>(sacc[0], qa, b0, b1);
-            mma16816<F16>(sacc[1], qa, b2, b3);
+          for (int n = 0; n < 2; ++n) sacc2[n][0] = sacc2[n][1] = sacc2[n][2] = sacc2[n][3] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t qa[4], b0, b1, b2, b3;
+            ldsm_x4(q_addr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
+            ldsm_x4(swz16(kt[0], key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+            if (ks & 1) {
+              mma16816<F16>(sacc2[0], qa, b0, b1);
+              mma16816<F16>(sacc2[1], qa, b2, b3);
+            } else {
+              mma16816<F16>(sacc[0], qa, b0, b1);
+              mma16816<F16>(sacc[1], qa, b2, b3);
+            }
+          }
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[n][e] += sacc2[n][e];
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t qa[4];
+            ldsm_x4(q_addr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
+#pragma unroll
+            for (int j = 0; j < kBPW; ++j) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(swz16(kt[j], key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+              mma16816<F16>(sacc[2 * j], qa, b0, b1);
+              mma16816<F16>(sacc[2 * j + 1], qa, b2, b3);
+            }
           }
         }
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[n][e] += sacc2[n][e];
       }
-      // ---- masking (tail blocks only) and online softmax -------------------
-      const int t0 = lb * kBS;
-      const bool tail = t0 + kBS - 1 > L - P.n_new;
-      float x[2][4];
+      // ---- masking (tail / missing blocks only) and online softmax -----------
+      float x[NT][4];
+      int nvk[kBPW];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
+      for (int j = 0; j < kBPW; ++j) {
+        const int lb = lbase + j;
+        const int t0 = lb * kBS;
+        const bool valid = lb < blk1;
+        nvk[j] = valid ? L - t0 : 0;   // valid keys of the block (>= 16 unless tail)
+        const bool tail = !valid || t0 + kBS - 1 > L - P.n_new;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = t0 + n * 8 + 2 * tq + (e & 1);
-          const int lim = (e < 2) ? lim_lo : lim_hi;
-          const float v = sacc[n][e] * scale_log2;
-          x[n][e] = (!tail || t <= lim) ? v : -INFINITY;
+        for (int n = 0; n < 2; ++n) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = t0 + n * 8 + 2 * tq + (e & 1);
+            const int lim = (e < 2) ? lim_lo : lim_hi;
+            const float v = sacc[2 * j + n][e] * scale_log2;
+            x[2 * j + n][e] = (!tail || (valid && t <= lim)) ? v : -INFINITY;
+          }
         }
       }
-      float mx_lo = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-      float mx_hi = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        mx_lo = fmaxf(mx_lo, fmaxf(x[n][0], x[n][1]));
+        mx_hi = fmaxf(mx_hi, fmaxf(x[n][2], x[n][3]));
+      }
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
@@ -398,48 +435,61 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
       const float a_lo = exp2f(m_lo - base_lo), a_hi = exp2f(m_hi - base_hi);
       m_lo = mn_lo;
       m_hi = mn_hi;
-      float p[2][4];
+      float ps_lo = 0.f, ps_hi = 0.f;
+      uint32_t pa[kBPW][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        p[n][0] = exp2f(x[n][0] - base_lo);
-        p[n][1] = exp2f(x[n][1] - base_lo);
-        p[n][2] = exp2f(x[n][2] - base_hi);
-        p[n][3] = exp2f(x[n][3] - base_hi);
+      for (int j = 0; j < kBPW; ++j) {
+        float pv[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          pv[n][0] = exp2f(x[2 * j + n][0] - base_lo);
+          pv[n][1] = exp2f(x[2 * j + n][1] - base_lo);
+          pv[n][2] = exp2f(x[2 * j + n][2] - base_hi);
+          pv[n][3] = exp2f(x[2 * j + n][3] - base_hi);
+          ps_lo += pv[n][0] + pv[n][1];
+          ps_hi += pv[n][2] + pv[n][3];
+        }
+        pa[j][0] = pack2<F16>(pv[0][0], pv[0][1]);
+        pa[j][1] = pack2<F16>(pv[0][2], pv[0][3]);
+        pa[j][2] = pack2<F16>(pv[1][0], pv[1][1]);
+        pa[j][3] = pack2<F16>(pv[1][2], pv[1][3]);
       }
-      l_lo = l_lo * a_lo + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-      l_hi = l_hi * a_hi + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+      l_lo = l_lo * a_lo + ps_lo;
+      l_hi = l_hi * a_hi + ps_hi;
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
         o[n][0] *= a_lo; o[n][1] *= a_lo;
         o[n][2] *= a_hi; o[n][3] *= a_hi;
       }
-      uint32_t pa[4];
-      pa[0] = pack2<F16>(p[0][0], p[0][1]);
-      pa[1] = pack2<F16>(p[0][2], p[0][3]);
-      pa[2] = pack2<F16>(p[1][0], p[1][1]);
-      pa[3] = pack2<F16>(p[1][2], p[1][3]);
       // ---- O += P V ---------------------------------------------------------
-      // keys at or past L in the tail block may hold anything: zero them
-      const int nvk = L - t0;   // valid keys in this block (>= 16 unless tail)
+      // keys at or past L (tail block, or a block past the split) may hold
+      // anything: their V entries are zeroed
       const int k0 = 2 * tq;    // keys k0, k0+1 (b0) and k0+8, k0+9 (b1)
-      const uint32_t m0 = (k0 < nvk ? 0x0000ffffu : 0u) | (k0 + 1 < nvk ? 0xffff0000u : 0u);
-      const uint32_t m1 = (k0 + 8 < nvk ? 0x0000ffffu : 0u) | (k0 + 9 < nvk ? 0xffff0000u : 0u);
+      uint32_t m0[kBPW], m1[kBPW];
+#pragma unroll
+      for (int j = 0; j < kBPW; ++j) {
+        m0[j] = (k0 < nvk[j] ? 0x0000ffffu : 0u) | (k0 + 1 < nvk[j] ? 0xffff0000u : 0u);
+        m1[j] = (k0 + 8 < nvk[j] ? 0x0000ffffu : 0u) | (k0 + 9 < nvk[j] ? 0xffff0000u : 0u);
+      }
       {
         const int mi = lane >> 3;
         const int key = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int np = 0; np < 8; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(swz16(vt, key, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
-          if (nvk < kBS) {
-            b0 &= m0; b1 &= m1; b2 &= m0; b3 &= m1;
+#pragma unroll
+          for (int j = 0; j < kBPW; ++j) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(swz16(vt[j], key, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
+            if (nvk[j] < kBS) {
+              b0 &= m0[j]; b1 &= m1[j]; b2 &= m0[j]; b3 &= m1[j];
+            }
+            mma16816<F16>(o[2 * np], pa[j], b0, b1);
+            mma16816<F16>(o[2 * np + 1], pa[j], b2, b3);
           }
-          mma16816<F16>(o[2 * np], pa, b0, b1);
-          mma16816<F16>(o[2 * np + 1], pa, b2, b3);
         }
       }
     }
-    if (!FP8) {
+    if constexpr (!FP8) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
