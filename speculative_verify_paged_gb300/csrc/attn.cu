@@ -718,37 +718,118 @@ struct MergeParams {
   int B, n_new, H_q, H_kv, G, R, d, bs, max_blocks, bps, S, per_split;
 };
 
-template <typename TO>
-__global__ void attn_merge_kernel(const __grid_constant__ MergeParams P) {
-  const int r = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int L = P.seq_lens[b];
-  if (L < P.n_new || L > P.max_blocks * P.bs) return;
-  const int nblk = (L + P.bs - 1) / P.bs;
-  const int nsplit = (nblk + P.bps - 1) / P.bps;
-  if (nsplit == 1) return;   // written directly by the attention kernel
-  const int S2 = P.S * P.per_split;
-  const int n_ent = nsplit * P.per_split;
-  const int64_t ent0 = ((int64_t)b * P.H_kv + g) * S2;
-  float m = -INFINITY;
-  for (int e = 0; e < n_ent; ++e) m = fmaxf(m, P.ws_ml[((ent0 + e) * P.R + r) * 2]);
-  const float base = m == -INFINITY ? 0.f : m;
-  float lsum = 0.f;
-  for (int e = 0; e < n_ent; ++e) {
-    const float me = P.ws_ml[((ent0 + e) * P.R + r) * 2];
-    lsum += P.ws_ml[((ent0 + e) * P.R + r) * 2 + 1] * exp2f(me - base);
+// Split merge: WPR warps per output row (sequence, kv head, packed query row),
+// each taking every WPR-th split in one pass with a running maximum (lanes
+// own float4 column chunks); the warps' states are then combined through
+// shared memory by the row's first warp.
+template <typename TO, int WPR>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams P) {
+  constexpr int kMaxChunks = 2;   // d <= 256
+  __shared__ float4 xs_acc[8][kMaxChunks][32];
+  __shared__ float xs_ml[8][2];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wr = warp % WPR;                       // warp within the row group
+  const int64_t rowid = (int64_t)blockIdx.x * (8 / WPR) + warp / WPR;
+  const int R = P.R;
+  const bool live = rowid < (int64_t)P.B * P.H_kv * R;
+  int nsplit = 0, r = 0, g = 0, b = 0;
+  int64_t bg = 0;
+  if (live) {
+    r = (int)(rowid % R);
+    bg = rowid / R;
+    g = (int)(bg % P.H_kv);
+    b = (int)(bg / P.H_kv);
+    const int L = P.seq_lens[b];
+    if (L >= P.n_new && L <= P.max_blocks * P.bs) {
+      const int nblk = (L + P.bs - 1) / P.bs;
+      nsplit = (nblk + P.bps - 1) / P.bps;
+    }
   }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const int nc = P.d >> 2;   // float4 chunks per row
+  float4 acc[kMaxChunks];
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float m = -INFINITY, l = 0.f;
+  if (nsplit > 1) {
+#pragma unroll 4
+    for (int e = wr; e < nsplit; e += WPR) {
+      const int64_t row = (bg * P.S + e) * R + r;
+      const float me = P.ws_ml[row * 2], le = P.ws_ml[row * 2 + 1];
+      const float mn = fmaxf(m, me);
+      const float base = mn == -INFINITY ? 0.f : mn;
+      const float a = exp2f(m - base), w = exp2f(me - base);
+      l = l * a + le * w;
+      m = mn;
+      const float4 *src = reinterpret_cast<const float4 *>(P.ws_acc + row * P.d);
+#pragma unroll
+      for (int k = 0; k < kMaxChunks; ++k) {
+        const int cidx = lane + 32 * k;
+        if (cidx < nc) {
+          const float4 v = src[cidx];
+          acc[k].x = acc[k].x * a + v.x * w;
+          acc[k].y = acc[k].y * a + v.y * w;
+          acc[k].z = acc[k].z * a + v.z * w;
+          acc[k].w = acc[k].w * a + v.w * w;
+        }
+      }
+    }
+  }
+  if constexpr (WPR > 1) {
+#pragma unroll
+    for (int k = 0; k < kMaxChunks; ++k) xs_acc[warp][k][lane] = acc[k];
+    if (lane == 0) { xs_ml[warp][0] = m; xs_ml[warp][1] = l; }
+    __syncthreads();
+    if (wr == 0) {
+      for (int w2 = 1; w2 < WPR; ++w2) {
+        const float me = xs_ml[warp + w2][0], le = xs_ml[warp + w2][1];
+        const float mn = fmaxf(m, me);
+        const float base = mn == -INFINITY ? 0.f : mn;
+        const float a = exp2f(m - base), w = exp2f(me - base);
+        l = l * a + le * w;
+        m = mn;
+#pragma unroll
+        for (int k = 0; k < kMaxChunks; ++k) {
+          const float4 v = xs_acc[warp + w2][k][lane];
+          acc[k].x = acc[k].x * a + v.x * w;
+          acc[k].y = acc[k].y * a + v.y * w;
+          acc[k].z = acc[k].z * a + v.z * w;
+          acc[k].w = acc[k].w * a + v.w * w;
+        }
+      }
+    }
+  }
+  // nsplit == 1: written directly by the attention kernel
+  if (!live || nsplit <= 1 || wr != 0) return;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
   const int j = r / P.G, hh = r % P.G;
   const int64_t out_off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * P.d;
-  for (int c = threadIdx.x; c < P.d; c += blockDim.x) {
-    float acc = 0.f;
-    for (int e = 0; e < n_ent; ++e) {
-      const float me = P.ws_ml[((ent0 + e) * P.R + r) * 2];
-      acc += P.ws_acc[((ent0 + e) * P.R + r) * P.d + c] * exp2f(me - base);
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int cidx = lane + 32 * k;
+    if (cidx < nc) {
+      const float4 v = acc[k];
+      if constexpr (std::is_same<TO, float>::value) {
+        reinterpret_cast<float4 *>(static_cast<float *>(P.out) + out_off)[cidx] =
+            make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+      } else {
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(P.out) + out_off + 4 * cidx;
+        *reinterpret_cast<__nv_bfloat162 *>(o) = __floats2bfloat162_rn(v.x * inv, v.y * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(o + 2) = __floats2bfloat162_rn(v.z * inv, v.w * inv);
+      }
     }
-    const float v = acc * inv;
-    if constexpr (std::is_same<TO, float>::value) static_cast<float *>(P.out)[out_off + c] = v;
-    else static_cast<__nv_bfloat16 *>(P.out)[out_off + c] = __float2bfloat16_rn(v);
+  }
+}
+
+template <typename TO>
+void launch_merge(const MergeParams &M, int64_t rows, cudaStream_t st) {
+  // more warps per row when there are many splits
+  const int wpr = M.S >= 64 ? 8 : (M.S >= 16 ? 4 : (M.S >= 8 ? 2 : 1));
+  const unsigned nb = (unsigned)((rows * wpr + 7) / 8);
+  switch (wpr) {
+    case 8: attn_merge_kernel<TO, 8><<<nb, 256, 0, st>>>(M); break;
+    case 4: attn_merge_kernel<TO, 4><<<nb, 256, 0, st>>>(M); break;
+    case 2: attn_merge_kernel<TO, 2><<<nb, 256, 0, st>>>(M); break;
+    default: attn_merge_kernel<TO, 1><<<nb, 256, 0, st>>>(M); break;
   }
 }
 
@@ -882,7 +963,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
   if (kv_dtype == SV_F16) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: f16 caches are not supported");
   if (kv_dtype == SV_FP8_E4M3 && (!k_scale || !v_scale))
     return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: fp8 caches need k_scale and v_scale");
-  if (d_head > 256) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: d_head > 256");
+  if (d_head > 256 || d_head % 4) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: d_head must be a multiple of 4 and <= 256");
   if (B > 65535 || H_kv > 65535) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: B or H_kv too large");
   if (layout && (layout->slot_stride < d_head || layout->head_stride < d_head || layout->block_stride < d_head))
     return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: layout strides smaller than d_head");
@@ -975,9 +1056,9 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
   M.ws_acc = ws_acc; M.ws_ml = ws_ml; M.seq_lens = seq_lens; M.out = out;
   M.B = B; M.n_new = n_new; M.H_q = H_q; M.H_kv = H_kv; M.G = G; M.R = plan.R; M.d = d_head; M.bs = block_size;
   M.max_blocks = max_blocks_per_seq; M.bps = plan.bps; M.S = plan.S; M.per_split = plan.per_split;
-  dim3 grid(plan.R, H_kv, B);
-  if (out_dtype == SV_F32) attn_merge_kernel<float><<<grid, 128, 0, st>>>(M);
-  else attn_merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(M);
+  const int64_t rows = (int64_t)B * H_kv * plan.R;
+  if (out_dtype == SV_F32) launch_merge<float>(M, rows, st);
+  else launch_merge<__nv_bfloat16>(M, rows, st);
   return check_launch("spec_verify_attn merge launch");
 }
 
