@@ -219,6 +219,31 @@ sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
                                 void *workspace, size_t workspace_bytes,
                                 int32_t *dev_status, unsigned flags, sv_stream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * spec_verify_sample_static
+ *   The pages have no counterpart to this call; it exists for callers that
+ *   cannot allocate device memory when they verify a round (an engine that
+ *   reserves all GPU memory for its KV pool at start-up and forbids later
+ *   allocations, or a caller whose fixed interface cannot pass a workspace).
+ *   Same as spec_verify_sample without the workspace arguments: the per-row
+ *   records go to a 1 MiB static device array inside the library, which every
+ *   GPU that loads the library holds until the process exits. Supports
+ *   B * (K+1) <= 21845; larger sizes return SV_ERR_UNSUPPORTED with a message.
+ *   Allocates nothing (no cudaMalloc / cudaFree or allocating library call).
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device shares the one array and leaves its contents
+ *   behind; no call needs it zeroed. Calls that overlap on the GPU (other
+ *   streams, other host threads) race on the array: serialise them.
+ * ------------------------------------------------------------------------ */
+sv_status spec_verify_sample_static(const void *target_logits, sv_dtype logit_dtype,
+                                    const void *draft, sv_dtype draft_dtype, int draft_is_probs,
+                                    const int32_t *draft_tokens, const float *uniforms,
+                                    int B, int K, int V, float temperature,
+                                    int32_t *out_tokens, int32_t *num_accepted,
+                                    float *p_at_draft, float *q_at_draft,
+                                    int32_t *dev_status, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1084,3 +1084,56 @@ extern "C" sv_status spec_verify_sample(const void *target_logits, sv_dtype logi
                                uniforms, B, K, V, temperature, out_tokens, num_accepted, p_at_draft,
                                q_at_draft, workspace, workspace_bytes, dev_status, 0u, stream);
 }
+
+// ------------------------------------------------- allocation-free entry ---
+// Some callers cannot allocate device memory when they verify a round: for
+// example an engine that reserves all of the GPU's memory for its KV pool at
+// start-up and forbids allocations afterwards, or a caller whose fixed C
+// interface has no way to pass a workspace. For them the records live in
+// this static device array (every GPU that loads the library keeps it until
+// the process exits).
+namespace {
+constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB: 21845 rows of (sequence, position)
+__device__ __align__(256) uint8_t g_sample_scratch[kStaticScratchBytes];
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" sv_status spec_verify_sample_static(const void *target_logits, sv_dtype logit_dtype,
+                                               const void *draft, sv_dtype draft_dtype, int draft_is_probs,
+                                               const int32_t *draft_tokens, const float *uniforms, int B, int K,
+                                               int V, float temperature, int32_t *out_tokens,
+                                               int32_t *num_accepted, float *p_at_draft, float *q_at_draft,
+                                               int32_t *dev_status, sv_stream_t stream) {
+  using namespace sv;
+  if (B < 0 || K < 0)
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_static: bad sizes B=%d K=%d", B, K);
+  const size_t need = records_bytes(B, K);
+  if (need > kStaticScratchBytes)
+    return fail(SV_ERR_UNSUPPORTED,
+                "spec_verify_sample_static: B*(K+1) = %lld rows exceed the static scratch of %zu bytes "
+                "(%zu rows); use spec_verify_sample with a caller workspace",
+                (long long)B * (K + 1), kStaticScratchBytes, kStaticScratchBytes / sizeof(RowRec));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_static: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_static: device %d", dev);
+  void *ptr = nullptr;
+  {
+    // first call on a device: resolve the array's device address (the
+    // device is current here)
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_sample_scratch);
+      if (e != cudaSuccess) {
+        g_scratch_ptr[dev] = nullptr;
+        return fail(SV_ERR_CUDA, "spec_verify_sample_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      }
+    }
+    ptr = g_scratch_ptr[dev];
+  }
+  return spec_verify_sample(target_logits, logit_dtype, draft, draft_dtype, draft_is_probs, draft_tokens,
+                            uniforms, B, K, V, temperature, out_tokens, num_accepted, p_at_draft, q_at_draft, ptr,
+                            kStaticScratchBytes, dev_status, stream);
+}
