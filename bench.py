@@ -33,8 +33,8 @@ NOMINAL_HBM_GBS = 8000.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_70b")
     ap.add_argument("--sigma", type=float, default=None)
@@ -49,6 +49,38 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_seed(seed, rank):
+    """Each rank verifies its own batch of sequences (weak scaling): the
+    inputs of rank r are those of seed + r."""
+    return seed + rank
+
+
+def max_over_ranks(x, device, world):
+    """The slowest rank's time: the job is done when every rank is."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_steps_per_sec(steps, world, total_ms):
+    """Whole-job throughput: every rank ran `steps` steps in total_ms."""
+    return world * steps / (total_ms / 1e3)
+
+
+def workload_config(cfg, sigma, lens, world, step_bytes):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": "%s: B=%d H_q=%d H_kv=%d d_head=%d %s KV, ctx %s, block 16, K=%d, V=%d %s logits, "
+                        "draft sigma %.2g" % (cfg.name, cfg.B, cfg.H_q, cfg.H_kv, cfg.d_head, cfg.kv_dtype,
+                                             cfg.ctx, cfg.K, cfg.V, cfg.logit_dtype, sigma),
+            "global_batch": cfg.B * world, "seq_len": int(sum(lens) / len(lens)),
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (%.2f GB touched per step)" % (step_bytes / 1e9)}
 
 
 def measured_peaks():
@@ -77,19 +109,67 @@ def attn_traffic_from_profile():
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    """SM clock and clock-event reasons sampled every 2 ms during the timed
+    region through NVML (read-only queries), falling back to nvidia-smi at
+    its 200 ms period when NVML cannot be loaded."""
 
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_s=0.002):
         self.index = index
+        self.period = period_s
+        self.samples = []      # (sm_mhz, reason bits)
+        self.max_mhz = None
         self.proc = None
         self.lines = []
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.nvml = self._open_nvml()
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = self.index
+            if vis and vis.split(",")[0].strip().isdigit():
+                idx = int(vis.split(",")[self.index].strip())
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+                return None
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            return (lib, h, reasons)
+        except (OSError, AttributeError):
+            return None
+
+    def _poll_nvml(self):
+        import ctypes
+        lib, h, reasons = self.nvml
+        clk = ctypes.c_uint()
+        bits = ctypes.c_ulonglong()
+        while True:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = int(bits.value) if reasons(h, ctypes.byref(bits)) == 0 else 0
+                self.samples.append((float(clk.value), r))
+            if self.stop_flag.wait(self.period):
+                break
 
     def start(self):
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
@@ -106,6 +186,14 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            if not self.samples:
+                return None
+            reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(self.samples), "source": "nvml, 2 ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -132,7 +220,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms"}
 
 
 # ------------------------------------------------------------ our arm -----
@@ -151,7 +239,7 @@ def run_ours(args, rank, world, local):
     sv.build()
     cfg = workloads.CONFIGS[args.workload]
     sigma = cfg.sigma if args.sigma is None else args.sigma
-    seed = args.seed + rank
+    seed = rank_seed(args.seed, rank)
     a = workloads.make_attention_inputs(cfg, seed=seed, device=dev)
     n = workloads.make_append_inputs(cfg, seed=seed, device=dev)
     s = workloads.make_sampling_inputs(cfg, seed=seed, device=dev, sigma=sigma)
@@ -214,10 +302,7 @@ def run_ours(args, rank, world, local):
     app_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     samp_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, world)
 
     # ---- end to end through the public API with host buffers -------------
     host = {k: v.cpu().pin_memory() for k, v in
@@ -258,10 +343,8 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e2e_ms, dev, world)
     if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
         dist.barrier()
     assert int(status.item()) == 0
 
@@ -270,7 +353,7 @@ def run_ours(args, rank, world, local):
             dist.destroy_process_group()
         return
     ms_step = total_ms / args.steps
-    value = world * args.steps / (total_ms / 1e3)
+    value = job_steps_per_sec(args.steps, world, total_ms)
     attn_us = 1e3 * statistics.mean(attn_ms)
     samp_us = 1e3 * statistics.mean(samp_ms)
     app_us = 1e3 * statistics.mean(app_ms)
@@ -281,12 +364,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s: B=%d H_q=%d H_kv=%d d_head=%d %s KV, ctx %s, block 16, K=%d, V=%d %s logits, "
-                               "draft sigma %.2g" % (cfg.name, cfg.B, cfg.H_q, cfg.H_kv, cfg.d_head,
-                                                    cfg.kv_dtype, cfg.ctx, cfg.K, cfg.V, cfg.logit_dtype, sigma),
-                   "global_batch": cfg.B * world, "seq_len": int(sum(lens) / len(lens)),
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (%.2f GB touched per step)" % (step_bytes / 1e9)},
+        "config": workload_config(cfg, sigma, lens, world, step_bytes),
         "tokens_per_sec": world * emitted_per_step * args.steps / (total_ms / 1e3),
         "hbm_gbs_step": step_bytes / (ms_step * 1e-3) / 1e9,
         "frac_of_8tbs_step": step_bytes / (ms_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
@@ -300,12 +378,12 @@ def run_ours(args, rank, world, local):
                      "frac": attn_gbs / peak, "traffic": attn_traffic_from_profile()},
         "roofline_sample": {"bound": "hbm", "kernel": "spec_verify_sample (rows + resolve)",
                             "achieved": samp_gbs, "peak": peak, "unit": "GB/s", "frac": samp_gbs / peak},
-        "e2e": ({"value": world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+        "e2e": ({"value": job_steps_per_sec(e2e_steps, world, e2e_ms), "unit": UNIT,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, a, n, s, sigma)
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -355,12 +433,17 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def cpu_baseline(cfg, a, n, s, sigma):
-    n_attn = min(cfg.B, 6)
-    n_samp = min(cfg.B, 8)
-    full, spent, desc = oracle_sample_time(cfg, a, n, s, n_attn, n_samp)
-    return {"value": 1.0 / full, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": desc + "; %.1f s of CPU work; numpy fp64 (BLAS threads = cores)" % spent}
+def cpu_baseline(cfg, a, n, s, sigma, min_seconds=10.0, max_reps=5):
+    """The oracle on the whole step (every sequence), repeated until at least
+    min_seconds of CPU work have been timed."""
+    reps, spent, desc = 0, 0.0, ""
+    while reps < max_reps and (reps == 0 or spent < min_seconds):
+        _, t, desc = oracle_sample_time(cfg, a, n, s, cfg.B, cfg.B)
+        spent += t
+        reps += 1
+    return {"value": reps / spent, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": "the full step (append, attention and sampling of all %d sequences), %d time(s), "
+                      "%.1f s of CPU work; numpy fp64 (BLAS threads = cores)" % (cfg.B, reps, spent)}
 
 
 def run_reference(args, rank, world):
@@ -374,7 +457,13 @@ def run_reference(args, rank, world):
     a = workloads.make_attention_inputs(cfg, seed=args.seed)
     n = workloads.make_append_inputs(cfg, seed=args.seed)
     s = workloads.make_sampling_inputs(cfg, seed=args.seed, sigma=sigma)
-    n_attn, n_samp = 1, 1
+    lens = a["seq_lens"].tolist()
+    step_bytes = (workloads.attention_bytes(cfg, lens) + workloads.sampling_bytes(cfg)
+                  + workloads.append_bytes(cfg))
+    # size each step's sample so the whole run stays near 90 s of CPU work
+    _, t_one, _ = oracle_sample_time(cfg, a, n, s, 1, 1)
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    n_attn = n_samp = max(1, min(cfg.B, int(per_step / max(t_one, 1e-3))))
     for _ in range(args.warmup):
         oracle_sample_time(cfg, a, n, s, n_attn, n_samp)
     fulls = []
@@ -389,7 +478,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(fulls),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": cfg.name, "global_batch": cfg.B, "parallelism": "cpu"},
+            "config": workload_config(cfg, sigma, lens, world, step_bytes),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": desc + "; each step is this sample (%.1f s wall for %d steps)"
                              % (wall, args.steps)},

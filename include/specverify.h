@@ -25,7 +25,8 @@
  *   - All tensor arguments are DEVICE pointers, row-major, densely packed in
  *     the layout stated next to them. The caller owns every buffer, including
  *     workspaces; the library never allocates or frees memory and keeps no
- *     state between calls (apart from a per-thread error string).
+ *     state between calls (apart from a per-thread error string and the
+ *     static scratch array of spec_verify_sample_static).
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
  *     stream). Outputs are valid once the stream has reached the call.
  *   - Argument errors are detected on the host before any launch: the call
@@ -125,9 +126,12 @@ sv_status kv_block_append(const void *k_new, const void *v_new, sv_dtype new_dty
  *   s_t = softmax_scale * q[b][j][h][:] . K_b[t][g][:], g = h / (H_q/H_kv),
  *   over keys t <= seq_lens[b] - n_new + j (the offset causal mask).
  *   q: [B][n_new][H_q][d_head] of q_dtype; out: same shape, out_dtype.
- *   Supported: kv_dtype SV_F32 with q/out SV_F32 (any d_head <= 256,
- *   any block_size); kv_dtype SV_BF16 or SV_FP8_E4M3 with q/out SV_BF16,
- *   d_head 128, block_size 16, H_q/H_kv * n_new <= 64.
+ *   Supported: kv_dtype SV_F32 with q/out SV_F32, or kv_dtype SV_BF16 /
+ *   SV_FP8_E4M3 with q/out SV_BF16; d_head a multiple of 4 and <= 256; any
+ *   block_size. The tensor-core kernel takes bf16 / fp8 caches with
+ *   d_head 128, block_size 16, (H_q/H_kv) * n_new <= 64 and pool strides
+ *   that are multiples of 16 bytes; every other supported shape runs on a
+ *   CUDA-core kernel with fp32 arithmetic.
  *   fp8 pools hold e4m3 codes; the key / value is code * k_scale[g] /
  *   code * v_scale[g] (k_scale, v_scale: float [H_kv] on the device).
  *   workspace: at least spec_verify_attn_workspace_size(...) bytes of device
@@ -187,8 +191,10 @@ sv_status spec_verify_attn_ex(const void *q, sv_dtype q_dtype,
  *   num_accepted int32 [B] = n in [0, K] (emitted = n + 1);
  *   p_at_draft / q_at_draft: float [B][K] = p_i(x_i), q_i(x_i) (optional,
  *   may be NULL).
- *   Decisions are those of exact arithmetic: rows whose fp32 result could be
- *   affected by rounding are re-evaluated with ~2^-44 relative error.
+ *   Decisions are those of exact arithmetic: the fp32 result of a row is used
+ *   only when a rounding bound certifies it; otherwise the row is
+ *   re-evaluated in float-float arithmetic (about 1e-9 relative error per
+ *   term).
  *   temperature > 0. V >= 1, K >= 0.
  *   workspace: at least spec_verify_sample_workspace_size(B, K, V) bytes of
  *   device memory, 256-byte aligned; its contents need no initialisation.
