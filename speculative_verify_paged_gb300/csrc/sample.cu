@@ -42,7 +42,7 @@ constexpr uint32_t kChunkBytes = 16384;
 constexpr int kMaxChunks = 32;              // per CTA, target + draft
 constexpr size_t kMaxSliceSmem = 200 * 1024;
 constexpr size_t kTargetSliceSmem = 64 * 1024;
-constexpr int kFinishClusters = 16;
+constexpr int kFinishClusters = 8;
 
 enum : uint32_t {
   REC_ACCEPT = 1u,       // fp32 accept decision of the draft at this position
@@ -78,6 +78,7 @@ struct SampleParams {
   int ns;        // elements per CTA slice (multiple of 8)
   int ns_x;      // elements per CTA slice in the finish kernel
   int aligned;   // rows are 16-byte aligned: bulk copies usable
+  int cache_x;   // finish kernel keeps the float-float exponentials in shared memory
   unsigned flags;
   float c;       // log2(e) / T
   float invT_hi, invT_lo;
@@ -234,17 +235,27 @@ __device__ __forceinline__ void online8(const T *buf, int g, float c, float &m, 
   for (int j = 0; j < 8; ++j) s += ex2(fmaf(x[j], c, -mc));
 }
 
-// Block sum of a float-float value (result in every thread).
-__device__ __forceinline__ ff block_sum_ff(ff v, ff *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Block sum of a float-float value (result in every thread): butterflies
+// within each warp, then over the warp partials (identical bits everywhere).
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff{__shfl_xor_sync(0xffffffffu, v.hi, o),
                                                      __shfl_xor_sync(0xffffffffu, v.lo, o)});
+  return v;
+}
+
+__device__ __forceinline__ ff block_sum_ff(ff v, ff *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_ff(v);
   __syncthreads();
   if (lane == 0) red[warp] = v;
   __syncthreads();
-  ff r{0.f, 0.f};
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = ff_add(r, red[w]);
+  return warp_sum_ff(lane < (int)(blockDim.x >> 5) ? red[lane] : ff{0.f, 0.f});
+}
+
+__device__ __forceinline__ int warp_max_s32(int v) {
+  int r;
+  asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
   return r;
 }
 
@@ -261,18 +272,112 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 
 constexpr int kMaxSteps = 32;   // 32-group steps per warp range
 
+// warp maximum on the reduction unit (NaN inputs are ignored, like fmaxf)
+__device__ __forceinline__ float warp_max_redux(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Thread-local maximum over groups g0, g0 + stride, ... of a slice. A maximum
+// is a selection, so the packed 16-bit forms are exact.
+template <typename T>
+__device__ __forceinline__ float slice_max(const T *buf, int g0, int n_grp, int stride);
+
+template <>
+__device__ __forceinline__ float slice_max<float>(const float *buf, int g0, int n_grp, int stride) {
+  float r0 = -INFINITY, r1 = -INFINITY;
+  const float4 *p = reinterpret_cast<const float4 *>(buf);
+  for (int g = g0; g < n_grp; g += stride) {
+    const float4 a = p[2 * g], b = p[2 * g + 1];
+    r0 = max3f(r0, a.x, a.y);
+    r1 = max3f(r1, a.z, a.w);
+    r0 = max3f(r0, b.x, b.y);
+    r1 = max3f(r1, b.z, b.w);
+  }
+  return fmaxf(r0, r1);
+}
+
+template <typename H2>
+__device__ __forceinline__ H2 as_h2(uint32_t w) {
+  H2 h;
+  memcpy(&h, &w, 4);
+  return h;
+}
+
+template <>
+__device__ __forceinline__ float slice_max<__nv_bfloat16>(const __nv_bfloat16 *buf, int g0, int n_grp, int stride) {
+  const __nv_bfloat162 ninf = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+  __nv_bfloat162 r0 = ninf, r1 = ninf;
+  const uint4 *p = reinterpret_cast<const uint4 *>(buf);
+  for (int g = g0; g < n_grp; g += stride) {
+    const uint4 v = p[g];
+    r0 = __hmax2(r0, as_h2<__nv_bfloat162>(v.x));
+    r1 = __hmax2(r1, as_h2<__nv_bfloat162>(v.y));
+    r0 = __hmax2(r0, as_h2<__nv_bfloat162>(v.z));
+    r1 = __hmax2(r1, as_h2<__nv_bfloat162>(v.w));
+  }
+  r0 = __hmax2(r0, r1);
+  return fmaxf(__low2float(r0), __high2float(r0));
+}
+
+template <>
+__device__ __forceinline__ float slice_max<__half>(const __half *buf, int g0, int n_grp, int stride) {
+  const __half2 ninf = __floats2half2_rn(-INFINITY, -INFINITY);
+  __half2 r0 = ninf, r1 = ninf;
+  const uint4 *p = reinterpret_cast<const uint4 *>(buf);
+  for (int g = g0; g < n_grp; g += stride) {
+    const uint4 v = p[g];
+    r0 = __hmax2(r0, as_h2<__half2>(v.x));
+    r1 = __hmax2(r1, as_h2<__half2>(v.y));
+    r0 = __hmax2(r0, as_h2<__half2>(v.z));
+    r1 = __hmax2(r1, as_h2<__half2>(v.w));
+  }
+  r0 = __hmax2(r0, r1);
+  return fmaxf(__low2float(r0), __high2float(r0));
+}
+
+// Negated rounded reference -fl(m c) of a partial maximum (0 for an empty or
+// all -inf partial: its exponents are then 2^-inf = 0).
+__device__ __forceinline__ float neg_ref(float m, float c) { return m == -INFINITY ? 0.f : -__fmul_rn(m, c); }
+
+// Rescale a partial sum taken against fl(m c) to the reference fl(mx c).
+__device__ __forceinline__ float rescale(float s, float m, float mx, float c) {
+  return m == -INFINITY ? 0.f : s * ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+}
+
+// Warp-wide (max, sum) of a partial pair: identical bits in every lane.
+__device__ __forceinline__ void warp_ms(float &m, float &s, float c) {
+  const float mx = warp_max_redux(m);
+  s = warp_sum(rescale(s, m, mx, c));
+  m = mx;
+}
+
 struct RowShared {
-  uint64_t bars[kMaxChunks];
-  float red_m[32], red_s[32], red_m2[32], red_s2[32];
+  uint64_t bars[2];
+  float red_m[kRowWarps], red_s[kRowWarps], red_m2[kRowWarps], red_s2[kRowWarps];
   float pub_mp, pub_sp, pub_mq, pub_sq;   // this CTA's (max, sum) pairs
   float pub_lp, pub_lq;                   // logits at the draft token (its owner CTA)
   float pub_tot;                          // this CTA's draw mass
   float wsum[kRowWarps];
-  float stepsum[kRowWarps][kMaxSteps];
 };
 
 // One cluster per (sequence, position) row; fp32 fast path only. Writes the
 // row's record: stats, accept test, speculative draw and their certificates.
+//
+// Pass A: exact thread-local maxima, then sums of 2^(l c - fl(m c)) with the
+// target and draft rows paired in packed fp32 arithmetic; (max, sum) pairs
+// are combined across warps and across the cluster.
+// Pass B (only when the draw can be used: the bonus row, or a certified
+// rejection): weights w'(y) = max(0, e_p(y) - r e_q(y)) against the row
+// maxima; each lane owns a contiguous run of groups, so one warp scan of the
+// lane totals locates the crossing of v Z, and one group rescan finds y.
 template <typename TT, int DK>
 __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_constant__ SampleParams P) {
   using TD = typename std::conditional<DK == 0, TT, float>::type;
@@ -287,6 +392,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   const bool q_logits = has_draft && DK == 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float c = P.c;
+  const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
 
   const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
   const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
@@ -301,7 +407,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   // into 16 KB bulk copies
   const uint32_t nb_t = (uint32_t)n_loc * sizeof(TT);
   const uint32_t nb_d = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
-  for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {   // pad the last group
+  for (int e = n_loc + tid; e < n_grp * 8; e += kRowThreads) {   // pad the last group
     st[e] = pad_value<TT>(false);
     if (has_draft) sd[e] = pad_value<TD>(DK == 1);
   }
@@ -323,24 +429,12 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
     }
     __syncthreads();   // barriers initialised before anyone waits on them
   } else {
-    for (int e = tid; e < n_loc; e += blockDim.x) {
+    for (int e = tid; e < n_loc; e += kRowThreads) {
       st[e] = trow[e0 + e];
       if (has_draft) sd[e] = drow[e0 + e];
     }
     __syncthreads();
   }
-
-  // ---- pass A: online (max, sum of exp) per thread ------------------------
-  bool timed_out = false;
-  float mt = -INFINITY, stt = 0.f, md = -INFINITY, sdd = 0.f;
-  if (P.aligned && n_loc > 0 && !mbar_wait(&sh.bars[0], 0)) timed_out = true;
-  for (int g = tid; g < n_grp; g += blockDim.x) online8(st, g, c, mt, stt);
-  if (has_draft) {
-    if (P.aligned && n_loc > 0 && !timed_out && !mbar_wait(&sh.bars[1], 0)) timed_out = true;
-    if (DK == 0)
-      for (int g = tid; g < n_grp; g += blockDim.x) online8(sd, g, c, md, sdd);
-  }
-  if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
   int x_tok = 0;
   if (has_draft) {
     x_tok = P.tokens[(int64_t)b * K + i];
@@ -349,16 +443,66 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
       x_tok = min(max(x_tok, 0), V - 1);
     }
   }
-  const int x_rank = x_tok / P.ns;
-  warp_ms_fast(mt, stt, c);
-  if (q_logits) warp_ms_fast(md, sdd, c);
-  if (lane == 0) { sh.red_m[warp] = mt; sh.red_s[warp] = stt; sh.red_m2[warp] = md; sh.red_s2[warp] = sdd; }
+  const float *uv = P.uniforms + ((int64_t)b * (K + 1) + i) * 2;
+  const float u = uv[0], v_u = uv[1];
+
+  // ---- pass A: thread maxima, then paired sums ---------------------------
+  bool timed_out = false;
+  if (P.aligned && n_loc > 0) {
+    if (!mbar_wait(&sh.bars[0], 0)) timed_out = true;
+    if (has_draft && !timed_out && !mbar_wait(&sh.bars[1], 0)) timed_out = true;
+  }
+  if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+  float mt = slice_max(st, tid, n_grp, kRowThreads);
+  float md = q_logits ? slice_max(sd, tid, n_grp, kRowThreads) : -INFINITY;
+  float s_t = 0.f, s_d = 0.f;
+  {
+    const float2 cc = make_float2(c, c);
+    if (q_logits) {
+      const float2 nm = make_float2(neg_ref(mt, c), neg_ref(md, c));
+      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+      for (int g = tid; g < n_grp; g += kRowThreads) {
+        float xt[8], xd[8];
+        load8(st, g, xt);
+        load8(sd, g, xd);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const float2 y0 = __ffma2_rn(make_float2(xt[j], xd[j]), cc, nm);
+          const float2 y1 = __ffma2_rn(make_float2(xt[j + 1], xd[j + 1]), cc, nm);
+          a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
+          a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
+        }
+      }
+      s_t = a0.x + a1.x;
+      s_d = a0.y + a1.y;
+    } else {
+      const float nr = neg_ref(mt, c);
+      const float2 nm = make_float2(nr, nr);
+      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+      for (int g = tid; g < n_grp; g += kRowThreads) {
+        float xt[8];
+        load8(st, g, xt);
+#pragma unroll
+        for (int j = 0; j < 8; j += 4) {
+          const float2 y0 = __ffma2_rn(make_float2(xt[j], xt[j + 1]), cc, nm);
+          const float2 y1 = __ffma2_rn(make_float2(xt[j + 2], xt[j + 3]), cc, nm);
+          a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
+          a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
+        }
+      }
+      s_t = (a0.x + a0.y) + (a1.x + a1.y);
+    }
+  }
+  warp_ms(mt, s_t, c);
+  if (q_logits) warp_ms(md, s_d, c);
+  if (lane == 0) { sh.red_m[warp] = mt; sh.red_s[warp] = s_t; sh.red_m2[warp] = md; sh.red_s2[warp] = s_d; }
   __syncthreads();
+  const int x_rank = x_tok / P.ns;
   if (warp == 0) {
     float m1 = lane < kRowWarps ? sh.red_m[lane] : -INFINITY, s1 = lane < kRowWarps ? sh.red_s[lane] : 0.f;
     float m2 = lane < kRowWarps ? sh.red_m2[lane] : -INFINITY, s2 = lane < kRowWarps ? sh.red_s2[lane] : 0.f;
-    warp_ms_fast(m1, s1, c);
-    if (q_logits) warp_ms_fast(m2, s2, c);
+    warp_ms(m1, s1, c);
+    if (q_logits) warp_ms(m2, s2, c);
     if (lane == 0) {
       sh.pub_mp = m1; sh.pub_sp = s1; sh.pub_mq = m2; sh.pub_sq = s2;
       if (has_draft && rank == x_rank) {   // the slice holding x_i publishes its logits
@@ -371,16 +515,16 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   float m_p = -INFINITY, S_p = 0.f, m_q = -INFINITY, S_q = 0.f;
   if (lane < cs) {
     m_p = ld_dsmem_f32(mapa(&sh.pub_mp, lane)); S_p = ld_dsmem_f32(mapa(&sh.pub_sp, lane));
-    m_q = ld_dsmem_f32(mapa(&sh.pub_mq, lane)); S_q = ld_dsmem_f32(mapa(&sh.pub_sq, lane));
+    if (q_logits) { m_q = ld_dsmem_f32(mapa(&sh.pub_mq, lane)); S_q = ld_dsmem_f32(mapa(&sh.pub_sq, lane)); }
   }
-  warp_ms_fast(m_p, S_p, c);
-  if (q_logits) warp_ms_fast(m_q, S_q, c);
-  else { m_q = 0.f; S_q = 1.f; }
   float lp_x = 0.f, lq_x = 0.f;
   if (has_draft) {
     lp_x = ld_dsmem_f32(mapa(&sh.pub_lp, x_rank));
     lq_x = ld_dsmem_f32(mapa(&sh.pub_lq, x_rank));
   }
+  warp_ms(m_p, S_p, c);
+  if (q_logits) warp_ms(m_q, S_q, c);
+  else { m_q = 0.f; S_q = 1.f; }
   const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
   // e_p(y) = 2^(fl(l(y) c - fl(m_p c))), p = e_p / S_p. The draw works on the
   // unnormalised weights w'(y) = S_p w(y) = max(0, e_p(y) - r e_q(y)),
@@ -388,8 +532,6 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   // invariant to the common scale.
   const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
   const float r_pq = q_logits ? S_p / S_q : S_p;
-  const float *uv = P.uniforms + ((int64_t)b * (K + 1) + i) * 2;
-  const float u = uv[0], v_u = uv[1];
 
   // ---- accept test in fp32 ------------------------------------------------
   bool accept = false, acc_cert = true;
@@ -403,8 +545,35 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
     // rounding, row sums): a decision this far from the boundary is exact
     acc_cert = fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f && finite;
   }
+  RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
+  const uint32_t acc_flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u);
+  if (rank == 0 && tid == 0) {
+    if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
+    rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
+    rec->p_x = p_x; rec->q_x = q_x;
+    rec->y_exact = -1;
+    if (has_draft) {
+      if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
+      if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
+    }
+  }
+  // The draw of this row is used only if it is the bonus row or a certified
+  // rejection; an uncertified accept test is redone (with its draw) by the
+  // finish kernel. The decision is identical in every CTA of the cluster.
+  const bool need_draw = finite && !force && (!has_draft || (acc_cert && !accept));
+  if (!need_draw) {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (rank == 0 && tid == 0) {
+      rec->y = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
+      rec->flags = acc_flags;
+    }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return;
+  }
 
   // ---- pass B: fp32 weights of the speculative draw ----------------------
+  const float2 cc = make_float2(c, c);
+  const float2 nref = make_float2(-mcp, -mcq);
   auto weight8 = [&](int g, float (&w)[8]) {
     float xp[8];
     load8(st, g, xp);
@@ -413,44 +582,74 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
       load8(sd, g, xq);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float ep = ex2(fmaf(xp[j], c, -mcp));
-        const float eq = DK == 0 ? ex2(fmaf(xq[j], c, -mcq)) : xq[j];
+        float eq;
+        float ep;
+        if (DK == 0) {
+          const float2 y = __ffma2_rn(make_float2(xp[j], xq[j]), cc, nref);
+          ep = ex2(y.x);
+          eq = ex2(y.y);
+        } else {
+          ep = ex2(fmaf(xp[j], c, -mcp));
+          eq = xq[j];
+        }
         w[j] = fmaxf(fmaf(-r_pq, eq, ep), 0.f);
       }
     } else {
+      const float2 np = make_float2(-mcp, -mcp);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = ex2(fmaf(xp[j], c, -mcp));
+      for (int j = 0; j < 8; j += 2) {
+        const float2 y = __ffma2_rn(make_float2(xp[j], xp[j + 1]), cc, np);
+        w[j] = ex2(y.x);
+        w[j + 1] = ex2(y.y);
+      }
     }
   };
-  const int gpw = (n_grp + kRowWarps - 1) / kRowWarps;   // groups per warp range
+  auto sum8 = [](const float (&w)[8]) {
+    const float2 a = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
+    const float2 bb = __fadd2_rn(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
+    const float2 t = __fadd2_rn(a, bb);
+    return t.x + t.y;
+  };
+  // warp `warp` owns groups [g_lo, g_hi); lane l owns the run
+  // [g_lo + l G, g_lo + (l+1) G) of it, visited in a lane-rotated order so
+  // the 16-byte shared-memory reads of a quarter warp hit distinct banks
+  const int gpw = (n_grp + kRowWarps - 1) / kRowWarps;
   const int g_lo = min(n_grp, warp * gpw), g_hi = min(n_grp, g_lo + gpw);
-  float run = 0.f;
-  for (int s0 = g_lo, sidx = 0; s0 < g_hi; s0 += 32, ++sidx) {
-    const int g = s0 + lane;
-    float v = 0.f;
-    if (g < g_hi) {
+  const int G = (gpw + 31) >> 5;
+  const int r_lo = min(g_hi, g_lo + lane * G), r_hi = min(g_hi, r_lo + G);
+  float t_l = 0.f;
+  const int rot = G > 0 ? lane % G : 0;
+  for (int s = 0; s < G; ++s) {
+    int k = s + rot;
+    k = k >= G ? k - G : k;
+    const int g = r_lo + k;
+    if (g < r_hi) {
       float w[8];
       weight8(g, w);
-      v = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+      t_l += sum8(w);
     }
-    v = warp_sum(v);
-    if (lane == 0) sh.stepsum[warp][sidx] = v;
-    run += v;
   }
-  if (lane == 0) sh.wsum[warp] = run;
+  float incl = t_l;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sh.wsum[warp] = incl;
   __syncthreads();
   float tot_cta = 0.f;
   for (int w = 0; w < kRowWarps; ++w) tot_cta += sh.wsum[w];
   if (tid == 0) sh.pub_tot = tot_cta;
   cluster_sync();   // #2: masses published
+  const float t_r = lane < cs ? ld_dsmem_f32(mapa(&sh.pub_tot, lane)) : 0.f;
+  // the last distributed read of this launch is done: arrive now, wait at exit
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   float off_c = 0.f, Z = 0.f;
   for (int rr = 0; rr < cs; ++rr) {
-    const float t = ld_dsmem_f32(mapa(&sh.pub_tot, rr));
+    const float t = __shfl_sync(0xffffffffu, t_r, rr);
     if (rr == rank) off_c = Z;
     Z += t;
   }
-  // the last distributed read of this launch is done: arrive now, wait at exit
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   const float thr = v_u * Z;
   // rounding bound of the fp32 CDF near thr, in units of w' = S_p w:
   // per-element exp / argument / ratio errors (~2^-22 relative, random:
@@ -458,73 +657,62 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   // running sums (~2^-24 per addition)
   const float e_abs = 4.7683716e-07f * S_p * sqrtf(1.f / S_p + (q_logits ? 1.f / S_q : 0.f)) +
                       1.1920929e-07f * (Z + S_p);   // 2^-21, 2^-23
-  const bool draw_ok = finite && Z > 0.f && thr < Z;
-  RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
+  const bool draw_ok = Z > 0.f && thr < Z;
   if (rank == 0 && tid == 0) {
-    if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
-    rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
-    rec->p_x = p_x; rec->q_x = q_x;
     rec->z = Z; rec->e_abs = e_abs;
-    rec->y_exact = -1;
-    if (has_draft) {
-      if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
-      if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
-    }
     if (!draw_ok) {   // no owner: the finish kernel evaluates the draw exactly
       rec->y = -1; rec->gap = 0.f;
-      rec->flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u);
+      rec->flags = acc_flags;
     }
   }
   if (draw_ok && off_c <= thr && thr < off_c + tot_cta) {
-    float woff = 0.f, a_w = off_c;
+    float woff = 0.f, base = off_c;
     int owner = kRowWarps - 1;
     for (int w = 0; w < kRowWarps; ++w) {
       const float nxt = woff + sh.wsum[w];
-      if (thr < off_c + nxt || w == kRowWarps - 1) { owner = w; a_w = off_c + woff; break; }
+      if (thr < off_c + nxt || w == kRowWarps - 1) { owner = w; base = off_c + woff; break; }
       woff = nxt;
     }
     if (warp == owner) {
-      // the step of this warp's range that holds thr, then one rescan
-      const int nsteps = (g_hi - g_lo + 31) / 32;
-      float base = a_w;
-      int sel = -1;
-      for (int sidx = 0; sidx < nsteps; ++sidx) {
-        const float nxt = base + sh.stepsum[warp][sidx];
-        if (thr < nxt) { sel = sidx; break; }
-        base = nxt;
-      }
+      // the lane whose run holds thr, then its groups rescanned in order
+      const unsigned hit = __ballot_sync(0xffffffffu, base + incl > thr);
       int y = -1;
       float c_lo = 0.f, c_hi = 0.f;
-      if (sel >= 0) {
-        const int g = g_lo + sel * 32 + lane;
-        float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float vsum = 0.f;
-        if (g < g_hi) {
-          weight8(g, w);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) vsum += w[j];
-        }
-        float incl = vsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, base + incl > thr);
-        if (hit) {
-          const int L = __ffs(hit) - 1;
-          if (lane == L) {
-            float run_c = base + (incl - vsum);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float nxt = run_c + w[j];
-              if (y < 0 && nxt > thr) { y = e0 + 8 * g + j; c_lo = run_c; c_hi = nxt; }
-              run_c = nxt;
-            }
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        float start = base + __shfl_sync(0xffffffffu, incl - t_l, L);
+        const int L_lo = __shfl_sync(0xffffffffu, r_lo, L), L_hi = __shfl_sync(0xffffffffu, r_hi, L);
+        for (int g0 = L_lo; g0 < L_hi && y < 0; g0 += 32) {   // one pass while G <= 32
+          const int g = g0 + lane;
+          float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          float vsum = 0.f;
+          if (g < L_hi) {
+            weight8(g, w);
+            vsum = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
           }
-          y = __shfl_sync(0xffffffffu, y, L);
-          c_lo = __shfl_sync(0xffffffffu, c_lo, L);
-          c_hi = __shfl_sync(0xffffffffu, c_hi, L);
+          float inc2 = vsum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, inc2, o);
+            if (lane >= o) inc2 += t;
+          }
+          const unsigned h2 = __ballot_sync(0xffffffffu, g < L_hi && start + inc2 > thr);
+          if (h2) {
+            const int L2 = __ffs(h2) - 1;
+            if (lane == L2) {
+              float run_c = start + (inc2 - vsum);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float nxt = run_c + w[j];
+                if (y < 0 && nxt > thr) { y = e0 + 8 * g + j; c_lo = run_c; c_hi = nxt; }
+                run_c = nxt;
+              }
+            }
+            y = __shfl_sync(0xffffffffu, y, L2);
+            c_lo = __shfl_sync(0xffffffffu, c_lo, L2);
+            c_hi = __shfl_sync(0xffffffffu, c_hi, L2);
+          }
+          start += __shfl_sync(0xffffffffu, inc2, 31);
         }
       }
       if (lane == 0) {
@@ -532,8 +720,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
         const float gap = found ? fminf(thr - c_lo, c_hi - thr) : 0.f;
         rec->y = found ? y : -1;
         rec->gap = gap;
-        rec->flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u) |
-                     ((found && gap > e_abs) ? REC_DRAW_CERT : 0u);
+        rec->flags = acc_flags | ((found && gap > e_abs) ? REC_DRAW_CERT : 0u);
       }
     }
   }
@@ -587,33 +774,42 @@ struct ExactShared {
 // slice [e0, e0 + n_grp*8) of the row (padded like the rows kernel does).
 template <typename TT, int DK>
 __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
-                          const typename std::conditional<DK == 0, TT, float>::type *sd, int n_grp, int e0,
-                          bool has_draft, bool need_acc, float m_p, float m_q, float lp_x, float lq_x,
-                          float u, float v_u, int *y_out) {
+                          const typename std::conditional<DK == 0, TT, float>::type *sd, ff *cp, ff *cq,
+                          int n_grp, int e0, bool has_draft, bool need_acc, float m_p, float m_q, float lp_x,
+                          float lq_x, float u, float v_u, int *y_out) {
   const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool q_logits = has_draft && DK == 0;
+  // cp / cq (when not null) keep e_p, e_q of element j of group g at
+  // [j * n_grp + g] for the weights pass
   ff sp{0.f, 0.f}, sq{0.f, 0.f};
   for (int g = tid; g < n_grp; g += blockDim.x) {
     float x[8];
     load8(st, g, x);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc_add(sp, ffx_exp(x[j], m_p, P, sh.tbl));
+    for (int j = 0; j < 8; ++j) {
+      const ff e = ffx_exp(x[j], m_p, P, sh.tbl);
+      if (cp) cp[j * n_grp + g] = e;
+      acc_add(sp, e);
+    }
     if (q_logits) {
       load8(sd, g, x);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc_add(sq, ffx_exp(x[j], m_q, P, sh.tbl));
+      for (int j = 0; j < 8; ++j) {
+        const ff e = ffx_exp(x[j], m_q, P, sh.tbl);
+        if (cp) cq[j * n_grp + g] = e;
+        acc_add(sq, e);
+      }
     }
   }
   sp = block_sum_ff(ff_norm(sp), sh.red);
   sq = block_sum_ff(ff_norm(sq), sh.red);
   if (tid == 0) { sh.pub_sp = sp; sh.pub_sq = sq; }
   cluster_sync();
-  ff Sp{0.f, 0.f}, Sq{0.f, 0.f};
-  for (int r = 0; r < cs; ++r) {
-    Sp = ff_add(Sp, ld_dsmem_ff(&sh.pub_sp, r));
-    Sq = ff_add(Sq, ld_dsmem_ff(&sh.pub_sq, r));
-  }
+  ff Sp = lane < cs ? ld_dsmem_ff(&sh.pub_sp, lane) : ff{0.f, 0.f};
+  ff Sq = lane < cs ? ld_dsmem_ff(&sh.pub_sq, lane) : ff{0.f, 0.f};
+  Sp = warp_sum_ff(Sp);
+  Sq = warp_sum_ff(Sq);
   cluster_sync();   // peers have read the published sums
   if (!q_logits) Sq = ff{1.f, 0.f};
   if (need_acc && has_draft) {
@@ -635,14 +831,19 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
   int mode = !has_draft ? 0 : (DK == 0 ? 1 : 2);
   auto wx8 = [&](int g, ff (&w)[8]) {
     float xp[8], xq[8];
-    load8(st, g, xp);
-    if (has_draft) load8(sd, g, xq);
+    if (!cp) load8(st, g, xp);
+    if (has_draft && (mode == 2 || !cp)) load8(sd, g, xq);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const ff ep = ffx_exp(xp[j], m_p, P, sh.tbl);
-      if (mode == 0) w[j] = ep;
-      else if (mode == 1) w[j] = ff_max0(ff_add(ff_mul(ep, Sq), ff_neg(ff_mul(ffx_exp(xq[j], m_q, P, sh.tbl), Sp))));
-      else w[j] = ff_max0(ff_add(ep, ff_neg(ff_mul(ff{xq[j], 0.f}, Sp))));
+      const ff ep = cp ? cp[j * n_grp + g] : ffx_exp(xp[j], m_p, P, sh.tbl);
+      if (mode == 0) {
+        w[j] = ep;
+      } else if (mode == 1) {
+        const ff eq = cp ? cq[j * n_grp + g] : ffx_exp(xq[j], m_q, P, sh.tbl);
+        w[j] = ff_max0(ff_add(ff_mul(ep, Sq), ff_neg(ff_mul(eq, Sp))));
+      } else {
+        w[j] = ff_max0(ff_add(ep, ff_neg(ff_mul(ff{xq[j], 0.f}, Sp))));
+      }
     }
   };
   const int gpw = (n_grp + kResWarps - 1) / kResWarps;
@@ -681,15 +882,17 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
     for (int w = 0; w < kResWarps; ++w) tot = ff_add(tot, sh.wsum[w]);
     if (tid == 0) sh.pub_tot = tot;
     cluster_sync();   // totals published
+    // CTA r owns [sum of totals before r, + its total): a sequential prefix
+    // in rank order, the same in every CTA
+    const ff t_r = lane < cs ? ld_dsmem_ff(&sh.pub_tot, lane) : ff{0.f, 0.f};
+    const int last_all = warp_max_s32(lane < cs ? ld_dsmem_s32(mapa(&sh.pub_last, lane)) : -1);
+    cluster_sync();   // peers have read the totals
     ff xoff{0.f, 0.f}, XZ{0.f, 0.f};
-    int last_all = -1;
     for (int r = 0; r < cs; ++r) {
-      const ff t = ld_dsmem_ff(&sh.pub_tot, r);
+      const ff t{__shfl_sync(0xffffffffu, t_r.hi, r), __shfl_sync(0xffffffffu, t_r.lo, r)};
       if (r == rank) xoff = XZ;
       XZ = ff_add(XZ, t);
-      last_all = max(last_all, ld_dsmem_s32(mapa(&sh.pub_last, r)));
     }
-    cluster_sync();   // peers have read the totals
     if (tid == 0) sh.pub_last = -1;
     if (!ff_pos(XZ)) {   // zero residual mass: draw from p_n instead
       __syncthreads();
@@ -752,7 +955,7 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
       }
     }
     cluster_sync();   // the draw is published
-    for (int r = 0; r < cs; ++r) y = max(y, ld_dsmem_s32(mapa(&sh.pub_y, r)));
+    y = warp_max_s32(lane < cs ? ld_dsmem_s32(mapa(&sh.pub_y, lane)) : -1);
     if (y < 0) y = last_all;   // v Z at the very top of the range (rounding)
     cluster_sync();   // peers have read pub_y
     if (tid == 0) sh.pub_y = -1;
@@ -763,13 +966,15 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
   return false;
 }
 
-// One cluster per group of sequences. Every thread walks one sequence's
-// records (certified accepts, then the first rejection or the bonus row) and
-// the tokens of fully certified sequences are written at once. The few
-// sequences whose next needed decision is not certified are then processed
-// one by one by the whole cluster: the row's slices are copied into shared
-// memory and re-evaluated in float-float arithmetic, continuing the walk.
-constexpr int kFinishMaxSeq = kResThreads;   // sequences per cluster
+// Every cluster walks every sequence (one thread per sequence, in rounds of
+// kResThreads sequences): certified accepts, then the first rejection or the
+// bonus row. All CTAs build the same ordered list of sequences whose next
+// needed decision is not certified, and cluster c re-evaluates entries
+// c, c + ncl, ... (the row's slices copied into shared memory, float-float
+// arithmetic, continuing the walk), so the rare exact rows spread over all
+// clusters. The tokens of a fully certified sequence b are written by
+// cluster b % ncl.
+constexpr int kFinishMaxSeq = kResThreads;   // sequences per walk round
 
 template <typename TT, int DK>
 __global__ void __launch_bounds__(kResThreads) sample_finish_kernel(const __grid_constant__ SampleParams P) {
@@ -785,139 +990,159 @@ __global__ void __launch_bounds__(kResThreads) sample_finish_kernel(const __grid
   const int K = P.K, V = P.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
-  const int chunk = (P.B + ncl - 1) / ncl;
-  const int b0 = cid * chunk, b1 = min(P.B, b0 + chunk);
   const int ns = P.ns_x;
   const int e0 = min(V, rank * ns);
   const int n_loc = max(0, min(V, e0 + ns) - e0);
   const int n_grp = (n_loc + 7) >> 3;
   TT *st = reinterpret_cast<TT *>(smem);
   TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)ns * sizeof(TT), 128));
+  ff *cp = nullptr, *cq = nullptr;
+  if (P.cache_x) {
+    cp = reinterpret_cast<ff *>(smem + align_up((size_t)ns * sizeof(TT), 128) + align_up((size_t)ns * sizeof(TD), 128));
+    cq = cp + ns;
+  }
   if (tid < 64) sh.tbl[tid] = P.tbl[tid];
   if (tid == 0) {
     sh.pub_y = -1; sh.pub_last = -1;
     mbar_init(&bar, 1);
     fence_mbarrier_init();
   }
-
-  // ---- parallel walk: one thread per sequence -----------------------------
-  const int b = b0 + tid;
-  int start = -1;   // first position whose decision needs the float-float pass
-  if (b < b1) {
-    const RowRec *recs = P.recs + (int64_t)b * (K + 1);
-    int n = K;
-    for (int i = 0; i < K; ++i) {
-      const uint32_t f = recs[i].flags;
-      if (force || !(f & REC_ACC_CERT)) { start = i; break; }
-      if (!(f & REC_ACCEPT)) { n = i; break; }
-    }
-    if (start < 0) {
-      if (!force && (recs[n].flags & REC_DRAW_CERT)) {
-        if (rank == 0) {
-          const int y = recs[n].y;
-          for (int j = 0; j <= K; ++j)
-            P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? y : -1);
-          P.num_acc[b] = n;
-        }
-      } else {
-        start = n;
-      }
-    }
-  }
-  // deterministic compaction (same order in every CTA of the cluster)
-  const unsigned vote = __ballot_sync(0xffffffffu, start >= 0);
-  if (lane == 0) warp_cnt[warp] = __popc(vote);
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int w = 0; w < kResWarps; ++w) { const int t = warp_cnt[w]; warp_cnt[w] = acc; acc += t; }
-    list_n = acc;
-  }
-  __syncthreads();
-  if (start >= 0) {
-    const int pos = warp_cnt[warp] + __popc(vote & ((1u << lane) - 1u));
-    list_b[pos] = b;
-    list_i[pos] = start;
-  }
   __syncthreads();
   cluster_sync();   // peers initialised before any distributed read
 
-  // ---- float-float re-evaluation of the listed sequences ------------------
   uint32_t phase = 0;
   const bool vec = P.aligned != 0;
-  for (int li = 0; li < list_n; ++li) {
-    const int bb = list_b[li];
-    const RowRec *recs = P.recs + (int64_t)bb * (K + 1);
-    const int32_t *toks = P.tokens + (int64_t)bb * K;
-    int i = list_i[li], n = K, y = -1;
-    for (;;) {
-      // next position needing evaluation from i on (certified accepts skipped)
-      int need = -1;
-      bool need_acc = false;
-      for (; i < K; ++i) {
-        const uint32_t f = recs[i].flags;
-        if (force || !(f & REC_ACC_CERT)) { need = i; need_acc = true; break; }
-        if (!(f & REC_ACCEPT)) break;
-      }
-      n = min(i, K);
-      if (need < 0) {
-        if (!force && (recs[n].flags & REC_DRAW_CERT)) { y = recs[n].y; break; }
-        need = n;
-      }
-      const bool has_draft = need < K;
-      const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + need) * V;
-      const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + need) * V : nullptr;
-      // slice -> shared memory (bulk copy when rows are 16-byte aligned)
-      for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {
-        st[e] = pad_value<TT>(false);
-        if (has_draft) sd[e] = pad_value<TD>(DK == 1);
-      }
-      if (vec) {
-        if (tid == 0 && n_loc > 0) {
-          const uint32_t nbt = (uint32_t)n_loc * sizeof(TT), nbd = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
-          fence_proxy_async_shared();
-          mbar_arrive_expect_tx(&bar, nbt + nbd);
-          bulk_g2s(st, trow + e0, nbt, &bar);
-          if (has_draft) bulk_g2s(sd, drow + e0, nbd, &bar);
+  for (int round0 = 0; round0 < P.B; round0 += kFinishMaxSeq) {
+    // ---- parallel walk: one thread per sequence ---------------------------
+    const int b = round0 + tid;
+    int start = -1;   // first position whose decision needs the float-float pass
+    if (b < P.B) {
+      const RowRec *recs = P.recs + (int64_t)b * (K + 1);
+      int n = K, ysel = -1;
+      bool done = false;
+      for (int i0 = 0; i0 <= K && !done; i0 += 8) {
+        uint32_t f[8];
+        int yv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // independent loads: one round trip
+          const int i = i0 + j;
+          f[j] = i <= K ? recs[i].flags : 0u;
+          yv[j] = i <= K ? recs[i].y : -1;
         }
-        if (n_loc > 0) {
-          if (!mbar_wait(&bar, phase) && tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-          phase ^= 1u;
-        }
-      } else {
-        for (int e = tid; e < n_loc; e += blockDim.x) {
-          st[e] = trow[e0 + e];
-          if (has_draft) sd[e] = drow[e0 + e];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + j;
+          if (done || i > K) continue;
+          if (i < K && (force || !(f[j] & REC_ACC_CERT))) {
+            start = i;
+            done = true;
+          } else if (i == K || !(f[j] & REC_ACCEPT)) {
+            n = i;
+            done = true;
+            if (!force && (f[j] & REC_DRAW_CERT)) ysel = yv[j];
+            else start = n;
+          }
         }
       }
-      __syncthreads();
-      const RowRec rr = recs[need];
-      const float *uv = P.uniforms + ((int64_t)bb * (K + 1) + need) * 2;
-      float lp_x = 0.f, lq_x = 0.f;
-      if (has_draft) {
-        const int x = min(max(toks[need], 0), V - 1);
-        lp_x = to_f32(trow[x]);
-        lq_x = to_f32(drow[x]);
+      if (start < 0 && rank == 0 && b % ncl == cid) {
+        for (int j = 0; j <= K; ++j)
+          P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? ysel : -1);
+        P.num_acc[b] = n;
       }
-      int yy = -1;
-      const bool acc = exact_row<TT, DK>(P, sh, st, sd, n_grp, e0, has_draft, need_acc, rr.m_p, rr.m_q,
-                                         lp_x, lq_x, uv[0], uv[1], &yy);
-      if (rank == 0 && tid == 0) {
-        RowRec *w = P.recs + (int64_t)bb * (K + 1) + need;
-        w->flags = rr.flags | (need_acc ? REC_EXACT_ACC : 0u) | (acc ? 0u : REC_EXACT_DRAW);
-        if (!acc) w->y_exact = yy;
-      }
-      __syncthreads();   // the slice buffers are rewritten next
-      if (need_acc && acc) { i = need + 1; continue; }   // accepted: continue the walk
-      n = need;
-      y = yy;
-      break;
     }
-    if (rank == 0) {
-      for (int j = tid; j <= K; j += blockDim.x)
-        P.out_tokens[(int64_t)bb * (K + 1) + j] = j < n ? toks[j] : (j == n ? y : -1);
-      if (tid == 0) P.num_acc[bb] = n;
+    // deterministic compaction (same order in every CTA of every cluster)
+    const unsigned vote = __ballot_sync(0xffffffffu, start >= 0);
+    if (lane == 0) warp_cnt[warp] = __popc(vote);
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      for (int w = 0; w < kResWarps; ++w) { const int t = warp_cnt[w]; warp_cnt[w] = acc; acc += t; }
+      list_n = acc;
     }
+    __syncthreads();
+    if (start >= 0) {
+      const int pos = warp_cnt[warp] + __popc(vote & ((1u << lane) - 1u));
+      list_b[pos] = b;
+      list_i[pos] = start;
+    }
+    __syncthreads();
+
+    // ---- float-float re-evaluation of this cluster's list entries ---------
+    for (int li = cid; li < list_n; li += ncl) {
+      const int bb = list_b[li];
+      const RowRec *recs = P.recs + (int64_t)bb * (K + 1);
+      const int32_t *toks = P.tokens + (int64_t)bb * K;
+      int i = list_i[li], n = K, y = -1;
+      for (;;) {
+        // next position needing evaluation from i on (certified accepts skipped)
+        int need = -1;
+        bool need_acc = false;
+        for (; i < K; ++i) {
+          const uint32_t f = recs[i].flags;
+          if (force || !(f & REC_ACC_CERT)) { need = i; need_acc = true; break; }
+          if (!(f & REC_ACCEPT)) break;
+        }
+        n = min(i, K);
+        if (need < 0) {
+          if (!force && (recs[n].flags & REC_DRAW_CERT)) { y = recs[n].y; break; }
+          need = n;
+        }
+        const bool has_draft = need < K;
+        const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + need) * V;
+        const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + need) * V : nullptr;
+        // slice -> shared memory (bulk copy when rows are 16-byte aligned)
+        for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {
+          st[e] = pad_value<TT>(false);
+          if (has_draft) sd[e] = pad_value<TD>(DK == 1);
+        }
+        if (vec) {
+          if (tid == 0 && n_loc > 0) {
+            const uint32_t nbt = (uint32_t)n_loc * sizeof(TT), nbd = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
+            fence_proxy_async_shared();
+            mbar_arrive_expect_tx(&bar, nbt + nbd);
+            bulk_g2s(st, trow + e0, nbt, &bar);
+            if (has_draft) bulk_g2s(sd, drow + e0, nbd, &bar);
+          }
+          if (n_loc > 0) {
+            if (!mbar_wait(&bar, phase) && tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+            phase ^= 1u;
+          }
+        } else {
+          for (int e = tid; e < n_loc; e += blockDim.x) {
+            st[e] = trow[e0 + e];
+            if (has_draft) sd[e] = drow[e0 + e];
+          }
+        }
+        __syncthreads();
+        const RowRec rr = recs[need];
+        const float *uv = P.uniforms + ((int64_t)bb * (K + 1) + need) * 2;
+        float lp_x = 0.f, lq_x = 0.f;
+        if (has_draft) {
+          const int x = min(max(toks[need], 0), V - 1);
+          lp_x = to_f32(trow[x]);
+          lq_x = to_f32(drow[x]);
+        }
+        int yy = -1;
+        const bool acc = exact_row<TT, DK>(P, sh, st, sd, cp, cq, n_grp, e0, has_draft, need_acc, rr.m_p,
+                                           rr.m_q, lp_x, lq_x, uv[0], uv[1], &yy);
+        if (rank == 0 && tid == 0) {
+          RowRec *w = P.recs + (int64_t)bb * (K + 1) + need;
+          w->flags = rr.flags | (need_acc ? REC_EXACT_ACC : 0u) | (acc ? 0u : REC_EXACT_DRAW);
+          if (!acc) w->y_exact = yy;
+        }
+        __syncthreads();   // the slice buffers are rewritten next
+        if (need_acc && acc) { i = need + 1; continue; }   // accepted: continue the walk
+        n = need;
+        y = yy;
+        break;
+      }
+      if (rank == 0) {
+        for (int j = tid; j <= K; j += blockDim.x)
+          P.out_tokens[(int64_t)bb * (K + 1) + j] = j < n ? toks[j] : (j == n ? y : -1);
+        if (tid == 0) P.num_acc[bb] = n;
+      }
+    }
+    __syncthreads();   // the list is rebuilt in the next round
   }
   cluster_sync();   // no CTA leaves while a peer may still read its shared memory
 }
@@ -967,7 +1192,7 @@ sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, si
     return fail(SV_ERR_CUDA, "spec_verify_sample: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   cudaError_t e = launch_cluster(sample_rows_kernel<TT, DK>, dim3(cs, P.K + 1, P.B), kRowThreads, smem, cs, s, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample rows launch: %s", cudaGetErrorString(e));
-  const int ncl = std::max(std::min(P.B, kFinishClusters), (P.B + kFinishMaxSeq - 1) / kFinishMaxSeq);
+  const int ncl = std::max(1, std::min(P.B, kFinishClusters));
   e = launch_cluster(sample_finish_kernel<TT, DK>, dim3(cs_x * ncl), kResThreads, smem_x, cs_x, s, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
   return ok();
@@ -1042,15 +1267,19 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   // finish kernel: 16-CTA clusters (8 for small vocabularies)
   const int cs_x = V >= 65536 ? 16 : 8;
   int ns_x = 0;
-  const size_t smem_x = slice_smem(cs_x, ns_x);
-  if (cs && (!steps_ok(ns, kRowWarps) || !steps_ok(ns_x, kResWarps) || smem_x > kMaxSliceSmem)) cs = 0;
+  size_t smem_x = slice_smem(cs_x, ns_x);
+  // float-float exponentials of both rows cached when they fit
+  const size_t cache_bytes = (size_t)ns_x * sizeof(ff) * ((draft_is_probs && K > 0) ? 1 : 2);
+  const bool cache_x = smem_x + cache_bytes <= kMaxSliceSmem;
+  if (cache_x) smem_x += cache_bytes;
+  if (cs && (!steps_ok(ns_x, kResWarps) || smem_x > kMaxSliceSmem)) cs = 0;
   if (!cs) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large", V);
 
   SampleParams P = {};
   P.target = target_logits; P.draft = draft; P.tokens = draft_tokens; P.uniforms = uniforms;
   P.p_at = p_at_draft; P.q_at = q_at_draft; P.out_tokens = out_tokens; P.num_acc = num_accepted;
   P.recs = static_cast<RowRec *>(workspace); P.status = dev_status;
-  P.B = B; P.K = K; P.V = V; P.ns = ns; P.ns_x = ns_x; P.flags = flags;
+  P.B = B; P.K = K; P.V = V; P.ns = ns; P.ns_x = ns_x; P.flags = flags; P.cache_x = cache_x ? 1 : 0;
   P.aligned = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0 &&
               (K == 0 || (aligned(draft, 16) && ((size_t)V * es_buf_d) % 16 == 0));
   const double log2e = 1.4426950408889634074, ln2 = 0.69314718055994530942;
