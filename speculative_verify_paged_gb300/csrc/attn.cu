@@ -91,6 +91,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// 2^x on the SFU (results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // two e4m3 codes (low byte first) -> f16x2
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t out;
@@ -407,15 +414,23 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
         const int t0 = lb * kBS;
         const bool valid = lb < blk1;
         nvk[j] = valid ? L - t0 : 0;   // valid keys of the block (>= 16 unless tail)
+        // warp-uniform: only blocks reaching the causal diagonal (or past
+        // the split) are masked
         const bool tail = !valid || t0 + kBS - 1 > L - P.n_new;
+        if (!tail) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
+          for (int n = 0; n < 2; ++n)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = t0 + n * 8 + 2 * tq + (e & 1);
-            const int lim = (e < 2) ? lim_lo : lim_hi;
-            const float v = sacc[2 * j + n][e] * scale_log2;
-            x[2 * j + n][e] = (!tail || (valid && t <= lim)) ? v : -INFINITY;
+            for (int e = 0; e < 4; ++e) x[2 * j + n][e] = sacc[2 * j + n][e] * scale_log2;
+        } else {
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = t0 + n * 8 + 2 * tq + (e & 1);
+              const int lim = (e < 2) ? lim_lo : lim_hi;
+              x[2 * j + n][e] = (valid && t <= lim) ? sacc[2 * j + n][e] * scale_log2 : -INFINITY;
+            }
           }
         }
       }
@@ -429,12 +444,16 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
       mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
       mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-      const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-      const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-      const float a_lo = exp2f(m_lo - base_lo), a_hi = exp2f(m_hi - base_hi);
-      m_lo = mn_lo;
-      m_hi = mn_hi;
+      // The reference m moves only when a tile's maximum exceeds it by more
+      // than 8 (log2 units): weights stay <= 2^8, and the accumulator is
+      // rescaled only then (the same m is stored with l, so nothing else
+      // depends on it being the running maximum).
+      const bool up_lo = mx_lo > m_lo + 8.f, up_hi = mx_hi > m_hi + 8.f;
+      float a_lo = 1.f, a_hi = 1.f;
+      if (up_lo) { a_lo = m_lo == -INFINITY ? 0.f : ex2f(m_lo - mx_lo); m_lo = mx_lo; }
+      if (up_hi) { a_hi = m_hi == -INFINITY ? 0.f : ex2f(m_hi - mx_hi); m_hi = mx_hi; }
+      const float base_lo = m_lo == -INFINITY ? 0.f : m_lo;
+      const float base_hi = m_hi == -INFINITY ? 0.f : m_hi;
       float ps_lo = 0.f, ps_hi = 0.f;
       uint32_t pa[kBPW][4];
 #pragma unroll
@@ -442,10 +461,10 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
         float pv[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
-          pv[n][0] = exp2f(x[2 * j + n][0] - base_lo);
-          pv[n][1] = exp2f(x[2 * j + n][1] - base_lo);
-          pv[n][2] = exp2f(x[2 * j + n][2] - base_hi);
-          pv[n][3] = exp2f(x[2 * j + n][3] - base_hi);
+          pv[n][0] = ex2f(x[2 * j + n][0] - base_lo);
+          pv[n][1] = ex2f(x[2 * j + n][1] - base_lo);
+          pv[n][2] = ex2f(x[2 * j + n][2] - base_hi);
+          pv[n][3] = ex2f(x[2 * j + n][3] - base_hi);
           ps_lo += pv[n][0] + pv[n][1];
           ps_hi += pv[n][2] + pv[n][3];
         }
@@ -456,10 +475,12 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
       }
       l_lo = l_lo * a_lo + ps_lo;
       l_hi = l_hi * a_hi + ps_hi;
+      if (__any_sync(0xffffffffu, up_lo || up_hi)) {
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= a_lo; o[n][1] *= a_lo;
-        o[n][2] *= a_hi; o[n][3] *= a_hi;
+        for (int n = 0; n < 16; ++n) {
+          o[n][0] *= a_lo; o[n][1] *= a_lo;
+          o[n][2] *= a_hi; o[n][3] *= a_hi;
+        }
       }
       // ---- O += P V ---------------------------------------------------------
       // keys at or past L (tail block, or a block past the split) may hold
@@ -511,56 +532,57 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
     *reinterpret_cast<float4 *>(xbuf + 64) = make_float4(m_lo, m_hi, l_lo, l_hi);
   }
   named_bar_sync(3, Cfg::kCompute * 32);
-  if (kg != 0) return;
-  {
-    const float4 ml = *reinterpret_cast<const float4 *>(xbuf + 64);
-    const float mn_lo = fmaxf(m_lo, ml.x), mn_hi = fmaxf(m_hi, ml.y);
-    const float b_lo = mn_lo == -INFINITY ? 0.f : mn_lo, b_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-    const float a0l = exp2f(m_lo - b_lo), a1l = exp2f(ml.x - b_lo);
-    const float a0h = exp2f(m_hi - b_hi), a1h = exp2f(ml.y - b_hi);
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const float4 v = *reinterpret_cast<const float4 *>(xbuf + 4 * n);
-      o[n][0] = o[n][0] * a0l + v.x * a1l;
-      o[n][1] = o[n][1] * a0l + v.y * a1l;
-      o[n][2] = o[n][2] * a0h + v.z * a1h;
-      o[n][3] = o[n][3] * a0h + v.w * a1h;
-    }
-    l_lo = l_lo * a0l + ml.z * a1l;
-    l_hi = l_hi * a0h + ml.w * a1h;
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-  }
   const float vs = FP8 ? P.v_scale[g] : 1.f;
   const int nsplit = (nblk + P.bps - 1) / P.bps;
-  if (nsplit == 1) {
-    // the whole sequence was this split: write the normalised output
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P.out);
-    const float il = l_lo > 0.f ? vs / l_lo : 0.f, ih = l_hi > 0.f ? vs / l_hi : 0.f;
-    auto orow = [&](int r) {
-      const int j = r / P.G, hh = r % P.G;
-      return out + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
-    };
+  if (kg == 0) {
+    {
+      const float4 ml = *reinterpret_cast<const float4 *>(xbuf + 64);
+      const float mn_lo = fmaxf(m_lo, ml.x), mn_hi = fmaxf(m_hi, ml.y);
+      const float b_lo = mn_lo == -INFINITY ? 0.f : mn_lo, b_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+      const float a0l = ex2f(m_lo - b_lo), a1l = ex2f(ml.x - b_lo);
+      const float a0h = ex2f(m_hi - b_hi), a1h = ex2f(ml.y - b_hi);
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int c = n * 8 + 2 * tq;
-      if (r_lo < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_lo) + c) = __floats2bfloat162_rn(o[n][0] * il, o[n][1] * il);
-      if (r_hi < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_hi) + c) = __floats2bfloat162_rn(o[n][2] * ih, o[n][3] * ih);
+      for (int n = 0; n < 16; ++n) {
+        const float4 v = *reinterpret_cast<const float4 *>(xbuf + 4 * n);
+        o[n][0] = o[n][0] * a0l + v.x * a1l;
+        o[n][1] = o[n][1] * a0l + v.y * a1l;
+        o[n][2] = o[n][2] * a0h + v.z * a1h;
+        o[n][3] = o[n][3] * a0h + v.w * a1h;
+      }
+      l_lo = l_lo * a0l + ml.z * a1l;
+      l_hi = l_hi * a0h + ml.w * a1h;
+      m_lo = mn_lo;
+      m_hi = mn_hi;
     }
-    return;
-  }
-  const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
-  float *acc = P.ws_acc + ent * P.R * kD;
-  float *mlp = P.ws_ml + ent * P.R * 2;
+    if (nsplit == 1) {
+      // the whole sequence was this split: write the normalised output
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P.out);
+      const float il = l_lo > 0.f ? vs / l_lo : 0.f, ih = l_hi > 0.f ? vs / l_hi : 0.f;
+      auto orow = [&](int r) {
+        const int j = r / P.G, hh = r % P.G;
+        return out + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
+      };
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const int c = n * 8 + 2 * tq;
-    if (r_lo < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_lo * kD + c) = make_float2(o[n][0] * vs, o[n][1] * vs);
-    if (r_hi < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_hi * kD + c) = make_float2(o[n][2] * vs, o[n][3] * vs);
-  }
-  if (tq == 0) {
-    if (r_lo < P.R) { mlp[r_lo * 2] = m_lo; mlp[r_lo * 2 + 1] = l_lo; }
-    if (r_hi < P.R) { mlp[r_hi * 2] = m_hi; mlp[r_hi * 2 + 1] = l_hi; }
+      for (int n = 0; n < 16; ++n) {
+        const int c = n * 8 + 2 * tq;
+        if (r_lo < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_lo) + c) = __floats2bfloat162_rn(o[n][0] * il, o[n][1] * il);
+        if (r_hi < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_hi) + c) = __floats2bfloat162_rn(o[n][2] * ih, o[n][3] * ih);
+      }
+    } else {
+      const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
+      float *acc = P.ws_acc + ent * P.R * kD;
+      float *mlp = P.ws_ml + ent * P.R * 2;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const int c = n * 8 + 2 * tq;
+        if (r_lo < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_lo * kD + c) = make_float2(o[n][0] * vs, o[n][1] * vs);
+        if (r_hi < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_hi * kD + c) = make_float2(o[n][2] * vs, o[n][3] * vs);
+      }
+      if (tq == 0) {
+        if (r_lo < P.R) { mlp[r_lo * 2] = m_lo; mlp[r_lo * 2 + 1] = l_lo; }
+        if (r_hi < P.R) { mlp[r_hi * 2] = m_hi; mlp[r_hi * 2 + 1] = l_hi; }
+      }
+    }
   }
 }
 
@@ -1052,6 +1074,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     else rc = launch_gen<uint8_t, __nv_bfloat16>(P, st);
   }
   if (rc != SV_OK) return rc;
+  if (plan.S == 1) return ok();   // every sequence was written directly
   MergeParams M;
   M.ws_acc = ws_acc; M.ws_ml = ws_ml; M.seq_lens = seq_lens; M.out = out;
   M.B = B; M.n_new = n_new; M.H_q = H_q; M.H_kv = H_kv; M.G = G; M.R = plan.R; M.d = d_head; M.bs = block_size;
