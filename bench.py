@@ -95,7 +95,7 @@ def measured_peaks():
 def attn_traffic_from_profile():
     """DRAM bytes per attention launch from the committed ncu summary, if the
     kernel source is unchanged since the capture (else None)."""
-    p = os.path.join(ROOT, "profiles", "attn_tc_llama3_70b.md")
+    p = os.path.join(ROOT, "profiles", "attn_tc5_llama3_70b.md")
     src = os.path.join(ROOT, "speculative_verify_paged_gb300", "csrc", "attn.cu")
     if not (os.path.exists(p) and os.path.exists(src)):
         return None
@@ -373,7 +373,7 @@ def run_ours(args, rank, world, local):
                 "attn_gbs": attn_gbs, "sample_gbs": samp_gbs,
                 "attn_frac_of_8tbs": attn_gbs / NOMINAL_HBM_GBS, "sample_frac_of_8tbs": samp_gbs / NOMINAL_HBM_GBS,
                 "emitted_tokens_per_step": emitted_per_step},
-        "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (attn_tc_kernel + attn_merge_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (attn_tc5_kernel + attn_merge_kernel)",
                      "achieved": attn_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": attn_gbs / peak, "traffic": attn_traffic_from_profile()},
         "roofline_sample": {"bound": "hbm", "kernel": "spec_verify_sample (rows + resolve)",

@@ -130,6 +130,7 @@ __device__ __forceinline__ uint32_t swz16(uint32_t tile, int row, int col) {
 struct TcParams {   // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmk;
   CUtensorMap tmv;
+  CUtensorMap tmq;   // q [B][n_new][H_q][d]: a box is one head-dim half of a GQA group's rows
   const void *q;
   void *out;       // [B][n_new][H_q][kD] bf16, written directly when a sequence has one split
   const float *k_scale;
@@ -586,6 +587,450 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
   }
 }
 
+// ------------------------------------------- tcgen05 tensor-core kernel ---
+// The same attention on the fifth-generation tensor cores: accumulators live
+// in tensor memory (TMEM), one thread issues the MMAs, and the softmax warps
+// read S and write P through TMEM, so no warp holds an accumulator in
+// registers.
+//
+// CTA = (split s, kv head g, sequence b), 192 threads:
+//   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
+//              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
+//   warp 4     TMA producers: lane 0 streams K tiles, lane 1 V tiles, each
+//              into its own shared-memory ring (a K stage is free again as
+//              soon as its Q K^T has run, a V stage after its P V)
+//   warp 5     TMEM owner; lane 0 issues the MMAs from a polling loop, so
+//              Q K^T runs ahead whenever K data and an S buffer are ready
+// A tile is kT5Blk paged blocks (N = 16 kT5Blk keys). Per tile t, with
+// buffer u = t % kT5SBuf:
+//   S[u] = Q K^T           (M=128 padded query rows, N keys, K=128)
+//   P[u] = 2^(S c - m)      bf16, written over the first N/2 columns of S[u]
+//   O   += P V              (M=128, N=128 head dims, K=16 keys per MMA)
+// Each buffer has its own "P V done" barrier, so every wait is at most one
+// phase behind its barrier.
+// Shared-memory operands use the 128-byte swizzle: Q and K are K-major
+// (head dim contiguous), V is MN-major (head dim contiguous along N).
+constexpr int kT5Blk = 2;                      // blocks per tile
+constexpr int kT5N = 16 * kT5Blk;              // keys per tile
+constexpr int kT5SBuf = 4;                     // S / P buffers in TMEM
+constexpr int kT5Threads = 192;
+constexpr int kT5MaxR = 128;
+constexpr int kT5HalfBytes = kT5Blk * 2048;    // one head-dim half of K (or V) for a tile
+constexpr int kT5TileBytes = 2 * kT5HalfBytes; // K (or V) of one tile
+// Q staging: 64 rows serve R <= 64 (the MMA's rows 64-127 then read other
+// shared memory; those rows of S, P and O are never used), else 128. The
+// rings take what two CTAs per SM leave.
+template <int QR> struct T5Cfg {
+  static constexpr int kQBytes = 2 * QR * 128;
+  static constexpr int kKS = QR == 64 ? 6 : 5;   // K stages
+  static constexpr int kVS = QR == 64 ? 5 : 4;   // V stages
+  static constexpr int kSmem = 1024 + kQBytes + (kKS + kVS) * kT5TileBytes;
+};
+constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O
+constexpr uint32_t kT5OCol = kT5SBuf * kT5N;
+static_assert(kT5OCol + 128 <= kT5Cols, "TMEM budget");
+
+__device__ __forceinline__ uint64_t t5_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;   // descriptor version of the sm_100 family
+  d |= (uint64_t)2 << 61;   // 128-byte swizzle
+  return d;
+}
+
+// byte offset of (row, col < 64) in a [rows][64] bf16 region with the
+// 128-byte swizzle (8-row atoms of 1024 bytes)
+__device__ __forceinline__ uint32_t t5_sw(int row, int col) {
+  return (row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
+}
+
+__device__ __forceinline__ void t5_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void t5_mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+               "r"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void t5_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void t5_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void t5_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void t5_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void t5_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void t5_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void t5_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Non-blocking probe of a barrier phase.
+__device__ __forceinline__ bool t5_test(uint64_t *bar, uint32_t phase) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait that gives up at once after any earlier wait of the CTA gave up.
+__device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile int *abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, phase)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
+template <int QR>
+__global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
+  using Cfg = T5Cfg<QR>;
+  constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
+  constexpr int kQHalf = QR * 128;   // bytes of one head-dim half of Q
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+  __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *q_smem = smem;
+  const uint32_t k_ring = smem_u32(smem) + Cfg::kQBytes;
+  const uint32_t v_ring = k_ring + KS * kT5TileBytes;
+
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * kBS) {
+    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int nblk = (L + kBS - 1) / kBS;
+  const int blk0 = s * P.bps;
+  if (blk0 >= nblk) return;   // the merge never reads this split
+  const int blk1 = min(nblk, blk0 + P.bps);
+  const int nblocks = blk1 - blk0;
+  const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+  const int R = P.R;
+
+  if (tid == 0) {
+    for (int k = 0; k < KS; ++k) {
+      mbar_init(&k_full[k], 1);
+      mbar_init(&k_empty[k], 1);
+    }
+    for (int k = 0; k < VS; ++k) {
+      mbar_init(&v_full[k], 1);
+      mbar_init(&v_empty[k], 1);
+    }
+    for (int k = 0; k < kT5SBuf; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&p_full[k], 4);
+      mbar_init(&o_done[k], 1);
+    }
+    mbar_init(&mma_drain, 1);
+    mbar_init(&q_full, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  volatile int *abf = &abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producers --
+    // lane 0 copies Q (rows past R are left as they are: their rows of S,
+    // P and O are never read) and then streams K; lane 1 streams V
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&q_full, (uint32_t)(2 * R * 128));
+      for (int h = 0; h < 2; ++h)
+        tma_load_4d(smem_u32(q_smem) + h * kQHalf, &P.tmq, h * 64, g * P.G, 0, b, &q_full);
+    }
+    if (lane < 2) {
+      const bool isv = lane == 1;
+      const int NS = isv ? VS : KS;
+      uint64_t *fullb = isv ? v_full : k_full;
+      uint64_t *emptyb = isv ? v_empty : k_empty;
+      const uint32_t ring = isv ? v_ring : k_ring;
+      const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
+      const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
+      int issued = 0;
+      int nxt[kT5Blk];   // table entries of the next tile, loaded one tile ahead
+#pragma unroll
+      for (int kk = 0; kk < kT5Blk; ++kk) nxt[kk] = kk < nblocks ? table[kk] : 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        int cur[kT5Blk];
+#pragma unroll
+        for (int kk = 0; kk < kT5Blk; ++kk) {
+          cur[kk] = nxt[kk];
+          const int e = (t + 1) * kT5Blk + kk;
+          nxt[kk] = e < nblocks ? table[e] : 0;
+        }
+        const int st = t % NS;
+        if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf)) break;
+        const int nvalid = min(kT5Blk, nblocks - t * kT5Blk);
+        mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * 2 * 2048));
+        const uint32_t base = ring + st * kT5TileBytes;
+        for (int kk = 0; kk < nvalid; ++kk) {
+          int ph = cur[kk];
+          if (ph < 0 || ph >= P.num_blocks) {
+            if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+            ph = 0;   // stay in bounds; the output of this sequence is flagged
+          }
+          int c[3];
+          tile_coords(P, g, ph, c);
+          tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
+          tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
+        }
+        issued = t + 1;
+      }
+      // the copies in flight land before the CTA may exit
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      if (lane == 0 && !mbar_wait(&q_full, 0)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+    }
+  } else {
+    if (warp == 5) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                   "r"(kT5Cols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    t5_fence_before();
+    named_bar_sync(1, 160);   // TMEM allocated
+    t5_fence_after();
+    const uint32_t tb = tmem_base;
+
+    if (warp == 5) {
+      // ---------------------------------------------------------- MMA issuer --
+      if (lane == 0) {
+        const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
+        const uint32_t idesc_pv = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (16u << 17) | (8u << 24);
+        static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
+        const uint32_t qa = smem_u32(q_smem);
+        int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
+        bool q_ready = false;
+        uint64_t t_last = global_ns();
+        while (tp < n_tiles) {
+          bool progressed = false;
+          if (!q_ready) q_ready = t5_test(&q_full, 0);
+          if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
+            const int ks = tq % KS, sb = tq % kT5SBuf;
+            // S buffer sb is free once the P V of tile tq - kT5SBuf has run
+            const bool sfree = tq < kT5SBuf || t5_test(&o_done[sb], ((tq / kT5SBuf) - 1) & 1);
+            if (sfree && t5_test(&k_full[ks], (tq / KS) & 1)) {
+              t5_fence_after();
+              const uint32_t kb = k_ring + ks * kT5TileBytes;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                t5_mma_ss(tb + sb * kT5N, t5_desc(qa + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+                          t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
+                          kk > 0 ? 1u : 0u);
+              t5_commit(&s_full[sb]);
+              t5_commit(&k_empty[ks]);
+              ++tq;
+              progressed = true;
+            }
+          }
+          if (tp < tq) {
+            const int vs = tp % VS, sb = tp % kT5SBuf;
+            if (t5_test(&p_full[sb], (tp / kT5SBuf) & 1) && t5_test(&v_full[vs], (tp / VS) & 1)) {
+              t5_fence_after();
+              const uint32_t vb = v_ring + vs * kT5TileBytes;
+#pragma unroll
+              for (int j = 0; j < kT5Blk; ++j)
+                t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
+                          idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
+              t5_commit(&v_empty[vs]);
+              t5_commit(&o_done[sb]);
+              ++tp;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            t_last = global_ns();
+          } else if (*abf || global_ns() - t_last > kWaitLimitNs) {
+            *abf = 1;
+            break;
+          }
+        }
+        // every MMA issued has completed before TMEM can be released
+        t5_commit(&mma_drain);
+        if (!mbar_wait(&mma_drain, 0)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ softmax ----
+      const int row = tid;   // warps 0-3
+      const bool warp_live = warp * 32 < R;
+      const bool live = row < R;
+      const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
+      const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
+      const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
+      const float sl2 = P.scale_log2;
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int sb = t % kT5SBuf, vs = t % VS;
+        ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (t / kT5SBuf) & 1, abf));
+        if (!ok) break;
+        t5_fence_after();
+        const int key0 = (blk0 + t * kT5Blk) * kBS;
+        if (warp_live) {
+          float x[kT5N];
+          {
+            uint32_t r[kT5N];
+#pragma unroll
+            for (int c0 = 0; c0 < kT5N; c0 += 16)
+              t5_ld16(lane_base + sb * kT5N + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+            t5_wait_ld();
+#pragma unroll
+            for (int k = 0; k < kT5N; ++k) x[k] = __uint_as_float(r[k]) * sl2;
+          }
+          if (key0 + kT5N > end_key || key0 + kT5N - 1 > L - P.n_new) {   // reaches the diagonal or the end
+#pragma unroll
+            for (int k = 0; k < kT5N; ++k)
+              if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
+          // the reference moves only when a tile exceeds it by more than 8
+          const bool up = mx > m_ref + 8.f;
+          float a = 1.f;
+          if (up) {
+            a = m_ref == -INFINITY ? 0.f : ex2f(m_ref - mx);
+            m_ref = mx;
+          }
+          if (t > 0 && __any_sync(0xffffffffu, up)) {
+            // rescale O: the previous P V must have landed first
+            const int pb = (t - 1) % kT5SBuf;
+            ok = __all_sync(0xffffffffu, t5_wait(&o_done[pb], ((t - 1) / kT5SBuf) & 1, abf));
+            t5_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+              uint32_t r[16];
+              t5_ld16(lane_base + kT5OCol + c0, r);
+              t5_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
+              t5_st16(lane_base + kT5OCol + c0, r);
+            }
+            t5_wait_st();
+          }
+          l *= a;
+          const float base = m_ref == -INFINITY ? 0.f : m_ref;
+          float ps = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kT5N; c0 += 32) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
+              ps += p0 + p1;
+              w[k] = pack2<false>(p0, p1);
+            }
+            t5_st16(lane_base + sb * kT5N + c0 / 2, w);
+          }
+          t5_wait_st();
+          l += ps;
+        }
+        if (key0 + kT5N > end_key && warp == 0) {
+          // keys past the split or the sequence (not loaded, or stale): V rows
+          // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
+          if (!t5_wait(&v_full[vs], (t / VS) & 1, abf)) ok = false;
+          const uint32_t vb = v_ring + vs * kT5TileBytes;
+          for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
+            const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + h * kT5HalfBytes + off + c * 16),
+                             "r"(0u)
+                             : "memory");
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        t5_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      // ---- epilogue: O of this row -------------------------------------------
+      const int lb = (n_tiles - 1) % kT5SBuf;
+      const bool have = __all_sync(0xffffffffu, ok && t5_wait(&o_done[lb], ((n_tiles - 1) / kT5SBuf) & 1, abf));
+      t5_fence_after();
+      if (have && warp_live) {
+        const int nsplit = (nblk + P.bps - 1) / P.bps;
+        const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
+        __nv_bfloat16 *out = nullptr;
+        float *acc = nullptr;
+        if (live) {
+          const int j = row / P.G, hh = row % P.G;
+          out = static_cast<__nv_bfloat16 *>(P.out) + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
+          acc = P.ws_acc + (ent * P.R + row) * kD;
+        }
+        const float il = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          uint32_t r[64];
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + kT5OCol + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+          t5_wait_ld();
+          if (live) {
+            if (nsplit == 1) {
+#pragma unroll
+              for (int c = 0; c < 64; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  w[k] = pack2<false>(__uint_as_float(r[c + 2 * k]) * il, __uint_as_float(r[c + 2 * k + 1]) * il);
+                *reinterpret_cast<uint4 *>(out + c0 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; c += 4)
+                *reinterpret_cast<float4 *>(acc + c0 + c) =
+                    make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]), __uint_as_float(r[c + 2]),
+                                __uint_as_float(r[c + 3]));
+            }
+          }
+        }
+        if (live && nsplit > 1) {
+          P.ws_ml[(ent * P.R + row) * 2] = m_ref;
+          P.ws_ml[(ent * P.R + row) * 2 + 1] = l;
+        }
+      }
+    }
+  }
+  if (tid == 0 && *abf) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+  t5_fence_before();
+  __syncthreads();
+  t5_fence_after();
+  if (warp == 5) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kT5Cols));
+}
+
 // ----------------------------------------------------- CUDA-core kernel ---
 struct GenParams {
   const void *q;
@@ -906,10 +1351,14 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
   if (lay)
     strides_ok = (lay->block_stride * es) % 16 == 0 && (lay->head_stride * es) % 16 == 0 &&
                  (lay->slot_stride * es) % 16 == 0;
-  p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS && p.R <= 16 * kMaxRT &&
-         strides_ok;
+  p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS &&
+         p.R <= (kv == SV_BF16 ? kT5MaxR : 16 * kMaxRT) && strides_ok;
   if (bps_req > 0) {
     p.bps = bps_req;
+  } else if (p.tc && kv == SV_BF16) {
+    // tcgen05 kernel: long splits amortise its per-CTA setup (TMEM, Q,
+    // pipeline fill); at least one split per SM when the batch is small
+    p.bps = std::min(128, std::max(16, pow2_floor((int64_t)max_blocks * B * H_kv / num_sms())));
   } else {
     // fp32 caches are planned like bf16 ones so every dtype fits the same
     // workspace
@@ -943,6 +1392,20 @@ sv_status launch_tc(const TcParams &P, cudaStream_t st) {
   dim3 grid(P.S, P.H_kv, P.B);
   attn_tc_kernel<RT, FP8><<<grid, Cfg::kThreads, Cfg::kSmem, st>>>(P);
   return check_launch("spec_verify_attn tensor-core launch");
+}
+
+template <int QR>
+sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_tc5_kernel<QR>, cudaFuncAttributeMaxDynamicSharedMemorySize, T5Cfg<QR>::kSmem);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  dim3 grid(P.S, P.H_kv, P.B);
+  attn_tc5_kernel<QR><<<grid, kT5Threads, T5Cfg<QR>::kSmem, st>>>(P);
+  return check_launch("spec_verify_attn tcgen05 launch");
 }
 
 template <typename TKV, typename TQ>
@@ -1045,21 +1508,35 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
+    if (!fp8) {
+      // q [B][n_new][H_q][d]: box = 64 dims x G heads x n_new positions of one
+      // batch entry, i.e. one head-dim half of the group's (K+1) G rows
+      if (!aligned(q, 16)) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: q must be 16-byte aligned");
+      cuuint64_t qd[4] = {(cuuint64_t)d_head, (cuuint64_t)H_q, (cuuint64_t)n_new, (cuuint64_t)B};
+      cuuint64_t qs[3] = {(cuuint64_t)d_head * 2, (cuuint64_t)H_q * d_head * 2, (cuuint64_t)n_new * H_q * d_head * 2};
+      cuuint32_t qb[4] = {64, (cuuint32_t)G, (cuuint32_t)n_new, 1};
+      if (G > 256 || n_new > 256)
+        return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: query group too large for the tensor-core path");
+      CUresult r = enc(&P.tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), qd, qs, qb, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
+    }
     P.q = q; P.out = out; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
     P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
     P.scale_log2 = scale_log2;
     const int RT = (plan.R + 15) / 16;
-    switch (RT * 2 + (fp8 ? 1 : 0)) {
-      case 2: rc = launch_tc<1, false>(P, st); break;
-      case 3: rc = launch_tc<1, true>(P, st); break;
-      case 4: rc = launch_tc<2, false>(P, st); break;
-      case 5: rc = launch_tc<2, true>(P, st); break;
-      case 6: rc = launch_tc<3, false>(P, st); break;
-      case 7: rc = launch_tc<3, true>(P, st); break;
-      case 8: rc = launch_tc<4, false>(P, st); break;
-      default: rc = launch_tc<4, true>(P, st); break;
+    if (!fp8) {
+      rc = plan.R <= 64 ? launch_tc5<64>(P, st) : launch_tc5<128>(P, st);
+    } else {
+      switch (RT) {
+        case 1: rc = launch_tc<1, true>(P, st); break;
+        case 2: rc = launch_tc<2, true>(P, st); break;
+        case 3: rc = launch_tc<3, true>(P, st); break;
+        default: rc = launch_tc<4, true>(P, st); break;
+      }
     }
   } else {
     GenParams P;
