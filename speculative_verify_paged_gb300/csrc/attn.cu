@@ -593,14 +593,19 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
 // read S and write P through TMEM, so no warp holds an accumulator in
 // registers.
 //
-// CTA = (split s, kv head g, sequence b), 192 threads:
+// CTA = (split s, kv head g, sequence b), 256 threads:
 //   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
 //              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
-//   warp 4     TMA producers: lane 0 streams K tiles, lane 1 V tiles, each
-//              into its own shared-memory ring (a K stage is free again as
-//              soon as its Q K^T has run, a V stage after its P V)
-//   warp 5     TMEM owner; lane 0 issues the MMAs from a polling loop, so
-//              Q K^T runs ahead whenever K data and an S buffer are ready
+//   warps 4, 5 TMA producers (one lane each, in separate warps so that neither
+//              waits behind the other's barrier): warp 4 copies Q and streams
+//              K tiles, warp 5 streams V tiles, each into its own shared-
+//              memory ring (a K stage is free again as soon as its Q K^T has
+//              run, a V stage after its P V)
+//   warp 6     TMEM owner; lane 0 issues the MMAs from a polling loop, so
+//              Q K^T runs ahead whenever K data and an S buffer are ready.
+//              It sits on the third scheduler (warp id % 4 = 2), away from
+//              the softmax warps that own rows 0-63.
+//   warp 7     idle
 // A tile is kT5Blk paged blocks (N = 16 kT5Blk keys). Per tile t, with
 // buffer u = t % kT5SBuf:
 //   S[u] = Q K^T           (M=128 padded query rows, N keys, K=128)
@@ -613,7 +618,8 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
 constexpr int kT5Blk = 2;                      // blocks per tile
 constexpr int kT5N = 16 * kT5Blk;              // keys per tile
 constexpr int kT5SBuf = 4;                     // S / P buffers in TMEM
-constexpr int kT5Threads = 192;
+constexpr int kT5Threads = 256;
+constexpr int kT5MmaWarp = 6;
 constexpr int kT5MaxR = 128;
 constexpr int kT5HalfBytes = kT5Blk * 2048;    // one head-dim half of K (or V) for a tile
 constexpr int kT5TileBytes = 2 * kT5HalfBytes; // K (or V) of one tile
@@ -758,60 +764,74 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
   __syncthreads();
   volatile int *abf = &abort_flag;
 
-  if (warp == 4) {
+  if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ producers --
     // lane 0 copies Q (rows past R are left as they are: their rows of S,
     // P and O are never read) and then streams K; lane 1 streams V
-    if (lane == 0) {
+    if (warp == 4 && lane == 0) {
       mbar_arrive_expect_tx(&q_full, (uint32_t)(2 * R * 128));
       for (int h = 0; h < 2; ++h)
         tma_load_4d(smem_u32(q_smem) + h * kQHalf, &P.tmq, h * 64, g * P.G, 0, b, &q_full);
     }
-    if (lane < 2) {
-      const bool isv = lane == 1;
+    {
+      // the whole warp walks the block table 32 entries at a time (the next
+      // 32 prefetched); lane 0 waits for free stages and issues the copies
+      const bool isv = warp == 5;
       const int NS = isv ? VS : KS;
       uint64_t *fullb = isv ? v_full : k_full;
       uint64_t *emptyb = isv ? v_empty : k_empty;
       const uint32_t ring = isv ? v_ring : k_ring;
       const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
       const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
+      int cur = lane < nblocks ? table[lane] : 0;
+      int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
+      int chunk = 0;
       int issued = 0;
-      int nxt[kT5Blk];   // table entries of the next tile, loaded one tile ahead
-#pragma unroll
-      for (int kk = 0; kk < kT5Blk; ++kk) nxt[kk] = kk < nblocks ? table[kk] : 0;
       for (int t = 0; t < n_tiles; ++t) {
-        int cur[kT5Blk];
+        const int first = t * kT5Blk;
+        if ((first >> 5) != chunk) {
+          chunk = first >> 5;
+          cur = nxt;
+          const int rel = (chunk + 1) * 32 + lane;
+          nxt = rel < nblocks ? table[rel] : 0;
+        }
+        int phys[kT5Blk];
 #pragma unroll
-        for (int kk = 0; kk < kT5Blk; ++kk) {
-          cur[kk] = nxt[kk];
-          const int e = (t + 1) * kT5Blk + kk;
-          nxt[kk] = e < nblocks ? table[e] : 0;
-        }
+        for (int kk = 0; kk < kT5Blk; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
         const int st = t % NS;
-        if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf)) break;
-        const int nvalid = min(kT5Blk, nblocks - t * kT5Blk);
-        mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * 2 * 2048));
-        const uint32_t base = ring + st * kT5TileBytes;
-        for (int kk = 0; kk < nvalid; ++kk) {
-          int ph = cur[kk];
-          if (ph < 0 || ph >= P.num_blocks) {
-            if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
-            ph = 0;   // stay in bounds; the output of this sequence is flagged
+        bool go = true;
+        if (lane == 0) {
+          if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf)) {
+            go = false;
+          } else {
+            const int nvalid = min(kT5Blk, nblocks - first);
+            mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * 2 * 2048));
+            const uint32_t base = ring + st * kT5TileBytes;
+            for (int kk = 0; kk < nvalid; ++kk) {
+              int ph = phys[kk];
+              if (ph < 0 || ph >= P.num_blocks) {
+                if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+                ph = 0;   // stay in bounds; the output of this sequence is flagged
+              }
+              int c[3];
+              tile_coords(P, g, ph, c);
+              tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
+              tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
+            }
+            issued = t + 1;
           }
-          int c[3];
-          tile_coords(P, g, ph, c);
-          tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
-          tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
         }
-        issued = t + 1;
+        if (!__shfl_sync(0xffffffffu, (int)go, 0)) break;
       }
       // the copies in flight land before the CTA may exit
-      for (int t = max(0, issued - NS); t < issued; ++t)
-        if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-      if (lane == 0 && !mbar_wait(&q_full, 0)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      if (lane == 0) {
+        for (int t = max(0, issued - NS); t < issued; ++t)
+          if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+        if (!isv && !mbar_wait(&q_full, 0)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      }
     }
-  } else {
-    if (warp == 5) {
+  } else if (warp < 4 || warp == kT5MmaWarp) {
+    if (warp == kT5MmaWarp) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                    "r"(kT5Cols));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -821,7 +841,7 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
     t5_fence_after();
     const uint32_t tb = tmem_base;
 
-    if (warp == 5) {
+    if (warp == kT5MmaWarp) {
       // ---------------------------------------------------------- MMA issuer --
       if (lane == 0) {
         const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
@@ -872,6 +892,8 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
           } else if (*abf || global_ns() - t_last > kWaitLimitNs) {
             *abf = 1;
             break;
+          } else {
+            __nanosleep(64);   // leave issue slots to the other warps of this scheduler
           }
         }
         // every MMA issued has completed before TMEM can be released
@@ -915,6 +937,9 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
           float mx = -INFINITY;
 #pragma unroll
           for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
+          // rows past R hold whatever Q's unused rows produce: they must not
+          // vote for a rescale of the warp
+          if (!live) mx = -INFINITY;
           // the reference moves only when a tile exceeds it by more than 8
           const bool up = mx > m_ref + 8.f;
           float a = 1.f;
@@ -1028,7 +1053,8 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
   t5_fence_before();
   __syncthreads();
   t5_fence_after();
-  if (warp == 5) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kT5Cols));
+  if (warp == kT5MmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kT5Cols));
 }
 
 // ----------------------------------------------------- CUDA-core kernel ---
