@@ -172,6 +172,8 @@ struct TcCfg {
 template <int RT, bool FP8>
 __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMinBlocks)
     attn_tc_kernel(const __grid_constant__ TcParams P) {
+  pdl_wait();
+  pdl_trigger();
   using Cfg = TcCfg<RT, FP8>;
   constexpr bool F16 = FP8;   // fp8 tiles are widened to f16; bf16 stays bf16
   extern __shared__ uint8_t smem_raw[];
@@ -713,6 +715,8 @@ __device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile 
 
 template <int QR>
 __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
+  pdl_wait();
+  pdl_trigger();
   using Cfg = T5Cfg<QR>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
   constexpr int kQHalf = QR * 128;   // bytes of one head-dim half of Q
@@ -1094,6 +1098,8 @@ __device__ __forceinline__ float kv_value<uint8_t>(const void *pool, int64_t off
 
 template <typename TKV, typename TQ>
 __global__ void __launch_bounds__(kGenThreads) attn_generic_kernel(const __grid_constant__ GenParams P) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float gsm[];
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1217,6 +1223,8 @@ struct MergeParams {
 // shared memory by the row's first warp.
 template <typename TO, int WPR>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams P) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kMaxChunks = 2;   // d <= 256
   __shared__ float4 xs_acc[8][kMaxChunks][32];
   __shared__ float xs_ml[8][2];
@@ -1319,10 +1327,10 @@ void launch_merge(const MergeParams &M, int64_t rows, cudaStream_t st) {
   const int wpr = M.S >= 64 ? 8 : (M.S >= 16 ? 4 : (M.S >= 8 ? 2 : 1));
   const unsigned nb = (unsigned)((rows * wpr + 7) / 8);
   switch (wpr) {
-    case 8: attn_merge_kernel<TO, 8><<<nb, 256, 0, st>>>(M); break;
-    case 4: attn_merge_kernel<TO, 4><<<nb, 256, 0, st>>>(M); break;
-    case 2: attn_merge_kernel<TO, 2><<<nb, 256, 0, st>>>(M); break;
-    default: attn_merge_kernel<TO, 1><<<nb, 256, 0, st>>>(M); break;
+    case 8: launch_k(attn_merge_kernel<TO, 8>, dim3(nb), dim3(256), 0, st, 1, M); break;
+    case 4: launch_k(attn_merge_kernel<TO, 4>, dim3(nb), dim3(256), 0, st, 1, M); break;
+    case 2: launch_k(attn_merge_kernel<TO, 2>, dim3(nb), dim3(256), 0, st, 1, M); break;
+    default: launch_k(attn_merge_kernel<TO, 1>, dim3(nb), dim3(256), 0, st, 1, M); break;
   }
 }
 
@@ -1416,7 +1424,7 @@ sv_status launch_tc(const TcParams &P, cudaStream_t st) {
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   dim3 grid(P.S, P.H_kv, P.B);
-  attn_tc_kernel<RT, FP8><<<grid, Cfg::kThreads, Cfg::kSmem, st>>>(P);
+  launch_k(attn_tc_kernel<RT, FP8>, grid, dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
   return check_launch("spec_verify_attn tensor-core launch");
 }
 
@@ -1430,7 +1438,7 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   dim3 grid(P.S, P.H_kv, P.B);
-  attn_tc5_kernel<QR><<<grid, kT5Threads, T5Cfg<QR>::kSmem, st>>>(P);
+  launch_k(attn_tc5_kernel<QR>, grid, dim3(kT5Threads), T5Cfg<QR>::kSmem, st, 1, P);
   return check_launch("spec_verify_attn tcgen05 launch");
 }
 
@@ -1442,7 +1450,7 @@ sv_status launch_gen(const GenParams &P, cudaStream_t st) {
                                        (int)smem);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
   dim3 grid(P.S, P.H_kv, P.B);
-  attn_generic_kernel<TKV, TQ><<<grid, kGenThreads, smem, st>>>(P);
+  launch_k(attn_generic_kernel<TKV, TQ>, grid, dim3(kGenThreads), smem, st, 1, P);
   return check_launch("spec_verify_attn fp32 launch");
 }
 

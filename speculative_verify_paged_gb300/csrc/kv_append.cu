@@ -35,6 +35,8 @@ __device__ __forceinline__ void store_elem(void *cache, int64_t off, TIn x_in, f
 // One CTA per (new position j, sequence b); threads stride over H_kv * d.
 template <typename TIn, int KV>
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int j = blockIdx.x, b = blockIdx.y;
   const int L = a.seq_lens[b];
   if (L < a.n_new || L > a.max_blocks * a.bs) {
@@ -70,9 +72,9 @@ template <typename TIn>
 sv_status launch_in(const AppendArgs &a, sv_dtype kv_dtype, int B, cudaStream_t s) {
   dim3 grid(a.n_new, B);
   switch (kv_dtype) {
-    case SV_F32: kv_append_kernel<TIn, SV_F32><<<grid, 256, 0, s>>>(a); break;
-    case SV_BF16: kv_append_kernel<TIn, SV_BF16><<<grid, 256, 0, s>>>(a); break;
-    case SV_FP8_E4M3: kv_append_kernel<TIn, SV_FP8_E4M3><<<grid, 256, 0, s>>>(a); break;
+    case SV_F32: launch_k(kv_append_kernel<TIn, SV_F32>, grid, dim3(256), 0, s, 1, a); break;
+    case SV_BF16: launch_k(kv_append_kernel<TIn, SV_BF16>, grid, dim3(256), 0, s, 1, a); break;
+    case SV_FP8_E4M3: launch_k(kv_append_kernel<TIn, SV_FP8_E4M3>, grid, dim3(256), 0, s, 1, a); break;
     default: return fail(SV_ERR_UNSUPPORTED, "kv_block_append: unsupported kv_dtype %d", kv_dtype);
   }
   return check_launch("kv_block_append launch");

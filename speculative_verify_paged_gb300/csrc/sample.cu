@@ -270,7 +270,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return r;
 }
 
-constexpr int kMaxSteps = 32;   // 32-group steps per warp range
 
 // warp maximum on the reduction unit (NaN inputs are ignored, like fmaxf)
 __device__ __forceinline__ float warp_max_redux(float v) {
@@ -380,6 +379,8 @@ struct RowShared {
 // lane totals locates the crossing of v Z, and one group rescan finds y.
 template <typename TT, int DK>
 __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_constant__ SampleParams P) {
+  pdl_wait();
+  pdl_trigger();
   using TD = typename std::conditional<DK == 0, TT, float>::type;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RowShared sh;
@@ -761,8 +762,8 @@ __device__ __forceinline__ ff ff_norm(ff a) { return quick_two_sum(a.hi, a.lo); 
 
 struct ExactShared {
   ff red[32];
-  ff wsum[kResWarps];
-  ff stepsum[kResWarps][kMaxSteps];
+  ff wsum[kResWarps];    // per-warp weight totals
+  ff wincl[kResWarps];   // their inclusive prefix
   ff pub_sp, pub_sq, pub_tot;
   int pub_y, pub_last;
   float2 tbl[64];
@@ -846,54 +847,53 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
       }
     }
   };
-  const int gpw = (n_grp + kResWarps - 1) / kResWarps;
+  // Each warp owns groups [g_lo, g_hi); lane l owns the run [r_lo, r_hi) of
+  // them, so one warp scan of the lane totals and one scan of the warp
+  // totals give every run its offset; the owner of v Z is found by ballots.
+  const int nw = (int)(blockDim.x >> 5);
+  const int gpw = (n_grp + nw - 1) / nw;
   const int g_lo = min(n_grp, warp * gpw), g_hi = min(n_grp, g_lo + gpw);
+  const int G = (gpw + 31) >> 5;
+  const int r_lo = min(g_hi, g_lo + lane * G), r_hi = min(g_hi, r_lo + G);
   int y = -1;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    ff wrun{0.f, 0.f};
+    ff t_l{0.f, 0.f};
     int last_pos = -1;
-    for (int s0 = g_lo, sidx = 0; s0 < g_hi; s0 += 32, ++sidx) {
-      const int g = s0 + lane;
-      ff gs{0.f, 0.f};
-      if (g < g_hi) {
-        ff w[8];
-        wx8(g, w);
+    for (int g = r_lo; g < r_hi; ++g) {
+      ff w[8];
+      wx8(g, w);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          acc_add(gs, w[j]);
-          if (w[j].hi > 0.f) last_pos = e0 + 8 * g + j;
-        }
+      for (int j = 0; j < 8; ++j) {
+        acc_add(t_l, w[j]);
+        if (w[j].hi > 0.f) last_pos = e0 + 8 * g + j;
       }
-      gs = ff_norm(gs);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) gs = ff_add(gs, ff{__shfl_xor_sync(0xffffffffu, gs.hi, o),
-                                                         __shfl_xor_sync(0xffffffffu, gs.lo, o)});
-      if (lane == 0) sh.stepsum[warp][sidx] = gs;
-      wrun = ff_add(wrun, gs);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
-    if (lane == 0) {
-      sh.wsum[warp] = wrun;
-      if (last_pos >= 0) atomicMax(&sh.pub_last, last_pos);
+    t_l = ff_norm(t_l);
+    const ff incl = scan32_ff(t_l, lane);
+    last_pos = warp_max_s32(last_pos);
+    if (lane == 31) sh.wsum[warp] = incl;
+    if (lane == 0 && last_pos >= 0) atomicMax(&sh.pub_last, last_pos);
+    __syncthreads();
+    if (warp == 0) {
+      // inclusive prefix of the warp totals; the CTA total is published
+      const ff wi = scan32_ff(lane < nw ? sh.wsum[lane] : ff{0.f, 0.f}, lane);
+      if (lane < nw) sh.wincl[lane] = wi;
+      if (lane == nw - 1) sh.pub_tot = wi;
     }
     __syncthreads();
-    ff tot{0.f, 0.f};
-    for (int w = 0; w < kResWarps; ++w) tot = ff_add(tot, sh.wsum[w]);
-    if (tid == 0) sh.pub_tot = tot;
     cluster_sync();   // totals published
-    // CTA r owns [sum of totals before r, + its total): a sequential prefix
-    // in rank order, the same in every CTA
+    // CTA r owns [sum of the totals before r, + its total): a sequential
+    // prefix in rank order, the same in every CTA
     const ff t_r = lane < cs ? ld_dsmem_ff(&sh.pub_tot, lane) : ff{0.f, 0.f};
     const int last_all = warp_max_s32(lane < cs ? ld_dsmem_s32(mapa(&sh.pub_last, lane)) : -1);
     cluster_sync();   // peers have read the totals
+    if (tid == 0) sh.pub_last = -1;
     ff xoff{0.f, 0.f}, XZ{0.f, 0.f};
     for (int r = 0; r < cs; ++r) {
       const ff t{__shfl_sync(0xffffffffu, t_r.hi, r), __shfl_sync(0xffffffffu, t_r.lo, r)};
       if (r == rank) xoff = XZ;
       XZ = ff_add(XZ, t);
     }
-    if (tid == 0) sh.pub_last = -1;
     if (!ff_pos(XZ)) {   // zero residual mass: draw from p_n instead
       __syncthreads();
       if (mode == 0) break;
@@ -901,43 +901,38 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
       continue;
     }
     const ff xthr = ff_mul(ff{v_u, 0.f}, XZ);
+    const ff tot{__shfl_sync(0xffffffffu, t_r.hi, rank), __shfl_sync(0xffffffffu, t_r.lo, rank)};
     if (!ff_gt(xoff, xthr) && ff_gt(ff_add(xoff, tot), xthr)) {
-      ff woff{0.f, 0.f}, a_w = xoff;
-      int owner = kResWarps - 1;
-      for (int w = 0; w < kResWarps; ++w) {
-        const ff nxt = ff_add(woff, sh.wsum[w]);
-        if (ff_gt(ff_add(xoff, nxt), xthr) || w == kResWarps - 1) {
-          owner = w;
-          a_w = ff_add(xoff, woff);
-          break;
-        }
-        woff = nxt;
-      }
+      // the first warp whose inclusive total passes v Z (the last one if
+      // rounding leaves none)
+      const bool past = lane < nw && ff_gt(ff_add(xoff, sh.wincl[lane]), xthr);
+      const unsigned wb = __ballot_sync(0xffffffffu, past);
+      const int owner = wb ? __ffs(wb) - 1 : nw - 1;
       if (warp == owner) {
-        const int nsteps = (g_hi - g_lo + 31) / 32;
-        ff base = a_w;
-        int sel = nsteps - 1;
-        for (int sidx = 0; sidx < nsteps; ++sidx) {
-          const ff nxt = ff_add(base, sh.stepsum[warp][sidx]);
-          if (ff_gt(nxt, xthr) || sidx == nsteps - 1) { sel = sidx; break; }
-          base = nxt;
-        }
+        const ff base = owner > 0 ? ff_add(xoff, sh.wincl[owner - 1]) : xoff;
+        const unsigned lb = __ballot_sync(0xffffffffu, ff_gt(ff_add(base, incl), xthr));
+        const int L = lb ? __ffs(lb) - 1 : 31;
+        const ff excl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+        ff start = ff_add(base, lane == 0 ? ff{0.f, 0.f} : excl);
+        start = ff{__shfl_sync(0xffffffffu, start.hi, L), __shfl_sync(0xffffffffu, start.lo, L)};
+        const int L_lo = __shfl_sync(0xffffffffu, r_lo, L), L_hi = __shfl_sync(0xffffffffu, r_hi, L);
+        // the run's groups, one per lane, in ascending order
         int found = -1, last_p = -1;
-        if (nsteps > 0) {
-          const int g = g_lo + sel * 32 + lane;
+        for (int g0 = L_lo; g0 < L_hi && found < 0; g0 += 32) {
+          const int g = g0 + lane;
           ff w[8];
           ff gs{0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < 8; ++j) w[j] = ff{0.f, 0.f};
-          if (g < g_hi) {
+          if (g < L_hi) {
             wx8(g, w);
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc_add(gs, w[j]);
           }
           gs = ff_norm(gs);
-          const ff incl = scan32_ff(gs, lane);
+          const ff inc2 = scan32_ff(gs, lane);
           int cand = -1;
-          ff run_c = ff_add(base, ff_add(incl, ff_neg(gs)));
+          ff run_c = ff_add(start, ff_add(inc2, ff_neg(gs)));
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const ff nxt = ff_add(run_c, w[j]);
@@ -947,10 +942,10 @@ __device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
           }
           const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
           if (hit) found = __shfl_sync(0xffffffffu, cand, __ffs(hit) - 1);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) last_p = max(last_p, __shfl_xor_sync(0xffffffffu, last_p, o));
+          start = ff_add(start, ff{__shfl_sync(0xffffffffu, inc2.hi, 31), __shfl_sync(0xffffffffu, inc2.lo, 31)});
         }
-        if (found < 0) found = last_p;   // crossing within rounding of the step end
+        last_p = warp_max_s32(last_p);
+        if (found < 0) found = last_p;   // crossing within rounding of the run's end
         if (lane == 0) sh.pub_y = found;
       }
     }
@@ -978,6 +973,8 @@ constexpr int kFinishMaxSeq = kResThreads;   // sequences per walk round
 
 template <typename TT, int DK>
 __global__ void __launch_bounds__(kResThreads) sample_finish_kernel(const __grid_constant__ SampleParams P) {
+  pdl_wait();
+  pdl_trigger();
   using TD = typename std::conditional<DK == 0, TT, float>::type;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ExactShared sh;
@@ -1156,23 +1153,6 @@ void split_ff(double d, float &hi, float &lo) {
   lo = (float)(d - (double)hi);
 }
 
-template <typename KernelT>
-cudaError_t launch_cluster(KernelT kernel, dim3 grid, int threads, size_t smem, int cs, cudaStream_t s,
-                           const SampleParams &P) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, P);
-}
 
 template <typename TT, int DK>
 sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, size_t smem_x, cudaStream_t s) {
@@ -1190,10 +1170,10 @@ sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, si
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_sample: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  cudaError_t e = launch_cluster(sample_rows_kernel<TT, DK>, dim3(cs, P.K + 1, P.B), kRowThreads, smem, cs, s, P);
+  cudaError_t e = launch_k(sample_rows_kernel<TT, DK>, dim3(cs, P.K + 1, P.B), dim3(kRowThreads), smem, s, cs, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample rows launch: %s", cudaGetErrorString(e));
   const int ncl = std::max(1, std::min(P.B, kFinishClusters));
-  e = launch_cluster(sample_finish_kernel<TT, DK>, dim3(cs_x * ncl), kResThreads, smem_x, cs_x, s, P);
+  e = launch_k(sample_finish_kernel<TT, DK>, dim3(cs_x * ncl), dim3(kResThreads), smem_x, s, cs_x, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -1259,11 +1239,6 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
     const size_t sm = slice_smem(16, n);
     if (sm <= kMaxSliceSmem) { cs = 16; ns = n; smem = sm; }
   }
-  // per-warp ranges of 32-group steps must fit the step tables
-  auto steps_ok = [&](int n_elems, int warps) {
-    const int grp = (n_elems + 7) / 8, gpw = (grp + warps - 1) / warps;
-    return (gpw + 31) / 32 <= kMaxSteps;
-  };
   // finish kernel: 16-CTA clusters (8 for small vocabularies)
   const int cs_x = V >= 65536 ? 16 : 8;
   int ns_x = 0;
@@ -1272,7 +1247,7 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   const size_t cache_bytes = (size_t)ns_x * sizeof(ff) * ((draft_is_probs && K > 0) ? 1 : 2);
   const bool cache_x = smem_x + cache_bytes <= kMaxSliceSmem;
   if (cache_x) smem_x += cache_bytes;
-  if (cs && (!steps_ok(ns_x, kResWarps) || smem_x > kMaxSliceSmem)) cs = 0;
+  if (cs && smem_x > kMaxSliceSmem) cs = 0;
   if (!cs) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large", V);
 
   SampleParams P = {};
