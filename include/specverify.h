@@ -231,10 +231,12 @@ sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
  *   cannot allocate device memory when they verify a round (an engine that
  *   reserves all GPU memory for its KV pool at start-up and forbids later
  *   allocations, or a caller whose fixed interface cannot pass a workspace).
- *   Same as spec_verify_sample without the workspace arguments: the per-row
- *   records go to a 1 MiB static device array inside the library, which every
- *   GPU that loads the library holds until the process exits. Supports
- *   B * (K+1) <= 21845; larger sizes return SV_ERR_UNSUPPORTED with a message.
+ *   Same as spec_verify_sample without the workspace arguments: the
+ *   workspace (a 48-byte record and 16 * ceil(V / 8192) bytes of chunk
+ *   statistics per (sequence, position)) goes to a 1 MiB static device array
+ *   inside the library, which every GPU that loads the library holds until
+ *   the process exits. For V = 128256 that is B * (K+1) <= 3449; larger
+ *   sizes return SV_ERR_UNSUPPORTED with a message.
  *   Allocates nothing (no cudaMalloc / cudaFree or allocating library call).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.

@@ -7,23 +7,26 @@
 // rejection n the token is drawn by inverse CDF (ascending token id, strict
 // '>') from max(0, p_n - q_n); if all K are accepted it is drawn from p_K.
 //
-// GB300 design:
-//   * sample_rows_kernel: one thread-block cluster per (sequence, position)
-//     row. Each CTA of the cluster pulls its slice of the target row and of
-//     the draft row into shared memory with 1-D bulk (TMA) copies, so every
-//     logit crosses HBM once. One online pass gives each CTA its (max, sum of
-//     exp) pair; pairs are combined across the cluster through distributed
-//     shared memory. The accept test and a speculative "if rejected here"
-//     inverse-CDF draw (the bonus draw for row K) are evaluated in fp32,
-//     each with a certificate that it lies outside its rounding bound. The
-//     result is one 48-byte record per row.
+// GB300 design (three launches, no host round trip):
+//   * sample_stats_kernel: a streaming reduction. One CTA per (8192-logit
+//     chunk, position, sequence) loads its chunk of the target row and of
+//     the draft row with 16-byte loads straight into registers, takes exact
+//     maxima and fp32 sums of exponentials (target and draft paired in
+//     packed fp32 arithmetic) and writes one (max, sum) pair per row; every
+//     logit crosses HBM once.
+//   * sample_draw_kernel: one cluster per sequence combines the chunk
+//     statistics, evaluates every accept test in fp32 with a certificate
+//     that it lies outside its rounding bound, and finds the position whose
+//     draw is used (the first certified rejection, or the bonus row). Only
+//     that row is read again; its residual weights are formed over the
+//     cluster's shared-memory slices and the inverse-CDF draw gets its own
+//     certificate. One 48-byte record per (sequence, position) results.
 //   * sample_finish_kernel: a few clusters walk each sequence's records in
-//     order, stop at the first rejection and write the emitted tokens; no
-//     host round-trip between positions. The rare decision that is not
-//     certified (a few percent of sequences) is re-evaluated from that row's
-//     logits in float-float arithmetic (~1e-9 relative error per term), so
-//     emitted tokens are those of exact arithmetic except for uniforms within
-//     ~1e-10 of a boundary.
+//     order, stop at the first rejection and write the emitted tokens. The
+//     rare decision that is not certified (a few percent of sequences) is
+//     re-evaluated from that row's logits in float-float arithmetic (~1e-9
+//     relative error per term), so emitted tokens are those of exact
+//     arithmetic except for uniforms within ~1e-10 of a boundary.
 #include <cmath>
 #include <algorithm>
 #include <mutex>
@@ -73,9 +76,11 @@ struct SampleParams {
   int32_t *out_tokens;
   int32_t *num_acc;
   RowRec *recs;
+  float4 *part;  // [B][K+1][nc] (max, sum) of the target and draft chunks
   int32_t *status;
   int B, K, V;
-  int ns;        // elements per CTA slice (multiple of 8)
+  int nc;        // statistics chunks per row
+  int ns;        // elements per CTA slice of the draw kernel (multiple of 8)
   int ns_x;      // elements per CTA slice in the finish kernel
   int aligned;   // rows are 16-byte aligned: bulk copies usable
   int cache_x;   // finish kernel keeps the float-float exponentials in shared memory
@@ -358,114 +363,143 @@ __device__ __forceinline__ void warp_ms(float &m, float &s, float c) {
   m = mx;
 }
 
-struct RowShared {
-  uint64_t bars[2];
-  float red_m[kRowWarps], red_s[kRowWarps], red_m2[kRowWarps], red_s2[kRowWarps];
-  float pub_mp, pub_sp, pub_mq, pub_sq;   // this CTA's (max, sum) pairs
-  float pub_lp, pub_lq;                   // logits at the draft token (its owner CTA)
-  float pub_tot;                          // this CTA's draw mass
-  float wsum[kRowWarps];
-};
+// ------------------------------------------------------ statistics pass ---
+// sample_stats_kernel: one CTA per (8192-logit chunk, position, sequence).
+// Each thread holds 32 logits of the target row and of the draft row in
+// registers (16-byte loads, all issued before any arithmetic), takes exact
+// maxima, then sums of 2^(l c - fl(m c)) with the two rows paired in packed
+// fp32 arithmetic; the CTA's (max, sum) pairs go to the workspace. No
+// shared-memory staging and no cluster: a streaming reduction.
+constexpr int kStatThreads = 256;
+constexpr int kStatChunk = 8192;                               // logits per CTA per row
+constexpr int kStatGroups = kStatChunk / (8 * kStatThreads);   // groups of 8 per thread
 
-// One cluster per (sequence, position) row; fp32 fast path only. Writes the
-// row's record: stats, accept test, speculative draw and their certificates.
-//
-// Pass A: exact thread-local maxima, then sums of 2^(l c - fl(m c)) with the
-// target and draft rows paired in packed fp32 arithmetic; (max, sum) pairs
-// are combined across warps and across the cluster.
-// Pass B (only when the draw can be used: the bonus row, or a certified
-// rejection): weights w'(y) = max(0, e_p(y) - r e_q(y)) against the row
-// maxima; each lane owns a contiguous run of groups, so one warp scan of the
-// lane totals locates the crossing of v Z, and one group rescan finds y.
+// raw bits of 8 logits: one 16-byte word for 16-bit types, two for f32
+template <typename T> struct Raw8 { uint4 w[sizeof(T) / 2]; };
+
+template <typename T>
+__device__ __forceinline__ uint32_t neg_inf_bits();
+template <> __device__ __forceinline__ uint32_t neg_inf_bits<float>() { return 0xff800000u; }
+template <> __device__ __forceinline__ uint32_t neg_inf_bits<__nv_bfloat16>() { return 0xff80ff80u; }
+template <> __device__ __forceinline__ uint32_t neg_inf_bits<__half>() { return 0xfc00fc00u; }
+
+// group g (elements 8g .. 8g+7) of a row; elements at or past e1 read as -inf
+// (as 0 for given probabilities: pad_zero)
+template <typename T>
+__device__ __forceinline__ Raw8<T> raw_load(const T *row, int g, int e1, bool vec, bool pad_zero) {
+  Raw8<T> r;
+  if (vec && 8 * g + 8 <= e1) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(row + 8 * g);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(T) / 2); ++k) r.w[k] = __ldg(p + k);
+    return r;
+  }
+  T v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = 8 * g + j;
+    if (e < e1) {
+      v[j] = row[e];
+    } else {
+      const uint32_t bits = pad_zero ? 0u : neg_inf_bits<T>();
+      memcpy(&v[j], &bits, sizeof(T));
+    }
+  }
+  memcpy(&r, v, sizeof(v));
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const Raw8<T> &r, float (&x)[8]) {
+  if constexpr (std::is_same<T, float>::value) {
+    x[0] = __uint_as_float(r.w[0].x); x[1] = __uint_as_float(r.w[0].y);
+    x[2] = __uint_as_float(r.w[0].z); x[3] = __uint_as_float(r.w[0].w);
+    x[4] = __uint_as_float(r.w[1].x); x[5] = __uint_as_float(r.w[1].y);
+    x[6] = __uint_as_float(r.w[1].z); x[7] = __uint_as_float(r.w[1].w);
+  } else {
+    const uint32_t w[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      } else {
+        const float2 f = __half22float2(as_h2<__half2>(w[k]));
+        x[2 * k] = f.x;
+        x[2 * k + 1] = f.y;
+      }
+    }
+  }
+}
+
+// exact maximum of 8 logits (a selection: the packed 16-bit forms are exact)
+template <typename T>
+__device__ __forceinline__ float max8(const Raw8<T> &r) {
+  if constexpr (std::is_same<T, float>::value) {
+    float x[8];
+    unpack8(r, x);
+    return fmaxf(max3f(x[0], x[1], x[2]), max3f(max3f(x[3], x[4], x[5]), x[6], x[7]));
+  } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    const __nv_bfloat162 a = __hmax2(as_h2<__nv_bfloat162>(r.w[0].x), as_h2<__nv_bfloat162>(r.w[0].y));
+    const __nv_bfloat162 bb = __hmax2(as_h2<__nv_bfloat162>(r.w[0].z), as_h2<__nv_bfloat162>(r.w[0].w));
+    const __nv_bfloat162 m = __hmax2(a, bb);
+    return fmaxf(__low2float(m), __high2float(m));
+  } else {
+    const __half2 a = __hmax2(as_h2<__half2>(r.w[0].x), as_h2<__half2>(r.w[0].y));
+    const __half2 bb = __hmax2(as_h2<__half2>(r.w[0].z), as_h2<__half2>(r.w[0].w));
+    const __half2 m = __hmax2(a, bb);
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+}
+
 template <typename TT, int DK>
-__global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_constant__ SampleParams P) {
+__global__ void __launch_bounds__(kStatThreads) sample_stats_kernel(const __grid_constant__ SampleParams P) {
   pdl_wait();
   pdl_trigger();
   using TD = typename std::conditional<DK == 0, TT, float>::type;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ RowShared sh;
-
-  const int cs = gridDim.x;
-  const int rank = (int)cluster_ctarank();
-  const int i = blockIdx.y, b = blockIdx.z;
+  __shared__ float red[4][kStatThreads / 32];
+  const int c = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
   const int K = P.K, V = P.V;
-  const bool has_draft = i < K;
-  const bool q_logits = has_draft && DK == 0;
+  const bool q_logits = i < K && DK == 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float c = P.c;
-  const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
-
+  const float cl = P.c;
   const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
-  const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
-  const int e0 = rank * P.ns;
-  const int n_loc = max(0, min(V, e0 + P.ns) - e0);
-  const int n_grp = (n_loc + 7) >> 3;
-  TT *st = reinterpret_cast<TT *>(smem);
-  TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)P.ns * sizeof(TT), 128));
+  const TD *drow = q_logits ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
+  const int e0 = c * kStatChunk, e1 = min(V, e0 + kStatChunk);
+  const int g0 = e0 / 8, g1 = (e1 + 7) / 8;
+  const bool vec = P.aligned != 0;
 
-  // ---- stage the slice into shared memory --------------------------------
-  // target slice completes on bars[0], draft slice on bars[1]; each is cut
-  // into 16 KB bulk copies
-  const uint32_t nb_t = (uint32_t)n_loc * sizeof(TT);
-  const uint32_t nb_d = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
-  for (int e = n_loc + tid; e < n_grp * 8; e += kRowThreads) {   // pad the last group
-    st[e] = pad_value<TT>(false);
-    if (has_draft) sd[e] = pad_value<TD>(DK == 1);
-  }
-  if (P.aligned) {
-    if (tid == 0) {
-      mbar_init(&sh.bars[0], 1);
-      mbar_init(&sh.bars[1], 1);
-      fence_mbarrier_init();
-      const uint8_t *gt = reinterpret_cast<const uint8_t *>(trow + e0);
-      mbar_arrive_expect_tx(&sh.bars[0], nb_t);
-      for (uint32_t off = 0; off < nb_t; off += kChunkBytes)
-        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, min(kChunkBytes, nb_t - off), &sh.bars[0]);
-      if (has_draft) {
-        const uint8_t *gd = reinterpret_cast<const uint8_t *>(drow + e0);
-        mbar_arrive_expect_tx(&sh.bars[1], nb_d);
-        for (uint32_t off = 0; off < nb_d; off += kChunkBytes)
-          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, min(kChunkBytes, nb_d - off), &sh.bars[1]);
-      }
-    }
-    __syncthreads();   // barriers initialised before anyone waits on them
-  } else {
-    for (int e = tid; e < n_loc; e += kRowThreads) {
-      st[e] = trow[e0 + e];
-      if (has_draft) sd[e] = drow[e0 + e];
-    }
-    __syncthreads();
-  }
-  int x_tok = 0;
-  if (has_draft) {
-    x_tok = P.tokens[(int64_t)b * K + i];
-    if (x_tok < 0 || x_tok >= V) {
-      if (rank == 0 && tid == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
-      x_tok = min(max(x_tok, 0), V - 1);
+  Raw8<TT> rt[kStatGroups];
+  Raw8<TD> rd[kStatGroups];
+#pragma unroll
+  for (int k = 0; k < kStatGroups; ++k) {
+    const int g = g0 + tid + k * kStatThreads;
+    if (g < g1) {
+      rt[k] = raw_load(trow, g, e1, vec, false);
+      if (q_logits) rd[k] = raw_load(drow, g, e1, vec, false);
     }
   }
-  const float *uv = P.uniforms + ((int64_t)b * (K + 1) + i) * 2;
-  const float u = uv[0], v_u = uv[1];
-
-  // ---- pass A: thread maxima, then paired sums ---------------------------
-  bool timed_out = false;
-  if (P.aligned && n_loc > 0) {
-    if (!mbar_wait(&sh.bars[0], 0)) timed_out = true;
-    if (has_draft && !timed_out && !mbar_wait(&sh.bars[1], 0)) timed_out = true;
+  float mt = -INFINITY, md = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kStatGroups; ++k) {
+    if (g0 + tid + k * kStatThreads < g1) {
+      mt = fmaxf(mt, max8(rt[k]));
+      if (q_logits) md = fmaxf(md, max8(rd[k]));
+    }
   }
-  if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-  float mt = slice_max(st, tid, n_grp, kRowThreads);
-  float md = q_logits ? slice_max(sd, tid, n_grp, kRowThreads) : -INFINITY;
   float s_t = 0.f, s_d = 0.f;
   {
-    const float2 cc = make_float2(c, c);
-    if (q_logits) {
-      const float2 nm = make_float2(neg_ref(mt, c), neg_ref(md, c));
-      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-      for (int g = tid; g < n_grp; g += kRowThreads) {
-        float xt[8], xd[8];
-        load8(st, g, xt);
-        load8(sd, g, xd);
+    const float2 cc = make_float2(cl, cl);
+    const float2 nm = make_float2(neg_ref(mt, cl), neg_ref(md, cl));
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+    for (int k = 0; k < kStatGroups; ++k) {
+      if (g0 + tid + k * kStatThreads >= g1) continue;
+      float xt[8];
+      unpack8(rt[k], xt);
+      if (q_logits) {
+        float xd[8];
+        unpack8(rd[k], xd);
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
           const float2 y0 = __ffma2_rn(make_float2(xt[j], xd[j]), cc, nm);
@@ -473,106 +507,213 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
           a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
           a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
         }
-      }
-      s_t = a0.x + a1.x;
-      s_d = a0.y + a1.y;
-    } else {
-      const float nr = neg_ref(mt, c);
-      const float2 nm = make_float2(nr, nr);
-      float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-      for (int g = tid; g < n_grp; g += kRowThreads) {
-        float xt[8];
-        load8(st, g, xt);
+      } else {
+        const float2 nt = make_float2(nm.x, nm.x);
 #pragma unroll
         for (int j = 0; j < 8; j += 4) {
-          const float2 y0 = __ffma2_rn(make_float2(xt[j], xt[j + 1]), cc, nm);
-          const float2 y1 = __ffma2_rn(make_float2(xt[j + 2], xt[j + 3]), cc, nm);
+          const float2 y0 = __ffma2_rn(make_float2(xt[j], xt[j + 1]), cc, nt);
+          const float2 y1 = __ffma2_rn(make_float2(xt[j + 2], xt[j + 3]), cc, nt);
           a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
           a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
         }
       }
+    }
+    if (q_logits) {
+      s_t = a0.x + a1.x;
+      s_d = a0.y + a1.y;
+    } else {
       s_t = (a0.x + a0.y) + (a1.x + a1.y);
     }
   }
-  warp_ms(mt, s_t, c);
-  if (q_logits) warp_ms(md, s_d, c);
-  if (lane == 0) { sh.red_m[warp] = mt; sh.red_s[warp] = s_t; sh.red_m2[warp] = md; sh.red_s2[warp] = s_d; }
+  warp_ms(mt, s_t, cl);
+  if (q_logits) warp_ms(md, s_d, cl);
+  if (lane == 0) { red[0][warp] = mt; red[1][warp] = s_t; red[2][warp] = md; red[3][warp] = s_d; }
   __syncthreads();
-  const int x_rank = x_tok / P.ns;
   if (warp == 0) {
-    float m1 = lane < kRowWarps ? sh.red_m[lane] : -INFINITY, s1 = lane < kRowWarps ? sh.red_s[lane] : 0.f;
-    float m2 = lane < kRowWarps ? sh.red_m2[lane] : -INFINITY, s2 = lane < kRowWarps ? sh.red_s2[lane] : 0.f;
-    warp_ms(m1, s1, c);
-    if (q_logits) warp_ms(m2, s2, c);
+    constexpr int nw = kStatThreads / 32;
+    float m1 = lane < nw ? red[0][lane] : -INFINITY, s1 = lane < nw ? red[1][lane] : 0.f;
+    float m2 = lane < nw ? red[2][lane] : -INFINITY, s2 = lane < nw ? red[3][lane] : 0.f;
+    warp_ms(m1, s1, cl);
+    if (q_logits) warp_ms(m2, s2, cl);
+    if (lane == 0) P.part[((int64_t)b * (K + 1) + i) * P.nc + c] = make_float4(m1, s1, m2, s2);
+  }
+}
+
+// ------------------------------------------------- decide and draw pass ---
+// sample_draw_kernel: one cluster per sequence. Every CTA combines the chunk
+// statistics of each row (lanes over chunks, the same order everywhere, so
+// every CTA holds the same bits) and the accept tests are evaluated in fp32
+// with their rounding certificates; CTA 0 writes every row's record. The
+// first position that rejects (or whose test is not certified) stops the
+// walk; only the row drawn from is read again: the residual of the first
+// certified rejection, or the bonus row when every draft is accepted. Its
+// weights w'(y) = max(0, e_p(y) - r e_q(y)) are formed over the cluster's
+// slices, one warp scan of lane totals and the cluster's prefix locate v Z,
+// and the draw gets its own certificate. Anything uncertified is left to
+// the finish kernel.
+struct DrawShared {
+  uint64_t bar;
+  int stop;               // 2 * position + (0: not certified, 1: certified rejection)
+  float row_m_p, row_s_p, row_m_q, row_s_q;
+  float pub_tot;          // this CTA's draw mass
+  float wsum[kRowWarps];
+};
+
+// combined (max, sum) of target (and draft) row i of sequence b: every lane
+// of the warp ends with the same bits
+__device__ __forceinline__ void row_stats(const SampleParams &P, int b, int i, bool q_logits, float &m_p, float &S_p,
+                                          float &m_q, float &S_q) {
+  const int lane = threadIdx.x & 31;
+  const float4 *pr = P.part + ((int64_t)b * (P.K + 1) + i) * P.nc;
+  m_p = -INFINITY; S_p = 0.f; m_q = -INFINITY; S_q = 0.f;
+  for (int c0 = 0; c0 < P.nc; c0 += 32) {
+    float a = -INFINITY, sa = 0.f, d = -INFINITY, sd = 0.f;
+    if (c0 + lane < P.nc) {
+      const float4 v = pr[c0 + lane];
+      a = v.x; sa = v.y; d = v.z; sd = v.w;
+    }
+    warp_ms(a, sa, P.c);
+    const float mp = fmaxf(m_p, a);
+    S_p = rescale(S_p, m_p, mp, P.c) + rescale(sa, a, mp, P.c);
+    m_p = mp;
+    if (q_logits) {
+      warp_ms(d, sd, P.c);
+      const float mq = fmaxf(m_q, d);
+      S_q = rescale(S_q, m_q, mq, P.c) + rescale(sd, d, mq, P.c);
+      m_q = mq;
+    }
+  }
+}
+
+template <typename TT, int DK>
+__global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_constant__ SampleParams P) {
+  pdl_wait();
+  pdl_trigger();
+  using TD = typename std::conditional<DK == 0, TT, float>::type;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ DrawShared sh;
+
+  const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+  const int b = blockIdx.y;
+  const int K = P.K, V = P.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float c = P.c;
+  const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
+  if (tid == 0) sh.stop = 2 * K + 1;
+  __syncthreads();
+
+  // ---- accept tests of every draft position --------------------------------
+  for (int i = warp; i < K; i += kRowWarps) {
+    float m_p, S_p, m_q, S_q;
+    row_stats(P, b, i, DK == 0, m_p, S_p, m_q, S_q);
+    if (DK != 0) { m_q = 0.f; S_q = 1.f; }
+    int x = P.tokens[(int64_t)b * K + i];
+    if (x < 0 || x >= V) {
+      if (rank == 0 && lane == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+      x = min(max(x, 0), V - 1);
+    }
+    const float lp_x = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + i) * V + x]);
+    const float lq_x = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + i) * V + x]);
+    const float u = P.uniforms[((int64_t)b * (K + 1) + i) * 2];
+    const bool finite = fabsf(m_p) <= 3.0e38f && (DK != 0 || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
+    const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
+    const float p_x = ex2(fmaf(lp_x, c, -mcp)) / S_p;
+    const float q_x = DK == 0 ? ex2(fmaf(lq_x, c, -mcq)) / S_q : lq_x;
+    const float lhs = u * q_x;
+    const bool accept = lhs < p_x;
+    // p_x and u q_x each carry < 2e-6 relative rounding (exp2, argument
+    // rounding, row sums): a decision this far from the boundary is exact
+    const bool acc_cert = fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f && finite;
     if (lane == 0) {
-      sh.pub_mp = m1; sh.pub_sp = s1; sh.pub_mq = m2; sh.pub_sq = s2;
-      if (has_draft && rank == x_rank) {   // the slice holding x_i publishes its logits
-        sh.pub_lp = to_f32(st[x_tok - e0]);
-        sh.pub_lq = to_f32(sd[x_tok - e0]);
+      if (!acc_cert) atomicMin(&sh.stop, 2 * i);
+      else if (!accept) atomicMin(&sh.stop, 2 * i + 1);
+      if (rank == 0) {
+        RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
+        if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
+        rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
+        rec->p_x = p_x; rec->q_x = q_x;
+        rec->y = -1; rec->y_exact = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
+        rec->flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u);
+        if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
+        if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
       }
     }
   }
-  cluster_sync();   // #1: (max, sum) pairs and the draft token's logits published
-  float m_p = -INFINITY, S_p = 0.f, m_q = -INFINITY, S_q = 0.f;
-  if (lane < cs) {
-    m_p = ld_dsmem_f32(mapa(&sh.pub_mp, lane)); S_p = ld_dsmem_f32(mapa(&sh.pub_sp, lane));
-    if (q_logits) { m_q = ld_dsmem_f32(mapa(&sh.pub_mq, lane)); S_q = ld_dsmem_f32(mapa(&sh.pub_sq, lane)); }
+  __syncthreads();
+  const int stop = sh.stop;
+  // the row drawn from: a certified rejection, or the bonus row (K)
+  const bool certain = (stop & 1) != 0;
+  const int n = stop >> 1;
+  const bool has_draft = n < K;
+  const bool q_logits = has_draft && DK == 0;
+  if (warp == 0 && certain) {   // statistics of the row drawn from
+    float m_p, S_p, m_q, S_q;
+    row_stats(P, b, n, q_logits, m_p, S_p, m_q, S_q);
+    if (!q_logits) { m_q = 0.f; S_q = 1.f; }
+    if (lane == 0) { sh.row_m_p = m_p; sh.row_s_p = S_p; sh.row_m_q = m_q; sh.row_s_q = S_q; }
   }
-  float lp_x = 0.f, lq_x = 0.f;
-  if (has_draft) {
-    lp_x = ld_dsmem_f32(mapa(&sh.pub_lp, x_rank));
-    lq_x = ld_dsmem_f32(mapa(&sh.pub_lq, x_rank));
+  if (warp == 1 && rank == 0) {
+    // the bonus row's record (the finish kernel may walk to it)
+    float m_p, S_p, m_q, S_q;
+    row_stats(P, b, K, false, m_p, S_p, m_q, S_q);
+    if (lane == 0) {
+      RowRec *rec = P.recs + (int64_t)b * (K + 1) + K;
+      rec->m_p = m_p; rec->s_p = S_p; rec->m_q = 0.f; rec->s_q = 1.f;
+      rec->p_x = 0.f; rec->q_x = 0.f;
+      rec->y = -1; rec->y_exact = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
+      rec->flags = 0u;
+      if (!(fabsf(m_p) <= 3.0e38f && S_p > 0.f)) atomic_or_status(P.status, SV_DEV_NONFINITE);
+    }
   }
-  warp_ms(m_p, S_p, c);
-  if (q_logits) warp_ms(m_q, S_q, c);
-  else { m_q = 0.f; S_q = 1.f; }
+  __syncthreads();
+  // identical in every CTA of the cluster: no shared memory of a peer is
+  // read on this path
+  if (!certain || force) return;
+  const float m_p = sh.row_m_p, S_p = sh.row_s_p, m_q = sh.row_m_q, S_q = sh.row_s_q;
   const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
-  // e_p(y) = 2^(fl(l(y) c - fl(m_p c))), p = e_p / S_p. The draw works on the
-  // unnormalised weights w'(y) = S_p w(y) = max(0, e_p(y) - r e_q(y)),
-  // r = S_p / S_q (or S_p for given probabilities): the inverse CDF is
-  // invariant to the common scale.
+
+  // ---- the draw: slices of row n -------------------------------------------
+  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + n) * V;
+  const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + n) * V : nullptr;
+  const int e0 = rank * P.ns;
+  const int n_loc = max(0, min(V, e0 + P.ns) - e0);
+  const int n_grp = (n_loc + 7) >> 3;
+  TT *st = reinterpret_cast<TT *>(smem);
+  TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)P.ns * sizeof(TT), 128));
+  for (int e = n_loc + tid; e < n_grp * 8; e += kRowThreads) {   // pad the last group
+    st[e] = pad_value<TT>(false);
+    if (has_draft) sd[e] = pad_value<TD>(DK == 1);
+  }
+  bool timed_out = false;
+  if (P.aligned) {
+    if (tid == 0) {
+      mbar_init(&sh.bar, 1);
+      fence_mbarrier_init();
+      const uint32_t nb_t = (uint32_t)n_loc * sizeof(TT), nb_d = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
+      mbar_arrive_expect_tx(&sh.bar, nb_t + nb_d);
+      const uint8_t *gt = reinterpret_cast<const uint8_t *>(trow + e0);
+      for (uint32_t off = 0; off < nb_t; off += kChunkBytes)
+        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, min(kChunkBytes, nb_t - off), &sh.bar);
+      if (has_draft) {
+        const uint8_t *gd = reinterpret_cast<const uint8_t *>(drow + e0);
+        for (uint32_t off = 0; off < nb_d; off += kChunkBytes)
+          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, min(kChunkBytes, nb_d - off), &sh.bar);
+      }
+    }
+    __syncthreads();   // the barrier is initialised before anyone waits on it
+    if (n_loc > 0 && !mbar_wait(&sh.bar, 0)) timed_out = true;
+  } else {
+    for (int e = tid; e < n_loc; e += kRowThreads) {
+      st[e] = trow[e0 + e];
+      if (has_draft) sd[e] = drow[e0 + e];
+    }
+    __syncthreads();
+  }
+  if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+
   const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
   const float r_pq = q_logits ? S_p / S_q : S_p;
-
-  // ---- accept test in fp32 ------------------------------------------------
-  bool accept = false, acc_cert = true;
-  float p_x = 0.f, q_x = 0.f;
-  if (has_draft) {
-    p_x = ex2(fmaf(lp_x, c, -mcp)) / S_p;
-    q_x = DK == 0 ? ex2(fmaf(lq_x, c, -mcq)) / S_q : lq_x;
-    const float lhs = u * q_x;
-    accept = lhs < p_x;
-    // p_x and u q_x each carry < 2e-6 relative rounding (exp2, argument
-    // rounding, row sums): a decision this far from the boundary is exact
-    acc_cert = fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f && finite;
-  }
-  RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
-  const uint32_t acc_flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u);
-  if (rank == 0 && tid == 0) {
-    if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
-    rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
-    rec->p_x = p_x; rec->q_x = q_x;
-    rec->y_exact = -1;
-    if (has_draft) {
-      if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
-      if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
-    }
-  }
-  // The draw of this row is used only if it is the bonus row or a certified
-  // rejection; an uncertified accept test is redone (with its draw) by the
-  // finish kernel. The decision is identical in every CTA of the cluster.
-  const bool need_draw = finite && !force && (!has_draft || (acc_cert && !accept));
-  if (!need_draw) {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    if (rank == 0 && tid == 0) {
-      rec->y = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
-      rec->flags = acc_flags;
-    }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    return;
-  }
-
-  // ---- pass B: fp32 weights of the speculative draw ----------------------
+  const float v_u = P.uniforms[((int64_t)b * (K + 1) + n) * 2 + 1];
   const float2 cc = make_float2(c, c);
   const float2 nref = make_float2(-mcp, -mcq);
   auto weight8 = [&](int g, float (&w)[8]) {
@@ -583,8 +724,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
       load8(sd, g, xq);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float eq;
-        float ep;
+        float eq, ep;
         if (DK == 0) {
           const float2 y = __ffma2_rn(make_float2(xp[j], xq[j]), cc, nref);
           ep = ex2(y.x);
@@ -641,7 +781,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   float tot_cta = 0.f;
   for (int w = 0; w < kRowWarps; ++w) tot_cta += sh.wsum[w];
   if (tid == 0) sh.pub_tot = tot_cta;
-  cluster_sync();   // #2: masses published
+  cluster_sync();   // masses published
   const float t_r = lane < cs ? ld_dsmem_f32(mapa(&sh.pub_tot, lane)) : 0.f;
   // the last distributed read of this launch is done: arrive now, wait at exit
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -658,13 +798,12 @@ __global__ void __launch_bounds__(kRowThreads) sample_rows_kernel(const __grid_c
   // running sums (~2^-24 per addition)
   const float e_abs = 4.7683716e-07f * S_p * sqrtf(1.f / S_p + (q_logits ? 1.f / S_q : 0.f)) +
                       1.1920929e-07f * (Z + S_p);   // 2^-21, 2^-23
-  const bool draw_ok = Z > 0.f && thr < Z;
+  const bool draw_ok = finite && Z > 0.f && thr < Z;
+  RowRec *rec = P.recs + (int64_t)b * (K + 1) + n;
+  const uint32_t acc_flags = has_draft ? REC_ACC_CERT : 0u;   // a certified rejection (or the bonus row)
   if (rank == 0 && tid == 0) {
     rec->z = Z; rec->e_abs = e_abs;
-    if (!draw_ok) {   // no owner: the finish kernel evaluates the draw exactly
-      rec->y = -1; rec->gap = 0.f;
-      rec->flags = acc_flags;
-    }
+    if (!draw_ok) { rec->y = -1; rec->gap = 0.f; rec->flags = acc_flags; }
   }
   if (draw_ok && off_c <= thr && thr < off_c + tot_cta) {
     float woff = 0.f, base = off_c;
@@ -1148,6 +1287,13 @@ __global__ void __launch_bounds__(kResThreads) sample_finish_kernel(const __grid
 
 size_t records_bytes(int B, int K) { return align_up((size_t)B * (K + 1) * sizeof(RowRec), 256); }
 
+int stat_chunks(int V) { return (V + kStatChunk - 1) / kStatChunk; }
+
+// per-row records, then the chunk statistics
+size_t workspace_bytes_for(int B, int K, int V) {
+  return records_bytes(B, K) + align_up((size_t)B * (K + 1) * stat_chunks(V) * sizeof(float4), 256);
+}
+
 void split_ff(double d, float &hi, float &lo) {
   hi = (float)d;
   lo = (float)(d - (double)hi);
@@ -1160,9 +1306,9 @@ sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, si
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     const int lim = (int)(kMaxSliceSmem + 1024);
-    attr_err = cudaFuncSetAttribute(sample_rows_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(sample_rows_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(sample_finish_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
     if (attr_err == cudaSuccess)
@@ -1170,8 +1316,10 @@ sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, si
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_sample: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  cudaError_t e = launch_k(sample_rows_kernel<TT, DK>, dim3(cs, P.K + 1, P.B), dim3(kRowThreads), smem, s, cs, P);
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample rows launch: %s", cudaGetErrorString(e));
+  cudaError_t e = launch_k(sample_stats_kernel<TT, DK>, dim3(P.nc, P.K + 1, P.B), dim3(kStatThreads), 0, s, 1, P);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample statistics launch: %s", cudaGetErrorString(e));
+  e = launch_k(sample_draw_kernel<TT, DK>, dim3(cs, P.B), dim3(kRowThreads), smem, s, cs, P);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample draw launch: %s", cudaGetErrorString(e));
   const int ncl = std::max(1, std::min(P.B, kFinishClusters));
   e = launch_k(sample_finish_kernel<TT, DK>, dim3(cs_x * ncl), dim3(kResThreads), smem_x, s, cs_x, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
@@ -1184,7 +1332,8 @@ sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, si
 extern "C" size_t spec_verify_sample_workspace_size(int B, int K, int V) {
   (void)V;
   if (B < 0 || K < 0) return 0;
-  return sv::records_bytes(B, K);
+  if (V < 1) return 0;
+  return sv::workspace_bytes_for(B, K, V);
 }
 
 extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
@@ -1213,8 +1362,8 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   } else if (K > 0 && draft_dtype != logit_dtype) {
     return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: draft logits must have the target's dtype");
   }
-  if (!workspace || workspace_bytes < records_bytes(B, K))
-    return fail(SV_ERR_WORKSPACE, "spec_verify_sample: workspace needs %zu bytes", records_bytes(B, K));
+  if (!workspace || workspace_bytes < workspace_bytes_for(B, K, V))
+    return fail(SV_ERR_WORKSPACE, "spec_verify_sample: workspace needs %zu bytes", workspace_bytes_for(B, K, V));
   if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_sample: workspace not 256-byte aligned");
   if (B == 0) return ok();
 
@@ -1254,6 +1403,8 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   P.target = target_logits; P.draft = draft; P.tokens = draft_tokens; P.uniforms = uniforms;
   P.p_at = p_at_draft; P.q_at = q_at_draft; P.out_tokens = out_tokens; P.num_acc = num_accepted;
   P.recs = static_cast<RowRec *>(workspace); P.status = dev_status;
+  P.part = reinterpret_cast<float4 *>(static_cast<uint8_t *>(workspace) + records_bytes(B, K));
+  P.nc = stat_chunks(V);
   P.B = B; P.K = K; P.V = V; P.ns = ns; P.ns_x = ns_x; P.flags = flags; P.cache_x = cache_x ? 1 : 0;
   P.aligned = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0 &&
               (K == 0 || (aligned(draft, 16) && ((size_t)V * es_buf_d) % 16 == 0));
@@ -1297,7 +1448,7 @@ extern "C" sv_status spec_verify_sample(const void *target_logits, sv_dtype logi
 // this static device array (every GPU that loads the library keeps it until
 // the process exits).
 namespace {
-constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB: 21845 rows of (sequence, position)
+constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB: 48 + 16 ceil(V / 8192) bytes per (sequence, position)
 __device__ __align__(256) uint8_t g_sample_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
@@ -1311,14 +1462,15 @@ extern "C" sv_status spec_verify_sample_static(const void *target_logits, sv_dty
                                                int32_t *num_accepted, float *p_at_draft, float *q_at_draft,
                                                int32_t *dev_status, sv_stream_t stream) {
   using namespace sv;
-  if (B < 0 || K < 0)
-    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_static: bad sizes B=%d K=%d", B, K);
-  const size_t need = records_bytes(B, K);
+  if (B < 0 || K < 0 || V < 1)
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_static: bad sizes B=%d K=%d V=%d", B, K, V);
+  const size_t need = workspace_bytes_for(B, K, V);
   if (need > kStaticScratchBytes)
     return fail(SV_ERR_UNSUPPORTED,
-                "spec_verify_sample_static: B*(K+1) = %lld rows exceed the static scratch of %zu bytes "
-                "(%zu rows); use spec_verify_sample with a caller workspace",
-                (long long)B * (K + 1), kStaticScratchBytes, kStaticScratchBytes / sizeof(RowRec));
+                "spec_verify_sample_static: B*(K+1) = %lld rows need %zu bytes (a %zu-byte record and %d "
+                "16-byte chunk statistics per row), more than the static scratch of %zu bytes; use "
+                "spec_verify_sample with a caller workspace",
+                (long long)B * (K + 1), need, sizeof(RowRec), stat_chunks(V), kStaticScratchBytes);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_static: cudaGetDevice: %s", cudaGetErrorString(e));

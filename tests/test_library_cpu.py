@@ -38,8 +38,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_workspace_sizes(lib):
-    # sampling: one 48-byte record per (sequence, position), 256-byte rounded
-    assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == 64 * 5 * 48 // 256 * 256 + (256 if 64 * 5 * 48 % 256 else 0)
+    # sampling: one 48-byte record per (sequence, position), then one 16-byte
+    # (max, sum) pair per 8192-logit chunk of each row, each part 256-byte rounded
+    up = lambda x: (x + 255) // 256 * 256
+    chunks = (128256 + 8191) // 8192
+    assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == up(64 * 5 * 48) + up(64 * 5 * chunks * 16)
     assert lib.spec_verify_sample_workspace_size(0, 4, 10) == 0
     s = lib.spec_verify_attn_workspace_size(64, 5, 64, 8, 128, 512, 16)
     # (acc d + m + l) floats per (sequence, kv head, split, row); splits of at
