@@ -232,11 +232,13 @@ sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
  *   reserves all GPU memory for its KV pool at start-up and forbids later
  *   allocations, or a caller whose fixed interface cannot pass a workspace).
  *   Same as spec_verify_sample without the workspace arguments: the
- *   workspace (a 48-byte record and 16 * ceil(V / 8192) bytes of chunk
- *   statistics per (sequence, position)) goes to a 1 MiB static device array
- *   inside the library, which every GPU that loads the library holds until
- *   the process exits. For V = 128256 that is B * (K+1) <= 3449; larger
- *   sizes return SV_ERR_UNSUPPORTED with a message.
+ *   workspace (spec_verify_sample_workspace_size(B, K, V) bytes: a 48-byte
+ *   record and 16 * ceil(V / 8192) bytes of chunk statistics per (sequence,
+ *   position), 8 bytes per sequence, plus 140.25 KB of scratch for the
+ *   float-float pass) goes to a 1 MiB static device array inside the
+ *   library, which every GPU that loads the library holds until the process
+ *   exits. For V = 128256 and K = 4 that is B <= 592; larger sizes return
+ *   SV_ERR_UNSUPPORTED with a message.
  *   Allocates nothing (no cudaMalloc / cudaFree or allocating library call).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.

@@ -39,13 +39,10 @@ namespace {
 
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kResThreads = 512;   // finish kernel
-constexpr int kResWarps = kResThreads / 32;
 constexpr uint32_t kChunkBytes = 16384;
 constexpr int kMaxChunks = 32;              // per CTA, target + draft
 constexpr size_t kMaxSliceSmem = 200 * 1024;
 constexpr size_t kTargetSliceSmem = 64 * 1024;
-constexpr int kFinishClusters = 8;
 
 enum : uint32_t {
   REC_ACCEPT = 1u,       // fp32 accept decision of the draft at this position
@@ -81,9 +78,12 @@ struct SampleParams {
   int B, K, V;
   int nc;        // statistics chunks per row
   int ns;        // elements per CTA slice of the draw kernel (multiple of 8)
-  int ns_x;      // elements per CTA slice in the finish kernel
   int aligned;   // rows are 16-byte aligned: bulk copies usable
-  int cache_x;   // finish kernel keeps the float-float exponentials in shared memory
+  unsigned *fin_sync;   // finish grid barrier: arrival count, generation; [2] pending count
+  int2 *pend;           // [B] sequences left to the finish grid: (b, first row to resolve)
+  float2 *fin_sum;      // [kMaxUnits][kMaxFinCtas][2] chunk sums of e_p, e_q (float-float)
+  float2 *fin_tot;      // [kMaxEntries][kMaxFinCtas] chunk totals of the weights
+  int *fin_last;        // [kMaxEntries][kMaxFinCtas] last positive weight of a chunk
   unsigned flags;
   float c;       // log2(e) / T
   float invT_hi, invT_lo;
@@ -466,6 +466,7 @@ __global__ void __launch_bounds__(kStatThreads) sample_stats_kernel(const __grid
   const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
   const TD *drow = q_logits ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
   const int e0 = c * kStatChunk, e1 = min(V, e0 + kStatChunk);
+  if (tid == 0 && c == 0 && i == 0 && b == 0) P.fin_sync[2] = 0u;   // no sequence pending yet
   const int g0 = e0 / 8, g1 = (e1 + 7) / 8;
   const bool vec = P.aligned != 0;
 
@@ -561,6 +562,20 @@ struct DrawShared {
 
 // combined (max, sum) of target (and draft) row i of sequence b: every lane
 // of the warp ends with the same bits
+// emitted tokens of sequence b: the n accepted drafts, then y, then -1
+__device__ __forceinline__ void write_outputs(const SampleParams &P, int b, int n, int y) {
+  const int K = P.K;
+  for (int j = 0; j <= K; ++j)
+    P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? y : -1);
+  P.num_acc[b] = n;
+}
+
+// hands sequence b to the finish grid, to be resolved from row `start` on
+__device__ __forceinline__ void push_pending(const SampleParams &P, int b, int start) {
+  const unsigned slot = atomicAdd(&P.fin_sync[2], 1u);
+  P.pend[slot] = make_int2(b, start);
+}
+
 __device__ __forceinline__ void row_stats(const SampleParams &P, int b, int i, bool q_logits, float &m_p, float &S_p,
                                           float &m_q, float &S_q) {
   const int lane = threadIdx.x & 31;
@@ -600,6 +615,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
   const float c = P.c;
   const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
   if (tid == 0) sh.stop = 2 * K + 1;
+  if (tid == 0 && blockIdx.x == 0 && b == 0) P.fin_sync[0] = 0u;   // the finish grid barrier starts empty
   __syncthreads();
 
   // ---- accept tests of every draft position --------------------------------
@@ -668,7 +684,10 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
   __syncthreads();
   // identical in every CTA of the cluster: no shared memory of a peer is
   // read on this path
-  if (!certain || force) return;
+  if (!certain || force) {   // the first uncertified accept test (or all, forced)
+    if (rank == 0 && tid == 0) push_pending(P, b, force ? 0 : n);
+    return;
+  }
   const float m_p = sh.row_m_p, S_p = sh.row_s_p, m_q = sh.row_m_q, S_q = sh.row_s_q;
   const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
 
@@ -803,7 +822,7 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
   const uint32_t acc_flags = has_draft ? REC_ACC_CERT : 0u;   // a certified rejection (or the bonus row)
   if (rank == 0 && tid == 0) {
     rec->z = Z; rec->e_abs = e_abs;
-    if (!draw_ok) { rec->y = -1; rec->gap = 0.f; rec->flags = acc_flags; }
+    if (!draw_ok) { rec->y = -1; rec->gap = 0.f; rec->flags = acc_flags; push_pending(P, b, n); }
   }
   if (draw_ok && off_c <= thr && thr < off_c + tot_cta) {
     float woff = 0.f, base = off_c;
@@ -858,9 +877,12 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
       if (lane == 0) {
         const bool found = y >= 0 && y < V;   // else: rounding moved the crossing
         const float gap = found ? fminf(thr - c_lo, c_hi - thr) : 0.f;
+        const bool cert = found && gap > e_abs;
         rec->y = found ? y : -1;
         rec->gap = gap;
-        rec->flags = acc_flags | ((found && gap > e_abs) ? REC_DRAW_CERT : 0u);
+        rec->flags = acc_flags | (cert ? REC_DRAW_CERT : 0u);
+        if (cert) write_outputs(P, b, n, y);
+        else push_pending(P, b, n);
       }
     }
   }
@@ -873,13 +895,25 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
 // n/64 + r (|r| <= 1/128), 2^r - 1 by its Taylor series to r^5, 2^(j/64)
 // from the (hi, lo) table, 2^k by exponent construction. Values below e^-87
 // relative to the row maximum are returned as 0.
-__device__ __forceinline__ ff ffx_exp(float l, float m, const SampleParams &P, const float2 *tbl) {
+// The finish grid runs its code once per call, with the instruction cache
+// cold, so the exponential and the weights are single out-of-line copies
+// called from rolled loops.
+struct FfK {
+  float inv_hi, inv_lo;     // 1/T
+  float l2e_hi, l2e_lo;     // log2(e)
+  int unitT;                // T == 1
+};
+__device__ __forceinline__ FfK ff_consts(const SampleParams &P) {
+  return FfK{P.invT_hi, P.invT_lo, P.log2e_hi, P.log2e_lo, P.unitT};
+}
+
+__device__ __noinline__ ff ffx_exp(float l, float m, FfK k, const float2 *tbl) {
   if (!(l > -INFINITY)) return ff{0.f, 0.f};
   ff x = two_sum(l, -m);
-  if (!P.unitT) x = ff_mul(x, ff{P.invT_hi, P.invT_lo});
+  if (!k.unitT) x = ff_mul(x, ff{k.inv_hi, k.inv_lo});
   if (!(x.hi > -87.f)) return ff{0.f, 0.f};
-  const float t_hi = x.hi * P.log2e_hi;
-  const float t_lo = fmaf(x.hi, P.log2e_hi, -t_hi) + fmaf(x.hi, P.log2e_lo, x.lo * P.log2e_hi);
+  const float t_hi = x.hi * k.l2e_hi;
+  const float t_lo = fmaf(x.hi, k.l2e_hi, -t_hi) + fmaf(x.hi, k.l2e_lo, x.lo * k.l2e_hi);
   const float n = rintf(t_hi * 64.f);
   const float r = fmaf(-n, 0.015625f, t_hi) + t_lo;
   const float y = r * 0.69314718f;
@@ -899,388 +933,545 @@ __device__ __forceinline__ void acc_add(ff &a, ff v) {
 
 __device__ __forceinline__ ff ff_norm(ff a) { return quick_two_sum(a.hi, a.lo); }
 
-struct ExactShared {
-  ff red[32];
-  ff wsum[kResWarps];    // per-warp weight totals
-  ff wincl[kResWarps];   // their inclusive prefix
-  ff pub_sp, pub_sq, pub_tot;
-  int pub_y, pub_last;
-  float2 tbl[64];
-};
+// ------------------------------------------------ cooperative finish pass ---
+// sample_finish_kernel: one CTA per SM, launched cooperatively (all CTAs
+// resident), so the grid can meet at barriers.
+//   * Every CTA walks every sequence's records (certified accepts, then the
+//     first rejection or the bonus row) and builds the same ordered list of
+//     sequences whose walk reaches a decision that is not certified; the
+//     tokens of the others are written by CTA b % gridDim.x.
+//   * Listed sequences are resolved in rounds. A round takes, for each one,
+//     the rows its walk may still need (uncertified accept tests and the row
+//     it ends on), at most kMaxUnits rows in all, and evaluates them together:
+//     every CTA sums e_p and e_q over its contiguous chunk of each row ->
+//     grid barrier -> every CTA forms the same row sums, takes the exact
+//     accept tests in walk order, picks each sequence's draw row and sums its
+//     residual weights over the chunk -> grid barrier -> every CTA forms the
+//     same prefix over chunks; the CTA whose chunk holds v Z finds the token
+//     and writes that sequence's outputs. Sequences whose rows ran past the
+//     round's budget continue in the next round.
+// Cross-CTA values go through the workspace and are read from L2; every CTA
+// combines them in the same order, so all CTAs take the same decisions.
+constexpr int kFinThreads = 512;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kMaxEntries = 32;     // sequences resolved together
+constexpr int kMaxUnits = 32;       // rows evaluated per round
+constexpr int kMaxFinCtas = 160;    // CTAs of the finish grid (one per SM)
+static_assert(kMaxUnits >= kMaxEntries && kMaxUnits <= 2 * kFinWarps, "unit slots per warp");
 
-// Exact-arithmetic (float-float) evaluation of row i of sequence b: the
-// accept test (when need_acc) and, unless accepted, the inverse-CDF draw.
-// Called by every thread of every CTA of the cluster; st / sd hold this CTA's
-// slice [e0, e0 + n_grp*8) of the row (padded like the rows kernel does).
-template <typename TT, int DK>
-__device__ bool exact_row(const SampleParams &P, ExactShared &sh, const TT *st,
-                          const typename std::conditional<DK == 0, TT, float>::type *sd, ff *cp, ff *cq,
-                          int n_grp, int e0, bool has_draft, bool need_acc, float m_p, float m_q, float lp_x,
-                          float lq_x, float u, float v_u, int *y_out) {
-  const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool q_logits = has_draft && DK == 0;
-  // cp / cq (when not null) keep e_p, e_q of element j of group g at
-  // [j * n_grp + g] for the weights pass
-  ff sp{0.f, 0.f}, sq{0.f, 0.f};
-  for (int g = tid; g < n_grp; g += blockDim.x) {
-    float x[8];
-    load8(st, g, x);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const ff e = ffx_exp(x[j], m_p, P, sh.tbl);
-      if (cp) cp[j * n_grp + g] = e;
-      acc_add(sp, e);
-    }
-    if (q_logits) {
-      load8(sd, g, x);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const ff e = ffx_exp(x[j], m_q, P, sh.tbl);
-        if (cp) cq[j * n_grp + g] = e;
-        acc_add(sq, e);
-      }
-    }
-  }
-  sp = block_sum_ff(ff_norm(sp), sh.red);
-  sq = block_sum_ff(ff_norm(sq), sh.red);
-  if (tid == 0) { sh.pub_sp = sp; sh.pub_sq = sq; }
-  cluster_sync();
-  ff Sp = lane < cs ? ld_dsmem_ff(&sh.pub_sp, lane) : ff{0.f, 0.f};
-  ff Sq = lane < cs ? ld_dsmem_ff(&sh.pub_sq, lane) : ff{0.f, 0.f};
-  Sp = warp_sum_ff(Sp);
-  Sq = warp_sum_ff(Sq);
-  cluster_sync();   // peers have read the published sums
-  if (!q_logits) Sq = ff{1.f, 0.f};
-  if (need_acc && has_draft) {
-    // u q(x) < p(x)  <=>  u e_q(x) S_p < e_p(x) S_q   (draft logits)
-    //                <=>  u q(x) S_p < e_p(x)         (draft probabilities)
-    const ff epx = ff_norm(ffx_exp(lp_x, m_p, P, sh.tbl));
-    ff lhs, rhs;
-    if (DK == 0) {
-      lhs = ff_mul(ff_mul(ff{u, 0.f}, ff_norm(ffx_exp(lq_x, m_q, P, sh.tbl))), Sp);
-      rhs = ff_mul(epx, Sq);
-    } else {
-      lhs = ff_mul(ff{u, 0.f}, ff_mul(ff{lq_x, 0.f}, Sp));
-      rhs = epx;
-    }
-    if (ff_gt(rhs, lhs)) return true;
-  }
-  // scaled weights w'(y) = S_p S_q w(y); mode 0: target row (bonus, or the
-  // zero-mass fallback), 1: two softmaxes, 2: given probabilities
-  int mode = !has_draft ? 0 : (DK == 0 ? 1 : 2);
-  auto wx8 = [&](int g, ff (&w)[8]) {
-    float xp[8], xq[8];
-    if (!cp) load8(st, g, xp);
-    if (has_draft && (mode == 2 || !cp)) load8(sd, g, xq);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const ff ep = cp ? cp[j * n_grp + g] : ffx_exp(xp[j], m_p, P, sh.tbl);
-      if (mode == 0) {
-        w[j] = ep;
-      } else if (mode == 1) {
-        const ff eq = cp ? cq[j * n_grp + g] : ffx_exp(xq[j], m_q, P, sh.tbl);
-        w[j] = ff_max0(ff_add(ff_mul(ep, Sq), ff_neg(ff_mul(eq, Sp))));
-      } else {
-        w[j] = ff_max0(ff_add(ep, ff_neg(ff_mul(ff{xq[j], 0.f}, Sp))));
-      }
-    }
-  };
-  // Each warp owns groups [g_lo, g_hi); lane l owns the run [r_lo, r_hi) of
-  // them, so one warp scan of the lane totals and one scan of the warp
-  // totals give every run its offset; the owner of v Z is found by ballots.
-  const int nw = (int)(blockDim.x >> 5);
-  const int gpw = (n_grp + nw - 1) / nw;
-  const int g_lo = min(n_grp, warp * gpw), g_hi = min(n_grp, g_lo + gpw);
-  const int G = (gpw + 31) >> 5;
-  const int r_lo = min(g_hi, g_lo + lane * G), r_hi = min(g_hi, r_lo + G);
-  int y = -1;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    ff t_l{0.f, 0.f};
-    int last_pos = -1;
-    for (int g = r_lo; g < r_hi; ++g) {
-      ff w[8];
-      wx8(g, w);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc_add(t_l, w[j]);
-        if (w[j].hi > 0.f) last_pos = e0 + 8 * g + j;
-      }
-    }
-    t_l = ff_norm(t_l);
-    const ff incl = scan32_ff(t_l, lane);
-    last_pos = warp_max_s32(last_pos);
-    if (lane == 31) sh.wsum[warp] = incl;
-    if (lane == 0 && last_pos >= 0) atomicMax(&sh.pub_last, last_pos);
-    __syncthreads();
-    if (warp == 0) {
-      // inclusive prefix of the warp totals; the CTA total is published
-      const ff wi = scan32_ff(lane < nw ? sh.wsum[lane] : ff{0.f, 0.f}, lane);
-      if (lane < nw) sh.wincl[lane] = wi;
-      if (lane == nw - 1) sh.pub_tot = wi;
-    }
-    __syncthreads();
-    cluster_sync();   // totals published
-    // CTA r owns [sum of the totals before r, + its total): a sequential
-    // prefix in rank order, the same in every CTA
-    const ff t_r = lane < cs ? ld_dsmem_ff(&sh.pub_tot, lane) : ff{0.f, 0.f};
-    const int last_all = warp_max_s32(lane < cs ? ld_dsmem_s32(mapa(&sh.pub_last, lane)) : -1);
-    cluster_sync();   // peers have read the totals
-    if (tid == 0) sh.pub_last = -1;
-    ff xoff{0.f, 0.f}, XZ{0.f, 0.f};
-    for (int r = 0; r < cs; ++r) {
-      const ff t{__shfl_sync(0xffffffffu, t_r.hi, r), __shfl_sync(0xffffffffu, t_r.lo, r)};
-      if (r == rank) xoff = XZ;
-      XZ = ff_add(XZ, t);
-    }
-    if (!ff_pos(XZ)) {   // zero residual mass: draw from p_n instead
-      __syncthreads();
-      if (mode == 0) break;
-      mode = 0;
-      continue;
-    }
-    const ff xthr = ff_mul(ff{v_u, 0.f}, XZ);
-    const ff tot{__shfl_sync(0xffffffffu, t_r.hi, rank), __shfl_sync(0xffffffffu, t_r.lo, rank)};
-    if (!ff_gt(xoff, xthr) && ff_gt(ff_add(xoff, tot), xthr)) {
-      // the first warp whose inclusive total passes v Z (the last one if
-      // rounding leaves none)
-      const bool past = lane < nw && ff_gt(ff_add(xoff, sh.wincl[lane]), xthr);
-      const unsigned wb = __ballot_sync(0xffffffffu, past);
-      const int owner = wb ? __ffs(wb) - 1 : nw - 1;
-      if (warp == owner) {
-        const ff base = owner > 0 ? ff_add(xoff, sh.wincl[owner - 1]) : xoff;
-        const unsigned lb = __ballot_sync(0xffffffffu, ff_gt(ff_add(base, incl), xthr));
-        const int L = lb ? __ffs(lb) - 1 : 31;
-        const ff excl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
-        ff start = ff_add(base, lane == 0 ? ff{0.f, 0.f} : excl);
-        start = ff{__shfl_sync(0xffffffffu, start.hi, L), __shfl_sync(0xffffffffu, start.lo, L)};
-        const int L_lo = __shfl_sync(0xffffffffu, r_lo, L), L_hi = __shfl_sync(0xffffffffu, r_hi, L);
-        // the run's groups, one per lane, in ascending order
-        int found = -1, last_p = -1;
-        for (int g0 = L_lo; g0 < L_hi && found < 0; g0 += 32) {
-          const int g = g0 + lane;
-          ff w[8];
-          ff gs{0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) w[j] = ff{0.f, 0.f};
-          if (g < L_hi) {
-            wx8(g, w);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc_add(gs, w[j]);
-          }
-          gs = ff_norm(gs);
-          const ff inc2 = scan32_ff(gs, lane);
-          int cand = -1;
-          ff run_c = ff_add(start, ff_add(inc2, ff_neg(gs)));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const ff nxt = ff_add(run_c, w[j]);
-            if (cand < 0 && w[j].hi > 0.f && ff_gt(nxt, xthr)) cand = e0 + 8 * g + j;
-            if (w[j].hi > 0.f) last_p = max(last_p, e0 + 8 * g + j);
-            run_c = nxt;
-          }
-          const unsigned hit = __ballot_sync(0xffffffffu, cand >= 0);
-          if (hit) found = __shfl_sync(0xffffffffu, cand, __ffs(hit) - 1);
-          start = ff_add(start, ff{__shfl_sync(0xffffffffu, inc2.hi, 31), __shfl_sync(0xffffffffu, inc2.lo, 31)});
-        }
-        last_p = warp_max_s32(last_p);
-        if (found < 0) found = last_p;   // crossing within rounding of the run's end
-        if (lane == 0) sh.pub_y = found;
-      }
-    }
-    cluster_sync();   // the draw is published
-    y = warp_max_s32(lane < cs ? ld_dsmem_s32(mapa(&sh.pub_y, lane)) : -1);
-    if (y < 0) y = last_all;   // v Z at the very top of the range (rounding)
-    cluster_sync();   // peers have read pub_y
-    if (tid == 0) sh.pub_y = -1;
-    __syncthreads();
-    break;
-  }
-  *y_out = y;
-  return false;
+// sequence phases: walk its records from e_i, redraw row e_i from p (zero
+// residual mass), or finished
+enum : int { ENT_WALK = 0, ENT_REDRAW = 1, ENT_DONE = 2 };
+
+// float-float weight of one element (target logit lp, draft value lq) of the
+// row drawn from: mode 0 the target row (e_p), 1 two softmaxes
+// (max(0, e_p S_q - e_q S_p)), 2 given draft probabilities
+// (max(0, e_p - q S_p)); a padding element (lp = -inf) weighs 0
+__device__ __noinline__ ff resid_weight(int mode, float lp, float lq, float m_p, float m_q, ff Sp, ff Sq, FfK k,
+                                        const float2 *tbl) {
+  const ff ep = ffx_exp(lp, m_p, k, tbl);
+  if (mode == 0) return ep;
+  if (mode == 1) return ff_max0(ff_add(ff_mul(ep, Sq), ff_neg(ff_mul(ffx_exp(lq, m_q, k, tbl), Sp))));
+  return ff_max0(ff_add(ep, ff_neg(ff_mul(ff{lq > -INFINITY ? lq : 0.f, 0.f}, Sp))));
 }
 
-// Every cluster walks every sequence (one thread per sequence, in rounds of
-// kResThreads sequences): certified accepts, then the first rejection or the
-// bonus row. All CTAs build the same ordered list of sequences whose next
-// needed decision is not certified, and cluster c re-evaluates entries
-// c, c + ncl, ... (the row's slices copied into shared memory, float-float
-// arithmetic, continuing the walk), so the rare exact rows spread over all
-// clusters. The tokens of a fully certified sequence b are written by
-// cluster b % ncl.
-constexpr int kFinishMaxSeq = kResThreads;   // sequences per walk round
+// Grid barrier of the cooperative launch: one arrival count in global memory
+// (zeroed before the launch); barrier j of the launch completes when the
+// count reaches j * gridDim.x, so the count is never reset. Bounded wait;
+// returns false after a timeout.
+__device__ __forceinline__ bool grid_sync(unsigned *count, unsigned &target, int *flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    target += gridDim.x;
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
+    const uint64_t t0 = global_ns();
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+      if ((int)(v - target) >= 0) break;
+      if (global_ns() - t0 > kWaitLimitNs) { ok = false; break; }
+      __nanosleep(16);
+    }
+    __threadfence();
+    *flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
+__device__ __forceinline__ ff ldcg_ff(const float2 *p) {
+  const float2 v = __ldcg(p);
+  return ff{v.x, v.y};
+}
+
+// exclusive block prefix (element order = thread order) and total of ff
+// values; every thread gets its exclusive prefix and the block total
+__device__ __forceinline__ void block_scan_ff(ff v, ff *wtot, ff &excl, ff &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const ff incl = scan32_ff(v, lane);
+  __syncthreads();
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  const ff wi = scan32_ff(lane < kFinWarps ? wtot[lane] : ff{0.f, 0.f}, lane);   // every warp, same bits
+  const ff wex{__shfl_sync(0xffffffffu, wi.hi, (warp + 31) & 31), __shfl_sync(0xffffffffu, wi.lo, (warp + 31) & 31)};
+  const ff w_off = warp == 0 ? ff{0.f, 0.f} : wex;
+  const ff tex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+  excl = ff_add(w_off, lane == 0 ? ff{0.f, 0.f} : tex);
+  total = ff{__shfl_sync(0xffffffffu, wi.hi, kFinWarps - 1), __shfl_sync(0xffffffffu, wi.lo, kFinWarps - 1)};
+}
+
+// Warps of a CTA shared among n items (rows or draws): with n <= kFinWarps,
+// item j gets warps j, j + n, j + 2n, ...; with more, warp w takes items w
+// and w + kFinWarps alone. For warp w: its first item, its index in the
+// item's group and the group's size in warps.
+struct WarpShare { int first, gi, gn; };
+__device__ __forceinline__ WarpShare warp_share(int warp, int n) {
+  if (n <= kFinWarps) return {warp % n, warp / n, (kFinWarps - 1 - warp % n) / n + 1};
+  return {warp, 0, 1};
+}
+
+// the per-warp partials of item j, in a fixed order: sum of slot[w][k] over
+// the warps of its group
+__device__ __forceinline__ ff group_sum(const ff (*slot)[2], int j, int n) {
+  if (n > kFinWarps) return slot[j % kFinWarps][j / kFinWarps];
+  ff s{0.f, 0.f};
+  for (int w = j; w < kFinWarps; w += n) s = ff_add(s, slot[w][0]);
+  return s;
+}
+
+// stages row[a + t * stride] (-inf from e1 on) for t < 8 into this thread's
+// slots st[t][threadIdx.x]: the eight loads are issued together
+template <typename T>
+__device__ __forceinline__ void stage8(float (*st)[kFinThreads], const T *row, int a, int stride, int e1) {
+  float x[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const int at = a + t * stride;
+    x[t] = at < e1 ? to_f32(row[at]) : -INFINITY;
+  }
+#pragma unroll
+  for (int t = 0; t < 8; ++t) st[t][threadIdx.x] = x[t];
+}
 
 template <typename TT, int DK>
-__global__ void __launch_bounds__(kResThreads) sample_finish_kernel(const __grid_constant__ SampleParams P) {
+__global__ void __launch_bounds__(kFinThreads, 1) sample_finish_kernel(const __grid_constant__ SampleParams P) {
   pdl_wait();
   pdl_trigger();
   using TD = typename std::conditional<DK == 0, TT, float>::type;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ ExactShared sh;
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int list_n;
-  __shared__ int list_b[kFinishMaxSeq], list_i[kFinishMaxSeq];
-  __shared__ int warp_cnt[kResWarps];
-  const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
-  const int cid = blockIdx.x / cs, ncl = gridDim.x / cs;
+  __shared__ ff red[32];
+  __shared__ float2 tbl[64];
+  __shared__ int sync_flag, n_units, n_draws, n_pend;
+  // sequences being resolved (the same in every CTA)
+  __shared__ int e_b[kMaxEntries], e_i[kMaxEntries], e_state[kMaxEntries];
+  __shared__ int e_nu[kMaxEntries], e_u0[kMaxEntries], e_du[kMaxEntries], e_dr[kMaxEntries];
+  // rows evaluated this round: sequence, row, whether it is an accept test,
+  // the test's inputs, its verdict and the row sums
+  __shared__ int u_e[kMaxUnits], u_row[kMaxUnits], u_test[kMaxUnits], u_acc[kMaxUnits];
+  __shared__ float u_lpx[kMaxUnits], u_lqx[kMaxUnits], u_u[kMaxUnits];
+  __shared__ ff u_sp[kMaxUnits], u_sq[kMaxUnits];
+  // draws of this round: sequence, unit, weight mode, owner CTA, its lower
+  // bound, the threshold v Z
+  __shared__ int d_e[kMaxEntries], d_u[kMaxEntries], d_mode[kMaxEntries], d_own[kMaxEntries];
+  __shared__ ff d_off[kMaxEntries], d_thr[kMaxEntries];
+  // per-warp partials (two slots: a warp serves at most two items)
+  __shared__ ff w_a[kFinWarps][2], w_b[kFinWarps][2];
+  __shared__ int w_last[kFinWarps][2];
+  __shared__ int pick, found;
+  // per-thread staging of a batch of eight loaded logits (target, draft)
+  __shared__ float stg[2][8][kFinThreads];
+
+  const int nb = gridDim.x, cta = blockIdx.x;
   const int K = P.K, V = P.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
-  const int ns = P.ns_x;
-  const int e0 = min(V, rank * ns);
-  const int n_loc = max(0, min(V, e0 + ns) - e0);
-  const int n_grp = (n_loc + 7) >> 3;
-  TT *st = reinterpret_cast<TT *>(smem);
-  TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)ns * sizeof(TT), 128));
-  ff *cp = nullptr, *cq = nullptr;
-  if (P.cache_x) {
-    cp = reinterpret_cast<ff *>(smem + align_up((size_t)ns * sizeof(TT), 128) + align_up((size_t)ns * sizeof(TD), 128));
-    cq = cp + ns;
-  }
-  if (tid < 64) sh.tbl[tid] = P.tbl[tid];
-  if (tid == 0) {
-    sh.pub_y = -1; sh.pub_last = -1;
-    mbar_init(&bar, 1);
-    fence_mbarrier_init();
-  }
+  if (tid < 64) tbl[tid] = P.tbl[tid];
+  if (tid == 0) n_pend = min((int)__ldcg(&P.fin_sync[2]), P.B);
+  unsigned gen = 0;   // arrivals the next barrier waits for (thread 0)
+  const FfK fk = ff_consts(P);
+  // this CTA's chunk of every row; in the owner's search thread t takes
+  // elements [a0, a1) of it
+  const int chunk = (int)align_up((size_t)((V + nb - 1) / nb), 8);
+  const int e0 = min(V, cta * chunk), e1 = min(V, e0 + chunk);
+  const int per_t = (chunk + kFinThreads - 1) / kFinThreads;
+  const int a0 = min(e1, e0 + tid * per_t), a1 = min(e1, a0 + per_t);
+  bool grid_ok = true;
   __syncthreads();
-  cluster_sync();   // peers initialised before any distributed read
+  const int np = n_pend;
 
-  uint32_t phase = 0;
-  const bool vec = P.aligned != 0;
-  for (int round0 = 0; round0 < P.B; round0 += kFinishMaxSeq) {
-    // ---- parallel walk: one thread per sequence ---------------------------
-    const int b = round0 + tid;
-    int start = -1;   // first position whose decision needs the float-float pass
-    if (b < P.B) {
-      const RowRec *recs = P.recs + (int64_t)b * (K + 1);
-      int n = K, ysel = -1;
-      bool done = false;
-      for (int i0 = 0; i0 <= K && !done; i0 += 8) {
-        uint32_t f[8];
-        int yv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {   // independent loads: one round trip
-          const int i = i0 + j;
-          f[j] = i <= K ? recs[i].flags : 0u;
-          yv[j] = i <= K ? recs[i].y : -1;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + j;
-          if (done || i > K) continue;
-          if (i < K && (force || !(f[j] & REC_ACC_CERT))) {
-            start = i;
-            done = true;
-          } else if (i == K || !(f[j] & REC_ACCEPT)) {
-            n = i;
-            done = true;
-            if (!force && (f[j] & REC_DRAW_CERT)) ysel = yv[j];
-            else start = n;
+  for (int base = 0; base < np; base += kMaxEntries) {
+    const int ne = min(kMaxEntries, np - base);
+    if (tid < ne) {
+      const int2 pe = __ldcg(P.pend + base + tid);
+      e_b[tid] = pe.x;
+      e_i[tid] = pe.y;
+      e_state[tid] = ENT_WALK;
+    }
+    __syncthreads();
+    // every round resolves a sequence or moves its walk past one row at least
+    for (int iter = 0; iter <= K + 2; ++iter) {
+      // ---- rows each sequence may still need -------------------------------
+      if (tid < ne) {
+        int nu = 0;
+        if (e_state[tid] == ENT_REDRAW) {
+          nu = 1;
+        } else if (e_state[tid] == ENT_WALK) {
+          const RowRec *recs = P.recs + (int64_t)e_b[tid] * (K + 1);
+          for (int r = e_i[tid]; r <= K; ++r) {
+            const uint32_t f = recs[r].flags;
+            if (r < K && (force || !(f & REC_ACC_CERT))) { ++nu; continue; }
+            if (r < K && (f & REC_ACCEPT)) continue;
+            if (force || !(f & REC_DRAW_CERT)) ++nu;
+            else if (nu == 0) {   // the walk ends on a certified draw
+              e_state[tid] = ENT_DONE;
+              if (cta == 0) write_outputs(P, e_b[tid], r, recs[r].y);
+            }
+            break;
           }
         }
+        e_nu[tid] = nu;
       }
-      if (start < 0 && rank == 0 && b % ncl == cid) {
-        for (int j = 0; j <= K; ++j)
-          P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? ysel : -1);
-        P.num_acc[b] = n;
+      __syncthreads();
+      if (tid == 0) {   // shares of the round's rows, in list order
+        int left = 0, used = 0;
+        for (int e = 0; e < ne; ++e) left += e_nu[e] > 0;
+        for (int e = 0; e < ne; ++e) {
+          if (e_nu[e] == 0) continue;
+          --left;
+          const int take = min(e_nu[e], kMaxUnits - used - left);
+          e_u0[e] = used;
+          e_nu[e] = take;
+          used += take;
+        }
+        n_units = used;
       }
-    }
-    // deterministic compaction (same order in every CTA of every cluster)
-    const unsigned vote = __ballot_sync(0xffffffffu, start >= 0);
-    if (lane == 0) warp_cnt[warp] = __popc(vote);
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0;
-      for (int w = 0; w < kResWarps; ++w) { const int t = warp_cnt[w]; warp_cnt[w] = acc; acc += t; }
-      list_n = acc;
-    }
-    __syncthreads();
-    if (start >= 0) {
-      const int pos = warp_cnt[warp] + __popc(vote & ((1u << lane) - 1u));
-      list_b[pos] = b;
-      list_i[pos] = start;
-    }
-    __syncthreads();
-
-    // ---- float-float re-evaluation of this cluster's list entries ---------
-    for (int li = cid; li < list_n; li += ncl) {
-      const int bb = list_b[li];
-      const RowRec *recs = P.recs + (int64_t)bb * (K + 1);
-      const int32_t *toks = P.tokens + (int64_t)bb * K;
-      int i = list_i[li], n = K, y = -1;
-      for (;;) {
-        // next position needing evaluation from i on (certified accepts skipped)
-        int need = -1;
-        bool need_acc = false;
-        for (; i < K; ++i) {
-          const uint32_t f = recs[i].flags;
-          if (force || !(f & REC_ACC_CERT)) { need = i; need_acc = true; break; }
-          if (!(f & REC_ACCEPT)) break;
-        }
-        n = min(i, K);
-        if (need < 0) {
-          if (!force && (recs[n].flags & REC_DRAW_CERT)) { y = recs[n].y; break; }
-          need = n;
-        }
-        const bool has_draft = need < K;
-        const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + need) * V;
-        const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + need) * V : nullptr;
-        // slice -> shared memory (bulk copy when rows are 16-byte aligned)
-        for (int e = n_loc + tid; e < n_grp * 8; e += blockDim.x) {
-          st[e] = pad_value<TT>(false);
-          if (has_draft) sd[e] = pad_value<TD>(DK == 1);
-        }
-        if (vec) {
-          if (tid == 0 && n_loc > 0) {
-            const uint32_t nbt = (uint32_t)n_loc * sizeof(TT), nbd = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
-            fence_proxy_async_shared();
-            mbar_arrive_expect_tx(&bar, nbt + nbd);
-            bulk_g2s(st, trow + e0, nbt, &bar);
-            if (has_draft) bulk_g2s(sd, drow + e0, nbd, &bar);
-          }
-          if (n_loc > 0) {
-            if (!mbar_wait(&bar, phase) && tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-            phase ^= 1u;
-          }
+      __syncthreads();
+      const int U = n_units;
+      if (U == 0) break;
+      if (tid < ne && e_nu[tid] > 0) {   // this sequence's units
+        int k = e_u0[tid];
+        const int kend = k + e_nu[tid];
+        if (e_state[tid] == ENT_REDRAW) {
+          u_e[k] = tid; u_row[k] = e_i[tid]; u_test[k] = 0;
         } else {
-          for (int e = tid; e < n_loc; e += blockDim.x) {
-            st[e] = trow[e0 + e];
-            if (has_draft) sd[e] = drow[e0 + e];
+          const RowRec *recs = P.recs + (int64_t)e_b[tid] * (K + 1);
+          for (int r = e_i[tid]; r <= K && k < kend; ++r) {
+            const uint32_t f = recs[r].flags;
+            const bool test = r < K && (force || !(f & REC_ACC_CERT));
+            if (!test && r < K && (f & REC_ACCEPT)) continue;
+            if (!test && !force && (f & REC_DRAW_CERT)) break;   // certified: no unit
+            u_e[k] = tid; u_row[k] = r; u_test[k] = test ? 1 : 0;
+            ++k;
+            if (!test) break;
           }
+        }
+      }
+      __syncthreads();
+
+      // ---- step 1: chunk sums of e_p and e_q of every unit ------------------
+      {
+        const WarpShare ws = warp_share(warp, U);
+        for (int k = ws.first, slot = 0; k < U; k += kFinWarps, ++slot) {
+          const int bb = e_b[u_e[k]], r = u_row[k];
+          const bool q_logits = DK == 0 && r < K && e_state[u_e[k]] == ENT_WALK;
+          const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + r) * V;
+          const TD *drow = r < K ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + r) * V : nullptr;
+          if (ws.gi == 0 && lane == 0 && u_test[k]) {   // inputs of the accept test
+            const int x = min(max(P.tokens[(int64_t)bb * K + r], 0), V - 1);
+            u_lpx[k] = to_f32(trow[x]);
+            u_lqx[k] = to_f32(drow[x]);
+            u_u[k] = P.uniforms[((int64_t)bb * (K + 1) + r) * 2];
+          }
+          const float m_p = P.recs[(int64_t)bb * (K + 1) + r].m_p, m_q = P.recs[(int64_t)bb * (K + 1) + r].m_q;
+          const int stride = ws.gn * 32;
+          ff sp{0.f, 0.f}, sq{0.f, 0.f};
+          for (int a = e0 + ws.gi * 32 + lane; a < e1; a += 8 * stride) {
+            stage8(stg[0], trow, a, stride, e1);
+            if (q_logits) stage8(stg[1], drow, a, stride, e1);
+#pragma unroll 1
+            for (int t = 0; t < 8; ++t) {
+              acc_add(sp, ffx_exp(stg[0][t][tid], m_p, fk, tbl));
+              if (q_logits) acc_add(sq, ffx_exp(stg[1][t][tid], m_q, fk, tbl));
+            }
+          }
+          sp = warp_sum_ff(ff_norm(sp));
+          sq = warp_sum_ff(ff_norm(sq));
+          if (lane == 0) { w_a[warp][slot] = sp; w_b[warp][slot] = sq; }
         }
         __syncthreads();
-        const RowRec rr = recs[need];
-        const float *uv = P.uniforms + ((int64_t)bb * (K + 1) + need) * 2;
-        float lp_x = 0.f, lq_x = 0.f;
-        if (has_draft) {
-          const int x = min(max(toks[need], 0), V - 1);
-          lp_x = to_f32(trow[x]);
-          lq_x = to_f32(drow[x]);
+        if (tid < U) {
+          const ff sp = group_sum(w_a, tid, U), sq = group_sum(w_b, tid, U);
+          float4 *dst = reinterpret_cast<float4 *>(P.fin_sum + ((size_t)tid * kMaxFinCtas + cta) * 2);
+          *dst = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
         }
-        int yy = -1;
-        const bool acc = exact_row<TT, DK>(P, sh, st, sd, cp, cq, n_grp, e0, has_draft, need_acc, rr.m_p,
-                                           rr.m_q, lp_x, lq_x, uv[0], uv[1], &yy);
-        if (rank == 0 && tid == 0) {
-          RowRec *w = P.recs + (int64_t)bb * (K + 1) + need;
-          w->flags = rr.flags | (need_acc ? REC_EXACT_ACC : 0u) | (acc ? 0u : REC_EXACT_DRAW);
-          if (!acc) w->y_exact = yy;
+      }
+      grid_ok = grid_sync(P.fin_sync, gen, &sync_flag) && grid_ok;
+
+      // ---- step 2: row sums and exact accept tests (warp per unit; lanes
+      // stride the CTAs, the same order in every CTA) -------------------------
+      for (int k = warp; k < U; k += kFinWarps) {
+        float4 v[(kMaxFinCtas + 31) / 32];
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+          const int c = lane + 32 * q;
+          v[q] = c < nb ? __ldcg(reinterpret_cast<const float4 *>(P.fin_sum + ((size_t)k * kMaxFinCtas + c) * 2))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        __syncthreads();   // the slice buffers are rewritten next
-        if (need_acc && acc) { i = need + 1; continue; }   // accepted: continue the walk
-        n = need;
-        y = yy;
-        break;
+        ff sp{0.f, 0.f}, sq{0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+          sp = ff_add(sp, ff{v[q].x, v[q].y});
+          sq = ff_add(sq, ff{v[q].z, v[q].w});
+        }
+        sp = warp_sum_ff(sp);
+        sq = warp_sum_ff(sq);
+        if (lane == 0) {
+          const int bb = e_b[u_e[k]], r = u_row[k];
+          if (!(DK == 0 && r < K && e_state[u_e[k]] == ENT_WALK)) sq = ff{1.f, 0.f};
+          u_sp[k] = sp;
+          u_sq[k] = sq;
+          int acc = 0;
+          if (u_test[k]) {
+            // u q(x) < p(x)  <=>  u e_q(x) S_p < e_p(x) S_q   (draft logits)
+            //                <=>  u q(x) S_p < e_p(x)         (draft probabilities)
+            const RowRec &rr = P.recs[(int64_t)bb * (K + 1) + r];
+            const float u = u_u[k], lq_x = u_lqx[k];
+            const ff epx = ff_norm(ffx_exp(u_lpx[k], rr.m_p, fk, tbl));
+            ff lhs, rhs;
+            if (DK == 0) {
+              lhs = ff_mul(ff_mul(ff{u, 0.f}, ff_norm(ffx_exp(lq_x, rr.m_q, fk, tbl))), sp);
+              rhs = ff_mul(epx, sq);
+            } else {
+              lhs = ff_mul(ff{u, 0.f}, ff_mul(ff{lq_x, 0.f}, sp));
+              rhs = epx;
+            }
+            acc = ff_gt(rhs, lhs) ? 1 : 0;
+          }
+          u_acc[k] = acc;
+        }
       }
-      if (rank == 0) {
-        for (int j = tid; j <= K; j += blockDim.x)
-          P.out_tokens[(int64_t)bb * (K + 1) + j] = j < n ? toks[j] : (j == n ? y : -1);
-        if (tid == 0) P.num_acc[bb] = n;
+      __syncthreads();
+      // each sequence walks its units: the first exact rejection, or the row
+      // it ends on, is its draw; a walk that runs out of units continues next
+      // round
+      if (tid < ne) {
+        int du = -1, dr = -1;
+        if (e_nu[tid] > 0) {
+          const int bb = e_b[tid];
+          int k = e_u0[tid];
+          const int kend = k + e_nu[tid];
+          if (e_state[tid] == ENT_REDRAW) {
+            du = k; dr = e_i[tid];
+          } else {
+            RowRec *recs = P.recs + (int64_t)bb * (K + 1);
+            int r = e_i[tid];
+            for (; r <= K; ++r) {
+              const uint32_t f = recs[r].flags;
+              const bool test = r < K && (force || !(f & REC_ACC_CERT));
+              if (!test && r < K && (f & REC_ACCEPT)) continue;
+              if (!test && !force && (f & REC_DRAW_CERT)) {   // ends on a certified draw
+                e_state[tid] = ENT_DONE;
+                if (cta == 0) write_outputs(P, bb, r, recs[r].y);
+                break;
+              }
+              if (k == kend) break;   // out of units: resume here
+              if (test) {
+                if (cta == 0) recs[r].flags = f | REC_EXACT_ACC;
+                if (u_acc[k]) { ++k; continue; }
+              }
+              du = k; dr = r;
+              break;
+            }
+            if (du < 0 && e_state[tid] == ENT_WALK) e_i[tid] = r;
+          }
+        }
+        e_du[tid] = du;
+        e_dr[tid] = dr;
       }
+      __syncthreads();
+      if (tid == 0) {   // draws of this round, in list order
+        int nd = 0;
+        for (int e = 0; e < ne; ++e) {
+          if (e_du[e] < 0) continue;
+          d_e[nd] = e;
+          d_u[nd] = e_du[e];
+          d_mode[nd] = e_state[e] == ENT_WALK && e_dr[e] < K ? (DK == 0 ? 1 : 2) : 0;
+          ++nd;
+        }
+        n_draws = nd;
+      }
+      __syncthreads();
+      const int D = n_draws;
+      // chunk totals of the residual weights and their last positive index
+      {
+        const WarpShare ws = warp_share(warp, max(D, 1));
+        for (int j = ws.first, slot = 0; j < D; j += kFinWarps, ++slot) {
+          const int e = d_e[j], k = d_u[j], mode = d_mode[j];
+          const int bb = e_b[e], r = e_dr[e];
+          const float m_p = P.recs[(int64_t)bb * (K + 1) + r].m_p, m_q = P.recs[(int64_t)bb * (K + 1) + r].m_q;
+          const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + r) * V;
+          const TD *drow = r < K ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + r) * V : nullptr;
+          const ff Sp = u_sp[k], Sq = u_sq[k];
+          const int stride = ws.gn * 32;
+          ff t{0.f, 0.f};
+          int last = -1;
+          for (int a = e0 + ws.gi * 32 + lane; a < e1; a += 8 * stride) {
+            stage8(stg[0], trow, a, stride, e1);
+            if (mode != 0) stage8(stg[1], drow, a, stride, e1);
+#pragma unroll 1
+            for (int s8 = 0; s8 < 8; ++s8) {
+              const ff w = resid_weight(mode, stg[0][s8][tid], mode != 0 ? stg[1][s8][tid] : 0.f, m_p, m_q, Sp, Sq,
+                                        fk, tbl);
+              acc_add(t, w);
+              if (w.hi > 0.f) last = a + s8 * stride;
+            }
+          }
+          t = warp_sum_ff(ff_norm(t));
+          last = warp_max_s32(last);
+          if (lane == 0) { w_a[warp][slot] = t; w_last[warp][slot] = last; }
+        }
+        __syncthreads();
+        if (tid < D) {
+          const ff t = group_sum(w_a, tid, D);
+          int m = -1;
+          if (D > kFinWarps) m = w_last[tid % kFinWarps][tid / kFinWarps];
+          else for (int w = tid; w < kFinWarps; w += D) m = max(m, w_last[w][0]);
+          P.fin_tot[(size_t)tid * kMaxFinCtas + cta] = make_float2(t.hi, t.lo);
+          P.fin_last[(size_t)tid * kMaxFinCtas + cta] = m;
+        }
+      }
+      grid_ok = grid_sync(P.fin_sync, gen, &sync_flag) && grid_ok;
+
+      // ---- step 3: prefix over chunks (warp per draw) -----------------------
+      // lane l sums CTAs [l per_l, (l+1) per_l) in order, lanes are scanned
+      // in a fixed order, and the CTAs of the lane holding v Z chain their
+      // boundaries in order (the last one closes on the next lane's start)
+      for (int j = warp; j < D; j += kFinWarps) {
+        const int e = d_e[j], bb = e_b[e], r = e_dr[e];
+        const float2 *tot = P.fin_tot + (size_t)j * kMaxFinCtas;
+        const int per_l = (nb + 31) / 32;   // <= 5
+        ff tv[(kMaxFinCtas + 31) / 32];
+        ff run{0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+          const int c = lane * per_l + q;
+          tv[q] = q < per_l && c < nb ? ldcg_ff(tot + c) : ff{0.f, 0.f};
+        }
+        const float v_u = P.uniforms[((int64_t)bb * (K + 1) + r) * 2 + 1];
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) run = ff_add(run, tv[q]);
+        const ff incl = scan32_ff(run, lane);
+        const ff XZ{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+        const ff tex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+        const ff excl = lane == 0 ? ff{0.f, 0.f} : tex;
+        int own = -2;   // zero residual mass
+        ff s0{0.f, 0.f}, xthr{0.f, 0.f};
+        if (ff_pos(XZ)) {
+          xthr = ff_mul(ff{v_u, 0.f}, XZ);
+          const unsigned past = __ballot_sync(0xffffffffu, ff_gt(incl, xthr));
+          const int L = past ? __ffs(past) - 1 : 31;
+          int mine = -1;
+          ff lo = excl;
+          if (lane == L) {
+            const int c_first = L * per_l, c_last = min(nb, (L + 1) * per_l) - 1;
+            mine = max(0, c_last);
+#pragma unroll
+            for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+              if (c_first + q >= c_last) break;
+              const ff s1 = ff_add(lo, tv[q]);
+              if (ff_gt(s1, xthr)) { mine = c_first + q; break; }
+              lo = s1;
+            }
+          }
+          own = __shfl_sync(0xffffffffu, mine, L);
+          s0 = ff{__shfl_sync(0xffffffffu, lo.hi, L), __shfl_sync(0xffffffffu, lo.lo, L)};
+        }
+        if (lane == 0) { d_own[j] = own; d_off[j] = s0; d_thr[j] = xthr; }
+      }
+      __syncthreads();
+      // the owner CTA finds the token within its chunk and writes the outputs
+      for (int j = 0; j < D; ++j) {
+        const int e = d_e[j], mode = d_mode[j];
+        const int bb = e_b[e], r = e_dr[e];
+        if (d_own[j] == -2) {   // zero residual mass: the draw falls back to p
+          if (mode == 0 && cta == 0 && tid == 0) {
+            write_outputs(P, bb, r, -1);
+            P.recs[(int64_t)bb * (K + 1) + r].flags |= REC_EXACT_DRAW;
+            P.recs[(int64_t)bb * (K + 1) + r].y_exact = -1;
+          }
+          continue;
+        }
+        if (d_own[j] != cta) continue;
+        const int k = d_u[j];
+        const float m_p = P.recs[(int64_t)bb * (K + 1) + r].m_p, m_q = P.recs[(int64_t)bb * (K + 1) + r].m_q;
+        const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + r) * V;
+        const TD *drow = r < K ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + r) * V : nullptr;
+        const ff Sp = u_sp[k], Sq = u_sq[k], xthr = d_thr[j];
+        ff t{0.f, 0.f};
+        int lastp = -1;
+        for (int a = a0; a < a1; a += 8) {
+          stage8(stg[0], trow, a, 1, a1);
+          if (mode != 0) stage8(stg[1], drow, a, 1, a1);
+#pragma unroll 1
+          for (int s8 = 0; s8 < 8; ++s8) {
+            const ff w = resid_weight(mode, stg[0][s8][tid], mode != 0 ? stg[1][s8][tid] : 0.f, m_p, m_q, Sp, Sq,
+                                      fk, tbl);
+            acc_add(t, w);
+            if (w.hi > 0.f) lastp = a + s8;
+          }
+        }
+        t = ff_norm(t);
+        ff excl, total;
+        block_scan_ff(t, red, excl, total);
+        // the first thread whose upper bound passes v Z
+        const ff lo = ff_add(d_off[j], excl);
+        const unsigned wb = __ballot_sync(0xffffffffu, ff_gt(ff_add(lo, t), xthr));
+        if (lane == 0) w_last[warp][0] = wb ? warp * 32 + __ffs(wb) - 1 : 1 << 30;
+        __syncthreads();
+        if (tid == 0) {
+          int first = 1 << 30;
+          for (int w = 0; w < kFinWarps; ++w) first = min(first, w_last[w][0]);
+          pick = first;
+          found = -1;
+        }
+        __syncthreads();
+        if (tid == pick) {
+          int cand = -1;
+          ff runc = lo;
+          for (int a = a0; a < a1 && cand < 0; ++a) {
+            const ff w = resid_weight(mode, to_f32(trow[a]), mode != 0 ? to_f32(drow[a]) : 0.f, m_p, m_q, Sp, Sq, fk,
+                                      tbl);
+            const ff nxt = ff_add(runc, w);
+            if (w.hi > 0.f && ff_gt(nxt, xthr)) cand = a;
+            runc = nxt;
+          }
+          if (cand < 0) cand = lastp;   // crossing within rounding of this thread's end
+          found = cand;
+        }
+        __syncthreads();
+        if (tid == 0) {
+          // v Z within rounding of the chunk's top: its last positive weight,
+          // else the row's
+          int y = found;
+          if (y < 0) y = __ldcg(P.fin_last + (size_t)j * kMaxFinCtas + cta);
+          for (int c = 0; c < nb && y < 0; ++c) y = max(y, __ldcg(P.fin_last + (size_t)j * kMaxFinCtas + c));
+          write_outputs(P, bb, r, y);
+          P.recs[(int64_t)bb * (K + 1) + r].flags |= REC_EXACT_DRAW;
+          P.recs[(int64_t)bb * (K + 1) + r].y_exact = y;
+        }
+        __syncthreads();
+      }
+      if (tid < D) {   // state changes, the same in every CTA
+        const int e = d_e[tid];
+        if (d_own[tid] == -2 && d_mode[tid] != 0) { e_state[e] = ENT_REDRAW; e_i[e] = e_dr[e]; }
+        else e_state[e] = ENT_DONE;
+      }
+      __syncthreads();
     }
-    __syncthreads();   // the list is rebuilt in the next round
+    __syncthreads();
   }
-  cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+  if (!grid_ok && tid == 0 && cta == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ host ---
@@ -1289,9 +1480,63 @@ size_t records_bytes(int B, int K) { return align_up((size_t)B * (K + 1) * sizeo
 
 int stat_chunks(int V) { return (V + kStatChunk - 1) / kStatChunk; }
 
-// per-row records, then the chunk statistics
+// scratch of the finish grid: barrier words, per-CTA row sums of every unit,
+// per-CTA weight totals and last positive indices of every draw
+constexpr size_t kFinSyncBytes = 256;
+constexpr size_t kFinSumBytes = (size_t)kMaxUnits * kMaxFinCtas * 2 * sizeof(float2);
+constexpr size_t kFinTotBytes = (size_t)kMaxEntries * kMaxFinCtas * sizeof(float2);
+constexpr size_t kFinLastBytes = (size_t)kMaxEntries * kMaxFinCtas * sizeof(int);
+constexpr size_t kFinScratchBytes = kFinSyncBytes + kFinSumBytes + kFinTotBytes + kFinLastBytes;
+
+size_t parts_bytes(int B, int K, int V) { return align_up((size_t)B * (K + 1) * stat_chunks(V) * sizeof(float4), 256); }
+
+size_t pending_bytes(int B) { return align_up((size_t)B * sizeof(int2), 256); }
+
+// per-row records, the chunk statistics, the finish grid's scratch, then the
+// list of sequences pending for it
 size_t workspace_bytes_for(int B, int K, int V) {
-  return records_bytes(B, K) + align_up((size_t)B * (K + 1) * stat_chunks(V) * sizeof(float4), 256);
+  return records_bytes(B, K) + parts_bytes(B, K, V) + kFinScratchBytes + pending_bytes(B);
+}
+
+int sm_count() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  });
+  return n;
+}
+
+// Cooperative launch of the finish grid (every CTA resident), staged behind
+// the previous launch when the driver accepts both attributes together.
+template <typename KernelT>
+cudaError_t launch_coop(KernelT kernel, int nb, cudaStream_t s, const SampleParams &P) {
+  static int pdl_ok = 1;
+  for (;;) {
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+    if (pdl_ok) {
+      attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[n].val.programmaticStreamSerializationAllowed = 1;
+      ++n;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nb);
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, P);
+    if (e == cudaSuccess || !pdl_ok) return e;
+    (void)cudaGetLastError();   // retry as a plain cooperative launch
+    pdl_ok = 0;
+  }
 }
 
 void split_ff(double d, float &hi, float &lo) {
@@ -1301,27 +1546,29 @@ void split_ff(double d, float &hi, float &lo) {
 
 
 template <typename TT, int DK>
-sv_status launch_sample(const SampleParams &P, int cs, size_t smem, int cs_x, size_t smem_x, cudaStream_t s) {
+sv_status launch_sample(const SampleParams &P, int cs, size_t smem, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int fin_blocks = 0;
   std::call_once(once, [] {
     const int lim = (int)(kMaxSliceSmem + 1024);
     attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    int per_sm = 0;
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(sample_finish_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(sample_finish_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_finish_kernel<TT, DK>, kFinThreads, 0);
+    // one CTA per SM (the kernel is bound to one by its registers), all resident
+    fin_blocks = std::min(kMaxFinCtas, sm_count() * std::min(per_sm, 1));
   });
   if (attr_err != cudaSuccess)
-    return fail(SV_ERR_CUDA, "spec_verify_sample: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+    return fail(SV_ERR_CUDA, "spec_verify_sample: kernel attributes: %s", cudaGetErrorString(attr_err));
+  if (fin_blocks < 1) return fail(SV_ERR_CUDA, "spec_verify_sample: the finish grid does not fit on the device");
   cudaError_t e = launch_k(sample_stats_kernel<TT, DK>, dim3(P.nc, P.K + 1, P.B), dim3(kStatThreads), 0, s, 1, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample statistics launch: %s", cudaGetErrorString(e));
   e = launch_k(sample_draw_kernel<TT, DK>, dim3(cs, P.B), dim3(kRowThreads), smem, s, cs, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample draw launch: %s", cudaGetErrorString(e));
-  const int ncl = std::max(1, std::min(P.B, kFinishClusters));
-  e = launch_k(sample_finish_kernel<TT, DK>, dim3(cs_x * ncl), dim3(kResThreads), smem_x, s, cs_x, P);
+  e = launch_coop(sample_finish_kernel<TT, DK>, fin_blocks, s, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -1389,14 +1636,6 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
     if (sm <= kMaxSliceSmem) { cs = 16; ns = n; smem = sm; }
   }
   // finish kernel: 16-CTA clusters (8 for small vocabularies)
-  const int cs_x = V >= 65536 ? 16 : 8;
-  int ns_x = 0;
-  size_t smem_x = slice_smem(cs_x, ns_x);
-  // float-float exponentials of both rows cached when they fit
-  const size_t cache_bytes = (size_t)ns_x * sizeof(ff) * ((draft_is_probs && K > 0) ? 1 : 2);
-  const bool cache_x = smem_x + cache_bytes <= kMaxSliceSmem;
-  if (cache_x) smem_x += cache_bytes;
-  if (cs && smem_x > kMaxSliceSmem) cs = 0;
   if (!cs) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large", V);
 
   SampleParams P = {};
@@ -1405,7 +1644,15 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   P.recs = static_cast<RowRec *>(workspace); P.status = dev_status;
   P.part = reinterpret_cast<float4 *>(static_cast<uint8_t *>(workspace) + records_bytes(B, K));
   P.nc = stat_chunks(V);
-  P.B = B; P.K = K; P.V = V; P.ns = ns; P.ns_x = ns_x; P.flags = flags; P.cache_x = cache_x ? 1 : 0;
+  {
+    uint8_t *fin = static_cast<uint8_t *>(workspace) + records_bytes(B, K) + parts_bytes(B, K, V);
+    P.fin_sync = reinterpret_cast<unsigned *>(fin);
+    P.fin_sum = reinterpret_cast<float2 *>(fin + kFinSyncBytes);
+    P.fin_tot = reinterpret_cast<float2 *>(fin + kFinSyncBytes + kFinSumBytes);
+    P.fin_last = reinterpret_cast<int *>(fin + kFinSyncBytes + kFinSumBytes + kFinTotBytes);
+    P.pend = reinterpret_cast<int2 *>(fin + kFinScratchBytes);
+  }
+  P.B = B; P.K = K; P.V = V; P.ns = ns; P.flags = flags;
   P.aligned = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0 &&
               (K == 0 || (aligned(draft, 16) && ((size_t)V * es_buf_d) % 16 == 0));
   const double log2e = 1.4426950408889634074, ln2 = 0.69314718055994530942;
@@ -1419,12 +1666,12 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool probs = draft_is_probs && K > 0;
   switch (logit_dtype) {
-    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, smem, cs_x, smem_x, s) : launch_sample<float, 0>(P, cs, smem, cs_x, smem_x, s);
+    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, smem, s) : launch_sample<float, 0>(P, cs, smem, s);
     case SV_BF16:
-      return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, smem, cs_x, smem_x, s)
-                   : launch_sample<__nv_bfloat16, 0>(P, cs, smem, cs_x, smem_x, s);
+      return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, smem, s)
+                   : launch_sample<__nv_bfloat16, 0>(P, cs, smem, s);
     default:
-      return probs ? launch_sample<__half, 1>(P, cs, smem, cs_x, smem_x, s) : launch_sample<__half, 0>(P, cs, smem, cs_x, smem_x, s);
+      return probs ? launch_sample<__half, 1>(P, cs, smem, s) : launch_sample<__half, 0>(P, cs, smem, s);
   }
 }
 

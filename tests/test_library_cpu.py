@@ -38,12 +38,18 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_workspace_sizes(lib):
-    # sampling: one 48-byte record per (sequence, position), then one 16-byte
-    # (max, sum) pair per 8192-logit chunk of each row, each part 256-byte rounded
+    # sampling: one 48-byte record per (sequence, position), one 16-byte
+    # (max, sum) pair per 8192-logit chunk of each row (each part 256-byte
+    # rounded), then the finish grid's fixed scratch (barrier words; per
+    # re-evaluated row and CTA two float-float sums; per re-evaluated draw and
+    # CTA a float-float total and an index), then one 8-byte entry per
+    # sequence for the list of sequences left to the float-float pass
     up = lambda x: (x + 255) // 256 * 256
     chunks = (128256 + 8191) // 8192
-    assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == up(64 * 5 * 48) + up(64 * 5 * chunks * 16)
-    assert lib.spec_verify_sample_workspace_size(0, 4, 10) == 0
+    fin = 256 + 32 * 160 * 16 + 32 * 160 * (8 + 4)
+    assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == (
+        up(64 * 5 * 48) + up(64 * 5 * chunks * 16) + fin + up(64 * 8))
+    assert lib.spec_verify_sample_workspace_size(0, 4, 10) == fin
     s = lib.spec_verify_attn_workspace_size(64, 5, 64, 8, 128, 512, 16)
     # (acc d + m + l) floats per (sequence, kv head, split, row); splits of at
     # least 16 blocks
