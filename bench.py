@@ -290,10 +290,12 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = sv.kernel_launches()
     t0.record(stream)
     for k in range(args.steps):
         step(evs[k])
     t1.record(stream)
+    timed_launches = sv.kernel_launches() - launches0
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -376,11 +378,11 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": "spec_verify_attn (attn_tc5_kernel + attn_merge_kernel)",
                      "achieved": attn_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": attn_gbs / peak, "traffic": attn_traffic_from_profile()},
-        "roofline_sample": {"bound": "hbm", "kernel": "spec_verify_sample (rows + resolve)",
+        "roofline_sample": {"bound": "hbm", "kernel": "spec_verify_sample (stats + draw + finish)",
                             "achieved": samp_gbs, "peak": peak, "unit": "GB/s", "frac": samp_gbs / peak},
         "e2e": ({"value": job_steps_per_sec(e2e_steps, world, e2e_ms), "unit": UNIT,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": timed_launches,
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:

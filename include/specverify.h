@@ -99,6 +99,11 @@ typedef struct {
 /* Message of the last error on the calling thread ("" after success). */
 const char *sv_last_error_string(void);
 
+/* Number of kernels this library has launched successfully in this process
+ * (all threads, all devices). Host-side count, no device access; a caller
+ * takes the difference around a region to count its launches. */
+unsigned long long sv_kernel_launches(void);
+
 /* ------------------------------------------------------------------------ *
  * kv_block_append
  *   Writes k_new[b][j][g][:] and v_new[b][j][g][:] (j = 0..n_new-1) to

@@ -56,6 +56,8 @@ def load_library(path: str = LIB_PATH):
     LP = ctypes.POINTER(_Layout)
     lib.sv_last_error_string.restype = ctypes.c_char_p
     lib.sv_last_error_string.argtypes = []
+    lib.sv_kernel_launches.restype = ctypes.c_ulonglong
+    lib.sv_kernel_launches.argtypes = []
     lib.kv_block_append.restype = I
     lib.kv_block_append.argtypes = [P, P, I, P, P, I, LP, P, P, P, I, P, I, I, I, I, I, I, P, P]
     lib.spec_verify_attn_workspace_size.restype = Z
@@ -187,6 +189,11 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=N
 
 
 # ------------------------------------------------------------- sampling ---
+
+def kernel_launches():
+    """Kernels the library has launched in this process (host-side count)."""
+    return int(load_library().sv_kernel_launches())
+
 
 def sample_workspace_size(B, K, V):
     return load_library().spec_verify_sample_workspace_size(B, K, V)

@@ -1533,6 +1533,7 @@ cudaError_t launch_coop(KernelT kernel, int nb, cudaStream_t s, const SamplePara
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)n;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, P);
+    if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
     if (e == cudaSuccess || !pdl_ok) return e;
     (void)cudaGetLastError();   // retry as a plain cooperative launch
     pdl_ok = 0;

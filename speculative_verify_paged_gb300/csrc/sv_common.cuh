@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <string>
+#include <atomic>
 #include <utility>
 
 #include "../../include/specverify.h"
@@ -21,6 +22,8 @@ namespace sv {
 
 // Per-thread message of the last failed call.
 std::string &last_error();
+// kernels this library launched successfully in this process
+std::atomic<unsigned long long> &launch_counter();
 
 inline sv_status fail(sv_status st, const char *fmt, ...) {
   char buf[512];
@@ -221,7 +224,9 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)n;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 // ----------------------------------------------------- warp reductions ---

@@ -21,20 +21,26 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^(?:const\s+)?(?:sv_status|size_t|char|void)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^(?:const\s+)?(?:sv_status|size_t|char|void|unsigned long long)\s*\*?\s*(\w+)\s*\(",
+                       text, flags=re.M)
     return sorted(set(names))
 
 
 def test_header_declares_the_three_operations():
     names = declared_functions()
     for n in ("kv_block_append", "spec_verify_attn", "spec_verify_sample", "sv_last_error_string",
-              "spec_verify_attn_workspace_size", "spec_verify_sample_workspace_size"):
+              "spec_verify_attn_workspace_size", "spec_verify_sample_workspace_size", "sv_kernel_launches"):
         assert n in names
 
 
 def test_every_declared_symbol_is_exported(lib):
     for n in declared_functions():
         assert hasattr(lib, n), n
+
+
+def test_launch_counter_starts_without_gpu_work(lib):
+    # host-side count; no kernel has run in this CPU-only process
+    assert lib.sv_kernel_launches() == 0
 
 
 def test_workspace_sizes(lib):
