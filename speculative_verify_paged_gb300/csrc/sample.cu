@@ -18,12 +18,15 @@
 //     statistics, evaluates every accept test in fp32 with a certificate
 //     that it lies outside its rounding bound, and finds the position whose
 //     draw is used (the first certified rejection, or the bonus row). Only
-//     that row is read again; its residual weights are formed over the
-//     cluster's shared-memory slices and the inverse-CDF draw gets its own
-//     certificate. One 48-byte record per (sequence, position) results.
-//   * sample_finish_kernel: a few clusters walk each sequence's records in
-//     order, stop at the first rejection and write the emitted tokens. The
-//     rare decision that is not certified (a few percent of sequences) is
+//     that row is read again, 16-byte loads straight into registers (no
+//     shared-memory slices, so every CTA of the grid is resident at once);
+//     its residual weights are summed per block of 256 elements, the
+//     cluster's prefix locates v Z, the owning warp rescans one block, and
+//     the inverse-CDF draw gets its own certificate. One 48-byte record per
+//     (sequence, position) results; certified sequences write their tokens.
+//   * sample_finish_kernel: one CTA per SM (cooperative launch) resolves the
+//     sequences the draw kernel queued. The rare decision that is not
+//     certified (a few percent of sequences) is
 //     re-evaluated from that row's logits in float-float arithmetic (~1e-9
 //     relative error per term), so emitted tokens are those of exact
 //     arithmetic except for uniforms within ~1e-10 of a boundary.
@@ -39,10 +42,6 @@ namespace {
 
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr uint32_t kChunkBytes = 16384;
-constexpr int kMaxChunks = 32;              // per CTA, target + draft
-constexpr size_t kMaxSliceSmem = 200 * 1024;
-constexpr size_t kTargetSliceSmem = 64 * 1024;
 
 enum : uint32_t {
   REC_ACCEPT = 1u,       // fp32 accept decision of the draft at this position
@@ -77,7 +76,7 @@ struct SampleParams {
   int32_t *status;
   int B, K, V;
   int nc;        // statistics chunks per row
-  int ns;        // elements per CTA slice of the draw kernel (multiple of 8)
+  int gpc;       // groups of eight elements per CTA slice of the draw kernel
   int aligned;   // rows are 16-byte aligned: bulk copies usable
   unsigned *fin_sync;   // finish grid barrier: arrival count, generation; [2] pending count
   int2 *pend;           // [B] sequences left to the finish grid: (b, first row to resolve)
@@ -548,16 +547,71 @@ __global__ void __launch_bounds__(kStatThreads) sample_stats_kernel(const __grid
 // first position that rejects (or whose test is not certified) stops the
 // walk; only the row drawn from is read again: the residual of the first
 // certified rejection, or the bonus row when every draft is accepted. Its
-// weights w'(y) = max(0, e_p(y) - r e_q(y)) are formed over the cluster's
-// slices, one warp scan of lane totals and the cluster's prefix locate v Z,
-// and the draw gets its own certificate. Anything uncertified is left to
-// the finish kernel.
+// weights w'(y) = max(0, e_p(y) - r e_q(y)) are formed from register loads
+// of each CTA's slice; block totals, warp totals and the cluster's prefix
+// locate v Z, the owning warp rescans one block, and the draw gets its own
+// certificate. Anything uncertified is left to the finish kernel.
+
+// sum of eight fp32 weights, pairwise in packed arithmetic
+__device__ __forceinline__ float sum8f(const float (&w)[8]) {
+  const float2 a = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
+  const float2 bb = __fadd2_rn(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
+  const float2 t = __fadd2_rn(a, bb);
+  return t.x + t.y;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// fp32 weights of one group of eight elements of the row drawn from, in
+// units of S_p times probability: max(0, e_p - r e_q) with r = S_p / S_q
+// (draft logits) or r = S_p (draft probabilities, e_q = q), e_p alone for
+// the bonus row; padding reads as -inf (logits) or 0 (probabilities)
+template <typename TT, typename TD, int DK>
+__device__ __forceinline__ void draw_weights8(const Raw8<TT> &rt, const Raw8<TD> &rd, bool has_draft, float c,
+                                              float mcp, float mcq, float r_pq, float (&w)[8]) {
+  float xp[8];
+  unpack8(rt, xp);
+  const float2 cc = make_float2(c, c);
+  if (has_draft) {
+    float xq[8];
+    unpack8(rd, xq);
+    const float2 nref = make_float2(-mcp, -mcq);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float ep, eq;
+      if (DK == 0) {
+        const float2 y = __ffma2_rn(make_float2(xp[j], xq[j]), cc, nref);
+        ep = ex2(y.x);
+        eq = ex2(y.y);
+      } else {
+        ep = ex2(fmaf(xp[j], c, -mcp));
+        eq = xq[j];
+      }
+      w[j] = fmaxf(fmaf(-r_pq, eq, ep), 0.f);
+    }
+  } else {
+    const float2 np = make_float2(-mcp, -mcp);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const float2 y = __ffma2_rn(make_float2(xp[j], xp[j + 1]), cc, np);
+      w[j] = ex2(y.x);
+      w[j + 1] = ex2(y.y);
+    }
+  }
+}
+
+constexpr int kMaxDrawBlocks = 64;   // blocks of 32 groups per CTA slice (2048 groups)
+
 struct DrawShared {
-  uint64_t bar;
   int stop;               // 2 * position + (0: not certified, 1: certified rejection)
   float row_m_p, row_s_p, row_m_q, row_s_q;
   float pub_tot;          // this CTA's draw mass
-  float wsum[kRowWarps];
+  float wsum[kRowWarps];  // per warp
+  float btot[kMaxDrawBlocks];   // per block of 32 groups
 };
 
 // combined (max, sum) of target (and draft) row i of sequence b: every lane
@@ -601,11 +655,10 @@ __device__ __forceinline__ void row_stats(const SampleParams &P, int b, int i, b
 }
 
 template <typename TT, int DK>
-__global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_constant__ SampleParams P) {
+__global__ void __launch_bounds__(kRowThreads, 4) sample_draw_kernel(const __grid_constant__ SampleParams P) {
   pdl_wait();
   pdl_trigger();
   using TD = typename std::conditional<DK == 0, TT, float>::type;
-  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ DrawShared sh;
 
   const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
@@ -691,116 +744,57 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
   const float m_p = sh.row_m_p, S_p = sh.row_s_p, m_q = sh.row_m_q, S_q = sh.row_s_q;
   const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
 
-  // ---- the draw: slices of row n -------------------------------------------
+  // ---- the draw: this CTA's slice of row n, straight into registers -------
+  // The slice is groups [gs0, gs1) of eight elements; warp w takes blocks
+  // [w bpw, (w+1) bpw) of 32 consecutive groups (lane l: group 32 k + l of
+  // the block), so element order is (warp, block, lane, element).
   const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + n) * V;
   const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + n) * V : nullptr;
-  const int e0 = rank * P.ns;
-  const int n_loc = max(0, min(V, e0 + P.ns) - e0);
-  const int n_grp = (n_loc + 7) >> 3;
-  TT *st = reinterpret_cast<TT *>(smem);
-  TD *sd = reinterpret_cast<TD *>(smem + align_up((size_t)P.ns * sizeof(TT), 128));
-  for (int e = n_loc + tid; e < n_grp * 8; e += kRowThreads) {   // pad the last group
-    st[e] = pad_value<TT>(false);
-    if (has_draft) sd[e] = pad_value<TD>(DK == 1);
-  }
-  bool timed_out = false;
-  if (P.aligned) {
-    if (tid == 0) {
-      mbar_init(&sh.bar, 1);
-      fence_mbarrier_init();
-      const uint32_t nb_t = (uint32_t)n_loc * sizeof(TT), nb_d = has_draft ? (uint32_t)n_loc * sizeof(TD) : 0u;
-      mbar_arrive_expect_tx(&sh.bar, nb_t + nb_d);
-      const uint8_t *gt = reinterpret_cast<const uint8_t *>(trow + e0);
-      for (uint32_t off = 0; off < nb_t; off += kChunkBytes)
-        bulk_g2s(reinterpret_cast<uint8_t *>(st) + off, gt + off, min(kChunkBytes, nb_t - off), &sh.bar);
-      if (has_draft) {
-        const uint8_t *gd = reinterpret_cast<const uint8_t *>(drow + e0);
-        for (uint32_t off = 0; off < nb_d; off += kChunkBytes)
-          bulk_g2s(reinterpret_cast<uint8_t *>(sd) + off, gd + off, min(kChunkBytes, nb_d - off), &sh.bar);
-      }
-    }
-    __syncthreads();   // the barrier is initialised before anyone waits on it
-    if (n_loc > 0 && !mbar_wait(&sh.bar, 0)) timed_out = true;
-  } else {
-    for (int e = tid; e < n_loc; e += kRowThreads) {
-      st[e] = trow[e0 + e];
-      if (has_draft) sd[e] = drow[e0 + e];
-    }
-    __syncthreads();
-  }
-  if (timed_out) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-
+  const int ngr = (V + 7) >> 3;
+  const int gs0 = min(ngr, rank * P.gpc), gs1 = min(ngr, gs0 + P.gpc);
+  const int nblk = (gs1 - gs0 + 31) >> 5;
+  const int bpw = (nblk + kRowWarps - 1) / kRowWarps;
+  const bool vec = P.aligned != 0;
   const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
   const float r_pq = q_logits ? S_p / S_q : S_p;
   const float v_u = P.uniforms[((int64_t)b * (K + 1) + n) * 2 + 1];
-  const float2 cc = make_float2(c, c);
-  const float2 nref = make_float2(-mcp, -mcq);
-  auto weight8 = [&](int g, float (&w)[8]) {
-    float xp[8];
-    load8(st, g, xp);
-    if (has_draft) {
-      float xq[8];
-      load8(sd, g, xq);
+  constexpr int kFly = sizeof(TT) == 4 || sizeof(TD) == 4 ? 2 : 4;   // blocks in flight per warp
+  for (int k0 = warp * bpw; k0 < min(nblk, (warp + 1) * bpw); k0 += kFly) {
+    Raw8<TT> rt[kFly];
+    Raw8<TD> rd[kFly];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float eq, ep;
-        if (DK == 0) {
-          const float2 y = __ffma2_rn(make_float2(xp[j], xq[j]), cc, nref);
-          ep = ex2(y.x);
-          eq = ex2(y.y);
-        } else {
-          ep = ex2(fmaf(xp[j], c, -mcp));
-          eq = xq[j];
-        }
-        w[j] = fmaxf(fmaf(-r_pq, eq, ep), 0.f);
-      }
-    } else {
-      const float2 np = make_float2(-mcp, -mcp);
-#pragma unroll
-      for (int j = 0; j < 8; j += 2) {
-        const float2 y = __ffma2_rn(make_float2(xp[j], xp[j + 1]), cc, np);
-        w[j] = ex2(y.x);
-        w[j + 1] = ex2(y.y);
+    for (int f = 0; f < kFly; ++f) {
+      const int g = gs0 + (k0 + f) * 32 + lane;
+      if (k0 + f < (warp + 1) * bpw && g < gs1) {
+        rt[f] = raw_load(trow, g, V, vec, false);
+        if (has_draft) rd[f] = raw_load(drow, g, V, vec, DK == 1);
       }
     }
-  };
-  auto sum8 = [](const float (&w)[8]) {
-    const float2 a = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
-    const float2 bb = __fadd2_rn(make_float2(w[4], w[5]), make_float2(w[6], w[7]));
-    const float2 t = __fadd2_rn(a, bb);
-    return t.x + t.y;
-  };
-  // warp `warp` owns groups [g_lo, g_hi); lane l owns the run
-  // [g_lo + l G, g_lo + (l+1) G) of it, visited in a lane-rotated order so
-  // the 16-byte shared-memory reads of a quarter warp hit distinct banks
-  const int gpw = (n_grp + kRowWarps - 1) / kRowWarps;
-  const int g_lo = min(n_grp, warp * gpw), g_hi = min(n_grp, g_lo + gpw);
-  const int G = (gpw + 31) >> 5;
-  const int r_lo = min(g_hi, g_lo + lane * G), r_hi = min(g_hi, r_lo + G);
-  float t_l = 0.f;
-  const int rot = G > 0 ? lane % G : 0;
-  for (int s = 0; s < G; ++s) {
-    int k = s + rot;
-    k = k >= G ? k - G : k;
-    const int g = r_lo + k;
-    if (g < r_hi) {
-      float w[8];
-      weight8(g, w);
-      t_l += sum8(w);
+#pragma unroll
+    for (int f = 0; f < kFly; ++f) {
+      const int k = k0 + f;
+      if (k >= min(nblk, (warp + 1) * bpw)) break;
+      float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (gs0 + k * 32 + lane < gs1) draw_weights8<TT, TD, DK>(rt[f], rd[f], has_draft, c, mcp, mcq, r_pq, w);
+      const float t = warp_sum_f(sum8f(w));
+      if (lane == 0) sh.btot[k] = t;
     }
   }
-  float incl = t_l;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) sh.wsum[warp] = incl;
   __syncthreads();
-  float tot_cta = 0.f;
-  for (int w = 0; w < kRowWarps; ++w) tot_cta += sh.wsum[w];
-  if (tid == 0) sh.pub_tot = tot_cta;
+  if (warp == 0) {   // warp totals (blocks in order), then the CTA's
+    float t = 0.f;
+    if (lane < kRowWarps)
+      for (int k = lane * bpw; k < min(nblk, (lane + 1) * bpw); ++k) t += sh.btot[k];
+    if (lane < kRowWarps) sh.wsum[lane] = t;
+    __syncwarp();
+    if (lane == 0) {
+      float tc = 0.f;
+      for (int w = 0; w < kRowWarps; ++w) tc += sh.wsum[w];
+      sh.pub_tot = tc;
+    }
+  }
   cluster_sync();   // masses published
+  const float tot_cta = sh.pub_tot;
   const float t_r = lane < cs ? ld_dsmem_f32(mapa(&sh.pub_tot, lane)) : 0.f;
   // the last distributed read of this launch is done: arrive now, wait at exit
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -825,54 +819,55 @@ __global__ void __launch_bounds__(kRowThreads) sample_draw_kernel(const __grid_c
     if (!draw_ok) { rec->y = -1; rec->gap = 0.f; rec->flags = acc_flags; push_pending(P, b, n); }
   }
   if (draw_ok && off_c <= thr && thr < off_c + tot_cta) {
-    float woff = 0.f, base = off_c;
-    int owner = kRowWarps - 1;
+    // the owner warp and block (prefixes in element order), the same in
+    // every thread of the CTA
+    float base = off_c;
+    int ow = kRowWarps - 1;
     for (int w = 0; w < kRowWarps; ++w) {
-      const float nxt = woff + sh.wsum[w];
-      if (thr < off_c + nxt || w == kRowWarps - 1) { owner = w; base = off_c + woff; break; }
-      woff = nxt;
+      if (thr < base + sh.wsum[w] || w == kRowWarps - 1) { ow = w; break; }
+      base += sh.wsum[w];
     }
-    if (warp == owner) {
-      // the lane whose run holds thr, then its groups rescanned in order
-      const unsigned hit = __ballot_sync(0xffffffffu, base + incl > thr);
+    const int kb0 = ow * bpw, kb1 = min(nblk, (ow + 1) * bpw);
+    int ob = max(kb0, kb1 - 1);
+    for (int k = kb0; k < kb1; ++k) {
+      if (thr < base + sh.btot[k] || k == kb1 - 1) { ob = k; break; }
+      base += sh.btot[k];
+    }
+    if (warp == ow) {
+      // rescan of block ob: lane sums, their prefix, then the crossing lane's
+      // eight elements in order
+      const int g = gs0 + ob * 32 + lane;
+      float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (ob < kb1 && g < gs1) {
+        Raw8<TT> rt = raw_load(trow, g, V, vec, false);
+        Raw8<TD> rd;
+        if (has_draft) rd = raw_load(drow, g, V, vec, DK == 1);
+        draw_weights8<TT, TD, DK>(rt, rd, has_draft, c, mcp, mcq, r_pq, w);
+      }
+      const float vs = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+      float inc2 = vs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, inc2, o);
+        if (lane >= o) inc2 += t;
+      }
+      const unsigned h2 = __ballot_sync(0xffffffffu, g < gs1 && base + inc2 > thr);
       int y = -1;
       float c_lo = 0.f, c_hi = 0.f;
-      if (hit) {
-        const int L = __ffs(hit) - 1;
-        float start = base + __shfl_sync(0xffffffffu, incl - t_l, L);
-        const int L_lo = __shfl_sync(0xffffffffu, r_lo, L), L_hi = __shfl_sync(0xffffffffu, r_hi, L);
-        for (int g0 = L_lo; g0 < L_hi && y < 0; g0 += 32) {   // one pass while G <= 32
-          const int g = g0 + lane;
-          float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          float vsum = 0.f;
-          if (g < L_hi) {
-            weight8(g, w);
-            vsum = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
-          }
-          float inc2 = vsum;
+      if (h2) {
+        const int L2 = __ffs(h2) - 1;
+        if (lane == L2) {
+          float run_c = base + (inc2 - vs);
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float t = __shfl_up_sync(0xffffffffu, inc2, o);
-            if (lane >= o) inc2 += t;
+          for (int j = 0; j < 8; ++j) {
+            const float nxt = run_c + w[j];
+            if (y < 0 && nxt > thr) { y = 8 * g + j; c_lo = run_c; c_hi = nxt; }
+            run_c = nxt;
           }
-          const unsigned h2 = __ballot_sync(0xffffffffu, g < L_hi && start + inc2 > thr);
-          if (h2) {
-            const int L2 = __ffs(h2) - 1;
-            if (lane == L2) {
-              float run_c = start + (inc2 - vsum);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float nxt = run_c + w[j];
-                if (y < 0 && nxt > thr) { y = e0 + 8 * g + j; c_lo = run_c; c_hi = nxt; }
-                run_c = nxt;
-              }
-            }
-            y = __shfl_sync(0xffffffffu, y, L2);
-            c_lo = __shfl_sync(0xffffffffu, c_lo, L2);
-            c_hi = __shfl_sync(0xffffffffu, c_hi, L2);
-          }
-          start += __shfl_sync(0xffffffffu, inc2, 31);
         }
+        y = __shfl_sync(0xffffffffu, y, L2);
+        c_lo = __shfl_sync(0xffffffffu, c_lo, L2);
+        c_hi = __shfl_sync(0xffffffffu, c_hi, L2);
       }
       if (lane == 0) {
         const bool found = y >= 0 && y < V;   // else: rounding moved the crossing
@@ -1547,15 +1542,12 @@ void split_ff(double d, float &hi, float &lo) {
 
 
 template <typename TT, int DK>
-sv_status launch_sample(const SampleParams &P, int cs, size_t smem, cudaStream_t s) {
+sv_status launch_sample(const SampleParams &P, int cs, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int fin_blocks = 0;
   std::call_once(once, [] {
-    const int lim = (int)(kMaxSliceSmem + 1024);
-    attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     int per_sm = 0;
     if (attr_err == cudaSuccess)
       attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_finish_kernel<TT, DK>, kFinThreads, 0);
@@ -1567,7 +1559,7 @@ sv_status launch_sample(const SampleParams &P, int cs, size_t smem, cudaStream_t
   if (fin_blocks < 1) return fail(SV_ERR_CUDA, "spec_verify_sample: the finish grid does not fit on the device");
   cudaError_t e = launch_k(sample_stats_kernel<TT, DK>, dim3(P.nc, P.K + 1, P.B), dim3(kStatThreads), 0, s, 1, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample statistics launch: %s", cudaGetErrorString(e));
-  e = launch_k(sample_draw_kernel<TT, DK>, dim3(cs, P.B), dim3(kRowThreads), smem, s, cs, P);
+  e = launch_k(sample_draw_kernel<TT, DK>, dim3(cs, P.B), dim3(kRowThreads), 0, s, cs, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample draw launch: %s", cudaGetErrorString(e));
   e = launch_coop(sample_finish_kernel<TT, DK>, fin_blocks, s, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
@@ -1616,28 +1608,16 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   if (B == 0) return ok();
 
   const int es_t = dtype_bytes(logit_dtype);
-  int cs = 0;
-  int ns = 0;
-  size_t smem = 0;
-  // rows kernel: the smallest cluster whose slices take <= 64 KB (three CTAs
-  // per SM), else the smallest that fits at all
   const int es_buf_d = (draft_is_probs && K > 0) ? 4 : es_t;
-  auto slice_smem = [&](int c, int &n) {
-    n = (int)align_up((size_t)((V + c - 1) / c), 8);
-    return align_up((size_t)n * es_t, 128) + align_up((size_t)n * es_buf_d, 128);
-  };
-  for (int c = 1; c <= 16 && !cs; c *= 2) {
-    int n;
-    const size_t sm = slice_smem(c, n);
-    if (sm <= kTargetSliceSmem) { cs = c; ns = n; smem = sm; }
-  }
-  if (!cs) {
-    int n;
-    const size_t sm = slice_smem(16, n);
-    if (sm <= kMaxSliceSmem) { cs = 16; ns = n; smem = sm; }
-  }
-  // finish kernel: 16-CTA clusters (8 for small vocabularies)
-  if (!cs) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large", V);
+  // draw kernel: the smallest cluster (up to 16 CTAs) whose slices take at
+  // most eight groups of eight elements per thread
+  const int ngr = (V + 7) / 8;
+  int cs = 1;
+  while (cs < 16 && (ngr + cs - 1) / cs > 8 * kRowThreads) cs *= 2;
+  const int gpc = (ngr + cs - 1) / cs;
+  if (gpc > kMaxDrawBlocks * 32)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large (at most %d)", V,
+                16 * kMaxDrawBlocks * 32 * 8);
 
   SampleParams P = {};
   P.target = target_logits; P.draft = draft; P.tokens = draft_tokens; P.uniforms = uniforms;
@@ -1653,7 +1633,7 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
     P.fin_last = reinterpret_cast<int *>(fin + kFinSyncBytes + kFinSumBytes + kFinTotBytes);
     P.pend = reinterpret_cast<int2 *>(fin + kFinScratchBytes);
   }
-  P.B = B; P.K = K; P.V = V; P.ns = ns; P.flags = flags;
+  P.B = B; P.K = K; P.V = V; P.gpc = gpc; P.flags = flags;
   P.aligned = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0 &&
               (K == 0 || (aligned(draft, 16) && ((size_t)V * es_buf_d) % 16 == 0));
   const double log2e = 1.4426950408889634074, ln2 = 0.69314718055994530942;
@@ -1667,12 +1647,9 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool probs = draft_is_probs && K > 0;
   switch (logit_dtype) {
-    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, smem, s) : launch_sample<float, 0>(P, cs, smem, s);
-    case SV_BF16:
-      return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, smem, s)
-                   : launch_sample<__nv_bfloat16, 0>(P, cs, smem, s);
-    default:
-      return probs ? launch_sample<__half, 1>(P, cs, smem, s) : launch_sample<__half, 0>(P, cs, smem, s);
+    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, s) : launch_sample<float, 0>(P, cs, s);
+    case SV_BF16: return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, s) : launch_sample<__nv_bfloat16, 0>(P, cs, s);
+    default: return probs ? launch_sample<__half, 1>(P, cs, s) : launch_sample<__half, 0>(P, cs, s);
   }
 }
 
