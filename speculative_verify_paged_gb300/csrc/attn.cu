@@ -139,6 +139,7 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   const int32_t *seq_lens;
   float *ws_acc;   // [B][H_kv][S][R][kD]
   float *ws_ml;    // [B][H_kv][S][R][2]
+  const int32_t *order;   // work items s + S (g + H_kv b), longest first (tcgen05 kernel)
   int32_t *status;
   int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
   int role[3];        // tensor-map dims 1..3 hold (0 = slot, 1 = kv head, 2 = block)
@@ -713,6 +714,48 @@ __device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile 
   return false;
 }
 
+// Longest-first order of the tcgen05 kernel's work items. A work item is
+// split s of kv head g of sequence b; its work is its number of 32-key
+// tiles. One CTA counting-sorts the (s, b) pairs by descending work (kv heads
+// innermost; empty splits, and sequences with invalid lengths, last). The
+// order within a bucket is that of the atomics: each item is still computed
+// once, and its result does not depend on when.
+constexpr int kOrdThreads = 1024;
+constexpr int kOrdMaxTiles = 1024;
+__global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *seq_lens, int B, int S, int H_kv,
+                                                                 int bps, int n_new, int max_blocks, int32_t *order) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int cur[kOrdMaxTiles + 1];
+  const int T = min(kOrdMaxTiles, (bps + kT5Blk - 1) / kT5Blk);
+  const int npairs = S * B;
+  auto work = [&](int p) {
+    const int sp = p % S, bp = p / S;
+    const int L = seq_lens[bp];
+    if (L < n_new || L > max_blocks * kBS) return 0;
+    const int blk = min(bps, (L + kBS - 1) / kBS - sp * bps);
+    return blk > 0 ? min(T, (blk + kT5Blk - 1) / kT5Blk) : 0;
+  };
+  for (int w = threadIdx.x; w <= T; w += blockDim.x) cur[w] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) atomicAdd(&cur[work(p)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {   // bucket starts, the most work first
+    int acc = 0;
+    for (int w = T; w >= 0; --w) {
+      const int c = cur[w];
+      cur[w] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    const int pos = atomicAdd(&cur[work(p)], 1);
+    const int sp = p % S, bp = p / S;
+    for (int gg = 0; gg < H_kv; ++gg) order[(int64_t)pos * H_kv + gg] = sp + S * (gg + H_kv * bp);
+  }
+}
+
 template <int QR>
 __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
   pdl_wait();
@@ -726,7 +769,11 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // the work item: split s of kv head g of sequence b, in the longest-first
+  // order the order kernel wrote (the CTAs launched first take the longest
+  // splits, so the last wave is made of the shortest ones)
+  const int item = __ldg(P.order + blockIdx.x);
+  const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *q_smem = smem;
@@ -1407,9 +1454,11 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
   return p;
 }
 
+// split partials (acc, then m and l), then the tcgen05 kernel's work order
 size_t ws_bytes(const Plan &p, int B, int H_kv) {
   const size_t ent = (size_t)B * H_kv * p.S * p.per_split * p.R;
-  return align_up(ent * p.d * sizeof(float), 256) + align_up(ent * 2 * sizeof(float), 256);
+  return align_up(ent * p.d * sizeof(float), 256) + align_up(ent * 2 * sizeof(float), 256) +
+         align_up((size_t)B * H_kv * p.S * sizeof(int32_t), 256);
 }
 
 template <int RT, bool FP8>
@@ -1437,8 +1486,11 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  dim3 grid(P.S, P.H_kv, P.B);
-  launch_k(attn_tc5_kernel<QR>, grid, dim3(kT5Threads), T5Cfg<QR>::kSmem, st, 1, P);
+  launch_k(attn_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, 1, P.seq_lens, P.B, P.S, P.H_kv, P.bps, P.n_new,
+           P.max_blocks, const_cast<int32_t *>(P.order));
+  sv_status rc = check_launch("spec_verify_attn order launch");
+  if (rc != SV_OK) return rc;
+  launch_k(attn_tc5_kernel<QR>, dim3(P.S * P.H_kv * P.B), dim3(kT5Threads), T5Cfg<QR>::kSmem, st, 1, P);
   return check_launch("spec_verify_attn tcgen05 launch");
 }
 
@@ -1558,6 +1610,8 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     }
     P.q = q; P.out = out; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
     P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
+    P.order = reinterpret_cast<const int32_t *>(reinterpret_cast<uint8_t *>(ws_ml) +
+                                                align_up(ent * 2 * sizeof(float), 256));
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
     P.scale_log2 = scale_log2;
