@@ -720,13 +720,20 @@ __device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile 
 // innermost; empty splits, and sequences with invalid lengths, last). The
 // order within a bucket is that of the atomics: each item is still computed
 // once, and its result does not depend on when.
+// It reads only seq_lens and writes only its own part of the workspace, so
+// it runs while the previous kernel of the stream is still running (that
+// kernel passed its own wait, so everything before it has completed; the
+// library's kernels never write seq_lens). It waits for that kernel at its
+// end, so the attention kernel's wait on this one still covers, for
+// example, the K/V rows the append kernel writes.
 constexpr int kOrdThreads = 1024;
-constexpr int kOrdMaxTiles = 1024;
+constexpr int kOrdMaxTiles = 1023;   // buckets 0..kOrdMaxTiles
+constexpr int kOrdPairs = 4;         // (s, b) pairs a thread keeps in registers
 __global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *seq_lens, int B, int S, int H_kv,
                                                                  int bps, int n_new, int max_blocks, int32_t *order) {
-  pdl_wait();
   pdl_trigger();
   __shared__ int cur[kOrdMaxTiles + 1];
+  const int tid = threadIdx.x, lane = tid & 31;
   const int T = min(kOrdMaxTiles, (bps + kT5Blk - 1) / kT5Blk);
   const int npairs = S * B;
   auto work = [&](int p) {
@@ -736,24 +743,51 @@ __global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *
     const int blk = min(bps, (L + kBS - 1) / kBS - sp * bps);
     return blk > 0 ? min(T, (blk + kT5Blk - 1) / kT5Blk) : 0;
   };
-  for (int w = threadIdx.x; w <= T; w += blockDim.x) cur[w] = 0;
+  for (int w = tid; w <= T; w += kOrdThreads) cur[w] = 0;
+  // the first kOrdPairs pairs of this thread keep their work in registers
+  int wk[kOrdPairs];
+#pragma unroll
+  for (int k = 0; k < kOrdPairs; ++k) {
+    const int p = tid + k * kOrdThreads;
+    wk[k] = p < npairs ? work(p) : 0;
+  }
   __syncthreads();
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) atomicAdd(&cur[work(p)], 1);
+#pragma unroll
+  for (int k = 0; k < kOrdPairs; ++k)
+    if (tid + k * kOrdThreads < npairs) atomicAdd(&cur[wk[k]], 1);
+  for (int p = tid + kOrdPairs * kOrdThreads; p < npairs; p += kOrdThreads) atomicAdd(&cur[work(p)], 1);
   __syncthreads();
-  if (threadIdx.x == 0) {   // bucket starts, the most work first
-    int acc = 0;
-    for (int w = T; w >= 0; --w) {
+  if (tid < 32) {
+    // bucket starts, the most work first: lane l takes buckets
+    // [T - (l+1) per + 1, T - l per] in descending order
+    const int per = (T + 1 + 31) / 32;
+    const int hi = T - lane * per, lo = max(0, hi - per + 1);
+    int sum = 0;
+    for (int w = hi; w >= lo; --w) sum += cur[w];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int acc = incl - sum;
+    for (int w = hi; w >= lo; --w) {
       const int c = cur[w];
       cur[w] = acc;
       acc += c;
     }
   }
   __syncthreads();
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int pos = atomicAdd(&cur[work(p)], 1);
+  auto place = [&](int p, int w) {
+    const int pos = atomicAdd(&cur[w], 1);
     const int sp = p % S, bp = p / S;
     for (int gg = 0; gg < H_kv; ++gg) order[(int64_t)pos * H_kv + gg] = sp + S * (gg + H_kv * bp);
-  }
+  };
+#pragma unroll
+  for (int k = 0; k < kOrdPairs; ++k)
+    if (tid + k * kOrdThreads < npairs) place(tid + k * kOrdThreads, wk[k]);
+  for (int p = tid + kOrdPairs * kOrdThreads; p < npairs; p += kOrdThreads) place(p, work(p));
+  pdl_wait();
 }
 
 template <int QR>
@@ -1438,8 +1472,10 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
     p.bps = bps_req;
   } else if (p.tc && kv == SV_BF16) {
     // tcgen05 kernel: long splits amortise its per-CTA setup (TMEM, Q,
-    // pipeline fill); at least one split per SM when the batch is small
-    p.bps = std::min(128, std::max(16, pow2_floor((int64_t)max_blocks * B * H_kv / num_sms())));
+    // pipeline fill) and the merge; at least one split per SM when the batch
+    // is small. The longest-first order keeps the last wave short, so
+    // splits of up to 256 blocks pay off.
+    p.bps = std::min(256, std::max(16, pow2_floor((int64_t)max_blocks * B * H_kv / num_sms())));
   } else {
     // fp32 caches are planned like bf16 ones so every dtype fits the same
     // workspace
