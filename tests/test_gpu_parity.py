@@ -136,6 +136,22 @@ def test_attention_split_count_invariance(lib, bps, kv):
     assert (out.float() - base.float()).abs().max().item() <= tol
 
 
+def test_attention_four_splits_repeated_calls(lib):
+    # four splits per sequence (partials merged by the merge kernel) and the
+    # longest-first work order, with one workspace reused across calls: every
+    # call gives the same result
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128, ctx=("fixed", (61, 250)))
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=11))
+    ref = oracle_attention(cfg, a)
+    nblk = a["block_table"].shape[1]
+    ws = lib.alloc_workspace(lib.attn_workspace_size(cfg.B, cfg.n_new, cfg.H_q, cfg.H_kv, cfg.d_head, nblk,
+                                                     block_size=cfg.block_size, blocks_per_split=4), DEV)
+    outs = [run_attention(lib, cfg, a, blocks_per_split=4, workspace=ws) for _ in range(3)]
+    for out in outs:
+        check_attention(out, ref, cfg)
+        assert torch.equal(out, outs[0])
+
+
 def test_attention_block_permutation_and_garbage_invariance(lib):
     cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128,
                                           ctx=("fixed", (45, 130)), spare_blocks=6)
