@@ -193,10 +193,12 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
 }
 
 // --------------------------------------------- programmatic launches ---
-// Every kernel of the library starts with pdl_wait() (the grids before it
-// in the stream have completed and their memory is visible) and then
-// pdl_trigger(), so the next launch of the stream may be scheduled while
-// this grid drains. Nothing touches global memory before pdl_wait().
+// pdl_wait(): the grids before this one in the stream have completed and
+// their memory is visible. pdl_trigger(): the next launch of the stream may
+// be scheduled while this grid drains. Kernels call both first, except where
+// a kernel reads only inputs no kernel of the library writes (lengths, block
+// table, new K/V rows, logits): those loads may come before the wait, and
+// every write still comes after it.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
