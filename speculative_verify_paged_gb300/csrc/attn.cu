@@ -599,11 +599,12 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
 // CTA = (split s, kv head g, sequence b), 256 threads:
 //   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
 //              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
+//              and first writes that row of Q into TMEM
 //   warps 4, 5 TMA producers (one lane each, in separate warps so that neither
-//              waits behind the other's barrier): warp 4 copies Q and streams
-//              K tiles, warp 5 streams V tiles, each into its own shared-
-//              memory ring (a K stage is free again as soon as its Q K^T has
-//              run, a V stage after its P V)
+//              waits behind the other's barrier): warp 4 streams K tiles,
+//              warp 5 V tiles, each into its own shared-memory ring (a K
+//              stage is free again as soon as its Q K^T has run, a V stage
+//              after its P V)
 //   warp 6     TMEM owner; lane 0 issues the MMAs from a polling loop, so
 //              Q K^T runs ahead whenever K data and an S buffer are ready.
 //              It sits on the third scheduler (warp id % 4 = 2), away from
@@ -616,28 +617,31 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
 //   O   += P V              (M=128, N=128 head dims, K=16 keys per MMA)
 // Each buffer has its own "P V done" barrier, so every wait is at most one
 // phase behind its barrier.
-// Shared-memory operands use the 128-byte swizzle: Q and K are K-major
-// (head dim contiguous), V is MN-major (head dim contiguous along N).
+// Q is the TMEM A operand of Q K^T (bf16 pairs along the head dim, one
+// query row per lane, written by the softmax warps). Shared-memory operands
+// use the 128-byte swizzle: K is K-major (head dim contiguous), V is MN-major
+// (head dim contiguous along N).
 constexpr int kT5Blk = 2;                      // blocks per tile
 constexpr int kT5N = 16 * kT5Blk;              // keys per tile
-constexpr int kT5SBuf = 4;                     // S / P buffers in TMEM
+constexpr int kT5SBuf = 2;                     // S / P buffers in TMEM
 constexpr int kT5Threads = 256;
 constexpr int kT5MmaWarp = 6;
 constexpr int kT5MaxR = 128;
 constexpr int kT5HalfBytes = kT5Blk * 2048;    // one head-dim half of K (or V) for a tile
 constexpr int kT5TileBytes = 2 * kT5HalfBytes; // K (or V) of one tile
-// Q staging: 64 rows serve R <= 64 (the MMA's rows 64-127 then read other
-// shared memory; those rows of S, P and O are never used), else 128. The
-// rings take what two CTAs per SM leave.
+// Q lives in TMEM (the A operand of Q K^T, like P for P V), so the rings take
+// all the shared memory two CTAs per SM leave. QR is the number of query rows
+// the softmax warps write (64 when R <= 64: rows 64-127 of S, P and O are
+// never used).
 template <int QR> struct T5Cfg {
-  static constexpr int kQBytes = 2 * QR * 128;
-  static constexpr int kKS = QR == 64 ? 6 : 5;   // K stages
-  static constexpr int kVS = QR == 64 ? 5 : 4;   // V stages
-  static constexpr int kSmem = 1024 + kQBytes + (kKS + kVS) * kT5TileBytes;
+  static constexpr int kKS = 7;   // K stages
+  static constexpr int kVS = 6;   // V stages
+  static constexpr int kSmem = 1024 + (kKS + kVS) * kT5TileBytes;
 };
-constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O
+constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O, Q
 constexpr uint32_t kT5OCol = kT5SBuf * kT5N;
-static_assert(kT5OCol + 128 <= kT5Cols, "TMEM budget");
+constexpr uint32_t kT5QCol = kT5OCol + 128;    // Q: 64 columns of bf16 pairs (d 2c, 2c+1)
+static_assert(kT5QCol + 64 <= kT5Cols, "TMEM budget");
 
 __device__ __forceinline__ uint64_t t5_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -796,7 +800,6 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
   pdl_trigger();
   using Cfg = T5Cfg<QR>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
-  constexpr int kQHalf = QR * 128;   // bytes of one head-dim half of Q
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
@@ -810,8 +813,7 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
   const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *q_smem = smem;
-  const uint32_t k_ring = smem_u32(smem) + Cfg::kQBytes;
+  const uint32_t k_ring = smem_u32(smem);
   const uint32_t v_ring = k_ring + KS * kT5TileBytes;
 
   const int L = P.seq_lens[b];
@@ -842,7 +844,7 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
       mbar_init(&o_done[k], 1);
     }
     mbar_init(&mma_drain, 1);
-    mbar_init(&q_full, 1);
+    mbar_init(&q_full, 4);   // the four softmax warps wrote their Q rows
     abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -851,13 +853,7 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
 
   if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ producers --
-    // lane 0 copies Q (rows past R are left as they are: their rows of S,
-    // P and O are never read) and then streams K; lane 1 streams V
-    if (warp == 4 && lane == 0) {
-      mbar_arrive_expect_tx(&q_full, (uint32_t)(2 * R * 128));
-      for (int h = 0; h < 2; ++h)
-        tma_load_4d(smem_u32(q_smem) + h * kQHalf, &P.tmq, h * 64, g * P.G, 0, b, &q_full);
-    }
+    // warp 4 streams K, warp 5 streams V
     {
       // the whole warp walks the block table 32 entries at a time (the next
       // 32 prefetched); lane 0 waits for free stages and issues the copies
@@ -912,7 +908,6 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
       if (lane == 0) {
         for (int t = max(0, issued - NS); t < issued; ++t)
           if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-        if (!isv && !mbar_wait(&q_full, 0)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
       }
     }
   } else if (warp < 4 || warp == kT5MmaWarp) {
@@ -932,7 +927,6 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
         const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (16u << 17) | (8u << 24);
         static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
-        const uint32_t qa = smem_u32(q_smem);
         int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
         bool q_ready = false;
         uint64_t t_last = global_ns();
@@ -947,8 +941,8 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
               t5_fence_after();
               const uint32_t kb = k_ring + ks * kT5TileBytes;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                t5_mma_ss(tb + sb * kT5N, t5_desc(qa + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+              for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
+                t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
                           t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
                           kk > 0 ? 1u : 0u);
               t5_commit(&s_full[sb]);
@@ -995,6 +989,40 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
       const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
       const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
       const float sl2 = P.scale_log2;
+      {
+        // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
+        // order). tcgen05.st is warp-collective: a warp holding live rows
+        // stores all 32 (zeros for rows past R); warps with none skip it
+        // (their rows of S, P and O are never read).
+        if (warp_live) {
+          uint4 qv[16];
+          if (live) {
+            const int j = row / P.G, hh = row % P.G;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                               (((int64_t)b * P.n_new + j) * P.H_q +
+                                                                (int64_t)g * P.G + hh) * kD);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < 4; ++c0) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
+              w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
+            }
+            t5_st16(lane_base + kT5QCol + 16 * c0, w);
+          }
+          t5_wait_st();
+        }
+        t5_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
+      }
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
