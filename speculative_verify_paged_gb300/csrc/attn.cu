@@ -1342,6 +1342,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
   const int64_t rowid = (int64_t)blockIdx.x * (8 / WPR) + warp / WPR;
   const int R = P.R;
   const bool live = rowid < (int64_t)P.B * P.H_kv * R;
+
   int nsplit = 0, r = 0, g = 0, b = 0;
   int64_t bg = 0;
   if (live) {
@@ -1430,8 +1431,84 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
   }
 }
 
+// Split merge for at most four splits: one CTA per (sequence, kv head). The
+// length is read once and a sequence with a single split (written by the
+// attention kernel) leaves at once; otherwise each warp merges a row (warp w
+// takes rows w, w + warps, ...), its splits loaded together in one round
+// trip.
+template <typename TO>
+__global__ void __launch_bounds__(1024) attn_merge_pair_kernel(const __grid_constant__ MergeParams P) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kMaxChunks = 2;   // d <= 256
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t bg = blockIdx.x;
+  const int g = (int)(bg % P.H_kv), b = (int)(bg / P.H_kv);
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * P.bs) return;
+  const int nsplit = ((L + P.bs - 1) / P.bs + P.bps - 1) / P.bps;
+  if (nsplit <= 1) return;
+  const int R = P.R, nc = P.d >> 2;
+  for (int r = warp; r < R; r += (int)(blockDim.x >> 5)) {
+    float me[4], le[4];
+    float4 va[4][kMaxChunks];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      me[e] = -INFINITY;
+      le[e] = 0.f;
+      if (e < nsplit) {
+        const int64_t row = (bg * P.S + e) * R + r;
+        me[e] = P.ws_ml[row * 2];
+        le[e] = P.ws_ml[row * 2 + 1];
+        const float4 *src = reinterpret_cast<const float4 *>(P.ws_acc + row * P.d);
+#pragma unroll
+        for (int k = 0; k < kMaxChunks; ++k)
+          if (lane + 32 * k < nc) va[e][k] = src[lane + 32 * k];
+      }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < nsplit) m = fmaxf(m, me[e]);
+    const float base = m == -INFINITY ? 0.f : m;
+    float l = 0.f, w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      w[e] = e < nsplit ? exp2f(me[e] - base) : 0.f;
+      l += e < nsplit ? le[e] * w[e] : 0.f;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int j = r / P.G, hh = r % P.G;
+    const int64_t out_off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * P.d;
+#pragma unroll
+    for (int k = 0; k < kMaxChunks; ++k) {
+      const int cidx = lane + 32 * k;
+      if (cidx >= nc) continue;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (e >= nsplit) continue;
+        v.x += va[e][k].x * w[e]; v.y += va[e][k].y * w[e];
+        v.z += va[e][k].z * w[e]; v.w += va[e][k].w * w[e];
+      }
+      if constexpr (std::is_same<TO, float>::value) {
+        reinterpret_cast<float4 *>(static_cast<float *>(P.out) + out_off)[cidx] =
+            make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+      } else {
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(P.out) + out_off + 4 * cidx;
+        *reinterpret_cast<__nv_bfloat162 *>(o) = __floats2bfloat162_rn(v.x * inv, v.y * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(o + 2) = __floats2bfloat162_rn(v.z * inv, v.w * inv);
+      }
+    }
+  }
+}
+
 template <typename TO>
 void launch_merge(const MergeParams &M, int64_t rows, cudaStream_t st) {
+  if (M.S <= 4) {
+    launch_k(attn_merge_pair_kernel<TO>, dim3((unsigned)(M.B * M.H_kv)), dim3(32 * std::min(32, M.R)), 0, st, 1, M);
+    return;
+  }
   // more warps per row when there are many splits
   const int wpr = M.S >= 64 ? 8 : (M.S >= 16 ? 4 : (M.S >= 8 ? 2 : 1));
   const unsigned nb = (unsigned)((rows * wpr + 7) / 8);
