@@ -6,8 +6,9 @@ fused rejection sampling) on the LLaMA-3-70B layer-shaped workload.
 
 Prints ONE JSON line on rank 0. `value` is verify steps/s of the whole job
 (inputs resident in HBM); `e2e` is the same metric through the public API with
-the step's inputs copied from pinned host memory and the outputs read back
-inside the timed region. The reference arm (`--impl reference`) times the CPU
+every step's inputs copied from pinned host memory and its outputs read back
+inside the timed region (two device copies of the inputs: a step's copy, on
+its own stream, overlaps the previous step's compute). The reference arm (`--impl reference`) times the CPU
 oracle on a bounded sample of the same workload and scales it to steps/s.
 Multi-GPU runs are independent replicas (one batch per GPU, no collective).
 """
@@ -311,28 +312,39 @@ def run_ours(args, rank, world, local):
             {"q": a["q"], "k_new": n["k_new"], "v_new": n["v_new"], "target_logits": s["target_logits"],
              "draft_logits": s["draft_logits"], "draft_tokens": s["draft_tokens"],
              "uniforms": s["uniforms"], "seq_lens": a["seq_lens"], "block_table": a["block_table"]}.items()}
-    devbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    # two device copies of the inputs: step i's copy (on its own stream)
+    # overlaps step i-1's compute, and waits until step i-2 released the copy
+    devbufs = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)   # (a second copy stream gained nothing: the link is the limit)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    released = [torch.cuda.Event() for _ in range(2)]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     toks_h = torch.empty(toks.shape, dtype=toks.dtype).pin_memory()
     nacc_h = torch.empty(nacc.shape, dtype=nacc.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(x.numel() * x.element_size() for x in (out_h, toks_h, nacc_h))
 
-    def e2e_step():
-        for k, v in host.items():
-            devbuf[k].copy_(v, non_blocking=True)
+    def e2e_step(i):
+        devbuf = devbufs[i % 2]
+        copy_stream.wait_event(released[i % 2])
+        with torch.cuda.stream(copy_stream):
+            for k, v in host.items():
+                devbuf[k].copy_(v, non_blocking=True)
+        copied[i % 2].record(copy_stream)
+        stream.wait_event(copied[i % 2])
         o, tk, na = sv.verify_step(devbuf["q"], devbuf["k_new"], devbuf["v_new"], k_cache, v_cache,
                                    devbuf["block_table"], devbuf["seq_lens"], devbuf["target_logits"],
                                    devbuf["draft_logits"], devbuf["draft_tokens"], devbuf["uniforms"],
                                    a["k_scale"], a["v_scale"], attn_out=out, attn_workspace=attn_ws,
                                    sample_workspace=samp_ws, status=status)
+        released[i % 2].record(stream)
         out_h.copy_(o, non_blocking=True)
         toks_h.copy_(tk, non_blocking=True)
         nacc_h.copy_(na, non_blocking=True)
 
     e2e_steps = 0 if args.no_e2e else max(5, args.steps // 2)
-    for _ in range(3 if e2e_steps else 0):
-        e2e_step()
+    for i in range(3 if e2e_steps else 0):
+        e2e_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -340,8 +352,9 @@ def run_ours(args, rank, world, local):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    copy_stream.wait_event(e0)   # the first copy starts inside the timed region
+    for i in range(e2e_steps):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
