@@ -74,7 +74,8 @@ typedef enum {
   SV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype, d_head)  */
   SV_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than required    */
   SV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed       */
-  SV_ERR_TIMEOUT = 5        /* a bounded device wait ran out              */
+  SV_ERR_TIMEOUT = 5,       /* a bounded device wait ran out              */
+  SV_ERR_OUT_OF_BLOCKS = 6  /* the block manager has too few free pages   */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1, SV_F16 = 2, SV_FP8_E4M3 = 3 } sv_dtype;
@@ -258,6 +259,107 @@ sv_status spec_verify_sample_static(const void *target_logits, sv_dtype logit_dt
                                     int32_t *out_tokens, int32_t *num_accepted,
                                     float *p_at_draft, float *q_at_draft,
                                     int32_t *dev_status, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Host block manager of the paged cache ("KV Cache + Speculative Decoding",
+ * section 6.2, PagedKVCache: a free list used as a stack, one reference count
+ * per physical page, one block table per sequence, copy-on-write on a write
+ * to a shared page, share_prefix over whole pages; "KV Cache" section 3.3,
+ * PagedAttention.fork). Pure host code: no call touches the GPU, allocates
+ * device memory or needs CUDA. One manager per paged pool; a manager is not
+ * thread-safe (serialise the calls on one manager).
+ *
+ * Sequences are named by caller-chosen int64 ids and record their length in
+ * tokens; a sequence of length L owns exactly ceil(L / page_size) pages.
+ * Free pages are handed out from the end of the free list and released pages
+ * go back on its end (sv_bm_free_list lists it bottom to top). A call that
+ * fails (SV_ERR_INVALID_ARG for a bad id or size, SV_ERR_OUT_OF_BLOCKS when
+ * the pool is too small) changes nothing, also for a batch of sequences.
+ *
+ * A verify round with the kernels above:
+ *   1. sv_bm_extend(ids, n_new = K+1): pages for the K+1 new rows; run the
+ *      returned copy-on-write pairs with sv_copy_blocks over every pool
+ *      (every layer's K and V) before anything writes those pages;
+ *   2. sv_bm_block_table(ids) -> block_table / seq_lens for kv_block_append,
+ *      spec_verify_attn (seq_lens then count the K+1 new rows);
+ *   3. after spec_verify_sample, sv_bm_commit_verify(ids, K+1, num_accepted)
+ *      with num_accepted copied to the host: each length becomes
+ *      L - (K+1) + num_accepted + 1 (every token of the sequence but the
+ *      resampled or bonus one, which enters the cache as the first new row
+ *      of the next round), and pages past the new length are released.
+ * ------------------------------------------------------------------------ */
+typedef struct sv_block_manager sv_block_manager;
+
+/* A manager of pages 0 .. num_blocks-1 (all free, free list in ascending
+ * order) of page_size tokens; *out = NULL on failure. */
+sv_status sv_bm_create(int num_blocks, int page_size, sv_block_manager **out);
+void sv_bm_destroy(sv_block_manager *bm);                  /* NULL is a no-op */
+int sv_bm_num_free(const sv_block_manager *bm);            /* -1 if bm NULL   */
+int sv_bm_ref_count(const sv_block_manager *bm, int block); /* -1 out of range */
+/* Copies the free list, bottom to top, to out[0 .. *n-1]; *n is set even when
+ * cap is too small (then SV_ERR_INVALID_ARG). */
+sv_status sv_bm_free_list(const sv_block_manager *bm, int32_t *out, int cap, int *n);
+
+/* A new sequence of n_tokens tokens on ceil(n_tokens / page_size) fresh
+ * pages (count 1); its first page is the last entry of the free list. */
+sv_status sv_bm_allocate(sv_block_manager *bm, int64_t seq_id, int64_t n_tokens);
+/* Drops the sequence; its pages lose one reference each, in table order, and
+ * a page whose count reaches 0 goes back on the free list. */
+sv_status sv_bm_free(sv_block_manager *bm, int64_t seq_id);
+/* dst (a new id) shares every page of src and takes its length. */
+sv_status sv_bm_fork(sv_block_manager *bm, int64_t src, int64_t dst);
+/* dst (a new id) shares the first n_tokens / page_size (rounded down) pages
+ * of src and has length (n_tokens / page_size) * page_size;
+ * 0 <= n_tokens <= len(src). */
+sv_status sv_bm_share_prefix(sv_block_manager *bm, int64_t src, int64_t dst, int64_t n_tokens);
+
+/* Makes positions len .. len+n_new-1 of each listed sequence writable and
+ * adds n_new to each length, sequence by sequence in list order: a position
+ * past the table opens a fresh page; the first position written on a page
+ * whose count is above 1 moves this sequence's reference to a fresh page
+ * and records the pair (old, fresh) in cow_src[i], cow_dst[i]. The caller
+ * copies each old page onto its fresh page (sv_copy_blocks) before any
+ * write to the fresh page. At most one pair per sequence, so cow_src and
+ * cow_dst (host int32 arrays) need cow_cap >= n_seqs entries; *n_cow is the
+ * number written. No fresh page is the old page of another pair.
+ * seq_ids: host int64 [n_seqs], distinct. */
+sv_status sv_bm_extend(sv_block_manager *bm, const int64_t *seq_ids, int n_seqs, int n_new,
+                       int32_t *cow_src, int32_t *cow_dst, int cow_cap, int *n_cow);
+/* Rollback: the length becomes new_len (0 <= new_len <= len); pages past
+ * ceil(new_len / page_size) are released in table order as by sv_bm_free. */
+sv_status sv_bm_truncate(sv_block_manager *bm, int64_t seq_id, int64_t new_len);
+/* After a verify round that appended n_new = K+1 rows: truncates sequence i
+ * to len - n_new + num_accepted[i] + 1. num_accepted: host int32 [n_seqs],
+ * each in [0, n_new - 1]; every length must be >= n_new. */
+sv_status sv_bm_commit_verify(sv_block_manager *bm, const int64_t *seq_ids, int n_seqs, int n_new,
+                              const int32_t *num_accepted);
+sv_status sv_bm_seq_len(const sv_block_manager *bm, int64_t seq_id, int64_t *len);
+/* Writes the listed sequences' tables, row i = seq_ids[i], into the host
+ * int32 array table[n_seqs][max_blocks_per_seq] (entries past a sequence's
+ * pages = -1) and their lengths into the host int32 array seq_lens[n_seqs].
+ * SV_ERR_INVALID_ARG if a sequence holds more than max_blocks_per_seq pages
+ * or is longer than INT32_MAX. */
+sv_status sv_bm_block_table(const sv_block_manager *bm, const int64_t *seq_ids, int n_seqs,
+                            int max_blocks_per_seq, int32_t *table, int32_t *seq_lens);
+
+/* ------------------------------------------------------------------------ *
+ * sv_copy_blocks
+ *   The device half of copy-on-write: for every pool p and pair i, copies
+ *   block_bytes bytes from pools[p] + src[i] * block_stride_bytes to
+ *   pools[p] + dst[i] * block_stride_bytes. pools: HOST array of n_pools
+ *   device pointers (16-byte aligned), e.g. every layer's K and V pool with
+ *   block_bytes = H_kv * block_size * d_head * element size for the default
+ *   layout, or one pool of [pages][page_size][layers][2][H_kv][d_head] with
+ *   block_bytes = its page size in bytes. block_bytes and block_stride_bytes:
+ *   multiples of 16, stride >= bytes. src, dst: DEVICE int32 [n_pairs]; a
+ *   pair with an entry outside [0, num_blocks) is skipped and sets
+ *   SV_DEV_BAD_BLOCK in *dev_status. Pairs must not chain (no dst is also a
+ *   src), which holds for the pairs of one sv_bm_extend call. The copy waits
+ *   for the previous kernel of the stream (its pages may be the source).
+ * ------------------------------------------------------------------------ */
+sv_status sv_copy_blocks(void *const *pools, int n_pools, int64_t block_stride_bytes, int64_t block_bytes,
+                         const int32_t *src, const int32_t *dst, int n_pairs, int num_blocks,
+                         int32_t *dev_status, sv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -167,13 +167,15 @@ class PagedBlockManager:
         self.length[seq_id] = new_len
 
     def commit_verify(self, seq_ids, n_new, num_accepted):
+        if len(set(seq_ids)) != len(seq_ids):
+            raise ValueError("a sequence appears twice")
         targets = []
         for s, n in zip(seq_ids, num_accepted, strict=True):
             if n < 0 or n > n_new - 1:
                 raise ValueError("num_accepted outside [0, n_new - 1]")
+            if self.length[s] < n_new:
+                raise ValueError("sequence shorter than the n_new rows of the round")
             new_len = self.length[s] - n_new + n + 1
-            if new_len < 0:
-                raise ValueError("sequence shorter than n_new")
             targets.append((s, new_len))
         for s, new_len in targets:
             self.truncate(s, new_len)

@@ -11,6 +11,8 @@ Entry points (names follow the C ABI in include/specverify.h):
   spec_verify_attn    paged GQA verify attention over the K+1 queries
   spec_verify_sample  fused rejection sampling (accept / residual / bonus)
   verify_step         the three in stream order (one verify round of one layer)
+  BlockManager        host block manager of the paged pool (sv_bm_*)
+  copy_blocks         device page copies for copy-on-write (sv_copy_blocks)
 """
 import ctypes
 import math
@@ -27,7 +29,8 @@ SV_F32, SV_BF16, SV_F16, SV_FP8_E4M3 = 0, 1, 2, 3
 SV_SAMPLE_FORCE_EXACT = 1
 DEV_STATUS_BITS = {1: "BAD_SEQ_LEN", 2: "BAD_BLOCK", 4: "BAD_TOKEN", 8: "TIMEOUT", 16: "NONFINITE"}
 _STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
-           4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT"}
+           4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT", 6: "SV_ERR_OUT_OF_BLOCKS"}
+SV_ERR_OUT_OF_BLOCKS = 6
 
 _lib = None
 
@@ -36,6 +39,10 @@ class SpecVerifyError(RuntimeError):
     def __init__(self, status, msg):
         super().__init__("%s: %s" % (_STATUS.get(status, status), msg))
         self.status = status
+
+
+class OutOfBlocks(SpecVerifyError):
+    """The block manager's pool has too few free pages for the call."""
 
 
 class _Layout(ctypes.Structure):
@@ -76,13 +83,45 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_sample.argtypes = samp_args + [P]
     lib.spec_verify_sample_ex.restype = I
     lib.spec_verify_sample_ex.argtypes = samp_args + [U, P]
+    I64, BMP = ctypes.c_int64, ctypes.c_void_p
+    lib.sv_bm_create.restype = I
+    lib.sv_bm_create.argtypes = [I, I, ctypes.POINTER(ctypes.c_void_p)]
+    lib.sv_bm_destroy.restype = None
+    lib.sv_bm_destroy.argtypes = [BMP]
+    lib.sv_bm_num_free.restype = I
+    lib.sv_bm_num_free.argtypes = [BMP]
+    lib.sv_bm_ref_count.restype = I
+    lib.sv_bm_ref_count.argtypes = [BMP, I]
+    lib.sv_bm_free_list.restype = I
+    lib.sv_bm_free_list.argtypes = [BMP, P, I, ctypes.POINTER(I)]
+    lib.sv_bm_allocate.restype = I
+    lib.sv_bm_allocate.argtypes = [BMP, I64, I64]
+    lib.sv_bm_free.restype = I
+    lib.sv_bm_free.argtypes = [BMP, I64]
+    lib.sv_bm_fork.restype = I
+    lib.sv_bm_fork.argtypes = [BMP, I64, I64]
+    lib.sv_bm_share_prefix.restype = I
+    lib.sv_bm_share_prefix.argtypes = [BMP, I64, I64, I64]
+    lib.sv_bm_extend.restype = I
+    lib.sv_bm_extend.argtypes = [BMP, P, I, I, P, P, I, ctypes.POINTER(I)]
+    lib.sv_bm_truncate.restype = I
+    lib.sv_bm_truncate.argtypes = [BMP, I64, I64]
+    lib.sv_bm_commit_verify.restype = I
+    lib.sv_bm_commit_verify.argtypes = [BMP, P, I, I, P]
+    lib.sv_bm_seq_len.restype = I
+    lib.sv_bm_seq_len.argtypes = [BMP, I64, ctypes.POINTER(I64)]
+    lib.sv_bm_block_table.restype = I
+    lib.sv_bm_block_table.argtypes = [BMP, P, I, I, P, P]
+    lib.sv_copy_blocks.restype = I
+    lib.sv_copy_blocks.argtypes = [P, I, I64, I64, P, P, I, I, P, P]
     _lib = lib
     return lib
 
 
 def _check(rc):
     if rc != 0:
-        raise SpecVerifyError(rc, load_library().sv_last_error_string().decode())
+        cls = OutOfBlocks if rc == SV_ERR_OUT_OF_BLOCKS else SpecVerifyError
+        raise cls(rc, load_library().sv_last_error_string().decode())
 
 
 def _ptr(t):
@@ -256,6 +295,135 @@ def verify_step(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, target
                                           draft_is_probs, temperature, workspace=sample_workspace,
                                           status=status, want_probs=False)
     return out, toks, nacc
+
+
+# ------------------------------------------------------- block manager ---
+
+def _host_i64(xs):
+    a = (ctypes.c_int64 * max(len(xs), 1))(*[int(x) for x in xs])
+    return a, len(xs)
+
+
+class BlockManager:
+    """Host block manager of one paged pool (sv_bm_* in the library).
+
+    Pages 0 .. num_blocks-1 of page_size tokens; sequences are named by int
+    ids. Every method runs in the library's C++ code; errors raise
+    SpecVerifyError (OutOfBlocks when the pool is too small), and a failed
+    call changes nothing.
+    """
+
+    def __init__(self, num_blocks, page_size=16):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check(self._lib.sv_bm_create(int(num_blocks), int(page_size), ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = int(num_blocks)
+        self.page_size = int(page_size)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.sv_bm_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def num_free(self):
+        return int(self._lib.sv_bm_num_free(self._h))
+
+    def ref_count(self, block):
+        return int(self._lib.sv_bm_ref_count(self._h, int(block)))
+
+    def ref_counts(self):
+        return [self.ref_count(b) for b in range(self.num_blocks)]
+
+    def free_list(self):
+        out = (ctypes.c_int32 * self.num_blocks)()
+        n = ctypes.c_int()
+        _check(self._lib.sv_bm_free_list(self._h, out, self.num_blocks, ctypes.byref(n)))
+        return list(out[: n.value])
+
+    def allocate(self, seq_id, n_tokens):
+        _check(self._lib.sv_bm_allocate(self._h, int(seq_id), int(n_tokens)))
+
+    def free(self, seq_id):
+        _check(self._lib.sv_bm_free(self._h, int(seq_id)))
+
+    def fork(self, src, dst):
+        _check(self._lib.sv_bm_fork(self._h, int(src), int(dst)))
+
+    def share_prefix(self, src, dst, n_tokens):
+        _check(self._lib.sv_bm_share_prefix(self._h, int(src), int(dst), int(n_tokens)))
+
+    def extend(self, seq_ids, n_new):
+        """Pages for n_new more tokens of each sequence; returns the
+        copy-on-write pairs [(src_page, dst_page), ...]."""
+        ids, n = _host_i64(seq_ids)
+        cap = max(n, 1)
+        src, dst = (ctypes.c_int32 * cap)(), (ctypes.c_int32 * cap)()
+        nc = ctypes.c_int()
+        _check(self._lib.sv_bm_extend(self._h, ids, n, int(n_new), src, dst, cap, ctypes.byref(nc)))
+        return [(src[i], dst[i]) for i in range(nc.value)]
+
+    def truncate(self, seq_id, new_len):
+        _check(self._lib.sv_bm_truncate(self._h, int(seq_id), int(new_len)))
+
+    def commit_verify(self, seq_ids, n_new, num_accepted):
+        """Rollback after a verify round of n_new = K+1 rows; num_accepted is a
+        host sequence or tensor (a CUDA tensor is copied to the host)."""
+        if isinstance(num_accepted, torch.Tensor):
+            num_accepted = num_accepted.detach().cpu().tolist()
+        ids, n = _host_i64(seq_ids)
+        if len(num_accepted) != n:
+            raise ValueError("one num_accepted per sequence")
+        acc = (ctypes.c_int32 * max(n, 1))(*[int(a) for a in num_accepted])
+        _check(self._lib.sv_bm_commit_verify(self._h, ids, n, int(n_new), acc))
+
+    def seq_len(self, seq_id):
+        out = ctypes.c_int64()
+        _check(self._lib.sv_bm_seq_len(self._h, int(seq_id), ctypes.byref(out)))
+        return out.value
+
+    def block_table(self, seq_ids, max_blocks_per_seq, device=None):
+        """(block_table int32 [n, max_blocks_per_seq] padded with -1, seq_lens
+        int32 [n]) as CPU tensors, or copied to `device`."""
+        ids, n = _host_i64(seq_ids)
+        table = torch.empty((n, int(max_blocks_per_seq)), dtype=torch.int32)
+        lens = torch.empty((n,), dtype=torch.int32)
+        _check(self._lib.sv_bm_block_table(self._h, ids, n, int(max_blocks_per_seq),
+                                           ctypes.c_void_p(table.data_ptr()),
+                                           ctypes.c_void_p(lens.data_ptr())))
+        if device is not None:
+            table, lens = table.to(device), lens.to(device)
+        return table, lens
+
+
+def copy_blocks(pools, pairs, num_blocks, block_bytes=None, block_stride_bytes=None, status=None):
+    """Copy page src onto page dst of every pool for each (src, dst) pair.
+
+    pools: CUDA tensors whose first dimension is the page index (each page a
+    contiguous slice), e.g. every layer's K and V pool; block sizes default to
+    one page of pools[0]."""
+    if not pairs or not pools:
+        return
+    lib = load_library()
+    _cuda(*pools, status)
+    dev = pools[0].device
+    if block_stride_bytes is None:
+        block_stride_bytes = pools[0].stride(0) * pools[0].element_size()
+    if block_bytes is None:
+        block_bytes = block_stride_bytes
+    for p in pools:
+        if p.shape[0] < num_blocks or p.stride(0) * p.element_size() != block_stride_bytes:
+            raise ValueError("every pool needs num_blocks pages of block_stride_bytes")
+    pp = (ctypes.c_void_p * len(pools))(*[p.data_ptr() for p in pools])
+    idx = torch.tensor(pairs, dtype=torch.int32).reshape(-1, 2).t().contiguous().to(dev)
+    _check(lib.sv_copy_blocks(pp, len(pools), int(block_stride_bytes), int(block_bytes),
+                              _ptr(idx[0]), _ptr(idx[1]), idx.shape[1], int(num_blocks),
+                              _ptr(status), _stream()))
+    return idx
 
 
 def build(verbose=False, force=False):

@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^(?:const\s+)?(?:sv_status|size_t|char|void|unsigned long long)\s*\*?\s*(\w+)\s*\(",
+    names = re.findall(r"^(?:const\s+)?(?:sv_status|size_t|char|void|int|unsigned long long)\s*\*?\s*(\w+)\s*\(",
                        text, flags=re.M)
     return sorted(set(names))
 
