@@ -66,16 +66,66 @@ def inverse_cdf(weights, v):
     return y, np.abs(margin), Z
 
 
+def top_p_nucleus(logits, top_p, temperature=1.0):
+    """The top-p set of softmax(logits / T) of every row, and its margin.
+
+    "KV Cache + Speculative Decoding" section 7.5 and Q21: under top-p the
+    target distribution becomes p truncated to its own top-p set and
+    renormalised. Reading of the set: order the tokens by logit, largest
+    first, equal logits by ascending token id; the set is the shortest
+    prefix of that order whose probability reaches top_p (mass >= top_p).
+    top_p >= 1 keeps every token.
+
+    Returns (mask [..., V] bool, margin [...]) where margin is the distance
+    of top_p * Z from the cumulative masses on either side of the cut, as a
+    fraction of the row mass Z (inf when nothing is cut).
+    """
+    x = _np64(logits)
+    V = x.shape[-1]
+    rows = x.reshape(-1, V)
+    mask = np.zeros(rows.shape, dtype=bool)
+    margin = np.full(rows.shape[0], np.inf)
+    ids = np.arange(V)
+    for r in range(rows.shape[0]):
+        if top_p >= 1.0:
+            mask[r] = True
+            continue
+        p = softmax(rows[r], temperature)
+        order = np.lexsort((ids, -rows[r]))
+        c = np.cumsum(p[order])
+        Z = c[-1]
+        thr = top_p * Z
+        k = int(np.argmax(c >= thr))
+        mask[r, order[: k + 1]] = True
+        below = c[k - 1] if k > 0 else 0.0
+        margin[r] = min(c[k] - thr, thr - below) / Z
+    return mask.reshape(x.shape), margin.reshape(x.shape[:-1])
+
+
+def top_p_filter(logits, top_p, temperature=1.0):
+    """logits (fp64) with -inf outside the top-p set: softmax of the result
+    (at the same T) is p truncated to the set and renormalised."""
+    x = _np64(logits)
+    mask, _ = top_p_nucleus(x, top_p, temperature)
+    return np.where(mask, x, -np.inf)
+
+
 def rejection_sample(target_logits, draft, draft_tokens, uniforms,
-                     draft_is_probs=False, temperature=1.0):
+                     draft_is_probs=False, temperature=1.0, top_p=None, draft_top_p=False):
     """Verify one round for every sequence of the batch.
 
     target_logits [B, K+1, V]; draft [B, K, V] (logits, or probabilities when
     draft_is_probs); draft_tokens [B, K]; uniforms [B, K+1, 2].
+    With top_p < 1 the target rows are cut to their top-p sets first (and the
+    draft logit rows too when draft_top_p), see top_p_nucleus.
     Returns a dict with out_tokens [B, K+1] (-1 padded), num_accepted [B] and
     diagnostics (p/q at the draft tokens, accept margins |u - p/q|, CDF margin,
     per-row alpha, the sampled row index and its mass).
     """
+    if top_p is not None and top_p < 1.0:
+        target_logits = top_p_filter(target_logits, top_p, temperature)
+        if draft_top_p and not draft_is_probs and draft is not None:
+            draft = top_p_filter(draft, top_p, temperature)
     p = softmax(target_logits, temperature)                      # [B, K+1, V]
     q = _np64(draft) if draft_is_probs else softmax(draft, temperature)
     return verify_from_probs(p, q, draft_tokens, uniforms)
