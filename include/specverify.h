@@ -39,6 +39,13 @@
  *     OR-ed into *dev_status (a device int32 the caller zeroes; may be NULL).
  *     Outputs that depended on the bad value are unspecified.
  *   - No C++ exception crosses this interface.
+ *   - Kernels are launched with programmatic stream serialization: a call
+ *     may start while the previous kernel of the stream drains, and
+ *     kv_block_append reads its inputs (new rows, table, lengths) before
+ *     it waits for that kernel. A kernel of the caller that produces those
+ *     inputs must therefore not release its dependents early
+ *     (griddepcontrol.launch_dependents before its last write); kernels that
+ *     never do (the default) and copies are safe.
  *
  * Paged KV cache
  *   K and V pools: [num_blocks][H_kv][block_size][d_head] by default
@@ -230,6 +237,53 @@ sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
                                 float *p_at_draft, float *q_at_draft,
                                 void *workspace, size_t workspace_bytes,
                                 int32_t *dev_status, unsigned flags, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Top-p ("KV Cache + Speculative Decoding", section 7.5 and Q21: the target
+ * distribution becomes p truncated to its own top-p set and renormalised;
+ * the draft distribution q is whatever the draft sampled from, and the
+ * rejection rule stays exact with both).
+ *
+ * The top-p set of a row of softmax(logits / T): order the tokens by logit,
+ * largest first, equal logits by ascending token id; the set is the shortest
+ * prefix of that order whose probability reaches top_p. The masses are
+ * taken in fixed point (weights of the row relative to its maximum, rounded
+ * to multiples of 2^-40, summed exactly), so the set is deterministic and
+ * matches exact arithmetic unless top_p lies within 5e-7 (as a fraction of
+ * the row mass) of a cumulative mass.
+ *
+ * spec_topp_filter
+ *   out[r][x] = logits[r][x] for x in the top-p set of row r, -inf elsewhere;
+ *   softmax(out[r] / T) is then the truncated, renormalised distribution.
+ *   logits, out: [rows][V] of dtype (SV_F32, SV_BF16 or SV_F16); out may
+ *   equal logits. 0 < top_p <= 1 (1 copies the rows); temperature > 0.
+ *   V <= 262144 for 16-bit logits, 131072 for SV_F32. A row with a NaN
+ *   logit has it removed from the set and sets SV_DEV_NONFINITE; a row
+ *   with a +inf logit or no finite logit is copied unchanged (the sampling
+ *   flags it).
+ *
+ * spec_verify_sample_topp
+ *   spec_verify_sample with every target row replaced by its top-p filtered
+ *   row (p -> p-tilde, including the bonus row) and, when draft_topp is 1,
+ *   every draft logit row filtered the same way (the draft sampled from its
+ *   own top-p distribution); draft_topp needs draft logits. top_p = 1 is
+ *   plain spec_verify_sample. The filtered rows live at the front of the
+ *   workspace: spec_verify_sample_topp_workspace_size(...) bytes, 256-byte
+ *   aligned.
+ * ------------------------------------------------------------------------ */
+sv_status spec_topp_filter(const void *logits, sv_dtype dtype, int rows, int V, float temperature, float top_p,
+                           void *out, int32_t *dev_status, sv_stream_t stream);
+
+size_t spec_verify_sample_topp_workspace_size(int B, int K, int V, sv_dtype logit_dtype, int draft_topp);
+
+sv_status spec_verify_sample_topp(const void *target_logits, sv_dtype logit_dtype,
+                                  const void *draft, sv_dtype draft_dtype, int draft_is_probs,
+                                  const int32_t *draft_tokens, const float *uniforms,
+                                  int B, int K, int V, float temperature, float top_p, int draft_topp,
+                                  int32_t *out_tokens, int32_t *num_accepted,
+                                  float *p_at_draft, float *q_at_draft,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * spec_verify_sample_static

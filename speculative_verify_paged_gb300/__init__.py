@@ -83,6 +83,12 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_sample.argtypes = samp_args + [P]
     lib.spec_verify_sample_ex.restype = I
     lib.spec_verify_sample_ex.argtypes = samp_args + [U, P]
+    lib.spec_topp_filter.restype = I
+    lib.spec_topp_filter.argtypes = [P, I, I, I, F, F, P, P, P]
+    lib.spec_verify_sample_topp_workspace_size.restype = Z
+    lib.spec_verify_sample_topp_workspace_size.argtypes = [I, I, I, I, I]
+    lib.spec_verify_sample_topp.restype = I
+    lib.spec_verify_sample_topp.argtypes = [P, I, P, I, I, P, P, I, I, I, F, F, I, P, P, P, P, P, Z, P, P]
     I64, BMP = ctypes.c_int64, ctypes.c_void_p
     lib.sv_bm_create.restype = I
     lib.sv_bm_create.argtypes = [I, I, ctypes.POINTER(ctypes.c_void_p)]
@@ -238,14 +244,29 @@ def sample_workspace_size(B, K, V):
     return load_library().spec_verify_sample_workspace_size(B, K, V)
 
 
+def topp_filter(logits, top_p, temperature=1.0, out=None, status=None):
+    """Rows of `logits` [..., V] with -inf outside each row's top-p set."""
+    lib = load_library()
+    _cuda(logits, out, status)
+    if out is None:
+        out = torch.empty_like(logits)
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    _check(lib.spec_topp_filter(_ptr(logits), _dtype_code(logits), rows, V, float(temperature),
+                                float(top_p), _ptr(out), _ptr(status), _stream()))
+    return out
+
+
 def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_probs=False,
                        temperature=1.0, out_tokens=None, num_accepted=None, p_at_draft=None,
                        q_at_draft=None, workspace=None, status=None, force_exact=False,
-                       want_probs=True):
+                       want_probs=True, top_p=None, draft_top_p=False):
     """Rejection sampling of one verify round.
 
     target_logits [B, K+1, V]; draft [B, K, V] logits (same dtype) or f32
     probabilities; draft_tokens int32 [B, K]; uniforms f32 [B, K+1, 2].
+    top_p (optional): sample from the top-p truncated target rows (and draft
+    logit rows too with draft_top_p).
     Returns (out_tokens [B, K+1], num_accepted [B], p_at_draft, q_at_draft).
     """
     lib = load_library()
@@ -262,9 +283,22 @@ def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_pr
         p_at_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
     if want_probs and q_at_draft is None:
         q_at_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
+    ddt = _dtype_code(draft) if draft is not None else SV_F32
+    if top_p is not None:
+        if force_exact:
+            raise ValueError("force_exact is not available with top_p")
+        ldt = _dtype_code(target_logits)
+        need = lib.spec_verify_sample_topp_workspace_size(B, K, V, ldt, int(bool(draft_top_p)))
+        if workspace is None:
+            workspace = alloc_workspace(need, dev)
+        _check(lib.spec_verify_sample_topp(
+            _ptr(target_logits), ldt, _ptr(draft), ddt, int(bool(draft_is_probs)), _ptr(draft_tokens),
+            _ptr(uniforms), B, K, V, float(temperature), float(top_p), int(bool(draft_top_p)),
+            _ptr(out_tokens), _ptr(num_accepted), _ptr(p_at_draft), _ptr(q_at_draft), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(status), _stream()))
+        return out_tokens, num_accepted, p_at_draft, q_at_draft
     if workspace is None:
         workspace = alloc_workspace(sample_workspace_size(B, K, V), dev)
-    ddt = _dtype_code(draft) if draft is not None else SV_F32
     args = [_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt, int(bool(draft_is_probs)),
             _ptr(draft_tokens), _ptr(uniforms), B, K, V, float(temperature), _ptr(out_tokens),
             _ptr(num_accepted), _ptr(p_at_draft), _ptr(q_at_draft), _ptr(workspace),

@@ -1569,21 +1569,22 @@ sv_status launch_sample(const SampleParams &P, int cs, cudaStream_t s) {
 }  // namespace
 }  // namespace sv
 
-extern "C" size_t spec_verify_sample_workspace_size(int B, int K, int V) {
-  (void)V;
-  if (B < 0 || K < 0) return 0;
-  if (V < 1) return 0;
-  return sv::workspace_bytes_for(B, K, V);
+namespace sv {
+namespace {
+// Draw-kernel cluster: the smallest (up to 16 CTAs) whose slices take at most
+// eight groups of eight elements per thread; gpc = groups per CTA slice.
+void draw_shape(int V, int &cs, int &gpc) {
+  const int ngr = (V + 7) / 8;
+  cs = 1;
+  while (cs < 16 && (ngr + cs - 1) / cs > 8 * kRowThreads) cs *= 2;
+  gpc = (ngr + cs - 1) / cs;
 }
 
-extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
-                                           const void *draft, sv_dtype draft_dtype, int draft_is_probs,
-                                           const int32_t *draft_tokens, const float *uniforms, int B,
-                                           int K, int V, float temperature, int32_t *out_tokens,
-                                           int32_t *num_accepted, float *p_at_draft, float *q_at_draft,
-                                           void *workspace, size_t workspace_bytes,
-                                           int32_t *dev_status, unsigned flags, sv_stream_t stream) {
-  using namespace sv;
+// Host checks of spec_verify_sample's arguments (everything but the workspace).
+sv_status check_sample_args(const void *target_logits, sv_dtype logit_dtype, const void *draft,
+                            sv_dtype draft_dtype, int draft_is_probs, const int32_t *draft_tokens,
+                            const float *uniforms, int B, int K, int V, float temperature,
+                            const int32_t *out_tokens, const int32_t *num_accepted) {
   if (B < 0 || K < 0 || V < 1)
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample: bad sizes B=%d K=%d V=%d", B, K, V);
   if (B > 65535 || K + 1 > 65535)
@@ -1602,6 +1603,36 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
   } else if (K > 0 && draft_dtype != logit_dtype) {
     return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: draft logits must have the target's dtype");
   }
+  int cs, gpc;
+  draw_shape(V, cs, gpc);
+  if (gpc > kMaxDrawBlocks * 32)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large (at most %d)", V,
+                16 * kMaxDrawBlocks * 32 * 8);
+  return SV_OK;
+}
+}  // namespace
+}  // namespace sv
+
+extern "C" size_t spec_verify_sample_workspace_size(int B, int K, int V) {
+  (void)V;
+  if (B < 0 || K < 0) return 0;
+  if (V < 1) return 0;
+  return sv::workspace_bytes_for(B, K, V);
+}
+
+extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
+                                           const void *draft, sv_dtype draft_dtype, int draft_is_probs,
+                                           const int32_t *draft_tokens, const float *uniforms, int B,
+                                           int K, int V, float temperature, int32_t *out_tokens,
+                                           int32_t *num_accepted, float *p_at_draft, float *q_at_draft,
+                                           void *workspace, size_t workspace_bytes,
+                                           int32_t *dev_status, unsigned flags, sv_stream_t stream) {
+  using namespace sv;
+  {
+    const sv_status st = check_sample_args(target_logits, logit_dtype, draft, draft_dtype, draft_is_probs,
+                                           draft_tokens, uniforms, B, K, V, temperature, out_tokens, num_accepted);
+    if (st != SV_OK) return st;
+  }
   if (!workspace || workspace_bytes < workspace_bytes_for(B, K, V))
     return fail(SV_ERR_WORKSPACE, "spec_verify_sample: workspace needs %zu bytes", workspace_bytes_for(B, K, V));
   if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_sample: workspace not 256-byte aligned");
@@ -1609,15 +1640,8 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
 
   const int es_t = dtype_bytes(logit_dtype);
   const int es_buf_d = (draft_is_probs && K > 0) ? 4 : es_t;
-  // draw kernel: the smallest cluster (up to 16 CTAs) whose slices take at
-  // most eight groups of eight elements per thread
-  const int ngr = (V + 7) / 8;
-  int cs = 1;
-  while (cs < 16 && (ngr + cs - 1) / cs > 8 * kRowThreads) cs *= 2;
-  const int gpc = (ngr + cs - 1) / cs;
-  if (gpc > kMaxDrawBlocks * 32)
-    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large (at most %d)", V,
-                16 * kMaxDrawBlocks * 32 * 8);
+  int cs, gpc;
+  draw_shape(V, cs, gpc);
 
   SampleParams P = {};
   P.target = target_logits; P.draft = draft; P.tokens = draft_tokens; P.uniforms = uniforms;
@@ -1663,6 +1687,72 @@ extern "C" sv_status spec_verify_sample(const void *target_logits, sv_dtype logi
   return spec_verify_sample_ex(target_logits, logit_dtype, draft, draft_dtype, draft_is_probs, draft_tokens,
                                uniforms, B, K, V, temperature, out_tokens, num_accepted, p_at_draft,
                                q_at_draft, workspace, workspace_bytes, dev_status, 0u, stream);
+}
+
+// ------------------------------------------------------------- top-p ---
+// The target rows (and, on request, the draft logit rows) go through the
+// top-p filter into the front of the workspace; the sampling kernels then
+// read the filtered rows. The statistics kernel waits for the filter before
+// its first load.
+namespace {
+size_t topp_rows_bytes(int B, int K, int V, sv_dtype dt, int draft_topp) {
+  const size_t es = (size_t)sv::dtype_bytes(dt);
+  size_t n = sv::align_up((size_t)B * (K + 1) * V * es, 256);
+  if (draft_topp && K > 0) n += sv::align_up((size_t)B * K * V * es, 256);
+  return n;
+}
+}  // namespace
+
+extern "C" size_t spec_verify_sample_topp_workspace_size(int B, int K, int V, sv_dtype logit_dtype,
+                                                         int draft_topp) {
+  if (B < 0 || K < 0 || V < 1) return 0;
+  if (logit_dtype != SV_F32 && logit_dtype != SV_BF16 && logit_dtype != SV_F16) return 0;
+  return topp_rows_bytes(B, K, V, logit_dtype, draft_topp) + sv::workspace_bytes_for(B, K, V);
+}
+
+extern "C" sv_status spec_verify_sample_topp(const void *target_logits, sv_dtype logit_dtype, const void *draft,
+                                             sv_dtype draft_dtype, int draft_is_probs,
+                                             const int32_t *draft_tokens, const float *uniforms, int B, int K,
+                                             int V, float temperature, float top_p, int draft_topp,
+                                             int32_t *out_tokens, int32_t *num_accepted, float *p_at_draft,
+                                             float *q_at_draft, void *workspace, size_t workspace_bytes,
+                                             int32_t *dev_status, sv_stream_t stream) {
+  using namespace sv;
+  if (!(top_p > 0.f) || !(top_p <= 1.f))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_topp: top_p must be in (0, 1]");
+  if (draft_topp && draft_is_probs)
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_topp: draft_topp needs draft logits, not probabilities");
+  if (top_p >= 1.f)
+    return spec_verify_sample_ex(target_logits, logit_dtype, draft, draft_dtype, draft_is_probs, draft_tokens,
+                                 uniforms, B, K, V, temperature, out_tokens, num_accepted, p_at_draft, q_at_draft,
+                                 workspace, workspace_bytes, dev_status, 0u, stream);
+  {
+    const sv_status st = check_sample_args(target_logits, logit_dtype, draft, draft_dtype, draft_is_probs,
+                                           draft_tokens, uniforms, B, K, V, temperature, out_tokens, num_accepted);
+    if (st != SV_OK) return st;
+  }
+  const int per_cta = 8 * 256 * (16 / dtype_bytes(logit_dtype));
+  if (V > 16 * per_cta)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_topp: V = %d above %d for this dtype", V, 16 * per_cta);
+  if ((long long)B * (K + 1) + (draft_topp ? (long long)B * K : 0) > 65535)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_topp: more than 65535 filtered rows");
+  const size_t front = topp_rows_bytes(B, K, V, logit_dtype, draft_topp);
+  const size_t need = front + workspace_bytes_for(B, K, V);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "spec_verify_sample_topp: workspace needs %zu bytes", need);
+  if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_sample_topp: workspace not 256-byte aligned");
+  if (B == 0) return ok();
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const size_t es = (size_t)dtype_bytes(logit_dtype);
+  void *ft = ws;
+  void *fd = (draft_topp && K > 0) ? ws + align_up((size_t)B * (K + 1) * V * es, 256) : nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const sv_status st = launch_topp_filter(logit_dtype, target_logits, ft, B * (K + 1), draft, fd,
+                                          fd ? B * K : 0, V, temperature, top_p, dev_status, s);
+  if (st != SV_OK) return st;
+  return spec_verify_sample_ex(ft, logit_dtype, fd ? fd : draft, draft_dtype, draft_is_probs, draft_tokens, uniforms,
+                               B, K, V, temperature, out_tokens, num_accepted, p_at_draft, q_at_draft, ws + front,
+                               workspace_bytes - front, dev_status, 0u, stream);
 }
 
 // ------------------------------------------------- allocation-free entry ---

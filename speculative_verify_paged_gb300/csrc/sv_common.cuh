@@ -20,6 +20,11 @@ namespace sv {
 
 // ----------------------------------------------------------------- host ---
 
+// Top-p filter (topp.cu): rows0 rows in0 -> out0, then rows1 rows in1 -> out1,
+// each [rows][V] of `dtype`; arguments already checked by the caller.
+sv_status launch_topp_filter(sv_dtype dtype, const void *in0, void *out0, int rows0, const void *in1, void *out1,
+                             int rows1, int V, float temperature, float top_p, int32_t *status, cudaStream_t s);
+
 // Per-thread message of the last failed call.
 std::string &last_error();
 // kernels this library launched successfully in this process

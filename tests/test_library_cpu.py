@@ -101,6 +101,34 @@ def test_host_validation_errors(lib):
     assert sv.SpecVerifyError(3, "x").status == 3
 
 
+def test_topp_host_validation_and_workspace(lib):
+    fake = ctypes.c_void_p(0x1000)
+    NULL = None
+    # top_p outside (0, 1], bad sizes, fp8 logits, a vocabulary too large for one cluster
+    assert lib.spec_topp_filter(fake, 1, 4, 100, 1.0, 0.0, fake, NULL, NULL) == 1
+    assert lib.spec_topp_filter(fake, 1, 4, 100, 1.0, 1.5, fake, NULL, NULL) == 1
+    assert lib.spec_topp_filter(fake, 1, -1, 100, 1.0, 0.5, fake, NULL, NULL) == 1
+    assert lib.spec_topp_filter(fake, 1, 4, 100, 0.0, 0.5, fake, NULL, NULL) == 1
+    assert lib.spec_topp_filter(fake, 3, 4, 100, 1.0, 0.5, fake, NULL, NULL) == 2
+    assert lib.spec_topp_filter(fake, 1, 4, 16 * 16384 + 1, 1.0, 0.5, fake, NULL, NULL) == 2
+    assert lib.spec_topp_filter(fake, 0, 4, 16 * 8192 + 1, 1.0, 0.5, fake, NULL, NULL) == 2
+    # workspace: filtered target rows (and draft rows), 256-byte rounded, in
+    # front of the sampling workspace
+    up = lambda x: (x + 255) // 256 * 256
+    base = lib.spec_verify_sample_workspace_size(64, 4, 128256)
+    assert lib.spec_verify_sample_topp_workspace_size(64, 4, 128256, 1, 0) == up(64 * 5 * 128256 * 2) + base
+    assert lib.spec_verify_sample_topp_workspace_size(64, 4, 128256, 1, 1) == (
+        up(64 * 5 * 128256 * 2) + up(64 * 4 * 128256 * 2) + base)
+    assert lib.spec_verify_sample_topp_workspace_size(64, 4, 128256, 3, 0) == 0
+    # sampling with top-p: draft_topp with probabilities, bad top_p, small workspace
+    args = lambda tp, dtp, probs, ddt, ws: (fake, 1, fake, ddt, probs, fake, fake, 2, 4, 100, 1.0, tp, dtp,
+                                            fake, fake, NULL, NULL, fake, ws, NULL, NULL)
+    assert lib.spec_verify_sample_topp(*args(0.9, 1, 1, 0, 1 << 30)) == 1
+    assert lib.spec_verify_sample_topp(*args(0.0, 0, 0, 1, 1 << 30)) == 1
+    assert lib.spec_verify_sample_topp(*args(0.9, 0, 0, 1, 16)) == 3
+    assert lib.spec_verify_sample_topp(*args(0.9, 0, 0, 0, 1 << 30)) == 2   # draft dtype mismatch
+
+
 def test_product_path_has_no_cpu_fallback():
     """The binding raises when tensors are not on a CUDA device."""
     import torch
