@@ -363,6 +363,8 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     assert int(status.item()) == 0
 
+    nxt = measure_next_rows(sv, cfg, a, s, dev, stream, status) if rank == 0 else None
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -397,6 +399,7 @@ def run_ours(args, rank, world, local):
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
         "gpu_launches": timed_launches,
         "clocks": clk,
+        "next": nxt,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, a, n, s, sigma)
@@ -406,6 +409,71 @@ def run_ours(args, rank, world, local):
 
 
 # ------------------------------------------------------------- oracle -----
+
+def measure_next_rows(sv, cfg, a, s, dev, stream, status, reps=20):
+    """The opt-in parts beyond the timed step, each timed alone with CUDA
+    events on the launching stream (outside the step's timed region):
+    sampling at top_p = 0.9 with the draft rows filtered too, the top-p
+    filter alone over those target and draft rows (HBM-bound: every row read
+    once and written once), and the copy-on-write page copy of one page per
+    sequence in this layer's K and V pools."""
+    import torch
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps
+
+    B, K, V = cfg.B, cfg.K, cfg.V
+    peak, _ = measured_peaks()
+    ws = sv.alloc_workspace(sv.load_library().spec_verify_sample_topp_workspace_size(
+        B, K, V, sv.SV_BF16 if s["target_logits"].dtype == torch.bfloat16 else sv.SV_F32, 1), dev)
+    toks = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    samp_us = timed(lambda: sv.spec_verify_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"],
+                                                  s["uniforms"], out_tokens=toks, num_accepted=nacc,
+                                                  workspace=ws, status=status, want_probs=False, top_p=0.9,
+                                                  draft_top_p=True))
+    rows = torch.cat([s["target_logits"].reshape(-1, V), s["draft_logits"].reshape(-1, V)])
+    filt = torch.empty_like(rows)
+    filt_us = timed(lambda: sv.topp_filter(rows, 0.9, out=filt, status=status))
+    filt_bytes = 2 * rows.numel() * rows.element_size()
+    kc, vc = a["k_cache"], a["v_cache"]
+    pages = [(int(b), int(b)) for b in a["block_table"][:, 0].tolist()]     # one page per sequence, onto itself
+    page_bytes = kc.stride(0) * kc.element_size()
+    idx = torch.tensor(pages, dtype=torch.int32).t().contiguous().to(dev)
+    lib = sv.load_library()
+    import ctypes
+    pools = (ctypes.c_void_p * 2)(kc.data_ptr(), vc.data_ptr())
+
+    def cow():
+        rc = lib.sv_copy_blocks(pools, 2, page_bytes, page_bytes, ctypes.c_void_p(idx[0].data_ptr()),
+                                ctypes.c_void_p(idx[1].data_ptr()), len(pages), kc.shape[0],
+                                ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+        assert rc == 0
+    cow_us = timed(cow)
+    cow_bytes = 2 * 2 * len(pages) * page_bytes
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return {
+        "top_p": {"top_p": 0.9, "draft_top_p": True, "sample_topp_us": samp_us,
+                  "filter_us": filt_us, "filter_rows": rows.shape[0],
+                  "roofline": {"bound": "hbm", "kernel": "topp_filter_kernel", "achieved": filt_bytes / (filt_us * 1e-6) / 1e9,
+                               "peak": peak, "unit": "GB/s",
+                               "frac": filt_bytes / (filt_us * 1e-6) / 1e9 / peak, "bytes": filt_bytes}},
+        "cow_copy": {"pairs": len(pages), "pools": 2, "page_bytes": page_bytes, "us": cow_us,
+                     "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel",
+                                  "achieved": cow_bytes / (cow_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                                  "frac": cow_bytes / (cow_us * 1e-6) / 1e9 / peak, "bytes": cow_bytes}},
+    }
+
 
 def oracle_sample_time(cfg, a, n, s, n_attn, n_samp):
     """Seconds the oracle takes for the append + attention of sequences

@@ -25,11 +25,14 @@
 //   2. a 2048-bin histogram of the masses by -log2(weight) in steps of 1/32
 //      (bins in descending logit order), summed over the cluster;
 //   3. the bin where the cumulative mass reaches ceil(top_p * Z);
-//   4. if that bin holds at most 512 tokens, they are gathered into the
-//      cluster's first CTA and each one's cumulative mass is computed by
-//      direct comparison of composites; otherwise the bin is split by the
-//      composite's bits, 8 at a time, until at most 512 remain;
-//   5. every element is written back, or -inf where composite < cut.
+//   4. that bin's tokens are gathered into the cluster's first CTA (if more
+//      than 512, the bin is first split by the composite's bits, 8 at a
+//      time, until at most 512 remain) and each one's cumulative mass is
+//      computed by direct comparison of composites, which gives the cut;
+//   5. every element is written back, or -inf below the cut: bins above the
+//      cut's bin stay, bins below go, the composite decides within it.
+// Bins are one fma from the logit, so only the histogram pass and the
+// gathered tokens compute the precise weights.
 
 #include <cmath>
 #include <mutex>
@@ -159,57 +162,56 @@ __device__ __forceinline__ u64 block_excl_scan_u64(u64 v, u64 *s_warp, u64 *tota
   return before + incl - v;
 }
 
-__device__ __forceinline__ int block_sum_int(int v, int *s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Calls f(e, bits) for every element e < n of this CTA's slice in shared
+// memory: full 16-byte groups round-robin over the threads, then the ragged
+// last group on one thread.
+template <typename T, typename F>
+__device__ __forceinline__ void tp_for_each(const uint4 *sl, int n, F f) {
+  constexpr int G = TpType<T>::G;
+  const int nfull = n / G;
+  for (int g = threadIdx.x; g < nfull; g += kTpThreads) {
+    const uint4 r = sl[g];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) s_warp[warp] = v;
-  __syncthreads();
-  int t = 0;
+    for (int k = 0; k < G; ++k) f(g * G + k, TpType<T>::get(r, k));
+  }
+  const int rem = n - nfull * G;
+  if (rem > 0 && (int)threadIdx.x == nfull % kTpThreads) {
+    const uint4 r = sl[nfull];
 #pragma unroll
-  for (int w = 0; w < kTpThreads / 32; ++w) t += s_warp[w];
-  __syncthreads();
-  return t;
+    for (int k = 0; k < G; ++k)
+      if (k < rem) f(nfull * G + k, TpType<T>::get(r, k));
+  }
 }
 
-// In a histogram h of nb entries read in logical order (descending: logical i
-// is entry nb-1-i), the entry where the running mass, starting from `above`,
-// first reaches thr. Writes the physical entry to *s_sel and the mass before
-// it to *s_above (exactly one entry qualifies when the total reaches thr).
-__device__ __forceinline__ void tp_find_cross(const u64 *h, int nb, bool desc, u64 above, u64 thr,
-                                              u64 *s_warp, int *s_sel, u64 *s_above) {
-  const int per = nb / kTpThreads;
-  const int i0 = threadIdx.x * per;
+__device__ __forceinline__ unsigned atom_add_dsmem_u32(uint32_t addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// In the histogram whose logical entries [threadIdx.x * PER, +PER) this
+// thread holds in h, the logical entry where the running mass, starting from
+// `above`, first reaches thr; the winner writes phys(entry) to *s_sel and the
+// mass before it to *s_above. Returns the total of all entries.
+template <int PER, typename Phys>
+__device__ __forceinline__ u64 tp_find_cross(const u64 (&h)[PER], Phys phys, u64 above, u64 thr, u64 *s_warp,
+                                             int *s_sel, u64 *s_above) {
   u64 mine = 0;
-  for (int j = 0; j < per; ++j) mine += h[desc ? nb - 1 - (i0 + j) : i0 + j];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) mine += h[j];
   u64 tot;
   u64 cum = above + block_excl_scan_u64(mine, s_warp, &tot);
-  for (int j = 0; j < per; ++j) {
-    const int p = desc ? nb - 1 - (i0 + j) : i0 + j;
-    const u64 nx = cum + h[p];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const u64 nx = cum + h[j];
     if (cum < thr && thr <= nx) {
-      *s_sel = p;
+      *s_sel = phys((int)threadIdx.x * PER + j);
       *s_above = cum;
     }
     cum = nx;
   }
   __syncthreads();
-}
-
-// Calls f(e, bits) for every element e < n of this CTA's slice in shared
-// memory (groups of one 16-byte vector per thread and step).
-template <typename T, typename F>
-__device__ __forceinline__ void tp_for_each(const uint4 *sl, int n, F f) {
-  constexpr int G = TpType<T>::G;
-  const int ng = (n + G - 1) / G;
-  for (int g = threadIdx.x; g < ng; g += kTpThreads) {
-    const uint4 r = sl[g];
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-      const int e = g * G + k;
-      if (e < n) f(e, TpType<T>::get(r, k));
-    }
-  }
+  return tot;
 }
 
 template <typename T>
@@ -218,7 +220,9 @@ __global__ void __launch_bounds__(kTpThreads) topp_filter_kernel(const __grid_co
   constexpr int G = TT::G;
   extern __shared__ uint4 sl[];     // this CTA's slice of the row (dynamic)
   __shared__ u64 h_mass[kTpBins];   // this CTA's histogram (read by the whole cluster)
-  __shared__ u64 h_tot[kTpBins];    // the cluster's totals
+  __shared__ u64 h_red[kTpBins];    // this CTA's segment of the cluster's totals
+  __shared__ u64 s_segtot;          // ... and its sum
+  __shared__ int s_owner;           // the CTA whose segment holds the crossing
   __shared__ u64 c_comp[kTpCap];    // first CTA: gathered candidates
   __shared__ u64 c_q[kTpCap];
   __shared__ u64 s_warp64[kTpThreads / 32];
@@ -226,11 +230,10 @@ __global__ void __launch_bounds__(kTpThreads) topp_filter_kernel(const __grid_co
   __shared__ int s_wflag[kTpThreads / 32];
   __shared__ float s_max;
   __shared__ int s_flag;            // bit 0: a NaN, bit 1: +inf
-  __shared__ int s_cnt;
   __shared__ int s_sel;
   __shared__ u64 s_above;
   __shared__ u64 s_cut;
-  __shared__ unsigned s_slot;
+  __shared__ unsigned s_gcount;     // first CTA: candidates gathered so far
 
   pdl_wait();
   pdl_trigger();
@@ -287,7 +290,6 @@ __global__ void __launch_bounds__(kTpThreads) topp_filter_kernel(const __grid_co
     s_warp32[threadIdx.x >> 5] = __float_as_int(mx);
     s_wflag[threadIdx.x >> 5] = flag;
   }
-  if (threadIdx.x == 0) s_slot = 0u;
   __syncthreads();
   if (threadIdx.x == 0) {
     float b = -INFINITY;
@@ -331,19 +333,19 @@ __global__ void __launch_bounds__(kTpThreads) topp_filter_kernel(const __grid_co
     return;
   }
 
-  // The weight of x is 2^(ex), ex = (x - m) c, taken as hi + lo: x - m by
-  // two-sum (exact), times c = c_hi + c_lo with an fma for the rounding of
-  // the product. 2^hi comes from the SFU (relative error below 1.5e-7 on
-  // [-30, 0]) and 2^lo as the first-order factor 1 + lo ln 2 (|lo| is at most
-  // an ulp of hi, so the neglected term is ~1e-12). Bins use hi alone, which
-  // is monotone in x.
+  // Bins: b(x) = floor(-32 (x c_hi - fl(m c_hi))), one fma from the logit,
+  // non-increasing in x and computed the same way in every pass (bin 2047
+  // also takes everything below 2^-64 of the maximum, and -inf).
+  // Weights: 2^ex with ex = (x - m) c taken as hi + lo: x - m by two-sum
+  // (exact), times c = c_hi + c_lo with an fma for the product's rounding.
+  // 2^hi comes from the SFU (relative error below 1.5e-7 on [-30, 0]) and
+  // 2^lo as the first-order factor 1 + lo ln 2 (|lo| is at most an ulp of
+  // hi, so the neglected term is ~1e-12).
   const float c_hi = P.c_hi, c_lo = P.c_lo;
-  struct Ex {
-    float hi, lo;
-  };
-  auto exponent = [&](uint32_t cb) -> Ex {
-    const float x = TT::val(cb);
-    if (!(x > -INFINITY)) return Ex{-INFINITY, 0.f};
+  const float mc = __fmul_rn(m, c_hi);
+  auto bin_of = [&](float x) { return min(kTpBins - 1, (int)(-fmaf(x, c_hi, -mc) * 32.f)); };
+  auto mass_of = [&](float x) -> u64 {
+    if (!(x > -INFINITY)) return 0ull;
     const float d = x - m;
     const float bb = d - x;
     const float d_lo = (x - (d - bb)) + (-m - bb);
@@ -351,128 +353,162 @@ __global__ void __launch_bounds__(kTpThreads) topp_filter_kernel(const __grid_co
     float l = fmaf(d, c_hi, -h);
     l = fmaf(d, c_lo, l);
     l = fmaf(d_lo, c_hi, l);
-    return Ex{h, l};
-  };
-  auto bin_of = [](Ex ex) { return min(kTpBins - 1, max(0, (int)(-ex.hi * 32.f))); };
-  auto mass_of = [](Ex ex) {
-    const float t = tp_ex2(ex.hi);
+    const float t = tp_ex2(h);
     if (!(t > 0.f)) return 0ull;
-    return __float2ull_rn(fmaf(t, ex.lo * 0.693147180559945309f, t) * kTpQuant);
+    return __float2ull_rn(fmaf(t, l * 0.693147180559945309f, t) * kTpQuant);
   };
+  const int lane = threadIdx.x & 31;
 
   // ---- first-level histogram of the quantised masses ----
   for (int i = threadIdx.x; i < kTpBins; i += kTpThreads) h_mass[i] = 0ull;
+  if (threadIdx.x == 0) { s_gcount = 0u; s_sel = -1; s_above = 0ull; s_cut = 0ull; }
   __syncthreads();
-  tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
+  tp_for_each<T>(sl, n, [&](int, uint32_t b) {
     bool nan;
-    const Ex ex = exponent(tp_canon<T>(b, nan));
-    const u64 q = mass_of(ex);
-    if (q) atomicAdd(&h_mass[bin_of(ex)], q);
+    const float x = TT::val(tp_canon<T>(b, nan));
+    const int bn = bin_of(x);
+    if (bn < kTpBins - 1) {
+      const u64 q = mass_of(x);
+      if (q) atomicAdd(&h_mass[bn], q);
+    }
   });
   __syncthreads();
   cluster_sync();
-  for (int i = threadIdx.x; i < kTpBins; i += kTpThreads) {
-    u64 s = 0;
-    for (int r = 0; r < CS; ++r) s += ld_dsmem_u64(mapa(&h_mass[i], r));
-    h_tot[i] = s;
-  }
-  __syncthreads();
 
   // ---- the bin where the running mass reaches ceil(top_p Z) ----
-  u64 Z = 0;
+  // Reduce-scatter: CTA `rank` sums the bins [b0, b1) over the cluster
+  // (coalesced reads of the others' shared memory), then only the segment
+  // totals are exchanged; the CTA whose segment holds the crossing finds the
+  // bin and publishes it.
+  const int seg = (kTpBins + CS - 1) / CS;
+  const int b0 = min(kTpBins, rank * seg), b1 = min(kTpBins, b0 + seg);
+  for (int i = b0 + (int)threadIdx.x; i < b1; i += kTpThreads) {
+    u64 t = 0;
+    for (int r = 0; r < CS; ++r) t += ld_dsmem_u64(mapa(&h_mass[i], r));
+    h_red[i - b0] = t;
+  }
+  __syncthreads();
+  constexpr int kPer = kTpBins / kTpThreads;   // entries per thread in the scan (segments are at most kTpBins)
+  u64 h8[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = (int)threadIdx.x * kPer + j;
+    h8[j] = i < b1 - b0 ? h_red[i] : 0ull;
+  }
+  u64 seg_tot;
   {
     u64 mine = 0;
-    for (int j = 0; j < kTpBins / kTpThreads; ++j) mine += h_tot[threadIdx.x * (kTpBins / kTpThreads) + j];
-    (void)block_excl_scan_u64(mine, s_warp64, &Z);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) mine += h8[j];
+    (void)block_excl_scan_u64(mine, s_warp64, &seg_tot);
+  }
+  if (threadIdx.x == 0) s_segtot = seg_tot;
+  cluster_sync();
+  u64 Z = 0, before = 0;
+  for (int r = 0; r < CS; ++r) {
+    const u64 t = ld_dsmem_u64(mapa(&s_segtot, r));
+    if (r < rank) before += t;
+    Z += t;
   }
   u64 thr = (u64)ceil(P.top_p * (double)Z);
   thr = thr < 1ull ? 1ull : (thr > Z ? Z : thr);
-  if (threadIdx.x == 0) { s_sel = -1; s_above = 0ull; s_cut = 0ull; }
-  __syncthreads();
-  tp_find_cross(h_tot, kTpBins, false, 0ull, thr, s_warp64, &s_sel, &s_above);
-  const int bin = s_sel;
-  u64 above = s_above;
-
-  // candidates: elements of that bin whose composite matches the radix prefix
-  // (the bits of the composite at and above sh equal pfx)
-  int sh = 64;
-  u64 pfx = 0ull;
-  auto is_cand = [&](int e, uint32_t b, u64 &comp, Ex &ex) {
-    bool nan;
-    const uint32_t cb = tp_canon<T>(b, nan);
-    ex = exponent(cb);
-    comp = tp_composite<T>(cb, lo + e);
-    return bin_of(ex) == bin && (sh >= 64 || (comp >> sh) == pfx);
-  };
-  int n_all = 0, my_off = 0;
-  for (int level = 0;; ++level) {
-    int cnt = 0;
-    tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
-      u64 comp;
-      Ex ex;
-      cnt += is_cand(e, b, comp, ex) ? 1 : 0;
-    });
-    cnt = block_sum_int(cnt, s_warp32);
-    if (threadIdx.x == 0) s_cnt = cnt;
-    cluster_sync();
-    n_all = 0;
-    my_off = 0;
+  if (before < thr && thr <= before + seg_tot)
+    (void)tp_find_cross<kPer>(h8, [b0](int i) { return b0 + i; }, before, thr, s_warp64, &s_sel, &s_above);
+  if (threadIdx.x == 0) {
+    // which CTA holds the crossing: the same arithmetic in every CTA
+    u64 acc = 0;
+    int owner = 0;
     for (int r = 0; r < CS; ++r) {
-      const int x = ld_dsmem_s32(mapa(&s_cnt, r));
-      if (r < rank) my_off += x;
-      n_all += x;
+      const u64 t = ld_dsmem_u64(mapa(&s_segtot, r));
+      if (acc < thr && thr <= acc + t) owner = r;
+      acc += t;
     }
-    if (n_all <= kTpCap || sh == 0 || level > 8) break;
-    // split the candidates by the next (up to) 8 bits of their composite;
-    // every CTA read the previous histogram before the count barrier above
-    const int nsh = sh > 8 ? sh - 8 : 0;
-    const int width = sh - nsh;
-    for (int i = threadIdx.x; i < 256; i += kTpThreads) h_mass[i] = 0ull;
-    __syncthreads();
-    tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
-      u64 comp;
-      Ex ex;
-      if (is_cand(e, b, comp, ex)) {
-        const u64 q = mass_of(ex);
-        if (q) atomicAdd(&h_mass[(int)((comp >> nsh) & ((1ull << width) - 1ull))], q);
-      }
-    });
-    __syncthreads();
-    cluster_sync();
-    for (int i = threadIdx.x; i < 256; i += kTpThreads) {
-      u64 s = 0;
-      for (int r = 0; r < CS; ++r) s += ld_dsmem_u64(mapa(&h_mass[i], r));
-      h_tot[i] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) s_sel = -1;
-    __syncthreads();
-    tp_find_cross(h_tot, 256, true, above, thr, s_warp64, &s_sel, &s_above);
-    above = s_above;
-    pfx = (sh >= 64 ? 0ull : (pfx << width)) | (u64)(s_sel < 0 ? 0 : s_sel);
-    sh = nsh;
-    cluster_sync();   // the counts of this level may be overwritten now
-  }
-
-  // ---- gather the candidates into the first CTA and rank them ----
-  if (n_all <= kTpCap) {
-    tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
-      u64 comp;
-      Ex ex;
-      if (is_cand(e, b, comp, ex)) {
-        const int slot = my_off + (int)atomicAdd(&s_slot, 1u);
-        if (slot < kTpCap) {
-          st_dsmem_u64(mapa(&c_comp[slot], 0), comp);
-          st_dsmem_u64(mapa(&c_q[slot], 0), mass_of(ex));
-        }
-      }
-    });
+    s_owner = owner;
   }
   cluster_sync();
+  const int bin = ld_dsmem_s32(mapa(&s_sel, s_owner));
+  u64 above = ld_dsmem_u64(mapa(&s_above, s_owner));
+
+  // ---- gather the bin's elements into the first CTA (warp-aggregated slots) ----
+  const uint32_t gcount = mapa(&s_gcount, 0);
+  auto gather = [&](int e, uint32_t cb, float x, bool cand) {
+    const unsigned am = __activemask();
+    const unsigned bal = __ballot_sync(am, cand);
+    if (!bal) return;
+    const int leader = __ffs(bal) - 1;
+    unsigned base = 0;
+    if (lane == leader) base = atom_add_dsmem_u32(gcount, (unsigned)__popc(bal));
+    base = __shfl_sync(am, base, leader);
+    if (cand) {
+      const unsigned slot = base + (unsigned)__popc(bal & ((1u << lane) - 1u));
+      if (slot < (unsigned)kTpCap) {
+        st_dsmem_u64(mapa(&c_comp[slot], 0), tp_composite<T>(cb, lo + e));
+        st_dsmem_u64(mapa(&c_q[slot], 0), mass_of(x));
+      }
+    }
+  };
+  tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
+    bool nan;
+    const uint32_t cb = tp_canon<T>(b, nan);
+    const float x = TT::val(cb);
+    gather(e, cb, x, bin_of(x) == bin);
+  });
+  cluster_sync();
+  int n_all = ld_dsmem_s32(gcount);
+
+  if (n_all > kTpCap) {
+    // Rare: more than kTpCap elements share the bin (many equal or nearly
+    // equal logits). Split them by the composite's bits, 8 at a time from
+    // the top, keeping the part where the running mass reaches thr, until at
+    // most kTpCap remain (composites are distinct, so this ends).
+    int sh = 64;
+    u64 pfx = 0ull;
+    auto is_cand = [&](int e, uint32_t cb, float x) {
+      if (bin_of(x) != bin) return false;
+      return sh >= 64 || (tp_composite<T>(cb, lo + e) >> sh) == pfx;
+    };
+    while (n_all > kTpCap && sh > 0) {
+      const int nsh = sh > 8 ? sh - 8 : 0;
+      const int width = sh - nsh;
+      cluster_sync();   // every CTA is done reading the previous histogram and counter
+      for (int i = threadIdx.x; i < 256; i += kTpThreads) h_mass[i] = 0ull;
+      if (threadIdx.x == 0) { s_gcount = 0u; s_sel = -1; }
+      __syncthreads();
+      tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
+        bool nan;
+        const uint32_t cb = tp_canon<T>(b, nan);
+        const float x = TT::val(cb);
+        if (is_cand(e, cb, x)) {
+          const u64 q = mass_of(x);
+          const int d = (int)((tp_composite<T>(cb, lo + e) >> nsh) & ((1ull << width) - 1ull));
+          if (q) atomicAdd(&h_mass[d], q);
+        }
+      });
+      __syncthreads();
+      cluster_sync();
+      u64 h1[1] = {0ull};
+      for (int r = 0; r < CS; ++r) h1[0] += ld_dsmem_u64(mapa(&h_mass[255 - threadIdx.x], r));
+      (void)tp_find_cross<1>(h1, [](int i) { return 255 - i; }, above, thr, s_warp64, &s_sel, &s_above);
+      above = s_above;
+      pfx = (sh >= 64 ? 0ull : (pfx << width)) | (u64)(s_sel < 0 ? 0 : s_sel);
+      sh = nsh;
+      cluster_sync();   // the first CTA's counter is zero everywhere it is read
+      tp_for_each<T>(sl, n, [&](int e, uint32_t b) {
+        bool nan;
+        const uint32_t cb = tp_canon<T>(b, nan);
+        const float x = TT::val(cb);
+        gather(e, cb, x, is_cand(e, cb, x));
+      });
+      cluster_sync();
+      n_all = ld_dsmem_s32(gcount);
+    }
+  }
+
+  // ---- rank the gathered candidates in the first CTA ----
   if (rank == 0 && n_all <= kTpCap) {
-    // candidate i is the cut iff the mass before it (the bins above, plus
-    // every candidate with a larger composite) is below thr and reaches thr
-    // with it
+    // candidate i is the cut iff the mass before it (the bins and radix parts
+    // above, plus every candidate with a larger composite) is below thr and
+    // reaches thr with it
     for (int i = threadIdx.x; i < n_all; i += kTpThreads) {
       const u64 ci = c_comp[i], qi = c_q[i];
       u64 before = 0;
@@ -482,21 +518,29 @@ __global__ void __launch_bounds__(kTpThreads) topp_filter_kernel(const __grid_co
   }
   __syncthreads();
   cluster_sync();
-  const u64 cut = ld_dsmem_u64(mapa(&s_cut, 0));   // 0 (keep all) if no cut was found
+  const u64 cut = ld_dsmem_u64(mapa(&s_cut, 0));   // 0: no cut found, keep the row
   cluster_sync();   // the first CTA stays until every CTA has read the cut
 
-  // ---- write the filtered slice ----
+  // ---- write the filtered slice: bins above the cut's bin stay, bins below
+  // go, and within the cut's bin the composite decides ----
+  auto keep_of = [&](int e, uint32_t b) {
+    bool nan;
+    const uint32_t cb = tp_canon<T>(b, nan);
+    if (nan) return false;
+    if (cut == 0ull) return true;
+    const int bn = bin_of(TT::val(cb));
+    return bn < bin || (bn == bin && tp_composite<T>(cb, lo + e) >= cut);
+  };
   for (int g = threadIdx.x; g < ng; g += kTpThreads) {
     const uint4 r = sl[g];
+    const bool full = (g + 1) * G <= n;
     uint32_t ob[G];
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       const uint32_t b = TT::get(r, k);
-      bool nan;
-      const uint32_t cb = tp_canon<T>(b, nan);
-      ob[k] = (!nan && tp_composite<T>(cb, lo + g * G + k) >= cut) ? b : TT::kNegInf;
+      ob[k] = (full || g * G + k < n) && keep_of(g * G + k, b) ? b : TT::kNegInf;
     }
-    if (P.vec && (g + 1) * G <= n) {
+    if (P.vec && full) {
       uint4 o;
       if (sizeof(T) == 4) {
         o = make_uint4(ob[0], ob[1 % G], ob[2 % G], ob[3 % G]);
