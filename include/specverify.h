@@ -257,7 +257,7 @@ sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype logit_dtype,
  *   softmax(out[r] / T) is then the truncated, renormalised distribution.
  *   logits, out: [rows][V] of dtype (SV_F32, SV_BF16 or SV_F16); out may
  *   equal logits. 0 < top_p <= 1 (1 copies the rows); temperature > 0.
- *   V <= 262144 for 16-bit logits, 131072 for SV_F32. A row with a NaN
+ *   V <= 2^28. A row with a NaN
  *   logit has it removed from the set and sets SV_DEV_NONFINITE; a row
  *   with a +inf logit or no finite logit is copied unchanged (the sampling
  *   flags it).

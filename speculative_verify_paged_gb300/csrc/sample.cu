@@ -1731,11 +1731,7 @@ extern "C" sv_status spec_verify_sample_topp(const void *target_logits, sv_dtype
                                            draft_tokens, uniforms, B, K, V, temperature, out_tokens, num_accepted);
     if (st != SV_OK) return st;
   }
-  const int per_cta = 8 * 256 * (16 / dtype_bytes(logit_dtype));
-  if (V > 16 * per_cta)
-    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_topp: V = %d above %d for this dtype", V, 16 * per_cta);
-  if ((long long)B * (K + 1) + (draft_topp ? (long long)B * K : 0) > 65535)
-    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_topp: more than 65535 filtered rows");
+  if (V > (1 << 28)) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_topp: V = %d above 2^28", V);
   const size_t front = topp_rows_bytes(B, K, V, logit_dtype, draft_topp);
   const size_t need = front + workspace_bytes_for(B, K, V);
   if (!workspace || workspace_bytes < need)

@@ -12,7 +12,8 @@ bit-identical to the input; every other entry is -inf.
 Rows are built to reach every path of the kernel: ordinary rows, rows with
 many equal logits, rows whose crossing bin holds more than the 512 tokens
 ranked directly (all logits equal; a dense f32 cluster), NaN and -inf
-entries, a vocabulary of one, and the full 128256-token vocabulary.
+entries, logits around 3e5, a vocabulary of one, and the full 128256-token
+vocabulary.
 """
 import numpy as np
 import pytest
@@ -73,6 +74,8 @@ def rows_for(kind, rows, V, dt, seed):
         x = torch.rand(rows, V, generator=g) * 0.01
     elif kind == "neginf":
         x[:, ::3] = float("-inf")
+    elif kind == "huge":                     # |max logit / T| above 2^18
+        x = 3.0e5 + torch.randn(rows, V, generator=g) * 3.0
     elif kind == "sharp":                    # a few dominant tokens and a long tail
         x = torch.randn(rows, V, generator=g) * 1.0
         x[:, :5] += 12.0
@@ -82,7 +85,7 @@ def rows_for(kind, rows, V, dt, seed):
 CASES = [("normal", "bf16", 1000), ("normal", "f32", 1000), ("normal", "f16", 4099), ("ties", "bf16", 5000),
          ("equal", "bf16", 4096), ("equal", "f32", 3000), ("dense", "f32", 50000), ("neginf", "bf16", 777),
          ("sharp", "bf16", 32000), ("normal", "bf16", 1), ("normal", "bf16", 17), ("normal", "bf16", 128256),
-         ("normal", "f32", 128256)]
+         ("normal", "f32", 128256), ("huge", "f32", 5000)]
 
 
 @pytest.mark.parametrize("kind,dt,V", CASES, ids=["%s-%s-%d" % c for c in CASES])
