@@ -93,7 +93,8 @@ enum {
   SV_DEV_BAD_BLOCK = 2,     /* block-table entry outside [0, num_blocks)             */
   SV_DEV_BAD_TOKEN = 4,     /* draft token outside [0, V)                             */
   SV_DEV_TIMEOUT = 8,       /* a bounded wait on an asynchronous copy ran out        */
-  SV_DEV_NONFINITE = 16     /* a logit row's maximum is not finite                   */
+  SV_DEV_NONFINITE = 16,    /* a logit row's maximum is not finite                   */
+  SV_DEV_BAD_TREE = 32      /* a draft-tree parent index is not a valid BFS parent   */
 };
 
 /* Strides of the paged pools in elements (d_head is contiguous). Each must be
@@ -185,6 +186,37 @@ sv_status spec_verify_attn_ex(const void *q, sv_dtype q_dtype,
                               void *out, sv_dtype out_dtype,
                               void *workspace, size_t workspace_bytes,
                               int32_t *dev_status, int blocks_per_split, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * spec_verify_attn_tree
+ *   Tree verification ("KV Cache + Speculative Decoding", Q14 and section
+ *   8.2): the n_new new positions of sequence b are the nodes of a draft
+ *   tree flattened in BFS order, node 0 the root (the last accepted token).
+ *   Query j sees every cached key before the new positions and, of the new
+ *   positions, exactly its ancestors A(j) (j itself included): key
+ *   seq_lens[b] - n_new + i is visible to query j iff i is in A(j). A chain
+ *   (tree_parent[b][j] = j - 1) gives spec_verify_attn's causal mask.
+ *   tree_parent: int32 [B][n_new] device; tree_parent[b][0] = -1 and
+ *   0 <= tree_parent[b][j] < j for j >= 1; a node with another parent sets
+ *   SV_DEV_BAD_TREE and is given the chain mask. n_new <= 64. Other
+ *   arguments, layouts and support as for spec_verify_attn; the workspace
+ *   is spec_verify_attn_tree_workspace_size(...) bytes (spec_verify_attn's
+ *   plus 8 bytes per node for the ancestor masks).
+ * ------------------------------------------------------------------------ */
+size_t spec_verify_attn_tree_workspace_size(int B, int n_new, int H_q, int H_kv, int d_head,
+                                            int max_blocks_per_seq, int block_size);
+
+sv_status spec_verify_attn_tree(const void *q, sv_dtype q_dtype,
+                                const void *k_cache, const void *v_cache, sv_dtype kv_dtype,
+                                const sv_kv_layout *layout,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, int max_blocks_per_seq,
+                                const int32_t *seq_lens, const int32_t *tree_parent,
+                                int B, int n_new, int H_q, int H_kv, int d_head, int block_size,
+                                int num_blocks, float softmax_scale,
+                                void *out, sv_dtype out_dtype,
+                                void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * spec_verify_sample

@@ -27,7 +27,8 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 
 SV_F32, SV_BF16, SV_F16, SV_FP8_E4M3 = 0, 1, 2, 3
 SV_SAMPLE_FORCE_EXACT = 1
-DEV_STATUS_BITS = {1: "BAD_SEQ_LEN", 2: "BAD_BLOCK", 4: "BAD_TOKEN", 8: "TIMEOUT", 16: "NONFINITE"}
+DEV_STATUS_BITS = {1: "BAD_SEQ_LEN", 2: "BAD_BLOCK", 4: "BAD_TOKEN", 8: "TIMEOUT", 16: "NONFINITE",
+                   32: "BAD_TREE"}
 _STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
            4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT", 6: "SV_ERR_OUT_OF_BLOCKS"}
 SV_ERR_OUT_OF_BLOCKS = 6
@@ -76,6 +77,10 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_attn.argtypes = attn_args + [P]
     lib.spec_verify_attn_ex.restype = I
     lib.spec_verify_attn_ex.argtypes = attn_args + [I, P]
+    lib.spec_verify_attn_tree_workspace_size.restype = Z
+    lib.spec_verify_attn_tree_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.spec_verify_attn_tree.restype = I
+    lib.spec_verify_attn_tree.argtypes = attn_args[:11] + [P] + attn_args[11:] + [P]
     lib.spec_verify_sample_workspace_size.restype = Z
     lib.spec_verify_sample_workspace_size.argtypes = [I, I, I]
     samp_args = [P, I, P, I, I, P, P, I, I, I, F, P, P, P, P, P, Z, P]
@@ -200,12 +205,15 @@ def alloc_workspace(nbytes, device):
 
 def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=None, k_scale=None,
                      v_scale=None, block_size=16, out=None, workspace=None, status=None,
-                     blocks_per_split=None, layout=None, num_blocks=None, H_kv=None):
+                     blocks_per_split=None, layout=None, num_blocks=None, H_kv=None, tree_parent=None):
     """Paged GQA verify attention. q [B, n_new, H_q, d]; caches [num_blocks, H_kv, bs, d],
     or, with `layout` = (block, head, slot) strides in elements, flat views whose first
-    element is (block 0, head 0, slot 0) plus explicit num_blocks and H_kv."""
+    element is (block 0, head 0, slot 0) plus explicit num_blocks and H_kv.
+    tree_parent (int32 [B, n_new], optional): the new positions are a draft tree in BFS
+    order and each query sees only its ancestors among them."""
     lib = load_library()
-    _cuda(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, out, workspace, status)
+    _cuda(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, out, workspace, status,
+          tree_parent)
     B, n_new, H_q, d = q.shape
     if layout is None:
         num_blocks_, H_kv = k_cache.shape[0], k_cache.shape[1]
@@ -218,7 +226,12 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=N
     if out is None:
         out = torch.empty_like(q)
     max_blocks = block_table.shape[1]
-    need = attn_workspace_size(B, n_new, H_q, H_kv, d, max_blocks, block_size, blocks_per_split)
+    if tree_parent is not None:
+        if blocks_per_split is not None:
+            raise ValueError("blocks_per_split is not available with tree_parent")
+        need = lib.spec_verify_attn_tree_workspace_size(B, n_new, H_q, H_kv, d, max_blocks, block_size)
+    else:
+        need = attn_workspace_size(B, n_new, H_q, H_kv, d, max_blocks, block_size, blocks_per_split)
     if workspace is None:
         workspace = alloc_workspace(need, q.device)
     args = [_ptr(q), _dtype_code(q), _ptr(k_cache), _ptr(v_cache), _dtype_code(k_cache, True),
@@ -226,7 +239,9 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=N
             _ptr(seq_lens), B, n_new, H_q, H_kv, d, block_size, num_blocks_, float(softmax_scale),
             _ptr(out), _dtype_code(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _ptr(status)]
-    if blocks_per_split is None:
+    if tree_parent is not None:
+        _check(lib.spec_verify_attn_tree(*args[:11], _ptr(tree_parent), *args[11:], _stream()))
+    elif blocks_per_split is None:
         _check(lib.spec_verify_attn(*args, _stream()))
     else:
         _check(lib.spec_verify_attn_ex(*args, int(blocks_per_split), _stream()))

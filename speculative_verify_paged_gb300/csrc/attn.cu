@@ -140,6 +140,7 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   float *ws_acc;   // [B][H_kv][S][R][kD]
   float *ws_ml;    // [B][H_kv][S][R][2]
   const int32_t *order;   // work items s + S (g + H_kv b), longest first (tcgen05 kernel)
+  const uint64_t *anc;    // [B][n_new] ancestor masks of a draft tree (NULL: a chain)
   int32_t *status;
   int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
   int role[3];        // tensor-map dims 1..3 hold (0 = slot, 1 = kv head, 2 = block)
@@ -306,6 +307,10 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
   // last visible absolute key position of the two rows of this thread
   const int lim_lo = L - P.n_new + min(r_lo, P.R - 1) / P.G;
   const int lim_hi = L - P.n_new + min(r_hi, P.R - 1) / P.G;
+  // draft tree: of the new keys, only the row's ancestors are visible
+  const uint64_t anc_lo = P.anc ? __ldg(P.anc + (int64_t)b * P.n_new + min(r_lo, P.R - 1) / P.G) : ~0ull;
+  const uint64_t anc_hi = P.anc ? __ldg(P.anc + (int64_t)b * P.n_new + min(r_hi, P.R - 1) / P.G) : ~0ull;
+  const int first_new = L - P.n_new;
 
   float o[16][4];
 #pragma unroll
@@ -433,7 +438,10 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
             for (int e = 0; e < 4; ++e) {
               const int t = t0 + n * 8 + 2 * tq + (e & 1);
               const int lim = (e < 2) ? lim_lo : lim_hi;
-              x[2 * j + n][e] = (valid && t <= lim) ? sacc[2 * j + n][e] * scale_log2 : -INFINITY;
+              const uint64_t anc = (e < 2) ? anc_lo : anc_hi;
+              const int rel = t - first_new;
+              const bool in_tree = rel < 0 || ((anc >> (rel & 63)) & 1ull);
+              x[2 * j + n][e] = (valid && t <= lim && in_tree) ? sacc[2 * j + n][e] * scale_log2 : -INFINITY;
             }
           }
         }
@@ -987,6 +995,8 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
       const bool live = row < R;
       const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
       const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
+      // draft tree: of the new keys, only the row's ancestors are visible
+      const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
       const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
       const float sl2 = P.scale_log2;
       {
@@ -1046,6 +1056,13 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
 #pragma unroll
             for (int k = 0; k < kT5N; ++k)
               if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
+            if (P.anc) {   // draft tree: new keys off the row's ancestor path go too
+#pragma unroll
+              for (int k = 0; k < kT5N; ++k) {
+                const int rel = key0 + k - (L - P.n_new);
+                if (rel >= 0 && !((anc >> (rel & 63)) & 1ull)) x[k] = -INFINITY;
+              }
+            }
           }
           float mx = -INFINITY;
 #pragma unroll
@@ -1182,6 +1199,7 @@ struct GenParams {
   const int32_t *seq_lens;
   float *ws_acc;   // [B][H_kv][S][R][d]
   float *ws_ml;    // [B][H_kv][S][R][2]
+  const uint64_t *anc;    // [B][n_new] ancestor masks of a draft tree (NULL: a chain)
   int32_t *status;
   int B, n_new, H_q, H_kv, G, R, d, bs, max_blocks, num_blocks, bps, S;
   int64_t block_stride, head_stride, slot_stride;
@@ -1268,8 +1286,10 @@ __global__ void __launch_bounds__(kGenThreads) attn_generic_kernel(const __grid_
     for (int r = warp; r < R; r += blockDim.x / 32) {
       const int t = t0 + lane;
       const int lim = L - P.n_new + r / P.G;
+      const int rel = t - (L - P.n_new);
+      const bool in_tree = !P.anc || rel < 0 || ((__ldg(P.anc + (int64_t)b * P.n_new + r / P.G) >> (rel & 63)) & 1ull);
       float sc = -INFINITY;
-      if (t < t_end && t <= lim) {
+      if (t < t_end && t <= lim && in_tree) {
         float acc = 0.f;
         for (int c = 0; c < d; ++c) acc = fmaf(q_s[r * d + c], k_s[lane * d + c], acc);
         sc = acc * P.scale_log2;
@@ -1602,6 +1622,34 @@ size_t ws_bytes(const Plan &p, int B, int H_kv) {
          align_up((size_t)B * H_kv * p.S * sizeof(int32_t), 256);
 }
 
+// Ancestor masks of the draft trees: bit i of anc[b][j] is set iff node i is
+// node j or one of its ancestors ("KV Cache + Speculative Decoding", Q14 and
+// section 8.2: tree nodes flattened in BFS order, mask M[j][i] = 1 iff i is
+// in A(j), the ancestors of j including j). One CTA per sequence, one thread
+// per node; parents are checked (node 0 the root with parent -1, else
+// 0 <= parent[j] < j, which BFS order guarantees), and a node with a bad
+// parent gets the chain mask of its position and sets SV_DEV_BAD_TREE.
+__global__ void __launch_bounds__(64) attn_tree_kernel(const int32_t *parent, int n_new, uint64_t *anc,
+                                                       int32_t *status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int par[64];
+  const int b = blockIdx.x, j = threadIdx.x;
+  if (j < n_new) par[j] = __ldg(parent + (int64_t)b * n_new + j);
+  __syncthreads();
+  if (j >= n_new) return;
+  bool ok = true;
+  for (int i = 0; i <= j; ++i) ok &= (i == 0) ? par[0] == -1 : (par[i] >= 0 && par[i] < i);
+  uint64_t m = 1ull << j;
+  if (ok) {
+    for (int p = par[j]; p >= 0; p = par[p]) m |= 1ull << p;   // strictly decreasing: at most j steps
+  } else {
+    m = (j == 63) ? ~0ull : ((1ull << (j + 1)) - 1ull);
+    atomic_or_status(status, SV_DEV_BAD_TREE);
+  }
+  anc[(int64_t)b * n_new + j] = m;
+}
+
 template <int RT, bool FP8>
 sv_status launch_tc(const TcParams &P, cudaStream_t st) {
   using Cfg = TcCfg<RT, FP8>;
@@ -1658,9 +1706,11 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
                            const int32_t *seq_lens, int B, int n_new, int H_q, int H_kv, int d_head,
                            int block_size, int num_blocks, float softmax_scale, void *out, sv_dtype out_dtype,
                            void *workspace, size_t workspace_bytes, int32_t *dev_status, int bps_req,
-                           sv_stream_t stream) {
+                           const int32_t *tree_parent, sv_stream_t stream) {
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
     return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: null pointer argument");
+  if (tree_parent && n_new > 64)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn_tree: at most 64 tree nodes (n_new = %d)", n_new);
   if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || d_head < 1 || block_size < 1 || num_blocks < 1 ||
       max_blocks_per_seq < 1)
     return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: bad sizes");
@@ -1682,7 +1732,8 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
   const Plan plan = make_plan(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, kv_dtype, q_dtype,
                               layout, bps_req);
   if (plan.R > 65535) return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: too many query rows per kv head");
-  const size_t need = ws_bytes(plan, B, H_kv);
+  const size_t base_need = ws_bytes(plan, B, H_kv);
+  const size_t need = base_need + (tree_parent ? align_up((size_t)B * n_new * sizeof(uint64_t), 256) : 0);
   if (!workspace || workspace_bytes < need)
     return fail(SV_ERR_WORKSPACE, "spec_verify_attn: workspace needs %zu bytes", need);
   if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_attn: workspace not 256-byte aligned");
@@ -1703,6 +1754,13 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
   const float scale_log2 = (float)((double)softmax_scale * 1.4426950408889634074);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   sv_status rc;
+  uint64_t *anc = nullptr;
+  if (tree_parent) {
+    anc = reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(workspace) + base_need);
+    launch_k(attn_tree_kernel, dim3(B), dim3(64), 0, st, 1, tree_parent, n_new, anc, dev_status);
+    rc = check_launch("spec_verify_attn_tree ancestor launch");
+    if (rc != SV_OK) return rc;
+  }
   if (plan.tc) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
     if (!enc) return fail(SV_ERR_CUDA, "spec_verify_attn: cuTensorMapEncodeTiled unavailable");
@@ -1750,7 +1808,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
       if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
     }
     P.q = q; P.out = out; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
-    P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
+    P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status; P.anc = anc;
     P.order = reinterpret_cast<const int32_t *>(reinterpret_cast<uint8_t *>(ws_ml) +
                                                 align_up(ent * 2 * sizeof(float), 256));
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
@@ -1771,6 +1829,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     GenParams P;
     P.q = q; P.out = out; P.k_cache = k_cache; P.v_cache = v_cache; P.k_scale = k_scale; P.v_scale = v_scale;
     P.block_table = block_table; P.seq_lens = seq_lens; P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status;
+    P.anc = anc;
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R; P.d = d_head; P.bs = block_size;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
     P.block_stride = block_stride; P.head_stride = head_stride; P.slot_stride = slot_stride;
@@ -1828,7 +1887,7 @@ extern "C" sv_status spec_verify_attn(const void *q, sv_dtype q_dtype, const voi
                                       int32_t *dev_status, sv_stream_t stream) {
   return attn_impl(q, q_dtype, k_cache, v_cache, kv_dtype, layout, k_scale, v_scale, block_table,
                    max_blocks_per_seq, seq_lens, B, n_new, H_q, H_kv, d_head, block_size, num_blocks,
-                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, 0, stream);
+                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, 0, nullptr, stream);
 }
 
 extern "C" sv_status spec_verify_attn_ex(const void *q, sv_dtype q_dtype, const void *k_cache,
@@ -1843,5 +1902,26 @@ extern "C" sv_status spec_verify_attn_ex(const void *q, sv_dtype q_dtype, const 
   return attn_impl(q, q_dtype, k_cache, v_cache, kv_dtype, layout, k_scale, v_scale, block_table,
                    max_blocks_per_seq, seq_lens, B, n_new, H_q, H_kv, d_head, block_size, num_blocks,
                    softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, blocks_per_split,
-                   stream);
+                   nullptr, stream);
+}
+
+extern "C" size_t spec_verify_attn_tree_workspace_size(int B, int n_new, int H_q, int H_kv, int d_head,
+                                                       int max_blocks_per_seq, int block_size) {
+  const size_t base = spec_verify_attn_workspace_size(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size);
+  if (base == 0 && B > 0) return 0;
+  return base + align_up((size_t)B * n_new * sizeof(uint64_t), 256);
+}
+
+extern "C" sv_status spec_verify_attn_tree(const void *q, sv_dtype q_dtype, const void *k_cache, const void *v_cache,
+                                           sv_dtype kv_dtype, const sv_kv_layout *layout, const float *k_scale,
+                                           const float *v_scale, const int32_t *block_table,
+                                           int max_blocks_per_seq, const int32_t *seq_lens,
+                                           const int32_t *tree_parent, int B, int n_new, int H_q, int H_kv,
+                                           int d_head, int block_size, int num_blocks, float softmax_scale,
+                                           void *out, sv_dtype out_dtype, void *workspace,
+                                           size_t workspace_bytes, int32_t *dev_status, sv_stream_t stream) {
+  if (!tree_parent) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn_tree: tree_parent is NULL");
+  return attn_impl(q, q_dtype, k_cache, v_cache, kv_dtype, layout, k_scale, v_scale, block_table,
+                   max_blocks_per_seq, seq_lens, B, n_new, H_q, H_kv, d_head, block_size, num_blocks,
+                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, 0, tree_parent, stream);
 }

@@ -1,0 +1,116 @@
+"""Draft-tree verify attention on the GPU against the oracle (C ABI).
+
+Every cache dtype path (the tcgen05 bf16 kernel, the fp8 mma.sync kernel,
+the fp32 kernel) runs random BFS trees of 2 to 64 nodes against the fp64
+oracle at the attention tolerances; a chain given as a tree must reproduce
+the causal call bit for bit; a bad parent must be flagged; and the 70B
+layer shape runs with a five-node tree on sampled sequences.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as oatt
+from parity_utils import attn_tolerance
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_verify_paged_gb300 as sv
+    sv.load_library()
+    return sv
+
+
+def random_trees(B, n, seed):
+    rng = np.random.default_rng(seed)
+    out = np.empty((B, n), dtype=np.int32)
+    for b in range(B):
+        out[b, 0] = -1
+        for j in range(1, n):
+            # mostly shallow, bushy trees (the shape speculative trees take),
+            # sometimes a long branch
+            out[b, j] = rng.integers(max(0, j - 3), j) if rng.random() < 0.3 else rng.integers(0, max(1, j // 2 + 1))
+    return out
+
+
+def run(sv, cfg, a, parents, status=None):
+    st = torch.zeros(1, dtype=torch.int32, device=DEV) if status is None else status
+    out = sv.spec_verify_attn(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"],
+                              1 / math.sqrt(cfg.d_head), a["k_scale"], a["v_scale"], block_size=cfg.block_size,
+                              status=st, tree_parent=parents)
+    torch.cuda.synchronize()
+    return out, int(st.item())
+
+
+CASES = [
+    ("f32", {}, 6),
+    ("bf16", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128}, 8),
+    ("bf16_g8_n16", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 16, "H_kv": 2,
+                     "ctx": ("fixed", (40, 700))}, 16),
+    ("bf16_n64", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 2, "H_kv": 1,
+                  "ctx": ("fixed", (64, 300))}, 64),
+    ("fp8", {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 128, "H_q": 8, "H_kv": 2}, 8),
+    ("fp8_n32", {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 128, "H_q": 4, "H_kv": 2,
+                 "ctx": ("fixed", (100, 33))}, 32),
+]
+
+
+@pytest.mark.parametrize("name,over,n_new", CASES, ids=[c[0] for c in CASES])
+def test_tree_matches_oracle(sv, name, over, n_new):
+    cfg = workloads.CONFIGS["tiny"].with_(K=n_new - 1, **over)
+    a = workloads.make_attention_inputs(cfg, seed=n_new)
+    parents = random_trees(cfg.B, n_new, seed=n_new)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
+    out, st = run(sv, cfg, g, torch.from_numpy(parents).to(DEV))
+    assert st == 0
+    ref = oatt.verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"],
+                                1 / math.sqrt(cfg.d_head), cfg.block_size, cfg.kv_dtype, a["k_scale"],
+                                a["v_scale"], tree_parent=torch.from_numpy(parents))
+    err = np.abs(out.float().cpu().numpy() - ref).max()
+    assert err <= attn_tolerance(cfg.kv_dtype), "max abs error %.3g" % err
+
+
+@pytest.mark.parametrize("name,over,n_new", CASES[:2] + CASES[4:5], ids=[c[0] for c in CASES[:2] + CASES[4:5]])
+def test_chain_tree_is_the_causal_call(sv, name, over, n_new):
+    cfg = workloads.CONFIGS["tiny"].with_(K=n_new - 1, **over)
+    a = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v)
+         for k, v in workloads.make_attention_inputs(cfg, seed=3).items()}
+    chain = torch.arange(-1, n_new - 1, dtype=torch.int32).repeat(cfg.B, 1).to(DEV)
+    out_t, st = run(sv, cfg, a, chain)
+    out_c = sv.spec_verify_attn(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"],
+                                1 / math.sqrt(cfg.d_head), a["k_scale"], a["v_scale"], block_size=cfg.block_size)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert torch.equal(out_t, out_c)
+
+
+def test_bad_parent_is_flagged(sv):
+    cfg = workloads.CONFIGS["tiny"].with_(K=4, kv_dtype="bf16", q_dtype="bf16", d_head=128)
+    a = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v)
+         for k, v in workloads.make_attention_inputs(cfg, seed=5).items()}
+    parents = torch.tensor([[-1, 0, 0, 3, 1], [-1, 0, 1, 2, 3]], dtype=torch.int32, device=DEV)  # 3 -> 3
+    _, st = run(sv, cfg, a, parents)
+    assert st & 32
+
+
+def test_tree_full_size_70b(sv):
+    # the 70B layer shape with a five-node tree: root, two children, one
+    # grandchild under each (K + 1 = 5 positions as in the chain workload)
+    cfg = workloads.CONFIGS["llama3_70b"]
+    a = workloads.make_attention_inputs(cfg, seed=0, device=DEV)
+    parents = torch.tensor([-1, 0, 0, 1, 2], dtype=torch.int32).repeat(cfg.B, 1)
+    out, st = run(sv, cfg, a, parents.to(DEV))
+    assert st == 0
+    idx = [0, 17, 40, 63]
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in a.items()}
+    ref = oatt.verify_attention(cpu["q"], cpu["k_cache"], cpu["v_cache"], cpu["block_table"], cpu["seq_lens"],
+                                1 / math.sqrt(cfg.d_head), cfg.block_size, cfg.kv_dtype, cpu["k_scale"],
+                                cpu["v_scale"], batch_indices=idx, tree_parent=parents)
+    err = np.abs(out.float().cpu().numpy()[idx] - ref[idx]).max()
+    assert err <= attn_tolerance(cfg.kv_dtype), "max abs error %.3g" % err

@@ -128,6 +128,18 @@ def test_topp_host_validation_and_workspace(lib):
     assert lib.spec_verify_sample_topp(*args(0.9, 0, 0, 0, 1 << 30)) == 2   # draft dtype mismatch
 
 
+def test_tree_attention_host_checks(lib):
+    fake = ctypes.c_void_p(0x1000)
+    NULL = None
+    base = lib.spec_verify_attn_workspace_size(64, 5, 64, 8, 128, 512, 16)
+    # the ancestor masks: 8 bytes per node, 256-byte rounded, after the usual workspace
+    assert lib.spec_verify_attn_tree_workspace_size(64, 5, 64, 8, 128, 512, 16) == base + (64 * 5 * 8 + 255) // 256 * 256
+    args = lambda tree, n_new: (fake, 1, fake, fake, 1, None, NULL, NULL, fake, 64, fake, tree,
+                                2, n_new, 8, 2, 128, 16, 100, 0.1, fake, 1, fake, 1 << 30, NULL, NULL)
+    assert lib.spec_verify_attn_tree(*args(NULL, 5)) == 1          # no parents
+    assert lib.spec_verify_attn_tree(*args(fake, 65)) == 2         # more than 64 nodes
+
+
 def test_product_path_has_no_cpu_fallback():
     """The binding raises when tensors are not on a CUDA device."""
     import torch
