@@ -198,3 +198,69 @@ def rejection_sample_chunked(target_logits, draft, draft_tokens, uniforms,
                                       draft_tokens[sel], uniforms[sel],
                                       draft_is_probs, temperature))
     return {k: np.concatenate([r[k] for r in parts]) for k in parts[0]}
+
+
+def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, uniforms,
+                          draft_is_probs=False, temperature=1.0):
+    """Verify a draft tree per sequence by recursive rejection sampling.
+
+    The pages give exact rejection sampling for a chain (quant67 section 3.1;
+    "KV Cache + Speculative Decoding" sections 7.1-7.3) and the BFS tree with
+    its ancestor mask (Q14, section 8.2), leaving the sampling rule over a
+    tree open ("standard rejection sampling" when exactness is wanted). The
+    reading taken here (the plainest exact one): walk from the root; at node
+    u the residual starts as r = p_u; its children, drafted from q_u, are
+    tried in BFS order, child c with token x accepted iff
+    uniforms[c][0] * q_u(x) < r(x); a rejection replaces r by
+    norm(max(0, r - q_u)); an accepted child becomes u; when every child of
+    u is rejected (or u is a leaf) the token is drawn from r by the inverse
+    CDF with v = uniforms[u][1]. For a chain this is rejection_sample.
+
+    target_logits [B, n, V]: row j is the target distribution after node j;
+    draft [B, n, V] logits (or probabilities): row u is what u's children
+    were drawn from; tree_parent [B, n] (node 0 the root, parent -1);
+    tree_tokens [B, n] (entry 0 unused); uniforms [B, n, 2].
+    Returns dict: out_tokens [B, n] (accepted tokens, the drawn one, then -1),
+    num_accepted [B], path_nodes [B, n] (accepted nodes, then -1) and
+    margin [B] (the smallest distance of a decision taken from its
+    boundary: |u - r/q| of every accept test and the CDF margin of the draw).
+    """
+    p_all = softmax(target_logits, temperature)
+    q_all = _np64(draft) if draft_is_probs else softmax(draft, temperature)
+    par = _np64(tree_parent).astype(np.int64)
+    tok = _np64(tree_tokens).astype(np.int64)
+    uv = _np64(uniforms)
+    B, n, V = p_all.shape
+    out = np.full((B, n), -1, dtype=np.int64)
+    path = np.full((B, n), -1, dtype=np.int64)
+    nacc = np.zeros(B, dtype=np.int64)
+    margin = np.full(B, np.inf)
+    for b in range(B):
+        u, depth = 0, 0
+        while True:
+            r = p_all[b, u].copy()
+            q = q_all[b, u]
+            accepted = -1
+            for c in [c for c in range(1, n) if par[b, c] == u]:
+                x = tok[b, c]
+                accept = uv[b, c, 0] * q[x] < r[x]
+                ratio = r[x] / q[x] if q[x] > 0 else np.inf
+                margin[b] = min(margin[b], abs(uv[b, c, 0] - ratio))
+                if accept:
+                    accepted = c
+                    break
+                res = np.maximum(0.0, r - q)
+                z = res.sum()
+                r = res / z if z > 0 else p_all[b, u].copy()   # z = 0 cannot happen in exact arithmetic
+            if accepted >= 0:
+                out[b, depth] = tok[b, accepted]
+                path[b, depth] = accepted
+                depth += 1
+                u = accepted
+                continue
+            y, m, _ = inverse_cdf(r[None, :], np.array([uv[b, u, 1]]))
+            out[b, depth] = y[0]
+            margin[b] = min(margin[b], m[0])
+            nacc[b] = depth
+            break
+    return {"out_tokens": out, "num_accepted": nacc, "path_nodes": path, "margin": margin}

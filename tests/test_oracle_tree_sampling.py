@@ -1,0 +1,133 @@
+"""Pins of the tree rejection-sampling oracle.
+
+- A chain given as a tree (node j + 1 is draft j, drafted from row j) gives
+  the chain oracle's tokens and accepted lengths exactly (uniform indices
+  mapped: node j + 1 takes draft j's accept uniform, node j the draw of row
+  j).
+- The reading's exactness, by exact enumeration with Fractions: siblings
+  drawn i.i.d. from q_u and tried in turn against the running residual give
+  a first emitted token distributed exactly as p_u, for any p and q (the
+  property that makes recursive rejection exact; it fails for a plain
+  "retry with p" rule, which the same enumeration shows).
+- The oracle's code against that law: Monte Carlo over random uniforms and
+  i.i.d. sibling tokens, within 4.5 sigma per token.
+"""
+from fractions import Fraction as F
+
+import numpy as np
+import pytest
+
+from oracle import sampling
+
+
+def chain_case(rng, B, K, V):
+    tl = rng.normal(0, 2, (B, K + 1, V))
+    dl = tl[:, :K] + rng.normal(0, 1, (B, K, V))
+    q = sampling.softmax(dl)
+    tok = np.array([[rng.choice(V, p=q[b, i]) for i in range(K)] for b in range(B)])
+    uv = rng.uniform(0, 1, (B, K + 1, 2))
+    return tl, dl, tok, uv
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_chain_tree_is_the_chain(seed):
+    rng = np.random.default_rng(seed)
+    B, K, V = 16, int(rng.integers(1, 6)), int(rng.integers(3, 40))
+    tl, dl, tok, uv = chain_case(rng, B, K, V)
+    ref = sampling.rejection_sample(tl, dl, tok, uv)
+    n = K + 1
+    parent = np.tile(np.arange(-1, n - 1), (B, 1))
+    ttok = np.concatenate([np.zeros((B, 1), dtype=np.int64), tok], axis=1)
+    tdraft = np.concatenate([dl, np.zeros((B, 1, V))], axis=1)       # the leaf's row is unused
+    tuv = np.empty((B, n, 2))
+    tuv[:, 1:, 0] = uv[:, :K, 0]
+    tuv[:, 0, 0] = 0.5
+    tuv[:, :, 1] = uv[:, :, 1]
+    got = sampling.tree_rejection_sample(tl, tdraft, parent, ttok, tuv)
+    assert np.array_equal(got["num_accepted"], ref["num_accepted"])
+    assert np.array_equal(got["out_tokens"], ref["out_tokens"])
+    for b in range(B):
+        assert list(got["path_nodes"][b, :ref["num_accepted"][b]]) == list(range(1, ref["num_accepted"][b] + 1))
+
+
+def first_token_law(p, q, k, residual=True):
+    """Exact law of the first emitted token when k siblings are drawn i.i.d.
+    from q and tried in turn (each sibling a leaf: an accepted one is the
+    emitted token). residual=False retries every sibling against p itself."""
+    V = len(p)
+    law = [F(0)] * V
+
+    def walk(r, left, weight):
+        if left == 0:
+            for y in range(V):
+                law[y] += weight * r[y]
+            return
+        for x in range(V):
+            if q[x] == 0:
+                continue
+            acc = min(F(1), r[x] / q[x])
+            law[x] += weight * q[x] * acc
+            if acc < 1:
+                if residual:
+                    res = [max(F(0), r[i] - q[i]) for i in range(V)]
+                    z = sum(res)
+                    nr = [v / z for v in res] if z > 0 else list(p)
+                else:
+                    nr = list(p)
+                walk(nr, left - 1, weight * q[x] * (1 - acc))
+
+    walk(list(p), k, F(1))
+    return law
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+@pytest.mark.parametrize("case", range(4))
+def test_sibling_rule_is_exact(k, case):
+    rng = np.random.default_rng(100 + case)
+    V = 3 + case % 2
+    p = [F(int(a), 64) for a in rng.multinomial(64, np.ones(V) / V)]
+    q = [F(int(a), 64) for a in rng.multinomial(64, np.ones(V) / V)]
+    assert first_token_law(p, q, k) == p
+    if k > 1 and p != q:
+        # the rule without the residual update is not exact on some case
+        pass
+
+
+def test_retrying_against_p_is_not_exact():
+    p = [F(1, 2), F(1, 4), F(1, 4)]
+    q = [F(1, 8), F(3, 4), F(1, 8)]
+    assert first_token_law(p, q, 2, residual=True) == p
+    assert first_token_law(p, q, 2, residual=False) != p
+
+
+def test_oracle_sibling_law_monte_carlo():
+    rng = np.random.default_rng(7)
+    V, N = 4, 40000
+    p = np.array([0.45, 0.3, 0.15, 0.1])
+    q = np.array([0.1, 0.2, 0.3, 0.4])
+    # root with three leaf children; logits are log-probabilities
+    tl = np.tile(np.log(p), (N, 4, 1))
+    dl = np.tile(np.log(q), (N, 4, 1))
+    parent = np.tile(np.array([-1, 0, 0, 0]), (N, 1))
+    tok = np.zeros((N, 4), dtype=np.int64)
+    tok[:, 1:] = rng.choice(V, size=(N, 3), p=q)
+    uv = rng.uniform(0, 1, (N, 4, 2))
+    got = sampling.tree_rejection_sample(tl, dl, parent, tok, uv)
+    first = got["out_tokens"][:, 0]
+    freq = np.bincount(first, minlength=V) / N
+    sigma = np.sqrt(p * (1 - p) / N)
+    assert np.all(np.abs(freq - p) < 4.5 * sigma), (freq, p)
+
+
+def test_siblings_are_tried_in_bfs_order_by_hand():
+    # q = p, so every child is accepted: the first child in BFS order wins
+    # (token 2 of node 1), then node 1 is a leaf and its row (one-hot on
+    # token 0) gives the bonus
+    V = 3
+    tl = np.log(np.array([[[1 / 3, 1 / 3, 1 / 3], [1.0, 1e-30, 1e-30], [1e-30, 1.0, 1e-30]]]))
+    dl = tl.copy()
+    got = sampling.tree_rejection_sample(tl, dl, np.array([[-1, 0, 0]]), np.array([[0, 2, 1]]),
+                                         np.full((1, 3, 2), 0.5))
+    assert got["num_accepted"][0] == 1
+    assert list(got["path_nodes"][0]) == [1, -1, -1]
+    assert list(got["out_tokens"][0]) == [2, 0, -1]
