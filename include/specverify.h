@@ -318,6 +318,41 @@ sv_status spec_verify_sample_topp(const void *target_logits, sv_dtype logit_dtyp
                                   int32_t *dev_status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * spec_verify_sample_tree
+ *   Rejection sampling over a draft tree (the BFS tree of
+ *   spec_verify_attn_tree; "KV Cache + Speculative Decoding", Q14 and
+ *   section 8.2, exact rejection of quant67 "speculative decoding" section
+ *   3.1). Per sequence, from the root u = 0: the residual starts as r = p_u;
+ *   u's children, drafted from q_u, are tried in BFS order, child c with
+ *   token x = tree_tokens[b][c] accepted iff uniforms[b][c][0] * q_u(x) <
+ *   r(x); a rejection replaces r by norm(max(0, r - q_u)); an accepted child
+ *   becomes u; when every child of u is rejected, or u is a leaf, the token
+ *   y = min{y : C(y) > v C(V-1)} is drawn from r (C the running sum in token
+ *   order, v = uniforms[b][u][1]). A chain is spec_verify_sample's rule.
+ *   target_logits: [B][n][V] (SV_F32, SV_BF16 or SV_F16), row j the target
+ *   distribution after node j; draft: [B][n][V] logits of the same dtype
+ *   (draft_is_probs == 0, softmax at T) or f32 probabilities, row u the
+ *   distribution u's children were drawn from (rows of leaves unused);
+ *   tree_parent: int32 [B][n] as for spec_verify_attn_tree; tree_tokens:
+ *   int32 [B][n] (entry 0 unused); uniforms: float [B][n][2] in [0, 1).
+ *   Outputs: out_tokens int32 [B][n] = the accepted tokens, the drawn one,
+ *   then -1; num_accepted int32 [B]; path_nodes int32 [B][n] = the accepted
+ *   nodes in order, then -1 (the caller keeps their K/V rows).
+ *   n <= 64, V <= 2^28, temperature > 0. A bad tree sets SV_DEV_BAD_TREE,
+ *   a token outside [0, V) SV_DEV_BAD_TOKEN (that child is never accepted),
+ *   a row without a finite maximum SV_DEV_NONFINITE.
+ *   fp32 arithmetic in a fixed order: deterministic, and equal to exact
+ *   arithmetic unless a uniform lies within ~1e-6 of its boundary.
+ *   No workspace.
+ * ------------------------------------------------------------------------ */
+sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype logit_dtype,
+                                  const void *draft, sv_dtype draft_dtype, int draft_is_probs,
+                                  const int32_t *tree_parent, const int32_t *tree_tokens,
+                                  const float *uniforms, int B, int n, int V, float temperature,
+                                  int32_t *out_tokens, int32_t *num_accepted, int32_t *path_nodes,
+                                  int32_t *dev_status, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * spec_verify_sample_static
  *   The pages have no counterpart to this call; it exists for callers that
  *   cannot allocate device memory when they verify a round (an engine that

@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_sample_topp_workspace_size.argtypes = [I, I, I, I, I]
     lib.spec_verify_sample_topp.restype = I
     lib.spec_verify_sample_topp.argtypes = [P, I, P, I, I, P, P, I, I, I, F, F, I, P, P, P, P, P, Z, P, P]
+    lib.spec_verify_sample_tree.restype = I
+    lib.spec_verify_sample_tree.argtypes = [P, I, P, I, I, P, P, P, I, I, I, F, P, P, P, P, P]
     I64, BMP = ctypes.c_int64, ctypes.c_void_p
     lib.sv_bm_create.restype = I
     lib.sv_bm_create.argtypes = [I, I, ctypes.POINTER(ctypes.c_void_p)]
@@ -323,6 +325,33 @@ def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_pr
     else:
         _check(lib.spec_verify_sample(*args, _stream()))
     return out_tokens, num_accepted, p_at_draft, q_at_draft
+
+
+def spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, uniforms, draft_is_probs=False,
+                            temperature=1.0, out_tokens=None, num_accepted=None, path_nodes=None, status=None):
+    """Rejection sampling over a draft tree of n nodes (BFS order, node 0 the root).
+
+    target_logits [B, n, V]; draft [B, n, V] logits (same dtype) or f32 probabilities;
+    tree_parent, tree_tokens int32 [B, n]; uniforms f32 [B, n, 2].
+    Returns (out_tokens [B, n], num_accepted [B], path_nodes [B, n]).
+    """
+    lib = load_library()
+    _cuda(target_logits, draft, tree_parent, tree_tokens, uniforms, out_tokens, num_accepted, path_nodes,
+          status)
+    B, n, V = target_logits.shape
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, n), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if path_nodes is None:
+        path_nodes = torch.empty((B, n), dtype=torch.int32, device=dev)
+    ddt = _dtype_code(draft) if draft is not None else SV_F32
+    _check(lib.spec_verify_sample_tree(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt,
+                                       int(bool(draft_is_probs)), _ptr(tree_parent), _ptr(tree_tokens),
+                                       _ptr(uniforms), B, n, V, float(temperature), _ptr(out_tokens),
+                                       _ptr(num_accepted), _ptr(path_nodes), _ptr(status), _stream()))
+    return out_tokens, num_accepted, path_nodes
 
 
 # ----------------------------------------------------------- verify step ---

@@ -1,0 +1,364 @@
+// Rejection sampling over a draft tree: one CTA per sequence walks the tree
+// from the root. At node u the residual starts as r = p_u; u's children
+// (drafted from q_u) are tried in BFS order, child c with token x accepted
+// iff uniforms[c][0] * q_u(x) < r(x); a rejection replaces r by
+// norm(max(0, r - q_u)); an accepted child becomes u; when every child of u
+// is rejected, or u is a leaf, the token is drawn from r by the inverse CDF
+// with v = uniforms[u][1] (the reading of "standard rejection sampling" over
+// the BFS tree of "KV Cache + Speculative Decoding", Q14 and section 8.2,
+// with the chain rule of quant67 "speculative decoding" section 3.1; for a
+// chain it is that rule).
+//
+// The residuals never need to be stored: after k rejections at u,
+//   r_k = max(0, p - c_k q) / D_k,  c_0 = 0, D_0 = 1,
+//   c_{k+1} = c_k + D_k,  D_{k+1} = sum_x max(0, p(x) - c_{k+1} q(x)),
+// (induction: max(0, r_k - q) = max(0, p - c_k q - D_k q) / D_k), so a
+// rejection costs one row-wide sum and the draw one more pass.
+//
+// Arithmetic is fp32 in a fixed order (each thread owns a contiguous chunk of
+// token ids, sums groups of 8, then a block tree), so the kernel is
+// deterministic; its decisions agree with exact arithmetic unless a uniform
+// lies within ~1e-6 (relative) of its boundary.
+
+#include <climits>
+#include <cmath>
+#include <type_traits>
+
+#include "sv_common.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kTrThreads = 1024;
+constexpr int kTrWarps = kTrThreads / 32;
+constexpr int kTrMaxNodes = 64;
+
+struct TreeParams {
+  const void *target;      // [B][n][V]
+  const void *draft;       // [B][n][V] logits (T) or probabilities (f32)
+  const int32_t *parent;   // [B][n]
+  const int32_t *tokens;   // [B][n]
+  const float *uniforms;   // [B][n][2]
+  int32_t *out_tokens;     // [B][n]
+  int32_t *num_acc;        // [B]
+  int32_t *path;           // [B][n]
+  int32_t *status;
+  int B, n, V, chunk;      // chunk: token ids per thread (a multiple of 8)
+  int vec_t, vec_d;        // rows 16-byte aligned: vector loads
+  float c;                 // log2(e) / T
+};
+
+__device__ __forceinline__ float tr_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float ld_f32(const float *p, int i) { return __ldg(p + i); }
+__device__ __forceinline__ float ld_f32(const __nv_bfloat16 *p, int i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float ld_f32(const __half *p, int i) { return __half2float(p[i]); }
+
+// Eight consecutive values starting at i (a multiple of 8) as floats.
+template <typename T>
+__device__ __forceinline__ void ld8(const T *row, int i, bool vec, float (&x)[8]) {
+  if (vec) {
+    if (sizeof(T) == 4) {
+      const float4 a = __ldg(reinterpret_cast<const float4 *>(row + i));
+      const float4 b = __ldg(reinterpret_cast<const float4 *>(row + i) + 1);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row + i));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (std::is_same<T, __nv_bfloat16>::value) {
+          x[2 * k] = __uint_as_float(w[k] << 16);
+          x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        } else {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+          x[2 * k] = f.x;
+          x[2 * k + 1] = f.y;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = ld_f32(row, i + k);
+  }
+}
+
+__device__ __forceinline__ float tr_block_sum(float v, float *s_red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float t = lane < kTrWarps ? s_red[lane] : 0.f;
+  t = warp_sum(t);
+  return t;   // every thread of warp 0..31 holds the total (all warps recompute it)
+}
+
+__device__ __forceinline__ float tr_block_max(float v, float *s_red) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float t = lane < kTrWarps ? s_red[lane] : -INFINITY;
+  return warp_max(t);
+}
+
+// Exclusive scan of one float per thread in thread order; *total the sum.
+__device__ __forceinline__ float tr_block_excl_scan(float v, float *s_red, float *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  float before = 0.f, tot = 0.f;
+  for (int w = 0; w < kTrWarps; ++w) {
+    const float x = s_red[w];
+    if (w < warp) before += x;
+    tot += x;
+  }
+  *total = tot;
+  return before + incl - v;
+}
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid_constant__ TreeParams P) {
+  using TD = typename std::conditional<DK == 1, float, T>::type;
+  __shared__ int par[kTrMaxNodes];
+  __shared__ int tok[kTrMaxNodes];
+  __shared__ float s_red[kTrWarps];
+  __shared__ int s_owner, s_y, s_first, s_last;
+
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, n = P.n, V = P.V;
+  const int tid = threadIdx.x;
+  if (tid < n) {
+    par[tid] = __ldg(P.parent + (int64_t)b * n + tid);
+    tok[tid] = __ldg(P.tokens + (int64_t)b * n + tid);
+  }
+  __syncthreads();
+  int32_t *out = P.out_tokens + (int64_t)b * n;
+  int32_t *path = P.path + (int64_t)b * n;
+  for (int j = tid; j < n; j += kTrThreads) { out[j] = -1; path[j] = -1; }
+  bool ok = par[0] == -1;
+  for (int j = 1; j < n; ++j) ok &= par[j] >= 0 && par[j] < j;
+  if (!ok) {
+    if (tid == 0) { atomic_or_status(P.status, SV_DEV_BAD_TREE); P.num_acc[b] = 0; }
+    return;
+  }
+
+  const float c = P.c;
+  const int lo = tid * P.chunk, hi = min(V, lo + P.chunk);
+  const int nfull = hi > lo ? (hi - lo) / 8 : 0;       // whole groups of 8 in this thread's chunk
+  const T *trow_base = static_cast<const T *>(P.target) + (int64_t)b * n * V;
+  const TD *drow_base = static_cast<const TD *>(P.draft) + (int64_t)b * n * V;
+  const bool vt = P.vec_t, vd = P.vec_d;
+
+  // f(x, id) over this thread's chunk of a row, in token order
+  auto each = [&](const auto *row, bool vec, auto f) {
+    for (int g = 0; g < nfull; ++g) {
+      float x[8];
+      ld8(row, lo + 8 * g, vec, x);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f(x[k], lo + 8 * g + k);
+    }
+    for (int i = lo + 8 * nfull; i < hi; ++i) f(ld_f32(row, i), i);
+  };
+  // (max, sum of 2^((l - max) c)) of a logit row
+  auto stats = [&](const auto *row, bool vec, float &m, float &s) {
+    float mx = -INFINITY;
+    each(row, vec, [&](float x, int) { mx = fmaxf(mx, x); });
+    m = tr_block_max(mx, s_red);
+    const float mc = __fmul_rn(m, c);
+    float acc = 0.f, grp = 0.f;
+    int k = 0;
+    each(row, vec, [&](float x, int) {
+      grp += tr_ex2(fmaf(x, c, -mc));
+      if (++k == 8) { acc += grp; grp = 0.f; k = 0; }
+    });
+    s = tr_block_sum(acc + grp, s_red);
+  };
+
+  int u = 0, depth = 0;
+  for (;;) {
+    const T *prow = trow_base + (int64_t)u * V;
+    const TD *qrow = drow_base + (int64_t)u * V;
+    float m_p, S_p, m_q = 0.f, S_q = 1.f;
+    stats(prow, vt, m_p, S_p);
+    const float mpc = __fmul_rn(m_p, c), inv_p = 1.f / S_p;
+    bool has_child = false;
+    for (int j = u + 1; j < n; ++j) has_child |= par[j] == u;
+    if (has_child && DK == 0) stats(qrow, vd, m_q, S_q);
+    if (!(m_p > -INFINITY && m_p < INFINITY) || (DK == 0 && has_child && !(m_q > -INFINITY && m_q < INFINITY))) {
+      // a row without a finite maximum: flagged, the walk stops here
+      if (tid == 0) { atomic_or_status(P.status, SV_DEV_NONFINITE); P.num_acc[b] = depth; }
+      return;
+    }
+    const float mqc = __fmul_rn(m_q, c), inv_q = 1.f / S_q;
+    auto p_of = [&](float l) { return tr_ex2(fmaf(l, c, -mpc)) * inv_p; };
+    auto q_of = [&](float l) { return DK == 1 ? l : tr_ex2(fmaf(l, c, -mqc)) * inv_q; };
+
+    float coef = 0.f, D = 1.f;   // the residual is max(0, p - coef q) / D
+    int accepted = -1;
+    for (int ch = u + 1; ch < n && accepted < 0; ++ch) {
+      if (par[ch] != u) continue;
+      const int x = tok[ch];
+      if (x < 0 || x >= V) {   // flagged; such a child is never accepted and changes nothing
+        if (tid == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+        continue;
+      }
+      const float px = p_of(ld_f32(prow, x)), qx = q_of(ld_f32(qrow, x));
+      const float rx = fmaxf(0.f, px - coef * qx) / D;
+      const float uu = __ldg(P.uniforms + ((int64_t)b * n + ch) * 2);
+      if (uu * qx < rx) {
+        accepted = ch;
+        break;
+      }
+      // rejected: the next residual
+      coef += D;
+      float acc = 0.f, grp = 0.f;
+      const T *pr = prow;
+      const TD *qr = qrow;
+      auto resid = [&](float lp, float lq) { return fmaxf(0.f, p_of(lp) - coef * q_of(lq)); };
+      for (int g = 0; g < nfull; ++g) {
+        float a[8], d[8];
+        ld8(pr, lo + 8 * g, vt, a);
+        ld8(qr, lo + 8 * g, vd, d);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) grp += resid(a[kk], d[kk]);
+        acc += grp;
+        grp = 0.f;
+      }
+      for (int i = lo + 8 * nfull; i < hi; ++i) acc += resid(ld_f32(pr, i), ld_f32(qr, i));
+      D = tr_block_sum(acc, s_red);
+      if (!(D > 0.f)) { coef = 0.f; D = 1.f; }   // cannot happen in exact arithmetic: draw from p
+    }
+    if (accepted >= 0) {
+      if (tid == 0) { out[depth] = tok[accepted]; path[depth] = accepted; }
+      ++depth;
+      u = accepted;
+      continue;
+    }
+
+    // ---- draw from max(0, p - coef q) (p itself when coef = 0) ----
+    auto w_of = [&](float lp, float lq) { return coef == 0.f ? p_of(lp) : fmaxf(0.f, p_of(lp) - coef * q_of(lq)); };
+    float mine = 0.f;
+    int first_pos = INT_MAX, last_pos = -1;
+    for (int g = 0; g < nfull; ++g) {
+      float a[8], d[8];
+      ld8(prow, lo + 8 * g, vt, a);
+      if (coef != 0.f) ld8(qrow, lo + 8 * g, vd, d);
+      float grp = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const float w = w_of(a[kk], coef != 0.f ? d[kk] : 0.f);
+        grp += w;
+        if (w > 0.f) { first_pos = min(first_pos, lo + 8 * g + kk); last_pos = lo + 8 * g + kk; }
+      }
+      mine += grp;
+    }
+    for (int i = lo + 8 * nfull; i < hi; ++i) {
+      const float w = w_of(ld_f32(prow, i), coef != 0.f ? ld_f32(qrow, i) : 0.f);
+      mine += w;
+      if (w > 0.f) { first_pos = min(first_pos, i); last_pos = i; }
+    }
+    float Z;
+    const float before = tr_block_excl_scan(mine, s_red, &Z);
+    const float target = __ldg(P.uniforms + ((int64_t)b * n + u) * 2 + 1) * Z;
+    if (tid == 0) { s_owner = 0; s_y = -1; s_first = INT_MAX; s_last = -1; }
+    __syncthreads();
+    // the chunk holding y = min{y : C(y) > v Z}: the last one whose running
+    // sum before it is <= v Z (prefix sums in thread order are one scan, so
+    // every thread sees the same boundaries)
+    if (before <= target) atomicMax(&s_owner, tid);
+    __syncthreads();
+    const int owner = s_owner;
+    if (tid == owner) {
+      float cum = before;
+      for (int i = lo; i < hi; ++i) {
+        cum += w_of(ld_f32(prow, i), coef != 0.f ? ld_f32(qrow, i) : 0.f);
+        if (cum > target) { s_y = i; break; }
+      }
+    }
+    if (tid > owner) atomicMin(&s_first, first_pos);
+    atomicMax(&s_last, last_pos);
+    __syncthreads();
+    // rounding can leave v Z past the owner's chunk: then the next token with
+    // weight, or the last one with weight when there is none after it
+    int y = s_y >= 0 ? s_y : (s_first != INT_MAX ? s_first : s_last);
+    if (tid == 0) {
+      out[depth] = y;
+      P.num_acc[b] = depth;
+    }
+    return;
+  }
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype logit_dtype, const void *draft,
+                                             sv_dtype draft_dtype, int draft_is_probs,
+                                             const int32_t *tree_parent, const int32_t *tree_tokens,
+                                             const float *uniforms, int B, int n, int V, float temperature,
+                                             int32_t *out_tokens, int32_t *num_accepted, int32_t *path_nodes,
+                                             int32_t *dev_status, sv_stream_t stream) {
+  using namespace sv;
+  if (B < 0 || n < 1 || V < 1)
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: bad sizes B=%d n=%d V=%d", B, n, V);
+  if (n > kTrMaxNodes) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: at most 64 tree nodes");
+  if (V > (1 << 28)) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: V above 2^28");
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: temperature must be finite and > 0");
+  if (!target_logits || !tree_parent || !tree_tokens || !uniforms || !out_tokens || !num_accepted || !path_nodes ||
+      (n > 1 && !draft))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: null pointer argument");
+  if (logit_dtype != SV_F32 && logit_dtype != SV_BF16 && logit_dtype != SV_F16)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: logits must be f32, bf16 or f16");
+  if (n > 1) {
+    if (draft_is_probs && draft_dtype != SV_F32)
+      return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: draft probabilities must be f32");
+    if (!draft_is_probs && draft_dtype != logit_dtype)
+      return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: draft logits must have the target's dtype");
+  }
+  if (B == 0) return ok();
+  TreeParams P = {};
+  P.target = target_logits; P.draft = draft ? draft : target_logits;
+  P.parent = tree_parent; P.tokens = tree_tokens; P.uniforms = uniforms;
+  P.out_tokens = out_tokens; P.num_acc = num_accepted; P.path = path_nodes; P.status = dev_status;
+  P.B = B; P.n = n; P.V = V;
+  P.chunk = ((V + kTrThreads - 1) / kTrThreads + 7) / 8 * 8;
+  const int es_t = dtype_bytes(logit_dtype), es_d = draft_is_probs ? 4 : es_t;
+  P.vec_t = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0;
+  P.vec_d = aligned(P.draft, 16) && ((size_t)V * es_d) % 16 == 0;
+  P.c = (float)(1.4426950408889634074 / (double)temperature);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const bool probs = draft_is_probs && n > 1;
+  switch (logit_dtype) {
+    case SV_F32:
+      e = probs ? launch_k(sample_tree_kernel<float, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
+                : launch_k(sample_tree_kernel<float, 0>, dim3(B), dim3(kTrThreads), 0, s, 1, P);
+      break;
+    case SV_BF16:
+      e = probs ? launch_k(sample_tree_kernel<__nv_bfloat16, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
+                : launch_k(sample_tree_kernel<__nv_bfloat16, 0>, dim3(B), dim3(kTrThreads), 0, s, 1, P);
+      break;
+    default:
+      e = probs ? launch_k(sample_tree_kernel<__half, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
+                : launch_k(sample_tree_kernel<__half, 0>, dim3(B), dim3(kTrThreads), 0, s, 1, P);
+      break;
+  }
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_tree launch: %s", cudaGetErrorString(e));
+  return ok();
+}
