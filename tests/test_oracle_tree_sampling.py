@@ -88,9 +88,6 @@ def test_sibling_rule_is_exact(k, case):
     p = [F(int(a), 64) for a in rng.multinomial(64, np.ones(V) / V)]
     q = [F(int(a), 64) for a in rng.multinomial(64, np.ones(V) / V)]
     assert first_token_law(p, q, k) == p
-    if k > 1 and p != q:
-        # the rule without the residual update is not exact on some case
-        pass
 
 
 def test_retrying_against_p_is_not_exact():
