@@ -415,9 +415,12 @@ def measure_next_rows(sv, cfg, a, s, dev, stream, status, reps=20):
     events on the launching stream (outside the step's timed region):
     sampling at top_p = 0.9 with the draft rows filtered too, the top-p
     filter alone over those target and draft rows (HBM-bound: every row read
-    once and written once), and the copy-on-write page copy of one page per
-    sequence in this layer's K and V pools."""
+    once and written once), the copy-on-write page copy of one page per
+    sequence in this layer's K and V pools, and tree verification (attention
+    and sampling) with a five-node draft tree in place of the chain."""
     import torch
+
+    import workloads
 
     def timed(fn):
         for _ in range(3):
@@ -460,12 +463,53 @@ def measure_next_rows(sv, cfg, a, s, dev, stream, status, reps=20):
         assert rc == 0
     cow_us = timed(cow)
     cow_bytes = 2 * 2 * len(pages) * page_bytes
+
+    # draft tree of K + 1 = 5 nodes per sequence: root, two children, one
+    # grandchild under each (the same positions and bytes as the chain)
+    n = K + 1
+    parents = [-1, 0, 0, 1, 2][:n] if n <= 5 else [-1] + list(range(n - 1))
+    par = torch.tensor(parents, dtype=torch.int32, device=dev).repeat(B, 1)
+    q_t, kc_t, vc_t = a["q"], a["k_cache"], a["v_cache"]
+    attn_out = torch.empty_like(q_t)
+    tws = sv.alloc_workspace(sv.load_library().spec_verify_attn_tree_workspace_size(
+        B, n, cfg.H_q, cfg.H_kv, cfg.d_head, a["block_table"].shape[1], cfg.block_size), dev)
+    tattn_us = timed(lambda: sv.spec_verify_attn(q_t, kc_t, vc_t, a["block_table"], a["seq_lens"], None,
+                                                a["k_scale"], a["v_scale"], out=attn_out, workspace=tws,
+                                                status=status, tree_parent=par))
+    attn_bytes = workloads.attention_bytes(cfg, a["seq_lens"].tolist())
+    drafts = torch.zeros((B, n, V), dtype=s["draft_logits"].dtype, device=dev)
+    drafts[:, :K] = s["draft_logits"]
+    ttok = torch.zeros((B, n), dtype=torch.int32, device=dev)
+    ttok[:, 1:] = s["draft_tokens"]
+    t_out = torch.empty((B, n), dtype=torch.int32, device=dev)
+    t_acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    t_path = torch.empty((B, n), dtype=torch.int32, device=dev)
+    tsamp_us = timed(lambda: sv.spec_verify_sample_tree(s["target_logits"], drafts, par, ttok, s["uniforms"],
+                                                        out_tokens=t_out, num_accepted=t_acc, path_nodes=t_path,
+                                                        status=status))
+    # rows the walk needs: p_u of every node it visits, q_u of those with children
+    has_child = [any(p == u for p in parents) for u in range(n)]
+    tree_rows = 0
+    for b_, acc in enumerate(t_acc.tolist()):
+        for u in [0] + t_path[b_, :acc].tolist():
+            tree_rows += 1 + (1 if has_child[u] else 0)
+    tsamp_bytes = tree_rows * V * s["target_logits"].element_size()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return {
+        "tree": {"parents": parents,
+                 "attn_us": tattn_us,
+                 "attn_roofline": {"bound": "hbm", "kernel": "attn_tc5_kernel (tree mask)",
+                                   "achieved": attn_bytes / (tattn_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                                   "frac": attn_bytes / (tattn_us * 1e-6) / 1e9 / peak, "bytes": attn_bytes},
+                 "sample_us": tsamp_us, "rows_read": tree_rows,
+                 "sample_roofline": {"bound": "hbm", "kernel": "sample_tree_kernel",
+                                     "achieved": tsamp_bytes / (tsamp_us * 1e-6) / 1e9, "peak": peak,
+                                     "unit": "GB/s", "frac": tsamp_bytes / (tsamp_us * 1e-6) / 1e9 / peak,
+                                     "bytes": tsamp_bytes}},
         "top_p": {"top_p": 0.9, "draft_top_p": True, "sample_topp_us": samp_us,
                   "filter_us": filt_us, "filter_rows": rows.shape[0],
-                  "roofline": {"bound": "hbm", "kernel": "topp_filter_kernel", "achieved": filt_bytes / (filt_us * 1e-6) / 1e9,
+                  "roofline": {"bound": "hbm", "kernel": "topp_row_kernel", "achieved": filt_bytes / (filt_us * 1e-6) / 1e9,
                                "peak": peak, "unit": "GB/s",
                                "frac": filt_bytes / (filt_us * 1e-6) / 1e9 / peak, "bytes": filt_bytes}},
         "cow_copy": {"pairs": len(pages), "pools": 2, "page_bytes": page_bytes, "us": cow_us,

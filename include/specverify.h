@@ -135,6 +135,29 @@ sv_status kv_block_append(const void *k_new, const void *v_new, sv_dtype new_dty
                           int num_blocks, int32_t *dev_status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * kv_tree_commit
+ *   After a tree round (spec_verify_attn_tree + spec_verify_sample_tree) the
+ *   n_new node rows of sequence b sit at positions L - n_new + j (node j,
+ *   L = seq_lens[b]). This moves the accepted path next to the root:
+ *   position L - n_new + 1 + i takes the row of node path_nodes[b][i] for
+ *   i < num_accepted[b], every kv head, K and V (every row read before any
+ *   is written). Rolling the length back to L - n_new + num_accepted[b] + 1
+ *   (sv_bm_commit_verify) then leaves the prefix, the root and the path in
+ *   order ("KV Cache + Speculative Decoding", section 7's invariant).
+ *   path_nodes int32 [B][n_new] and num_accepted int32 [B]: device, as
+ *   spec_verify_sample_tree writes them (num_accepted in [0, n_new - 1],
+ *   path entries in [1, n_new)); a bad value sets SV_DEV_* bits and leaves
+ *   that sequence unchanged. Pools as for kv_block_append (SV_F32, SV_BF16
+ *   or SV_FP8_E4M3 codes, any sv_kv_layout); n_new <= 64, d_head * element
+ *   size <= 1024.
+ * ------------------------------------------------------------------------ */
+sv_status kv_tree_commit(void *k_cache, void *v_cache, sv_dtype kv_dtype, const sv_kv_layout *layout,
+                         const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens,
+                         const int32_t *path_nodes, const int32_t *num_accepted,
+                         int B, int n_new, int H_kv, int d_head, int block_size, int num_blocks,
+                         int32_t *dev_status, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * spec_verify_attn
  *   out[b][j][h][:] = sum_t softmax_t(s_t) * V_b[t][g][:] with
  *   s_t = softmax_scale * q[b][j][h][:] . K_b[t][g][:], g = h / (H_q/H_kv),

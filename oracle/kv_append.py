@@ -42,3 +42,36 @@ def kv_block_append(k_cache, v_cache, k_new, v_new, block_table, seq_lens,
                     else:
                         cache[blk, g, slot] = row.to(cache.dtype)
     return kc, vc
+
+
+def kv_tree_commit(k_cache, v_cache, block_table, seq_lens, n_new, path_nodes, num_accepted,
+                   block_size=16):
+    """Return new (k_cache, v_cache) with each sequence's accepted tree path
+    moved next to the root.
+
+    After a tree round ("KV Cache + Speculative Decoding", Q14 and section
+    8.2) the n_new node rows sit at positions L - n_new + j (node j). The
+    cache must then hold the prefix, the root and the accepted path, in
+    order (the generation-loop invariant of section 7: every token of the
+    sequence but the last one is cached): position L - n_new + 1 + i takes
+    the row of node path_nodes[b][i], i < num_accepted[b], for every kv head
+    of K and V. Other positions are left as they are (the rollback drops
+    them).
+    """
+    kc = k_cache.detach().cpu().clone()
+    vc = v_cache.detach().cpu().clone()
+    src_k = k_cache.detach().cpu()
+    src_v = v_cache.detach().cpu()
+    table = block_table.detach().cpu().numpy()
+    lens = seq_lens.detach().cpu().numpy()
+    path = path_nodes.detach().cpu().numpy()
+    nacc = num_accepted.detach().cpu().numpy()
+    for b in range(table.shape[0]):
+        base = int(lens[b]) - n_new
+        for i in range(int(nacc[b])):
+            s, d = base + int(path[b, i]), base + 1 + i
+            sb, ss = int(table[b, s // block_size]), s % block_size
+            db, ds = int(table[b, d // block_size]), d % block_size
+            kc[db, :, ds] = src_k[sb, :, ss]
+            vc[db, :, ds] = src_v[sb, :, ss]
+    return kc, vc

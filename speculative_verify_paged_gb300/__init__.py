@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_sample_topp_workspace_size.argtypes = [I, I, I, I, I]
     lib.spec_verify_sample_topp.restype = I
     lib.spec_verify_sample_topp.argtypes = [P, I, P, I, I, P, P, I, I, I, F, F, I, P, P, P, P, P, Z, P, P]
+    lib.kv_tree_commit.restype = I
+    lib.kv_tree_commit.argtypes = [P, P, I, LP, P, I, P, P, P, I, I, I, I, I, I, P, P]
     lib.spec_verify_sample_tree.restype = I
     lib.spec_verify_sample_tree.argtypes = [P, I, P, I, I, P, P, P, I, I, I, F, P, P, P, P, P]
     I64, BMP = ctypes.c_int64, ctypes.c_void_p
@@ -187,6 +189,25 @@ def kv_block_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_sca
                                _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
                                block_table.shape[1], _ptr(seq_lens), B, n_new, H_kv, d, block_size,
                                num_blocks, _ptr(status), _stream()))
+
+
+def kv_tree_commit(k_cache, v_cache, block_table, seq_lens, path_nodes, num_accepted, block_size=16,
+                   layout=None, num_blocks=None, H_kv=None, status=None):
+    """Move each sequence's accepted tree path (path_nodes [B, n_new], num_accepted [B])
+    next to the root in the paged pools; pools [num_blocks, H_kv, bs, d] unless layout."""
+    lib = load_library()
+    _cuda(k_cache, v_cache, block_table, seq_lens, path_nodes, num_accepted, status)
+    B, n_new = path_nodes.shape
+    if layout is None:
+        num_blocks, H_kv, d = k_cache.shape[0], k_cache.shape[1], k_cache.shape[3]
+    else:
+        if num_blocks is None or H_kv is None:
+            raise ValueError("with an explicit layout pass num_blocks and H_kv")
+        d = k_cache.shape[-1]
+    _check(lib.kv_tree_commit(_ptr(k_cache), _ptr(v_cache), _dtype_code(k_cache, True), _layout_arg(layout),
+                              _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(path_nodes),
+                              _ptr(num_accepted), B, n_new, H_kv, d, block_size, num_blocks, _ptr(status),
+                              _stream()))
 
 
 # ------------------------------------------------------------ attention ---

@@ -6,6 +6,8 @@
 #include <cstring>
 #include <type_traits>
 
+#include <mutex>
+
 #include "sv_common.cuh"
 
 namespace sv {
@@ -192,7 +194,133 @@ sv_status launch_in(const AppendArgs &a, sv_dtype kv_dtype, int B, cudaStream_t 
 }
 
 }  // namespace
+// ------------------------------------------------------------ tree commit ---
+// After a tree round ("KV Cache + Speculative Decoding", Q14 and section 8.2)
+// the accepted path's rows move next to the root: position L - n_new + 1 + i
+// takes node path[i]'s row (position L - n_new + path[i]), for every kv head
+// of K and V, so that the cache again holds every token of the sequence but
+// the last one (section 7's invariant) once the length is rolled back. A
+// path node's row can be a later destination (path[i] >= i + 1), so a CTA
+// reads all of a head's moved rows into shared memory before it writes any.
+
+constexpr int kCmThreads = 256;
+constexpr int kCmMaxRowBytes = 1024;   // d_head * element size
+
+struct CommitArgs {
+  uint8_t *cache[2];                    // K, V
+  const int32_t *block_table, *seq_lens, *path, *nacc;
+  int max_blocks, n_new, H_kv, row_bytes, bs, num_blocks, unit;   // unit: 16 or 1 byte
+  int64_t block_stride, head_stride, slot_stride;                 // bytes
+  int32_t *status;
+};
+
+// grid (B, 2): sequence b, K (0) or V (1)
+__global__ void __launch_bounds__(kCmThreads) kv_tree_commit_kernel(const __grid_constant__ CommitArgs a) {
+  extern __shared__ __align__(16) uint8_t cm_buf[];
+  __shared__ int64_t src_off[64], dst_off[64];
+  __shared__ int s_ok;
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  uint8_t *cache = a.cache[blockIdx.y];
+  const int L = __ldg(a.seq_lens + b);
+  const int nacc = __ldg(a.nacc + b);
+  if (L < a.n_new || L > a.max_blocks * a.bs || nacc < 0 || nacc > a.n_new - 1) {
+    if (tid == 0 && blockIdx.y == 0) atomic_or_status(a.status, SV_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  if (tid == 0) s_ok = 1;
+  __syncthreads();
+  const int base = L - a.n_new;
+  for (int i = tid; i < nacc; i += kCmThreads) {
+    const int node = __ldg(a.path + (int64_t)b * a.n_new + i);
+    const int s = base + node, d = base + 1 + i;
+    bool ok = node >= 1 && node < a.n_new;
+    int sb = 0, db = 0;
+    if (ok) {
+      sb = __ldg(a.block_table + (int64_t)b * a.max_blocks + s / a.bs);
+      db = __ldg(a.block_table + (int64_t)b * a.max_blocks + d / a.bs);
+      ok = sb >= 0 && sb < a.num_blocks && db >= 0 && db < a.num_blocks;
+    }
+    if (!ok) {
+      s_ok = 0;
+      continue;
+    }
+    src_off[i] = (int64_t)sb * a.block_stride + (int64_t)(s % a.bs) * a.slot_stride;
+    dst_off[i] = (int64_t)db * a.block_stride + (int64_t)(d % a.bs) * a.slot_stride;
+  }
+  __syncthreads();
+  if (!s_ok) {
+    if (tid == 0 && blockIdx.y == 0) atomic_or_status(a.status, SV_DEV_BAD_TREE | SV_DEV_BAD_BLOCK);
+    return;
+  }
+  const int units = a.row_bytes / a.unit;
+  for (int g = 0; g < a.H_kv; ++g) {
+    const int64_t hoff = (int64_t)g * a.head_stride;
+    for (int idx = tid; idx < nacc * units; idx += kCmThreads) {
+      const int i = idx / units, v = idx % units;
+      const uint8_t *src = cache + src_off[i] + hoff + (int64_t)v * a.unit;
+      if (a.unit == 16) reinterpret_cast<uint4 *>(cm_buf)[idx] = *reinterpret_cast<const uint4 *>(src);
+      else cm_buf[idx] = *src;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nacc * units; idx += kCmThreads) {
+      const int i = idx / units, v = idx % units;
+      uint8_t *dst = cache + dst_off[i] + hoff + (int64_t)v * a.unit;
+      if (a.unit == 16) *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(cm_buf)[idx];
+      else *dst = cm_buf[idx];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace sv
+
+extern "C" sv_status kv_tree_commit(void *k_cache, void *v_cache, sv_dtype kv_dtype, const sv_kv_layout *layout,
+                                    const int32_t *block_table, int max_blocks_per_seq, const int32_t *seq_lens,
+                                    const int32_t *path_nodes, const int32_t *num_accepted, int B, int n_new,
+                                    int H_kv, int d_head, int block_size, int num_blocks, int32_t *dev_status,
+                                    sv_stream_t stream) {
+  using namespace sv;
+  if (!k_cache || !v_cache || !block_table || !seq_lens || !path_nodes || !num_accepted)
+    return fail(SV_ERR_INVALID_ARG, "kv_tree_commit: null pointer argument");
+  if (B < 0 || n_new < 1 || H_kv < 1 || d_head < 1 || block_size < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return fail(SV_ERR_INVALID_ARG, "kv_tree_commit: bad sizes");
+  if (n_new > 64) return fail(SV_ERR_UNSUPPORTED, "kv_tree_commit: at most 64 tree nodes");
+  const int es = dtype_bytes(kv_dtype);
+  if (es == 0 || kv_dtype == SV_F16) return fail(SV_ERR_UNSUPPORTED, "kv_tree_commit: pools must be f32, bf16 or fp8");
+  if (d_head * es > kCmMaxRowBytes) return fail(SV_ERR_UNSUPPORTED, "kv_tree_commit: rows above 1024 bytes");
+  if (B == 0) return ok();
+  CommitArgs a = {};
+  a.cache[0] = static_cast<uint8_t *>(k_cache);
+  a.cache[1] = static_cast<uint8_t *>(v_cache);
+  a.block_table = block_table; a.seq_lens = seq_lens; a.path = path_nodes; a.nacc = num_accepted;
+  a.max_blocks = max_blocks_per_seq; a.n_new = n_new; a.H_kv = H_kv; a.row_bytes = d_head * es;
+  a.bs = block_size; a.num_blocks = num_blocks; a.status = dev_status;
+  int64_t bst, hst, sst;
+  if (layout) {
+    bst = layout->block_stride; hst = layout->head_stride; sst = layout->slot_stride;
+    if (sst < d_head || hst < d_head || bst < d_head)
+      return fail(SV_ERR_INVALID_ARG, "kv_tree_commit: layout strides smaller than d_head");
+  } else {
+    sst = d_head; hst = (int64_t)block_size * d_head; bst = (int64_t)H_kv * block_size * d_head;
+  }
+  a.block_stride = bst * es; a.head_stride = hst * es; a.slot_stride = sst * es;
+  a.unit = (a.row_bytes % 16 == 0 && aligned(k_cache, 16) && aligned(v_cache, 16) && a.block_stride % 16 == 0 &&
+            a.head_stride % 16 == 0 && a.slot_stride % 16 == 0) ? 16 : 1;
+  const size_t smem = (size_t)(n_new - 1) * a.row_bytes + 16;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(kv_tree_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    63 * kCmMaxRowBytes + 16);
+  });
+  if (attr_err != cudaSuccess) return fail(SV_ERR_CUDA, "kv_tree_commit attributes: %s", cudaGetErrorString(attr_err));
+  const cudaError_t e = launch_k(kv_tree_commit_kernel, dim3(B, 2), dim3(kCmThreads), smem,
+                                 reinterpret_cast<cudaStream_t>(stream), 1, a);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "kv_tree_commit launch: %s", cudaGetErrorString(e));
+  return ok();
+}
 
 extern "C" sv_status kv_block_append(const void *k_new, const void *v_new, sv_dtype new_dtype,
                                      void *k_cache, void *v_cache, sv_dtype kv_dtype,

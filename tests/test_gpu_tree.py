@@ -3,8 +3,10 @@
 Every cache dtype path (the tcgen05 bf16 kernel, the fp8 mma.sync kernel,
 the fp32 kernel) runs random BFS trees of 2 to 64 nodes against the fp64
 oracle at the attention tolerances; a chain given as a tree must reproduce
-the causal call bit for bit; a bad parent must be flagged; and the 70B
-layer shape runs with a five-node tree on sampled sequences.
+the causal call bit for bit; a bad parent must be flagged; the 70B layer
+shape runs with a five-node tree on sampled sequences; and a whole tree
+round (append, tree attention, tree sampling, kv_tree_commit) leaves the
+pools equal to the oracle's commit bit for bit.
 """
 import math
 
@@ -114,3 +116,48 @@ def test_tree_full_size_70b(sv):
                                 cpu["v_scale"], batch_indices=idx, tree_parent=parents)
     err = np.abs(out.float().cpu().numpy()[idx] - ref[idx]).max()
     assert err <= attn_tolerance(cfg.kv_dtype), "max abs error %.3g" % err
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "f32"])
+def test_tree_round_commit(sv, kv):
+    # a full tree round: append the n node rows, tree attention, tree
+    # sampling, then move the accepted paths next to the root; the pools must
+    # equal the oracle's commit bit for bit
+    from oracle import kv_append as oapp
+    from oracle import sampling as osamp
+    over = {"f32": {}, "bf16": {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128},
+            "fp8_e4m3": {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 128}}[kv]
+    n = 8
+    cfg = workloads.CONFIGS["tiny"].with_(K=n - 1, B=4, ctx=("fixed", (40, 64, 100, 9)), V=500, **over)
+    a = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v)
+         for k, v in workloads.make_attention_inputs(cfg, seed=21).items()}
+    new = {k: v.to(DEV) for k, v in workloads.make_append_inputs(cfg, seed=21).items()}
+    sv.kv_block_append(new["k_new"], new["v_new"], a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"],
+                       a["k_scale"], a["v_scale"], block_size=cfg.block_size)
+    parents = torch.from_numpy(random_trees(cfg.B, n, seed=21)).to(DEV)
+    out, st = run(sv, cfg, a, parents)
+    assert st == 0
+    g = torch.Generator().manual_seed(21)
+    tl = (torch.randn(cfg.B, n, cfg.V, generator=g) * 3).to(torch.bfloat16)
+    dl = (tl.float() + torch.randn(cfg.B, n, cfg.V, generator=g)).to(torch.bfloat16)
+    q = torch.softmax(dl.double(), -1)
+    par_h = parents.cpu()
+    tok = torch.zeros(cfg.B, n, dtype=torch.int32)
+    for b in range(cfg.B):
+        for c in range(1, n):
+            tok[b, c] = int(torch.multinomial(q[b, par_h[b, c]], 1, generator=g))
+    uv = torch.rand(cfg.B, n, 2, generator=g)
+    toks, nacc, path = sv.spec_verify_sample_tree(tl.to(DEV), dl.to(DEV), parents, tok.to(DEV), uv.to(DEV))
+    before_k, before_v = a["k_cache"].cpu(), a["v_cache"].cpu()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sv.kv_tree_commit(a["k_cache"], a["v_cache"], a["block_table"], a["seq_lens"], path, nacc,
+                      block_size=cfg.block_size, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ek, ev = oapp.kv_tree_commit(before_k, before_v, a["block_table"], a["seq_lens"], n, path.cpu(), nacc.cpu(),
+                                 cfg.block_size)
+    view = (lambda t: t.view(torch.uint8)) if kv == "fp8_e4m3" else (lambda t: t)
+    assert torch.equal(view(a["k_cache"].cpu()), view(ek)) and torch.equal(view(a["v_cache"].cpu()), view(ev))
+    ref = osamp.tree_rejection_sample(tl, dl, par_h, tok, uv)
+    clear = ref["margin"] > 1e-5
+    assert np.array_equal(nacc.cpu().numpy()[clear], ref["num_accepted"][clear])
