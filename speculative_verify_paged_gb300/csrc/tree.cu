@@ -87,6 +87,87 @@ __device__ __forceinline__ void ld8(const T *row, int i, bool vec, float (&x)[8]
   }
 }
 
+// Eight consecutive elements as loaded (16-bit types: one 16-byte vector;
+// f32: two), decoded only when used, so that several loads can be in flight.
+template <typename T>
+struct Raw8 {
+  uint4 a, b;
+};
+
+template <typename T>
+__device__ __forceinline__ void ld_raw(const T *row, int i, Raw8<T> &r) {
+  r.a = __ldg(reinterpret_cast<const uint4 *>(row + i));
+  if (sizeof(T) == 4) r.b = __ldg(reinterpret_cast<const uint4 *>(row + i) + 1);
+}
+
+template <typename T>
+__device__ __forceinline__ float raw_at(const Raw8<T> &r, int k) {
+  if (sizeof(T) == 4) return __uint_as_float(k < 4 ? (&r.a.x)[k] : (&r.b.x)[k - 4]);
+  const uint32_t w = (&r.a.x)[k >> 1];
+  const uint32_t h = (k & 1) ? (w >> 16) : (w & 0xffffu);
+  if (std::is_same<T, __nv_bfloat16>::value) return __uint_as_float(h << 16);
+  return __half2float(__ushort_as_half((unsigned short)h));
+}
+
+// f(x, id) over the chunk [lo, hi) of a row in token order; nfull whole
+// groups of eight from lo, then the rest one element at a time. Aligned rows
+// keep NB 16-byte loads in flight per thread.
+template <typename T, typename F>
+__device__ __forceinline__ void tr_each(const T *row, bool vec, int lo, int nfull, int hi, F f) {
+  constexpr int NB = sizeof(T) == 4 ? 2 : 4;
+  int g = 0;
+  if (vec) {
+    for (; g + NB <= nfull; g += NB) {
+      Raw8<T> r[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) ld_raw(row, lo + 8 * (g + u), r[u]);
+#pragma unroll
+      for (int u = 0; u < NB; ++u)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f(raw_at(r[u], k), lo + 8 * (g + u) + k);
+    }
+  }
+  for (; g < nfull; ++g) {
+    float x[8];
+    ld8(row, lo + 8 * g, vec, x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f(x[k], lo + 8 * g + k);
+  }
+  for (int i = lo + 8 * nfull; i < hi; ++i) f(ld_f32(row, i), i);
+}
+
+// The same over two rows at once (p and q), f(lp, lq, id); with use_q false
+// the q row is not read and lq is 0.
+template <typename T, typename TD, typename F>
+__device__ __forceinline__ void tr_each2(const T *pr, bool vt, const TD *qr, bool vd, bool use_q, int lo, int nfull,
+                                         int hi, F f) {
+  constexpr int NB = 2;
+  int g = 0;
+  if (vt && (vd || !use_q)) {
+    for (; g + NB <= nfull; g += NB) {
+      Raw8<T> a[NB];
+      Raw8<TD> d[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        ld_raw(pr, lo + 8 * (g + u), a[u]);
+        if (use_q) ld_raw(qr, lo + 8 * (g + u), d[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < NB; ++u)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f(raw_at(a[u], k), use_q ? raw_at(d[u], k) : 0.f, lo + 8 * (g + u) + k);
+    }
+  }
+  for (; g < nfull; ++g) {
+    float x[8], y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    ld8(pr, lo + 8 * g, vt, x);
+    if (use_q) ld8(qr, lo + 8 * g, vd, y);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f(x[k], y[k], lo + 8 * g + k);
+  }
+  for (int i = lo + 8 * nfull; i < hi; ++i) f(ld_f32(pr, i), use_q ? ld_f32(qr, i) : 0.f, i);
+}
+
 __device__ __forceinline__ float tr_block_sum(float v, float *s_red) {
   v = warp_sum(v);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -165,15 +246,7 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
   const bool vt = P.vec_t, vd = P.vec_d;
 
   // f(x, id) over this thread's chunk of a row, in token order
-  auto each = [&](const auto *row, bool vec, auto f) {
-    for (int g = 0; g < nfull; ++g) {
-      float x[8];
-      ld8(row, lo + 8 * g, vec, x);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) f(x[k], lo + 8 * g + k);
-    }
-    for (int i = lo + 8 * nfull; i < hi; ++i) f(ld_f32(row, i), i);
-  };
+  auto each = [&](const auto *row, bool vec, auto f) { tr_each(row, vec, lo, nfull, hi, f); };
   // (max, sum of 2^((l - max) c)) of a logit row
   auto stats = [&](const auto *row, bool vec, float &m, float &s) {
     float mx = -INFINITY;
@@ -227,20 +300,12 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
       // rejected: the next residual
       coef += D;
       float acc = 0.f, grp = 0.f;
-      const T *pr = prow;
-      const TD *qr = qrow;
-      auto resid = [&](float lp, float lq) { return fmaxf(0.f, p_of(lp) - coef * q_of(lq)); };
-      for (int g = 0; g < nfull; ++g) {
-        float a[8], d[8];
-        ld8(pr, lo + 8 * g, vt, a);
-        ld8(qr, lo + 8 * g, vd, d);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) grp += resid(a[kk], d[kk]);
-        acc += grp;
-        grp = 0.f;
-      }
-      for (int i = lo + 8 * nfull; i < hi; ++i) acc += resid(ld_f32(pr, i), ld_f32(qr, i));
-      D = tr_block_sum(acc, s_red);
+      int cnt = 0;
+      tr_each2(prow, vt, qrow, vd, true, lo, nfull, hi, [&](float lp, float lq, int) {
+        grp += fmaxf(0.f, p_of(lp) - coef * q_of(lq));
+        if (++cnt == 8) { acc += grp; grp = 0.f; cnt = 0; }
+      });
+      D = tr_block_sum(acc + grp, s_red);
       if (!(D > 0.f)) { coef = 0.f; D = 1.f; }   // cannot happen in exact arithmetic: draw from p
     }
     if (accepted >= 0) {
@@ -252,26 +317,15 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
 
     // ---- draw from max(0, p - coef q) (p itself when coef = 0) ----
     auto w_of = [&](float lp, float lq) { return coef == 0.f ? p_of(lp) : fmaxf(0.f, p_of(lp) - coef * q_of(lq)); };
-    float mine = 0.f;
-    int first_pos = INT_MAX, last_pos = -1;
-    for (int g = 0; g < nfull; ++g) {
-      float a[8], d[8];
-      ld8(prow, lo + 8 * g, vt, a);
-      if (coef != 0.f) ld8(qrow, lo + 8 * g, vd, d);
-      float grp = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const float w = w_of(a[kk], coef != 0.f ? d[kk] : 0.f);
-        grp += w;
-        if (w > 0.f) { first_pos = min(first_pos, lo + 8 * g + kk); last_pos = lo + 8 * g + kk; }
-      }
-      mine += grp;
-    }
-    for (int i = lo + 8 * nfull; i < hi; ++i) {
-      const float w = w_of(ld_f32(prow, i), coef != 0.f ? ld_f32(qrow, i) : 0.f);
-      mine += w;
+    float mine = 0.f, grp = 0.f;
+    int cnt = 0, first_pos = INT_MAX, last_pos = -1;
+    tr_each2(prow, vt, qrow, vd, coef != 0.f, lo, nfull, hi, [&](float lp, float lq, int i) {
+      const float w = w_of(lp, lq);
+      grp += w;
       if (w > 0.f) { first_pos = min(first_pos, i); last_pos = i; }
-    }
+      if (++cnt == 8) { mine += grp; grp = 0.f; cnt = 0; }
+    });
+    mine += grp;
     float Z;
     const float before = tr_block_excl_scan(mine, s_red, &Z);
     const float target = __ldg(P.uniforms + ((int64_t)b * n + u) * 2 + 1) * Z;
@@ -283,11 +337,32 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
     if (before <= target) atomicMax(&s_owner, tid);
     __syncthreads();
     const int owner = s_owner;
-    if (tid == owner) {
-      float cum = before;
-      for (int i = lo; i < hi; ++i) {
-        cum += w_of(ld_f32(prow, i), coef != 0.f ? ld_f32(qrow, i) : 0.f);
-        if (cum > target) { s_y = i; break; }
+    if ((tid >> 5) == (owner >> 5)) {
+      // the owner's warp rescans the owner's chunk: lane l takes per
+      // consecutive tokens, a warp scan of their weights (from the owner's
+      // running sum) finds the lane holding the first y with C(y) > v Z
+      const int lane = tid & 31;
+      const int olo = owner * P.chunk, ohi = min(V, olo + P.chunk);
+      const int per = (P.chunk + 31) / 32;
+      const int a0 = min(ohi, olo + lane * per), a1 = min(ohi, a0 + per);
+      float part = 0.f;
+      for (int i = a0; i < a1; ++i) part += w_of(ld_f32(prow, i), coef != 0.f ? ld_f32(qrow, i) : 0.f);
+      float incl = part;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const float obefore = __shfl_sync(0xffffffffu, before, owner & 31);
+      const float start = obefore + incl - part;
+      const bool here = a0 < a1 && start + part > target && start <= target;
+      const unsigned hit = __ballot_sync(0xffffffffu, here);
+      if (hit && lane == __ffs(hit) - 1) {
+        float cum = start;
+        for (int i = a0; i < a1; ++i) {
+          cum += w_of(ld_f32(prow, i), coef != 0.f ? ld_f32(qrow, i) : 0.f);
+          if (cum > target) { s_y = i; break; }
+        }
       }
     }
     if (tid > owner) atomicMin(&s_first, first_pos);
