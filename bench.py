@@ -484,9 +484,10 @@ def measure_next_rows(sv, cfg, a, s, dev, stream, status, reps=20):
     t_out = torch.empty((B, n), dtype=torch.int32, device=dev)
     t_acc = torch.empty((B,), dtype=torch.int32, device=dev)
     t_path = torch.empty((B, n), dtype=torch.int32, device=dev)
+    t_ws = sv.alloc_workspace(sv.load_library().spec_verify_sample_tree_workspace_size(B, n), dev)
     tsamp_us = timed(lambda: sv.spec_verify_sample_tree(s["target_logits"], drafts, par, ttok, s["uniforms"],
                                                         out_tokens=t_out, num_accepted=t_acc, path_nodes=t_path,
-                                                        status=status))
+                                                        status=status, workspace=t_ws))
     # rows the walk needs: p_u of every node it visits, q_u of those with children
     has_child = [any(p == u for p in parents) for u in range(n)]
     tree_rows = 0

@@ -96,8 +96,10 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_sample_topp.argtypes = [P, I, P, I, I, P, P, I, I, I, F, F, I, P, P, P, P, P, Z, P, P]
     lib.kv_tree_commit.restype = I
     lib.kv_tree_commit.argtypes = [P, P, I, LP, P, I, P, P, P, I, I, I, I, I, I, P, P]
+    lib.spec_verify_sample_tree_workspace_size.restype = Z
+    lib.spec_verify_sample_tree_workspace_size.argtypes = [I, I]
     lib.spec_verify_sample_tree.restype = I
-    lib.spec_verify_sample_tree.argtypes = [P, I, P, I, I, P, P, P, I, I, I, F, P, P, P, P, P]
+    lib.spec_verify_sample_tree.argtypes = [P, I, P, I, I, P, P, P, I, I, I, F, P, P, P, P, Z, P, P]
     I64, BMP = ctypes.c_int64, ctypes.c_void_p
     lib.sv_bm_create.restype = I
     lib.sv_bm_create.argtypes = [I, I, ctypes.POINTER(ctypes.c_void_p)]
@@ -349,7 +351,8 @@ def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_pr
 
 
 def spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, uniforms, draft_is_probs=False,
-                            temperature=1.0, out_tokens=None, num_accepted=None, path_nodes=None, status=None):
+                            temperature=1.0, out_tokens=None, num_accepted=None, path_nodes=None, status=None,
+                            workspace=None):
     """Rejection sampling over a draft tree of n nodes (BFS order, node 0 the root).
 
     target_logits [B, n, V]; draft [B, n, V] logits (same dtype) or f32 probabilities;
@@ -358,7 +361,7 @@ def spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, unif
     """
     lib = load_library()
     _cuda(target_logits, draft, tree_parent, tree_tokens, uniforms, out_tokens, num_accepted, path_nodes,
-          status)
+          status, workspace)
     B, n, V = target_logits.shape
     dev = target_logits.device
     if out_tokens is None:
@@ -368,10 +371,13 @@ def spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, unif
     if path_nodes is None:
         path_nodes = torch.empty((B, n), dtype=torch.int32, device=dev)
     ddt = _dtype_code(draft) if draft is not None else SV_F32
+    if workspace is None:
+        workspace = alloc_workspace(lib.spec_verify_sample_tree_workspace_size(B, n), dev)
     _check(lib.spec_verify_sample_tree(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt,
                                        int(bool(draft_is_probs)), _ptr(tree_parent), _ptr(tree_tokens),
                                        _ptr(uniforms), B, n, V, float(temperature), _ptr(out_tokens),
-                                       _ptr(num_accepted), _ptr(path_nodes), _ptr(status), _stream()))
+                                       _ptr(num_accepted), _ptr(path_nodes), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(status), _stream()))
     return out_tokens, num_accepted, path_nodes
 
 

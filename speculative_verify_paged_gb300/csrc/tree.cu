@@ -13,7 +13,8 @@
 //   r_k = max(0, p - c_k q) / D_k,  c_0 = 0, D_0 = 1,
 //   c_{k+1} = c_k + D_k,  D_{k+1} = sum_x max(0, p(x) - c_{k+1} q(x)),
 // (induction: max(0, r_k - q) = max(0, p - c_k q - D_k q) / D_k), so a
-// rejection costs one row-wide sum and the draw one more pass.
+// rejection costs one row-wide sum and the draw one more pass. The rows'
+// (max, sum) statistics come from a pre-pass over all rows in parallel.
 //
 // Arithmetic is fp32 in a fixed order (each thread owns a contiguous chunk of
 // token ids, sums groups of 8, then a block tree), so the kernel is
@@ -43,6 +44,7 @@ struct TreeParams {
   int32_t *num_acc;        // [B]
   int32_t *path;           // [B][n]
   int32_t *status;
+  float2 *stats;           // [B][2n] (max, sum of 2^(fl(l c) - fl(max c))): target rows, then draft rows
   int B, n, V, chunk;      // chunk: token ids per thread (a multiple of 8)
   int vec_t, vec_d;        // rows 16-byte aligned: vector loads
   float c;                 // log2(e) / T
@@ -211,6 +213,87 @@ __device__ __forceinline__ float tr_block_excl_scan(float v, float *s_red, float
   return before + incl - v;
 }
 
+// (max, sum) of every row the walk may need, one CTA per row, all rows of all
+// sequences at once: grid (2n, B); row x < n is target row x, row n + u the
+// draft row of node u (skipped for leaves and for draft probabilities). One
+// online pass: each thread keeps (m, s) over its 16-byte groups (coalesced,
+// round-robin), rescaling s when m grows; the block combines the pairs.
+// The terms are 2^(fl(l c) - fl(m c)) with the final m, the reference the
+// walk evaluates p(x) and q(x) against.
+constexpr int kTsThreads = 512;
+
+__device__ __forceinline__ void tr_ms_combine(float &m, float &s, float m2, float s2, float c) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) { m = mn; s = 0.f; return; }
+  const float rc = __fmul_rn(mn, c);
+  s = (m == -INFINITY ? 0.f : s * tr_ex2(__fmul_rn(m, c) - rc)) +
+      (m2 == -INFINITY ? 0.f : s2 * tr_ex2(__fmul_rn(m2, c) - rc));
+  m = mn;
+}
+
+template <typename T, int DK>
+__global__ void __launch_bounds__(kTsThreads) tree_row_stats_kernel(const __grid_constant__ TreeParams P) {
+  using TD = typename std::conditional<DK == 1, float, T>::type;
+  __shared__ float s_m[kTsThreads / 32], s_s[kTsThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.y, x = blockIdx.x, n = P.n, V = P.V;
+  const bool draft_row = x >= n;
+  const int node = draft_row ? x - n : x;
+  if (draft_row) {
+    if (DK == 1) return;
+    bool has_child = false;
+    for (int j = node + 1; j < n; ++j) has_child |= __ldg(P.parent + (int64_t)b * n + j) == node;
+    if (!has_child) return;
+  }
+  const float c = P.c;
+  float m = -INFINITY, sum = 0.f;
+  auto add8 = [&](const float (&v)[8]) {
+    float mx = v[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) mx = fmaxf(mx, v[k]);
+    if (mx > m) {
+      sum = (m == -INFINITY) ? 0.f : sum * tr_ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+      m = mx;
+    }
+    if (m == -INFINITY) return;
+    const float mc = __fmul_rn(m, c);
+    float g = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) g += tr_ex2(fmaf(v[k], c, -mc));
+    sum += g;
+  };
+  auto run = [&](const auto *row, bool vec) {
+    const int ng = V / 8;
+    for (int g = threadIdx.x; g < ng; g += kTsThreads) {
+      float v[8];
+      ld8(row, 8 * g, vec, v);
+      add8(v);
+    }
+    if ((int)threadIdx.x == 0 && V % 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 8 * ng + k < V ? ld_f32(row, 8 * ng + k) : -INFINITY;
+      add8(v);
+    }
+  };
+  if (draft_row) run(static_cast<const TD *>(P.draft) + ((int64_t)b * n + node) * V, P.vec_d);
+  else run(static_cast<const T *>(P.target) + ((int64_t)b * n + node) * V, P.vec_t);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+    tr_ms_combine(m, sum, m2, s2, c);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { s_m[warp] = m; s_s[warp] = sum; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = s_m[0], ss = s_s[0];
+    for (int w = 1; w < kTsThreads / 32; ++w) tr_ms_combine(mm, ss, s_m[w], s_s[w], c);
+    P.stats[(int64_t)b * 2 * n + x] = make_float2(mm, ss);
+  }
+}
+
 template <typename T, int DK>
 __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid_constant__ TreeParams P) {
   using TD = typename std::conditional<DK == 1, float, T>::type;
@@ -245,33 +328,21 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
   const TD *drow_base = static_cast<const TD *>(P.draft) + (int64_t)b * n * V;
   const bool vt = P.vec_t, vd = P.vec_d;
 
-  // f(x, id) over this thread's chunk of a row, in token order
-  auto each = [&](const auto *row, bool vec, auto f) { tr_each(row, vec, lo, nfull, hi, f); };
-  // (max, sum of 2^((l - max) c)) of a logit row
-  auto stats = [&](const auto *row, bool vec, float &m, float &s) {
-    float mx = -INFINITY;
-    each(row, vec, [&](float x, int) { mx = fmaxf(mx, x); });
-    m = tr_block_max(mx, s_red);
-    const float mc = __fmul_rn(m, c);
-    float acc = 0.f, grp = 0.f;
-    int k = 0;
-    each(row, vec, [&](float x, int) {
-      grp += tr_ex2(fmaf(x, c, -mc));
-      if (++k == 8) { acc += grp; grp = 0.f; k = 0; }
-    });
-    s = tr_block_sum(acc + grp, s_red);
-  };
-
   int u = 0, depth = 0;
   for (;;) {
     const T *prow = trow_base + (int64_t)u * V;
     const TD *qrow = drow_base + (int64_t)u * V;
-    float m_p, S_p, m_q = 0.f, S_q = 1.f;
-    stats(prow, vt, m_p, S_p);
+    float m_q = 0.f, S_q = 1.f;
+    const float2 sp = P.stats[(int64_t)b * 2 * n + u];
+    const float m_p = sp.x, S_p = sp.y;
     const float mpc = __fmul_rn(m_p, c), inv_p = 1.f / S_p;
     bool has_child = false;
     for (int j = u + 1; j < n; ++j) has_child |= par[j] == u;
-    if (has_child && DK == 0) stats(qrow, vd, m_q, S_q);
+    if (has_child && DK == 0) {
+      const float2 sq = P.stats[(int64_t)b * 2 * n + n + u];
+      m_q = sq.x;
+      S_q = sq.y;
+    }
     if (!(m_p > -INFINITY && m_p < INFINITY) || (DK == 0 && has_child && !(m_q > -INFINITY && m_q < INFINITY))) {
       // a row without a finite maximum: flagged, the walk stops here
       if (tid == 0) { atomic_or_status(P.status, SV_DEV_NONFINITE); P.num_acc[b] = depth; }
@@ -382,12 +453,18 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
 }  // namespace
 }  // namespace sv
 
+extern "C" size_t spec_verify_sample_tree_workspace_size(int B, int n) {
+  if (B < 0 || n < 1) return 0;
+  return sv::align_up((size_t)B * 2 * n * sizeof(float2), 256);
+}
+
 extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype logit_dtype, const void *draft,
                                              sv_dtype draft_dtype, int draft_is_probs,
                                              const int32_t *tree_parent, const int32_t *tree_tokens,
                                              const float *uniforms, int B, int n, int V, float temperature,
                                              int32_t *out_tokens, int32_t *num_accepted, int32_t *path_nodes,
-                                             int32_t *dev_status, sv_stream_t stream) {
+                                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                             sv_stream_t stream) {
   using namespace sv;
   if (B < 0 || n < 1 || V < 1)
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: bad sizes B=%d n=%d V=%d", B, n, V);
@@ -406,8 +483,13 @@ extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype
     if (!draft_is_probs && draft_dtype != logit_dtype)
       return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: draft logits must have the target's dtype");
   }
+  const size_t need = align_up((size_t)B * 2 * n * sizeof(float2), 256);
+  if (!workspace || workspace_bytes < need)
+    return fail(SV_ERR_WORKSPACE, "spec_verify_sample_tree: workspace needs %zu bytes", need);
+  if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_sample_tree: workspace not 256-byte aligned");
   if (B == 0) return ok();
   TreeParams P = {};
+  P.stats = static_cast<float2 *>(workspace);
   P.target = target_logits; P.draft = draft ? draft : target_logits;
   P.parent = tree_parent; P.tokens = tree_tokens; P.uniforms = uniforms;
   P.out_tokens = out_tokens; P.num_acc = num_accepted; P.path = path_nodes; P.status = dev_status;
@@ -420,6 +502,22 @@ extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   const bool probs = draft_is_probs && n > 1;
+  const dim3 sgrid(2 * n, B);
+  switch (logit_dtype) {
+    case SV_F32:
+      e = probs ? launch_k(tree_row_stats_kernel<float, 1>, sgrid, dim3(kTsThreads), 0, s, 1, P)
+                : launch_k(tree_row_stats_kernel<float, 0>, sgrid, dim3(kTsThreads), 0, s, 1, P);
+      break;
+    case SV_BF16:
+      e = probs ? launch_k(tree_row_stats_kernel<__nv_bfloat16, 1>, sgrid, dim3(kTsThreads), 0, s, 1, P)
+                : launch_k(tree_row_stats_kernel<__nv_bfloat16, 0>, sgrid, dim3(kTsThreads), 0, s, 1, P);
+      break;
+    default:
+      e = probs ? launch_k(tree_row_stats_kernel<__half, 1>, sgrid, dim3(kTsThreads), 0, s, 1, P)
+                : launch_k(tree_row_stats_kernel<__half, 0>, sgrid, dim3(kTsThreads), 0, s, 1, P);
+      break;
+  }
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_tree statistics launch: %s", cudaGetErrorString(e));
   switch (logit_dtype) {
     case SV_F32:
       e = probs ? launch_k(sample_tree_kernel<float, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
