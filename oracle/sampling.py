@@ -200,8 +200,16 @@ def rejection_sample_chunked(target_logits, draft, draft_tokens, uniforms,
     return {k: np.concatenate([r[k] for r in parts]) for k in parts[0]}
 
 
+def entropy(p):
+    """H(p) = -sum p ln p in nats over the last axis (0 ln 0 = 0)."""
+    p = _np64(p)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(p > 0, p * np.log(np.where(p > 0, p, 1.0)), 0.0)
+    return -t.sum(axis=-1)
+
+
 def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, uniforms,
-                          draft_is_probs=False, temperature=1.0):
+                          draft_is_probs=False, temperature=1.0, typical=None):
     """Verify a draft tree per sequence by recursive rejection sampling.
 
     The pages give exact rejection sampling for a chain (quant67 section 3.1;
@@ -220,10 +228,18 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
     draft [B, n, V] logits (or probabilities): row u is what u's children
     were drawn from; tree_parent [B, n] (node 0 the root, parent -1);
     tree_tokens [B, n] (entry 0 unused); uniforms [B, n, 2].
+    typical = (epsilon, delta) switches to typical acceptance ("speculative
+    decoding" survey section 9.1 and "KV Cache + Speculative Decoding"
+    section 8.2 / Q18: the Medusa rule, not exact): child c of u is accepted
+    iff p_u(x) > min(epsilon, delta * exp(-H(p_u))), H in nats; the walk is
+    otherwise the same, except that no residual is formed: when no child is
+    accepted the token is drawn from p_u itself.
+
     Returns dict: out_tokens [B, n] (accepted tokens, the drawn one, then -1),
     num_accepted [B], path_nodes [B, n] (accepted nodes, then -1) and
     margin [B] (the smallest distance of a decision taken from its
-    boundary: |u - r/q| of every accept test and the CDF margin of the draw).
+    boundary: |u - r/q| of every accept test, or |p(x) - tau| / tau of every
+    typical test, and the CDF margin of the draw).
     """
     p_all = softmax(target_logits, temperature)
     q_all = _np64(draft) if draft_is_probs else softmax(draft, temperature)
@@ -241,6 +257,25 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
             r = p_all[b, u].copy()
             q = q_all[b, u]
             accepted = -1
+            if typical is not None:
+                tau = min(typical[0], typical[1] * np.exp(-entropy(r)))
+                for c in [c for c in range(1, n) if par[b, c] == u]:
+                    x = tok[b, c]
+                    margin[b] = min(margin[b], abs(r[x] - tau) / tau)
+                    if r[x] > tau:
+                        accepted = c
+                        break
+                if accepted >= 0:
+                    out[b, depth] = tok[b, accepted]
+                    path[b, depth] = accepted
+                    depth += 1
+                    u = accepted
+                    continue
+                y, m, _ = inverse_cdf(r[None, :], np.array([uv[b, u, 1]]))
+                out[b, depth] = y[0]
+                margin[b] = min(margin[b], m[0])
+                nacc[b] = depth
+                break
             for c in [c for c in range(1, n) if par[b, c] == u]:
                 x = tok[b, c]
                 accept = uv[b, c, 0] * q[x] < r[x]

@@ -128,3 +128,46 @@ def test_siblings_are_tried_in_bfs_order_by_hand():
     assert got["num_accepted"][0] == 1
     assert list(got["path_nodes"][0]) == [1, -1, -1]
     assert list(got["out_tokens"][0]) == [2, 0, -1]
+
+
+# ---- typical acceptance (the Medusa rule, opt-in and not exact) ----
+
+def test_entropy_matches_scipy():
+    import scipy.stats
+    rng = np.random.default_rng(4)
+    p = rng.dirichlet(np.ones(50), size=6)
+    p[0, :10] = 0
+    p[0] /= p[0].sum()
+    assert np.allclose(sampling.entropy(p), scipy.stats.entropy(p, axis=-1), rtol=1e-12, atol=0)
+
+
+def test_typical_threshold_by_hand():
+    # uniform p over V: H = ln V, tau = min(eps, delta / V); a draft is accepted
+    # iff 1/V > tau
+    V = 8
+    tl = np.zeros((2, 2, V))
+    dl = np.zeros((2, 2, V))
+    par = np.array([[-1, 0], [-1, 0]])
+    tok = np.array([[0, 3], [0, 3]])
+    uv = np.full((2, 2, 2), 0.5)
+    acc = sampling.tree_rejection_sample(tl, dl, par, tok, uv, typical=(0.3, 0.9))   # tau = 0.1125 < 0.125
+    rej = sampling.tree_rejection_sample(tl, dl, par, tok, uv, typical=(0.3, 1.1))   # tau = 0.1375 > 0.125
+    assert list(acc["num_accepted"]) == [1, 1] and list(acc["out_tokens"][0]) == [3, 4]
+    assert list(rej["num_accepted"]) == [0, 0] and list(rej["out_tokens"][0]) == [4, -1]
+
+
+def test_typical_never_accepting_draws_from_p():
+    # tau = min(1, huge) = 1 is never exceeded: the first token is drawn from
+    # p_root itself (no residual), so its law is p_root (Monte Carlo)
+    rng = np.random.default_rng(5)
+    V, N = 5, 30000
+    p = np.array([0.4, 0.25, 0.2, 0.1, 0.05])
+    tl = np.tile(np.log(p), (N, 3, 1))
+    par = np.tile(np.array([-1, 0, 0]), (N, 1))
+    tok = np.zeros((N, 3), dtype=np.int64)
+    tok[:, 1:] = rng.integers(0, V, (N, 2))
+    uv = rng.uniform(0, 1, (N, 3, 2))
+    got = sampling.tree_rejection_sample(tl, tl.copy(), par, tok, uv, typical=(1.0, 1e9))
+    assert (got["num_accepted"] == 0).all()
+    freq = np.bincount(got["out_tokens"][:, 0], minlength=V) / N
+    assert np.all(np.abs(freq - p) < 4.5 * np.sqrt(p * (1 - p) / N))
