@@ -366,16 +366,29 @@ sv_status spec_verify_sample_topp(const void *target_logits, sv_dtype logit_dtyp
  *   a row without a finite maximum SV_DEV_NONFINITE.
  *   fp32 arithmetic in a fixed order: deterministic, and equal to exact
  *   arithmetic unless a uniform lies within ~1e-6 of its boundary.
+ *   typical: NULL for the exact rule above, else typical acceptance (below).
  *   workspace: spec_verify_sample_tree_workspace_size(B, n) bytes (each
- *   row's (max, sum), 16 bytes per node), 256-byte aligned, no
+ *   row's (max, sum, entropy), 32 bytes per node), 256-byte aligned, no
  *   initialisation needed.
  * ------------------------------------------------------------------------ */
+/* Typical acceptance (opt-in, not exact): a draft x at node u is accepted
+ * iff p_u(x) > min(epsilon, delta * exp(-H(p_u))), H the entropy of p_u in
+ * nats; the first child in BFS order that passes is taken, and when none
+ * does the token is drawn from p_u itself (no residual). The draft rows are
+ * not read (draft may be NULL). "speculative decoding" survey section 9.1,
+ * "KV Cache + Speculative Decoding" section 8.2 and Q18. */
+typedef struct {
+  float epsilon;
+  float delta;
+} sv_typical_acceptance;
+
 size_t spec_verify_sample_tree_workspace_size(int B, int n);
 
 sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype logit_dtype,
                                   const void *draft, sv_dtype draft_dtype, int draft_is_probs,
                                   const int32_t *tree_parent, const int32_t *tree_tokens,
                                   const float *uniforms, int B, int n, int V, float temperature,
+                                  const sv_typical_acceptance *typical,
                                   int32_t *out_tokens, int32_t *num_accepted, int32_t *path_nodes,
                                   void *workspace, size_t workspace_bytes,
                                   int32_t *dev_status, sv_stream_t stream);

@@ -46,6 +46,10 @@ class OutOfBlocks(SpecVerifyError):
     """The block manager's pool has too few free pages for the call."""
 
 
+class _Typical(ctypes.Structure):
+    _fields_ = [("epsilon", ctypes.c_float), ("delta", ctypes.c_float)]
+
+
 class _Layout(ctypes.Structure):
     _fields_ = [("block_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64),
                 ("slot_stride", ctypes.c_int64)]
@@ -99,7 +103,7 @@ def load_library(path: str = LIB_PATH):
     lib.spec_verify_sample_tree_workspace_size.restype = Z
     lib.spec_verify_sample_tree_workspace_size.argtypes = [I, I]
     lib.spec_verify_sample_tree.restype = I
-    lib.spec_verify_sample_tree.argtypes = [P, I, P, I, I, P, P, P, I, I, I, F, P, P, P, P, Z, P, P]
+    lib.spec_verify_sample_tree.argtypes = [P, I, P, I, I, P, P, P, I, I, I, F, P, P, P, P, P, Z, P, P]
     I64, BMP = ctypes.c_int64, ctypes.c_void_p
     lib.sv_bm_create.restype = I
     lib.sv_bm_create.argtypes = [I, I, ctypes.POINTER(ctypes.c_void_p)]
@@ -352,8 +356,10 @@ def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_pr
 
 def spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, uniforms, draft_is_probs=False,
                             temperature=1.0, out_tokens=None, num_accepted=None, path_nodes=None, status=None,
-                            workspace=None):
+                            workspace=None, typical=None):
     """Rejection sampling over a draft tree of n nodes (BFS order, node 0 the root).
+
+    typical=(epsilon, delta) switches to typical acceptance (not exact; draft unused).
 
     target_logits [B, n, V]; draft [B, n, V] logits (same dtype) or f32 probabilities;
     tree_parent, tree_tokens int32 [B, n]; uniforms f32 [B, n, 2].
@@ -375,7 +381,9 @@ def spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, unif
         workspace = alloc_workspace(lib.spec_verify_sample_tree_workspace_size(B, n), dev)
     _check(lib.spec_verify_sample_tree(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft), ddt,
                                        int(bool(draft_is_probs)), _ptr(tree_parent), _ptr(tree_tokens),
-                                       _ptr(uniforms), B, n, V, float(temperature), _ptr(out_tokens),
+                                       _ptr(uniforms), B, n, V, float(temperature),
+                                       None if typical is None else ctypes.byref(_Typical(*typical)),
+                                       _ptr(out_tokens),
                                        _ptr(num_accepted), _ptr(path_nodes), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _ptr(status), _stream()))
     return out_tokens, num_accepted, path_nodes

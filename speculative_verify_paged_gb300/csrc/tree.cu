@@ -14,7 +14,14 @@
 //   c_{k+1} = c_k + D_k,  D_{k+1} = sum_x max(0, p(x) - c_{k+1} q(x)),
 // (induction: max(0, r_k - q) = max(0, p - c_k q - D_k q) / D_k), so a
 // rejection costs one row-wide sum and the draw one more pass. The rows'
-// (max, sum) statistics come from a pre-pass over all rows in parallel.
+// (max, sum, entropy) statistics come from a pre-pass over all rows in
+// parallel.
+//
+// Optionally (typical != NULL) the accept test is typical acceptance, the
+// Medusa rule the pages describe as an approximate alternative ("speculative
+// decoding" survey section 9.1, "KV Cache + Speculative Decoding" Q18): child
+// x of u is accepted iff p_u(x) > min(epsilon, delta exp(-H(p_u))), with no
+// residual; when no child passes, the token is drawn from p_u.
 //
 // Arithmetic is fp32 in a fixed order (each thread owns a contiguous chunk of
 // token ids, sums groups of 8, then a block tree), so the kernel is
@@ -44,7 +51,9 @@ struct TreeParams {
   int32_t *num_acc;        // [B]
   int32_t *path;           // [B][n]
   int32_t *status;
-  float2 *stats;           // [B][2n] (max, sum of 2^(fl(l c) - fl(max c))): target rows, then draft rows
+  float4 *stats;           // [B][2n] (max, S = sum of 2^t, H in nats, 0), t = fl(l c) - fl(max c): target rows, then draft rows
+  int typical;             // typical acceptance instead of rejection sampling
+  float tau_eps, tau_delta;
   int B, n, V, chunk;      // chunk: token ids per thread (a multiple of 8)
   int vec_t, vec_d;        // rows 16-byte aligned: vector loads
   float c;                 // log2(e) / T
@@ -222,46 +231,72 @@ __device__ __forceinline__ float tr_block_excl_scan(float v, float *s_red, float
 // walk evaluates p(x) and q(x) against.
 constexpr int kTsThreads = 512;
 
-__device__ __forceinline__ void tr_ms_combine(float &m, float &s, float m2, float s2, float c) {
+// (m, S, A) with S = sum 2^t and A = sum 2^t t, t = fl(l c) - fl(m c):
+// moving the reference from m to m' > m (d = fl(m' c) - fl(m c)) scales S by
+// 2^-d and turns A into 2^-d (A - d S).
+__device__ __forceinline__ void tr_msa_combine(float &m, float &s, float &a, float m2, float s2, float a2, float c) {
   const float mn = fmaxf(m, m2);
-  if (mn == -INFINITY) { m = mn; s = 0.f; return; }
+  if (mn == -INFINITY) { m = mn; s = 0.f; a = 0.f; return; }
   const float rc = __fmul_rn(mn, c);
-  s = (m == -INFINITY ? 0.f : s * tr_ex2(__fmul_rn(m, c) - rc)) +
-      (m2 == -INFINITY ? 0.f : s2 * tr_ex2(__fmul_rn(m2, c) - rc));
+  float s1 = 0.f, a1 = 0.f, s3 = 0.f, a3 = 0.f;
+  if (m != -INFINITY) {
+    const float d = rc - __fmul_rn(m, c), f = tr_ex2(-d);
+    s1 = s * f;
+    a1 = (a - d * s) * f;
+  }
+  if (m2 != -INFINITY) {
+    const float d = rc - __fmul_rn(m2, c), f = tr_ex2(-d);
+    s3 = s2 * f;
+    a3 = (a2 - d * s2) * f;
+  }
+  s = s1 + s3;
+  a = a1 + a3;
   m = mn;
 }
 
 template <typename T, int DK>
 __global__ void __launch_bounds__(kTsThreads) tree_row_stats_kernel(const __grid_constant__ TreeParams P) {
   using TD = typename std::conditional<DK == 1, float, T>::type;
-  __shared__ float s_m[kTsThreads / 32], s_s[kTsThreads / 32];
+  __shared__ float s_m[kTsThreads / 32], s_s[kTsThreads / 32], s_a[kTsThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.y, x = blockIdx.x, n = P.n, V = P.V;
   const bool draft_row = x >= n;
   const int node = draft_row ? x - n : x;
   if (draft_row) {
-    if (DK == 1) return;
+    if (DK == 1 || P.typical) return;
     bool has_child = false;
     for (int j = node + 1; j < n; ++j) has_child |= __ldg(P.parent + (int64_t)b * n + j) == node;
     if (!has_child) return;
   }
   const float c = P.c;
-  float m = -INFINITY, sum = 0.f;
+  float m = -INFINITY, sum = 0.f, ent = 0.f;   // ent: sum 2^t t
   auto add8 = [&](const float (&v)[8]) {
     float mx = v[0];
 #pragma unroll
     for (int k = 1; k < 8; ++k) mx = fmaxf(mx, v[k]);
     if (mx > m) {
-      sum = (m == -INFINITY) ? 0.f : sum * tr_ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+      if (m == -INFINITY) {
+        sum = 0.f;
+        ent = 0.f;
+      } else {
+        const float d = __fmul_rn(mx, c) - __fmul_rn(m, c), f = tr_ex2(-d);
+        ent = (ent - d * sum) * f;
+        sum *= f;
+      }
       m = mx;
     }
     if (m == -INFINITY) return;
     const float mc = __fmul_rn(m, c);
-    float g = 0.f;
+    float g = 0.f, h = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) g += tr_ex2(fmaf(v[k], c, -mc));
+    for (int k = 0; k < 8; ++k) {
+      const float t = fmaf(v[k], c, -mc), e = tr_ex2(t);
+      g += e;
+      h += t > -INFINITY ? e * t : 0.f;
+    }
     sum += g;
+    ent += h;
   };
   auto run = [&](const auto *row, bool vec) {
     const int ng = V / 8;
@@ -281,16 +316,19 @@ __global__ void __launch_bounds__(kTsThreads) tree_row_stats_kernel(const __grid
   else run(static_cast<const T *>(P.target) + ((int64_t)b * n + node) * V, P.vec_t);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-    tr_ms_combine(m, sum, m2, s2, c);
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o),
+                a2 = __shfl_xor_sync(0xffffffffu, ent, o);
+    tr_msa_combine(m, sum, ent, m2, s2, a2, c);
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) { s_m[warp] = m; s_s[warp] = sum; }
+  if (lane == 0) { s_m[warp] = m; s_s[warp] = sum; s_a[warp] = ent; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    float mm = s_m[0], ss = s_s[0];
-    for (int w = 1; w < kTsThreads / 32; ++w) tr_ms_combine(mm, ss, s_m[w], s_s[w], c);
-    P.stats[(int64_t)b * 2 * n + x] = make_float2(mm, ss);
+    float mm = s_m[0], ss = s_s[0], aa = s_a[0];
+    for (int w = 1; w < kTsThreads / 32; ++w) tr_msa_combine(mm, ss, aa, s_m[w], s_s[w], s_a[w], c);
+    // H = -sum p ln p = ln S - ln 2 * A / S  (p = 2^t / S, ln p = t ln 2 - ln S)
+    const float H = (ss > 0.f) ? logf(ss) - 0.693147180559945309f * aa / ss : 0.f;
+    P.stats[(int64_t)b * 2 * n + x] = make_float4(mm, ss, H, 0.f);
   }
 }
 
@@ -333,17 +371,20 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
     const T *prow = trow_base + (int64_t)u * V;
     const TD *qrow = drow_base + (int64_t)u * V;
     float m_q = 0.f, S_q = 1.f;
-    const float2 sp = P.stats[(int64_t)b * 2 * n + u];
+    const float4 sp = P.stats[(int64_t)b * 2 * n + u];
     const float m_p = sp.x, S_p = sp.y;
+    // typical acceptance: the threshold min(eps, delta exp(-H(p_u)))
+    const float tau = P.typical ? fminf(P.tau_eps, P.tau_delta * expf(-sp.z)) : 0.f;
     const float mpc = __fmul_rn(m_p, c), inv_p = 1.f / S_p;
     bool has_child = false;
     for (int j = u + 1; j < n; ++j) has_child |= par[j] == u;
-    if (has_child && DK == 0) {
-      const float2 sq = P.stats[(int64_t)b * 2 * n + n + u];
+    if (has_child && DK == 0 && !P.typical) {
+      const float4 sq = P.stats[(int64_t)b * 2 * n + n + u];
       m_q = sq.x;
       S_q = sq.y;
     }
-    if (!(m_p > -INFINITY && m_p < INFINITY) || (DK == 0 && has_child && !(m_q > -INFINITY && m_q < INFINITY))) {
+    if (!(m_p > -INFINITY && m_p < INFINITY) ||
+        (DK == 0 && has_child && !P.typical && !(m_q > -INFINITY && m_q < INFINITY))) {
       // a row without a finite maximum: flagged, the walk stops here
       if (tid == 0) { atomic_or_status(P.status, SV_DEV_NONFINITE); P.num_acc[b] = depth; }
       return;
@@ -359,6 +400,13 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
       const int x = tok[ch];
       if (x < 0 || x >= V) {   // flagged; such a child is never accepted and changes nothing
         if (tid == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+        continue;
+      }
+      if (P.typical) {   // no residual: the next child is tested against the same threshold
+        if (p_of(ld_f32(prow, x)) > tau) {
+          accepted = ch;
+          break;
+        }
         continue;
       }
       const float px = p_of(ld_f32(prow, x)), qx = q_of(ld_f32(qrow, x));
@@ -455,16 +503,16 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
 
 extern "C" size_t spec_verify_sample_tree_workspace_size(int B, int n) {
   if (B < 0 || n < 1) return 0;
-  return sv::align_up((size_t)B * 2 * n * sizeof(float2), 256);
+  return sv::align_up((size_t)B * 2 * n * sizeof(float4), 256);
 }
 
 extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype logit_dtype, const void *draft,
                                              sv_dtype draft_dtype, int draft_is_probs,
                                              const int32_t *tree_parent, const int32_t *tree_tokens,
                                              const float *uniforms, int B, int n, int V, float temperature,
-                                             int32_t *out_tokens, int32_t *num_accepted, int32_t *path_nodes,
-                                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                                             sv_stream_t stream) {
+                                             const sv_typical_acceptance *typical, int32_t *out_tokens,
+                                             int32_t *num_accepted, int32_t *path_nodes, void *workspace,
+                                             size_t workspace_bytes, int32_t *dev_status, sv_stream_t stream) {
   using namespace sv;
   if (B < 0 || n < 1 || V < 1)
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: bad sizes B=%d n=%d V=%d", B, n, V);
@@ -473,23 +521,29 @@ extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype
   if (!(temperature > 0.f) || !std::isfinite(temperature))
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: temperature must be finite and > 0");
   if (!target_logits || !tree_parent || !tree_tokens || !uniforms || !out_tokens || !num_accepted || !path_nodes ||
-      (n > 1 && !draft))
+      (n > 1 && !draft && !typical))
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: null pointer argument");
   if (logit_dtype != SV_F32 && logit_dtype != SV_BF16 && logit_dtype != SV_F16)
     return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: logits must be f32, bf16 or f16");
-  if (n > 1) {
+  if (n > 1 && draft) {
     if (draft_is_probs && draft_dtype != SV_F32)
       return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: draft probabilities must be f32");
     if (!draft_is_probs && draft_dtype != logit_dtype)
       return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_tree: draft logits must have the target's dtype");
   }
-  const size_t need = align_up((size_t)B * 2 * n * sizeof(float2), 256);
+  if (typical && !(typical->epsilon > 0.f && typical->delta > 0.f && std::isfinite(typical->epsilon) &&
+                   std::isfinite(typical->delta)))
+    return fail(SV_ERR_INVALID_ARG, "spec_verify_sample_tree: typical acceptance needs epsilon, delta > 0");
+  const size_t need = align_up((size_t)B * 2 * n * sizeof(float4), 256);
   if (!workspace || workspace_bytes < need)
     return fail(SV_ERR_WORKSPACE, "spec_verify_sample_tree: workspace needs %zu bytes", need);
   if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_sample_tree: workspace not 256-byte aligned");
   if (B == 0) return ok();
   TreeParams P = {};
-  P.stats = static_cast<float2 *>(workspace);
+  P.stats = static_cast<float4 *>(workspace);
+  P.typical = typical != nullptr;
+  P.tau_eps = typical ? typical->epsilon : 0.f;
+  P.tau_delta = typical ? typical->delta : 0.f;
   P.target = target_logits; P.draft = draft ? draft : target_logits;
   P.parent = tree_parent; P.tokens = tree_tokens; P.uniforms = uniforms;
   P.out_tokens = out_tokens; P.num_acc = num_accepted; P.path = path_nodes; P.status = dev_status;
@@ -501,7 +555,7 @@ extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype
   P.c = (float)(1.4426950408889634074 / (double)temperature);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  const bool probs = draft_is_probs && n > 1;
+  const bool probs = draft_is_probs && n > 1 && draft;
   const dim3 sgrid(2 * n, B);
   switch (logit_dtype) {
     case SV_F32:

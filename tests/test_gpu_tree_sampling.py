@@ -52,13 +52,14 @@ def make_inputs(B, n, V, dt, seed, sigma=1.5, T=1.0, parents=None, probs=False):
     return tl, draft, torch.from_numpy(par), torch.from_numpy(tok), uv
 
 
-def check(sv, tl, draft, par, tok, uv, T=1.0, probs=False, max_excused_frac=0.02):
+def check(sv, tl, draft, par, tok, uv, T=1.0, probs=False, max_excused_frac=0.02, typical=None):
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     out, nacc, path = sv.spec_verify_sample_tree(tl.to(DEV), draft.to(DEV), par.to(DEV), tok.to(DEV), uv.to(DEV),
-                                                 draft_is_probs=probs, temperature=T, status=st)
+                                                 draft_is_probs=probs, temperature=T, status=st, typical=typical)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    ref = osamp.tree_rejection_sample(tl, draft, par, tok, uv, draft_is_probs=probs, temperature=T)
+    ref = osamp.tree_rejection_sample(tl, draft, par, tok, uv, draft_is_probs=probs, temperature=T,
+                                      typical=typical)
     out, nacc, path = out.cpu().numpy(), nacc.cpu().numpy(), path.cpu().numpy()
     excused = 0
     for b in range(tl.shape[0]):
@@ -121,3 +122,11 @@ def test_bad_tree_and_token_are_flagged(sv):
     sv.spec_verify_sample_tree(tl.to(DEV), dl.to(DEV), par.to(DEV), tok.to(DEV), uv.to(DEV), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 32 and int(st.item()) & 4
+
+
+@pytest.mark.parametrize("dt,V,n,T,eps,delta", [("bf16", 2000, 8, 1.0, 0.09, 0.3), ("f32", 5000, 16, 1.6, 0.05, 0.5),
+                                                ("bf16", 128256, 5, 1.0, 0.09, 0.3)])
+def test_typical_acceptance_matches_oracle(sv, dt, V, n, T, eps, delta):
+    inputs = make_inputs(32 if V < 100000 else 16, n, V, dt, seed=V + 7, T=T)
+    ref = check(sv, *inputs, T=T, typical=(eps, delta))
+    assert ref["num_accepted"].max() >= 1 and (ref["num_accepted"] < n - 1).any()

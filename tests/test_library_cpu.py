@@ -143,8 +143,8 @@ def test_tree_attention_host_checks(lib):
 def test_tree_sampling_workspace_and_host_checks(lib):
     fake = ctypes.c_void_p(0x1000)
     NULL = None
-    assert lib.spec_verify_sample_tree_workspace_size(64, 5) == (64 * 2 * 5 * 8 + 255) // 256 * 256
-    args = lambda n, ws: (fake, 1, fake, 1, 0, fake, fake, fake, 2, n, 100, 1.0, fake, fake, fake, fake, ws,
+    assert lib.spec_verify_sample_tree_workspace_size(64, 5) == (64 * 2 * 5 * 16 + 255) // 256 * 256
+    args = lambda n, ws: (fake, 1, fake, 1, 0, fake, fake, fake, 2, n, 100, 1.0, NULL, fake, fake, fake, fake, ws,
                           NULL, NULL)
     assert lib.spec_verify_sample_tree(*args(5, 16)) == 3        # workspace too small
     assert lib.spec_verify_sample_tree(*args(65, 1 << 20)) == 2  # more than 64 nodes
