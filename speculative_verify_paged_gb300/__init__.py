@@ -11,6 +11,7 @@ Entry points (names follow the C ABI in include/specverify.h):
   spec_verify_attn    paged GQA verify attention over the K+1 queries
   spec_verify_sample  fused rejection sampling (accept / residual / bonus)
   verify_step         the three in stream order (one verify round of one layer)
+  tree_verify_step    the same for a draft tree, with the commit of the accepted path
   BlockManager        host block manager of the paged pool (sv_bm_*)
   copy_blocks         device page copies for copy-on-write (sv_copy_blocks)
 """
@@ -537,6 +538,22 @@ def copy_blocks(pools, pairs, num_blocks, block_bytes=None, block_stride_bytes=N
                               _ptr(idx[0]), _ptr(idx[1]), idx.shape[1], int(num_blocks),
                               _ptr(status), _stream()))
     return idx
+
+
+def tree_verify_step(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, tree_parent, target_logits,
+                     draft, tree_tokens, uniforms, k_scale=None, v_scale=None, draft_is_probs=False,
+                     temperature=1.0, softmax_scale=None, typical=None, status=None):
+    """One tree-verify round of one layer, in stream order: append the n node rows,
+    tree attention, tree sampling, then move each accepted path next to its root
+    (kv_tree_commit). Returns (attn_out, out_tokens, num_accepted, path_nodes); the
+    next round's length is seq_lens - n + num_accepted + 1 (BlockManager.commit_verify)."""
+    kv_block_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, status=status)
+    out = spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale, k_scale, v_scale,
+                           status=status, tree_parent=tree_parent)
+    toks, nacc, path = spec_verify_sample_tree(target_logits, draft, tree_parent, tree_tokens, uniforms,
+                                               draft_is_probs, temperature, status=status, typical=typical)
+    kv_tree_commit(k_cache, v_cache, block_table, seq_lens, path, nacc, status=status)
+    return out, toks, nacc, path
 
 
 def build(verbose=False, force=False):

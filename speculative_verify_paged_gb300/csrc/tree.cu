@@ -289,11 +289,16 @@ __global__ void __launch_bounds__(kTsThreads) tree_row_stats_kernel(const __grid
     if (m == -INFINITY) return;
     const float mc = __fmul_rn(m, c);
     float g = 0.f, h = 0.f;
+    if (P.typical) {   // the entropy term only matters to typical acceptance
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float t = fmaf(v[k], c, -mc), e = tr_ex2(t);
-      g += e;
-      h += t > -INFINITY ? e * t : 0.f;
+      for (int k = 0; k < 8; ++k) {
+        const float t = fmaf(v[k], c, -mc), e = tr_ex2(t);
+        g += e;
+        h += t > -INFINITY ? e * t : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) g += tr_ex2(fmaf(v[k], c, -mc));
     }
     sum += g;
     ent += h;

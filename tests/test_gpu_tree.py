@@ -161,3 +161,42 @@ def test_tree_round_commit(sv, kv):
     ref = osamp.tree_rejection_sample(tl, dl, par_h, tok, uv)
     clear = ref["margin"] > 1e-5
     assert np.array_equal(nacc.cpu().numpy()[clear], ref["num_accepted"][clear])
+
+
+def test_tree_verify_step_and_block_manager(sv):
+    # tree_verify_step through the binding, then the manager's rollback: the
+    # rows read back through the manager's table are prefix, root and path
+    from oracle import kv_append as oapp
+    n, bs, H_kv, d = 6, 16, 2, 128
+    cfg = workloads.CONFIGS["tiny"].with_(K=n - 1, B=3, ctx=("fixed", (50, 90, 33)), V=400, kv_dtype="bf16",
+                                          q_dtype="bf16", d_head=d)
+    bm = sv.BlockManager(64, bs)
+    for b, L in enumerate((50 - n, 90 - n, 33 - n)):
+        bm.allocate(b, L)
+    ids = [0, 1, 2]
+    assert bm.extend(ids, n) == []
+    table, lens = bm.block_table(ids, 16, device=DEV)
+    assert lens.tolist() == [50, 90, 33]
+    g = torch.Generator().manual_seed(8)
+    kc = torch.randn(64, H_kv, bs, d, generator=g).to(torch.bfloat16).to(DEV)
+    vc = torch.randn(64, H_kv, bs, d, generator=g).to(torch.bfloat16).to(DEV)
+    q = torch.randn(3, n, 4, d, generator=g).to(torch.bfloat16).to(DEV)
+    kn = torch.randn(3, n, H_kv, d, generator=g).to(torch.bfloat16).to(DEV)
+    vn = torch.randn(3, n, H_kv, d, generator=g).to(torch.bfloat16).to(DEV)
+    parents = torch.tensor([[-1, 0, 0, 1, 1, 2]] * 3, dtype=torch.int32, device=DEV)
+    tl = torch.randn(3, n, cfg.V, generator=g).to(torch.bfloat16).to(DEV)
+    tok = torch.randint(0, cfg.V, (3, n), generator=g, dtype=torch.int32).to(DEV)
+    uv = torch.rand(3, n, 2, generator=g).to(DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kc0 = kc.clone()
+    _, toks, nacc, path = sv.tree_verify_step(q, kn, vn, kc, vc, table, lens, parents, tl, tl, tok, uv, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # the expected pools: append by the oracle, then the oracle's commit
+    ka, _ = oapp.kv_block_append(kc0.cpu(), kc0.cpu(), kn.cpu(), vn.cpu(), table.cpu(), lens.cpu(), bs, "bf16")
+    ek, _ = oapp.kv_tree_commit(ka, ka, table.cpu(), lens.cpu(), n, path.cpu(), nacc.cpu(), bs)
+    assert torch.equal(kc.cpu(), ek)
+    bm.commit_verify(ids, n, nacc)
+    table2, lens2 = bm.block_table(ids, 16)
+    for b in range(3):
+        assert lens2[b] == lens[b].item() - n + int(nacc[b]) + 1
