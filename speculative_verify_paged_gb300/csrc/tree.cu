@@ -1,4 +1,4 @@
-// Rejection sampling over a draft tree: one CTA per sequence walks the tree
+// Rejection sampling over a draft tree: one cluster per sequence walks the tree
 // from the root. At node u the residual starts as r = p_u; u's children
 // (drafted from q_u) are tried in BFS order, child c with token x accepted
 // iff uniforms[c][0] * q_u(x) < r(x); a rejection replaces r by
@@ -37,7 +37,8 @@
 namespace sv {
 namespace {
 
-constexpr int kTrThreads = 1024;
+constexpr int kTrThreads = 512;
+constexpr int kTrCluster = 4;            // CTAs per sequence in the walk
 constexpr int kTrWarps = kTrThreads / 32;
 constexpr int kTrMaxNodes = 64;
 
@@ -54,7 +55,7 @@ struct TreeParams {
   float4 *stats;           // [B][2n] (max, S = sum of 2^t, H in nats, 0), t = fl(l c) - fl(max c): target rows, then draft rows
   int typical;             // typical acceptance instead of rejection sampling
   float tau_eps, tau_delta;
-  int B, n, V, chunk;      // chunk: token ids per thread (a multiple of 8)
+  int B, n, V, slice, chunk;   // token ids per walk CTA and per thread (multiples of 8)
   int vec_t, vec_d;        // rows 16-byte aligned: vector loads
   float c;                 // log2(e) / T
 };
@@ -337,17 +338,24 @@ __global__ void __launch_bounds__(kTsThreads) tree_row_stats_kernel(const __grid
   }
 }
 
+// The walk: one cluster of kTrCluster CTAs per sequence, CTA r owning the
+// token slice [r slice, (r + 1) slice) and each of its threads a chunk of
+// it. Every decision is computed identically in every CTA (point loads, and
+// cluster sums read in rank order), so control flow is cluster-uniform.
 template <typename T, int DK>
-__global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid_constant__ TreeParams P) {
+__global__ void __launch_bounds__(kTrThreads, 2) sample_tree_kernel(const __grid_constant__ TreeParams P) {
   using TD = typename std::conditional<DK == 1, float, T>::type;
   __shared__ int par[kTrMaxNodes];
   __shared__ int tok[kTrMaxNodes];
   __shared__ float s_red[kTrWarps];
+  __shared__ float s_part[2];            // this CTA's block total, alternating per cluster exchange
   __shared__ int s_owner, s_y, s_first, s_last;
 
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x, n = P.n, V = P.V;
+  const int rank = (int)cluster_ctarank();
+  const int CS = (int)gridDim.x;         // the cluster spans the grid's x dimension
+  const int b = blockIdx.y, n = P.n, V = P.V;
   const int tid = threadIdx.x;
   if (tid < n) {
     par[tid] = __ldg(P.parent + (int64_t)b * n + tid);
@@ -356,20 +364,32 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
   __syncthreads();
   int32_t *out = P.out_tokens + (int64_t)b * n;
   int32_t *path = P.path + (int64_t)b * n;
-  for (int j = tid; j < n; j += kTrThreads) { out[j] = -1; path[j] = -1; }
+  if (rank == 0)
+    for (int j = tid; j < n; j += kTrThreads) { out[j] = -1; path[j] = -1; }
   bool ok = par[0] == -1;
   for (int j = 1; j < n; ++j) ok &= par[j] >= 0 && par[j] < j;
   if (!ok) {
-    if (tid == 0) { atomic_or_status(P.status, SV_DEV_BAD_TREE); P.num_acc[b] = 0; }
+    if (rank == 0 && tid == 0) { atomic_or_status(P.status, SV_DEV_BAD_TREE); P.num_acc[b] = 0; }
     return;
   }
 
   const float c = P.c;
-  const int lo = tid * P.chunk, hi = min(V, lo + P.chunk);
-  const int nfull = hi > lo ? (hi - lo) / 8 : 0;       // whole groups of 8 in this thread's chunk
+  const int s_lo = min(V, rank * P.slice), s_hi = min(V, s_lo + P.slice);
+  const int lo = min(s_hi, s_lo + tid * P.chunk), hi = min(s_hi, lo + P.chunk);
+  const int nfull = (hi - lo) / 8;       // whole groups of 8 in this thread's chunk
   const T *trow_base = static_cast<const T *>(P.target) + (int64_t)b * n * V;
   const TD *drow_base = static_cast<const TD *>(P.draft) + (int64_t)b * n * V;
   const bool vt = P.vec_t, vd = P.vec_d;
+  int xchg = 0;
+  // the per-CTA totals of every CTA, in rank order (one cluster barrier)
+  auto cluster_parts = [&](float mine_cta, float (&parts)[kTrCluster]) {
+    const int slot = xchg & 1;
+    ++xchg;
+    if (tid == 0) s_part[slot] = mine_cta;
+    cluster_sync();
+#pragma unroll
+    for (int r = 0; r < kTrCluster; ++r) parts[r] = r < CS ? ld_dsmem_f32(mapa(&s_part[slot], r)) : 0.f;
+  };
 
   int u = 0, depth = 0;
   for (;;) {
@@ -391,7 +411,8 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
     if (!(m_p > -INFINITY && m_p < INFINITY) ||
         (DK == 0 && has_child && !P.typical && !(m_q > -INFINITY && m_q < INFINITY))) {
       // a row without a finite maximum: flagged, the walk stops here
-      if (tid == 0) { atomic_or_status(P.status, SV_DEV_NONFINITE); P.num_acc[b] = depth; }
+      if (rank == 0 && tid == 0) { atomic_or_status(P.status, SV_DEV_NONFINITE); P.num_acc[b] = depth; }
+      cluster_sync();   // no CTA leaves while another may read its shared memory
       return;
     }
     const float mqc = __fmul_rn(m_q, c), inv_q = 1.f / S_q;
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
       if (par[ch] != u) continue;
       const int x = tok[ch];
       if (x < 0 || x >= V) {   // flagged; such a child is never accepted and changes nothing
-        if (tid == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+        if (rank == 0 && tid == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
         continue;
       }
       if (P.typical) {   // no residual: the next child is tested against the same threshold
@@ -429,11 +450,15 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
         grp += fmaxf(0.f, p_of(lp) - coef * q_of(lq));
         if (++cnt == 8) { acc += grp; grp = 0.f; cnt = 0; }
       });
-      D = tr_block_sum(acc + grp, s_red);
+      float parts[kTrCluster];
+      cluster_parts(tr_block_sum(acc + grp, s_red), parts);
+      D = 0.f;
+#pragma unroll
+      for (int r = 0; r < kTrCluster; ++r) D += parts[r];
       if (!(D > 0.f)) { coef = 0.f; D = 1.f; }   // cannot happen in exact arithmetic: draw from p
     }
     if (accepted >= 0) {
-      if (tid == 0) { out[depth] = tok[accepted]; path[depth] = accepted; }
+      if (rank == 0 && tid == 0) { out[depth] = tok[accepted]; path[depth] = accepted; }
       ++depth;
       u = accepted;
       continue;
@@ -450,23 +475,40 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
       if (++cnt == 8) { mine += grp; grp = 0.f; cnt = 0; }
     });
     mine += grp;
-    float Z;
-    const float before = tr_block_excl_scan(mine, s_red, &Z);
+    float Zc;
+    const float before_cta = tr_block_excl_scan(mine, s_red, &Zc);
+    float parts[kTrCluster];
+    cluster_parts(Zc, parts);
+    float Z = 0.f, off = 0.f;
+#pragma unroll
+    for (int r = 0; r < kTrCluster; ++r) {
+      if (r < rank) off += parts[r];
+      Z += parts[r];
+    }
     const float target = __ldg(P.uniforms + ((int64_t)b * n + u) * 2 + 1) * Z;
+    // the CTA, then the chunk, holding y = min{y : C(y) > v Z}: the last
+    // whose running sum before it is <= v Z (the same sums in every CTA)
+    int owner_rank = 0;
+    {
+      float o = 0.f;
+#pragma unroll
+      for (int r = 0; r < kTrCluster; ++r) {
+        if (r < CS && o <= target) owner_rank = r;
+        o += parts[r];
+      }
+    }
+    const float before = off + before_cta;
     if (tid == 0) { s_owner = 0; s_y = -1; s_first = INT_MAX; s_last = -1; }
     __syncthreads();
-    // the chunk holding y = min{y : C(y) > v Z}: the last one whose running
-    // sum before it is <= v Z (prefix sums in thread order are one scan, so
-    // every thread sees the same boundaries)
-    if (before <= target) atomicMax(&s_owner, tid);
+    if (rank == owner_rank && before <= target) atomicMax(&s_owner, tid);
     __syncthreads();
     const int owner = s_owner;
-    if ((tid >> 5) == (owner >> 5)) {
+    if (rank == owner_rank && (tid >> 5) == (owner >> 5)) {
       // the owner's warp rescans the owner's chunk: lane l takes per
       // consecutive tokens, a warp scan of their weights (from the owner's
       // running sum) finds the lane holding the first y with C(y) > v Z
       const int lane = tid & 31;
-      const int olo = owner * P.chunk, ohi = min(V, olo + P.chunk);
+      const int olo = min(s_hi, s_lo + owner * P.chunk), ohi = min(s_hi, olo + P.chunk);
       const int per = (P.chunk + 31) / 32;
       const int a0 = min(ohi, olo + lane * per), a1 = min(ohi, a0 + per);
       float part = 0.f;
@@ -489,16 +531,23 @@ __global__ void __launch_bounds__(kTrThreads, 1) sample_tree_kernel(const __grid
         }
       }
     }
-    if (tid > owner) atomicMin(&s_first, first_pos);
-    atomicMax(&s_last, last_pos);
-    __syncthreads();
     // rounding can leave v Z past the owner's chunk: then the next token with
     // weight, or the last one with weight when there is none after it
-    int y = s_y >= 0 ? s_y : (s_first != INT_MAX ? s_first : s_last);
-    if (tid == 0) {
-      out[depth] = y;
+    if (rank > owner_rank || (rank == owner_rank && tid > owner)) atomicMin(&s_first, first_pos);
+    atomicMax(&s_last, last_pos);
+    __syncthreads();
+    cluster_sync();
+    if (rank == 0 && tid == 0) {
+      int y = -1, first = INT_MAX, last = -1;
+      for (int r = 0; r < CS; ++r) {
+        if (r == owner_rank) y = ld_dsmem_s32(mapa(&s_y, r));
+        first = min(first, ld_dsmem_s32(mapa(&s_first, r)));
+        last = max(last, ld_dsmem_s32(mapa(&s_last, r)));
+      }
+      out[depth] = y >= 0 ? y : (first != INT_MAX ? first : last);
       P.num_acc[b] = depth;
     }
+    cluster_sync();   // the first CTA has read every CTA's results
     return;
   }
 }
@@ -553,7 +602,8 @@ extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype
   P.parent = tree_parent; P.tokens = tree_tokens; P.uniforms = uniforms;
   P.out_tokens = out_tokens; P.num_acc = num_accepted; P.path = path_nodes; P.status = dev_status;
   P.B = B; P.n = n; P.V = V;
-  P.chunk = ((V + kTrThreads - 1) / kTrThreads + 7) / 8 * 8;
+  P.slice = ((V + kTrCluster - 1) / kTrCluster + 7) / 8 * 8;
+  P.chunk = ((P.slice + kTrThreads - 1) / kTrThreads + 7) / 8 * 8;
   const int es_t = dtype_bytes(logit_dtype), es_d = draft_is_probs ? 4 : es_t;
   P.vec_t = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0;
   P.vec_d = aligned(P.draft, 16) && ((size_t)V * es_d) % 16 == 0;
@@ -579,16 +629,16 @@ extern "C" sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_tree statistics launch: %s", cudaGetErrorString(e));
   switch (logit_dtype) {
     case SV_F32:
-      e = probs ? launch_k(sample_tree_kernel<float, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
-                : launch_k(sample_tree_kernel<float, 0>, dim3(B), dim3(kTrThreads), 0, s, 1, P);
+      e = probs ? launch_k(sample_tree_kernel<float, 1>, dim3(kTrCluster, B), dim3(kTrThreads), 0, s, kTrCluster, P)
+                : launch_k(sample_tree_kernel<float, 0>, dim3(kTrCluster, B), dim3(kTrThreads), 0, s, kTrCluster, P);
       break;
     case SV_BF16:
-      e = probs ? launch_k(sample_tree_kernel<__nv_bfloat16, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
-                : launch_k(sample_tree_kernel<__nv_bfloat16, 0>, dim3(B), dim3(kTrThreads), 0, s, 1, P);
+      e = probs ? launch_k(sample_tree_kernel<__nv_bfloat16, 1>, dim3(kTrCluster, B), dim3(kTrThreads), 0, s, kTrCluster, P)
+                : launch_k(sample_tree_kernel<__nv_bfloat16, 0>, dim3(kTrCluster, B), dim3(kTrThreads), 0, s, kTrCluster, P);
       break;
     default:
-      e = probs ? launch_k(sample_tree_kernel<__half, 1>, dim3(B), dim3(kTrThreads), 0, s, 1, P)
-                : launch_k(sample_tree_kernel<__half, 0>, dim3(B), dim3(kTrThreads), 0, s, 1, P);
+      e = probs ? launch_k(sample_tree_kernel<__half, 1>, dim3(kTrCluster, B), dim3(kTrThreads), 0, s, kTrCluster, P)
+                : launch_k(sample_tree_kernel<__half, 0>, dim3(kTrCluster, B), dim3(kTrThreads), 0, s, kTrCluster, P);
       break;
   }
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_tree launch: %s", cudaGetErrorString(e));
