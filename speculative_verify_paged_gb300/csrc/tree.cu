@@ -121,35 +121,10 @@ __device__ __forceinline__ float raw_at(const Raw8<T> &r, int k) {
   return __half2float(__ushort_as_half((unsigned short)h));
 }
 
-// f(x, id) over the chunk [lo, hi) of a row in token order; nfull whole
-// groups of eight from lo, then the rest one element at a time. Aligned rows
-// keep NB 16-byte loads in flight per thread.
-template <typename T, typename F>
-__device__ __forceinline__ void tr_each(const T *row, bool vec, int lo, int nfull, int hi, F f) {
-  constexpr int NB = sizeof(T) == 4 ? 2 : 4;
-  int g = 0;
-  if (vec) {
-    for (; g + NB <= nfull; g += NB) {
-      Raw8<T> r[NB];
-#pragma unroll
-      for (int u = 0; u < NB; ++u) ld_raw(row, lo + 8 * (g + u), r[u]);
-#pragma unroll
-      for (int u = 0; u < NB; ++u)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f(raw_at(r[u], k), lo + 8 * (g + u) + k);
-    }
-  }
-  for (; g < nfull; ++g) {
-    float x[8];
-    ld8(row, lo + 8 * g, vec, x);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) f(x[k], lo + 8 * g + k);
-  }
-  for (int i = lo + 8 * nfull; i < hi; ++i) f(ld_f32(row, i), i);
-}
-
-// The same over two rows at once (p and q), f(lp, lq, id); with use_q false
-// the q row is not read and lq is 0.
+// f(lp, lq, id) over the chunk [lo, hi) of two rows (p and q) in token
+// order: nfull whole groups of eight from lo (two groups of 16-byte loads in
+// flight when the rows are aligned), then the rest one element at a time;
+// with use_q false the q row is not read and lq is 0.
 template <typename T, typename TD, typename F>
 __device__ __forceinline__ void tr_each2(const T *pr, bool vt, const TD *qr, bool vd, bool use_q, int lo, int nfull,
                                          int hi, F f) {
@@ -189,16 +164,6 @@ __device__ __forceinline__ float tr_block_sum(float v, float *s_red) {
   float t = lane < kTrWarps ? s_red[lane] : 0.f;
   t = warp_sum(t);
   return t;   // every thread of warp 0..31 holds the total (all warps recompute it)
-}
-
-__device__ __forceinline__ float tr_block_max(float v, float *s_red) {
-  v = warp_max(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  float t = lane < kTrWarps ? s_red[lane] : -INFINITY;
-  return warp_max(t);
 }
 
 // Exclusive scan of one float per thread in thread order; *total the sum.
