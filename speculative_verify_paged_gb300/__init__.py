@@ -12,6 +12,7 @@ Entry points (names follow the C ABI in include/specverify.h):
   spec_verify_sample  fused rejection sampling (accept / residual / bonus)
   verify_step         the three in stream order (one verify round of one layer)
   tree_verify_step    the same for a draft tree, with the commit of the accepted path
+  MultiLayerVerify    a round over many layers' pools, runnable as one CUDA graph
   BlockManager        host block manager of the paged pool (sv_bm_*)
   copy_blocks         device page copies for copy-on-write (sv_copy_blocks)
 """
@@ -436,8 +437,12 @@ class BlockManager:
         self.page_size = int(page_size)
 
     def close(self):
-        if getattr(self, "_h", None) is not None and self._h.value:
-            self._lib.sv_bm_destroy(self._h)
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            try:
+                self._lib.sv_bm_destroy(h)
+            except Exception:   # interpreter shutdown: the library may be gone already
+                pass
         self._h = None
 
     def __del__(self):
@@ -554,6 +559,69 @@ def tree_verify_step(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, t
                                                draft_is_probs, temperature, status=status, typical=typical)
     kv_tree_commit(k_cache, v_cache, block_table, seq_lens, path, nacc, status=status)
     return out, toks, nacc, path
+
+
+class MultiLayerVerify:
+    """One verify round over several layers on one stream: per layer, append its
+    K+1 rows into its own paged pools and attend; then one sampling pass.
+
+    layers: list of dicts with device tensors q, k_new, v_new, k_cache, v_cache
+    (and optionally k_scale, v_scale), all layers sharing block_table and
+    seq_lens (one page table for the whole model, one pool pair per layer).
+    Inputs and outputs stay in these static buffers, so the round can be
+    captured once as a CUDA graph (capture()) and replayed (replay()); run()
+    launches it directly. Attention outputs: self.outs[layer]; sampling:
+    self.out_tokens, self.num_accepted.
+    """
+
+    def __init__(self, layers, block_table, seq_lens, target_logits, draft, draft_tokens, uniforms,
+                 draft_is_probs=False, temperature=1.0, block_size=16):
+        self.layers = layers
+        self.block_table, self.seq_lens = block_table, seq_lens
+        self.target_logits, self.draft = target_logits, draft
+        self.draft_tokens, self.uniforms = draft_tokens, uniforms
+        self.draft_is_probs, self.temperature, self.block_size = draft_is_probs, temperature, block_size
+        q0 = layers[0]["q"]
+        B, n_new, H_q, d = q0.shape
+        H_kv = layers[0]["k_cache"].shape[1]
+        dev = q0.device
+        self.outs = [torch.empty_like(l["q"]) for l in layers]
+        self.attn_ws = alloc_workspace(attn_workspace_size(B, n_new, H_q, H_kv, d, block_table.shape[1],
+                                                           block_size), dev)
+        Bs, K1, V = target_logits.shape
+        self.samp_ws = alloc_workspace(sample_workspace_size(Bs, K1 - 1, V), dev)
+        self.out_tokens = torch.empty((Bs, K1), dtype=torch.int32, device=dev)
+        self.num_accepted = torch.empty((Bs,), dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def run(self):
+        for l, out in zip(self.layers, self.outs):
+            kv_block_append(l["k_new"], l["v_new"], l["k_cache"], l["v_cache"], self.block_table, self.seq_lens,
+                            l.get("k_scale"), l.get("v_scale"), block_size=self.block_size, status=self.status)
+            spec_verify_attn(l["q"], l["k_cache"], l["v_cache"], self.block_table, self.seq_lens, None,
+                             l.get("k_scale"), l.get("v_scale"), block_size=self.block_size, out=out,
+                             workspace=self.attn_ws, status=self.status)
+        spec_verify_sample(self.target_logits, self.draft, self.draft_tokens, self.uniforms, self.draft_is_probs,
+                           self.temperature, out_tokens=self.out_tokens, num_accepted=self.num_accepted,
+                           workspace=self.samp_ws, status=self.status, want_probs=False)
+
+    def capture(self):
+        """Record the round once as a CUDA graph (after one direct run, which
+        also sets the kernels' attributes outside the capture)."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
 
 
 def build(verbose=False, force=False):

@@ -348,3 +348,46 @@ def test_verify_step_end_to_end(lib):
     assert np.abs(out.float().cpu().numpy() - ref).max() <= 2e-2
     r = osamp.rejection_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"])
     compare_sampling(tok.cpu().numpy(), nac.cpu().numpy(), r)
+
+
+def test_multi_layer_round_as_cuda_graph(lib):
+    # three layers' pools behind one page table: each layer's output equals the
+    # oracle's, and replaying the captured graph reproduces the direct run
+    import speculative_verify_paged_gb300 as sv
+    cfg = workloads.CONFIGS["llama3_8b"].with_(B=3, ctx=("fixed", (200, 1500, 33)), V=5000)
+    s = workloads.make_sampling_inputs(cfg, seed=11)
+    layers, refs = [], []
+    for li in range(3):
+        a = workloads.make_attention_inputs(cfg, seed=20 + li)
+        n = workloads.make_append_inputs(cfg, seed=20 + li)
+        if li:
+            a["block_table"], a["seq_lens"] = layers[0]["_table"], layers[0]["_lens"]
+        rk, rv = oapp.kv_block_append(a["k_cache"], a["v_cache"], n["k_new"], n["v_new"], a["block_table"],
+                                      a["seq_lens"], 16, "bf16")
+        refs.append(oatt.verify_attention(a["q"], rk, rv, a["block_table"], a["seq_lens"], 1 / math.sqrt(128)))
+        g = to_dev({"q": a["q"], "k_new": n["k_new"], "v_new": n["v_new"], "k_cache": a["k_cache"],
+                    "v_cache": a["v_cache"]})
+        g["_table"], g["_lens"] = a["block_table"], a["seq_lens"]
+        layers.append(g)
+    table, lens = to_dev({"t": layers[0]["_table"], "l": layers[0]["_lens"]}).values()
+    gs = to_dev(s)
+    mv = sv.MultiLayerVerify([{k: v for k, v in l.items() if not k.startswith("_")} for l in layers], table, lens,
+                             gs["target_logits"], gs["draft_logits"], gs["draft_tokens"], gs["uniforms"])
+    mv.run()
+    torch.cuda.synchronize()
+    direct = [o.clone() for o in mv.outs]
+    tok0, nac0 = mv.out_tokens.clone(), mv.num_accepted.clone()
+    for o, ref in zip(direct, refs):
+        assert np.abs(o.float().cpu().numpy() - ref).max() <= 2e-2
+    r = osamp.rejection_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"])
+    compare_sampling(tok0.cpu().numpy(), nac0.cpu().numpy(), r)
+    for o in mv.outs:
+        o.zero_()
+    mv.capture()
+    for _ in range(2):
+        mv.replay()
+    torch.cuda.synchronize()
+    assert int(mv.status.item()) == 0
+    for o, d in zip(mv.outs, direct):
+        assert torch.equal(o, d)
+    assert torch.equal(mv.out_tokens, tok0) and torch.equal(mv.num_accepted, nac0)
