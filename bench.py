@@ -363,7 +363,11 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     assert int(status.item()) == 0
 
-    nxt = measure_next_rows(sv, cfg, a, s, dev, stream, status) if rank == 0 else None
+    nxt = None
+    if rank == 0:
+        nxt = measure_next_rows(sv, cfg, a, s, dev, stream, status)
+        nxt["mla"] = measure_mla(sv, dev, stream, status)
+        nxt["multi_layer"] = measure_multi_layer(sv, cfg, a, n, s, dev, stream, status)
 
     if rank != 0:
         if world > 1:
@@ -518,6 +522,87 @@ def measure_next_rows(sv, cfg, a, s, dev, stream, status, reps=20):
                                   "achieved": cow_bytes / (cow_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
                                   "frac": cow_bytes / (cow_us * 1e-6) / 1e9 / peak, "bytes": cow_bytes}},
     }
+
+
+def measure_mla(sv, dev, stream, status, reps=10, B=64, n_new=5, H=128, ctx=(1024, 8192), seed=0):
+    """MLA verify attention on a DeepSeek-V2 layer shape: 128 heads, latent rows
+    of d_c + d_r = 512 + 64 bf16 values, K = 4 drafts (5 query positions), the
+    70B config's batch and ragged context lengths, 16-token blocks in a
+    random permutation. The cache (about 340 MB) is larger than L2. Work is
+    counted as the algorithm's multiply-adds (Q K^T over 576 values and P V
+    over 512 per visible key and query row), not the kernel's own (it
+    computes Q K^T once per output half)."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    lens = torch.randint(ctx[0], ctx[1] + 1, (B,), generator=g).tolist()
+    nblk = [(L + 15) // 16 for L in lens]
+    nb = sum(nblk) + 8
+    perm = torch.randperm(nb, generator=g).to(torch.int32)
+    table = torch.full((B, max(nblk)), -1, dtype=torch.int32)
+    off = 0
+    for b, k in enumerate(nblk):
+        table[b, :k] = perm[off:off + k]
+        off += k
+    gd = torch.Generator(device=dev).manual_seed(seed)
+    cache = torch.randn((nb, 16, 576), generator=gd, device=dev).to(torch.bfloat16)
+    q = torch.randn((B, n_new, H, 576), generator=gd, device=dev).to(torch.bfloat16)
+    table, seq = table.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = torch.empty((B, n_new, H, 512), dtype=torch.bfloat16, device=dev)
+    ws = sv.alloc_workspace(sv.mla_workspace_size(B, n_new, H, table.shape[1]), dev)
+    scale = 1.0 / math.sqrt(128 + 64)
+    fn = lambda: sv.spec_verify_attn_mla(q, cache, table, seq, scale, out=out, workspace=ws, status=status)
+    for _ in range(3):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / reps
+    assert int(status.item()) == 0
+    vis = sum(H * (L - n_new + j + 1) for L in lens for j in range(n_new))
+    flops = 2.0 * vis * (576 + 512)
+    nbytes = sum(lens) * 1152 + q.numel() * 2 + out.numel() * 2
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        tpeak = float(json.load(f)["bf16_tflops"])
+    return {"workload": "DeepSeek-V2 MLA layer shape: B=%d, H=%d, d_c=512, d_r=64, K=%d, ctx uniform [%d, %d], "
+                        "block_size 16, bf16" % (B, H, n_new - 1, ctx[0], ctx[1]),
+            "us": us, "flops": flops, "bytes": nbytes,
+            "roofline": {"bound": "tensor", "kernel": "attn_mla_kernel", "achieved": flops / (us * 1e-6) / 1e12,
+                         "peak": tpeak, "unit": "TFLOP/s", "frac": flops / (us * 1e-6) / 1e12 / tpeak,
+                         "hbm_gbs": nbytes / (us * 1e-6) / 1e9}}
+
+
+def measure_multi_layer(sv, cfg, a, n, s, dev, stream, status, n_layers=8, reps=5):
+    """One verify round over n_layers layers (append + attention per layer, one
+    sampling pass) launched directly and as a replayed CUDA graph. The layers
+    share this layer's pools (each layer's working set is far above L2, so a
+    layer reads its KV from HBM either way) and have their own queries."""
+    import torch
+    layers = [{"q": a["q"].clone(), "k_new": n["k_new"], "v_new": n["v_new"], "k_cache": a["k_cache"],
+               "v_cache": a["v_cache"], "k_scale": a["k_scale"], "v_scale": a["v_scale"]} for _ in range(n_layers)]
+    mv = sv.MultiLayerVerify(layers, a["block_table"], a["seq_lens"], s["target_logits"], s["draft_logits"],
+                             s["draft_tokens"], s["uniforms"], block_size=cfg.block_size)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(torch.cuda.current_stream())
+        for _ in range(reps):
+            fn()
+        e1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps
+    direct_us = timed(mv.run)
+    mv.capture()
+    graph_us = timed(mv.replay)
+    assert int(mv.status.item()) == 0
+    return {"layers": n_layers, "direct_us": direct_us, "graph_us": graph_us,
+            "per_layer_us_graph": graph_us / n_layers}
 
 
 def oracle_sample_time(cfg, a, n, s, n_attn, n_samp):

@@ -523,6 +523,54 @@ sv_status sv_copy_blocks(void *const *pools, int n_pools, int64_t block_stride_b
                          const int32_t *src, const int32_t *dst, int n_pairs, int num_blocks,
                          int32_t *dev_status, sv_stream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * Multi-head latent attention (MLA), absorbed form
+ *   ("KV Cache + Speculative Decoding", sections 4.3-4.4: the cache holds,
+ *   per token and layer, one row [c ; k^R] of d_c + d_r values shared by all
+ *   heads; section 4.3.3 and Q22: the up-projection W_UK of head i is
+ *   absorbed into its query and W_UV into the output projection.)
+ *
+ * kv_block_append_latent
+ *   Writes c_new[b][j][:] (bf16 [B][n_new][d_latent]) into the paged pool
+ *   cache (bf16 [num_blocks][block_size][d_latent]) at position
+ *   seq_lens[b] - n_new + j: block block_table[b][pos / block_size], slot
+ *   pos % block_size. d_latent = 576, block_size = 16 (SV_ERR_UNSUPPORTED
+ *   otherwise). Pointers 16-byte aligned. A length outside
+ *   [n_new, max_blocks_per_seq * 16] sets SV_DEV_BAD_SEQ_LEN, a block
+ *   outside [0, num_blocks) SV_DEV_BAD_BLOCK; that row is not written.
+ *   Waits for the previous kernel of the stream before its stores.
+ *   dev_status may be NULL (device errors then go unreported).
+ *
+ * spec_verify_attn_mla
+ *   q_lat: bf16 [B][n_new][H][d_c + d_r], the absorbed query of position j,
+ *   head i: [W_UK[i]^T q^C ; q^R] (q^R already rotated). cache: bf16
+ *   [num_blocks][block_size][d_c + d_r] (k^R already rotated). For every
+ *   (b, j, i): score_t = q_lat . cache_row(t) * softmax_scale for keys
+ *   t <= seq_lens[b] - n_new + j, w = softmax(score), and
+ *   out[b][j][i][:] = sum_t w_t cache_row(t)[0 .. d_c) (bf16
+ *   [B][n_new][H][d_c]). The caller multiplies by W_UV[i] (or folds it into
+ *   W_O). softmax_scale: 1 / sqrt(d_head + d_r) in the pages' model.
+ *   d_c = 512, d_r = 64, block_size = 16, bf16 only (SV_ERR_UNSUPPORTED
+ *   otherwise). workspace: spec_verify_attn_mla_workspace_size(...) bytes,
+ *   256-byte aligned (the partial outputs of a split context; may be NULL
+ *   when that size is 0). Device errors as for spec_verify_attn. Waits for
+ *   the previous kernel of the stream before it reads anything.
+ * ------------------------------------------------------------------------ */
+sv_status kv_block_append_latent(const void *c_new, sv_dtype dtype, void *cache,
+                                 const int32_t *block_table, int max_blocks_per_seq,
+                                 const int32_t *seq_lens, int B, int n_new, int d_latent,
+                                 int block_size, int num_blocks, int32_t *dev_status,
+                                 sv_stream_t stream);
+
+size_t spec_verify_attn_mla_workspace_size(int B, int n_new, int H, int max_blocks_per_seq);
+
+sv_status spec_verify_attn_mla(const void *q_lat, sv_dtype q_dtype, const void *cache,
+                               sv_dtype cache_dtype, const int32_t *block_table,
+                               int max_blocks_per_seq, const int32_t *seq_lens, int B, int n_new,
+                               int H, int d_c, int d_r, int block_size, int num_blocks,
+                               float softmax_scale, void *out, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

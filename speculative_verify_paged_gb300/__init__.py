@@ -13,6 +13,8 @@ Entry points (names follow the C ABI in include/specverify.h):
   verify_step         the three in stream order (one verify round of one layer)
   tree_verify_step    the same for a draft tree, with the commit of the accepted path
   MultiLayerVerify    a round over many layers' pools, runnable as one CUDA graph
+  spec_verify_attn_mla, kv_block_append_latent
+                      the same verify attention for a latent (MLA) cache
   BlockManager        host block manager of the paged pool (sv_bm_*)
   copy_blocks         device page copies for copy-on-write (sv_copy_blocks)
 """
@@ -137,6 +139,12 @@ def load_library(path: str = LIB_PATH):
     lib.sv_bm_block_table.argtypes = [BMP, P, I, I, P, P]
     lib.sv_copy_blocks.restype = I
     lib.sv_copy_blocks.argtypes = [P, I, I64, I64, P, P, I, I, P, P]
+    lib.kv_block_append_latent.restype = I
+    lib.kv_block_append_latent.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P]
+    lib.spec_verify_attn_mla_workspace_size.restype = Z
+    lib.spec_verify_attn_mla_workspace_size.argtypes = [I, I, I, I]
+    lib.spec_verify_attn_mla.restype = I
+    lib.spec_verify_attn_mla.argtypes = [P, I, P, I, P, I, P, I, I, I, I, I, I, I, F, P, P, Z, P, P]
     _lib = lib
     return lib
 
@@ -276,6 +284,43 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=N
         _check(lib.spec_verify_attn(*args, _stream()))
     else:
         _check(lib.spec_verify_attn_ex(*args, int(blocks_per_split), _stream()))
+    return out
+
+
+# ------------------------------------------------------------------ MLA ---
+
+def kv_block_append_latent(c_new, cache, block_table, seq_lens, block_size=16, status=None):
+    """Write latent rows c_new [B, n_new, d_c + d_r] (bf16) at positions
+    seq_lens - n_new .. seq_lens - 1 of the pool cache [num_blocks, bs, d_c + d_r]."""
+    lib = load_library()
+    _cuda(c_new, cache, block_table, seq_lens, status)
+    B, n_new, D = c_new.shape
+    _check(lib.kv_block_append_latent(_ptr(c_new), _dtype_code(c_new), _ptr(cache), _ptr(block_table),
+                                      block_table.shape[1], _ptr(seq_lens), B, n_new, D, block_size,
+                                      cache.shape[0], _ptr(status), _stream()))
+
+
+def mla_workspace_size(B, n_new, H, max_blocks_per_seq):
+    return load_library().spec_verify_attn_mla_workspace_size(B, n_new, H, max_blocks_per_seq)
+
+
+def spec_verify_attn_mla(q_lat, cache, block_table, seq_lens, softmax_scale, d_c=512, block_size=16, out=None,
+                         workspace=None, status=None):
+    """Absorbed MLA verify attention: q_lat [B, n_new, H, d_c + d_r] bf16 against
+    the latent pool cache [num_blocks, bs, d_c + d_r] bf16; returns the latent
+    outputs [B, n_new, H, d_c] (bf16), to be multiplied by each head's W_UV."""
+    lib = load_library()
+    _cuda(q_lat, cache, block_table, seq_lens, out, workspace, status)
+    B, n_new, H, D = q_lat.shape
+    if out is None:
+        out = torch.empty((B, n_new, H, d_c), dtype=q_lat.dtype, device=q_lat.device)
+    max_blocks = block_table.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(mla_workspace_size(B, n_new, H, max_blocks), q_lat.device)
+    _check(lib.spec_verify_attn_mla(_ptr(q_lat), _dtype_code(q_lat), _ptr(cache), _dtype_code(cache),
+                                    _ptr(block_table), max_blocks, _ptr(seq_lens), B, n_new, H, d_c, D - d_c,
+                                    block_size, cache.shape[0], float(softmax_scale), _ptr(out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(status), _stream()))
     return out
 
 

@@ -161,3 +161,24 @@ def test_product_path_has_no_cpu_fallback():
                               torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, 5, 2))
     with pytest.raises((ValueError, RuntimeError)):
         sv.spec_verify_attn(x, x, x, torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32))
+
+
+def test_mla_host_checks_and_workspace(lib):
+    fake = ctypes.c_void_p(0x1000)
+    NULL = None
+    args = lambda B, n, H, dc, dr, bs, qdt, ws: (fake, qdt, fake, 1, fake, 64, fake, B, n, H, dc, dr, bs, 100, 0.07,
+                                                 fake, fake, ws, NULL, NULL)
+    assert lib.spec_verify_attn_mla(*args(2, 5, 128, 256, 64, 16, 1, 1 << 30)) == 2   # d_c other than 512
+    assert lib.spec_verify_attn_mla(*args(2, 5, 128, 512, 64, 32, 1, 1 << 30)) == 2   # block size
+    assert lib.spec_verify_attn_mla(*args(2, 5, 128, 512, 64, 16, 0, 1 << 30)) == 2   # f32 queries
+    assert lib.spec_verify_attn_mla(*args(2, 0, 128, 512, 64, 16, 1, 1 << 30)) == 1   # n_new = 0
+    assert lib.spec_verify_attn_mla(*args(1, 8, 16, 512, 64, 16, 1, 16)) == 3         # split context, small workspace
+    assert lib.spec_verify_attn_mla(*args(0, 5, 128, 512, 64, 16, 1, 0)) == 0         # empty batch
+    # splits only when the batch leaves the GPU short of work: partial outputs
+    # of 512 floats and an (m, l) pair per row and split, 256-byte rounded
+    up = lambda x: (x + 255) // 256 * 256
+    assert lib.spec_verify_attn_mla_workspace_size(64, 5, 128, 512) == 0
+    S = 24   # 376 blocks in splits of 16
+    assert lib.spec_verify_attn_mla_workspace_size(1, 8, 16, 376) == up(S * 128 * 512 * 4) + up(S * 128 * 2 * 4)
+    assert lib.kv_block_append_latent(fake, 1, fake, fake, 4, fake, 2, 5, 512, 16, 10, NULL, NULL) == 2
+    assert lib.kv_block_append_latent(fake, 0, fake, fake, 4, fake, 2, 5, 576, 16, 10, NULL, NULL) == 2
