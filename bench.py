@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--mla-only", action="store_true",
+                    help="time only the MLA verify attention (prints its JSON object; for profiling)")
+    ap.add_argument("--mla-batch", type=int, default=64, help="sequences of the --mla-only workload")
     return ap.parse_args()
 
 
@@ -703,7 +706,15 @@ def run_reference(args, rank, world):
 def main():
     args = parse()
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.mla_only:
+        import torch
+        import speculative_verify_paged_gb300 as sv
+        sv.build()
+        sv.load_library()
+        dev = torch.device("cuda:0")
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        print(json.dumps(measure_mla(sv, dev, torch.cuda.current_stream(), status, B=args.mla_batch)))
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

@@ -549,11 +549,13 @@ sv_status sv_copy_blocks(void *const *pools, int n_pools, int64_t block_stride_b
  *   t <= seq_lens[b] - n_new + j, w = softmax(score), and
  *   out[b][j][i][:] = sum_t w_t cache_row(t)[0 .. d_c) (bf16
  *   [B][n_new][H][d_c]). The caller multiplies by W_UV[i] (or folds it into
- *   W_O). softmax_scale: 1 / sqrt(d_head + d_r) in the pages' model.
+ *   W_O). softmax_scale: 1 / sqrt(d_head + d_r) in MLAAttention (section 6.3).
  *   d_c = 512, d_r = 64, block_size = 16, bf16 only (SV_ERR_UNSUPPORTED
  *   otherwise). workspace: spec_verify_attn_mla_workspace_size(...) bytes,
- *   256-byte aligned (the partial outputs of a split context; may be NULL
- *   when that size is 0). Device errors as for spec_verify_attn. Waits for
+ *   256-byte aligned: the partial outputs of a split context (only when the
+ *   batch is too small to fill the GPU) and the longest-first order of the
+ *   sequences (batches of up to 4096). Device errors as for
+ *   spec_verify_attn. Waits for
  *   the previous kernel of the stream before it reads anything.
  * ------------------------------------------------------------------------ */
 sv_status kv_block_append_latent(const void *c_new, sv_dtype dtype, void *cache,

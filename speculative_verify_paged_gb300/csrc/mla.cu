@@ -28,22 +28,31 @@ constexpr int kLR = kLD - kLC;                     // d_r
 constexpr int kLChunks = kLD / 64;                 // 64-wide chunks (one 128-byte swizzle span each)
 constexpr int kLHalf = kLC / 2;                    // output columns per CTA
 constexpr int kLBS = 16;                           // block size
-constexpr int kLN = 32;                            // keys per tile (two blocks)
-constexpr int kLStages = 4;
-constexpr int kLChunkBytes = kLN * 128;            // one chunk of a tile: 32 keys x 64 values
-constexpr int kLTileBytes = kLChunks * kLChunkBytes;
-constexpr int kLQTm = 6;                           // Q chunks held in TMEM
-constexpr int kLQSm = kLChunks - kLQTm;            // Q chunks held in shared memory
-constexpr int kLQChunkBytes = 128 * 128;           // 128 rows x 64 values
+constexpr int kLQChunkBytes = 128 * 128;           // 128 query rows x 64 values
 constexpr int kLThreads = 192;
 constexpr int kLProdWarp = 4;
 constexpr int kLMmaWarp = 5;
-constexpr int kLSmem = 1024 + kLQSm * kLQChunkBytes + kLStages * kLTileBytes;
 constexpr uint32_t kLCols = 512;                   // TMEM columns
-constexpr uint32_t kLOCol = 2 * kLN;               // O after the two S/P buffers
-constexpr uint32_t kLQCol = kLOCol + kLHalf;       // Q: 32 columns (bf16 pairs) per chunk
-static_assert(kLQCol + 32 * kLQTm <= kLCols, "TMEM budget");
-static_assert(kLSmem <= 227 * 1024, "shared memory budget");
+
+// Tile geometry for NK keys per tile. TMEM holds two S/P buffers of NK
+// columns, the 256-column output half and as many Q chunks (32 columns of
+// bf16 pairs each) as fit; the other Q chunks and the ring of NK-key stages
+// share the shared memory.
+template <int NK> struct MlaCfg {
+  static constexpr int kBlk = NK / kLBS;                      // blocks per tile
+  static constexpr int kChunkBytes = NK * 128;                // one 64-wide chunk of a tile
+  static constexpr int kTileBytes = kLChunks * kChunkBytes;
+  static constexpr uint32_t kOCol = 2 * NK;
+  static constexpr uint32_t kQCol = kOCol + kLHalf;
+  static constexpr int kQTm = (int)(kLCols - kQCol) / 32;     // Q chunks in TMEM
+  static constexpr int kQSm = kLChunks - kQTm;                // Q chunks in shared memory
+  static constexpr int kStages = (227 * 1024 - 1024 - 256 - kQSm * kLQChunkBytes) / kTileBytes;
+  static constexpr int kSmem = 1024 + kQSm * kLQChunkBytes + kStages * kTileBytes;
+  static_assert(kQCol + 32 * kQTm <= kLCols, "TMEM budget");
+  static_assert(kStages >= 2, "at least two stages");
+  static_assert(NK % 16 == 0 && NK <= 256, "MMA N");
+};
+constexpr int kLNK = 64;                           // keys per tile of the launched kernel
 constexpr int kLCtaTarget = 2 * 152;               // CTAs that fill the GPU twice over
 constexpr int kLMinBlocksPerSplit = 16;
 
@@ -56,6 +65,7 @@ struct MlaParams {   // 64-byte aligned through its CUtensorMap members
   float *ws_ml;         // [B][S][R][2]   (reference max in log2 units, sum)
   const int32_t *block_table;
   const int32_t *seq_lens;
+  const int32_t *order;   // sequences longest first (NULL: batch order)
   int32_t *status;
   int B, n_new, H, R, n_mt, max_blocks, num_blocks, bps, S, q_box;
   float scale_log2;
@@ -168,9 +178,14 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 // A ring stage is free again once the P V of its tile has run. Both output
 // halves compute the same S: the 128 x 512 fp32 output and an S tile do not
 // fit in one CTA's 512 TMEM columns.
+template <int NK>
 __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_constant__ MlaParams P) {
   pdl_wait();
   pdl_trigger();
+  using Cfg = MlaCfg<NK>;
+  constexpr int kLN = NK, kLStages = Cfg::kStages, kLChunkBytes = Cfg::kChunkBytes, kLTileBytes = Cfg::kTileBytes;
+  constexpr int kLQTm = Cfg::kQTm, kLQSm = Cfg::kQSm, kBlk = Cfg::kBlk;
+  constexpr uint32_t kLOCol = Cfg::kOCol, kLQCol = Cfg::kQCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t kv_full[kLStages], kv_empty[kLStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], q_tm, q_sm, mma_drain;
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
   const int hv = blockIdx.x & 1;
   const int mt = (blockIdx.x >> 1) % P.n_mt;
   const int s = (blockIdx.x >> 1) / P.n_mt;
-  const int b = blockIdx.y;
+  const int b = P.order ? __ldg(P.order + blockIdx.y) : (int)blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t q_smem = smem_u32(smem);
@@ -196,7 +211,7 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
   if (blk0 >= nblk) return;   // the merge never reads this split
   const int blk1 = min(nblk, blk0 + P.bps);
   const int nblocks = blk1 - blk0;
-  const int n_tiles = (nblocks + 1) / 2;
+  const int n_tiles = (nblocks + kBlk - 1) / kBlk;
 
   if (tid == 0) {
     for (int k = 0; k < kLStages; ++k) {
@@ -231,26 +246,27 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
     int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
     int chunk = 0, issued = 0;
     for (int t = 0; t < n_tiles; ++t) {
-      const int first = 2 * t;
+      const int first = kBlk * t;
       if ((first >> 5) != chunk) {
         chunk = first >> 5;
         cur = nxt;
         const int rel = (chunk + 1) * 32 + lane;
         nxt = rel < nblocks ? table[rel] : 0;
       }
-      const int ph0 = __shfl_sync(0xffffffffu, cur, first & 31);
-      const int ph1 = __shfl_sync(0xffffffffu, cur, (first + 1) & 31);
+      int phys[kBlk];
+#pragma unroll
+      for (int kk = 0; kk < kBlk; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
       const int st = t % kLStages;
       bool go = true;
       if (lane == 0) {
         if (t >= kLStages && !ml_wait(&kv_empty[st], ((t / kLStages) & 1) ^ 1, abf)) {
           go = false;
         } else {
-          const int nvalid = min(2, nblocks - first);
+          const int nvalid = min(kBlk, nblocks - first);
           mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(nvalid * kLChunks * 2048));
           const uint32_t base = ring + st * kLTileBytes;
           for (int kk = 0; kk < nvalid; ++kk) {
-            int ph = kk ? ph1 : ph0;
+            int ph = phys[kk];
             if (ph < 0 || ph >= P.num_blocks) {
               atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
               ph = 0;   // stay in bounds; the output of this sequence is flagged
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
               ml_fence_after();
               const uint32_t vb = ring + st * kLTileBytes + 4 * hv * kLChunkBytes;
 #pragma unroll
-              for (int j = 0; j < 2; ++j)
+              for (int j = 0; j < kBlk; ++j)
                 ml_mma_ts(tb + kLOCol, tb + sb * kLN + 8 * j, ml_desc(vb + j * 2048, kLChunkBytes, 1024), idesc_pv,
                           (tp > 0 || j > 0) ? 1u : 0u);
               ml_commit(&kv_empty[st]);
@@ -384,13 +400,14 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
         ok = __all_sync(0xffffffffu, ml_wait(&s_full[sb], (t >> 1) & 1, abf));
         if (!ok) break;
         ml_fence_after();
-        const int key0 = (blk0 + 2 * t) * kLBS;
+        const int key0 = (blk0 + kBlk * t) * kLBS;
         if (warp_live) {
           float x[kLN];
           {
             uint32_t rr[kLN];
-            ml_ld16(lane_base + sb * kLN, *reinterpret_cast<uint32_t(*)[16]>(rr));
-            ml_ld16(lane_base + sb * kLN + 16, *reinterpret_cast<uint32_t(*)[16]>(rr + 16));
+#pragma unroll
+            for (int c0 = 0; c0 < kLN; c0 += 16)
+              ml_ld16(lane_base + sb * kLN + c0, *reinterpret_cast<uint32_t(*)[16]>(rr + c0));
             ml_wait_ld();
 #pragma unroll
             for (int k = 0; k < kLN; ++k) x[k] = __uint_as_float(rr[k]) * sl2;
@@ -429,14 +446,17 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
           l *= a;
           const float base = m_ref == -INFINITY ? 0.f : m_ref;
           float ps = 0.f;
-          uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float p0 = ml_ex2(x[2 * k] - base), p1 = ml_ex2(x[2 * k + 1] - base);
-            ps += p0 + p1;
-            w[k] = ml_pack_bf16(p0, p1);
+          for (int c0 = 0; c0 < kLN; c0 += 32) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float p0 = ml_ex2(x[c0 + 2 * k] - base), p1 = ml_ex2(x[c0 + 2 * k + 1] - base);
+              ps += p0 + p1;
+              w[k] = ml_pack_bf16(p0, p1);
+            }
+            ml_st16(lane_base + sb * kLN + c0 / 2, w);
           }
-          ml_st16(lane_base + sb * kLN, w);
           ml_wait_st();
           l += ps;
         }
@@ -512,6 +532,26 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kLCols));
 }
 
+// Longest-first order of the sequences (ties by batch index): the CTAs of
+// the longest contexts start first, so the last wave holds short ones. Rank
+// of b = number of sequences that come before it; order[rank] = b. It reads
+// only seq_lens (which no kernel of the library writes), so it runs while the
+// previous kernel of the stream finishes, and waits for it at its end.
+constexpr int kLMaxOrder = 4096;
+__global__ void __launch_bounds__(1024) mla_order_kernel(const int32_t *seq_lens, int B, int32_t *order) {
+  pdl_trigger();
+  __shared__ int lens[kLMaxOrder];
+  for (int b = threadIdx.x; b < B; b += blockDim.x) lens[b] = seq_lens[b];
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int L = lens[b];
+    int rank = 0;
+    for (int c = 0; c < B; ++c) rank += (lens[c] > L) || (lens[c] == L && c < b);
+    order[rank] = b;
+  }
+  pdl_wait();
+}
+
 // Merge of the splits of one query row: weights 2^(m_s - M) on the partial
 // sums and normalisers (the log-sum-exp combination of split-KV attention).
 // CTA = (row r, sequence b), 128 threads x 4 values.
@@ -581,19 +621,26 @@ MlaPlan mla_plan(int B, int n_new, int H, int max_blocks) {
   if (per_split < kLCtaTarget)
     S = std::max(1, std::min((kLCtaTarget + per_split - 1) / per_split,
                              (max_blocks + kLMinBlocksPerSplit - 1) / kLMinBlocksPerSplit));
+  constexpr int blk = MlaCfg<kLNK>::kBlk;
   int bps = (max_blocks + S - 1) / S;
-  bps += bps & 1;   // whole 32-key tiles
-  p.bps = std::max(2, bps);
+  bps = (bps + blk - 1) / blk * blk;   // whole tiles
+  p.bps = std::max(blk, bps);
   p.S = (max_blocks + p.bps - 1) / p.bps;
   return p;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-size_t mla_ws_bytes(int B, const MlaPlan &p) {
+// workspace: [partial outputs, (m, l) pairs] of a split context, then the
+// sequence order (batches of at most kLMaxOrder sequences)
+size_t mla_split_bytes(int B, const MlaPlan &p) {
   if (p.S <= 1) return 0;
   const size_t ent = (size_t)B * p.S * p.R;
   return align256(ent * kLC * sizeof(float)) + align256(ent * 2 * sizeof(float));
+}
+
+size_t mla_ws_bytes(int B, const MlaPlan &p) {
+  return mla_split_bytes(B, p) + (B <= kLMaxOrder ? align256((size_t)B * sizeof(int32_t)) : 0);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
@@ -647,9 +694,9 @@ extern "C" sv_status spec_verify_attn_mla(const void *q_lat, sv_dtype q_dtype, c
   if ((int64_t)2 * plan.n_mt * plan.S > 0x7fffffff)
     return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn_mla: grid too large");
   const size_t need = mla_ws_bytes(B, plan);
-  if (need > 0 && (!workspace || workspace_bytes < need))
+  if (!workspace || workspace_bytes < need)
     return fail(SV_ERR_WORKSPACE, "spec_verify_attn_mla: workspace of %zu bytes, %zu needed", workspace_bytes, need);
-  if (need > 0 && !aligned(workspace, 256))
+  if (!aligned(workspace, 256))
     return fail(SV_ERR_WORKSPACE, "spec_verify_attn_mla: workspace must be 256-byte aligned");
 
   PFN_cuTensorMapEncodeTiled_v12000 enc = mla_encode_fn();
@@ -681,9 +728,14 @@ extern "C" sv_status spec_verify_attn_mla(const void *q_lat, sv_dtype q_dtype, c
   P.q = static_cast<const __nv_bfloat16 *>(q_lat);
   P.out = static_cast<__nv_bfloat16 *>(out);
   const size_t ent = (size_t)B * plan.S * plan.R;
-  P.ws_acc = need ? static_cast<float *>(workspace) : nullptr;
-  P.ws_ml = need ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + align256(ent * kLC * sizeof(float)))
-                 : nullptr;
+  const size_t split_bytes = mla_split_bytes(B, plan);
+  P.ws_acc = split_bytes ? static_cast<float *>(workspace) : nullptr;
+  P.ws_ml = split_bytes
+                ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + align256(ent * kLC * sizeof(float)))
+                : nullptr;
+  int32_t *order = B <= kLMaxOrder ? reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + split_bytes)
+                                   : nullptr;
+  P.order = order;
   P.block_table = block_table;
   P.seq_lens = seq_lens;
   P.status = dev_status;
@@ -694,12 +746,19 @@ extern "C" sv_status spec_verify_attn_mla(const void *q_lat, sv_dtype q_dtype, c
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmem);
+    attr_err = cudaFuncSetAttribute(attn_mla_kernel<kLNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    MlaCfg<kLNK>::kSmem);
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn_mla: kernel attributes: %s", cudaGetErrorString(attr_err));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_k(attn_mla_kernel, dim3(2 * plan.n_mt * plan.S, B), dim3(kLThreads), (size_t)kLSmem, st, 1, P);
+  cudaError_t e;
+  if (order) {
+    e = launch_k(mla_order_kernel, dim3(1), dim3(1024), 0, st, 1, seq_lens, B, order);
+    if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_attn_mla order launch: %s", cudaGetErrorString(e));
+  }
+  e = launch_k(attn_mla_kernel<kLNK>, dim3(2 * plan.n_mt * plan.S, B), dim3(kLThreads),
+                           (size_t)MlaCfg<kLNK>::kSmem, st, 1, P);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_attn_mla launch: %s", cudaGetErrorString(e));
   if (plan.S > 1) {
     e = launch_k(attn_mla_merge_kernel, dim3(plan.R, B), dim3(128), 0, st, 1, (const float *)P.ws_acc,

@@ -173,12 +173,15 @@ def test_mla_host_checks_and_workspace(lib):
     assert lib.spec_verify_attn_mla(*args(2, 5, 128, 512, 64, 16, 0, 1 << 30)) == 2   # f32 queries
     assert lib.spec_verify_attn_mla(*args(2, 0, 128, 512, 64, 16, 1, 1 << 30)) == 1   # n_new = 0
     assert lib.spec_verify_attn_mla(*args(1, 8, 16, 512, 64, 16, 1, 16)) == 3         # split context, small workspace
+    assert lib.spec_verify_attn_mla(*args(2, 5, 128, 512, 64, 16, 1, 0)) == 3         # no room for the order
     assert lib.spec_verify_attn_mla(*args(0, 5, 128, 512, 64, 16, 1, 0)) == 0         # empty batch
     # splits only when the batch leaves the GPU short of work: partial outputs
-    # of 512 floats and an (m, l) pair per row and split, 256-byte rounded
+    # of 512 floats and an (m, l) pair per row and split, 256-byte rounded,
+    # then the longest-first order of the sequences (up to 4096 of them)
     up = lambda x: (x + 255) // 256 * 256
-    assert lib.spec_verify_attn_mla_workspace_size(64, 5, 128, 512) == 0
+    assert lib.spec_verify_attn_mla_workspace_size(64, 5, 128, 512) == 256
+    assert lib.spec_verify_attn_mla_workspace_size(5000, 5, 128, 512) == 0
     S = 24   # 376 blocks in splits of 16
-    assert lib.spec_verify_attn_mla_workspace_size(1, 8, 16, 376) == up(S * 128 * 512 * 4) + up(S * 128 * 2 * 4)
+    assert lib.spec_verify_attn_mla_workspace_size(1, 8, 16, 376) == up(S * 128 * 512 * 4) + up(S * 128 * 2 * 4) + 256
     assert lib.kv_block_append_latent(fake, 1, fake, fake, 4, fake, 2, 5, 512, 16, 10, NULL, NULL) == 2
     assert lib.kv_block_append_latent(fake, 0, fake, fake, 4, fake, 2, 5, 576, 16, 10, NULL, NULL) == 2
