@@ -104,3 +104,35 @@ def test_mla_bad_inputs_are_flagged(sv):
     assert st & 2 and st & 1           # SV_DEV_BAD_BLOCK | SV_DEV_BAD_SEQ_LEN
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify_attn_mla(q.to(DEV), cache.to(DEV), table.to(DEV), L.to(DEV), SCALE, d_c=256)
+
+
+def test_mla_full_size_sampled_sequences(sv):
+    # the bench's DeepSeek-V2 shape, inputs and launch (64 sequences of
+    # 1024-8192 tokens, 128 heads, no splits, longest-first order); the oracle
+    # checks the shortest, the longest and a middle sequence
+    B, n_new, H = 64, 5, 128
+    g = torch.Generator(device="cpu").manual_seed(0)
+    lens = torch.randint(1024, 8193, (B,), generator=g).tolist()
+    nblk = [(L + BS - 1) // BS for L in lens]
+    nb = sum(nblk) + 8
+    perm = torch.randperm(nb, generator=g).to(torch.int32)
+    table = torch.full((B, max(nblk)), -1, dtype=torch.int32)
+    off = 0
+    for b, k in enumerate(nblk):
+        table[b, :k] = perm[off:off + k]
+        off += k
+    gd = torch.Generator(device=DEV).manual_seed(0)
+    cache = torch.randn((nb, BS, D), generator=gd, device=DEV).to(torch.bfloat16)
+    q = torch.randn((B, n_new, H, D), generator=gd, device=DEV).to(torch.bfloat16)
+    assert sv.mla_workspace_size(B, n_new, H, table.shape[1]) == 256   # one split per sequence
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = sv.spec_verify_attn_mla(q, cache, table.to(DEV), torch.tensor(lens, dtype=torch.int32, device=DEV),
+                                  SCALE, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    order = np.argsort(lens)
+    for b in (int(order[0]), int(order[-1]), int(order[B // 2])):
+        rows = cache[table[b, :nblk[b]].long().to(DEV)].reshape(-1, D)[: lens[b]].cpu()
+        ref = omla.latent_attention(q[b].cpu(), rows, SCALE, DC)
+        err = np.abs(out[b].float().cpu().numpy() - ref).max()
+        assert err <= 2e-2, (b, lens[b], err)
