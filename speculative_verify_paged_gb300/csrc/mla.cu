@@ -164,16 +164,18 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// CTA = (output half hv, row tile mt, split s) x sequence b; 192 threads:
+// CTA = (output half hv, row tile mt, split s) x sequence b; 192 threads.
+// The numbers below are for the launched NK = 64 (two stages; Q chunks 0-3
+// in TMEM, 4-8 in shared memory).
 //   warps 0-3  softmax: thread t owns query row 128 mt + t (TMEM lane t);
-//              they first write Q chunks 0-5 of their rows into TMEM
-//   warp 4     TMA producer: Q chunks 6-8 of the row tile, then the ring of
-//              32-key tiles (every chunk of every row: keys and values are
-//              the same cached rows)
+//              they first write their rows' TMEM chunks of Q
+//   warp 4     TMA producer: the shared-memory chunks of Q for the row tile,
+//              then the ring of NK-key tiles (every chunk of every row: keys
+//              and values are the same cached rows)
 //   warp 5     TMEM owner; lane 0 issues the MMAs from a polling loop
 // Per tile t, buffer u = t % 2:
-//   S[u] = Q K^T        M=128 rows, N=32 keys, K=576 (36 MMAs of K=16)
-//   P[u] = 2^(S c - m)  bf16 over the first 16 columns of S[u]
+//   S[u] = Q K^T        M=128 rows, N=NK keys, K=576 (36 MMAs of K=16)
+//   P[u] = 2^(S c - m)  bf16 over the first NK/2 columns of S[u]
 //   O   += P V          M=128, N=256 values of half hv, K=16 keys per MMA
 // A ring stage is free again once the P V of its tile has run. Both output
 // halves compute the same S: the 128 x 512 fp32 output and an S tile do not
