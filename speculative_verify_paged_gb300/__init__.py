@@ -294,6 +294,8 @@ def kv_block_append_latent(c_new, cache, block_table, seq_lens, block_size=16, s
     seq_lens - n_new .. seq_lens - 1 of the pool cache [num_blocks, bs, d_c + d_r]."""
     lib = load_library()
     _cuda(c_new, cache, block_table, seq_lens, status)
+    if cache.dtype != c_new.dtype:
+        raise ValueError("the latent pool and the new rows must have the same dtype (bf16)")
     B, n_new, D = c_new.shape
     _check(lib.kv_block_append_latent(_ptr(c_new), _dtype_code(c_new), _ptr(cache), _ptr(block_table),
                                       block_table.shape[1], _ptr(seq_lens), B, n_new, D, block_size,
@@ -311,6 +313,8 @@ def spec_verify_attn_mla(q_lat, cache, block_table, seq_lens, softmax_scale, d_c
     outputs [B, n_new, H, d_c] (bf16), to be multiplied by each head's W_UV."""
     lib = load_library()
     _cuda(q_lat, cache, block_table, seq_lens, out, workspace, status)
+    if out is not None and (out.dtype != q_lat.dtype or out.shape != q_lat.shape[:3] + (d_c,)):
+        raise ValueError("out must be [B, n_new, H, d_c] in the queries' dtype")
     B, n_new, H, D = q_lat.shape
     if out is None:
         out = torch.empty((B, n_new, H, d_c), dtype=q_lat.dtype, device=q_lat.device)
