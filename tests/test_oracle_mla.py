@@ -10,8 +10,10 @@
 - causality: rows after a query's position do not move it, its own row does;
 - RoPE: shifting every position by the same offset leaves the output unchanged
   (R_t^T R_s depends on s - t only), and the rotation keeps norms;
-- the pages' cache figures: 1152 bytes per token and layer, ~0.27 GB for
-  60 layers x 4096 tokens in fp16;
+- the pages' cache figures (tests/golden/pages_numbers.json): 1152 bytes per
+  token and layer, ~0.27 GB for 60 layers x 4096 tokens in fp16, ~57x / 64x
+  against 128-head MHA, ~1/3.5 of the 70B GQA cache and ~1/28 of same-scale
+  MHA;
 - the latent append writes the right slots and nothing else.
 """
 import math
@@ -163,3 +165,19 @@ def test_latent_append_slots():
         for s in range(bs):
             if (blk, s) not in touched:
                 assert np.array_equal(out[blk, s], pool[blk, s])
+
+
+def test_golden_mla_cache_numbers():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_numbers.json")))["mla_cache"]
+    per_tok, sample, ratios, vs = g
+    assert mla.cache_bytes(1, 1, per_tok["d_c"], per_tok["d_r"], per_tok["bytes"]) == per_tok["printed_bytes_per_token_layer"]
+    gib = mla.cache_bytes(sample["n_layers"], sample["L"], sample["d_c"], sample["d_r"], sample["bytes"]) / 2 ** 30
+    assert abs(gib - sample["printed_gib_approx"]) < 0.01
+    mha = 2 * ratios["H"] * ratios["d_head"]
+    assert round(mha / (ratios["d_c"] + ratios["d_r"])) == ratios["printed_ratio_full"]
+    assert round(mha / ratios["d_c"]) == ratios["printed_ratio_latent_only"]
+    assert vs["mla_elems"] == mla.cache_bytes(1, 1, 512, 64, 1)
+    assert abs(vs["gqa_elems"] / vs["mla_elems"] - vs["printed_gqa_ratio"]) < 0.1   # 3.56, printed as about 3.5
+    assert round(vs["mha_elems"] / vs["mla_elems"]) == vs["printed_mha_ratio"]
