@@ -570,12 +570,34 @@ def measure_mla(sv, dev, stream, status, reps=10, B=64, n_new=5, H=128, ctx=(102
     nbytes = sum(lens) * 1152 + q.numel() * 2 + out.numel() * 2
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         tpeak = float(json.load(f)["bf16_tflops"])
+    cpu = mla_oracle_time(q, cache, table, lens, nblk, scale)
     return {"workload": "DeepSeek-V2 MLA layer shape: B=%d, H=%d, d_c=512, d_r=64, K=%d, ctx uniform [%d, %d], "
                         "block_size 16, bf16" % (B, H, n_new - 1, ctx[0], ctx[1]),
-            "us": us, "flops": flops, "bytes": nbytes,
+            "us": us, "flops": flops, "bytes": nbytes, "cpu_baseline": cpu,
             "roofline": {"bound": "tensor", "kernel": "attn_mla_kernel", "achieved": flops / (us * 1e-6) / 1e12,
                          "peak": tpeak, "unit": "TFLOP/s", "frac": flops / (us * 1e-6) / 1e12 / tpeak,
                          "hbm_gbs": nbytes / (us * 1e-6) / 1e9}}
+
+
+def mla_oracle_time(q, cache, table, lens, nblk, scale):
+    """The fp64 oracle on the host cores for the sequence of median length,
+    scaled to the whole batch by visible keys (its work is linear in them)."""
+    import numpy as np
+    import torch
+
+    from oracle import mla as omla
+    b = int(np.argsort(lens)[len(lens) // 2])
+    rows = cache[table[b, :nblk[b]].long()].reshape(-1, cache.shape[-1])[: lens[b]].cpu()
+    qb = q[b].cpu()
+    n_new = q.shape[1]
+    t0 = time.perf_counter()
+    omla.latent_attention(qb, rows, scale, 512)
+    dt = time.perf_counter() - t0
+    keys = lambda L: sum(L - n_new + j + 1 for j in range(n_new))
+    full = dt * sum(keys(L) for L in lens) / keys(lens[b])
+    return {"value": full * 1e6, "unit": "us per call", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "oracle.mla.latent_attention (numpy fp64) on sequence %d (%d tokens), %.2f s, scaled to all "
+                      "%d sequences by visible keys" % (b, lens[b], dt, len(lens))}
 
 
 def measure_multi_layer(sv, cfg, a, n, s, dev, stream, status, n_layers=8, reps=5):
