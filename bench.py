@@ -2,7 +2,7 @@
 fused rejection sampling) on the LLaMA-3-70B layer-shaped workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3_70b] [--sigma 1.5]
+                    [--workload llama3_70b] [--sigma 1.5] [--no-configs]
 
 Prints ONE JSON line on rank 0. `value` is verify steps/s of the whole job
 (inputs resident in HBM); `e2e` is the same metric through the public API with
@@ -10,7 +10,12 @@ every step's inputs copied from pinned host memory and its outputs read back
 inside the timed region (two device copies of the inputs: a step's copy, on
 its own stream, overlaps the previous step's compute). The reference arm (`--impl reference`) times the CPU
 oracle on a bounded sample of the same workload and scales it to steps/s.
-Multi-GPU runs are independent replicas (one batch per GPU, no collective).
+`configs` holds one object per other workload of the verify step (the
+LLaMA-3-8B layer, the 128K-token context, the fp8 cache with fp32 logits, and
+the 70B layer at the other draft-noise levels of its sweep), each timed the
+same way with its own attention and sampling rooflines and oracle baseline.
+Multi-GPU runs are independent replicas (one batch per GPU, no collective);
+--gpus must equal the number of ranks the launcher started.
 """
 import argparse
 import hashlib
@@ -45,7 +50,34 @@ def parse():
     ap.add_argument("--mla-only", action="store_true",
                     help="time only the MLA verify attention (prints its JSON object; for profiling)")
     ap.add_argument("--mla-batch", type=int, default=64, help="sequences of the --mla-only workload")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' objects")
+    ap.add_argument("--config-steps", type=int, default=40, help="timed steps per object of `configs`")
     return ap.parse_args()
+
+
+def check_world(args, world):
+    """--gpus N is the number of ranks the launcher started (torchrun for N > 1):
+    a disagreement would print a line for a job that did not run."""
+    if args.gpus != world:
+        raise SystemExit("bench.py: --gpus %d but WORLD_SIZE is %d; for N > 1 launch one rank per GPU with "
+                         "python -m torch.distributed.run --nproc-per-node N bench.py --gpus N" % (args.gpus, world))
+
+
+def pct(xs, q):
+    """q-th percentile (0..100) of a list, linear interpolation."""
+    ys = sorted(xs)
+    if not ys:
+        return None
+    k = (len(ys) - 1) * q / 100.0
+    lo = int(math.floor(k))
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (k - lo)
+
+
+def dist_summary(xs_ms):
+    """median, p10 and p90 of per-step event times, in microseconds."""
+    us = [1e3 * x for x in xs_ms]
+    return {"median_us": pct(us, 50), "p10_us": pct(us, 10), "p90_us": pct(us, 90)}
 
 
 def dist_env():
@@ -229,6 +261,124 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm -----
 
+class StepSetup:
+    """Inputs, outputs and workspaces of one verify step (append, attention,
+    sampling) of a workload on the device, and the step itself."""
+
+    def __init__(self, sv, cfg, sigma, seed, dev, stream):
+        import torch
+
+        import workloads
+        self.sv, self.cfg, self.stream = sv, cfg, stream
+        a = self.a = workloads.make_attention_inputs(cfg, seed=seed, device=dev)
+        self.n = workloads.make_append_inputs(cfg, seed=seed, device=dev)
+        self.s = workloads.make_sampling_inputs(cfg, seed=seed, device=dev, sigma=sigma)
+        self.lens = a["seq_lens"].tolist()
+        self.attn_bytes = workloads.attention_bytes(cfg, self.lens)
+        self.samp_bytes = workloads.sampling_bytes(cfg)
+        self.app_bytes = workloads.append_bytes(cfg)
+        self.step_bytes = self.attn_bytes + self.samp_bytes + self.app_bytes
+        self.k_cache, self.v_cache = a["k_cache"], a["v_cache"]
+        self.out = torch.empty_like(a["q"])
+        self.attn_ws = sv.alloc_workspace(sv.attn_workspace_size(cfg.B, cfg.n_new, cfg.H_q, cfg.H_kv, cfg.d_head,
+                                                                 a["block_table"].shape[1]), dev)
+        self.samp_ws = sv.alloc_workspace(sv.sample_workspace_size(cfg.B, cfg.K, cfg.V), dev)
+        self.toks = torch.empty((cfg.B, cfg.K + 1), dtype=torch.int32, device=dev)
+        self.nacc = torch.empty((cfg.B,), dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(self, ev=None):
+        sv, a, n, s, stream = self.sv, self.a, self.n, self.s, self.stream
+        if ev is not None:
+            ev[0].record(stream)
+        sv.kv_block_append(n["k_new"], n["v_new"], self.k_cache, self.v_cache, a["block_table"], a["seq_lens"],
+                           a["k_scale"], a["v_scale"], status=self.status)
+        if ev is not None:
+            ev[1].record(stream)
+        sv.spec_verify_attn(a["q"], self.k_cache, self.v_cache, a["block_table"], a["seq_lens"], None,
+                            a["k_scale"], a["v_scale"], out=self.out, workspace=self.attn_ws, status=self.status)
+        if ev is not None:
+            ev[2].record(stream)
+        sv.spec_verify_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"],
+                              out_tokens=self.toks, num_accepted=self.nacc, workspace=self.samp_ws,
+                              status=self.status, want_probs=False)
+        if ev is not None:
+            ev[3].record(stream)
+
+
+def other_configs(headline, sigma):
+    """The workloads of the verify step other than the headline line's: every
+    other configuration, and the 70B layer at the sweep's other noise levels."""
+    import workloads
+    out = [(name, workloads.CONFIGS[name].sigma) for name in ("llama3_8b", "long", "fp8") if name != headline]
+    if headline == "llama3_70b":
+        out += [("llama3_70b", sg) for sg in workloads.SIGMA_SWEEP_70B if sg != sigma]
+    else:
+        out += [("llama3_70b", sg) for sg in workloads.SIGMA_SWEEP_70B]
+    return out
+
+
+def measure_config(sv, cfg, sigma, seed, dev, stream, steps, warmup=5, cpu=True):
+    """One object of `configs`: the verify step of this workload timed like the
+    headline (per-op CUDA events on the launching stream over `steps` steps,
+    each step's working set above twice the L2), with the median, p10 and
+    p90 of each op, the attention and sampling rooflines, and the oracle on a
+    bounded sample of the same inputs."""
+    import torch
+
+    import workloads
+    st = StepSetup(sv, cfg, sigma, seed, dev, stream)
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0, "device status %d (%s)" % (int(st.status.item()), cfg.name)
+    emitted = int((st.nacc.long() + 1).sum().item())
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        st.step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    total_ms = t0.elapsed_time(t1)
+    app = [e[0].elapsed_time(e[1]) for e in evs]
+    att = [e[1].elapsed_time(e[2]) for e in evs]
+    smp = [e[2].elapsed_time(e[3]) for e in evs]
+    peak, peak_kind = measured_peaks()
+    a_us, s_us = 1e3 * pct(att, 50), 1e3 * pct(smp, 50)
+    a_gbs, s_gbs = st.attn_bytes / (a_us * 1e-6) / 1e9, st.samp_bytes / (s_us * 1e-6) / 1e9
+    res = {"workload": workload_config(cfg, sigma, st.lens, 1, st.step_bytes)["workload"],
+           "sigma": sigma, "steps": steps, "stat": "median of per-step CUDA events",
+           "steps_per_sec": steps / (total_ms / 1e3), "ms_per_step": total_ms / steps,
+           "tokens_per_sec": emitted * steps / (total_ms / 1e3), "emitted_tokens_per_step": emitted,
+           "append": dist_summary(app), "attn": dist_summary(att), "sample": dist_summary(smp),
+           "step": dist_summary([x + y + z for x, y, z in zip(app, att, smp)]),
+           "bytes": {"attn": st.attn_bytes, "sample": st.samp_bytes, "append": st.app_bytes},
+           "roofline_attn": {"bound": "hbm", "kernel": "spec_verify_attn", "achieved": a_gbs, "peak": peak,
+                             "peak_kind": peak_kind, "unit": "GB/s", "frac": a_gbs / peak,
+                             "frac_of_8tbs": a_gbs / NOMINAL_HBM_GBS},
+           "roofline_sample": {"bound": "hbm", "kernel": "spec_verify_sample", "achieved": s_gbs, "peak": peak,
+                               "peak_kind": peak_kind, "unit": "GB/s", "frac": s_gbs / peak,
+                               "frac_of_8tbs": s_gbs / NOMINAL_HBM_GBS},
+           "l2": "inputs larger than twice the L2 (%.2f GB touched per step)" % (st.step_bytes / 1e9)}
+    if cpu:
+        res["cpu_baseline"] = cpu_baseline_bounded(cfg, st.a, st.n, st.s)
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_bounded(cfg, a, n, s, budget_s=6.0):
+    """The oracle on the first sequences of the workload, sized from a
+    one-sequence probe to about budget_s seconds, scaled to the full step."""
+    _, t_one, _ = oracle_sample_time(cfg, a, n, s, 1, 1)
+    k = max(1, min(cfg.B, int(budget_s / max(t_one, 1e-3))))
+    full, spent, desc = oracle_sample_time(cfg, a, n, s, k, k) if k > 1 else oracle_sample_time(cfg, a, n, s, 1, 1)
+    return {"value": 1.0 / full, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": desc + "; %.1f s of CPU work; numpy fp64 (BLAS threads = cores)" % spent}
+
 def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -236,6 +386,7 @@ def run_ours(args, rank, world, local):
     import speculative_verify_paged_gb300 as sv
     import workloads
 
+    check_world(args, world)
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -244,41 +395,14 @@ def run_ours(args, rank, world, local):
     cfg = workloads.CONFIGS[args.workload]
     sigma = cfg.sigma if args.sigma is None else args.sigma
     seed = rank_seed(args.seed, rank)
-    a = workloads.make_attention_inputs(cfg, seed=seed, device=dev)
-    n = workloads.make_append_inputs(cfg, seed=seed, device=dev)
-    s = workloads.make_sampling_inputs(cfg, seed=seed, device=dev, sigma=sigma)
-    lens = a["seq_lens"].tolist()
-    attn_bytes = workloads.attention_bytes(cfg, lens)
-    samp_bytes = workloads.sampling_bytes(cfg)
-    app_bytes = workloads.append_bytes(cfg)
-    step_bytes = attn_bytes + samp_bytes + app_bytes
-
-    k_cache, v_cache = a["k_cache"], a["v_cache"]
-    out = torch.empty_like(a["q"])
-    attn_ws = sv.alloc_workspace(sv.attn_workspace_size(cfg.B, cfg.n_new, cfg.H_q, cfg.H_kv, cfg.d_head,
-                                                        a["block_table"].shape[1]), dev)
-    samp_ws = sv.alloc_workspace(sv.sample_workspace_size(cfg.B, cfg.K, cfg.V), dev)
-    toks = torch.empty((cfg.B, cfg.K + 1), dtype=torch.int32, device=dev)
-    nacc = torch.empty((cfg.B,), dtype=torch.int32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        sv.kv_block_append(n["k_new"], n["v_new"], k_cache, v_cache, a["block_table"], a["seq_lens"],
-                           a["k_scale"], a["v_scale"], status=status)
-        if ev is not None:
-            ev[1].record(stream)
-        sv.spec_verify_attn(a["q"], k_cache, v_cache, a["block_table"], a["seq_lens"], None,
-                            a["k_scale"], a["v_scale"], out=out, workspace=attn_ws, status=status)
-        if ev is not None:
-            ev[2].record(stream)
-        sv.spec_verify_sample(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"],
-                              out_tokens=toks, num_accepted=nacc, workspace=samp_ws, status=status,
-                              want_probs=False)
-        if ev is not None:
-            ev[3].record(stream)
+    st = StepSetup(sv, cfg, sigma, seed, dev, stream)
+    a, n, s = st.a, st.n, st.s
+    lens, attn_bytes, samp_bytes, app_bytes, step_bytes = st.lens, st.attn_bytes, st.samp_bytes, st.app_bytes, \
+        st.step_bytes
+    k_cache, v_cache, out, attn_ws, samp_ws = st.k_cache, st.v_cache, st.out, st.attn_ws, st.samp_ws
+    toks, nacc, status = st.toks, st.nacc, st.status
+    step = st.step
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -367,10 +491,16 @@ def run_ours(args, rank, world, local):
     assert int(status.item()) == 0
 
     nxt = None
+    others = None
     if rank == 0:
         nxt = measure_next_rows(sv, cfg, a, s, dev, stream, status)
         nxt["mla"] = measure_mla(sv, dev, stream, status)
         nxt["multi_layer"] = measure_multi_layer(sv, cfg, a, n, s, dev, stream, status)
+        if not args.no_configs:
+            others = []
+            for name, sg in other_configs(args.workload, sigma):
+                others.append(measure_config(sv, workloads.CONFIGS[name], sg, seed, dev, stream,
+                                             args.config_steps, cpu=not args.no_cpu_baseline))
 
     if rank != 0:
         if world > 1:
@@ -378,9 +508,10 @@ def run_ours(args, rank, world, local):
         return
     ms_step = total_ms / args.steps
     value = job_steps_per_sec(args.steps, world, total_ms)
-    attn_us = 1e3 * statistics.mean(attn_ms)
-    samp_us = 1e3 * statistics.mean(samp_ms)
-    app_us = 1e3 * statistics.mean(app_ms)
+    # per-op times: medians of the per-step events (p10 / p90 beside them)
+    attn_us = 1e3 * pct(attn_ms, 50)
+    samp_us = 1e3 * pct(samp_ms, 50)
+    app_us = 1e3 * pct(app_ms, 50)
     peak, peak_kind = measured_peaks()
     attn_gbs = attn_bytes / (attn_us * 1e-6) / 1e9
     samp_gbs = samp_bytes / (samp_us * 1e-6) / 1e9
@@ -392,7 +523,10 @@ def run_ours(args, rank, world, local):
         "tokens_per_sec": world * emitted_per_step * args.steps / (total_ms / 1e3),
         "hbm_gbs_step": step_bytes / (ms_step * 1e-3) / 1e9,
         "frac_of_8tbs_step": step_bytes / (ms_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
-        "ops": {"append_us": app_us, "attn_us": attn_us, "sample_us": samp_us,
+        "ops": {"stat": "median of per-step CUDA events", "append_us": app_us, "attn_us": attn_us,
+                "sample_us": samp_us, "append": dist_summary(app_ms), "attn": dist_summary(attn_ms),
+                "sample": dist_summary(samp_ms),
+                "step": dist_summary([x + y + z for x, y, z in zip(app_ms, attn_ms, samp_ms)]),
                 "attn_bytes": attn_bytes, "sample_bytes": samp_bytes, "append_bytes": app_bytes,
                 "attn_gbs": attn_gbs, "sample_gbs": samp_gbs,
                 "attn_frac_of_8tbs": attn_gbs / NOMINAL_HBM_GBS, "sample_frac_of_8tbs": samp_gbs / NOMINAL_HBM_GBS,
@@ -407,6 +541,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": timed_launches,
         "clocks": clk,
         "next": nxt,
+        "configs": others,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, a, n, s, sigma)
@@ -685,6 +820,7 @@ def cpu_baseline(cfg, a, n, s, sigma, min_seconds=10.0, max_reps=5):
 
 
 def run_reference(args, rank, world):
+    check_world(args, world)
     if rank != 0:
         return
     import torch

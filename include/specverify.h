@@ -410,6 +410,9 @@ sv_status spec_verify_sample_tree(const void *target_logits, sv_dtype logit_dtyp
  *   Allocates nothing (no cudaMalloc / cudaFree or allocating library call).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
+ *   The address is kept per device together with the id of the context it
+ *   was found in; a call in a new context of the device (after the old one
+ *   was destroyed, e.g. by cudaDeviceReset) looks it up again.
  *   Every call on a device shares the one array and leaves its contents
  *   behind; no call needs it zeroed. Calls that overlap on the GPU (other
  *   streams, other host threads) race on the array: serialise them.

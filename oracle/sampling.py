@@ -236,10 +236,14 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
     accepted the token is drawn from p_u itself.
 
     Returns dict: out_tokens [B, n] (accepted tokens, the drawn one, then -1),
-    num_accepted [B], path_nodes [B, n] (accepted nodes, then -1) and
+    num_accepted [B], path_nodes [B, n] (accepted nodes, then -1),
     margin [B] (the smallest distance of a decision taken from its
     boundary: |u - r/q| of every accept test, or |p(x) - tau| / tau of every
-    typical test, and the CDF margin of the draw).
+    typical test, and the CDF margin of the draw) and decisions [B]: the
+    walk's decisions in the order taken, each a tuple (node u, child c,
+    margin, outcome): an accept (or typical) test of child c at u with
+    outcome True / False, and last the draw at u with c = -1 and the drawn
+    token as its outcome.
     """
     p_all = softmax(target_logits, temperature)
     q_all = _np64(draft) if draft_is_probs else softmax(draft, temperature)
@@ -251,6 +255,7 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
     path = np.full((B, n), -1, dtype=np.int64)
     nacc = np.zeros(B, dtype=np.int64)
     margin = np.full(B, np.inf)
+    decisions = [[] for _ in range(B)]
     for b in range(B):
         u, depth = 0, 0
         while True:
@@ -261,7 +266,9 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
                 tau = min(typical[0], typical[1] * np.exp(-entropy(r)))
                 for c in [c for c in range(1, n) if par[b, c] == u]:
                     x = tok[b, c]
-                    margin[b] = min(margin[b], abs(r[x] - tau) / tau)
+                    mt = abs(r[x] - tau) / tau
+                    margin[b] = min(margin[b], mt)
+                    decisions[b].append((u, c, mt, bool(r[x] > tau)))
                     if r[x] > tau:
                         accepted = c
                         break
@@ -274,6 +281,7 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
                 y, m, _ = inverse_cdf(r[None, :], np.array([uv[b, u, 1]]))
                 out[b, depth] = y[0]
                 margin[b] = min(margin[b], m[0])
+                decisions[b].append((u, -1, float(m[0]), int(y[0])))
                 nacc[b] = depth
                 break
             for c in [c for c in range(1, n) if par[b, c] == u]:
@@ -281,6 +289,7 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
                 accept = uv[b, c, 0] * q[x] < r[x]
                 ratio = r[x] / q[x] if q[x] > 0 else np.inf
                 margin[b] = min(margin[b], abs(uv[b, c, 0] - ratio))
+                decisions[b].append((u, c, float(abs(uv[b, c, 0] - ratio)), bool(accept)))
                 if accept:
                     accepted = c
                     break
@@ -296,6 +305,8 @@ def tree_rejection_sample(target_logits, draft, tree_parent, tree_tokens, unifor
             y, m, _ = inverse_cdf(r[None, :], np.array([uv[b, u, 1]]))
             out[b, depth] = y[0]
             margin[b] = min(margin[b], m[0])
+            decisions[b].append((u, -1, float(m[0]), int(y[0])))
             nacc[b] = depth
             break
-    return {"out_tokens": out, "num_accepted": nacc, "path_nodes": path, "margin": margin}
+    return {"out_tokens": out, "num_accepted": nacc, "path_nodes": path, "margin": margin,
+            "decisions": decisions}

@@ -185,6 +185,27 @@ def _cuda(*ts):
             raise ValueError("tensor arguments must be contiguous")
 
 
+def _int32(**ts):
+    for name, t in ts.items():
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError("%s must be int32, not %s" % (name, t.dtype))
+
+
+def _check_latent_pool(cache, d_total, block_size, what):
+    """The latent kernels index a pool [num_blocks, block_size, d_total] (d_total =
+    d_c + d_r values per token, no head axis); any other shape would send their
+    TMA boxes and stores past the allocation."""
+    if cache.dim() != 3:
+        raise ValueError("%s: the latent pool must be [num_blocks, block_size, d_c + d_r], got %d dims"
+                         % (what, cache.dim()))
+    if cache.shape[1] != block_size:
+        raise ValueError("%s: the latent pool holds %d slots per block, block_size is %d"
+                         % (what, cache.shape[1], block_size))
+    if cache.shape[2] != d_total:
+        raise ValueError("%s: the latent pool rows hold %d values, the queries / new rows %d"
+                         % (what, cache.shape[2], d_total))
+
+
 def _layout_arg(layout):
     if layout is None:
         return None
@@ -196,6 +217,7 @@ def _layout_arg(layout):
 def kv_block_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_scale=None,
                     v_scale=None, block_size=16, layout=None, status=None):
     """Write k_new/v_new [B, n_new, H_kv, d] at positions seq_lens-n_new .. seq_lens-1."""
+    _int32(block_table=block_table, seq_lens=seq_lens)
     lib = load_library()
     _cuda(k_new, v_new, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, status)
     B, n_new, H_kv, d = k_new.shape
@@ -211,6 +233,7 @@ def kv_tree_commit(k_cache, v_cache, block_table, seq_lens, path_nodes, num_acce
                    layout=None, num_blocks=None, H_kv=None, status=None):
     """Move each sequence's accepted tree path (path_nodes [B, n_new], num_accepted [B])
     next to the root in the paged pools; pools [num_blocks, H_kv, bs, d] unless layout."""
+    _int32(block_table=block_table, seq_lens=seq_lens, path_nodes=path_nodes, num_accepted=num_accepted)
     lib = load_library()
     _cuda(k_cache, v_cache, block_table, seq_lens, path_nodes, num_accepted, status)
     B, n_new = path_nodes.shape
@@ -250,6 +273,7 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=N
     element is (block 0, head 0, slot 0) plus explicit num_blocks and H_kv.
     tree_parent (int32 [B, n_new], optional): the new positions are a draft tree in BFS
     order and each query sees only its ancestors among them."""
+    _int32(block_table=block_table, seq_lens=seq_lens, tree_parent=tree_parent)
     lib = load_library()
     _cuda(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, out, workspace, status,
           tree_parent)
@@ -292,10 +316,14 @@ def spec_verify_attn(q, k_cache, v_cache, block_table, seq_lens, softmax_scale=N
 def kv_block_append_latent(c_new, cache, block_table, seq_lens, block_size=16, status=None):
     """Write latent rows c_new [B, n_new, d_c + d_r] (bf16) at positions
     seq_lens - n_new .. seq_lens - 1 of the pool cache [num_blocks, bs, d_c + d_r]."""
-    lib = load_library()
-    _cuda(c_new, cache, block_table, seq_lens, status)
+    if c_new.dim() != 3:
+        raise ValueError("kv_block_append_latent: c_new must be [B, n_new, d_c + d_r]")
+    _check_latent_pool(cache, c_new.shape[-1], block_size, "kv_block_append_latent")
+    _int32(block_table=block_table, seq_lens=seq_lens)
     if cache.dtype != c_new.dtype:
         raise ValueError("the latent pool and the new rows must have the same dtype (bf16)")
+    lib = load_library()
+    _cuda(c_new, cache, block_table, seq_lens, status)
     B, n_new, D = c_new.shape
     _check(lib.kv_block_append_latent(_ptr(c_new), _dtype_code(c_new), _ptr(cache), _ptr(block_table),
                                       block_table.shape[1], _ptr(seq_lens), B, n_new, D, block_size,
@@ -311,10 +339,14 @@ def spec_verify_attn_mla(q_lat, cache, block_table, seq_lens, softmax_scale, d_c
     """Absorbed MLA verify attention: q_lat [B, n_new, H, d_c + d_r] bf16 against
     the latent pool cache [num_blocks, bs, d_c + d_r] bf16; returns the latent
     outputs [B, n_new, H, d_c] (bf16), to be multiplied by each head's W_UV."""
-    lib = load_library()
-    _cuda(q_lat, cache, block_table, seq_lens, out, workspace, status)
+    if q_lat.dim() != 4:
+        raise ValueError("spec_verify_attn_mla: q_lat must be [B, n_new, H, d_c + d_r]")
+    _check_latent_pool(cache, q_lat.shape[-1], block_size, "spec_verify_attn_mla")
+    _int32(block_table=block_table, seq_lens=seq_lens)
     if out is not None and (out.dtype != q_lat.dtype or out.shape != q_lat.shape[:3] + (d_c,)):
         raise ValueError("out must be [B, n_new, H, d_c] in the queries' dtype")
+    lib = load_library()
+    _cuda(q_lat, cache, block_table, seq_lens, out, workspace, status)
     B, n_new, H, D = q_lat.shape
     if out is None:
         out = torch.empty((B, n_new, H, d_c), dtype=q_lat.dtype, device=q_lat.device)
@@ -364,6 +396,7 @@ def spec_verify_sample(target_logits, draft, draft_tokens, uniforms, draft_is_pr
     logit rows too with draft_top_p).
     Returns (out_tokens [B, K+1], num_accepted [B], p_at_draft, q_at_draft).
     """
+    _int32(draft_tokens=draft_tokens, out_tokens=out_tokens, num_accepted=num_accepted)
     lib = load_library()
     _cuda(target_logits, draft, draft_tokens, uniforms, out_tokens, num_accepted, p_at_draft,
           q_at_draft, workspace, status)

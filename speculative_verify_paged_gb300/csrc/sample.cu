@@ -1763,7 +1763,40 @@ constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB: 48 + 16 ceil(V / 81
 __device__ __align__(256) uint8_t g_sample_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+// the array's device address per device, and the id of the context it was
+// resolved in: a context that was destroyed and created again (after a
+// cudaDeviceReset, say) loads the module anew, possibly at another address
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void *ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+typedef int (*PfnCtxGetCurrent)(void **ctx);
+typedef int (*PfnCtxGetId)(void *ctx, unsigned long long *id);
+
+// id of the calling thread's current context (0 if the driver cannot say, in
+// which case the address is resolved again on every call)
+unsigned long long current_ctx_id() {
+  static PfnCtxGetCurrent get_cur = nullptr;
+  static PfnCtxGetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PfnCtxGetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PfnCtxGetId>(p);
+  });
+  void *ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
 }  // namespace
 
 extern "C" sv_status spec_verify_sample_static(const void *target_logits, sv_dtype logit_dtype,
@@ -1788,17 +1821,20 @@ extern "C" sv_status spec_verify_sample_static(const void *target_logits, sv_dty
   if (dev < 0 || dev >= kMaxDevices) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample_static: device %d", dev);
   void *ptr = nullptr;
   {
-    // first call on a device: resolve the array's device address (the
-    // device is current here)
+    // first call on a device (or in a new context of it): resolve the array's
+    // device address, with that device current
+    const unsigned long long ctx = current_ctx_id();
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-      e = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_sample_scratch);
+    if (!g_scratch[dev].ptr || ctx == 0 || g_scratch[dev].ctx_id != ctx) {
+      void *addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_sample_scratch);
       if (e != cudaSuccess) {
-        g_scratch_ptr[dev] = nullptr;
+        g_scratch[dev] = ScratchAddr{0ull, nullptr};
         return fail(SV_ERR_CUDA, "spec_verify_sample_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
       }
+      g_scratch[dev] = ScratchAddr{ctx, addr};
     }
-    ptr = g_scratch_ptr[dev];
+    ptr = g_scratch[dev].ptr;
   }
   return spec_verify_sample(target_logits, logit_dtype, draft, draft_dtype, draft_is_probs, draft_tokens,
                             uniforms, B, K, V, temperature, out_tokens, num_accepted, p_at_draft, q_at_draft, ptr,

@@ -33,3 +33,28 @@ def test_cli_defaults(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse()
     assert a.gpus == 1 and a.impl == "ours" and not a.mla_only and a.mla_batch == 64
+
+
+def test_gpus_must_match_the_launched_world(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "8"])
+    a = bench.parse()
+    import pytest
+    with pytest.raises(SystemExit, match="WORLD_SIZE is 1"):
+        bench.check_world(a, 1)
+    bench.check_world(a, 8)
+
+
+def test_percentiles_and_summary():
+    xs = [float(i) for i in range(11)]   # 0..10 ms
+    assert bench.pct(xs, 50) == 5.0 and bench.pct(xs, 10) == 1.0 and bench.pct(xs, 90) == 9.0
+    assert bench.pct([3.0, 1.0], 50) == 2.0
+    d = bench.dist_summary([0.1, 0.2, 0.3])
+    assert abs(d["median_us"] - 200.0) < 1e-9 and d["p10_us"] < d["median_us"] < d["p90_us"]
+
+
+def test_other_configs_cover_every_workload_and_the_sigma_sweep():
+    got = bench.other_configs("llama3_70b", 1.5)
+    names = [n for n, _ in got]
+    assert {"llama3_8b", "long", "fp8"} <= set(names)
+    assert sorted(sg for n, sg in got if n == "llama3_70b") == [0.5, 3.0]
+    assert "tiny" not in names

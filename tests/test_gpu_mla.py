@@ -73,6 +73,33 @@ def test_mla_attention_matches_oracle(sv, B, n_new, H, lens):
     assert err <= 2e-2, err
 
 
+@pytest.mark.parametrize("lens", [[771], [771, 2051]], ids=["one", "two"])
+def test_mla_last_split_fully_masked_for_early_rows(sv, lens):
+    # lengths of 3 past a split boundary: the first n_new - 3 query rows see
+    # no key of the last split, whose (m, l) then reach the merge as
+    # (-inf, 0) with P = 0 against that split's V rows
+    B, n_new, H = len(lens), 8, 16
+    q, cache, table, L = make(B, n_new, H, lens, seed=55 + B)
+    R = n_new * H
+    ws = sv.mla_workspace_size(B, n_new, H, table.shape[1])
+    # the workspace holds fp32 partials (512) and (m, l) per (sequence,
+    # split, row), then the order: S from its size, the split size from the
+    # plan's rounding to whole 64-key tiles
+    per_split = B * R * (512 + 2) * 4
+    S = (ws - 256) // per_split
+    assert S >= 2 and ws == S * per_split + 256
+    bps = -(-table.shape[1] // S)
+    bps = -(-bps // 4) * 4
+    for Lb in lens:
+        assert 0 < Lb % (16 * bps) < n_new, (Lb, bps)
+    out, st = run(sv, q, cache, table, L)
+    assert st == 0
+    ref = omla.paged_mla_attention(q, cache, table, L, SCALE, DC, BS)
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    err = np.abs(out.float().cpu().numpy() - ref).max()
+    assert err <= 2e-2, err
+
+
 def test_mla_split_plan_is_used(sv):
     # one sequence of 6000 tokens leaves most of the GPU idle without splits
     assert sv.mla_workspace_size(1, 8, 16, 376) > 0

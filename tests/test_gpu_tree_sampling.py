@@ -4,15 +4,17 @@ Inputs follow the sampling workloads: target logits N(0, 3^2), draft logits
 target + N(0, sigma^2), random BFS trees, and every child's token drawn from
 its parent's draft row (siblings i.i.d., as the exactness of the sibling rule
 assumes). Tokens, accepted lengths and accepted paths must equal the
-oracle's, except sequences one of whose decisions lies within 1e-5 of its
-boundary (the kernel decides in fp32); those are counted and must stay rare.
+oracle's. The only excuse is a sequence whose first differing decision (in
+the walk's order) has its uniform within 1e-5 of that decision's boundary;
+such sequences are counted against 0.01 % of the decisions compared, which
+at these batch sizes allows none.
 """
 import numpy as np
 import pytest
 import torch
 
 from oracle import sampling as osamp
-from parity_utils import MARGIN
+from parity_utils import MAX_EXCUSED_FRACTION, compare_tree_sampling, first_tree_difference
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -52,7 +54,7 @@ def make_inputs(B, n, V, dt, seed, sigma=1.5, T=1.0, parents=None, probs=False):
     return tl, draft, torch.from_numpy(par), torch.from_numpy(tok), uv
 
 
-def check(sv, tl, draft, par, tok, uv, T=1.0, probs=False, max_excused_frac=0.02, typical=None):
+def check(sv, tl, draft, par, tok, uv, T=1.0, probs=False, typical=None):
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     out, nacc, path = sv.spec_verify_sample_tree(tl.to(DEV), draft.to(DEV), par.to(DEV), tok.to(DEV), uv.to(DEV),
                                                  draft_is_probs=probs, temperature=T, status=st, typical=typical)
@@ -60,18 +62,7 @@ def check(sv, tl, draft, par, tok, uv, T=1.0, probs=False, max_excused_frac=0.02
     assert int(st.item()) == 0
     ref = osamp.tree_rejection_sample(tl, draft, par, tok, uv, draft_is_probs=probs, temperature=T,
                                       typical=typical)
-    out, nacc, path = out.cpu().numpy(), nacc.cpu().numpy(), path.cpu().numpy()
-    excused = 0
-    for b in range(tl.shape[0]):
-        same = (nacc[b] == ref["num_accepted"][b] and np.array_equal(out[b], ref["out_tokens"][b])
-                and np.array_equal(path[b], ref["path_nodes"][b]))
-        if not same:
-            assert ref["margin"][b] < MARGIN, ("sequence %d differs: gpu %s / %s, oracle %s / %s (margin %.3g)"
-                                               % (b, out[b].tolist(), path[b].tolist(),
-                                                  ref["out_tokens"][b].tolist(), ref["path_nodes"][b].tolist(),
-                                                  ref["margin"][b]))
-            excused += 1
-    assert excused <= max_excused_frac * tl.shape[0] + 1, "%d excused" % excused
+    compare_tree_sampling(out.cpu().numpy(), nacc.cpu().numpy(), path.cpu().numpy(), ref)
     return ref
 
 
@@ -93,9 +84,22 @@ def test_chain_tree_agrees_with_the_oracle_chain(sv):
     tl, dl, par, tok, uv = make_inputs(48, n, 3000, "bf16", seed=9, parents=[-1, 0, 1, 2, 3])
     ref = check(sv, tl, dl, par, tok, uv)
     chain = osamp.rejection_sample(tl, dl[:, :n - 1], tok[:, 1:], _chain_uniforms(uv))
-    clear = ref["margin"] > MARGIN
-    assert np.array_equal(chain["num_accepted"][clear], ref["num_accepted"][clear])
-    assert np.array_equal(chain["out_tokens"][clear], ref["out_tokens"][clear])
+    # the two oracles walk the same chain in fp64 (the tree one renormalises
+    # the residual before its draw): they may part only at a decision within
+    # rounding of its boundary, and no more often than the parity bar allows
+    excused, n_dec = 0, 0
+    for b in range(tl.shape[0]):
+        n_dec += len(ref["decisions"][b])
+        if (chain["num_accepted"][b] == ref["num_accepted"][b]
+                and np.array_equal(chain["out_tokens"][b], ref["out_tokens"][b])):
+            continue
+        path = np.full(n, -1)
+        path[:chain["num_accepted"][b]] = np.arange(1, chain["num_accepted"][b] + 1)
+        k, m = first_tree_difference(path, chain["out_tokens"][b], int(chain["num_accepted"][b]),
+                                     ref["decisions"][b])
+        assert m < 1e-12, "sequence %d: the chain and tree oracles differ at decision %d (margin %.3g)" % (b, k, m)
+        excused += 1
+    assert excused <= MAX_EXCUSED_FRACTION * n_dec
 
 
 def _chain_uniforms(uv):

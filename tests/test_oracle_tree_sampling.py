@@ -50,6 +50,40 @@ def test_chain_tree_is_the_chain(seed):
         assert list(got["path_nodes"][b, :ref["num_accepted"][b]]) == list(range(1, ref["num_accepted"][b] + 1))
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_decision_record_of_a_chain_matches_the_chain_oracle(seed):
+    # the walk's decision list against the chain oracle's own record: one
+    # accept test per visited draft (its margin |u - p/q| and outcome), then
+    # the draw at the last node with its CDF margin and the emitted token
+    rng = np.random.default_rng(100 + seed)
+    B, K, V = 12, int(rng.integers(1, 5)), int(rng.integers(3, 30))
+    tl, dl, tok, uv = chain_case(rng, B, K, V)
+    ref = sampling.rejection_sample(tl, dl, tok, uv)
+    n = K + 1
+    parent = np.tile(np.arange(-1, n - 1), (B, 1))
+    ttok = np.concatenate([np.zeros((B, 1), dtype=np.int64), tok], axis=1)
+    tdraft = np.concatenate([dl, np.zeros((B, 1, V))], axis=1)
+    tuv = np.empty((B, n, 2))
+    tuv[:, 1:, 0] = uv[:, :K, 0]
+    tuv[:, 0, 0] = 0.5
+    tuv[:, :, 1] = uv[:, :, 1]
+    got = sampling.tree_rejection_sample(tl, tdraft, parent, ttok, tuv)
+    for b in range(B):
+        dec = got["decisions"][b]
+        na = int(ref["num_accepted"][b])
+        tests = dec[:-1]
+        assert len(tests) == min(na + 1, K)
+        for i, (u, c, m, outcome) in enumerate(tests):
+            assert (u, c) == (i, i + 1)
+            assert outcome == (i < na)
+            assert m == pytest.approx(ref["accept_margin"][b, i], rel=1e-12, abs=1e-15)
+        u, c, m, y = dec[-1]
+        assert (u, c) == (na, -1)
+        assert y == ref["out_tokens"][b, na]
+        assert m == pytest.approx(ref["cdf_margin"][b], rel=1e-9, abs=1e-15)
+        assert got["margin"][b] == min(d[2] for d in dec)
+
+
 def first_token_law(p, q, k, residual=True):
     """Exact law of the first emitted token when k siblings are drawn i.i.d.
     from q and tried in turn (each sibling a leaf: an accepted one is the

@@ -44,6 +44,18 @@ def test_fp8_codes_never_nan():
     assert (a["k_scale"] > 0).all()
 
 
+def test_fp8_codes_cover_every_finite_code():
+    # the generator draws all 254 finite e4m3 patterns: zeros, subnormals
+    # (exponent field 0) and the largest magnitudes (0x7E = 448, 0xFE = -448)
+    codes = workloads._fp8_codes((200000,), 0, "k_pool", "cpu")
+    seen = torch.bincount(codes.to(torch.int64), minlength=256)
+    finite = [c for c in range(256) if c & 0x7F != 0x7F]
+    assert all(int(seen[c]) > 0 for c in finite)
+    assert int(seen[0x7F]) == 0 and int(seen[0xFF]) == 0
+    # roughly uniform: 200000 / 254 ~ 787 per code
+    assert int(seen[finite].min()) > 600 and int(seen[finite].max()) < 1000
+
+
 def test_draft_tokens_in_range_and_mostly_likely_tokens():
     cfg = workloads.CONFIGS["tiny"]
     s = workloads.make_sampling_inputs(cfg, seed=0)

@@ -46,17 +46,36 @@ def test_static_entry_point_matches_workspace_entry_point(name, over):
                                                            s["draft_tokens"], s["uniforms"])
     torch.cuda.synchronize()
     B, K = cfg.B, cfg.K
+    outs = []
+    for call in range(2):   # outputs allocated up front: the checked calls run with nothing new allocated
+        outs.append((torch.full((B, K + 1), -7, dtype=torch.int32, device="cuda"),
+                     torch.full((B,), -7, dtype=torch.int32, device="cuda"),
+                     torch.zeros((B, K), dtype=torch.float32, device="cuda"),
+                     torch.zeros((B, K), dtype=torch.float32, device="cuda"),
+                     torch.zeros(1, dtype=torch.int32, device="cuda")))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # a warm-up call: the first call on a device resolves the array's address
+    warm = outs[0]
+    assert fn(_ptr(s["target_logits"]), sv.SV_BF16, _ptr(s["draft_logits"]), sv.SV_BF16, 0,
+              _ptr(s["draft_tokens"]), _ptr(s["uniforms"]), B, K, cfg.V, 1.0, _ptr(warm[0]), _ptr(warm[1]),
+              _ptr(warm[2]), _ptr(warm[3]), _ptr(warm[4]), stream) == 0, lib.sv_last_error_string()
+    torch.cuda.synchronize()
+    for t, v in zip(warm, (-7, -7, 0, 0, 0)):
+        t.fill_(v)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    alloc0 = torch.cuda.memory_allocated()
     for call in range(2):
-        tok = torch.full((B, K + 1), -7, dtype=torch.int32, device="cuda")
-        nac = torch.full((B,), -7, dtype=torch.int32, device="cuda")
-        p = torch.zeros((B, K), dtype=torch.float32, device="cuda")
-        q = torch.zeros((B, K), dtype=torch.float32, device="cuda")
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        tok, nac, p, q, status = outs[call]
         rc = fn(_ptr(s["target_logits"]), sv.SV_BF16, _ptr(s["draft_logits"]), sv.SV_BF16, 0,
                 _ptr(s["draft_tokens"]), _ptr(s["uniforms"]), B, K, cfg.V, 1.0, _ptr(tok), _ptr(nac),
-                _ptr(p), _ptr(q), _ptr(status), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                _ptr(p), _ptr(q), _ptr(status), stream)
         assert rc == 0, lib.sv_last_error_string()
         torch.cuda.synchronize()
+        # nothing was allocated: neither through torch's caching allocator nor
+        # on the device as a whole
+        assert torch.cuda.memory_allocated() == alloc0
+        assert torch.cuda.mem_get_info()[0] == free0, "device memory changed across the call"
         assert int(status.item()) == 0
         assert torch.equal(tok, ref_tok), "call %d: tokens differ" % call
         assert torch.equal(nac, ref_nac), "call %d: accepted lengths differ" % call

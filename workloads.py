@@ -18,9 +18,10 @@ reproducible on its own and independent of which other fields are drawn):
     random permutation of the pool; the pool also holds `spare_blocks` unused
     blocks full of finite garbage. Unused table entries are -1.
   * K/V pools, Q, new K/V rows: N(0, 1), rounded to the storage dtype.
-  * fp8 e4m3 pools: random codes built from bit fields (sign uniform, exponent
-    field uniform in [3, 12], mantissa uniform in [0, 7]) with per-kv-head
-    fp32 scales uniform in [1/64, 3/64]; no NaN code is ever produced.
+  * fp8 e4m3 pools: random codes drawn uniformly from the 254 finite e4m3
+    bit patterns (both zeros, the subnormals of exponent field 0 and the
+    largest magnitudes, +-448, included; the two NaN patterns S.1111.111
+    excluded), with per-kv-head fp32 scales uniform in [1/64, 3/64].
   * target logits ~ N(0, 3^2); draft logits = target + N(0, sigma^2).
   * draft tokens: x_i = argmax(draft_logits_i / T + Gumbel noise), which draws
     x_i from softmax(draft_logits_i / T) without evaluating that softmax.
@@ -151,12 +152,12 @@ def paged_layout(cfg: VerifyConfig, seed: int, seq_lens: Optional[list] = None,
 
 
 def _fp8_codes(shape, seed, field, device):
-    """Random e4m3 bit patterns: sign | exponent field in [3,12] | mantissa."""
+    """Random e4m3 bit patterns, uniform over the 254 finite codes: a draw k in
+    [0, 254) is the code k for k < 127 (0x00 .. 0x7E) and k + 1 above
+    (0x80 .. 0xFE), which skips the NaN patterns 0x7F and 0xFF."""
     g = _gen(seed, field, device)
-    s = torch.randint(0, 2, shape, generator=g, device=device, dtype=torch.int32)
-    e = torch.randint(3, 13, shape, generator=g, device=device, dtype=torch.int32)
-    m = torch.randint(0, 8, shape, generator=g, device=device, dtype=torch.int32)
-    return ((s << 7) | (e << 3) | m).to(torch.uint8)
+    k = torch.randint(0, 254, shape, generator=g, device=device, dtype=torch.int32)
+    return (k + (k >= 127).to(torch.int32)).to(torch.uint8)
 
 
 def make_attention_inputs(cfg: VerifyConfig, seed: int = 0, device="cpu",
