@@ -6,20 +6,21 @@
 // t <= L_b - n_new + j, K_t / V_t read through the block table.
 //
 // Design (flash-decoding style split-KV, CS336 lecture 10 section 9.2):
-//   * one CTA per (split of the sequence's blocks, kv head, sequence); all
-//     (K+1)*G query rows of the GQA group are packed into 16-row tiles, so
-//     every K/V byte is read from HBM once per step;
-//   * a producer warp streams (block, head) K and V tiles with 4-D TMA
-//     tensor copies (128-byte swizzle) through a ring of shared-memory
-//     stages guarded by mbarriers; the block table is read by the producer;
-//   * consumer warps own (16-row tile, key group) pairs: QK^T and PV on the
-//     tensor cores (mma.sync m16n8k16, fp32 accumulate), online softmax in
-//     the log2 domain with quad shuffles, causal / length masking only on the
-//     tail blocks; fp8 e4m3 tiles are widened to f16 in shared memory by the
-//     warps that share them, k_scale folded into the score scale and v_scale
-//     into the output;
-//   * every (split, key group) writes an unnormalised partial (acc, m, l) and
-//     attn_merge_kernel combines them with the log-sum-exp rule
+//   * attn_order_kernel sorts the work items (split of a sequence's blocks,
+//     kv head, sequence) longest first;
+//   * attn_tc5_kernel, one CTA per work item on the fifth-generation tensor
+//     cores: all (K+1)*G query rows of the GQA group share one M = 128 MMA
+//     tile, so every K/V byte is read from HBM once per step; two producer
+//     warps stream (block, head) K and V tiles with 4-D TMA tensor copies
+//     (128-byte swizzle) through shared-memory rings guarded by mbarriers;
+//     one thread issues tcgen05.mma with S, P and O in tensor memory; a
+//     softmax warpgroup runs the online softmax in the log2 domain with a
+//     lazy rescale, masking only the tiles that reach the diagonal or the
+//     end of the split. bf16 caches feed the MMAs directly; fp8 e4m3 tiles
+//     are widened exactly to f16 by two converter warps, with k_scale folded
+//     into the score scale and v_scale into the output;
+//   * a split writes an unnormalised partial (acc, m, l) and the merge
+//     kernels combine them with the log-sum-exp rule
 //     m = max m_s, l = sum l_s 2^(m_s - m), O = sum acc_s 2^(m_s - m) / l.
 // A plain CUDA-core kernel covers fp32 caches and shapes outside the
 // tensor-core path (any d_head <= 256, any block size).
@@ -40,46 +41,10 @@ namespace {
 // ------------------------------------------------------------ constants ---
 constexpr int kD = 128;           // head dim of the tensor-core path
 constexpr int kBS = 16;           // block size of the tensor-core path
-constexpr int kNWK = 2;           // key groups (consumer warps per row tile)
-constexpr int kMaxStages = 6;
-constexpr int kMaxRT = 4;         // up to 64 packed query rows
-constexpr int kQStride = kD * 2 + 16;   // bytes per staged Q row (padded)
-constexpr int kTcAutoBps = 64;
 constexpr int kGenThreads = 128;
 constexpr int kGenKeys = 32;
 
 // ------------------------------------------------------ PTX: tensor core ---
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  if constexpr (F16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-}
-
 template <bool F16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (F16) {
@@ -119,12 +84,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Byte address of element (row, col) of a 16 x 128 16-bit tile stored as two
-// 16 x 64 boxes with the 128-byte swizzle (16-byte chunk ^= row % 8).
-__device__ __forceinline__ uint32_t swz16(uint32_t tile, int row, int col) {
-  const int box = col >> 6, c = col & 63;
-  return tile + box * 2048 + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + ((c & 7) << 1);
-}
 
 // ------------------------------------------------- tensor-core kernel -----
 struct TcParams {   // 64-byte aligned through its CUtensorMap members
@@ -151,451 +110,6 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
 __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, int (&c)[3]) {
 #pragma unroll
   for (int k = 0; k < 3; ++k) c[k] = P.role[k] == 0 ? 0 : (P.role[k] == 1 ? g : phys);
-}
-
-template <int RT, bool FP8>
-struct TcCfg {
-  static constexpr int kCompute = RT * kNWK;              // consumer warps
-  // blocks a consumer warp takes per pipeline step (two give it four
-  // independent MMA chains); fp8 tiles are widened one block at a time
-  static constexpr int kBPW = FP8 ? 1 : 2;
-  static constexpr int kBlocksPerStage = kNWK * kBPW;
-  static constexpr int kStages = FP8 ? 6 : (RT <= 2 ? 2 : 3);
-  static constexpr int kThreads = 32 * (kCompute + 1);     // + producer warp
-  static constexpr int kTile = FP8 ? kBS * kD : kBS * kD * 2;   // one K or V tile in bytes
-  static constexpr int kStageBytes = kBlocksPerStage * 2 * kTile;
-  static constexpr int kStageArea = kStages * kStageBytes;
-  static constexpr int kConvBytes = FP8 ? kNWK * 2 * 2 * (kBS * kD * 2) : 0;  // K,V f16 double-buffered
-  static constexpr int kQBytes = RT * 16 * kQStride;
-  static constexpr int kSmem = 1024 + kStageArea + kConvBytes + kQBytes;
-  static constexpr int kMinBlocks = RT <= 2 ? 3 : (RT == 3 ? 2 : 1);   // resident CTAs per SM the registers allow
-};
-
-template <int RT, bool FP8>
-__global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMinBlocks)
-    attn_tc_kernel(const __grid_constant__ TcParams P) {
-  pdl_wait();
-  pdl_trigger();
-  using Cfg = TcCfg<RT, FP8>;
-  constexpr bool F16 = FP8;   // fp8 tiles are widened to f16; bf16 stays bf16
-  extern __shared__ uint8_t smem_raw[];
-  constexpr int kStages = Cfg::kStages, kBPW = Cfg::kBPW, kBPS = Cfg::kBlocksPerStage;
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t stage_base = smem_u32(smem);
-  const uint32_t conv_base = stage_base + Cfg::kStageArea;
-  uint8_t *q_smem = smem + Cfg::kStageArea + Cfg::kConvBytes;
-
-  const int L = P.seq_lens[b];
-  if (L < P.n_new || L > P.max_blocks * kBS) {
-    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
-    return;
-  }
-  const int nblk = (L + kBS - 1) / kBS;
-  const int blk0 = s * P.bps;
-  if (blk0 >= nblk) return;                       // the merge never reads this split
-  const int blk1 = min(nblk, blk0 + P.bps);
-  const int n_iter = (blk1 - blk0 + kBPS - 1) / kBPS;
-
-  if (tid == 0) {
-    for (int k = 0; k < kStages; ++k) {
-      mbar_init(&full_bar[k], 1);
-      mbar_init(&empty_bar[k], Cfg::kCompute);
-    }
-    fence_mbarrier_init();
-  }
-  // stage Q rows of this GQA group (zero rows past R); fp8 path widens to f16
-  {
-    const int R = P.R;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(P.q);
-    for (int idx = tid; idx < RT * 16 * (kD / 8); idx += blockDim.x) {
-      const int r = idx / (kD / 8), c8 = idx % (kD / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        const int j = r / P.G, hh = r % P.G;
-        const int64_t off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD + c8 * 8;
-        v = *reinterpret_cast<const uint4 *>(q + off);
-        if (F16) {
-          uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xffff0000u);
-            __half2 h = __floats2half2_rn(lo, hi);
-            w[k] = *reinterpret_cast<uint32_t *>(&h);
-          }
-          v = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      *reinterpret_cast<uint4 *>(q_smem + r * kQStride + c8 * 16) = v;
-    }
-  }
-  __syncthreads();
-
-  // ------------------------------------------------------------ producer ---
-  // The whole warp reads the block table 32 entries at a time (the next 32
-  // are prefetched); lane 0 waits for free stages and issues the copies.
-  if (warp == 0) {
-    const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
-    const int nblocks = blk1 - blk0;
-    int cur = lane < nblocks ? table[lane] : 0;
-    int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
-    int chunk = 0;
-    bool ok_wait = true;
-    for (int it = 0; it < n_iter; ++it) {
-      const int first = it * kBPS;
-      if ((first >> 5) != chunk) {
-        chunk = first >> 5;
-        cur = nxt;
-        const int rel = (chunk + 1) * 32 + lane;
-        nxt = rel < nblocks ? table[rel] : 0;
-      }
-      int phys[kBPS];
-#pragma unroll
-      for (int kk = 0; kk < kBPS; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
-      if (lane == 0) {
-        const int st = it % kStages;
-        if (it >= kStages && !mbar_wait(&empty_bar[st], ((it / kStages) & 1) ^ 1)) {
-          ok_wait = false;   // consumers stopped: issue nothing more
-        } else {
-          const int nvalid = min(kBPS, nblocks - first);
-          mbar_arrive_expect_tx(&full_bar[st], (uint32_t)(nvalid * 2 * Cfg::kTile));
-          for (int kk = 0; kk < nvalid; ++kk) {
-            int ph = phys[kk];
-            if (ph < 0 || ph >= P.num_blocks) {
-              atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
-              ph = 0;   // stay in bounds; the output of this sequence is flagged
-            }
-            const uint32_t kt = stage_base + st * Cfg::kStageBytes + kk * 2 * Cfg::kTile;
-            const uint32_t vt = kt + Cfg::kTile;
-            int c[3];
-            tile_coords(P, g, ph, c);
-            if (FP8) {
-              tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
-              tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
-            } else {
-              tma_load_4d(kt, &P.tmk, 0, c[0], c[1], c[2], &full_bar[st]);
-              tma_load_4d(kt + 2048, &P.tmk, 64, c[0], c[1], c[2], &full_bar[st]);
-              tma_load_4d(vt, &P.tmv, 0, c[0], c[1], c[2], &full_bar[st]);
-              tma_load_4d(vt + 2048, &P.tmv, 64, c[0], c[1], c[2], &full_bar[st]);
-            }
-          }
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, (int)ok_wait, 0)) break;
-    }
-    if (lane == 0 && !ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers ---
-  const int cw = warp - 1;
-  const int rt = cw % RT, kg = cw / RT;
-  const int gq = lane >> 2, tq = lane & 3;
-
-  // Q A-fragments for the 8 k-steps of d = 128
-  // Q A-fragments are re-read from shared memory for every block (keeps 32
-  // registers free for more resident warps)
-  const uint32_t q_addr = smem_u32(q_smem) + (rt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7)) * kQStride +
-                          ((lane >> 4) * 8) * 2;
-  float scale_log2 = P.scale_log2;
-  if (FP8) scale_log2 *= P.k_scale[g];
-  const int r_lo = rt * 16 + gq, r_hi = r_lo + 8;
-  // last visible absolute key position of the two rows of this thread
-  const int lim_lo = L - P.n_new + min(r_lo, P.R - 1) / P.G;
-  const int lim_hi = L - P.n_new + min(r_hi, P.R - 1) / P.G;
-  // draft tree: of the new keys, only the row's ancestors are visible
-  const uint64_t anc_lo = P.anc ? __ldg(P.anc + (int64_t)b * P.n_new + min(r_lo, P.R - 1) / P.G) : ~0ull;
-  const uint64_t anc_hi = P.anc ? __ldg(P.anc + (int64_t)b * P.n_new + min(r_hi, P.R - 1) / P.G) : ~0ull;
-  const int first_new = L - P.n_new;
-
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-  bool ok_wait = true;
-
-  for (int it = 0; it < n_iter; ++it) {
-    const int st = it % kStages;
-    // after a timed-out wait this warp stops waiting but keeps its place in
-    // every named barrier (it then computes on stale tiles; status reports it)
-    if (ok_wait && !mbar_wait(&full_bar[st], (it / kStages) & 1)) ok_wait = false;
-    const int lbase = blk0 + it * kBPS + kg * kBPW;     // first logical block of this warp
-    const int nvalid_stage = min(kBPS, blk1 - (blk0 + it * kBPS));
-    uint32_t kt[kBPW], vt[kBPW];
-#pragma unroll
-    for (int j = 0; j < kBPW; ++j) {
-      kt[j] = stage_base + st * Cfg::kStageBytes + (kg * kBPW + j) * 2 * Cfg::kTile;
-      vt[j] = kt[j] + Cfg::kTile;
-    }
-    if constexpr (FP8) {
-      // widen this key group's K and V tiles to f16 (same swizzled layout);
-      // the RT warps of the key group share the work, then sync by name.
-      const uint32_t ck = conv_base + (kg * 2 + (it & 1)) * 2 * 4096;
-      const uint32_t cv = ck + 4096;
-      if (kg < nvalid_stage) {
-        for (int idx = rt * 32 + lane; idx < 2 * kBS * (kD / 16); idx += RT * 32) {
-          const int which = idx / (kBS * (kD / 16));
-          const int rem = idx % (kBS * (kD / 16));
-          const int row = rem / (kD / 16), ch = rem % (kD / 16);   // 16-byte chunk of 16 codes
-          const uint32_t src = (which ? vt[0] : kt[0]) + row * 128 + ((ch ^ (row & 7)) << 4);
-          uint4 raw;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                       : "r"(src));
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t h[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffff));
-            h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
-          }
-          const uint32_t dst0 = swz16(which ? cv : ck, row, ch * 16);
-          const uint32_t dst1 = swz16(which ? cv : ck, row, ch * 16 + 8);
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
-                       "r"(h[3]));
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst1), "r"(h[4]), "r"(h[5]), "r"(h[6]),
-                       "r"(h[7]));
-        }
-      }
-      named_bar_sync(1 + kg, RT * 32);
-      kt[0] = ck;
-      vt[0] = cv;
-      // the fp8 stage is no longer needed
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-    }
-    if (lbase < blk1) {
-      // ---- S = Q K^T for the 16 * kBPW keys of this warp ---------------------
-      constexpr int NT = 2 * kBPW;   // n8 key tiles
-      float sacc[NT][4];
-#pragma unroll
-      for (int n = 0; n < NT; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-      {
-        const int mi = lane >> 3;
-        const int key = (mi >> 1) * 8 + (lane & 7);
-        if constexpr (kBPW == 1) {
-          // two independent chains (even / odd k-steps) for a single block
-          float sacc2[2][4];
-#pragma unroll
-          for (int n = 0; n < 2; ++n) sacc2[n][0] = sacc2[n][1] = sacc2[n][2] = sacc2[n][3] = 0.f;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t qa[4], b0, b1, b2, b3;
-            ldsm_x4(q_addr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
-            ldsm_x4(swz16(kt[0], key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
-            if (ks & 1) {
-              mma16816<F16>(sacc2[0], qa, b0, b1);
-              mma16816<F16>(sacc2[1], qa, b2, b3);
-            } else {
-              mma16816<F16>(sacc[0], qa, b0, b1);
-              mma16816<F16>(sacc[1], qa, b2, b3);
-            }
-          }
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[n][e] += sacc2[n][e];
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t qa[4];
-            ldsm_x4(q_addr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
-#pragma unroll
-            for (int j = 0; j < kBPW; ++j) {
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(swz16(kt[j], key, ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
-              mma16816<F16>(sacc[2 * j], qa, b0, b1);
-              mma16816<F16>(sacc[2 * j + 1], qa, b2, b3);
-            }
-          }
-        }
-      }
-      // ---- masking (tail / missing blocks only) and online softmax -----------
-      float x[NT][4];
-      int nvk[kBPW];
-#pragma unroll
-      for (int j = 0; j < kBPW; ++j) {
-        const int lb = lbase + j;
-        const int t0 = lb * kBS;
-        const bool valid = lb < blk1;
-        nvk[j] = valid ? L - t0 : 0;   // valid keys of the block (>= 16 unless tail)
-        // warp-uniform: only blocks reaching the causal diagonal (or past
-        // the split) are masked
-        const bool tail = !valid || t0 + kBS - 1 > L - P.n_new;
-        if (!tail) {
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[2 * j + n][e] = sacc[2 * j + n][e] * scale_log2;
-        } else {
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = t0 + n * 8 + 2 * tq + (e & 1);
-              const int lim = (e < 2) ? lim_lo : lim_hi;
-              const uint64_t anc = (e < 2) ? anc_lo : anc_hi;
-              const int rel = t - first_new;
-              const bool in_tree = rel < 0 || ((anc >> (rel & 63)) & 1ull);
-              x[2 * j + n][e] = (valid && t <= lim && in_tree) ? sacc[2 * j + n][e] * scale_log2 : -INFINITY;
-            }
-          }
-        }
-      }
-      float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        mx_lo = fmaxf(mx_lo, fmaxf(x[n][0], x[n][1]));
-        mx_hi = fmaxf(mx_hi, fmaxf(x[n][2], x[n][3]));
-      }
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      // The reference m moves only when a tile's maximum exceeds it by more
-      // than 8 (log2 units): weights stay <= 2^8, and the accumulator is
-      // rescaled only then (the same m is stored with l, so nothing else
-      // depends on it being the running maximum).
-      const bool up_lo = mx_lo > m_lo + 8.f, up_hi = mx_hi > m_hi + 8.f;
-      float a_lo = 1.f, a_hi = 1.f;
-      if (up_lo) { a_lo = m_lo == -INFINITY ? 0.f : ex2f(m_lo - mx_lo); m_lo = mx_lo; }
-      if (up_hi) { a_hi = m_hi == -INFINITY ? 0.f : ex2f(m_hi - mx_hi); m_hi = mx_hi; }
-      const float base_lo = m_lo == -INFINITY ? 0.f : m_lo;
-      const float base_hi = m_hi == -INFINITY ? 0.f : m_hi;
-      float ps_lo = 0.f, ps_hi = 0.f;
-      uint32_t pa[kBPW][4];
-#pragma unroll
-      for (int j = 0; j < kBPW; ++j) {
-        float pv[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          pv[n][0] = ex2f(x[2 * j + n][0] - base_lo);
-          pv[n][1] = ex2f(x[2 * j + n][1] - base_lo);
-          pv[n][2] = ex2f(x[2 * j + n][2] - base_hi);
-          pv[n][3] = ex2f(x[2 * j + n][3] - base_hi);
-          ps_lo += pv[n][0] + pv[n][1];
-          ps_hi += pv[n][2] + pv[n][3];
-        }
-        pa[j][0] = pack2<F16>(pv[0][0], pv[0][1]);
-        pa[j][1] = pack2<F16>(pv[0][2], pv[0][3]);
-        pa[j][2] = pack2<F16>(pv[1][0], pv[1][1]);
-        pa[j][3] = pack2<F16>(pv[1][2], pv[1][3]);
-      }
-      l_lo = l_lo * a_lo + ps_lo;
-      l_hi = l_hi * a_hi + ps_hi;
-      if (__any_sync(0xffffffffu, up_lo || up_hi)) {
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          o[n][0] *= a_lo; o[n][1] *= a_lo;
-          o[n][2] *= a_hi; o[n][3] *= a_hi;
-        }
-      }
-      // ---- O += P V ---------------------------------------------------------
-      // keys at or past L (tail block, or a block past the split) may hold
-      // anything: their V entries are zeroed
-      const int k0 = 2 * tq;    // keys k0, k0+1 (b0) and k0+8, k0+9 (b1)
-      uint32_t m0[kBPW], m1[kBPW];
-#pragma unroll
-      for (int j = 0; j < kBPW; ++j) {
-        m0[j] = (k0 < nvk[j] ? 0x0000ffffu : 0u) | (k0 + 1 < nvk[j] ? 0xffff0000u : 0u);
-        m1[j] = (k0 + 8 < nvk[j] ? 0x0000ffffu : 0u) | (k0 + 9 < nvk[j] ? 0xffff0000u : 0u);
-      }
-      {
-        const int mi = lane >> 3;
-        const int key = (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-#pragma unroll
-          for (int j = 0; j < kBPW; ++j) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(swz16(vt[j], key, np * 16 + (mi >> 1) * 8), b0, b1, b2, b3);
-            if (nvk[j] < kBS) {
-              b0 &= m0[j]; b1 &= m1[j]; b2 &= m0[j]; b3 &= m1[j];
-            }
-            mma16816<F16>(o[2 * np], pa[j], b0, b1);
-            mma16816<F16>(o[2 * np + 1], pa[j], b2, b3);
-          }
-        }
-      }
-    }
-    if constexpr (!FP8) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-    }
-  }
-  if (!ok_wait) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-
-  // ---- combine the two key groups of each row tile, then write -------------
-  static_assert(kNWK == 2, "the epilogue merges two key groups");
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  named_bar_sync(3, Cfg::kCompute * 32);   // every stage consumed: the ring is free
-  float *xbuf = reinterpret_cast<float *>(smem) + (rt * 32 + lane) * 68;
-  if (kg == 1) {
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<float4 *>(xbuf + 4 * n) = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
-    *reinterpret_cast<float4 *>(xbuf + 64) = make_float4(m_lo, m_hi, l_lo, l_hi);
-  }
-  named_bar_sync(3, Cfg::kCompute * 32);
-  const float vs = FP8 ? P.v_scale[g] : 1.f;
-  const int nsplit = (nblk + P.bps - 1) / P.bps;
-  if (kg == 0) {
-    {
-      const float4 ml = *reinterpret_cast<const float4 *>(xbuf + 64);
-      const float mn_lo = fmaxf(m_lo, ml.x), mn_hi = fmaxf(m_hi, ml.y);
-      const float b_lo = mn_lo == -INFINITY ? 0.f : mn_lo, b_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-      const float a0l = ex2f(m_lo - b_lo), a1l = ex2f(ml.x - b_lo);
-      const float a0h = ex2f(m_hi - b_hi), a1h = ex2f(ml.y - b_hi);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const float4 v = *reinterpret_cast<const float4 *>(xbuf + 4 * n);
-        o[n][0] = o[n][0] * a0l + v.x * a1l;
-        o[n][1] = o[n][1] * a0l + v.y * a1l;
-        o[n][2] = o[n][2] * a0h + v.z * a1h;
-        o[n][3] = o[n][3] * a0h + v.w * a1h;
-      }
-      l_lo = l_lo * a0l + ml.z * a1l;
-      l_hi = l_hi * a0h + ml.w * a1h;
-      m_lo = mn_lo;
-      m_hi = mn_hi;
-    }
-    if (nsplit == 1) {
-      // the whole sequence was this split: write the normalised output
-      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P.out);
-      const float il = l_lo > 0.f ? vs / l_lo : 0.f, ih = l_hi > 0.f ? vs / l_hi : 0.f;
-      auto orow = [&](int r) {
-        const int j = r / P.G, hh = r % P.G;
-        return out + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
-      };
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int c = n * 8 + 2 * tq;
-        if (r_lo < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_lo) + c) = __floats2bfloat162_rn(o[n][0] * il, o[n][1] * il);
-        if (r_hi < P.R) *reinterpret_cast<__nv_bfloat162 *>(orow(r_hi) + c) = __floats2bfloat162_rn(o[n][2] * ih, o[n][3] * ih);
-      }
-    } else {
-      const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
-      float *acc = P.ws_acc + ent * P.R * kD;
-      float *mlp = P.ws_ml + ent * P.R * 2;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int c = n * 8 + 2 * tq;
-        if (r_lo < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_lo * kD + c) = make_float2(o[n][0] * vs, o[n][1] * vs);
-        if (r_hi < P.R) *reinterpret_cast<float2 *>(acc + (int64_t)r_hi * kD + c) = make_float2(o[n][2] * vs, o[n][3] * vs);
-      }
-      if (tq == 0) {
-        if (r_lo < P.R) { mlp[r_lo * 2] = m_lo; mlp[r_lo * 2 + 1] = l_lo; }
-        if (r_hi < P.R) { mlp[r_hi * 2] = m_hi; mlp[r_hi * 2 + 1] = l_hi; }
-      }
-    }
-  }
 }
 
 // ------------------------------------------- tcgen05 tensor-core kernel ---
@@ -632,7 +146,6 @@ __global__ void __launch_bounds__(TcCfg<RT, FP8>::kThreads, TcCfg<RT, FP8>::kMin
 constexpr int kT5Blk = 2;                      // blocks per tile
 constexpr int kT5N = 16 * kT5Blk;              // keys per tile
 constexpr int kT5SBuf = 2;                     // S / P buffers in TMEM
-constexpr int kT5Threads = 256;
 constexpr int kT5MmaWarp = 6;
 constexpr int kT5MaxR = 128;
 constexpr int kT5HalfBytes = kT5Blk * 2048;    // one head-dim half of K (or V) for a tile
@@ -641,10 +154,17 @@ constexpr int kT5TileBytes = 2 * kT5HalfBytes; // K (or V) of one tile
 // all the shared memory two CTAs per SM leave. QR is the number of query rows
 // the softmax warps write (64 when R <= 64: rows 64-127 of S, P and O are
 // never used).
-template <int QR> struct T5Cfg {
-  static constexpr int kKS = 7;   // K stages
-  static constexpr int kVS = 6;   // V stages
-  static constexpr int kSmem = 1024 + (kKS + kVS) * kT5TileBytes;
+// FP8: e4m3 caches. TMA lands each block's raw 16 x 128-byte tile in a ring
+// of its own; warps 7 (K) and 8 (V) widen them exactly to f16 (every e4m3
+// value is an f16 value) into a second ring laid out as the bf16 tiles are,
+// and the MMAs run on f16 operands (Q and P in f16 too).
+template <int QR, bool FP8> struct T5Cfg {
+  static constexpr int kKS = 7;                                  // K stages (raw for FP8)
+  static constexpr int kVS = FP8 ? 7 : 6;                        // V stages
+  static constexpr int kCS = FP8 ? 3 : 0;                        // widened f16 stages, each of K and V
+  static constexpr int kRawBytes = FP8 ? kT5Blk * 2048 : kT5TileBytes;
+  static constexpr int kThreads = FP8 ? 288 : 256;
+  static constexpr int kSmem = 1024 + (kKS + kVS) * kRawBytes + 2 * kCS * kT5TileBytes;
 };
 constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O, Q
 constexpr uint32_t kT5OCol = kT5SBuf * kT5N;
@@ -659,18 +179,6 @@ __device__ __forceinline__ uint64_t t5_desc(uint32_t saddr, uint32_t lbo, uint32
   d |= (uint64_t)1 << 46;   // descriptor version of the sm_100 family
   d |= (uint64_t)2 << 61;   // 128-byte swizzle
   return d;
-}
-
-// byte offset of (row, col < 64) in a [rows][64] bf16 region with the
-// 128-byte swizzle (8-row atoms of 1024 bytes)
-__device__ __forceinline__ uint32_t t5_sw(int row, int col) {
-  return (row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
-}
-
-__device__ __forceinline__ void t5_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-               "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void t5_mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -802,14 +310,17 @@ __global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *
   pdl_wait();
 }
 
-template <int QR>
-__global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
+template <int QR, bool FP8>
+__global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
   pdl_wait();
   pdl_trigger();
-  using Cfg = T5Cfg<QR>;
-  constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
+  using Cfg = T5Cfg<QR, FP8>;
+  constexpr int KS = Cfg::kKS, VS = Cfg::kVS, CS = Cfg::kCS > 0 ? Cfg::kCS : 1;
+  constexpr int RAW = Cfg::kRawBytes;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+  // FP8: widened stages, filled by the converter warps, freed by the MMAs
+  __shared__ __align__(8) uint64_t kc_full[CS], kc_empty[CS], vc_full[CS], vc_empty[CS];
   __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -822,7 +333,10 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t k_ring = smem_u32(smem);
-  const uint32_t v_ring = k_ring + KS * kT5TileBytes;
+  const uint32_t v_ring = k_ring + KS * RAW;
+  // the rings the MMAs read: the widened ones for FP8, else the TMA rings
+  const uint32_t kc_ring = FP8 ? v_ring + VS * RAW : k_ring;
+  const uint32_t vc_ring = FP8 ? kc_ring + CS * kT5TileBytes : v_ring;
 
   const int L = P.seq_lens[b];
   if (L < P.n_new || L > P.max_blocks * kBS) {
@@ -846,6 +360,13 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
       mbar_init(&v_full[k], 1);
       mbar_init(&v_empty[k], 1);
     }
+    if (FP8)
+      for (int k = 0; k < CS; ++k) {
+        mbar_init(&kc_full[k], 1);
+        mbar_init(&kc_empty[k], 1);
+        mbar_init(&vc_full[k], 1);
+        mbar_init(&vc_empty[k], 1);
+      }
     for (int k = 0; k < kT5SBuf; ++k) {
       mbar_init(&s_full[k], 1);
       mbar_init(&p_full[k], 4);
@@ -894,8 +415,10 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
             go = false;
           } else {
             const int nvalid = min(kT5Blk, nblocks - first);
-            mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * 2 * 2048));
-            const uint32_t base = ring + st * kT5TileBytes;
+            // a block is 2 KB of e4m3 (one 128-byte box row per slot) or two
+            // 2 KB head-dim halves of bf16
+            mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * (FP8 ? 2048 : 2 * 2048)));
+            const uint32_t base = ring + st * RAW;
             for (int kk = 0; kk < nvalid; ++kk) {
               int ph = phys[kk];
               if (ph < 0 || ph >= P.num_blocks) {
@@ -905,7 +428,7 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
               int c[3];
               tile_coords(P, g, ph, c);
               tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
-              tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
+              if (!FP8) tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
             }
             issued = t + 1;
           }
@@ -932,8 +455,10 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
     if (warp == kT5MmaWarp) {
       // ---------------------------------------------------------- MMA issuer --
       if (lane == 0) {
-        const uint32_t idesc_qk = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
-        const uint32_t idesc_pv = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (16u << 17) | (8u << 24);
+        // f32 accumulators; A and B bf16 (formats 1), or f16 for FP8 (0)
+        constexpr uint32_t ab = FP8 ? 0u : (1u << 7) | (1u << 10);
+        const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
+        const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
         static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
         int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
         bool q_ready = false;
@@ -942,33 +467,38 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
           bool progressed = false;
           if (!q_ready) q_ready = t5_test(&q_full, 0);
           if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
-            const int ks = tq % KS, sb = tq % kT5SBuf;
+            // K stage: the TMA ring (bf16) or the widened ring (FP8)
+            const int KR = FP8 ? CS : KS;
+            const int ks = tq % KR, sb = tq % kT5SBuf;
+            uint64_t *kf = FP8 ? kc_full : k_full;
             // S buffer sb is free once the P V of tile tq - kT5SBuf has run
             const bool sfree = tq < kT5SBuf || t5_test(&o_done[sb], ((tq / kT5SBuf) - 1) & 1);
-            if (sfree && t5_test(&k_full[ks], (tq / KS) & 1)) {
+            if (sfree && t5_test(&kf[ks], (tq / KR) & 1)) {
               t5_fence_after();
-              const uint32_t kb = k_ring + ks * kT5TileBytes;
+              const uint32_t kb = kc_ring + ks * kT5TileBytes;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
                 t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
                           t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
                           kk > 0 ? 1u : 0u);
               t5_commit(&s_full[sb]);
-              t5_commit(&k_empty[ks]);
+              t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
               ++tq;
               progressed = true;
             }
           }
           if (tp < tq) {
-            const int vs = tp % VS, sb = tp % kT5SBuf;
-            if (t5_test(&p_full[sb], (tp / kT5SBuf) & 1) && t5_test(&v_full[vs], (tp / VS) & 1)) {
+            const int VR = FP8 ? CS : VS;
+            const int vs = tp % VR, sb = tp % kT5SBuf;
+            uint64_t *vf = FP8 ? vc_full : v_full;
+            if (t5_test(&p_full[sb], (tp / kT5SBuf) & 1) && t5_test(&vf[vs], (tp / VR) & 1)) {
               t5_fence_after();
-              const uint32_t vb = v_ring + vs * kT5TileBytes;
+              const uint32_t vb = vc_ring + vs * kT5TileBytes;
 #pragma unroll
               for (int j = 0; j < kT5Blk; ++j)
                 t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
                           idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
-              t5_commit(&v_empty[vs]);
+              t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
               t5_commit(&o_done[sb]);
               ++tp;
               progressed = true;
@@ -998,34 +528,76 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
       // draft tree: of the new keys, only the row's ancestors are visible
       const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
       const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
-      const float sl2 = P.scale_log2;
+      float sl2 = P.scale_log2;
       {
         // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
         // order). tcgen05.st is warp-collective: a warp holding live rows
         // stores all 32 (zeros for rows past R); warps with none skip it
         // (their rows of S, P and O are never read).
         if (warp_live) {
-          uint4 qv[16];
+          const uint4 *src = nullptr;
           if (live) {
             const int j = row / P.G, hh = row % P.G;
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
-                                                               (((int64_t)b * P.n_new + j) * P.H_q +
-                                                                (int64_t)g * P.G + hh) * kD);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                  (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
           }
+          if constexpr (FP8) {
+            // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
+            // in [2^14, 2^15): the f16 range then holds the whole row with no
+            // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
+            // exact, and 2^-s, k_scale and the softmax scale fold into the
+            // row's scale (values below 2^-31 of the maximum lose bits in the
+            // f16 subnormals; their products are far below the fp32 sum's
+            // rounding). Two passes over the row (the second from L1) keep
+            // few registers live.
+            float amax = 0.f;
+            if (live) {
+#pragma unroll 4
+              for (int k = 0; k < 16; ++k) {
+                const uint4 v = __ldg(src + k);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int c0 = 0; c0 < 4; ++c0) {
-            uint32_t w[16];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
-              w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
+                for (int e = 0; e < 4; ++e)
+                  amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
+              }
             }
-            t5_st16(lane_base + kT5QCol + 16 * c0, w);
+            const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
+            const float up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);     // 2^s, s = 14 - ex
+            const float down = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);   // 2^-s
+            sl2 *= P.k_scale[g] * down;
+            auto widen = [up](uint32_t w) {
+              return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
+            };
+#pragma unroll 1
+            for (int c0 = 0; c0 < 4; ++c0) {
+              uint32_t w[16];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint4 v = live ? __ldg(src + 4 * c0 + k) : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
+                w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
+              }
+              t5_st16(lane_base + kT5QCol + 16 * c0, w);
+            }
+          } else {
+            uint4 qv[16];
+            if (live) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < 4; ++c0) {
+              uint32_t w[16];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
+                w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
+              }
+              t5_st16(lane_base + kT5QCol + 16 * c0, w);
+            }
           }
           t5_wait_st();
         }
@@ -1103,16 +675,17 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
             for (int k = 0; k < 16; ++k) {
               const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
               ps += p0 + p1;
-              w[k] = pack2<false>(p0, p1);
+              w[k] = pack2<FP8>(p0, p1);
             }
             t5_st16(lane_base + sb * kT5N + c0 / 2, w);
           }
           t5_wait_st();
           l += ps;
         }
-        if (key0 + kT5N > end_key && warp == 0) {
+        if (!FP8 && key0 + kT5N > end_key && warp == 0) {
           // keys past the split or the sequence (not loaded, or stale): V rows
           // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
+          // (FP8: the converter writes those rows as zeros)
           if (!t5_wait(&v_full[vs], (t / VS) & 1, abf)) ok = false;
           const uint32_t vb = v_ring + vs * kT5TileBytes;
           for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
@@ -1146,7 +719,9 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
           out = static_cast<__nv_bfloat16 *>(P.out) + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
           acc = P.ws_acc + (ent * P.R + row) * kD;
         }
-        const float il = l > 0.f ? 1.f / l : 0.f;
+        // FP8: the values are codes; v_scale makes them values again
+        const float vsc = FP8 ? P.v_scale[g] : 1.f;
+        const float il = (l > 0.f ? 1.f / l : 0.f) * vsc;
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 64) {
           uint32_t r[64];
@@ -1167,8 +742,8 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
 #pragma unroll
               for (int c = 0; c < 64; c += 4)
                 *reinterpret_cast<float4 *>(acc + c0 + c) =
-                    make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]), __uint_as_float(r[c + 2]),
-                                __uint_as_float(r[c + 3]));
+                    make_float4(__uint_as_float(r[c]) * vsc, __uint_as_float(r[c + 1]) * vsc,
+                                __uint_as_float(r[c + 2]) * vsc, __uint_as_float(r[c + 3]) * vsc);
             }
           }
         }
@@ -1176,6 +751,67 @@ __global__ void __launch_bounds__(kT5Threads, 2) attn_tc5_kernel(const __grid_co
           P.ws_ml[(ent * P.R + row) * 2] = m_ref;
           P.ws_ml[(ent * P.R + row) * 2 + 1] = l;
         }
+      }
+    }
+  }
+  if (FP8 && (warp == 7 || warp == 8)) {
+    // ----------------------------------------------------- e4m3 -> f16 ---
+    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is kT5Blk blocks of
+    // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
+    // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
+    // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
+    // keys past the split or the sequence are written as zeros.
+    const bool isv = warp == 8;
+    const int NS = isv ? VS : KS;
+    uint64_t *rfull = isv ? v_full : k_full;
+    uint64_t *rempty = isv ? v_empty : k_empty;
+    uint64_t *cfull = isv ? vc_full : kc_full;
+    uint64_t *cempty = isv ? vc_empty : kc_empty;
+    const uint32_t rring = isv ? v_ring : k_ring;
+    const uint32_t cring = isv ? vc_ring : kc_ring;
+    const int end_key = min(L, blk1 * kBS);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int rs = t % NS, cs = t % CS;
+      bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf));
+      if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf));
+      if (!ok) break;
+      const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
+      const int key0 = (blk0 + t * kT5Blk) * kBS;
+#pragma unroll 2
+      for (int j = 0; j < 8; ++j) {
+        const int q = lane + 32 * j;
+        const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
+        uint32_t v0, v1, v2, v3;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                     : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
+        uint32_t h[8];
+        if (key0 + row < end_key) {
+          const uint32_t w[4] = {v0, v1, v2, v3};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffffu));
+            h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) h[k] = 0u;
+        }
+        const uint32_t rowb = dst + (ch >> 2) * kT5HalfBytes + blk * 2048 + r16 * 128;
+        const int c8 = 2 * (ch & 3);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
+                     "r"(h[1]), "r"(h[2]), "r"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
+                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                     : "memory");
+      }
+      // the tensor cores read the widened tile through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
+        mbar_arrive(&cfull[cs]);    // the widened stage may be read
       }
     }
   }
@@ -1591,11 +1227,11 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
   if (lay)
     strides_ok = (lay->block_stride * es) % 16 == 0 && (lay->head_stride * es) % 16 == 0 &&
                  (lay->slot_stride * es) % 16 == 0;
-  p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS &&
-         p.R <= (kv == SV_BF16 ? kT5MaxR : 16 * kMaxRT) && strides_ok;
+  p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS && p.R <= kT5MaxR &&
+         strides_ok;
   if (bps_req > 0) {
     p.bps = bps_req;
-  } else if (p.tc && kv == SV_BF16) {
+  } else if (p.tc) {
     // tcgen05 kernel: long splits amortise its per-CTA setup (TMEM, Q,
     // pipeline fill) and the merge; at least one split per SM when the batch
     // is small. The longest-first order keeps the last wave short, so
@@ -1650,28 +1286,13 @@ __global__ void __launch_bounds__(64) attn_tree_kernel(const int32_t *parent, in
   anc[(int64_t)b * n_new + j] = m;
 }
 
-template <int RT, bool FP8>
-sv_status launch_tc(const TcParams &P, cudaStream_t st) {
-  using Cfg = TcCfg<RT, FP8>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_tc_kernel<RT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg::kSmem);
-  });
-  if (attr_err != cudaSuccess)
-    return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  dim3 grid(P.S, P.H_kv, P.B);
-  launch_k(attn_tc_kernel<RT, FP8>, grid, dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
-  return check_launch("spec_verify_attn tensor-core launch");
-}
-
-template <int QR>
+template <int QR, bool FP8>
 sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
+  using Cfg = T5Cfg<QR, FP8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_tc5_kernel<QR>, cudaFuncAttributeMaxDynamicSharedMemorySize, T5Cfg<QR>::kSmem);
+    attr_err = cudaFuncSetAttribute(attn_tc5_kernel<QR, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
@@ -1679,7 +1300,7 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
            P.max_blocks, const_cast<int32_t *>(P.order));
   sv_status rc = check_launch("spec_verify_attn order launch");
   if (rc != SV_OK) return rc;
-  launch_k(attn_tc5_kernel<QR>, dim3(P.S * P.H_kv * P.B), dim3(kT5Threads), T5Cfg<QR>::kSmem, st, 1, P);
+  launch_k(attn_tc5_kernel<QR, FP8>, dim3(P.S * P.H_kv * P.B), dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
   return check_launch("spec_verify_attn tcgen05 launch");
 }
 
@@ -1814,17 +1435,8 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
     P.scale_log2 = scale_log2;
-    const int RT = (plan.R + 15) / 16;
-    if (!fp8) {
-      rc = plan.R <= 64 ? launch_tc5<64>(P, st) : launch_tc5<128>(P, st);
-    } else {
-      switch (RT) {
-        case 1: rc = launch_tc<1, true>(P, st); break;
-        case 2: rc = launch_tc<2, true>(P, st); break;
-        case 3: rc = launch_tc<3, true>(P, st); break;
-        default: rc = launch_tc<4, true>(P, st); break;
-      }
-    }
+    if (!fp8) rc = plan.R <= 64 ? launch_tc5<64, false>(P, st) : launch_tc5<128, false>(P, st);
+    else rc = plan.R <= 64 ? launch_tc5<64, true>(P, st) : launch_tc5<128, true>(P, st);
   } else {
     GenParams P;
     P.q = q; P.out = out; P.k_cache = k_cache; P.v_cache = v_cache; P.k_scale = k_scale; P.v_scale = v_scale;

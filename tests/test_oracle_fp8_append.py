@@ -96,9 +96,14 @@ def test_append_writes_positions_through_block_table(kv_dtype):
                     if kv_dtype == "fp8_e4m3":
                         expect = torch.from_numpy(fp8.quantize(row.numpy(), np.float32(sc[g].item())))
                         assert torch.equal(cache[blk, g, pos % 16], expect)
-                        # decoded value is within half an e4m3 step of x
+                        # decoded value is within half an e4m3 step of x,
+                        # or +-448 scale where x lies beyond (saturation)
                         dec = fp8.decode(expect.numpy()) * sc[g].item()
-                        assert np.all(np.abs(dec - row.double().numpy()) <= 0.0625 * np.abs(row.double().numpy()) + 2 ** -10 * sc[g].item())
+                        lim = 448.0 * np.float64(np.float32(sc[g].item()))
+                        x = np.clip(row.double().numpy(), -lim, lim)
+                        assert np.all(np.abs(dec - x) <= 0.0625 * np.abs(x) + 2 ** -10 * sc[g].item())
+                        sat = np.abs(row.double().numpy()) > lim * (1 + 2 ** -4)
+                        assert np.all(np.abs(np.abs(dec[sat]) - lim) <= 1e-12 * lim)
                     else:
                         assert torch.equal(cache[blk, g, pos % 16], row.to(cache.dtype))
     # nothing else changed

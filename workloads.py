@@ -21,7 +21,9 @@ reproducible on its own and independent of which other fields are drawn):
   * fp8 e4m3 pools: random codes drawn uniformly from the 254 finite e4m3
     bit patterns (both zeros, the subnormals of exponent field 0 and the
     largest magnitudes, +-448, included; the two NaN patterns S.1111.111
-    excluded), with per-kv-head fp32 scales uniform in [1/64, 3/64].
+    excluded), with per-kv-head fp32 scales amax / 448 for amax uniform in
+    [2, 6] (the largest code then stands for a magnitude of 2 to 6, like
+    N(0, 1) data quantised with a per-head amax).
   * target logits ~ N(0, 3^2); draft logits = target + N(0, sigma^2).
   * draft tokens: x_i = argmax(draft_logits_i / T + Gumbel noise), which draws
     x_i from softmax(draft_logits_i / T) without evaluating that softmax.
@@ -171,8 +173,8 @@ def make_attention_inputs(cfg: VerifyConfig, seed: int = 0, device="cpu",
         out["k_cache"] = _fp8_codes(shape, seed, "k_pool", device)
         out["v_cache"] = _fp8_codes(shape, seed, "v_pool", device)
         gk, gv = _gen(seed, "k_scale", "cpu"), _gen(seed, "v_scale", "cpu")
-        out["k_scale"] = ((1 + 2 * torch.rand(cfg.H_kv, generator=gk)) / 64).to(device)
-        out["v_scale"] = ((1 + 2 * torch.rand(cfg.H_kv, generator=gv)) / 64).to(device)
+        out["k_scale"] = ((2 + 4 * torch.rand(cfg.H_kv, generator=gk)) / 448).to(device)
+        out["v_scale"] = ((2 + 4 * torch.rand(cfg.H_kv, generator=gv)) / 448).to(device)
     else:
         dt = torch_dtype(cfg.kv_dtype)
         out["k_cache"] = _normal(shape, seed, "k_pool", device, dtype=dt)
