@@ -113,6 +113,25 @@ const char *sv_last_error_string(void);
  * takes the difference around a region to count its launches. */
 unsigned long long sv_kernel_launches(void);
 
+/* Test hooks for the bounded waits (no counterpart in the pages; they exist
+ * so that a test can make a wait run out without faulting anything).
+ *   wait_limit_ns: the limit every later launch gives each of its device
+ *     waits (0 restores the default of one second);
+ *   withhold: signals later launches leave unsent, so that a wait on them
+ *     runs out:
+ *       SV_TEST_WITHHOLD_COPIES   spec_verify_attn's tensor-core kernel
+ *         issues no K/V copies (nothing is in flight when its waits give up);
+ *       SV_TEST_WITHHOLD_ARRIVALS  CTA 0 of spec_verify_sample's
+ *         float-float pass does not arrive at its grid barriers, so every
+ *         CTA's wait there runs out (the pass runs when a decision is not
+ *         certified, or always with SV_SAMPLE_FORCE_EXACT).
+ * A wait that runs out sets SV_DEV_TIMEOUT in the call's device status and
+ * the kernel returns (outputs of that call are not valid); the next call
+ * with the hooks cleared is unaffected. Process-wide; not for production
+ * use. */
+enum { SV_TEST_WITHHOLD_COPIES = 1, SV_TEST_WITHHOLD_ARRIVALS = 2 };
+void sv_test_hooks(unsigned long long wait_limit_ns, unsigned withhold);
+
 /* ------------------------------------------------------------------------ *
  * kv_block_append
  *   Writes k_new[b][j][g][:] and v_new[b][j][g][:] (j = 0..n_new-1) to

@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH):
     lib.sv_last_error_string.argtypes = []
     lib.sv_kernel_launches.restype = ctypes.c_ulonglong
     lib.sv_kernel_launches.argtypes = []
+    lib.sv_test_hooks.restype = None
+    lib.sv_test_hooks.argtypes = [ctypes.c_ulonglong, ctypes.c_uint]
     lib.kv_block_append.restype = I
     lib.kv_block_append.argtypes = [P, P, I, P, P, I, LP, P, P, P, I, P, I, I, I, I, I, I, P, P]
     lib.spec_verify_attn_workspace_size.restype = Z
@@ -361,6 +363,17 @@ def spec_verify_attn_mla(q_lat, cache, block_table, seq_lens, softmax_scale, d_c
 
 
 # ------------------------------------------------------------- sampling ---
+
+SV_TEST_WITHHOLD_COPIES, SV_TEST_WITHHOLD_ARRIVALS = 1, 2
+SV_DEV_TIMEOUT = 8
+
+
+def test_hooks(wait_limit_ns=0, withhold=0):
+    """Wait limit of later launches' device waits (0: the default second) and
+    the signals they withhold (SV_TEST_WITHHOLD_*), for tests of the bounded
+    waits."""
+    load_library().sv_test_hooks(int(wait_limit_ns), int(withhold))
+
 
 def kernel_launches():
     """Kernels the library has launched in this process (host-side count)."""

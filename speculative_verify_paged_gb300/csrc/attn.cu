@@ -104,6 +104,8 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
   int role[3];        // tensor-map dims 1..3 hold (0 = slot, 1 = kv head, 2 = block)
   float scale_log2;   // softmax_scale * log2(e)
+  uint64_t wait_ns;   // limit of each wait on another warp's signal
+  unsigned withhold;  // test hook: SV_TEST_WITHHOLD_COPIES issues no K/V copies
 };
 
 // TMA coordinates {d, dim1, dim2, dim3} of tile (kv head g, physical block)
@@ -118,7 +120,7 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 // read S and write P through TMEM, so no warp holds an accumulator in
 // registers.
 //
-// CTA = (split s, kv head g, sequence b), 256 threads:
+// CTA = (split s, kv head g, sequence b), 256 threads (288 for fp8 caches):
 //   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
 //              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
 //              and first writes that row of Q into TMEM
@@ -131,7 +133,7 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 //              Q K^T runs ahead whenever K data and an S buffer are ready.
 //              It sits on the third scheduler (warp id % 4 = 2), away from
 //              the softmax warps that own rows 0-63.
-//   warp 7     idle
+//   warp 7     idle (fp8 caches: widens K tiles to f16; warp 8 widens V)
 // A tile is kT5Blk paged blocks (N = 16 kT5Blk keys). Per tile t, with
 // buffer u = t % kT5SBuf:
 //   S[u] = Q K^T           (M=128 padded query rows, N keys, K=128)
@@ -226,10 +228,11 @@ __device__ __forceinline__ bool t5_test(uint64_t *bar, uint32_t phase) {
   return done != 0;
 }
 
-// Bounded wait that gives up at once after any earlier wait of the CTA gave up.
-__device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile int *abort_flag) {
+// Bounded wait (limit_ns) that gives up at once after any earlier wait of the
+// CTA gave up.
+__device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile int *abort_flag, uint64_t limit_ns) {
   if (*abort_flag) return false;
-  if (mbar_wait(bar, phase)) return true;
+  if (mbar_wait(bar, phase, limit_ns)) return true;
   *abort_flag = 1;
   return false;
 }
@@ -397,7 +400,10 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
       int chunk = 0;
       int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
+      // (test hook: with the copies withheld every wait on them runs out,
+      // with nothing in flight)
+      const int n_issue = (P.withhold & SV_TEST_WITHHOLD_COPIES) ? 0 : n_tiles;
+      for (int t = 0; t < n_issue; ++t) {
         const int first = t * kT5Blk;
         if ((first >> 5) != chunk) {
           chunk = first >> 5;
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
         const int st = t % NS;
         bool go = true;
         if (lane == 0) {
-          if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf)) {
+          if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf, P.wait_ns)) {
             go = false;
           } else {
             const int nvalid = min(kT5Blk, nblocks - first);
@@ -506,7 +512,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           }
           if (progressed) {
             t_last = global_ns();
-          } else if (*abf || global_ns() - t_last > kWaitLimitNs) {
+          } else if (*abf || global_ns() - t_last > P.wait_ns) {
             *abf = 1;
             break;
           } else {
@@ -609,7 +615,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int sb = t % kT5SBuf, vs = t % VS;
-        ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (t / kT5SBuf) & 1, abf));
+        ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (t / kT5SBuf) & 1, abf, P.wait_ns));
         if (!ok) break;
         t5_fence_after();
         const int key0 = (blk0 + t * kT5Blk) * kBS;
@@ -652,7 +658,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           if (t > 0 && __any_sync(0xffffffffu, up)) {
             // rescale O: the previous P V must have landed first
             const int pb = (t - 1) % kT5SBuf;
-            ok = __all_sync(0xffffffffu, t5_wait(&o_done[pb], ((t - 1) / kT5SBuf) & 1, abf));
+            ok = __all_sync(0xffffffffu, t5_wait(&o_done[pb], ((t - 1) / kT5SBuf) & 1, abf, P.wait_ns));
             t5_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < 128; c0 += 16) {
@@ -686,7 +692,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           // keys past the split or the sequence (not loaded, or stale): V rows
           // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
           // (FP8: the converter writes those rows as zeros)
-          if (!t5_wait(&v_full[vs], (t / VS) & 1, abf)) ok = false;
+          if (!t5_wait(&v_full[vs], (t / VS) & 1, abf, P.wait_ns)) ok = false;
           const uint32_t vb = v_ring + vs * kT5TileBytes;
           for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
             const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
@@ -707,7 +713,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       }
       // ---- epilogue: O of this row -------------------------------------------
       const int lb = (n_tiles - 1) % kT5SBuf;
-      const bool have = __all_sync(0xffffffffu, ok && t5_wait(&o_done[lb], ((n_tiles - 1) / kT5SBuf) & 1, abf));
+      const bool have = __all_sync(0xffffffffu, ok && t5_wait(&o_done[lb], ((n_tiles - 1) / kT5SBuf) & 1, abf, P.wait_ns));
       t5_fence_after();
       if (have && warp_live) {
         const int nsplit = (nblk + P.bps - 1) / P.bps;
@@ -772,8 +778,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     const int end_key = min(L, blk1 * kBS);
     for (int t = 0; t < n_tiles; ++t) {
       const int rs = t % NS, cs = t % CS;
-      bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf));
-      if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf));
+      bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf, P.wait_ns));
+      if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf, P.wait_ns));
       if (!ok) break;
       const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
       const int key0 = (blk0 + t * kT5Blk) * kBS;
@@ -1435,6 +1441,8 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
     P.scale_log2 = scale_log2;
+    P.wait_ns = wait_limit_ns();
+    P.withhold = test_withhold();
     if (!fp8) rc = plan.R <= 64 ? launch_tc5<64, false>(P, st) : launch_tc5<128, false>(P, st);
     else rc = plan.R <= 64 ? launch_tc5<64, true>(P, st) : launch_tc5<128, true>(P, st);
   } else {

@@ -7,32 +7,29 @@
 // rejection n the token is drawn by inverse CDF (ascending token id, strict
 // '>') from max(0, p_n - q_n); if all K are accepted it is drawn from p_K.
 //
-// GB300 design: sample_init_kernel (one CTA) zeroes the call's counters;
-// sample_fused_kernel does the work; sample_exact_kernel resolves, in
-// float-float arithmetic, the rare sequences the fused kernel could not
-// certify. Every CTA of the two working kernels takes a ticket from a global
-// counter when it starts; the ticket names its work item, so a CTA only ever
-// waits for CTAs holding smaller tickets, which are already running or done.
-//   * statistics items, (chunk c, position i) of sequence b: the 8192-logit
-//     chunk of target row i and of draft row i, loaded with 16-byte loads
-//     straight into registers (every logit crosses HBM once); exact maxima,
-//     fp32 sums of exponentials (the two rows paired in packed fp32
-//     arithmetic); one (max, sum) pair per row and chunk. The last item of a
-//     sequence to finish combines them, evaluates the accept tests in fp32
-//     with a certificate that each lies outside its rounding bound, walks to
-//     the first rejection (or the bonus row) and publishes the row drawn from.
-//   * draw items, (chunk c) of sequence b, ticketed a few sequences behind
-//     b's statistics so that draws run while other sequences still stream:
-//     each waits for b's decisions, streams its chunk of the row drawn from
-//     (the residual max(0, p - q), or the bonus row) and publishes per-warp
-//     sums of the weights; the last draw item of the sequence locates v Z
-//     (chunk, warp, then one warp's 1024 logits reloaded from L2) and
-//     certifies the token.
-//   * a decision that is not certified (a few percent of sequences at a
-//     128K vocabulary) goes to sample_exact_kernel, which re-evaluates it in
-//     float-float arithmetic (~1e-9 relative error per term), so emitted
-//     tokens are those of exact arithmetic except for uniforms within
-//     ~1e-10 of a boundary.
+// GB300 design (three launches, no host round trip):
+//   * sample_stats_kernel: a streaming reduction. One CTA per (8192-logit
+//     chunk, position, sequence) loads its chunk of the target row and of
+//     the draft row with 16-byte loads straight into registers, takes exact
+//     maxima and fp32 sums of exponentials (target and draft paired in
+//     packed fp32 arithmetic) and writes one (max, sum) pair per row; every
+//     logit crosses HBM once.
+//   * sample_draw_kernel: one cluster per sequence combines the chunk
+//     statistics, evaluates every accept test in fp32 with a certificate
+//     that it lies outside its rounding bound, and finds the position whose
+//     draw is used (the first certified rejection, or the bonus row). Only
+//     that row is read again, 16-byte loads straight into registers (no
+//     shared-memory slices, so every CTA of the grid is resident at once);
+//     its residual weights are summed per block of 256 elements, the
+//     cluster's prefix locates v Z, the owning warp rescans one block, and
+//     the inverse-CDF draw gets its own certificate. One 48-byte record per
+//     (sequence, position) results; certified sequences write their tokens.
+//   * sample_finish_kernel: one CTA per SM (cooperative launch) resolves the
+//     sequences the draw kernel queued. The rare decision that is not
+//     certified (a few percent of sequences) is
+//     re-evaluated from that row's logits in float-float arithmetic (~1e-9
+//     relative error per term), so emitted tokens are those of exact
+//     arithmetic except for uniforms within ~1e-10 of a boundary.
 #include <cmath>
 #include <algorithm>
 #include <mutex>
@@ -43,55 +40,57 @@
 namespace sv {
 namespace {
 
-constexpr int kFThreads = 256;
-constexpr int kFWarps = kFThreads / 32;
-constexpr int kChunk = 8192;                          // logits of a row per item
-constexpr int kChunkGroups = kChunk / 8;              // groups of eight
-constexpr int kGrp = kChunkGroups / kFThreads;        // groups per thread (4)
-constexpr int kMaxChunks = 32;                        // V <= 262144
-constexpr int kMaxPos = 64;                           // K + 1 <= 64
-static_assert(kGrp == 4 && kChunkGroups == 32 * kGrp * kFWarps, "draw layout: warp, block of 32 groups, lane");
+constexpr int kRowThreads = 256;
+constexpr int kRowWarps = kRowThreads / 32;
 
-// per-sequence words (zeroed by sample_init_kernel): statistics items done,
-// draw items done, decisions published
-enum : int { SEQ_STATS = 0, SEQ_DRAW = 1, SEQ_DEC = 2, SEQ_WORDS = 4 };
-// what the decisions leave to the draw items: the draw, or nothing (the
-// sequence went to the float-float kernel)
-enum : int { DEC_DRAW = 1, DEC_EXACT = 2 };
-// the call's words: tickets of the two kernels, the pending count, then one
-// barrier counter per float-float group
-enum : int { SYNC_TICKET = 0, SYNC_XTICKET = 1, SYNC_PCOUNT = 2, SYNC_XBAR = 4, SYNC_WORDS = 64 };
-constexpr int kWtStride = 12;   // per chunk of a draw: kFWarps warp totals, the chunk total, padding
+enum : uint32_t {
+  REC_ACCEPT = 1u,       // fp32 accept decision of the draft at this position
+  REC_ACC_CERT = 2u,     // ... certified: outside the rounding bound
+  REC_DRAW_CERT = 4u,    // the fp32 draw was found and certified
+  REC_EXACT_ACC = 8u,    // set by the finish kernel: accept re-evaluated in float-float
+  REC_EXACT_DRAW = 16u,  // set by the finish kernel: draw re-evaluated in float-float
+};
+
+struct RowRec {
+  float m_p, s_p, m_q, s_q;  // row max and sum of exp2((l - m) c) (fp32)
+  float p_x, q_x;            // p_i(x_i), q_i(x_i) in fp32
+  float gap, z;              // margin of the fp32 draw and the mass it was drawn from
+  int32_t y;                 // fp32 draw of this row (-1 if not found)
+  uint32_t flags;            // REC_*
+  int32_t y_exact;           // float-float draw (finish kernel; -1 if not evaluated)
+  float e_abs;               // rounding bound the fp32 margin was compared with
+};
+static_assert(sizeof(RowRec) == 48, "record layout");
 
 struct SampleParams {
-  const void *target;     // [B][K+1][V]
-  const void *draft;      // [B][K][V] logits (target dtype) or f32 probabilities
-  const int32_t *tokens;  // [B][K]
-  const float *uniforms;  // [B][K+1][2]
+  const void *target;
+  const void *draft;
+  const int32_t *tokens;
+  const float *uniforms;
   float *p_at;
   float *q_at;
   int32_t *out_tokens;
   int32_t *num_acc;
-  float4 *part;           // [B][K+1][nc] (max, sum) of the target and draft chunks; the float-float
-                          // kernel reuses a pending sequence's rows for (S_p hi, lo, S_q hi, lo)
-  float4 *rowrec;         // [B][K+1] (m_p, S_p, m_q, S_q) of each row
-  int *rowflag;           // [B][K+1] accept test: bit 0 accepted, bit 1 certified
-  float *wtot;            // [B][nc][kWtStride] per-warp and chunk totals of the draw
-  float4 *xtot;           // [B][nc] float-float chunk totals (hi, lo) and last positive index
-  int2 *dec;              // [B] (row drawn from, DEC_*)
-  int2 *pend;             // [B] sequences left to the float-float kernel: (b, first row to resolve)
-  unsigned *seq;          // [B][SEQ_WORDS]
-  unsigned *sync;         // [SYNC_WORDS]
+  RowRec *recs;
+  float4 *part;  // [B][K+1][nc] (max, sum) of the target and draft chunks
   int32_t *status;
-  int B, K, V, nc;
-  int lag;                // sequences a draw item is ticketed behind its statistics
-  int aligned;            // rows are 16-byte aligned: vector loads
+  int B, K, V;
+  int nc;        // statistics chunks per row
+  int gpc;       // groups of eight elements per CTA slice of the draw kernel
+  int aligned;   // rows are 16-byte aligned: bulk copies usable
+  unsigned *fin_sync;   // finish grid barrier: arrival count, generation; [2] pending count
+  int2 *pend;           // [B] sequences left to the finish grid: (b, first row to resolve)
+  float2 *fin_sum;      // [kMaxUnits][kMaxFinCtas][2] chunk sums of e_p, e_q (float-float)
+  float2 *fin_tot;      // [kMaxEntries][kMaxFinCtas] chunk totals of the weights
+  int *fin_last;        // [kMaxEntries][kMaxFinCtas] last positive weight of a chunk
   unsigned flags;
-  float c;                // log2(e) / T
+  uint64_t wait_ns;     // limit of each wait on another CTA's arrival
+  unsigned withhold;    // test hook: SV_TEST_WITHHOLD_ARRIVALS keeps CTA 0 of the finish grid from arriving
+  float c;       // log2(e) / T
   float invT_hi, invT_lo;
   int unitT;
-  float log2e_hi, log2e_lo;
-  float2 tbl[64];         // 2^(j/64) split into (hi, lo)
+  float log2e_hi, log2e_lo, ln2_hi, ln2_lo;
+  float2 tbl[64];  // 2^(j/64) split into (hi, lo)
 };
 
 // ------------------------------------------------- float-float arithmetic ---
@@ -160,6 +159,88 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+template <typename T>
+__device__ __forceinline__ void load8(const T *s, int g, float (&x)[8]);
+
+template <>
+__device__ __forceinline__ void load8<float>(const float *s, int g, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(s)[2 * g];
+  const float4 b = reinterpret_cast<const float4 *>(s)[2 * g + 1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *s, int g, float (&x)[8]) {
+  const uint4 v = reinterpret_cast<const uint4 *>(s)[g];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
+
+template <>
+__device__ __forceinline__ void load8<__half>(const __half *s, int g, float (&x)[8]) {
+  const uint4 v = reinterpret_cast<const uint4 *>(s)[g];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __half2 h = *reinterpret_cast<const __half2 *>(&w[k]);
+    const float2 f = __half22float2(h);
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T pad_value(bool is_prob) {
+  if (is_prob) return T(0.f);
+  return T(-INFINITY);
+}
+
+// (m, s) pairs of an online softmax: s = sum 2^(fl(x c - fl(m c))). Every
+// exponent is taken against the rounded reference fl(m c), the same one the
+// weights of pass B use, so sums and weights share one scale. Commutative,
+// so butterfly reductions leave the same bits in every lane.
+__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2, float c) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) { m = mn; s = 0.f; return; }
+  // __fmul_rn: the references must be the rounded products, never fused
+  // into an fma (a fused m c - fl(m c) would rescale the leading partial by
+  // its rounding residual at every reduction level)
+  const float rc = __fmul_rn(mn, c);
+  s = s * ex2(__fmul_rn(m, c) - rc) + s2 * ex2(__fmul_rn(m2, c) - rc);
+  m = mn;
+}
+
+
+// Warp-wide combination of (m, s) pairs: the maximum first, then every lane
+// rescales its own sum to it (one ex2), then a plain sum. Butterfly
+// reductions leave identical bits in every lane.
+__device__ __forceinline__ void warp_ms_fast(float &m, float &s, float c) {
+  const float mx = warp_max(m);
+  s = (m == -INFINITY) ? 0.f : s * ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+  s = warp_sum(s);
+  m = mx;
+}
+
+template <typename T>
+__device__ __forceinline__ void online8(const T *buf, int g, float c, float &m, float &s) {
+  float x[8];
+  load8(buf, g, x);
+  float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  if (mx > m) {
+    s = (m == -INFINITY) ? 0.f : s * ex2(__fmul_rn(m, c) - __fmul_rn(mx, c));
+    m = mx;
+  }
+  if (m == -INFINITY) return;
+  const float mc = __fmul_rn(m, c);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += ex2(fmaf(x[j], c, -mc));
+}
+
 // Block sum of a float-float value (result in every thread): butterflies
 // within each warp, then over the warp partials (identical bits everywhere).
 __device__ __forceinline__ ff warp_sum_ff(ff v) {
@@ -184,6 +265,17 @@ __device__ __forceinline__ int warp_max_s32(int v) {
   return r;
 }
 
+__device__ __forceinline__ ff ld_dsmem_ff(const ff *p, int rank) {
+  const uint32_t a = mapa(p, rank);
+  return ff{ld_dsmem_f32(a), ld_dsmem_f32(a + 4)};
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
 
 // warp maximum on the reduction unit (NaN inputs are ignored, like fmaxf)
 __device__ __forceinline__ float warp_max_redux(float v) {
@@ -198,11 +290,62 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
+// Thread-local maximum over groups g0, g0 + stride, ... of a slice. A maximum
+// is a selection, so the packed 16-bit forms are exact.
+template <typename T>
+__device__ __forceinline__ float slice_max(const T *buf, int g0, int n_grp, int stride);
+
+template <>
+__device__ __forceinline__ float slice_max<float>(const float *buf, int g0, int n_grp, int stride) {
+  float r0 = -INFINITY, r1 = -INFINITY;
+  const float4 *p = reinterpret_cast<const float4 *>(buf);
+  for (int g = g0; g < n_grp; g += stride) {
+    const float4 a = p[2 * g], b = p[2 * g + 1];
+    r0 = max3f(r0, a.x, a.y);
+    r1 = max3f(r1, a.z, a.w);
+    r0 = max3f(r0, b.x, b.y);
+    r1 = max3f(r1, b.z, b.w);
+  }
+  return fmaxf(r0, r1);
+}
+
 template <typename H2>
 __device__ __forceinline__ H2 as_h2(uint32_t w) {
   H2 h;
   memcpy(&h, &w, 4);
   return h;
+}
+
+template <>
+__device__ __forceinline__ float slice_max<__nv_bfloat16>(const __nv_bfloat16 *buf, int g0, int n_grp, int stride) {
+  const __nv_bfloat162 ninf = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+  __nv_bfloat162 r0 = ninf, r1 = ninf;
+  const uint4 *p = reinterpret_cast<const uint4 *>(buf);
+  for (int g = g0; g < n_grp; g += stride) {
+    const uint4 v = p[g];
+    r0 = __hmax2(r0, as_h2<__nv_bfloat162>(v.x));
+    r1 = __hmax2(r1, as_h2<__nv_bfloat162>(v.y));
+    r0 = __hmax2(r0, as_h2<__nv_bfloat162>(v.z));
+    r1 = __hmax2(r1, as_h2<__nv_bfloat162>(v.w));
+  }
+  r0 = __hmax2(r0, r1);
+  return fmaxf(__low2float(r0), __high2float(r0));
+}
+
+template <>
+__device__ __forceinline__ float slice_max<__half>(const __half *buf, int g0, int n_grp, int stride) {
+  const __half2 ninf = __floats2half2_rn(-INFINITY, -INFINITY);
+  __half2 r0 = ninf, r1 = ninf;
+  const uint4 *p = reinterpret_cast<const uint4 *>(buf);
+  for (int g = g0; g < n_grp; g += stride) {
+    const uint4 v = p[g];
+    r0 = __hmax2(r0, as_h2<__half2>(v.x));
+    r1 = __hmax2(r1, as_h2<__half2>(v.y));
+    r0 = __hmax2(r0, as_h2<__half2>(v.z));
+    r1 = __hmax2(r1, as_h2<__half2>(v.w));
+  }
+  r0 = __hmax2(r0, r1);
+  return fmaxf(__low2float(r0), __high2float(r0));
 }
 
 // Negated rounded reference -fl(m c) of a partial maximum (0 for an empty or
@@ -220,6 +363,17 @@ __device__ __forceinline__ void warp_ms(float &m, float &s, float c) {
   s = warp_sum(rescale(s, m, mx, c));
   m = mx;
 }
+
+// ------------------------------------------------------ statistics pass ---
+// sample_stats_kernel: one CTA per (8192-logit chunk, position, sequence).
+// Each thread holds 32 logits of the target row and of the draft row in
+// registers (16-byte loads, all issued before any arithmetic), takes exact
+// maxima, then sums of 2^(l c - fl(m c)) with the two rows paired in packed
+// fp32 arithmetic; the CTA's (max, sum) pairs go to the workspace. No
+// shared-memory staging and no cluster: a streaming reduction.
+constexpr int kStatThreads = 256;
+constexpr int kStatChunk = 8192;                               // logits per CTA per row
+constexpr int kStatGroups = kStatChunk / (8 * kStatThreads);   // groups of 8 per thread
 
 // raw bits of 8 logits: one 16-byte word for 16-bit types, two for f32
 template <typename T> struct Raw8 { uint4 w[sizeof(T) / 2]; };
@@ -299,6 +453,107 @@ __device__ __forceinline__ float max8(const Raw8<T> &r) {
   }
 }
 
+template <typename TT, int DK>
+__global__ void __launch_bounds__(kStatThreads) sample_stats_kernel(const __grid_constant__ SampleParams P) {
+  pdl_wait();
+  pdl_trigger();
+  using TD = typename std::conditional<DK == 0, TT, float>::type;
+  __shared__ float red[4][kStatThreads / 32];
+  const int c = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
+  const int K = P.K, V = P.V;
+  const bool q_logits = i < K && DK == 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float cl = P.c;
+  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
+  const TD *drow = q_logits ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
+  const int e0 = c * kStatChunk, e1 = min(V, e0 + kStatChunk);
+  if (tid == 0 && c == 0 && i == 0 && b == 0) P.fin_sync[2] = 0u;   // no sequence pending yet
+  const int g0 = e0 / 8, g1 = (e1 + 7) / 8;
+  const bool vec = P.aligned != 0;
+
+  Raw8<TT> rt[kStatGroups];
+  Raw8<TD> rd[kStatGroups];
+#pragma unroll
+  for (int k = 0; k < kStatGroups; ++k) {
+    const int g = g0 + tid + k * kStatThreads;
+    if (g < g1) {
+      rt[k] = raw_load(trow, g, e1, vec, false);
+      if (q_logits) rd[k] = raw_load(drow, g, e1, vec, false);
+    }
+  }
+  float mt = -INFINITY, md = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kStatGroups; ++k) {
+    if (g0 + tid + k * kStatThreads < g1) {
+      mt = fmaxf(mt, max8(rt[k]));
+      if (q_logits) md = fmaxf(md, max8(rd[k]));
+    }
+  }
+  float s_t = 0.f, s_d = 0.f;
+  {
+    const float2 cc = make_float2(cl, cl);
+    const float2 nm = make_float2(neg_ref(mt, cl), neg_ref(md, cl));
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+#pragma unroll
+    for (int k = 0; k < kStatGroups; ++k) {
+      if (g0 + tid + k * kStatThreads >= g1) continue;
+      float xt[8];
+      unpack8(rt[k], xt);
+      if (q_logits) {
+        float xd[8];
+        unpack8(rd[k], xd);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const float2 y0 = __ffma2_rn(make_float2(xt[j], xd[j]), cc, nm);
+          const float2 y1 = __ffma2_rn(make_float2(xt[j + 1], xd[j + 1]), cc, nm);
+          a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
+          a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
+        }
+      } else {
+        const float2 nt = make_float2(nm.x, nm.x);
+#pragma unroll
+        for (int j = 0; j < 8; j += 4) {
+          const float2 y0 = __ffma2_rn(make_float2(xt[j], xt[j + 1]), cc, nt);
+          const float2 y1 = __ffma2_rn(make_float2(xt[j + 2], xt[j + 3]), cc, nt);
+          a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
+          a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
+        }
+      }
+    }
+    if (q_logits) {
+      s_t = a0.x + a1.x;
+      s_d = a0.y + a1.y;
+    } else {
+      s_t = (a0.x + a0.y) + (a1.x + a1.y);
+    }
+  }
+  warp_ms(mt, s_t, cl);
+  if (q_logits) warp_ms(md, s_d, cl);
+  if (lane == 0) { red[0][warp] = mt; red[1][warp] = s_t; red[2][warp] = md; red[3][warp] = s_d; }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int nw = kStatThreads / 32;
+    float m1 = lane < nw ? red[0][lane] : -INFINITY, s1 = lane < nw ? red[1][lane] : 0.f;
+    float m2 = lane < nw ? red[2][lane] : -INFINITY, s2 = lane < nw ? red[3][lane] : 0.f;
+    warp_ms(m1, s1, cl);
+    if (q_logits) warp_ms(m2, s2, cl);
+    if (lane == 0) P.part[((int64_t)b * (K + 1) + i) * P.nc + c] = make_float4(m1, s1, m2, s2);
+  }
+}
+
+// ------------------------------------------------- decide and draw pass ---
+// sample_draw_kernel: one cluster per sequence. Every CTA combines the chunk
+// statistics of each row (lanes over chunks, the same order everywhere, so
+// every CTA holds the same bits) and the accept tests are evaluated in fp32
+// with their rounding certificates; CTA 0 writes every row's record. The
+// first position that rejects (or whose test is not certified) stops the
+// walk; only the row drawn from is read again: the residual of the first
+// certified rejection, or the bonus row when every draft is accepted. Its
+// weights w'(y) = max(0, e_p(y) - r e_q(y)) are formed from register loads
+// of each CTA's slice; block totals, warp totals and the cluster's prefix
+// locate v Z, the owning warp rescans one block, and the draw gets its own
+// certificate. Anything uncertified is left to the finish kernel.
+
 // sum of eight fp32 weights, pairwise in packed arithmetic
 __device__ __forceinline__ float sum8f(const float (&w)[8]) {
   const float2 a = __fadd2_rn(make_float2(w[0], w[1]), make_float2(w[2], w[3]));
@@ -351,20 +606,303 @@ __device__ __forceinline__ void draw_weights8(const Raw8<TT> &rt, const Raw8<TD>
   }
 }
 
+constexpr int kMaxDrawBlocks = 64;   // blocks of 32 groups per CTA slice (2048 groups)
+
+struct DrawShared {
+  int stop;               // 2 * position + (0: not certified, 1: certified rejection)
+  float row_m_p, row_s_p, row_m_q, row_s_q;
+  float pub_tot;          // this CTA's draw mass
+  float wsum[kRowWarps];  // per warp
+  float btot[kMaxDrawBlocks];   // per block of 32 groups
+};
+
+// combined (max, sum) of target (and draft) row i of sequence b: every lane
+// of the warp ends with the same bits
+// emitted tokens of sequence b: the n accepted drafts, then y, then -1
+__device__ __forceinline__ void write_outputs(const SampleParams &P, int b, int n, int y) {
+  const int K = P.K;
+  for (int j = 0; j <= K; ++j)
+    P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? y : -1);
+  P.num_acc[b] = n;
+}
+
+// hands sequence b to the finish grid, to be resolved from row `start` on
+__device__ __forceinline__ void push_pending(const SampleParams &P, int b, int start) {
+  const unsigned slot = atomicAdd(&P.fin_sync[2], 1u);
+  P.pend[slot] = make_int2(b, start);
+}
+
+__device__ __forceinline__ void row_stats(const SampleParams &P, int b, int i, bool q_logits, float &m_p, float &S_p,
+                                          float &m_q, float &S_q) {
+  const int lane = threadIdx.x & 31;
+  const float4 *pr = P.part + ((int64_t)b * (P.K + 1) + i) * P.nc;
+  m_p = -INFINITY; S_p = 0.f; m_q = -INFINITY; S_q = 0.f;
+  for (int c0 = 0; c0 < P.nc; c0 += 32) {
+    float a = -INFINITY, sa = 0.f, d = -INFINITY, sd = 0.f;
+    if (c0 + lane < P.nc) {
+      const float4 v = pr[c0 + lane];
+      a = v.x; sa = v.y; d = v.z; sd = v.w;
+    }
+    warp_ms(a, sa, P.c);
+    const float mp = fmaxf(m_p, a);
+    S_p = rescale(S_p, m_p, mp, P.c) + rescale(sa, a, mp, P.c);
+    m_p = mp;
+    if (q_logits) {
+      warp_ms(d, sd, P.c);
+      const float mq = fmaxf(m_q, d);
+      S_q = rescale(S_q, m_q, mq, P.c) + rescale(sd, d, mq, P.c);
+      m_q = mq;
+    }
+  }
+}
+
+template <typename TT, int DK>
+__global__ void __launch_bounds__(kRowThreads, 4) sample_draw_kernel(const __grid_constant__ SampleParams P) {
+  pdl_wait();
+  pdl_trigger();
+  using TD = typename std::conditional<DK == 0, TT, float>::type;
+  __shared__ DrawShared sh;
+
+  const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+  const int b = blockIdx.y;
+  const int K = P.K, V = P.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float c = P.c;
+  const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
+  if (tid == 0) sh.stop = 2 * K + 1;
+  if (tid == 0 && blockIdx.x == 0 && b == 0) P.fin_sync[0] = 0u;   // the finish grid barrier starts empty
+  __syncthreads();
+
+  // ---- accept tests of every draft position --------------------------------
+  for (int i = warp; i < K; i += kRowWarps) {
+    float m_p, S_p, m_q, S_q;
+    row_stats(P, b, i, DK == 0, m_p, S_p, m_q, S_q);
+    if (DK != 0) { m_q = 0.f; S_q = 1.f; }
+    int x = P.tokens[(int64_t)b * K + i];
+    if (x < 0 || x >= V) {
+      if (rank == 0 && lane == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+      x = min(max(x, 0), V - 1);
+    }
+    const float lp_x = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + i) * V + x]);
+    const float lq_x = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + i) * V + x]);
+    const float u = P.uniforms[((int64_t)b * (K + 1) + i) * 2];
+    const bool finite = fabsf(m_p) <= 3.0e38f && (DK != 0 || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
+    const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
+    const float p_x = ex2(fmaf(lp_x, c, -mcp)) / S_p;
+    const float q_x = DK == 0 ? ex2(fmaf(lq_x, c, -mcq)) / S_q : lq_x;
+    const float lhs = u * q_x;
+    const bool accept = lhs < p_x;
+    // p_x and u q_x each carry < 2e-6 relative rounding (exp2, argument
+    // rounding, row sums): a decision this far from the boundary is exact
+    const bool acc_cert = fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f && finite;
+    if (lane == 0) {
+      if (!acc_cert) atomicMin(&sh.stop, 2 * i);
+      else if (!accept) atomicMin(&sh.stop, 2 * i + 1);
+      if (rank == 0) {
+        RowRec *rec = P.recs + (int64_t)b * (K + 1) + i;
+        if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
+        rec->m_p = m_p; rec->s_p = S_p; rec->m_q = m_q; rec->s_q = S_q;
+        rec->p_x = p_x; rec->q_x = q_x;
+        rec->y = -1; rec->y_exact = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
+        rec->flags = (accept ? REC_ACCEPT : 0u) | (acc_cert ? REC_ACC_CERT : 0u);
+        if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
+        if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
+      }
+    }
+  }
+  __syncthreads();
+  const int stop = sh.stop;
+  // the row drawn from: a certified rejection, or the bonus row (K)
+  const bool certain = (stop & 1) != 0;
+  const int n = stop >> 1;
+  const bool has_draft = n < K;
+  const bool q_logits = has_draft && DK == 0;
+  if (warp == 0 && certain) {   // statistics of the row drawn from
+    float m_p, S_p, m_q, S_q;
+    row_stats(P, b, n, q_logits, m_p, S_p, m_q, S_q);
+    if (!q_logits) { m_q = 0.f; S_q = 1.f; }
+    if (lane == 0) { sh.row_m_p = m_p; sh.row_s_p = S_p; sh.row_m_q = m_q; sh.row_s_q = S_q; }
+  }
+  if (warp == 1 && rank == 0) {
+    // the bonus row's record (the finish kernel may walk to it)
+    float m_p, S_p, m_q, S_q;
+    row_stats(P, b, K, false, m_p, S_p, m_q, S_q);
+    if (lane == 0) {
+      RowRec *rec = P.recs + (int64_t)b * (K + 1) + K;
+      rec->m_p = m_p; rec->s_p = S_p; rec->m_q = 0.f; rec->s_q = 1.f;
+      rec->p_x = 0.f; rec->q_x = 0.f;
+      rec->y = -1; rec->y_exact = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
+      rec->flags = 0u;
+      if (!(fabsf(m_p) <= 3.0e38f && S_p > 0.f)) atomic_or_status(P.status, SV_DEV_NONFINITE);
+    }
+  }
+  __syncthreads();
+  // identical in every CTA of the cluster: no shared memory of a peer is
+  // read on this path
+  if (!certain || force) {   // the first uncertified accept test (or all, forced)
+    if (rank == 0 && tid == 0) push_pending(P, b, force ? 0 : n);
+    return;
+  }
+  const float m_p = sh.row_m_p, S_p = sh.row_s_p, m_q = sh.row_m_q, S_q = sh.row_s_q;
+  const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
+
+  // ---- the draw: this CTA's slice of row n, straight into registers -------
+  // The slice is groups [gs0, gs1) of eight elements; warp w takes blocks
+  // [w bpw, (w+1) bpw) of 32 consecutive groups (lane l: group 32 k + l of
+  // the block), so element order is (warp, block, lane, element).
+  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + n) * V;
+  const TD *drow = has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + n) * V : nullptr;
+  const int ngr = (V + 7) >> 3;
+  const int gs0 = min(ngr, rank * P.gpc), gs1 = min(ngr, gs0 + P.gpc);
+  const int nblk = (gs1 - gs0 + 31) >> 5;
+  const int bpw = (nblk + kRowWarps - 1) / kRowWarps;
+  const bool vec = P.aligned != 0;
+  const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
+  const float r_pq = q_logits ? S_p / S_q : S_p;
+  const float v_u = P.uniforms[((int64_t)b * (K + 1) + n) * 2 + 1];
+  constexpr int kFly = sizeof(TT) == 4 || sizeof(TD) == 4 ? 2 : 4;   // blocks in flight per warp
+  for (int k0 = warp * bpw; k0 < min(nblk, (warp + 1) * bpw); k0 += kFly) {
+    Raw8<TT> rt[kFly];
+    Raw8<TD> rd[kFly];
+#pragma unroll
+    for (int f = 0; f < kFly; ++f) {
+      const int g = gs0 + (k0 + f) * 32 + lane;
+      if (k0 + f < (warp + 1) * bpw && g < gs1) {
+        rt[f] = raw_load(trow, g, V, vec, false);
+        if (has_draft) rd[f] = raw_load(drow, g, V, vec, DK == 1);
+      }
+    }
+#pragma unroll
+    for (int f = 0; f < kFly; ++f) {
+      const int k = k0 + f;
+      if (k >= min(nblk, (warp + 1) * bpw)) break;
+      float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (gs0 + k * 32 + lane < gs1) draw_weights8<TT, TD, DK>(rt[f], rd[f], has_draft, c, mcp, mcq, r_pq, w);
+      const float t = warp_sum_f(sum8f(w));
+      if (lane == 0) sh.btot[k] = t;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {   // warp totals (blocks in order), then the CTA's
+    float t = 0.f;
+    if (lane < kRowWarps)
+      for (int k = lane * bpw; k < min(nblk, (lane + 1) * bpw); ++k) t += sh.btot[k];
+    if (lane < kRowWarps) sh.wsum[lane] = t;
+    __syncwarp();
+    if (lane == 0) {
+      float tc = 0.f;
+      for (int w = 0; w < kRowWarps; ++w) tc += sh.wsum[w];
+      sh.pub_tot = tc;
+    }
+  }
+  cluster_sync();   // masses published
+  const float tot_cta = sh.pub_tot;
+  const float t_r = lane < cs ? ld_dsmem_f32(mapa(&sh.pub_tot, lane)) : 0.f;
+  // the last distributed read of this launch is done: arrive now, wait at exit
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  float off_c = 0.f, Z = 0.f;
+  for (int rr = 0; rr < cs; ++rr) {
+    const float t = __shfl_sync(0xffffffffu, t_r, rr);
+    if (rr == rank) off_c = Z;
+    Z += t;
+  }
+  const float thr = v_u * Z;
+  // rounding bound of the fp32 CDF near thr, in units of w' = S_p w:
+  // per-element exp / argument / ratio errors (~2^-22 relative, random:
+  // sqrt(sum p^2) <= sqrt(max p) = sqrt(1/S)), and the rounding of the
+  // running sums (~2^-24 per addition)
+  const float e_abs = 4.7683716e-07f * S_p * sqrtf(1.f / S_p + (q_logits ? 1.f / S_q : 0.f)) +
+                      1.1920929e-07f * (Z + S_p);   // 2^-21, 2^-23
+  const bool draw_ok = finite && Z > 0.f && thr < Z;
+  RowRec *rec = P.recs + (int64_t)b * (K + 1) + n;
+  const uint32_t acc_flags = has_draft ? REC_ACC_CERT : 0u;   // a certified rejection (or the bonus row)
+  if (rank == 0 && tid == 0) {
+    rec->z = Z; rec->e_abs = e_abs;
+    if (!draw_ok) { rec->y = -1; rec->gap = 0.f; rec->flags = acc_flags; push_pending(P, b, n); }
+  }
+  if (draw_ok && off_c <= thr && thr < off_c + tot_cta) {
+    // the owner warp and block (prefixes in element order), the same in
+    // every thread of the CTA
+    float base = off_c;
+    int ow = kRowWarps - 1;
+    for (int w = 0; w < kRowWarps; ++w) {
+      if (thr < base + sh.wsum[w] || w == kRowWarps - 1) { ow = w; break; }
+      base += sh.wsum[w];
+    }
+    const int kb0 = ow * bpw, kb1 = min(nblk, (ow + 1) * bpw);
+    int ob = max(kb0, kb1 - 1);
+    for (int k = kb0; k < kb1; ++k) {
+      if (thr < base + sh.btot[k] || k == kb1 - 1) { ob = k; break; }
+      base += sh.btot[k];
+    }
+    if (warp == ow) {
+      // rescan of block ob: lane sums, their prefix, then the crossing lane's
+      // eight elements in order
+      const int g = gs0 + ob * 32 + lane;
+      float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (ob < kb1 && g < gs1) {
+        Raw8<TT> rt = raw_load(trow, g, V, vec, false);
+        Raw8<TD> rd;
+        if (has_draft) rd = raw_load(drow, g, V, vec, DK == 1);
+        draw_weights8<TT, TD, DK>(rt, rd, has_draft, c, mcp, mcq, r_pq, w);
+      }
+      const float vs = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+      float inc2 = vs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, inc2, o);
+        if (lane >= o) inc2 += t;
+      }
+      const unsigned h2 = __ballot_sync(0xffffffffu, g < gs1 && base + inc2 > thr);
+      int y = -1;
+      float c_lo = 0.f, c_hi = 0.f;
+      if (h2) {
+        const int L2 = __ffs(h2) - 1;
+        if (lane == L2) {
+          float run_c = base + (inc2 - vs);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float nxt = run_c + w[j];
+            if (y < 0 && nxt > thr) { y = 8 * g + j; c_lo = run_c; c_hi = nxt; }
+            run_c = nxt;
+          }
+        }
+        y = __shfl_sync(0xffffffffu, y, L2);
+        c_lo = __shfl_sync(0xffffffffu, c_lo, L2);
+        c_hi = __shfl_sync(0xffffffffu, c_hi, L2);
+      }
+      if (lane == 0) {
+        const bool found = y >= 0 && y < V;   // else: rounding moved the crossing
+        const float gap = found ? fminf(thr - c_lo, c_hi - thr) : 0.f;
+        const bool cert = found && gap > e_abs;
+        rec->y = found ? y : -1;
+        rec->gap = gap;
+        rec->flags = acc_flags | (cert ? REC_DRAW_CERT : 0u);
+        if (cert) write_outputs(P, b, n, y);
+        else push_pending(P, b, n);
+      }
+    }
+  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------- float-float re-evaluation ---
 // Lean float-float exp: exp((l - m)/T) for l <= m as an unevaluated pair
 // hi + lo with ~1e-9 relative error: t = (l - m) log2(e) split into
 // n/64 + r (|r| <= 1/128), 2^r - 1 by its Taylor series to r^5, 2^(j/64)
 // from the (hi, lo) table, 2^k by exponent construction. Values below e^-87
 // relative to the row maximum are returned as 0.
-// The float-float pass runs rarely, with the instruction cache cold for its
-// code, so the exponential and the weights are single out-of-line copies
+// The finish grid runs its code once per call, with the instruction cache
+// cold, so the exponential and the weights are single out-of-line copies
 // called from rolled loops.
 struct FfK {
   float inv_hi, inv_lo;     // 1/T
   float l2e_hi, l2e_lo;     // log2(e)
   int unitT;                // T == 1
 };
+__device__ __forceinline__ FfK ff_consts(const SampleParams &P) {
+  return FfK{P.invT_hi, P.invT_lo, P.log2e_hi, P.log2e_lo, P.unitT};
+}
 
 __device__ __noinline__ ff ffx_exp(float l, float m, FfK k, const float2 *tbl) {
   if (!(l > -INFINITY)) return ff{0.f, 0.f};
@@ -392,6 +930,36 @@ __device__ __forceinline__ void acc_add(ff &a, ff v) {
 
 __device__ __forceinline__ ff ff_norm(ff a) { return quick_two_sum(a.hi, a.lo); }
 
+// ------------------------------------------------ cooperative finish pass ---
+// sample_finish_kernel: one CTA per SM, launched cooperatively (all CTAs
+// resident), so the grid can meet at barriers.
+//   * Every CTA walks every sequence's records (certified accepts, then the
+//     first rejection or the bonus row) and builds the same ordered list of
+//     sequences whose walk reaches a decision that is not certified; the
+//     tokens of the others are written by CTA b % gridDim.x.
+//   * Listed sequences are resolved in rounds. A round takes, for each one,
+//     the rows its walk may still need (uncertified accept tests and the row
+//     it ends on), at most kMaxUnits rows in all, and evaluates them together:
+//     every CTA sums e_p and e_q over its contiguous chunk of each row ->
+//     grid barrier -> every CTA forms the same row sums, takes the exact
+//     accept tests in walk order, picks each sequence's draw row and sums its
+//     residual weights over the chunk -> grid barrier -> every CTA forms the
+//     same prefix over chunks; the CTA whose chunk holds v Z finds the token
+//     and writes that sequence's outputs. Sequences whose rows ran past the
+//     round's budget continue in the next round.
+// Cross-CTA values go through the workspace and are read from L2; every CTA
+// combines them in the same order, so all CTAs take the same decisions.
+constexpr int kFinThreads = 512;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kMaxEntries = 32;     // sequences resolved together
+constexpr int kMaxUnits = 32;       // rows evaluated per round
+constexpr int kMaxFinCtas = 160;    // CTAs of the finish grid (one per SM)
+static_assert(kMaxUnits >= kMaxEntries && kMaxUnits <= 2 * kFinWarps, "unit slots per warp");
+
+// sequence phases: walk its records from e_i, redraw row e_i from p (zero
+// residual mass), or finished
+enum : int { ENT_WALK = 0, ENT_REDRAW = 1, ENT_DONE = 2 };
+
 // float-float weight of one element (target logit lp, draft value lq) of the
 // row drawn from: mode 0 the target row (e_p), 1 two softmaxes
 // (max(0, e_p S_q - e_q S_p)), 2 given draft probabilities
@@ -404,859 +972,534 @@ __device__ __noinline__ ff resid_weight(int mode, float lp, float lq, float m_p,
   return ff_max0(ff_add(ep, ff_neg(ff_mul(ff{lq > -INFINITY ? lq : 0.f, 0.f}, Sp))));
 }
 
-// ------------------------------------------------- cross-CTA signalling ---
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-// Thread 0 polls *ctr until it reaches target (acquire), at most the wait
-// limit; every thread of the CTA gets the result through *flag. Counters are
-// zeroed for each call and only grow.
-__device__ __forceinline__ bool cta_wait_geq(const unsigned *ctr, unsigned target, unsigned *flag) {
+// Grid barrier of the cooperative launch: one arrival count in global memory
+// (zeroed before the launch); barrier j of the launch completes when the
+// count reaches j * gridDim.x, so the count is never reset. Bounded wait
+// (limit_ns); returns false after a timeout. (Test hook: withheld, this
+// CTA does not arrive, so every CTA's wait runs out.)
+__device__ __forceinline__ bool grid_sync(unsigned *count, unsigned &target, int *flag, uint64_t limit_ns,
+                                          bool withhold) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned ok = 1u;
+    bool ok = true;
+    target += gridDim.x;
+    __threadfence();
+    if (!withhold) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
     const uint64_t t0 = global_ns();
-    while (ld_acquire(ctr) < target) {
-      if (global_ns() - t0 > kWaitLimitNs) { ok = 0u; break; }
-      __nanosleep(64);
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+      if ((int)(v - target) >= 0) break;
+      if (global_ns() - t0 > limit_ns) { ok = false; break; }
+      __nanosleep(16);
     }
-    *flag = ok;
-  }
-  __syncthreads();
-  return *flag != 0u;
-}
-
-// The CTA's global writes so far become visible to whoever sees the count.
-__device__ __forceinline__ void cta_arrive(unsigned *ctr) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) red_release_add(ctr, 1u);
-}
-
-// sequence b is left to the float-float kernel, from row i0 on
-__device__ __forceinline__ void push_pending(const SampleParams &P, int b, int i0) {
-  const unsigned slot = atomicAdd(P.sync + SYNC_PCOUNT, 1u);
-  P.pend[slot] = make_int2(b, i0);
-}
-
-// emitted tokens of sequence b: the n accepted drafts, then y, then -1
-__device__ __forceinline__ void write_outputs(const SampleParams &P, int b, int n, int y) {
-  const int K = P.K;
-  for (int j = 0; j <= K; ++j)
-    P.out_tokens[(int64_t)b * (K + 1) + j] = j < n ? P.tokens[(int64_t)b * K + j] : (j == n ? y : -1);
-  P.num_acc[b] = n;
-}
-
-struct FusedShared {
-  int kind, b, i, c;            // the decoded ticket (kind 0 statistics, 1 draw, -1 none)
-  unsigned flag;                // result of thread 0's wait
-  int last;                     // this CTA was the last of its kind to arrive for the sequence
-  float red[4][kFWarps];        // statistics reductions
-  float4 rs[kMaxPos];           // decision: (m_p, S_p, m_q, S_q) of every row of the sequence
-  int rfl[kMaxPos];             // decision: accept test, bit 0 accepted, bit 1 certified
-  float btot[kFWarps][kGrp];    // draw: block totals
-};
-
-// ------------------------------------------------------ statistics item ---
-
-// combined (max, sum) of target (and draft) row i of sequence b from its
-// chunk pairs: every lane of the warp ends with the same bits
-__device__ __forceinline__ void row_stats(const SampleParams &P, int b, int i, bool q_logits, float &m_p, float &S_p,
-                                          float &m_q, float &S_q) {
-  const int lane = threadIdx.x & 31;
-  const float4 *pr = P.part + ((int64_t)b * (P.K + 1) + i) * P.nc;
-  m_p = -INFINITY; S_p = 0.f; m_q = -INFINITY; S_q = 0.f;
-  for (int c0 = 0; c0 < P.nc; c0 += 32) {
-    float a = -INFINITY, sa = 0.f, d = -INFINITY, sd = 0.f;
-    if (c0 + lane < P.nc) {
-      const float4 v = __ldcg(pr + c0 + lane);
-      a = v.x; sa = v.y; d = v.z; sd = v.w;
-    }
-    warp_ms(a, sa, P.c);
-    const float mp = fmaxf(m_p, a);
-    S_p = rescale(S_p, m_p, mp, P.c) + rescale(sa, a, mp, P.c);
-    m_p = mp;
-    if (q_logits) {
-      warp_ms(d, sd, P.c);
-      const float mq = fmaxf(m_q, d);
-      S_q = rescale(S_q, m_q, mq, P.c) + rescale(sd, d, mq, P.c);
-      m_q = mq;
-    }
-  }
-}
-
-// The decisions of sequence b, taken once by the last statistics CTA of the
-// sequence: every row's statistics, the accept tests in fp32 with their
-// certificates, and the walk (the first rejection stops it; an uncertified
-// test sends the sequence to the float-float kernel from that row on). The
-// row drawn from is published for the draw items.
-template <typename TT, int DK>
-__device__ __noinline__ void decide(const SampleParams &P, FusedShared &sh, int b) {
-  using TD = typename std::conditional<DK == 0, TT, float>::type;
-  const int K = P.K, V = P.V;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float cl = P.c;
-  for (int i = warp; i <= K; i += kFWarps) {
-    const bool ql = i < K && DK == 0;
-    float m_p, S_p, m_q, S_q;
-    row_stats(P, b, i, ql, m_p, S_p, m_q, S_q);
-    if (!ql) { m_q = 0.f; S_q = 1.f; }
-    const bool finite = fabsf(m_p) <= 3.0e38f && (!ql || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
-    int fl = 0;
-    if (i < K) {
-      int x = P.tokens[(int64_t)b * K + i];
-      if (x < 0 || x >= V) {
-        if (lane == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
-        x = min(max(x, 0), V - 1);
-      }
-      const float lp_x = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + i) * V + x]);
-      const float lq_x = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + i) * V + x]);
-      const float u = P.uniforms[((int64_t)b * (K + 1) + i) * 2];
-      const float mcp = __fmul_rn(m_p, cl), mcq = __fmul_rn(m_q, cl);
-      const float p_x = ex2(fmaf(lp_x, cl, -mcp)) / S_p;
-      const float q_x = DK == 0 ? ex2(fmaf(lq_x, cl, -mcq)) / S_q : lq_x;
-      const float lhs = u * q_x;
-      const bool accept = lhs < p_x;
-      // p_x and u q_x each carry < 2e-6 relative rounding (exp2, argument
-      // rounding, row sums): a decision this far from the boundary is exact
-      const bool cert = fabsf(p_x - lhs) > 4e-6f * fmaxf(p_x, lhs) && p_x > 0.f && q_x > 0.f && finite;
-      fl = (accept ? 1 : 0) | (cert ? 2 : 0);
-      if (lane == 0) {
-        if (P.p_at) P.p_at[(int64_t)b * K + i] = p_x;
-        if (P.q_at) P.q_at[(int64_t)b * K + i] = q_x;
-      }
-    }
-    if (lane == 0) {
-      if (!finite) atomic_or_status(P.status, SV_DEV_NONFINITE);
-      sh.rs[i] = make_float4(m_p, S_p, m_q, S_q);
-      sh.rfl[i] = fl;
-      P.rowrec[(int64_t)b * (K + 1) + i] = make_float4(m_p, S_p, m_q, S_q);
-      P.rowflag[(int64_t)b * (K + 1) + i] = fl;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int n = K, unc = -1;
-    for (int i = 0; i < K; ++i) {
-      const int fl = sh.rfl[i];
-      if (!(fl & 2)) { unc = i; break; }
-      if (!(fl & 1)) { n = i; break; }
-    }
-    if (P.flags & SV_SAMPLE_FORCE_EXACT) unc = 0;
-    const float4 r = sh.rs[n];
-    const bool finite = fabsf(r.x) <= 3.0e38f && fabsf(r.z) <= 3.0e38f && r.y > 0.f;
-    int state = DEC_DRAW;
-    if (unc >= 0 || !finite) {
-      state = DEC_EXACT;
-      push_pending(P, b, unc >= 0 ? unc : n);
-    }
-    P.dec[b] = make_int2(n, state);
     __threadfence();
-    st_release(P.seq + (size_t)b * SEQ_WORDS + SEQ_DEC, 1u);
-  }
-}
-
-// (chunk c, position i) of sequence b: each thread holds 32 logits of the
-// target row and of the draft row in registers (16-byte loads, all issued
-// before any arithmetic), takes exact maxima, then sums of
-// 2^(l c - fl(m c)) with the two rows paired in packed fp32 arithmetic.
-template <typename TT, int DK>
-__device__ __forceinline__ void stats_item(const SampleParams &P, FusedShared &sh, int b, int i, int c) {
-  using TD = typename std::conditional<DK == 0, TT, float>::type;
-  const int K = P.K, V = P.V;
-  const bool q_logits = i < K && DK == 0;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float cl = P.c;
-  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + i) * V;
-  const TD *drow = q_logits ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + i) * V : nullptr;
-  const int e0 = c * kChunk, e1 = min(V, e0 + kChunk);
-  const int g0 = e0 / 8, g1 = (e1 + 7) / 8;
-  const bool vec = P.aligned != 0;
-
-  Raw8<TT> rt[kGrp];
-  Raw8<TD> rd[kGrp];
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-    const int g = g0 + tid + k * kFThreads;
-    if (g < g1) {
-      rt[k] = raw_load(trow, g, e1, vec, false);
-      if (q_logits) rd[k] = raw_load(drow, g, e1, vec, false);
-    }
-  }
-  float mt = -INFINITY, md = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-    if (g0 + tid + k * kFThreads < g1) {
-      mt = fmaxf(mt, max8(rt[k]));
-      if (q_logits) md = fmaxf(md, max8(rd[k]));
-    }
-  }
-  float s_t = 0.f, s_d = 0.f;
-  {
-    const float2 cc = make_float2(cl, cl);
-    const float2 nm = make_float2(neg_ref(mt, cl), neg_ref(md, cl));
-    float2 a0 = make_float2(0.f, 0.f), a1 = a0;
-#pragma unroll
-    for (int k = 0; k < kGrp; ++k) {
-      if (g0 + tid + k * kFThreads >= g1) continue;
-      float xt[8];
-      unpack8(rt[k], xt);
-      if (q_logits) {
-        float xd[8];
-        unpack8(rd[k], xd);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          const float2 y0 = __ffma2_rn(make_float2(xt[j], xd[j]), cc, nm);
-          const float2 y1 = __ffma2_rn(make_float2(xt[j + 1], xd[j + 1]), cc, nm);
-          a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
-          a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
-        }
-      } else {
-        const float2 nt = make_float2(nm.x, nm.x);
-#pragma unroll
-        for (int j = 0; j < 8; j += 4) {
-          const float2 y0 = __ffma2_rn(make_float2(xt[j], xt[j + 1]), cc, nt);
-          const float2 y1 = __ffma2_rn(make_float2(xt[j + 2], xt[j + 3]), cc, nt);
-          a0 = __fadd2_rn(a0, make_float2(ex2(y0.x), ex2(y0.y)));
-          a1 = __fadd2_rn(a1, make_float2(ex2(y1.x), ex2(y1.y)));
-        }
-      }
-    }
-    if (q_logits) {
-      s_t = a0.x + a1.x;
-      s_d = a0.y + a1.y;
-    } else {
-      s_t = (a0.x + a0.y) + (a1.x + a1.y);
-    }
-  }
-  warp_ms(mt, s_t, cl);
-  if (q_logits) warp_ms(md, s_d, cl);
-  if (lane == 0) { sh.red[0][warp] = mt; sh.red[1][warp] = s_t; sh.red[2][warp] = md; sh.red[3][warp] = s_d; }
-  __syncthreads();
-  if (warp == 0) {
-    float m1 = lane < kFWarps ? sh.red[0][lane] : -INFINITY, s1 = lane < kFWarps ? sh.red[1][lane] : 0.f;
-    float m2 = lane < kFWarps ? sh.red[2][lane] : -INFINITY, s2 = lane < kFWarps ? sh.red[3][lane] : 0.f;
-    warp_ms(m1, s1, cl);
-    if (q_logits) warp_ms(m2, s2, cl);
-    if (lane == 0) {
-      P.part[((int64_t)b * (K + 1) + i) * P.nc + c] = make_float4(m1, s1, m2, s2);
-      __threadfence();
-      const unsigned NS = (unsigned)(P.nc * (K + 1));
-      sh.last = atom_add_acq_rel(P.seq + (size_t)b * SEQ_WORDS + SEQ_STATS, 1u) == NS - 1;
-    }
+    *flag = ok ? 1 : 0;
   }
   __syncthreads();
-  if (sh.last) decide<TT, DK>(P, sh, b);
+  return *flag != 0;
 }
 
-// ------------------------------------------------------------ draw item ---
-
-// Group gbase + 32 k (k < kGrp) of chunk c is lane `lane`'s group of block
-// k of warp `warp`: element order within a chunk is (warp, block, lane,
-// element), i.e. token order.
-__device__ __forceinline__ int draw_gbase(int c, int warp, int lane) {
-  return c * kChunkGroups + warp * (32 * kGrp) + lane;
+__device__ __forceinline__ ff ldcg_ff(const float2 *p) {
+  const float2 v = __ldcg(p);
+  return ff{v.x, v.y};
 }
 
-// weights and totals the draw of sequence b shares between its items
-struct DrawRow {
-  int n;
-  bool has_draft, q_logits, finite;
-  float m_p, S_p, m_q, S_q, mcp, mcq, r_pq;
-};
-
-__device__ __forceinline__ DrawRow draw_row(const SampleParams &P, int b, int n, int DK) {
-  DrawRow d;
-  d.n = n;
-  d.has_draft = n < P.K;
-  d.q_logits = d.has_draft && DK == 0;
-  const float4 r = __ldcg(P.rowrec + (int64_t)b * (P.K + 1) + n);
-  d.m_p = r.x; d.S_p = r.y; d.m_q = r.z; d.S_q = r.w;
-  d.finite = fabsf(d.m_p) <= 3.0e38f && (!d.q_logits || fabsf(d.m_q) <= 3.0e38f) && d.S_p > 0.f;
-  d.mcp = __fmul_rn(d.m_p, P.c);
-  d.mcq = __fmul_rn(d.m_q, P.c);
-  d.r_pq = d.q_logits ? d.S_p / d.S_q : d.S_p;
-  return d;
-}
-
-// The token of sequence b, found by the last of its draw items: the prefix
-// of the chunk totals locates v Z, the per-warp totals of that chunk the
-// warp, and one warp reloads that warp's 1024 logits (from L2) to find the
-// block, the lane and the element. The draw is certified against its
-// rounding bound, or the sequence goes to the float-float kernel.
-template <typename TT, int DK>
-__device__ __noinline__ void locate(const SampleParams &P, int b, const DrawRow &d) {
-  using TD = typename std::conditional<DK == 0, TT, float>::type;
-  const int K = P.K, V = P.V, nc = P.nc;
-  const int lane = threadIdx.x & 31;
-  const float cl = P.c;
-  const float *wt = P.wtot + (int64_t)b * nc * kWtStride;
-  const float t_r = lane < nc ? __ldcg(wt + lane * kWtStride + kFWarps) : 0.f;
-  float Z = 0.f;
-  for (int rr = 0; rr < nc; ++rr) Z += __shfl_sync(0xffffffffu, t_r, rr);
-  const float v_u = P.uniforms[((int64_t)b * (K + 1) + d.n) * 2 + 1];
-  const float thr = v_u * Z;
-  float o = 0.f, base = 0.f;
-  int own = -1;
-  for (int rr = 0; rr < nc; ++rr) {
-    const float t = __shfl_sync(0xffffffffu, t_r, rr);
-    if (own < 0 && t > 0.f && o <= thr && thr < o + t) { own = rr; base = o; }
-    o += t;
-  }
-  if (!(d.finite && Z > 0.f && own >= 0)) {   // zero mass, non-finite, or rounding
-    if (lane == 0) push_pending(P, b, d.n);
-    return;
-  }
-  // the warp of the owner chunk (per-warp totals in order)
-  const float wv = lane < kFWarps ? __ldcg(wt + own * kWtStride + lane) : 0.f;
-  int ow = kFWarps - 1;
-  for (int w = 0; w < kFWarps; ++w) {
-    const float t = __shfl_sync(0xffffffffu, wv, w);
-    if (thr < base + t || w == kFWarps - 1) { ow = w; break; }
-    base += t;
-  }
-  // that warp's four blocks of 32 groups, from L2
-  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + d.n) * V;
-  const TD *drow = d.has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + d.n) * V : nullptr;
-  const int ngr = (V + 7) >> 3;
-  const bool vec = P.aligned != 0;
-  const int gb = draw_gbase(own, ow, lane);
-  Raw8<TT> rt[kGrp];
-  Raw8<TD> rd[kGrp];
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-    const int g = gb + 32 * k;
-    if (g < ngr) {
-      rt[k] = raw_load(trow, g, V, vec, false);
-      if (d.has_draft) rd[k] = raw_load(drow, g, V, vec, DK == 1);
-    }
-  }
-  float ls[kGrp], w8[kGrp][8];
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w8[k][j] = 0.f;
-    if (gb + 32 * k < ngr) draw_weights8<TT, TD, DK>(rt[k], rd[k], d.has_draft, cl, d.mcp, d.mcq, d.r_pq, w8[k]);
-    ls[k] = sum8f(w8[k]);
-  }
-  int ob = kGrp - 1;
-  float vs = ls[kGrp - 1];
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-    const float t = warp_sum_f(ls[k]);
-    if (ob == kGrp - 1 && k < kGrp - 1) {
-      if (thr < base + t) { ob = k; vs = ls[k]; }
-      else base += t;
-    }
-  }
-  // the lane, then the element, within block ob
-  const int g = gb + 32 * ob;
-  float inc = vs;
-#pragma unroll
-  for (int s = 1; s < 32; s <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, inc, s);
-    if (lane >= s) inc += t;
-  }
-  const unsigned hit = __ballot_sync(0xffffffffu, g < ngr && base + inc > thr);
-  int y = -1;
-  float c_lo = 0.f, c_hi = 0.f;
-  if (hit) {
-    const int L = __ffs(hit) - 1;
-    if (lane == L) {
-      float run_c = base + (inc - vs);
-#pragma unroll
-      for (int k = 0; k < kGrp; ++k) {
-        if (k != ob) continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float nxt = run_c + w8[k][j];
-          if (y < 0 && nxt > thr) { y = 8 * g + j; c_lo = run_c; c_hi = nxt; }
-          run_c = nxt;
-        }
-      }
-    }
-    y = __shfl_sync(0xffffffffu, y, L);
-    c_lo = __shfl_sync(0xffffffffu, c_lo, L);
-    c_hi = __shfl_sync(0xffffffffu, c_hi, L);
-  }
-  if (lane == 0) {
-    // rounding bound of the fp32 CDF near thr, in units of w' = S_p w:
-    // per-element exp / argument / ratio errors (~2^-22 relative, random:
-    // sqrt(sum p^2) <= sqrt(max p) = sqrt(1/S)), and the rounding of the
-    // running sums (~2^-24 per addition)
-    const float e_abs = 4.7683716e-07f * d.S_p * sqrtf(1.f / d.S_p + (d.q_logits ? 1.f / d.S_q : 0.f)) +
-                        1.1920929e-07f * (Z + d.S_p);   // 2^-21, 2^-23
-    const bool found = y >= 0 && y < V;   // else: rounding moved the crossing
-    const float gap = found ? fminf(thr - c_lo, c_hi - thr) : 0.f;
-    if (found && gap > e_abs) write_outputs(P, b, d.n, y);
-    else push_pending(P, b, d.n);
-  }
-}
-
-// (chunk c) of sequence b: once the sequence's decisions are out, the chunk
-// of the row drawn from (the residual max(0, p - q) of the first rejection,
-// or the bonus row) is streamed into registers, its weights summed per warp;
-// the last draw item of the sequence locates the token.
-template <typename TT, int DK>
-__device__ __forceinline__ void draw_item(const SampleParams &P, FusedShared &sh, int b, int c) {
-  using TD = typename std::conditional<DK == 0, TT, float>::type;
-  const int K = P.K, V = P.V, nc = P.nc;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  unsigned *sq = P.seq + (size_t)b * SEQ_WORDS;
-  if (!cta_wait_geq(sq + SEQ_DEC, 1u, &sh.flag)) {
-    if (tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-    return;
-  }
-  const int2 dec = __ldcg(P.dec + b);
-  if (dec.y != DEC_DRAW) return;
-  const DrawRow d = draw_row(P, b, dec.x, DK);
-  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + d.n) * V;
-  const TD *drow = d.has_draft ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + d.n) * V : nullptr;
-  const int ngr = (V + 7) >> 3;
-  const bool vec = P.aligned != 0;
-  const int gb = draw_gbase(c, warp, lane);
-  Raw8<TT> rt[kGrp];
-  Raw8<TD> rd[kGrp];
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-    const int g = gb + 32 * k;
-    if (g < ngr) {
-      rt[k] = raw_load(trow, g, V, vec, false);
-      if (d.has_draft) rd[k] = raw_load(drow, g, V, vec, DK == 1);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kGrp; ++k) {
-    float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (gb + 32 * k < ngr) draw_weights8<TT, TD, DK>(rt[k], rd[k], d.has_draft, P.c, d.mcp, d.mcq, d.r_pq, w);
-    const float t = warp_sum_f(sum8f(w));
-    if (lane == 0) sh.btot[warp][k] = t;
-  }
+// exclusive block prefix (element order = thread order) and total of ff
+// values; every thread gets its exclusive prefix and the block total
+__device__ __forceinline__ void block_scan_ff(ff v, ff *wtot, ff &excl, ff &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const ff incl = scan32_ff(v, lane);
   __syncthreads();
-  if (tid == 0) {   // warp totals (blocks in order), then the chunk's
-    float *wt = P.wtot + ((int64_t)b * nc + c) * kWtStride;
-    float tc = 0.f;
-    for (int w = 0; w < kFWarps; ++w) {
-      float t = 0.f;
-      for (int k = 0; k < kGrp; ++k) t += sh.btot[w][k];
-      wt[w] = t;
-      tc += t;
-    }
-    wt[kFWarps] = tc;
-    __threadfence();
-    sh.last = atom_add_acq_rel(sq + SEQ_DRAW, 1u) == (unsigned)(nc - 1);
-  }
+  if (lane == 31) wtot[warp] = incl;
   __syncthreads();
-  if (sh.last && warp == 0) locate<TT, DK>(P, b, d);
+  const ff wi = scan32_ff(lane < kFinWarps ? wtot[lane] : ff{0.f, 0.f}, lane);   // every warp, same bits
+  const ff wex{__shfl_sync(0xffffffffu, wi.hi, (warp + 31) & 31), __shfl_sync(0xffffffffu, wi.lo, (warp + 31) & 31)};
+  const ff w_off = warp == 0 ? ff{0.f, 0.f} : wex;
+  const ff tex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+  excl = ff_add(w_off, lane == 0 ? ff{0.f, 0.f} : tex);
+  total = ff{__shfl_sync(0xffffffffu, wi.hi, kFinWarps - 1), __shfl_sync(0xffffffffu, wi.lo, kFinWarps - 1)};
 }
 
-// ---------------------------------------------------------------- kernels ---
+// Warps of a CTA shared among n items (rows or draws): with n <= kFinWarps,
+// item j gets warps j, j + n, j + 2n, ...; with more, warp w takes items w
+// and w + kFinWarps alone. For warp w: its first item, its index in the
+// item's group and the group's size in warps.
+struct WarpShare { int first, gi, gn; };
+__device__ __forceinline__ WarpShare warp_share(int warp, int n) {
+  if (n <= kFinWarps) return {warp % n, warp / n, (kFinWarps - 1 - warp % n) / n + 1};
+  return {warp, 0, 1};
+}
 
-// Work item of a ticket. Per sequence: NS = nc (K+1) statistics items and
-// ND = nc draw items. Tickets run in steps s = 0, 1, ...: step s holds the
-// statistics items of sequence s (s < B), then the draw items of sequence
-// s - lag (0 <= s - lag < B).
-__device__ __forceinline__ void decode_ticket(const SampleParams &P, unsigned t, int &kind, int &b, int &i, int &c) {
-  const int nc = P.nc, NS = nc * (P.K + 1), ND = nc, B = P.B, L = P.lag;
-  const long long c1 = (long long)min(L, B) * NS;
-  const long long c2 = (long long)max(0, B - L) * (NS + ND);
-  const long long tt = t;
-  kind = -1; b = 0; i = 0; c = 0;
-  if (tt < c1) {
-    b = (int)(tt / NS);
-    const int r = (int)(tt % NS);
-    kind = 0; i = r / nc; c = r % nc;
-  } else if (tt < c1 + c2) {
-    const long long u = tt - c1;
-    const int s = L + (int)(u / (NS + ND)), r = (int)(u % (NS + ND));
-    if (r < NS) { kind = 0; b = s; i = r / nc; c = r % nc; }
-    else { kind = 1; b = s - L; c = r - NS; }
-  } else {
-    const long long u = tt - c1 - c2;
-    b = max(0, B - L) + (int)(u / ND);
-    c = (int)(u % ND);
-    kind = b < B ? 1 : -1;
+// the per-warp partials of item j, in a fixed order: sum of slot[w][k] over
+// the warps of its group
+__device__ __forceinline__ ff group_sum(const ff (*slot)[2], int j, int n) {
+  if (n > kFinWarps) return slot[j % kFinWarps][j / kFinWarps];
+  ff s{0.f, 0.f};
+  for (int w = j; w < kFinWarps; w += n) s = ff_add(s, slot[w][0]);
+  return s;
+}
+
+// stages row[a + t * stride] (-inf from e1 on) for t < 8 into this thread's
+// slots st[t][threadIdx.x]: the eight loads are issued together
+template <typename T>
+__device__ __forceinline__ void stage8(float (*st)[kFinThreads], const T *row, int a, int stride, int e1) {
+  float x[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const int at = a + t * stride;
+    x[t] = at < e1 ? to_f32(row[at]) : -INFINITY;
   }
+#pragma unroll
+  for (int t = 0; t < 8; ++t) st[t][threadIdx.x] = x[t];
 }
 
 template <typename TT, int DK>
-__global__ void __launch_bounds__(kFThreads, sizeof(TT) == 4 ? 3 : 4) sample_fused_kernel(const __grid_constant__ SampleParams P) {
-  __shared__ FusedShared sh;
+__global__ void __launch_bounds__(kFinThreads, 1) sample_finish_kernel(const __grid_constant__ SampleParams P) {
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) {
-    int kind, b, i, c;
-    decode_ticket(P, atomicAdd(P.sync + SYNC_TICKET, 1u), kind, b, i, c);
-    sh.kind = kind; sh.b = b; sh.i = i; sh.c = c;
-  }
-  __syncthreads();
-  const int kind = sh.kind, b = sh.b, i = sh.i, c = sh.c;
-  if (kind == 0) stats_item<TT, DK>(P, sh, b, i, c);
-  else if (kind == 1) draw_item<TT, DK>(P, sh, b, c);
-}
-
-// ------------------------------------------------ float-float kernel -------
-// The sequences the fused kernel could not certify, resolved in float-float
-// arithmetic by kXGroups groups of nc CTAs (CTA c of a group owns chunk c of
-// every row); a group takes pending sequences j = group, group + kXGroups, ...
-// For each, from row i0 on:
-//   A. float-float sums of e_p and e_q over this CTA's chunk of each row
-//      i0 .. j_end (j_end: the first certified rejection at or after i0,
-//      else K; the walk cannot pass it) -> group barrier;
-//   B. every CTA forms the same row sums and takes the exact accept tests in
-//      walk order (certified ones keep their fp32 outcome), which fixes the
-//      row n2 drawn from; float-float weights of this chunk of row n2, kept
-//      per (warp, block, lane) group in registers -> group barrier;
-//   C. every CTA forms the same prefix over chunks; the chunk holding v Z
-//      finds the token (warp, block, lane from the totals, then the crossing
-//      lane's eight elements in order) and writes the outputs.
-// With zero residual mass (reading R9) the draw falls back to p_n2, whose
-// chunk sums are those of step A. Group barriers are counters that only
-// grow; a CTA waits only for CTAs of its own group.
-constexpr int kXGroups = 4;
-
-struct ExactShared {
-  unsigned flag;
-  float4 rs[kMaxPos];
-  int rfl[kMaxPos];
-  ff fbt[kFWarps][kGrp];        // float-float block totals
-  ff fws[kFWarps];
-  ff fred[kFWarps];
-  int wlast[kFWarps];
-  ff rowS[kMaxPos][2];          // float-float row sums (S_p, S_q)
-  ff xz, xthr, xoff;
-  int n2, xown, xlast;
-  float2 tbl[64];
-};
-
-template <typename TT, int DK>
-__device__ void exact_sequence(const SampleParams &P, ExactShared &sh, int b, int c, int i0, unsigned *bar,
-                               unsigned base) {
   using TD = typename std::conditional<DK == 0, TT, float>::type;
-  const int K = P.K, V = P.V, nc = P.nc;
+  __shared__ ff red[32];
+  __shared__ float2 tbl[64];
+  __shared__ int sync_flag, n_units, n_draws, n_pend;
+  // sequences being resolved (the same in every CTA)
+  __shared__ int e_b[kMaxEntries], e_i[kMaxEntries], e_state[kMaxEntries];
+  __shared__ int e_nu[kMaxEntries], e_u0[kMaxEntries], e_du[kMaxEntries], e_dr[kMaxEntries];
+  // rows evaluated this round: sequence, row, whether it is an accept test,
+  // the test's inputs, its verdict and the row sums
+  __shared__ int u_e[kMaxUnits], u_row[kMaxUnits], u_test[kMaxUnits], u_acc[kMaxUnits];
+  __shared__ float u_lpx[kMaxUnits], u_lqx[kMaxUnits], u_u[kMaxUnits];
+  __shared__ ff u_sp[kMaxUnits], u_sq[kMaxUnits];
+  // draws of this round: sequence, unit, weight mode, owner CTA, its lower
+  // bound, the threshold v Z
+  __shared__ int d_e[kMaxEntries], d_u[kMaxEntries], d_mode[kMaxEntries], d_own[kMaxEntries];
+  __shared__ ff d_off[kMaxEntries], d_thr[kMaxEntries];
+  // per-warp partials (two slots: a warp serves at most two items)
+  __shared__ ff w_a[kFinWarps][2], w_b[kFinWarps][2];
+  __shared__ int w_last[kFinWarps][2];
+  __shared__ int pick, found;
+  // per-thread staging of a batch of eight loaded logits (target, draft)
+  __shared__ float stg[2][8][kFinThreads];
+
+  const int nb = gridDim.x, cta = blockIdx.x;
+  const int K = P.K, V = P.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
-  const bool vec = P.aligned != 0;
-  const FfK fk{P.invT_hi, P.invT_lo, P.log2e_hi, P.log2e_lo, P.unitT};
-  const int ngr = (V + 7) >> 3;
-  const int gb = draw_gbase(c, warp, lane);
-  int j_end = K;
-  if (!force)
-    for (int j = i0; j < K; ++j)
-      if ((sh.rfl[j] & 3) == 2) { j_end = j; break; }
-
-  // ---- A: float-float row sums over this chunk -----------------------------
-  for (int j = i0; j <= j_end; ++j) {
-    const bool ql = j < K && DK == 0;
-    const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + j) * V;
-    const TD *drow = ql ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + j) * V : nullptr;
-    const float m_p = sh.rs[j].x, m_q = sh.rs[j].z;
-    ff sp{0.f, 0.f}, sqs{0.f, 0.f};
-#pragma unroll 1
-    for (int k = 0; k < kGrp; ++k) {
-      const int g = gb + 32 * k;
-      if (g >= ngr) continue;
-      float x[8];
-      unpack8(raw_load(trow, g, V, vec, false), x);
-#pragma unroll 1
-      for (int e = 0; e < 8; ++e) acc_add(sp, ffx_exp(x[e], m_p, fk, sh.tbl));
-      if (ql) {
-        unpack8(raw_load(drow, g, V, vec, false), x);
-#pragma unroll 1
-        for (int e = 0; e < 8; ++e) acc_add(sqs, ffx_exp(x[e], m_q, fk, sh.tbl));
-      }
-    }
-    sp = block_sum_ff(ff_norm(sp), sh.fred);
-    sqs = block_sum_ff(ff_norm(sqs), sh.fred);
-    if (tid == 0) P.part[((int64_t)b * (K + 1) + j) * nc + c] = make_float4(sp.hi, sp.lo, sqs.hi, sqs.lo);
-  }
-  cta_arrive(bar);
-  if (!cta_wait_geq(bar, base + (unsigned)nc, &sh.flag)) {
-    if (tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-    return;
-  }
-
-  // ---- B: row sums, exact walk, float-float weights of the drawn row -------
-  for (int j = i0 + warp; j <= j_end; j += kFWarps) {
-    const float4 v = lane < nc ? __ldcg(P.part + ((int64_t)b * (K + 1) + j) * nc + lane)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-    const ff sp = warp_sum_ff(ff{v.x, v.y}), sqs = warp_sum_ff(ff{v.z, v.w});
-    if (lane == 0) {
-      sh.rowS[j][0] = sp;
-      sh.rowS[j][1] = (j < K && DK == 0) ? sqs : ff{1.f, 0.f};
-    }
-  }
+  if (tid < 64) tbl[tid] = P.tbl[tid];
+  if (tid == 0) n_pend = min((int)__ldcg(&P.fin_sync[2]), P.B);
+  unsigned gen = 0;   // arrivals the next barrier waits for (thread 0)
+  const FfK fk = ff_consts(P);
+  // this CTA's chunk of every row; in the owner's search thread t takes
+  // elements [a0, a1) of it
+  const int chunk = (int)align_up((size_t)((V + nb - 1) / nb), 8);
+  const int e0 = min(V, cta * chunk), e1 = min(V, e0 + chunk);
+  const int per_t = (chunk + kFinThreads - 1) / kFinThreads;
+  const int a0 = min(e1, e0 + tid * per_t), a1 = min(e1, a0 + per_t);
+  bool grid_ok = true;
   __syncthreads();
-  if (tid == 0) {
-    int n2 = j_end;
-    for (int j = i0; j < j_end; ++j) {
-      if (!force && (sh.rfl[j] & 2)) continue;   // a certified acceptance (j < j_end)
-      // u q(x) < p(x)  <=>  u e_q(x) S_p < e_p(x) S_q   (draft logits)
-      //                <=>  u q(x) S_p < e_p(x)         (draft probabilities)
-      const int x = min(max(P.tokens[(int64_t)b * K + j], 0), V - 1);
-      const float lp_x = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + j) * V + x]);
-      const float lq_x = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + j) * V + x]);
-      const float u = P.uniforms[((int64_t)b * (K + 1) + j) * 2];
-      const ff Sp = sh.rowS[j][0], Sq = sh.rowS[j][1];
-      const ff epx = ff_norm(ffx_exp(lp_x, sh.rs[j].x, fk, sh.tbl));
-      ff lhs, rhs;
-      if (DK == 0) {
-        lhs = ff_mul(ff_mul(ff{u, 0.f}, ff_norm(ffx_exp(lq_x, sh.rs[j].z, fk, sh.tbl))), Sp);
-        rhs = ff_mul(epx, Sq);
-      } else {
-        lhs = ff_mul(ff{u, 0.f}, ff_mul(ff{lq_x, 0.f}, Sp));
-        rhs = epx;
-      }
-      if (!ff_gt(rhs, lhs)) { n2 = j; break; }
-    }
-    sh.n2 = n2;
-  }
-  __syncthreads();
-  const int n2 = sh.n2;
-  const int mode = n2 < K ? (DK == 0 ? 1 : 2) : 0;
-  const float m_p = sh.rs[n2].x, m_q = sh.rs[n2].z;
-  const ff Sp = sh.rowS[n2][0], Sqn = mode == 1 ? sh.rowS[n2][1] : ff{1.f, 0.f};
-  const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)b * (K + 1) + n2) * V;
-  const TD *drow = n2 < K ? static_cast<const TD *>(P.draft) + ((int64_t)b * K + n2) * V : nullptr;
-  // weights of group g of row n2 in the given mode, summed; last positive index
-  auto group_sum = [&](int g, int md, ff &s, int &last) {
-    s = ff{0.f, 0.f};
-    if (g >= ngr) return;
-    float xp[8], xq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    unpack8(raw_load(trow, g, V, vec, false), xp);
-    if (md != 0) unpack8(raw_load(drow, g, V, vec, DK == 1), xq);
-#pragma unroll 1
-    for (int e = 0; e < 8; ++e) {
-      const ff w = resid_weight(md, xp[e], xq[e], m_p, m_q, Sp, Sqn, fk, sh.tbl);
-      acc_add(s, w);
-      if (w.hi > 0.f) last = 8 * g + e;
-    }
-    s = ff_norm(s);
-  };
-  // the chunk's group sums (registers), block and warp totals (shared)
-  ff gs[kGrp];
-  auto chunk_sums = [&](int md) {
-    int last = -1;
-#pragma unroll
-    for (int k = 0; k < kGrp; ++k) {
-      group_sum(gb + 32 * k, md, gs[k], last);
-      const ff t = warp_sum_ff(gs[k]);
-      if (lane == 0) sh.fbt[warp][k] = t;
-    }
-    last = warp_max_s32(last);
-    if (lane == 0) sh.wlast[warp] = last;
-    __syncthreads();
-    if (tid == 0) {
-      int lc = -1;
-      for (int w = 0; w < kFWarps; ++w) {
-        ff t{0.f, 0.f};
-        for (int k = 0; k < kGrp; ++k) t = ff_add(t, sh.fbt[w][k]);
-        sh.fws[w] = t;
-        lc = max(lc, sh.wlast[w]);
-      }
-      sh.xlast = lc;
-    }
-    __syncthreads();
-  };
-  chunk_sums(mode);
-  if (tid == 0) {
-    ff tc{0.f, 0.f};
-    for (int w = 0; w < kFWarps; ++w) tc = ff_add(tc, sh.fws[w]);
-    P.xtot[(int64_t)b * nc + c] = make_float4(tc.hi, tc.lo, __int_as_float(sh.xlast), 0.f);
-  }
-  cta_arrive(bar);
-  if (!cta_wait_geq(bar, base + 2u * (unsigned)nc, &sh.flag)) {
-    if (tid == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-    return;
-  }
+  const int np = n_pend;
 
-  // ---- C: prefix over chunks (the same bits in every CTA), owner, token ----
-  const float v_u = P.uniforms[((int64_t)b * (K + 1) + n2) * 2 + 1];
-  // chunk weights: the row's own, or p_n2's (step A's sums) when the residual
-  // has no mass
-  auto prefix = [&](bool from_p) {
-    if (warp == 0) {
-      ff tv{0.f, 0.f};
-      if (lane < nc) {
-        if (from_p) {
-          const float4 v = __ldcg(P.part + ((int64_t)b * (K + 1) + n2) * nc + lane);
-          tv = ff{v.x, v.y};
-        } else {
-          const float4 v = __ldcg(P.xtot + (int64_t)b * nc + lane);
-          tv = ff{v.x, v.y};
-        }
-      }
-      ff XZ{0.f, 0.f};
-      for (int rr = 0; rr < nc; ++rr)
-        XZ = ff_add(XZ, ff{__shfl_sync(0xffffffffu, tv.hi, rr), __shfl_sync(0xffffffffu, tv.lo, rr)});
-      const ff thr = ff_mul(ff{v_u, 0.f}, XZ);
-      ff o{0.f, 0.f}, off{0.f, 0.f};
-      int own = -1, lastc = -1;
-      for (int rr = 0; rr < nc; ++rr) {
-        const ff t{__shfl_sync(0xffffffffu, tv.hi, rr), __shfl_sync(0xffffffffu, tv.lo, rr)};
-        if (rr == c) off = o;
-        const ff nx = ff_add(o, t);
-        if (ff_pos(t)) {
-          lastc = rr;
-          if (own < 0 && ff_gt(nx, thr)) own = rr;
-        }
-        o = nx;
-      }
-      // v Z past the last CDF value through rounding (reading R10): the last
-      // chunk with weight, whose search then ends on its last positive token
-      if (own < 0) own = lastc;
-      if (lane == 0) {
-        sh.xz = XZ;
-        sh.xthr = thr;
-        sh.xoff = off;
-        sh.xown = own;
-      }
+  for (int base = 0; base < np; base += kMaxEntries) {
+    const int ne = min(kMaxEntries, np - base);
+    if (tid < ne) {
+      const int2 pe = __ldcg(P.pend + base + tid);
+      e_b[tid] = pe.x;
+      e_i[tid] = pe.y;
+      e_state[tid] = ENT_WALK;
     }
     __syncthreads();
-  };
-  prefix(false);
-  bool from_p = false;
-  if (!ff_pos(sh.xz)) {
-    if (mode == 0) {   // a bonus row without mass (non-finite logits; flagged): no token
-      if (c == 0 && tid == 0) write_outputs(P, b, n2, -1);
-      return;
-    }
-    from_p = true;     // zero residual mass (reading R9): draw from p_n2
-    __syncthreads();
-    prefix(true);
-  }
-  const int own = sh.xown;
-  if (own < 0) {   // no token carries weight (non-finite logits; flagged)
-    if (c == 0 && tid == 0) write_outputs(P, b, n2, -1);
-    return;
-  }
-  if (own != c) return;
-  if (from_p) chunk_sums(0);
-  const ff thr = sh.xthr;
-  ff fb = sh.xoff;
-  int ow = kFWarps - 1;
-  for (int w = 0; w < kFWarps; ++w) {
-    const ff nb = ff_add(fb, sh.fws[w]);
-    if (ff_gt(nb, thr) || w == kFWarps - 1) { ow = w; break; }
-    fb = nb;
-  }
-  int ob = kGrp - 1;
-  for (int k = 0; k < kGrp; ++k) {
-    const ff nb = ff_add(fb, sh.fbt[ow][k]);
-    if (ff_gt(nb, thr) || k == kGrp - 1) { ob = k; break; }
-    fb = nb;
-  }
-  if (warp == ow) {
-    ff vs{0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < kGrp; ++k)
-      if (k == ob) vs = gs[k];
-    const ff incl = scan32_ff(vs, lane);
-    const ff tex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
-    const ff excl = lane == 0 ? ff{0.f, 0.f} : tex;
-    const int g = gb + 32 * ob;
-    const unsigned hit = __ballot_sync(0xffffffffu, g < ngr && ff_gt(ff_add(fb, incl), thr));
-    int y = -1;
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      if (lane == L) {
-        float xp[8], xq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const int md = from_p ? 0 : mode;
-        unpack8(raw_load(trow, g, V, vec, false), xp);
-        if (md != 0) unpack8(raw_load(drow, g, V, vec, DK == 1), xq);
-        ff run = ff_add(fb, excl);
-        int lastp = -1;
-        for (int e = 0; e < 8 && y < 0; ++e) {
-          const ff w = resid_weight(md, xp[e], xq[e], m_p, m_q, Sp, Sqn, fk, sh.tbl);
-          const ff nxt = ff_add(run, w);
-          if (w.hi > 0.f) {
-            lastp = 8 * g + e;
-            if (ff_gt(nxt, thr)) y = 8 * g + e;
+    // every round resolves a sequence or moves its walk past one row at least
+    for (int iter = 0; iter <= K + 2; ++iter) {
+      // ---- rows each sequence may still need -------------------------------
+      if (tid < ne) {
+        int nu = 0;
+        if (e_state[tid] == ENT_REDRAW) {
+          nu = 1;
+        } else if (e_state[tid] == ENT_WALK) {
+          const RowRec *recs = P.recs + (int64_t)e_b[tid] * (K + 1);
+          for (int r = e_i[tid]; r <= K; ++r) {
+            const uint32_t f = recs[r].flags;
+            if (r < K && (force || !(f & REC_ACC_CERT))) { ++nu; continue; }
+            if (r < K && (f & REC_ACCEPT)) continue;
+            if (force || !(f & REC_DRAW_CERT)) ++nu;
+            else if (nu == 0) {   // the walk ends on a certified draw
+              e_state[tid] = ENT_DONE;
+              if (cta == 0) write_outputs(P, e_b[tid], r, recs[r].y);
+            }
+            break;
           }
-          run = nxt;
         }
-        if (y < 0) y = lastp;   // the crossing within rounding of this group's end
+        e_nu[tid] = nu;
       }
-      y = __shfl_sync(0xffffffffu, y, L);
-    }
-    if (y < 0) y = sh.xlast;   // ... or of the chunk's
-    if (lane == 0) write_outputs(P, b, n2, y);
-  }
-}
+      __syncthreads();
+      if (tid == 0) {   // shares of the round's rows, in list order
+        int left = 0, used = 0;
+        for (int e = 0; e < ne; ++e) left += e_nu[e] > 0;
+        for (int e = 0; e < ne; ++e) {
+          if (e_nu[e] == 0) continue;
+          --left;
+          const int take = min(e_nu[e], kMaxUnits - used - left);
+          e_u0[e] = used;
+          e_nu[e] = take;
+          used += take;
+        }
+        n_units = used;
+      }
+      __syncthreads();
+      const int U = n_units;
+      if (U == 0) break;
+      if (tid < ne && e_nu[tid] > 0) {   // this sequence's units
+        int k = e_u0[tid];
+        const int kend = k + e_nu[tid];
+        if (e_state[tid] == ENT_REDRAW) {
+          u_e[k] = tid; u_row[k] = e_i[tid]; u_test[k] = 0;
+        } else {
+          const RowRec *recs = P.recs + (int64_t)e_b[tid] * (K + 1);
+          for (int r = e_i[tid]; r <= K && k < kend; ++r) {
+            const uint32_t f = recs[r].flags;
+            const bool test = r < K && (force || !(f & REC_ACC_CERT));
+            if (!test && r < K && (f & REC_ACCEPT)) continue;
+            if (!test && !force && (f & REC_DRAW_CERT)) break;   // certified: no unit
+            u_e[k] = tid; u_row[k] = r; u_test[k] = test ? 1 : 0;
+            ++k;
+            if (!test) break;
+          }
+        }
+      }
+      __syncthreads();
 
-template <typename TT, int DK>
-__global__ void __launch_bounds__(kFThreads) sample_exact_kernel(const __grid_constant__ SampleParams P) {
-  __shared__ ExactShared sh;
-  __shared__ int s_grp, s_c, s_np;
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x < 64) sh.tbl[threadIdx.x] = P.tbl[threadIdx.x];
-  if (threadIdx.x == 0) {
-    const unsigned t = atomicAdd(P.sync + SYNC_XTICKET, 1u);
-    s_grp = (int)(t / (unsigned)P.nc);
-    s_c = (int)(t % (unsigned)P.nc);
-    s_np = (int)min(__ldcg(P.sync + SYNC_PCOUNT), (unsigned)P.B);
-  }
-  __syncthreads();
-  const int grp = s_grp, c = s_c, np = s_np;
-  unsigned *bar = P.sync + SYNC_XBAR + grp;
-  unsigned base = 0;
-  for (int j = grp; j < np; j += kXGroups) {
-    const int2 pe = __ldcg(P.pend + j);
-    const int b = pe.x, i0 = pe.y;
-    for (int i = threadIdx.x; i <= P.K; i += blockDim.x) {
-      sh.rs[i] = __ldcg(P.rowrec + (int64_t)b * (P.K + 1) + i);
-      sh.rfl[i] = __ldcg(P.rowflag + (int64_t)b * (P.K + 1) + i);
+      // ---- step 1: chunk sums of e_p and e_q of every unit ------------------
+      {
+        const WarpShare ws = warp_share(warp, U);
+        for (int k = ws.first, slot = 0; k < U; k += kFinWarps, ++slot) {
+          const int bb = e_b[u_e[k]], r = u_row[k];
+          const bool q_logits = DK == 0 && r < K && e_state[u_e[k]] == ENT_WALK;
+          const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + r) * V;
+          const TD *drow = r < K ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + r) * V : nullptr;
+          if (ws.gi == 0 && lane == 0 && u_test[k]) {   // inputs of the accept test
+            const int x = min(max(P.tokens[(int64_t)bb * K + r], 0), V - 1);
+            u_lpx[k] = to_f32(trow[x]);
+            u_lqx[k] = to_f32(drow[x]);
+            u_u[k] = P.uniforms[((int64_t)bb * (K + 1) + r) * 2];
+          }
+          const float m_p = P.recs[(int64_t)bb * (K + 1) + r].m_p, m_q = P.recs[(int64_t)bb * (K + 1) + r].m_q;
+          const int stride = ws.gn * 32;
+          ff sp{0.f, 0.f}, sq{0.f, 0.f};
+          for (int a = e0 + ws.gi * 32 + lane; a < e1; a += 8 * stride) {
+            stage8(stg[0], trow, a, stride, e1);
+            if (q_logits) stage8(stg[1], drow, a, stride, e1);
+#pragma unroll 1
+            for (int t = 0; t < 8; ++t) {
+              acc_add(sp, ffx_exp(stg[0][t][tid], m_p, fk, tbl));
+              if (q_logits) acc_add(sq, ffx_exp(stg[1][t][tid], m_q, fk, tbl));
+            }
+          }
+          sp = warp_sum_ff(ff_norm(sp));
+          sq = warp_sum_ff(ff_norm(sq));
+          if (lane == 0) { w_a[warp][slot] = sp; w_b[warp][slot] = sq; }
+        }
+        __syncthreads();
+        if (tid < U) {
+          const ff sp = group_sum(w_a, tid, U), sq = group_sum(w_b, tid, U);
+          float4 *dst = reinterpret_cast<float4 *>(P.fin_sum + ((size_t)tid * kMaxFinCtas + cta) * 2);
+          *dst = make_float4(sp.hi, sp.lo, sq.hi, sq.lo);
+        }
+      }
+      grid_ok = grid_sync(P.fin_sync, gen, &sync_flag, P.wait_ns,
+                          cta == 0 && (P.withhold & SV_TEST_WITHHOLD_ARRIVALS)) && grid_ok;
+      if (!grid_ok) break;   // a barrier gave up: no further waits in this launch
+
+      // ---- step 2: row sums and exact accept tests (warp per unit; lanes
+      // stride the CTAs, the same order in every CTA) -------------------------
+      for (int k = warp; k < U; k += kFinWarps) {
+        float4 v[(kMaxFinCtas + 31) / 32];
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+          const int c = lane + 32 * q;
+          v[q] = c < nb ? __ldcg(reinterpret_cast<const float4 *>(P.fin_sum + ((size_t)k * kMaxFinCtas + c) * 2))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        ff sp{0.f, 0.f}, sq{0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+          sp = ff_add(sp, ff{v[q].x, v[q].y});
+          sq = ff_add(sq, ff{v[q].z, v[q].w});
+        }
+        sp = warp_sum_ff(sp);
+        sq = warp_sum_ff(sq);
+        if (lane == 0) {
+          const int bb = e_b[u_e[k]], r = u_row[k];
+          if (!(DK == 0 && r < K && e_state[u_e[k]] == ENT_WALK)) sq = ff{1.f, 0.f};
+          u_sp[k] = sp;
+          u_sq[k] = sq;
+          int acc = 0;
+          if (u_test[k]) {
+            // u q(x) < p(x)  <=>  u e_q(x) S_p < e_p(x) S_q   (draft logits)
+            //                <=>  u q(x) S_p < e_p(x)         (draft probabilities)
+            const RowRec &rr = P.recs[(int64_t)bb * (K + 1) + r];
+            const float u = u_u[k], lq_x = u_lqx[k];
+            const ff epx = ff_norm(ffx_exp(u_lpx[k], rr.m_p, fk, tbl));
+            ff lhs, rhs;
+            if (DK == 0) {
+              lhs = ff_mul(ff_mul(ff{u, 0.f}, ff_norm(ffx_exp(lq_x, rr.m_q, fk, tbl))), sp);
+              rhs = ff_mul(epx, sq);
+            } else {
+              lhs = ff_mul(ff{u, 0.f}, ff_mul(ff{lq_x, 0.f}, sp));
+              rhs = epx;
+            }
+            acc = ff_gt(rhs, lhs) ? 1 : 0;
+          }
+          u_acc[k] = acc;
+        }
+      }
+      __syncthreads();
+      // each sequence walks its units: the first exact rejection, or the row
+      // it ends on, is its draw; a walk that runs out of units continues next
+      // round
+      if (tid < ne) {
+        int du = -1, dr = -1;
+        if (e_nu[tid] > 0) {
+          const int bb = e_b[tid];
+          int k = e_u0[tid];
+          const int kend = k + e_nu[tid];
+          if (e_state[tid] == ENT_REDRAW) {
+            du = k; dr = e_i[tid];
+          } else {
+            RowRec *recs = P.recs + (int64_t)bb * (K + 1);
+            int r = e_i[tid];
+            for (; r <= K; ++r) {
+              const uint32_t f = recs[r].flags;
+              const bool test = r < K && (force || !(f & REC_ACC_CERT));
+              if (!test && r < K && (f & REC_ACCEPT)) continue;
+              if (!test && !force && (f & REC_DRAW_CERT)) {   // ends on a certified draw
+                e_state[tid] = ENT_DONE;
+                if (cta == 0) write_outputs(P, bb, r, recs[r].y);
+                break;
+              }
+              if (k == kend) break;   // out of units: resume here
+              if (test) {
+                if (cta == 0) recs[r].flags = f | REC_EXACT_ACC;
+                if (u_acc[k]) { ++k; continue; }
+              }
+              du = k; dr = r;
+              break;
+            }
+            if (du < 0 && e_state[tid] == ENT_WALK) e_i[tid] = r;
+          }
+        }
+        e_du[tid] = du;
+        e_dr[tid] = dr;
+      }
+      __syncthreads();
+      if (tid == 0) {   // draws of this round, in list order
+        int nd = 0;
+        for (int e = 0; e < ne; ++e) {
+          if (e_du[e] < 0) continue;
+          d_e[nd] = e;
+          d_u[nd] = e_du[e];
+          d_mode[nd] = e_state[e] == ENT_WALK && e_dr[e] < K ? (DK == 0 ? 1 : 2) : 0;
+          ++nd;
+        }
+        n_draws = nd;
+      }
+      __syncthreads();
+      const int D = n_draws;
+      // chunk totals of the residual weights and their last positive index
+      {
+        const WarpShare ws = warp_share(warp, max(D, 1));
+        for (int j = ws.first, slot = 0; j < D; j += kFinWarps, ++slot) {
+          const int e = d_e[j], k = d_u[j], mode = d_mode[j];
+          const int bb = e_b[e], r = e_dr[e];
+          const float m_p = P.recs[(int64_t)bb * (K + 1) + r].m_p, m_q = P.recs[(int64_t)bb * (K + 1) + r].m_q;
+          const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + r) * V;
+          const TD *drow = r < K ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + r) * V : nullptr;
+          const ff Sp = u_sp[k], Sq = u_sq[k];
+          const int stride = ws.gn * 32;
+          ff t{0.f, 0.f};
+          int last = -1;
+          for (int a = e0 + ws.gi * 32 + lane; a < e1; a += 8 * stride) {
+            stage8(stg[0], trow, a, stride, e1);
+            if (mode != 0) stage8(stg[1], drow, a, stride, e1);
+#pragma unroll 1
+            for (int s8 = 0; s8 < 8; ++s8) {
+              const ff w = resid_weight(mode, stg[0][s8][tid], mode != 0 ? stg[1][s8][tid] : 0.f, m_p, m_q, Sp, Sq,
+                                        fk, tbl);
+              acc_add(t, w);
+              if (w.hi > 0.f) last = a + s8 * stride;
+            }
+          }
+          t = warp_sum_ff(ff_norm(t));
+          last = warp_max_s32(last);
+          if (lane == 0) { w_a[warp][slot] = t; w_last[warp][slot] = last; }
+        }
+        __syncthreads();
+        if (tid < D) {
+          const ff t = group_sum(w_a, tid, D);
+          int m = -1;
+          if (D > kFinWarps) m = w_last[tid % kFinWarps][tid / kFinWarps];
+          else for (int w = tid; w < kFinWarps; w += D) m = max(m, w_last[w][0]);
+          P.fin_tot[(size_t)tid * kMaxFinCtas + cta] = make_float2(t.hi, t.lo);
+          P.fin_last[(size_t)tid * kMaxFinCtas + cta] = m;
+        }
+      }
+      grid_ok = grid_sync(P.fin_sync, gen, &sync_flag, P.wait_ns,
+                          cta == 0 && (P.withhold & SV_TEST_WITHHOLD_ARRIVALS)) && grid_ok;
+      if (!grid_ok) break;   // a barrier gave up: no further waits in this launch
+
+      // ---- step 3: prefix over chunks (warp per draw) -----------------------
+      // lane l sums CTAs [l per_l, (l+1) per_l) in order, lanes are scanned
+      // in a fixed order, and the CTAs of the lane holding v Z chain their
+      // boundaries in order (the last one closes on the next lane's start)
+      for (int j = warp; j < D; j += kFinWarps) {
+        const int e = d_e[j], bb = e_b[e], r = e_dr[e];
+        const float2 *tot = P.fin_tot + (size_t)j * kMaxFinCtas;
+        const int per_l = (nb + 31) / 32;   // <= 5
+        ff tv[(kMaxFinCtas + 31) / 32];
+        ff run{0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+          const int c = lane * per_l + q;
+          tv[q] = q < per_l && c < nb ? ldcg_ff(tot + c) : ff{0.f, 0.f};
+        }
+        const float v_u = P.uniforms[((int64_t)bb * (K + 1) + r) * 2 + 1];
+#pragma unroll
+        for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) run = ff_add(run, tv[q]);
+        const ff incl = scan32_ff(run, lane);
+        const ff XZ{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+        const ff tex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+        const ff excl = lane == 0 ? ff{0.f, 0.f} : tex;
+        int own = -2;   // zero residual mass
+        ff s0{0.f, 0.f}, xthr{0.f, 0.f};
+        if (ff_pos(XZ)) {
+          xthr = ff_mul(ff{v_u, 0.f}, XZ);
+          const unsigned past = __ballot_sync(0xffffffffu, ff_gt(incl, xthr));
+          const int L = past ? __ffs(past) - 1 : 31;
+          int mine = -1;
+          ff lo = excl;
+          if (lane == L) {
+            const int c_first = L * per_l, c_last = min(nb, (L + 1) * per_l) - 1;
+            mine = max(0, c_last);
+#pragma unroll
+            for (int q = 0; q < (kMaxFinCtas + 31) / 32; ++q) {
+              if (c_first + q >= c_last) break;
+              const ff s1 = ff_add(lo, tv[q]);
+              if (ff_gt(s1, xthr)) { mine = c_first + q; break; }
+              lo = s1;
+            }
+          }
+          own = __shfl_sync(0xffffffffu, mine, L);
+          s0 = ff{__shfl_sync(0xffffffffu, lo.hi, L), __shfl_sync(0xffffffffu, lo.lo, L)};
+        }
+        if (lane == 0) { d_own[j] = own; d_off[j] = s0; d_thr[j] = xthr; }
+      }
+      __syncthreads();
+      // the owner CTA finds the token within its chunk and writes the outputs
+      for (int j = 0; j < D; ++j) {
+        const int e = d_e[j], mode = d_mode[j];
+        const int bb = e_b[e], r = e_dr[e];
+        if (d_own[j] == -2) {   // zero residual mass: the draw falls back to p
+          if (mode == 0 && cta == 0 && tid == 0) {
+            write_outputs(P, bb, r, -1);
+            P.recs[(int64_t)bb * (K + 1) + r].flags |= REC_EXACT_DRAW;
+            P.recs[(int64_t)bb * (K + 1) + r].y_exact = -1;
+          }
+          continue;
+        }
+        if (d_own[j] != cta) continue;
+        const int k = d_u[j];
+        const float m_p = P.recs[(int64_t)bb * (K + 1) + r].m_p, m_q = P.recs[(int64_t)bb * (K + 1) + r].m_q;
+        const TT *trow = static_cast<const TT *>(P.target) + ((int64_t)bb * (K + 1) + r) * V;
+        const TD *drow = r < K ? static_cast<const TD *>(P.draft) + ((int64_t)bb * K + r) * V : nullptr;
+        const ff Sp = u_sp[k], Sq = u_sq[k], xthr = d_thr[j];
+        ff t{0.f, 0.f};
+        int lastp = -1;
+        for (int a = a0; a < a1; a += 8) {
+          stage8(stg[0], trow, a, 1, a1);
+          if (mode != 0) stage8(stg[1], drow, a, 1, a1);
+#pragma unroll 1
+          for (int s8 = 0; s8 < 8; ++s8) {
+            const ff w = resid_weight(mode, stg[0][s8][tid], mode != 0 ? stg[1][s8][tid] : 0.f, m_p, m_q, Sp, Sq,
+                                      fk, tbl);
+            acc_add(t, w);
+            if (w.hi > 0.f) lastp = a + s8;
+          }
+        }
+        t = ff_norm(t);
+        ff excl, total;
+        block_scan_ff(t, red, excl, total);
+        // the first thread whose upper bound passes v Z
+        const ff lo = ff_add(d_off[j], excl);
+        const unsigned wb = __ballot_sync(0xffffffffu, ff_gt(ff_add(lo, t), xthr));
+        if (lane == 0) w_last[warp][0] = wb ? warp * 32 + __ffs(wb) - 1 : 1 << 30;
+        __syncthreads();
+        if (tid == 0) {
+          int first = 1 << 30;
+          for (int w = 0; w < kFinWarps; ++w) first = min(first, w_last[w][0]);
+          pick = first;
+          found = -1;
+        }
+        __syncthreads();
+        if (tid == pick) {
+          int cand = -1;
+          ff runc = lo;
+          for (int a = a0; a < a1 && cand < 0; ++a) {
+            const ff w = resid_weight(mode, to_f32(trow[a]), mode != 0 ? to_f32(drow[a]) : 0.f, m_p, m_q, Sp, Sq, fk,
+                                      tbl);
+            const ff nxt = ff_add(runc, w);
+            if (w.hi > 0.f && ff_gt(nxt, xthr)) cand = a;
+            runc = nxt;
+          }
+          if (cand < 0) cand = lastp;   // crossing within rounding of this thread's end
+          found = cand;
+        }
+        __syncthreads();
+        if (tid == 0) {
+          // v Z within rounding of the chunk's top: its last positive weight,
+          // else the row's
+          int y = found;
+          if (y < 0) y = __ldcg(P.fin_last + (size_t)j * kMaxFinCtas + cta);
+          for (int c = 0; c < nb && y < 0; ++c) y = max(y, __ldcg(P.fin_last + (size_t)j * kMaxFinCtas + c));
+          write_outputs(P, bb, r, y);
+          P.recs[(int64_t)bb * (K + 1) + r].flags |= REC_EXACT_DRAW;
+          P.recs[(int64_t)bb * (K + 1) + r].y_exact = y;
+        }
+        __syncthreads();
+      }
+      if (tid < D) {   // state changes, the same in every CTA
+        const int e = d_e[tid];
+        if (d_own[tid] == -2 && d_mode[tid] != 0) { e_state[e] = ENT_REDRAW; e_i[e] = e_dr[e]; }
+        else e_state[e] = ENT_DONE;
+      }
+      __syncthreads();
     }
     __syncthreads();
-    exact_sequence<TT, DK>(P, sh, b, c, i0, bar, base);
-    base += 2u * (unsigned)P.nc;
-    __syncthreads();
+    if (!grid_ok) break;
   }
-}
-
-// Zeroes the call's tickets, pending count, group barriers and per-sequence
-// counters once the previous kernel of the stream (which may be an earlier
-// call on this workspace) has completed.
-__global__ void __launch_bounds__(1024) sample_init_kernel(unsigned *sync, unsigned *seq, int n_words) {
-  pdl_trigger();
-  pdl_wait();
-  for (int j = threadIdx.x; j < n_words; j += blockDim.x) seq[j] = 0u;
-  if (threadIdx.x < SYNC_WORDS) sync[threadIdx.x] = 0u;
+  if (!grid_ok && tid == 0 && cta == 0) atomic_or_status(P.status, SV_DEV_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ host ---
 
-int stat_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+size_t records_bytes(int B, int K) { return align_up((size_t)B * (K + 1) * sizeof(RowRec), 256); }
+
+int stat_chunks(int V) { return (V + kStatChunk - 1) / kStatChunk; }
+
+// scratch of the finish grid: barrier words, per-CTA row sums of every unit,
+// per-CTA weight totals and last positive indices of every draw
+constexpr size_t kFinSyncBytes = 256;
+constexpr size_t kFinSumBytes = (size_t)kMaxUnits * kMaxFinCtas * 2 * sizeof(float2);
+constexpr size_t kFinTotBytes = (size_t)kMaxEntries * kMaxFinCtas * sizeof(float2);
+constexpr size_t kFinLastBytes = (size_t)kMaxEntries * kMaxFinCtas * sizeof(int);
+constexpr size_t kFinScratchBytes = kFinSyncBytes + kFinSumBytes + kFinTotBytes + kFinLastBytes;
 
 size_t parts_bytes(int B, int K, int V) { return align_up((size_t)B * (K + 1) * stat_chunks(V) * sizeof(float4), 256); }
-size_t rows_bytes(int B, int K) { return align_up((size_t)B * (K + 1) * (sizeof(float4) + sizeof(int)), 256); }
-size_t wtot_bytes(int B, int V) { return align_up((size_t)B * stat_chunks(V) * kWtStride * sizeof(float), 256); }
-size_t xtot_bytes(int B, int V) { return align_up((size_t)B * stat_chunks(V) * sizeof(float4), 256); }
-size_t small_bytes(int B) {   // decisions, pending list, per-sequence counters, then the call's words
-  return align_up((size_t)B * sizeof(int2), 256) * 2 + align_up((size_t)B * SEQ_WORDS * sizeof(unsigned), 256) + 256;
-}
 
+size_t pending_bytes(int B) { return align_up((size_t)B * sizeof(int2), 256); }
+
+// per-row records, the chunk statistics, the finish grid's scratch, then the
+// list of sequences pending for it
 size_t workspace_bytes_for(int B, int K, int V) {
-  return parts_bytes(B, K, V) + rows_bytes(B, K) + wtot_bytes(B, V) + xtot_bytes(B, V) + small_bytes(B);
+  return records_bytes(B, K) + parts_bytes(B, K, V) + kFinScratchBytes + pending_bytes(B);
 }
 
 int sm_count() {
@@ -1270,36 +1513,80 @@ int sm_count() {
   return n;
 }
 
+// Cooperative launch of the finish grid (every CTA resident), staged behind
+// the previous launch when the driver accepts both attributes together.
+template <typename KernelT>
+cudaError_t launch_coop(KernelT kernel, int nb, cudaStream_t s, const SampleParams &P) {
+  static int pdl_ok = 1;
+  for (;;) {
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+    if (pdl_ok) {
+      attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[n].val.programmaticStreamSerializationAllowed = 1;
+      ++n;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nb);
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, P);
+    if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+    if (e == cudaSuccess || !pdl_ok) return e;
+    (void)cudaGetLastError();   // retry as a plain cooperative launch
+    pdl_ok = 0;
+  }
+}
+
 void split_ff(double d, float &hi, float &lo) {
   hi = (float)d;
   lo = (float)(d - (double)hi);
 }
 
+
 template <typename TT, int DK>
-sv_status launch_sample(SampleParams &P, cudaStream_t s) {
+sv_status launch_sample(const SampleParams &P, int cs, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  static int per_sm = 0;
+  static int fin_blocks = 0;
   std::call_once(once, [] {
-    attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_fused_kernel<TT, DK>, kFThreads, 0);
+    attr_err = cudaFuncSetAttribute(sample_draw_kernel<TT, DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    int per_sm = 0;
+    if (attr_err == cudaSuccess)
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_finish_kernel<TT, DK>, kFinThreads, 0);
+    // one CTA per SM (the kernel is bound to one by its registers), all resident
+    fin_blocks = std::min(kMaxFinCtas, sm_count() * std::min(per_sm, 1));
   });
   if (attr_err != cudaSuccess)
-    return fail(SV_ERR_CUDA, "spec_verify_sample: occupancy query: %s", cudaGetErrorString(attr_err));
-  // draw items of a sequence are ticketed after the statistics items of the
-  // sequences that fill the GPU's CTA slots once more, so that by the time
-  // they run the sequence's decisions are normally out
-  const int NS = P.nc * (P.K + 1);
-  const long long slots = (long long)sm_count() * std::max(per_sm, 1);
-  P.lag = (int)std::min<long long>(P.B, std::max<long long>(1, (slots + NS - 1) / NS + 1));
-  cudaError_t e = launch_k(sample_init_kernel, dim3(1), dim3(1024), 0, s, 1, P.sync, P.seq, P.B * SEQ_WORDS);
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample init launch: %s", cudaGetErrorString(e));
-  const long long items = (long long)P.B * (NS + P.nc);
-  if (items > 0x7fffffffLL) return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: %lld work items", items);
-  e = launch_k(sample_fused_kernel<TT, DK>, dim3((unsigned)items), dim3(kFThreads), 0, s, 1, P);
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample launch: %s", cudaGetErrorString(e));
-  e = launch_k(sample_exact_kernel<TT, DK>, dim3(kXGroups * P.nc), dim3(kFThreads), 0, s, 1, P);
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample float-float launch: %s", cudaGetErrorString(e));
+    return fail(SV_ERR_CUDA, "spec_verify_sample: kernel attributes: %s", cudaGetErrorString(attr_err));
+  if (fin_blocks < 1) return fail(SV_ERR_CUDA, "spec_verify_sample: the finish grid does not fit on the device");
+  cudaError_t e = launch_k(sample_stats_kernel<TT, DK>, dim3(P.nc, P.K + 1, P.B), dim3(kStatThreads), 0, s, 1, P);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample statistics launch: %s", cudaGetErrorString(e));
+  e = launch_k(sample_draw_kernel<TT, DK>, dim3(cs, P.B), dim3(kRowThreads), 0, s, cs, P);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample draw launch: %s", cudaGetErrorString(e));
+  e = launch_coop(sample_finish_kernel<TT, DK>, fin_blocks, s, P);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample finish launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+}  // namespace
+}  // namespace sv
+
+namespace sv {
+namespace {
+// Draw-kernel cluster: the smallest (up to 16 CTAs) whose slices take at most
+// eight groups of eight elements per thread; gpc = groups per CTA slice.
+void draw_shape(int V, int &cs, int &gpc) {
+  const int ngr = (V + 7) / 8;
+  cs = 1;
+  while (cs < 16 && (ngr + cs - 1) / cs > 8 * kRowThreads) cs *= 2;
+  gpc = (ngr + cs - 1) / cs;
 }
 
 // Host checks of spec_verify_sample's arguments (everything but the workspace).
@@ -1309,11 +1596,8 @@ sv_status check_sample_args(const void *target_logits, sv_dtype logit_dtype, con
                             const int32_t *out_tokens, const int32_t *num_accepted) {
   if (B < 0 || K < 0 || V < 1)
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample: bad sizes B=%d K=%d V=%d", B, K, V);
-  if (B > 65535 || K + 1 > kMaxPos)
-    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: B must be <= 65535 and K + 1 <= %d", kMaxPos);
-  if (V > kMaxChunks * kChunk)
-    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large (at most %d)", V,
-                kMaxChunks * kChunk);
+  if (B > 65535 || K + 1 > 65535)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: B and K+1 must be <= 65535");
   if (!(temperature > 0.f) || !std::isfinite(temperature))
     return fail(SV_ERR_INVALID_ARG, "spec_verify_sample: temperature must be finite and > 0");
   if (!target_logits || !uniforms || !out_tokens || !num_accepted)
@@ -1328,14 +1612,20 @@ sv_status check_sample_args(const void *target_logits, sv_dtype logit_dtype, con
   } else if (K > 0 && draft_dtype != logit_dtype) {
     return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: draft logits must have the target's dtype");
   }
+  int cs, gpc;
+  draw_shape(V, cs, gpc);
+  if (gpc > kMaxDrawBlocks * 32)
+    return fail(SV_ERR_UNSUPPORTED, "spec_verify_sample: vocabulary of %d too large (at most %d)", V,
+                16 * kMaxDrawBlocks * 32 * 8);
   return SV_OK;
 }
-
 }  // namespace
 }  // namespace sv
 
 extern "C" size_t spec_verify_sample_workspace_size(int B, int K, int V) {
-  if (B < 0 || K < 0 || V < 1) return 0;
+  (void)V;
+  if (B < 0 || K < 0) return 0;
+  if (V < 1) return 0;
   return sv::workspace_bytes_for(B, K, V);
 }
 
@@ -1359,45 +1649,42 @@ extern "C" sv_status spec_verify_sample_ex(const void *target_logits, sv_dtype l
 
   const int es_t = dtype_bytes(logit_dtype);
   const int es_buf_d = (draft_is_probs && K > 0) ? 4 : es_t;
+  int cs, gpc;
+  draw_shape(V, cs, gpc);
 
   SampleParams P = {};
   P.target = target_logits; P.draft = draft; P.tokens = draft_tokens; P.uniforms = uniforms;
   P.p_at = p_at_draft; P.q_at = q_at_draft; P.out_tokens = out_tokens; P.num_acc = num_accepted;
-  P.status = dev_status;
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  P.part = reinterpret_cast<float4 *>(ws);
-  ws += parts_bytes(B, K, V);
-  P.rowrec = reinterpret_cast<float4 *>(ws);
-  P.rowflag = reinterpret_cast<int *>(ws + (size_t)B * (K + 1) * sizeof(float4));
-  ws += rows_bytes(B, K);
-  P.wtot = reinterpret_cast<float *>(ws);
-  ws += wtot_bytes(B, V);
-  P.xtot = reinterpret_cast<float4 *>(ws);
-  ws += xtot_bytes(B, V);
-  P.dec = reinterpret_cast<int2 *>(ws);
-  ws += align_up((size_t)B * sizeof(int2), 256);
-  P.pend = reinterpret_cast<int2 *>(ws);
-  ws += align_up((size_t)B * sizeof(int2), 256);
-  P.seq = reinterpret_cast<unsigned *>(ws);
-  ws += align_up((size_t)B * SEQ_WORDS * sizeof(unsigned), 256);
-  P.sync = reinterpret_cast<unsigned *>(ws);
+  P.recs = static_cast<RowRec *>(workspace); P.status = dev_status;
+  P.part = reinterpret_cast<float4 *>(static_cast<uint8_t *>(workspace) + records_bytes(B, K));
   P.nc = stat_chunks(V);
-  P.B = B; P.K = K; P.V = V; P.flags = flags;
+  {
+    uint8_t *fin = static_cast<uint8_t *>(workspace) + records_bytes(B, K) + parts_bytes(B, K, V);
+    P.fin_sync = reinterpret_cast<unsigned *>(fin);
+    P.fin_sum = reinterpret_cast<float2 *>(fin + kFinSyncBytes);
+    P.fin_tot = reinterpret_cast<float2 *>(fin + kFinSyncBytes + kFinSumBytes);
+    P.fin_last = reinterpret_cast<int *>(fin + kFinSyncBytes + kFinSumBytes + kFinTotBytes);
+    P.pend = reinterpret_cast<int2 *>(fin + kFinScratchBytes);
+  }
+  P.B = B; P.K = K; P.V = V; P.gpc = gpc; P.flags = flags;
+  P.wait_ns = wait_limit_ns();
+  P.withhold = test_withhold();
   P.aligned = aligned(target_logits, 16) && ((size_t)V * es_t) % 16 == 0 &&
               (K == 0 || (aligned(draft, 16) && ((size_t)V * es_buf_d) % 16 == 0));
-  const double log2e = 1.4426950408889634074;
+  const double log2e = 1.4426950408889634074, ln2 = 0.69314718055994530942;
   P.c = (float)(log2e / (double)temperature);
   P.unitT = temperature == 1.0f;
   split_ff(1.0 / (double)temperature, P.invT_hi, P.invT_lo);
   split_ff(log2e, P.log2e_hi, P.log2e_lo);
+  split_ff(ln2, P.ln2_hi, P.ln2_lo);
   for (int j = 0; j < 64; ++j) split_ff(std::exp2((double)j / 64.0), P.tbl[j].x, P.tbl[j].y);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool probs = draft_is_probs && K > 0;
   switch (logit_dtype) {
-    case SV_F32: return probs ? launch_sample<float, 1>(P, s) : launch_sample<float, 0>(P, s);
-    case SV_BF16: return probs ? launch_sample<__nv_bfloat16, 1>(P, s) : launch_sample<__nv_bfloat16, 0>(P, s);
-    default: return probs ? launch_sample<__half, 1>(P, s) : launch_sample<__half, 0>(P, s);
+    case SV_F32: return probs ? launch_sample<float, 1>(P, cs, s) : launch_sample<float, 0>(P, cs, s);
+    case SV_BF16: return probs ? launch_sample<__nv_bfloat16, 1>(P, cs, s) : launch_sample<__nv_bfloat16, 0>(P, cs, s);
+    default: return probs ? launch_sample<__half, 1>(P, cs, s) : launch_sample<__half, 0>(P, cs, s);
   }
 }
 
@@ -1483,7 +1770,7 @@ extern "C" sv_status spec_verify_sample_topp(const void *target_logits, sv_dtype
 // this static device array (every GPU that loads the library keeps it until
 // the process exits).
 namespace {
-constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB
+constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB: 48 + 16 ceil(V / 8192) bytes per (sequence, position)
 __device__ __align__(256) uint8_t g_sample_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
@@ -1535,10 +1822,10 @@ extern "C" sv_status spec_verify_sample_static(const void *target_logits, sv_dty
   const size_t need = workspace_bytes_for(B, K, V);
   if (need > kStaticScratchBytes)
     return fail(SV_ERR_UNSUPPORTED,
-                "spec_verify_sample_static: B = %d sequences of %d rows need %zu bytes (%d 16-byte chunk "
-                "statistics per row and per sequence, 16 bytes per sequence), more than the static scratch "
-                "of %zu bytes; use spec_verify_sample with a caller workspace",
-                B, K + 1, need, stat_chunks(V), kStaticScratchBytes);
+                "spec_verify_sample_static: B*(K+1) = %lld rows need %zu bytes (a %zu-byte record and %d "
+                "16-byte chunk statistics per row), more than the static scratch of %zu bytes; use "
+                "spec_verify_sample with a caller workspace",
+                (long long)B * (K + 1), need, sizeof(RowRec), stat_chunks(V), kStaticScratchBytes);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "spec_verify_sample_static: cudaGetDevice: %s", cudaGetErrorString(e));

@@ -25,6 +25,11 @@ namespace sv {
 sv_status launch_topp_filter(sv_dtype dtype, const void *in0, void *out0, int rows0, const void *in1, void *out1,
                              int rows1, int V, float temperature, float top_p, int32_t *status, cudaStream_t s);
 
+// Wait limit for device waits of later launches (sv_test_hooks; default
+// kWaitLimitNs) and the signals a test asks launches to withhold.
+uint64_t wait_limit_ns();
+unsigned test_withhold();
+
 // Per-thread message of the last failed call.
 std::string &last_error();
 // kernels this library launched successfully in this process
@@ -144,13 +149,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t phas
 }
 
 // Bounded wait: returns false (and the caller reports SV_DEV_TIMEOUT) if the
-// phase did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase) {
+// phase did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, phase)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, phase)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -103,6 +103,12 @@ SMALL_ATTN = [
                     "ctx": ("fixed", (5, 700))}),
     ("tc_bf16_rows64", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 16, "H_kv": 2,
                         "K": 7, "ctx": ("fixed", (1000, 33))}),
+    ("tc_bf16_rows72", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 16, "H_kv": 2,
+                        "K": 8, "ctx": ("fixed", (900, 45))}),
+    ("tc_bf16_rows128", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "H_q": 16, "H_kv": 1,
+                         "K": 7, "ctx": ("fixed", (333, 1200))}),
+    ("tc_fp8_rows96", {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 128, "H_q": 32, "H_kv": 2,
+                       "K": 5, "ctx": ("fixed", (700, 21))}),
     ("tc_bf16_n1", {"kv_dtype": "bf16", "q_dtype": "bf16", "d_head": 128, "K": 0,
                     "ctx": ("fixed", (1, 250))}),
     ("tc_fp8", {"kv_dtype": "fp8_e4m3", "q_dtype": "bf16", "d_head": 128, "H_q": 8, "H_kv": 2,

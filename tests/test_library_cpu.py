@@ -44,18 +44,18 @@ def test_launch_counter_starts_without_gpu_work(lib):
 
 
 def test_workspace_sizes(lib):
-    # sampling, each part 256-byte rounded: one 16-byte (max, sum) pair per
-    # 8192-logit chunk of each row; per row its 16-byte statistics and 4-byte
-    # accept flags; per chunk of each sequence 12 floats of draw totals and a
-    # 16-byte float-float total; per sequence its decision and a pending-list
-    # entry (8 bytes each) and four counters; 256 bytes of the call's words
+    # sampling: one 48-byte record per (sequence, position), one 16-byte
+    # (max, sum) pair per 8192-logit chunk of each row (each part 256-byte
+    # rounded), then the finish grid's fixed scratch (barrier words; per
+    # re-evaluated row and CTA two float-float sums; per re-evaluated draw and
+    # CTA a float-float total and an index), then one 8-byte entry per
+    # sequence for the list of sequences left to the float-float pass
     up = lambda x: (x + 255) // 256 * 256
     chunks = (128256 + 8191) // 8192
-    B, K = 64, 4
-    assert lib.spec_verify_sample_workspace_size(B, K, 128256) == (
-        up(B * (K + 1) * chunks * 16) + up(B * (K + 1) * 20) + up(B * chunks * 48) + up(B * chunks * 16)
-        + 2 * up(B * 8) + up(B * 16) + 256)
-    assert lib.spec_verify_sample_workspace_size(0, 4, 10) == 256
+    fin = 256 + 32 * 160 * 16 + 32 * 160 * (8 + 4)
+    assert lib.spec_verify_sample_workspace_size(64, 4, 128256) == (
+        up(64 * 5 * 48) + up(64 * 5 * chunks * 16) + fin + up(64 * 8))
+    assert lib.spec_verify_sample_workspace_size(0, 4, 10) == fin
     s = lib.spec_verify_attn_workspace_size(64, 5, 64, 8, 128, 512, 16)
     # (acc d + m + l) floats per (sequence, kv head, split, row); splits of at
     # least 16 blocks
