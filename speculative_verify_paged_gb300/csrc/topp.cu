@@ -10,32 +10,37 @@
 // - x), so that order is plain descending order of the composite, and the set
 // is {x : composite(x) >= cut} for one cut value.
 //
-// Masses are the weights 2^((l - m) log2(e) / T) of the row (m its maximum),
-// rounded to multiples of 2^-40 and summed as 64-bit integers: the sums, and
-// so the set, do not depend on the order of the additions (the kernel is
-// deterministic). Each weight is within about 2.2e-7 (relative) of its exact
-// value (the SFU exp2, the first-order correction, the rounding to 2^-40), so
-// a cumulative mass as a fraction of the row mass is within 5e-7: the set is
-// exact unless top_p lies that close to a cumulative mass.
+// Masses are the weights w = 2^((l - m) log2(e) / T) of the row (m its
+// maximum); each is within about 2.2e-7 (relative) of its exact value (the
+// SFU exp2 and a first-order correction for the rounding of the exponent).
+// Sums that decide the set are compensated fp32 sums per thread (within two
+// ulps) combined in fp64 in a fixed order, and sums of the few tokens ranked
+// directly are exact 64-bit sums of masses in 2^-40 fixed point, so a
+// cumulative mass as a fraction of the row mass is within 5e-7 of exact, and
+// the kernel is deterministic: the set is exact unless top_p lies that close
+// to a cumulative mass.
 //
-// One 512-thread CTA per row. The first pass reads the row from memory; the
-// later passes read it again, from L2 (the rows in flight, two CTAs per SM,
-// take about a half of it at 128K bf16 logits per row). Passes:
-//   1. the row maximum m;
-//   2. every thread adds the masses of its logits into its own row of 8
-//      coarse bins of 8 binades of weight each (shared memory, no atomics);
-//      the block sums them, giving Z and the coarse bin where the running
-//      mass reaches ceil(top_p Z);
-//   3. a histogram of that coarse bin in fine bins of 1/32 of a binade
-//      (shared atomics, only for the logits of that bin) gives the fine bin
-//      of the crossing;
-//   4. the fine bin's tokens are gathered (if more than 512, the bin is
-//      first split by the composite's bits, 8 at a time, until at most 512
-//      remain) and ranked by direct comparison of composites: the cut;
-//   5. the row is written: logits in fine bins above the cut's bin stay,
-//      those below go, the composite decides within it.
-// Bins come from one fma of the logit and are non-increasing in it; only
-// pass 2 (and the gathered tokens) compute the precise weights.
+// One 512-thread CTA per row, two per SM. The first pass reads the row from
+// memory, the other two from L2. Passes:
+//   1. the row maximum m, with packed two-lane max instructions (a second,
+//      NaN-propagating max flags NaN);
+//   2. Z, the row's mass; and an approximate mass for each of 2048 fine bins
+//      of 1/32 of a binade of weight: every w of bin f is scaled by
+//      2^(f/32 + s), rounded to an integer and added with a 32-bit shared
+//      atomic (exact integer sums: deterministic, and within 2^-(s+1) of the
+//      bin's mass, relative). A block scan gives the window of bins
+//      [f_lo, f_hi] where the running mass can reach top_p Z, given that
+//      error bound (one bin in nearly every row);
+//   3. the row is written: logits in bins above the window stay (their
+//      masses summed into `above`), those below go, and the window's logits
+//      are written as kept and gathered (composite, mass, position). The
+//      gathered tokens (at most 512; more only with many equal or nearly
+//      equal logits, then the window is split by the composite's bits, 8 at
+//      a time, over extra passes) are ranked by direct comparison: the cut.
+//      Those below it are then overwritten with -inf.
+// A logit's bin is round(32 (m - x) c) from the same roundings in every pass,
+// so it is non-increasing in x and a bin boundary never separates equal
+// logits; NaN and -inf fall in the last bin, which takes no mass.
 
 #include <cmath>
 #include <mutex>
@@ -47,12 +52,12 @@ namespace {
 
 constexpr int kTpThreads = 512;
 constexpr int kTpWarps = kTpThreads / 32;
-constexpr int kTpCoarse = 8;          // coarse bins of kTpFinePer fine bins
-constexpr int kTpFinePer = 256;       // 8 binades of 1/32 each
-constexpr int kTpFineAll = kTpCoarse * kTpFinePer;
+constexpr int kTpBins = 2048;         // 64 binades of weight in steps of 1/32
+constexpr int kTpBinsPer = kTpBins / kTpThreads;
 constexpr int kTpCap = 512;           // candidates ranked directly
 constexpr int kTpUnroll = 4;          // 16-byte loads in flight per thread
 constexpr float kTpQuant = 1099511627776.0f;  // 2^40
+static_assert(kTpBinsPer * kTpThreads == kTpBins, "bins per thread");
 
 typedef unsigned long long u64;
 
@@ -66,9 +71,14 @@ struct TpParams {
   int vec;            // rows are 16-byte aligned: vector loads and stores
   float c_hi, c_lo;   // log2(e) / T as a float-float pair
   double top_p;
+  int qbits;          // s: pass 2 scales bin f's weights by 2^(f/32 + s)
+  double win_eps;     // relative error bound of pass 2's cumulative masses
   int32_t *status;
 };
 
+// Per logit type: the element at position k of a 16-byte group, its value,
+// scalar loads and stores, and the packed maxima of pass 1 over one 32-bit
+// word (two 16-bit logits or one f32 logit).
 template <typename T>
 struct TpType;
 template <>
@@ -76,6 +86,7 @@ struct TpType<float> {
   static constexpr int G = 4;
   static constexpr uint32_t kSign = 0x80000000u, kMag = 0x7fffffffu, kInf = 0x7f800000u;
   static constexpr uint32_t kNegInf = 0xff800000u, kKeyMask = 0xffffffffu;
+  static constexpr uint32_t kNegInfWord = 0xff800000u;
   static constexpr bool kExactDiff = false;   // x - m needs a two-sum
   static __device__ __forceinline__ uint32_t get(const uint4 &r, int k) { return (&r.x)[k]; }
   static __device__ __forceinline__ float val(uint32_t b) { return __uint_as_float(b); }
@@ -83,12 +94,25 @@ struct TpType<float> {
     return __float_as_uint(__ldg(static_cast<const float *>(p) + e));
   }
   static __device__ __forceinline__ void st1(void *p, int e, uint32_t b) { static_cast<uint32_t *>(p)[e] = b; }
+  static __device__ __forceinline__ uint32_t pmax(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.f32 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+  }
+  static __device__ __forceinline__ uint32_t pmax_nan(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.NaN.f32 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+  }
+  static __device__ __forceinline__ float word_max(uint32_t w) { return __uint_as_float(w); }
+  static __device__ __forceinline__ bool word_nan(uint32_t w) { return (w & kMag) > kInf; }
 };
 template <>
 struct TpType<__nv_bfloat16> {
   static constexpr int G = 8;
   static constexpr uint32_t kSign = 0x8000u, kMag = 0x7fffu, kInf = 0x7f80u;
   static constexpr uint32_t kNegInf = 0xff80u, kKeyMask = 0xffffu;
+  static constexpr uint32_t kNegInfWord = 0xff80ff80u;
   // x - m of two bf16 values is exact in fp32 unless their binades are more
   // than 16 apart; then |x| < 2^-16 |m| and the rounding (an ulp of m) moves
   // the weight of such a token by ~1e-6 relative, and such tokens carry a
@@ -105,12 +129,29 @@ struct TpType<__nv_bfloat16> {
   static __device__ __forceinline__ void st1(void *p, int e, uint32_t b) {
     static_cast<unsigned short *>(p)[e] = (unsigned short)b;
   }
+  static __device__ __forceinline__ uint32_t pmax(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+  }
+  static __device__ __forceinline__ uint32_t pmax_nan(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+  }
+  static __device__ __forceinline__ float word_max(uint32_t w) {
+    return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  static __device__ __forceinline__ bool word_nan(uint32_t w) {
+    return (w & kMag) > kInf || ((w >> 16) & kMag) > kInf;
+  }
 };
 template <>
 struct TpType<__half> {
   static constexpr int G = 8;
   static constexpr uint32_t kSign = 0x8000u, kMag = 0x7fffu, kInf = 0x7c00u;
   static constexpr uint32_t kNegInf = 0xfc00u, kKeyMask = 0xffffu;
+  static constexpr uint32_t kNegInfWord = 0xfc00fc00u;
   static constexpr bool kExactDiff = true;    // 11-bit significands: as for bf16
   static __device__ __forceinline__ uint32_t get(const uint4 &r, int k) {
     const uint32_t w = (&r.x)[k >> 1];
@@ -125,6 +166,22 @@ struct TpType<__half> {
   static __device__ __forceinline__ void st1(void *p, int e, uint32_t b) {
     static_cast<unsigned short *>(p)[e] = (unsigned short)b;
   }
+  static __device__ __forceinline__ uint32_t pmax(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+  }
+  static __device__ __forceinline__ uint32_t pmax_nan(uint32_t a, uint32_t b) {
+    uint32_t y;
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+    return y;
+  }
+  static __device__ __forceinline__ float word_max(uint32_t w) {
+    return fmaxf(val(w & 0xffffu), val(w >> 16));
+  }
+  static __device__ __forceinline__ bool word_nan(uint32_t w) {
+    return (w & kMag) > kInf || ((w >> 16) & kMag) > kInf;
+  }
 };
 
 __device__ __forceinline__ float tp_ex2(float x) {
@@ -133,28 +190,29 @@ __device__ __forceinline__ float tp_ex2(float x) {
   return y;
 }
 
-// Canonical bits: NaN becomes -inf (and is reported), -0 becomes +0.
+// Canonical bits: NaN becomes -inf, -0 becomes +0.
 template <typename T>
-__device__ __forceinline__ uint32_t tp_canon(uint32_t b, bool &nan) {
+__device__ __forceinline__ uint32_t tp_canon(uint32_t b) {
   using TT = TpType<T>;
-  nan = (b & TT::kMag) > TT::kInf;
-  if (nan) b = TT::kNegInf;
+  if ((b & TT::kMag) > TT::kInf) b = TT::kNegInf;
   if (b == TT::kSign) b = 0u;
   return b;
 }
 
 template <typename T>
-__device__ __forceinline__ u64 tp_composite(uint32_t canon, int id) {
+__device__ __forceinline__ u64 tp_composite(uint32_t b, int id) {
   using TT = TpType<T>;
+  const uint32_t canon = tp_canon<T>(b);
   const uint32_t key = (canon & TT::kSign) ? (~canon & TT::kKeyMask) : (canon | TT::kSign);
   return ((u64)key << 32) | (u64)(0xffffffffu - (uint32_t)id);
 }
 
 // Calls f(e0, r, nv) for every group of a row of V elements: r holds the
 // elements e0 .. e0 + nv - 1 packed as in memory (nv = G except in the last
-// group). Full 16-byte groups go round-robin over the threads, kTpUnroll
-// loads in flight per thread; the ragged end (and the whole row when it is
-// not 16-byte aligned) is loaded one element at a time.
+// group); the lanes of a short group past nv hold -inf. Full 16-byte groups go
+// round-robin over the threads, kTpUnroll loads in flight per thread; the
+// ragged end (and the whole row when it is not 16-byte aligned) is loaded one
+// element at a time.
 template <typename T, typename F>
 __device__ __forceinline__ void tp_row_groups(const void *row, int V, int vec, F f) {
   using TT = TpType<T>;
@@ -172,13 +230,17 @@ __device__ __forceinline__ void tp_row_groups(const void *row, int V, int vec, F
   for (; g < ng; g += kTpThreads) f(g * G, __ldg(rv + g), G);
   for (int h = ng + (int)threadIdx.x; h * G < V; h += kTpThreads) {
     const int nv = min(G, V - h * G);
-    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    uint4 r = make_uint4(TT::kNegInfWord, TT::kNegInfWord, TT::kNegInfWord, TT::kNegInfWord);
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       if (k < nv) {
         const uint32_t b = TT::ld1(row, h * G + k);
-        if (sizeof(T) == 4) (&r.x)[k] = b;
-        else (&r.x)[k >> 1] |= b << ((k & 1) * 16);
+        if (sizeof(T) == 4) {
+          (&r.x)[k] = b;
+        } else {
+          const int sh = (k & 1) * 16;
+          (&r.x)[k >> 1] = ((&r.x)[k >> 1] & ~(0xffffu << sh)) | (b << sh);
+        }
       }
     }
     f(h * G, r, nv);
@@ -208,36 +270,46 @@ __device__ __forceinline__ u64 tp_block_excl_scan(u64 v, u64 *s_warp, u64 *total
   return before + incl - v;
 }
 
-// Over entries h[phys(0)], h[phys(1)], ... (n <= kTpThreads of them, thread
-// i holding entry i), the entry where the running mass from `above` first
-// reaches thr: writes phys(i) to *s_sel and the mass before it to *s_above.
-template <typename Phys>
-__device__ __forceinline__ void tp_cross(const u64 *h, int n, Phys phys, u64 above, u64 thr, u64 *s_warp,
-                                         int *s_sel, u64 *s_above) {
-  const int i = threadIdx.x;
-  const u64 mine = i < n ? h[phys(i)] : 0ull;
-  u64 tot;
-  const u64 cum = above + tp_block_excl_scan(mine, s_warp, &tot);
-  if (i < n && cum < thr && thr <= cum + mine) {
-    *s_sel = phys(i);
-    *s_above = cum;
-  }
+// Compensated (Kahan) addition of w to the fp32 pair (s, c): s - c tracks
+// the exact sum to about two ulps of it.
+__device__ __forceinline__ void tp_kahan(float &s, float &c, float w) {
+  const float y = w - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
+// Sum over the block of one double per thread, in a fixed order (so every
+// run gives the same bits); every thread gets the total.
+__device__ __forceinline__ double tp_block_sum_d(double v, double *s_wd) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) s_wd[warp] = v;
   __syncthreads();
+  double tot = 0.0;
+#pragma unroll
+  for (int w = 0; w < kTpWarps; ++w) tot += s_wd[w];
+  __syncthreads();
+  return tot;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kTpThreads, 2) topp_row_kernel(const __grid_constant__ TpParams P) {
   using TT = TpType<T>;
-  __shared__ u64 acc[kTpCoarse][kTpThreads];   // per-thread coarse masses
-  __shared__ u64 h_fine[256];                  // fine (or radix) histogram
+  constexpr int G = TT::G;
+  __shared__ unsigned hist[kTpBins];           // approximate masses per fine bin, fixed point
+  __shared__ float s_tbl[kTpBins];             // 2^(f/32 + s): the fixed-point scale of bin f
+  __shared__ u64 rhist[256];                   // masses per radix digit (the rare split)
   __shared__ u64 c_comp[kTpCap];               // gathered candidates
   __shared__ u64 c_q[kTpCap];
+  __shared__ int c_pos[kTpCap];
   __shared__ u64 s_warp64[kTpWarps];
+  __shared__ double s_wd[kTpWarps];
   __shared__ float s_wmax[kTpWarps];
   __shared__ int s_wflag[kTpWarps];
-  __shared__ int s_sel;
-  __shared__ u64 s_above;
-  __shared__ u64 s_cut;
+  __shared__ int s_flo, s_fhi, s_sel;
+  __shared__ u64 s_above_q, s_cut, s_cmax, s_cmin;
   __shared__ unsigned s_count;
 
   pdl_wait();
@@ -255,32 +327,35 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_row_kernel(const __grid_co
   const int V = P.V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  // ---- 1. row maximum (NaN is flagged; fmaxf ignores it) ----
-  float mx = -INFINITY;
-  int flag = 0;
-  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int nv) {
+  // ---- 1. row maximum (max ignores NaN; max.NaN propagates it, for the flag) ----
+  uint32_t wmax = TT::kNegInfWord, wnan = TT::kNegInfWord;
+  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
 #pragma unroll
-    for (int k = 0; k < TT::G; ++k) {
-      if (k < nv) {
-        const uint32_t b = TT::get(r, k);
-        const float x = TT::val(b);
-        flag |= ((b & TT::kMag) > TT::kInf) ? 1 : 0;
-        flag |= (x == INFINITY) ? 2 : 0;
-        mx = fmaxf(mx, x);
-      }
+    for (int j = 0; j < 4; ++j) {
+      wmax = TT::pmax(wmax, (&r.x)[j]);
+      wnan = TT::pmax_nan(wnan, (&r.x)[j]);
     }
   });
-  mx = warp_max(mx);
-  flag = (int)__reduce_or_sync(0xffffffffu, (unsigned)flag);
-  if (lane == 0) { s_wmax[warp] = mx; s_wflag[warp] = flag; }
-  for (int i = threadIdx.x; i < kTpCoarse * kTpThreads; i += kTpThreads) (&acc[0][0])[i] = 0ull;
-  if (threadIdx.x == 0) { s_count = 0u; s_sel = -1; s_above = 0ull; s_cut = 0ull; }
+  for (int i = threadIdx.x; i < kTpBins; i += kTpThreads) {
+    hist[i] = 0u;
+    s_tbl[i] = exp2f((float)i * 0.03125f + (float)P.qbits);
+  }
+  if (threadIdx.x == 0) {
+    s_count = 0u; s_sel = -1; s_flo = 0; s_fhi = kTpBins - 2;
+    s_above_q = 0ull; s_cut = 0ull; s_cmax = 0ull; s_cmin = ~0ull;
+  }
+  {
+    float mx = warp_max(TT::word_max(wmax));
+    int flag = TT::word_nan(wnan) ? 1 : 0;
+    flag = (int)__reduce_or_sync(0xffffffffu, (unsigned)flag);
+    if (lane == 0) { s_wmax[warp] = mx; s_wflag[warp] = flag; }
+  }
   __syncthreads();
   float m = -INFINITY;
-  flag = 0;
+  int flag = 0;
 #pragma unroll
   for (int w = 0; w < kTpWarps; ++w) { m = fmaxf(m, s_wmax[w]); flag |= s_wflag[w]; }
-  if (flag && threadIdx.x == 0) atomic_or_status(P.status, SV_DEV_NONFINITE);
+  if ((flag || m == INFINITY) && threadIdx.x == 0) atomic_or_status(P.status, SV_DEV_NONFINITE);
 
   if (!(m > -INFINITY) || m == INFINITY) {
     // nothing to rank (no finite logit, or a +inf one): the row is passed
@@ -288,234 +363,292 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_row_kernel(const __grid_co
     if (out != in)
       tp_row_groups<T>(in, V, 0, [&](int e0, const uint4 &r, int nv) {
 #pragma unroll
-        for (int k = 0; k < TT::G; ++k)
+        for (int k = 0; k < G; ++k)
           if (k < nv) TT::st1(out, e0 + k, TT::get(r, k));
       });
     return;
   }
 
-  // Fine bin of a logit x: round(32 (fl(m c_hi) - x c_hi)) from one fma onto
-  // the integer grid of [2^23, 2^24), capped at the last fine bin; it is
-  // non-increasing in x, needs no conversion instruction, and puts -inf and
-  // NaN (fminf drops the NaN) in the last bin, which takes no mass.
-  // Weight: 2^ex with ex = (x - m) c taken as hi + lo (c = c_hi + c_lo, an fma
-  // for the product's rounding, a two-sum for x - m where it is not exact);
-  // 2^hi from the SFU (relative error below 1.5e-7 on [-30, 0]), 2^lo as the
-  // first-order factor 1 + lo ln 2 (|lo| is about an ulp of hi).
+  // Bin of a logit x: d = x - m (<= 0), h = d c_hi (<= 0, the exponent of the
+  // weight), bin = round(-32 h) from one fma onto the integer grid of
+  // [2^23, 2^24), capped at the last bin. Each step rounds monotonically, so
+  // the bin is non-increasing in x; -inf and NaN (fminf drops the NaN) land in
+  // the last bin, as do weights below 2^-63.98, which take no part.
+  // Weight: 2^(d c) with d c taken as h + lo (c = c_hi + c_lo, an fma for the
+  // product's rounding, a two-sum for x - m where it is not exact); 2^h from
+  // the SFU (relative error below 1.5e-7 on [-64, 0]), 2^lo as the first-order
+  // factor 1 + lo ln 2 (|lo| is about an ulp of h).
   const float c_hi = P.c_hi, c_lo = P.c_lo;
-  const float mc = __fmul_rn(m, c_hi);
-  const float c32 = 32.f * c_hi;                    // exact (a power of two)
-  const float mc32 = fmaf(32.f, mc, 8388608.f);     // 32 mc + 2^23, exact when |32 mc| < 2^22
-  const float top = 8388608.f + (float)(kTpFineAll - 1);
-  // (fminf first, so NaN goes to the last bin; the fmaxf keeps bins >= 0 when
-  // the rounding of mc32 at huge |m c| pushes the maximum just below 2^23)
-  auto fine_of = [&](float x) {
-    return __float_as_int(fmaxf(fminf(fmaf(-x, c32, mc32), top), 8388608.f)) - 0x4B000000;
+  const float top = 8388608.f + (float)(kTpBins - 1);
+  auto bin_of = [&](float x, float &d, float &h) {
+    d = __fsub_rn(x, m);
+    h = __fmul_rn(d, c_hi);
+    return __float_as_int(fminf(fmaf(h, -32.f, 8388608.f), top)) - 0x4B000000;
   };
-  auto mass_of = [&](float x) -> u64 {
-    const float d = x - m;
-    float d_lo = 0.f;
-    if (!TT::kExactDiff) {
-      const float bb = d - x;
-      d_lo = (x - (d - bb)) + (-m - bb);
-    }
-    const float h = d * c_hi;
+  auto weight_of = [&](float x, float d, float h) -> float {
     float l = fmaf(d, c_hi, -h);
     l = fmaf(d, c_lo, l);
-    if (!TT::kExactDiff) l = fmaf(d_lo, c_hi, l);
+    if (!TT::kExactDiff) {
+      const float bb = d - x;
+      const float d_lo = (x - (d - bb)) + (-m - bb);
+      l = fmaf(d_lo, c_hi, l);
+    }
     const float t = tp_ex2(h);
-    if (!(t > 0.f)) return 0ull;   // also -inf and NaN
-    return __float2ull_rn(fmaf(t, l * 0.693147180559945309f, t) * kTpQuant);
-  };
-  auto comp_of = [&](uint32_t b, int e) {
-    bool nan;
-    return tp_composite<T>(tp_canon<T>(b, nan), e);
+    return fmaf(t, l * 0.693147180559945309f, t);
   };
 
-  // ---- 2. coarse masses, private per thread ----
-  u64 *my_acc = &acc[0][threadIdx.x];
-  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int nv) {
+  // ---- 2. Z, and approximate masses per bin ----
+  // Z: compensated fp32 sums per thread, combined in fp64. Bin f: the weights
+  // w (within 2^(+-1/64) of 2^(-f/32)) scaled by 2^(f/32 + s) and rounded to
+  // integers, summed with 32-bit shared atomics (order-independent); with s
+  // chosen so that V 2^(s + 1/64) < 2^31 the sums cannot overflow, and a bin's
+  // sum over 2^(f/32 + s) is within 2^-(s+1) 2^(1/64) (relative) of the exact
+  // mass of the bin.
+  float zs = 0.f, zc = 0.f;
+  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
 #pragma unroll
-    for (int k = 0; k < TT::G; ++k) {
-      if (k < nv) {
-        const float x = TT::val(TT::get(r, k));
-        const int fb = fine_of(x);
-        if (fb < kTpFineAll - 1) my_acc[(fb >> 8) * kTpThreads] += mass_of(x);
+    for (int k = 0; k < G; ++k) {
+      const float x = TT::val(TT::get(r, k));
+      float d, h;
+      const int fb = bin_of(x, d, h);
+      if (fb < kTpBins - 1) {
+        const float w = weight_of(x, d, h);
+        tp_kahan(zs, zc, w);
+        const float v = fmaf(w, s_tbl[fb], 8388608.f);   // round(w 2^(f/32 + s)) + 2^23
+        atomicAdd(&hist[fb], (unsigned)__float_as_uint(v) - 0x4B000000u);
       }
     }
   });
-  __syncthreads();
-  // block sums of the coarse bins: warp w adds half of bin w / 2
+  const double Z = tp_block_sum_d((double)zs - (double)zc, s_wd);   // also orders hist's atomics
+  const double thr = P.top_p * Z;
   {
-    const int cb = warp >> 1, base = (warp & 1) * (kTpThreads / 2);
-    u64 sum = 0;
+    // the window [f_lo, f_hi] that must hold the bin where the running mass
+    // reaches thr: cumulative approximate masses in 2^-32 fixed point (exact
+    // u64 scan), widened by their error bound
+    u64 a[kTpBinsPer];
+    u64 part = 0;
 #pragma unroll
-    for (int j = 0; j < kTpThreads / 64; ++j) sum += acc[cb][base + lane + 32 * j];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) s_warp64[warp] = sum;
-  }
-  __syncthreads();
-  u64 coarse[kTpCoarse];
-  u64 Z = 0;
-#pragma unroll
-  for (int c = 0; c < kTpCoarse; ++c) {
-    coarse[c] = s_warp64[2 * c] + s_warp64[2 * c + 1];
-    Z += coarse[c];
-  }
-  u64 thr = (u64)ceil(P.top_p * (double)Z);
-  thr = thr < 1ull ? 1ull : (thr > Z ? Z : thr);
-  int cbin = -1;
-  u64 above = 0;
-  {
-    u64 cum = 0;
-#pragma unroll
-    for (int c = 0; c < kTpCoarse; ++c) {
-      if (cbin < 0 && cum < thr && thr <= cum + coarse[c]) { cbin = c; above = cum; }
-      cum += coarse[c];
+    for (int j = 0; j < kTpBinsPer; ++j) {
+      const int f = threadIdx.x * kTpBinsPer + j;
+      a[j] = __float2ull_rn((float)hist[f] / s_tbl[f] * 4294967296.f);
+      part += a[j];
     }
-  }
-  __syncthreads();   // s_warp64 is reused below
-
-  // ---- 3. fine histogram of the crossing coarse bin ----
-  for (int i = threadIdx.x; i < kTpFinePer; i += kTpThreads) h_fine[i] = 0ull;
-  __syncthreads();
-  const int f0 = cbin * kTpFinePer;
-  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int nv) {
+    u64 tot;
+    u64 cum = tp_block_excl_scan(part, s_warp64, &tot);
+    const double err = Z * 4294967296.0 * P.win_eps;
+    const double lo_t = thr * 4294967296.0 - err, hi_t = thr * 4294967296.0 + err;
+    const u64 lo_u = lo_t <= 0.0 ? 0ull : (u64)lo_t, hi_u = (u64)ceil(hi_t);
 #pragma unroll
-    for (int k = 0; k < TT::G; ++k) {
-      if (k < nv) {
-        const float x = TT::val(TT::get(r, k));
-        const unsigned rel = (unsigned)(fine_of(x) - f0);
-        if (rel < (unsigned)kTpFinePer) {
-          const u64 q = mass_of(x);
-          if (q) atomicAdd(&h_fine[rel], q);
-        }
-      }
-    }
-  });
-  __syncthreads();
-  tp_cross(h_fine, kTpFinePer, [](int i) { return i; }, above, thr, s_warp64, &s_sel, &s_above);
-  const int fbin = s_sel >= 0 ? f0 + s_sel : -1;   // -1 only if nothing reached thr (not expected)
-  above = s_above;
-
-  // ---- 4. gather the fine bin's tokens (one vote per group) and rank them ----
-  int sh = 64;        // radix split: the composite's bits at and above sh equal pfx
-  u64 pfx = 0ull;
-  auto gather_pass = [&]() {
-    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
-      unsigned cm = 0;
-#pragma unroll
-      for (int k = 0; k < TT::G; ++k) {
-        if (k < nv && fine_of(TT::val(TT::get(r, k))) == fbin &&
-            (sh >= 64 || (comp_of(TT::get(r, k), e0 + k) >> sh) == pfx))
-          cm |= 1u << k;
-      }
-      const unsigned am = __activemask();
-      if (!__ballot_sync(am, cm != 0u)) return;
-#pragma unroll 1
-      for (int k = 0; k < TT::G; ++k) {
-        const bool cand = (cm >> k) & 1u;
-        const unsigned bal = __ballot_sync(am, cand);
-        if (!bal) continue;
-        const int leader = __ffs(bal) - 1;
-        unsigned base = 0;
-        if (lane == leader) base = atomicAdd(&s_count, (unsigned)__popc(bal));
-        base = __shfl_sync(am, base, leader);
-        if (cand) {
-          const unsigned slot = base + (unsigned)__popc(bal & ((1u << lane) - 1u));
-          if (slot < (unsigned)kTpCap) {
-            const uint32_t b = TT::get(r, k);
-            c_comp[slot] = comp_of(b, e0 + k);
-            c_q[slot] = mass_of(TT::val(b));
-          }
-        }
-      }
-    });
-    __syncthreads();
-  };
-  gather_pass();
-  int n_all = (int)s_count;
-  while (n_all > kTpCap && sh > 0) {
-    // Rare: more than kTpCap tokens in the fine bin (many equal or nearly
-    // equal logits). Split them by the next 8 bits of the composite, keep the
-    // part where the running mass reaches thr, and gather again.
-    const int nsh = sh > 8 ? sh - 8 : 0;
-    const int width = sh - nsh;
-    for (int i = threadIdx.x; i < 256; i += kTpThreads) h_fine[i] = 0ull;
-    if (threadIdx.x == 0) { s_count = 0u; s_sel = -1; }
-    __syncthreads();
-    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
-#pragma unroll
-      for (int k = 0; k < TT::G; ++k) {
-        if (k < nv) {
-          const uint32_t b = TT::get(r, k);
-          const float x = TT::val(b);
-          if (fine_of(x) != fbin) continue;
-          const u64 comp = comp_of(b, e0 + k);
-          if (sh < 64 && (comp >> sh) != pfx) continue;
-          const u64 q = mass_of(x);
-          if (q) atomicAdd(&h_fine[(int)((comp >> nsh) & ((1ull << width) - 1ull))], q);
-        }
-      }
-    });
-    __syncthreads();
-    tp_cross(h_fine, 256, [](int i) { return 255 - i; }, above, thr, s_warp64, &s_sel, &s_above);
-    above = s_above;
-    pfx = (sh >= 64 ? 0ull : (pfx << width)) | (u64)(s_sel < 0 ? 0 : s_sel);
-    sh = nsh;
-    gather_pass();
-    n_all = (int)s_count;
-  }
-  if (n_all <= kTpCap) {
-    // candidate i is the cut iff the mass before it (everything in higher
-    // bins and radix parts, plus every candidate with a larger composite) is
-    // below thr and reaches thr with it
-    for (int i = threadIdx.x; i < n_all; i += kTpThreads) {
-      const u64 ci = c_comp[i], qi = c_q[i];
-      u64 before = 0;
-      for (int j = 0; j < n_all; ++j) before += (c_comp[j] > ci) ? c_q[j] : 0ull;
-      if (above + before < thr && thr <= above + before + qi) s_cut = ci;
+    for (int j = 0; j < kTpBinsPer; ++j) {
+      const int f = threadIdx.x * kTpBinsPer + j;
+      if (cum < lo_u && lo_u <= cum + a[j]) s_flo = f;
+      if (cum < hi_u && hi_u <= cum + a[j]) s_fhi = f;
+      cum += a[j];
     }
   }
   __syncthreads();
-  const u64 cut = s_cut;   // 0: no cut found, the row is kept whole
+  const int f_lo = s_flo, f_hi = max(s_flo, min(s_fhi, kTpBins - 2));
 
-  // ---- 5. write the filtered row: fine bins above the cut's stay, bins
-  // below go (NaN and -inf are in the last bin), the composite decides in it ----
+  // ---- 3. write the row: bins above the window stay (their accurate masses
+  // summed, compensated, into `above`), bins below go (NaN and -inf are in
+  // the last bin), the window's tokens stay for now and are gathered
+  // (composite, mass in 2^-40 fixed point, position) ----
+  float as = 0.f, ac = 0.f;
   tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
-    uint32_t ob[TT::G];
+    uint32_t ob[G];
+    unsigned cm = 0;
 #pragma unroll
-    for (int k = 0; k < TT::G; ++k) {
+    for (int k = 0; k < G; ++k) {
       const uint32_t b = TT::get(r, k);
-      const int fb = fine_of(TT::val(b));
-      const bool nan = (b & TT::kMag) > TT::kInf;
-      const bool keep = cut == 0ull ? !nan : (fb < fbin || (fb == fbin && comp_of(b, e0 + k) >= cut));
-      ob[k] = keep ? b : TT::kNegInf;
+      const float x = TT::val(b);
+      float d, h;
+      const int fb = bin_of(x, d, h);
+      const float w = weight_of(x, d, h);
+      tp_kahan(as, ac, fb < f_lo ? w : 0.f);
+      ob[k] = fb <= f_hi ? b : TT::kNegInf;
+      cm |= (fb >= f_lo && fb <= f_hi && k < nv) ? 1u << k : 0u;
     }
-    if (P.vec && nv == TT::G) {
+    if (P.vec && nv == G) {
       uint4 o;
       if (sizeof(T) == 4) {
-        o = make_uint4(ob[0], ob[1 % TT::G], ob[2 % TT::G], ob[3 % TT::G]);
+        o = make_uint4(ob[0], ob[1 % G], ob[2 % G], ob[3 % G]);
       } else {
 #pragma unroll
-        for (int k = 0; k < TT::G; k += 2) (&o.x)[k >> 1] = ob[k] | (ob[(k + 1) % TT::G] << 16);
+        for (int k = 0; k < G; k += 2) (&o.x)[k >> 1] = ob[k] | (ob[(k + 1) % G] << 16);
       }
       *reinterpret_cast<uint4 *>(static_cast<T *>(out) + e0) = o;
     } else {
 #pragma unroll
-      for (int k = 0; k < TT::G; ++k)
+      for (int k = 0; k < G; ++k)
         if (k < nv) TT::st1(out, e0 + k, ob[k]);
     }
+    if (cm) {
+      unsigned slot = atomicAdd(&s_count, (unsigned)__popc(cm));
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (((cm >> k) & 1u) && slot < (unsigned)kTpCap) {
+          const uint32_t b = TT::get(r, k);
+          const float x = TT::val(b);
+          float d, h;
+          bin_of(x, d, h);
+          c_comp[slot] = tp_composite<T>(b, e0 + k);
+          c_q[slot] = __float2ull_rn(weight_of(x, d, h) * kTpQuant);
+          c_pos[slot] = e0 + k;
+        }
+        slot += (cm >> k) & 1u;
+      }
+    }
   });
+  // the mass above the window, in 2^-40 units as a double (the block sum
+  // also orders the gathers above before the reads below)
+  const double above = tp_block_sum_d((double)as - (double)ac, s_wd) * (double)kTpQuant;
+  const double thr_q = thr * (double)kTpQuant;
+
+  // ---- the rare split: more than kTpCap tokens in the window (many equal
+  // or nearly equal logits). Histogram them by the next 8 bits of the
+  // composite, keep the digit where the running mass reaches thr, and gather
+  // again. Bins outside the window were final after pass 3 and the window's
+  // logits are unchanged in `in` (also when out == in), so the passes read
+  // `in`. ----
+  int sh = 64;        // the composite's bits at and above sh equal pfx
+  u64 pfx = 0ull;
+  u64 above_q = 0ull; // exact mass of the window's tokens above the prefix
+  int n_all = (int)s_count;
+  auto in_window = [&](uint32_t b, int e, u64 &comp) {
+    float d, h;
+    const int fb = bin_of(TT::val(b), d, h);
+    if (fb < f_lo || fb > f_hi) return false;
+    comp = tp_composite<T>(b, e);
+    return sh >= 64 || (comp >> sh) == pfx;
+  };
+  while (n_all > kTpCap && sh > 0) {
+    const int nsh = sh > 8 ? sh - 8 : 0;
+    const int width = sh - nsh;
+    __syncthreads();   // every thread has read s_count and s_sel before they are reset
+    for (int i = threadIdx.x; i < 256; i += kTpThreads) rhist[i] = 0ull;
+    if (threadIdx.x == 0) { s_count = 0u; s_sel = -1; }
+    __syncthreads();
+    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const uint32_t b = TT::get(r, k);
+        u64 comp;
+        if (k < nv && in_window(b, e0 + k, comp)) {
+          const float x = TT::val(b);
+          float d, h;
+          bin_of(x, d, h);
+          atomicAdd(&rhist[(int)((comp >> nsh) & ((1ull << width) - 1ull))],
+                    __float2ull_rn(weight_of(x, d, h) * kTpQuant));
+        }
+      }
+    });
+    __syncthreads();
+    {
+      // digits in descending order: entry i is digit 255 - i
+      const int i = threadIdx.x;
+      const u64 mine = i < 256 ? rhist[255 - i] : 0ull;
+      u64 tot;
+      const u64 cum = above_q + tp_block_excl_scan(mine, s_warp64, &tot);
+      if (i < 256 && mine > 0ull && above + (double)cum < thr_q && thr_q <= above + (double)(cum + mine)) {
+        s_sel = 255 - i;
+        s_above_q = cum;
+      }
+      __syncthreads();
+      const int sel0 = s_sel;
+      __syncthreads();   // read by every thread before thread 0 may write it
+      if (sel0 < 0) {
+        if (threadIdx.x == 0) {
+          const bool before_all = above + (double)above_q >= thr_q;
+          u64 c = above_q;
+          for (int dgt = 255; dgt >= 0; --dgt) {
+            if (rhist[dgt] == 0ull) continue;
+            if (before_all) { s_sel = dgt; s_above_q = c; break; }
+            s_sel = dgt; s_above_q = c;   // keeps the last nonempty digit
+            c += rhist[dgt];
+          }
+        }
+        __syncthreads();
+      }
+    }
+    above_q = s_above_q;
+    pfx = (sh >= 64 ? 0ull : (pfx << width)) | (u64)(s_sel < 0 ? 0 : s_sel);
+    sh = nsh;
+    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+      unsigned cm = 0;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        u64 comp;
+        if (k < nv && in_window(TT::get(r, k), e0 + k, comp)) cm |= 1u << k;
+      }
+      if (cm) {
+        unsigned slot = atomicAdd(&s_count, (unsigned)__popc(cm));
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+          if (((cm >> k) & 1u) && slot < (unsigned)kTpCap) {
+            const uint32_t b = TT::get(r, k);
+            const float x = TT::val(b);
+            float d, h;
+            bin_of(x, d, h);
+            c_comp[slot] = tp_composite<T>(b, e0 + k);
+            c_q[slot] = __float2ull_rn(weight_of(x, d, h) * kTpQuant);
+            c_pos[slot] = e0 + k;
+          }
+          slot += (cm >> k) & 1u;
+        }
+      }
+    });
+    __syncthreads();
+    n_all = (int)s_count;
+  }
+
+  // ---- the cut: candidate i is the cut iff the mass before it (everything
+  // above the window and the prefix, plus every candidate with a larger
+  // composite) is below thr and reaches thr with it ----
+  if (n_all <= kTpCap) {
+    for (int i = threadIdx.x; i < n_all; i += kTpThreads) {
+      const u64 ci = c_comp[i], qi = c_q[i];
+      u64 before = above_q;
+      for (int j = 0; j < n_all; ++j) before += (c_comp[j] > ci) ? c_q[j] : 0ull;
+      if (above + (double)before < thr_q && thr_q <= above + (double)(before + qi)) s_cut = ci;
+      atomicMax(&s_cmax, ci);
+      atomicMin(&s_cmin, ci);
+    }
+  }
+  __syncthreads();
+  u64 cut = s_cut;
+  if (cut == 0ull && n_all > 0 && n_all <= kTpCap) {
+    // rounding at the window's edge left no candidate that crosses thr: the
+    // first candidate when the mass above already reaches thr, else the last
+    cut = above + (double)above_q >= thr_q ? s_cmax : s_cmin;
+  }
+  if (cut == 0ull) return;   // not reached: the window is kept whole
+  if (sh == 64) {
+    // every token of the window was gathered: drop those below the cut
+    for (int i = threadIdx.x; i < n_all; i += kTpThreads)
+      if (c_comp[i] < cut) TT::st1(out, c_pos[i], TT::kNegInf);
+  } else {
+    // the split narrowed the candidates: drop the window's tokens below the cut
+    sh = 64;
+    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const uint32_t b = TT::get(r, k);
+        u64 comp;
+        if (k < nv && in_window(b, e0 + k, comp) && comp < cut) TT::st1(out, e0 + k, TT::kNegInf);
+      }
+    });
+  }
 }
 
 }  // namespace
 
 // Launches the filter over rows0 rows of in0 -> out0 followed by rows1 rows of
 // in1 -> out1 (all [rows][V] of one dtype). Host checks are the caller's.
-// In place (out == in) is allowed: a row's CTA reads its row in every pass but
-// writes it only in the last, and no CTA touches another row.
+// In place (out == in) is allowed: no CTA touches another row, and after a
+// row's pass 3 every later read of it only asks whether a logit is in fbin,
+// whose logits pass 3 leaves unchanged (and any other logit is in another bin
+// both before and after its write), so a read that still sees the old value
+// classifies it the same way.
 sv_status launch_topp_filter(sv_dtype dtype, const void *in0, void *out0, int rows0, const void *in1, void *out1,
                              int rows1, int V, float temperature, float top_p, int32_t *status, cudaStream_t s) {
   const int es = dtype_bytes(dtype);
@@ -530,6 +663,12 @@ sv_status launch_topp_filter(sv_dtype dtype, const void *in0, void *out0, int ro
   P.c_hi = (float)cd;
   P.c_lo = (float)(cd - (double)P.c_hi);
   P.top_p = (double)top_p;
+  // the largest s (at most 22, so that w 2^(f/32 + s) + 2^23 rounds to an
+  // integer) with V (2^(s + 1/64) + 1/2) < 2^32: no bin sum overflows
+  int qb = 22;
+  while (qb > 0 && (double)V * (std::ldexp(1.0111, qb) + 0.5) >= 4294967296.0) --qb;
+  P.qbits = qb;
+  P.win_eps = std::ldexp(1.0111, -(qb + 1)) + 4e-6;
   P.status = status;
   cudaError_t e = cudaSuccess;
   const dim3 grid(rows0 + rows1);
