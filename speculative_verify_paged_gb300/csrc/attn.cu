@@ -6,9 +6,14 @@
 // t <= L_b - n_new + j, K_t / V_t read through the block table.
 //
 // Design (flash-decoding style split-KV, CS336 lecture 10 section 9.2):
-//   * attn_order_kernel sorts the work items (split of a sequence's blocks,
-//     kv head, sequence) longest first;
-//   * attn_tc5_kernel, one CTA per work item on the fifth-generation tensor
+//   * work items are pieces of (sequence, kv head) pairs. With at least as
+//     many pairs as CTA slots (two per SM), attn_order_kernel sorts splits
+//     of a fixed size longest first and each CTA takes one. With fewer pairs
+//     (a small batch, long contexts) attn_part_kernel cuts the tiles of all
+//     sequences into equal ranges, one per CTA slot and kv head, and a CTA
+//     walks its range through one or more pairs, so every CTA streams the
+//     same number of tiles;
+//   * attn_tc5_kernel on the fifth-generation tensor
 //     cores: all (K+1)*G query rows of the GQA group share one M = 128 MMA
 //     tile, so every K/V byte is read from HBM once per step; two producer
 //     warps stream (block, head) K and V tiles with 4-D TMA tensor copies
@@ -19,8 +24,9 @@
 //     end of the split. bf16 caches feed the MMAs directly; fp8 e4m3 tiles
 //     are widened exactly to f16 by two converter warps, with k_scale folded
 //     into the score scale and v_scale into the output;
-//   * a split writes an unnormalised partial (acc, m, l) and the merge
-//     kernels combine them with the log-sum-exp rule
+//   * a piece that does not cover its whole pair writes an unnormalised
+//     partial (acc, m, l) and the merge kernels combine them with the
+//     log-sum-exp rule
 //     m = max m_s, l = sum l_s 2^(m_s - m), O = sum acc_s 2^(m_s - m) / l.
 // A plain CUDA-core kernel covers fp32 caches and shapes outside the
 // tensor-core path (any d_head <= 256, any block size).
@@ -98,7 +104,12 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   const int32_t *seq_lens;
   float *ws_acc;   // [B][H_kv][S][R][kD]
   float *ws_ml;    // [B][H_kv][S][R][2]
-  const int32_t *order;   // work items s + S (g + H_kv b), longest first (tcgen05 kernel)
+  const int32_t *order;   // split mode: work items s + S (g + H_kv b), longest first
+  const int4 *work;       // balanced mode: per CTA (b, g, first tile, tiles) of its tile range
+  int32_t *seq_pre_w;     // balanced mode: first tile of each sequence (written by the partition)
+  int4 *split_w;          // balanced mode: (count, T), then the sequences split across CTAs
+  int balanced;           // 1: CTA c takes tiles [c T / C, (c + 1) T / C) of all (b, g) pairs
+  int ncta;               // balanced mode: C
   const uint64_t *anc;    // [B][n_new] ancestor masks of a draft tree (NULL: a chain)
   int32_t *status;
   int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
@@ -120,7 +131,8 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 // read S and write P through TMEM, so no warp holds an accumulator in
 // registers.
 //
-// CTA = (split s, kv head g, sequence b), 256 threads (288 for fp8 caches):
+// CTA = its work items in order (one split, or a balanced range), 256
+// threads (288 for fp8 caches):
 //   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
 //              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
 //              and first writes that row of Q into TMEM
@@ -237,6 +249,77 @@ __device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile 
   return false;
 }
 
+// The work items of a CTA of the tcgen05 kernel: blocks [blk0, blk1) of kv
+// head g of sequence b. Split mode: one item, split s of (b, g) in the order
+// the order kernel wrote; its partial goes to entry (b H_kv + g) S + s.
+// Balanced mode: the sequence of 32-key tiles of all sequences in order is
+// cut into NR equal ranges, and CTA c runs range c / H_kv for kv head
+// c % H_kv, so every CTA streams the same number of tiles; a range may end
+// inside one sequence and go on through whole sequences into the next. A
+// piece of a (b, g) pair that another CTA shares writes a partial: entry 2c
+// for the CTA's first item, 2c + 1 for its last. Every role of the CTA walks
+// the same items in the same order.
+struct T5Item {
+  int b, g, blk0, blk1, L, nblk;
+  int64_t ent;   // partial entry
+  bool whole;    // the item covers all of (b, g): written directly
+};
+struct T5Walk {
+  int b, g, off, left, idx;
+};
+
+__device__ __forceinline__ bool t5_len_ok(const TcParams &P, int L) {
+  return L >= P.n_new && L <= P.max_blocks * kBS;
+}
+
+__device__ __forceinline__ bool t5_item(const TcParams &P, T5Walk &w, T5Item &it) {
+  if (!P.balanced) {
+    if (w.idx > 0) return false;
+    w.idx = 1;
+    const int item = __ldg(P.order + blockIdx.x);
+    const int s = item % P.S;
+    it.g = (item / P.S) % P.H_kv;
+    it.b = item / (P.S * P.H_kv);
+    it.L = P.seq_lens[it.b];
+    if (!t5_len_ok(P, it.L)) {
+      if (threadIdx.x == 0 && it.g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
+      return false;
+    }
+    it.nblk = (it.L + kBS - 1) / kBS;
+    it.blk0 = s * P.bps;
+    if (it.blk0 >= it.nblk) return false;   // the merge never reads this split
+    it.blk1 = min(it.nblk, it.blk0 + P.bps);
+    it.whole = it.nblk <= P.bps;
+    it.ent = ((int64_t)it.b * P.H_kv + it.g) * P.S + s;
+    return true;
+  }
+  if (w.idx == 0) {
+    const int4 wk = __ldg(P.work + blockIdx.x / P.H_kv);
+    w.b = wk.x; w.g = (int)(blockIdx.x % P.H_kv); w.off = wk.z; w.left = wk.w;
+  }
+  if (w.left <= 0) return false;
+  int L = 0, nt = 0;
+  for (;;) {   // sequences with invalid lengths hold no tiles
+    if (w.b >= P.B) return false;
+    L = P.seq_lens[w.b];
+    nt = t5_len_ok(P, L) ? ((L + kBS - 1) / kBS + kT5Blk - 1) / kT5Blk : 0;
+    if (nt > 0) break;
+    ++w.b;
+  }
+  const int take = min(nt - w.off, w.left);
+  it.b = w.b; it.g = w.g; it.L = L;
+  it.nblk = (L + kBS - 1) / kBS;
+  it.blk0 = w.off * kT5Blk;
+  it.blk1 = min(it.nblk, (w.off + take) * kT5Blk);
+  it.whole = w.off == 0 && take == nt;
+  it.ent = 2 * (int64_t)blockIdx.x + (w.idx > 0 ? 1 : 0);
+  w.left -= take;
+  w.off = 0;
+  ++w.b;   // the range goes on with the next sequence, same kv head
+  ++w.idx;
+  return true;
+}
+
 // Longest-first order of the tcgen05 kernel's work items. A work item is
 // split s of kv head g of sequence b; its work is its number of 32-key
 // tiles. One CTA counting-sorts the (s, b) pairs by descending work (kv heads
@@ -313,6 +396,102 @@ __global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *
   pdl_wait();
 }
 
+// Balanced partition for the tcgen05 kernel: one CTA. The global tile
+// sequence holds, for every sequence b in order, the ceil(ceil(L_b / 16) / 2)
+// 32-key tiles of b (none for an invalid length, which it flags). It is cut
+// into NR equal ranges, range r = [r T / NR, (r + 1) T / NR), and CTAs
+// r H_kv .. r H_kv + H_kv - 1 run range r for kv heads 0 .. H_kv - 1: the
+// CTAs reading the heads of one block run side by side, as the heads of a
+// block sit next to each other in the pool. work[r] = (b, 0, first tile
+// within b, tile count); seq_pre[b] is the first tile of sequence b
+// (seq_pre[B] = T), from which the merge finds a pair's pieces. Like the
+// order kernel it overlaps the previous kernel of the stream and waits for it
+// only before its first global write (the previous kernel may be a merge
+// that still reads this workspace).
+constexpr int kPartThreads = 1024;
+constexpr int kPartSmemB = 4096;   // prefixes kept in shared memory up to this batch
+__global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *seq_lens, int B, int n_new,
+                                                                 int max_blocks, int NR, int4 *work, int32_t *seq_pre,
+                                                                 int4 *split, int32_t *status) {
+  pdl_trigger();
+  __shared__ int s_pre[kPartSmemB + 1];
+  __shared__ int s_warp[kPartThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool big = B > kPartSmemB;
+  if (big) pdl_wait();
+  int carry = 0;
+  for (int base = 0; base < B; base += kPartThreads) {
+    const int b = base + tid;
+    int v = 0;
+    if (b < B) {
+      const int L = seq_lens[b];
+      if (L >= n_new && L <= max_blocks * kBS) v = ((L + kBS - 1) / kBS + kT5Blk - 1) / kT5Blk;
+      else atomic_or_status(status, SV_DEV_BAD_SEQ_LEN);
+    }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w = 0; w < kPartThreads / 32; ++w) {
+      const int x = s_warp[w];
+      before += w < warp ? x : 0;
+      tot += x;
+    }
+    if (b < B) {
+      const int ex = carry + before + incl - v;
+      if (big) seq_pre[b] = ex;
+      else s_pre[b] = ex;
+    }
+    carry += tot;
+    __syncthreads();
+  }
+  const int T = carry;
+  if (!big) {
+    pdl_wait();
+    for (int b = tid; b < B; b += kPartThreads) seq_pre[b] = s_pre[b];
+    if (tid == 0) s_pre[B] = T;
+  }
+  if (tid == 0) seq_pre[B] = T;
+  __syncthreads();
+  const int32_t *pre = big ? seq_pre : s_pre;
+  for (int r = tid; r < NR; r += kPartThreads) {
+    const int t0 = (int)((int64_t)r * T / NR), t1 = (int)((int64_t)(r + 1) * T / NR);
+    int4 wk = make_int4(0, 0, 0, 0);
+    if (t1 > t0) {
+      // the last sequence whose first tile is at or before t0 holds it
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= t0) lo = mid;
+        else hi = mid - 1;
+      }
+      wk = make_int4(lo, 0, t0 - pre[lo], t1 - t0);
+    }
+    work[r] = wk;
+  }
+  // the sequences that more than one range holds (each meets a range
+  // boundary, so there are at most NR - 1): split[1..n] = (b, first tile A,
+  // tiles nt, first range r0), split[0] = (n, T)
+  __shared__ int s_n;
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  if (T > 0) {
+    for (int b = tid; b < B; b += kPartThreads) {
+      const int64_t A = pre[b], nt = pre[b + 1] - pre[b];
+      const int64_t r0 = ((A + 1) * NR - 1) / T;
+      if (nt > 0 && ((A + nt) * NR - 1) / T > r0)
+        split[1 + atomicAdd(&s_n, 1)] = make_int4(b, (int)A, (int)nt, (int)r0);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) split[0] = make_int4(s_n, T, 0, 0);
+}
+
 template <int QR, bool FP8>
 __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
   pdl_wait();
@@ -328,30 +507,19 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  // the work item: split s of kv head g of sequence b, in the longest-first
-  // order the order kernel wrote (the CTAs launched first take the longest
-  // splits, so the last wave is made of the shortest ones)
-  const int item = __ldg(P.order + blockIdx.x);
-  const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    // a CTA with no work leaves before it sets anything up
+    T5Walk w0 = {};
+    T5Item it0;
+    if (!t5_item(P, w0, it0)) return;
+  }
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t k_ring = smem_u32(smem);
   const uint32_t v_ring = k_ring + KS * RAW;
   // the rings the MMAs read: the widened ones for FP8, else the TMA rings
   const uint32_t kc_ring = FP8 ? v_ring + VS * RAW : k_ring;
   const uint32_t vc_ring = FP8 ? kc_ring + CS * kT5TileBytes : v_ring;
-
-  const int L = P.seq_lens[b];
-  if (L < P.n_new || L > P.max_blocks * kBS) {
-    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
-    return;
-  }
-  const int nblk = (L + kBS - 1) / kBS;
-  const int blk0 = s * P.bps;
-  if (blk0 >= nblk) return;   // the merge never reads this split
-  const int blk1 = min(nblk, blk0 + P.bps);
-  const int nblocks = blk1 - blk0;
-  const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
   const int R = P.R;
 
   if (tid == 0) {
@@ -376,34 +544,42 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       mbar_init(&o_done[k], 1);
     }
     mbar_init(&mma_drain, 1);
-    mbar_init(&q_full, 4);   // the four softmax warps wrote their Q rows
+    mbar_init(&q_full, 4);   // the four softmax warps wrote their Q rows (one phase per item)
     abort_flag = 0;
     fence_mbarrier_init();
   }
   __syncthreads();
   volatile int *abf = &abort_flag;
+  // Every ring stage, S buffer and barrier phase below is indexed by the
+  // CTA's running tile count u over all its items, so the pipelines flow from
+  // one item into the next.
 
   if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ producers --
-    // warp 4 streams K, warp 5 streams V
-    {
-      // the whole warp walks the block table 32 entries at a time (the next
-      // 32 prefetched); lane 0 waits for free stages and issues the copies
-      const bool isv = warp == 5;
-      const int NS = isv ? VS : KS;
-      uint64_t *fullb = isv ? v_full : k_full;
-      uint64_t *emptyb = isv ? v_empty : k_empty;
-      const uint32_t ring = isv ? v_ring : k_ring;
-      const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
-      const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
+    // warp 4 streams K, warp 5 streams V; the whole warp walks the block
+    // table 32 entries at a time (the next 32 prefetched); lane 0 waits for
+    // free stages and issues the copies
+    const bool isv = warp == 5;
+    const int NS = isv ? VS : KS;
+    uint64_t *fullb = isv ? v_full : k_full;
+    uint64_t *emptyb = isv ? v_empty : k_empty;
+    const uint32_t ring = isv ? v_ring : k_ring;
+    const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
+    T5Walk wk = {};
+    T5Item it;
+    int u = 0, issued = 0;
+    bool go = true;
+    // (test hook: with the copies withheld every wait on them runs out,
+    // with nothing in flight)
+    const bool withhold = (P.withhold & SV_TEST_WITHHOLD_COPIES) != 0;
+    while (go && !withhold && t5_item(P, wk, it)) {
+      const int nblocks = it.blk1 - it.blk0;
+      const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+      const int32_t *table = P.block_table + (int64_t)it.b * P.max_blocks + it.blk0;
       int cur = lane < nblocks ? table[lane] : 0;
       int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
       int chunk = 0;
-      int issued = 0;
-      // (test hook: with the copies withheld every wait on them runs out,
-      // with nothing in flight)
-      const int n_issue = (P.withhold & SV_TEST_WITHHOLD_COPIES) ? 0 : n_tiles;
-      for (int t = 0; t < n_issue; ++t) {
+      for (int t = 0; t < n_tiles; ++t, ++u) {
         const int first = t * kT5Blk;
         if ((first >> 5) != chunk) {
           chunk = first >> 5;
@@ -414,10 +590,9 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
         int phys[kT5Blk];
 #pragma unroll
         for (int kk = 0; kk < kT5Blk; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
-        const int st = t % NS;
-        bool go = true;
+        const int st = u % NS;
         if (lane == 0) {
-          if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf, P.wait_ns)) {
+          if (u >= NS && !t5_wait(&emptyb[st], ((u / NS) & 1) ^ 1, abf, P.wait_ns)) {
             go = false;
           } else {
             const int nvalid = min(kT5Blk, nblocks - first);
@@ -432,20 +607,21 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
                 ph = 0;   // stay in bounds; the output of this sequence is flagged
               }
               int c[3];
-              tile_coords(P, g, ph, c);
+              tile_coords(P, it.g, ph, c);
               tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
               if (!FP8) tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
             }
-            issued = t + 1;
+            issued = u + 1;
           }
         }
-        if (!__shfl_sync(0xffffffffu, (int)go, 0)) break;
+        go = __shfl_sync(0xffffffffu, (int)go, 0) != 0;
+        if (!go) break;
       }
-      // the copies in flight land before the CTA may exit
-      if (lane == 0) {
-        for (int t = max(0, issued - NS); t < issued; ++t)
-          if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
-      }
+    }
+    // the copies in flight land before the CTA may exit
+    if (lane == 0) {
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
     }
   } else if (warp < 4 || warp == kT5MmaWarp) {
     if (warp == kT5MmaWarp) {
@@ -466,20 +642,28 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
         const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
         static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
-        int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
+        // Q K^T and P V each walk the items on their own: (item index, tiles
+        // of the item, next tile in it) and the running tile count
+        T5Walk wq = {}, wp = {};
+        T5Item iq, ip;
+        bool hq = t5_item(P, wq, iq), hp = t5_item(P, wp, ip);
+        int nq = hq ? (iq.blk1 - iq.blk0 + kT5Blk - 1) / kT5Blk : 0;
+        int np = hp ? (ip.blk1 - ip.blk0 + kT5Blk - 1) / kT5Blk : 0;
+        int xq = 0, tq_l = 0, tp_l = 0;   // item of Q K^T; tiles done in the current items
+        int uq = 0, up = 0;               // running tile counts
         bool q_ready = false;
         uint64_t t_last = global_ns();
-        while (tp < n_tiles) {
+        while (hp) {
           bool progressed = false;
-          if (!q_ready) q_ready = t5_test(&q_full, 0);
-          if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
+          if (hq && !q_ready) q_ready = t5_test(&q_full, xq & 1);
+          if (hq && q_ready && uq - up < kT5SBuf) {
             // K stage: the TMA ring (bf16) or the widened ring (FP8)
             const int KR = FP8 ? CS : KS;
-            const int ks = tq % KR, sb = tq % kT5SBuf;
+            const int ks = uq % KR, sb = uq % kT5SBuf;
             uint64_t *kf = FP8 ? kc_full : k_full;
-            // S buffer sb is free once the P V of tile tq - kT5SBuf has run
-            const bool sfree = tq < kT5SBuf || t5_test(&o_done[sb], ((tq / kT5SBuf) - 1) & 1);
-            if (sfree && t5_test(&kf[ks], (tq / KR) & 1)) {
+            // S buffer sb is free once the P V of tile uq - kT5SBuf has run
+            const bool sfree = uq < kT5SBuf || t5_test(&o_done[sb], ((uq / kT5SBuf) - 1) & 1);
+            if (sfree && t5_test(&kf[ks], (uq / KR) & 1)) {
               t5_fence_after();
               const uint32_t kb = kc_ring + ks * kT5TileBytes;
 #pragma unroll
@@ -489,24 +673,36 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
                           kk > 0 ? 1u : 0u);
               t5_commit(&s_full[sb]);
               t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
-              ++tq;
+              ++uq;
+              if (++tq_l == nq) {   // next item: its Q is written after this item's epilogue
+                hq = t5_item(P, wq, iq);
+                nq = hq ? (iq.blk1 - iq.blk0 + kT5Blk - 1) / kT5Blk : 0;
+                tq_l = 0;
+                ++xq;
+                q_ready = false;
+              }
               progressed = true;
             }
           }
-          if (tp < tq) {
+          if (up < uq) {
             const int VR = FP8 ? CS : VS;
-            const int vs = tp % VR, sb = tp % kT5SBuf;
+            const int vs = up % VR, sb = up % kT5SBuf;
             uint64_t *vf = FP8 ? vc_full : v_full;
-            if (t5_test(&p_full[sb], (tp / kT5SBuf) & 1) && t5_test(&vf[vs], (tp / VR) & 1)) {
+            if (t5_test(&p_full[sb], (up / kT5SBuf) & 1) && t5_test(&vf[vs], (up / VR) & 1)) {
               t5_fence_after();
               const uint32_t vb = vc_ring + vs * kT5TileBytes;
 #pragma unroll
-              for (int j = 0; j < kT5Blk; ++j)
+              for (int j = 0; j < kT5Blk; ++j)   // an item's first P V starts O afresh
                 t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
-                          idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
+                          idesc_pv, (tp_l > 0 || j > 0) ? 1u : 0u);
               t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
               t5_commit(&o_done[sb]);
-              ++tp;
+              ++up;
+              if (++tp_l == np) {
+                hp = t5_item(P, wp, ip);
+                np = hp ? (ip.blk1 - ip.blk0 + kT5Blk - 1) / kT5Blk : 0;
+                tp_l = 0;
+              }
               progressed = true;
             }
           }
@@ -530,233 +726,247 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       const bool warp_live = warp * 32 < R;
       const bool live = row < R;
       const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
-      const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
-      // draft tree: of the new keys, only the row's ancestors are visible
-      const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
-      const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
-      float sl2 = P.scale_log2;
-      {
-        // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
-        // order). tcgen05.st is warp-collective: a warp holding live rows
-        // stores all 32 (zeros for rows past R); warps with none skip it
-        // (their rows of S, P and O are never read).
-        if (warp_live) {
-          const uint4 *src = nullptr;
-          if (live) {
-            const int j = row / P.G, hh = row % P.G;
-            src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
-                                                  (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
-          }
-          if constexpr (FP8) {
-            // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
-            // in [2^14, 2^15): the f16 range then holds the whole row with no
-            // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
-            // exact, and 2^-s, k_scale and the softmax scale fold into the
-            // row's scale (values below 2^-31 of the maximum lose bits in the
-            // f16 subnormals; their products are far below the fp32 sum's
-            // rounding). Two passes over the row (the second from L1) keep
-            // few registers live.
-            float amax = 0.f;
-            if (live) {
-#pragma unroll 4
-              for (int k = 0; k < 16; ++k) {
-                const uint4 v = __ldg(src + k);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
-              }
-            }
-            const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
-            const float up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);     // 2^s, s = 14 - ex
-            const float down = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);   // 2^-s
-            sl2 *= P.k_scale[g] * down;
-            auto widen = [up](uint32_t w) {
-              return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
-            };
-#pragma unroll 1
-            for (int c0 = 0; c0 < 4; ++c0) {
-              uint32_t w[16];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint4 v = live ? __ldg(src + 4 * c0 + k) : make_uint4(0u, 0u, 0u, 0u);
-                w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
-                w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
-              }
-              t5_st16(lane_base + kT5QCol + 16 * c0, w);
-            }
-          } else {
-            uint4 qv[16];
-            if (live) {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int c0 = 0; c0 < 4; ++c0) {
-              uint32_t w[16];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
-                w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
-              }
-              t5_st16(lane_base + kT5QCol + 16 * c0, w);
-            }
-          }
-          t5_wait_st();
-        }
-        t5_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full);
-      }
-      float m_ref = -INFINITY, l = 0.f;
+      T5Walk wk = {};
+      T5Item it;
+      int u = 0;
       bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int sb = t % kT5SBuf, vs = t % VS;
-        ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (t / kT5SBuf) & 1, abf, P.wait_ns));
-        if (!ok) break;
-        t5_fence_after();
-        const int key0 = (blk0 + t * kT5Blk) * kBS;
-        if (warp_live) {
-          float x[kT5N];
-          {
-            uint32_t r[kT5N];
-#pragma unroll
-            for (int c0 = 0; c0 < kT5N; c0 += 16)
-              t5_ld16(lane_base + sb * kT5N + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
-            t5_wait_ld();
-#pragma unroll
-            for (int k = 0; k < kT5N; ++k) x[k] = __uint_as_float(r[k]) * sl2;
-          }
-          if (key0 + kT5N > end_key || key0 + kT5N - 1 > L - P.n_new) {   // reaches the diagonal or the end
-#pragma unroll
-            for (int k = 0; k < kT5N; ++k)
-              if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
-            if (P.anc) {   // draft tree: new keys off the row's ancestor path go too
-#pragma unroll
-              for (int k = 0; k < kT5N; ++k) {
-                const int rel = key0 + k - (L - P.n_new);
-                if (rel >= 0 && !((anc >> (rel & 63)) & 1ull)) x[k] = -INFINITY;
-              }
+      while (ok && t5_item(P, wk, it)) {
+        const int b = it.b, g = it.g, L = it.L;
+        const int nblocks = it.blk1 - it.blk0;
+        const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+        const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
+        // draft tree: of the new keys, only the row's ancestors are visible
+        const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
+        const int end_key = min(L, it.blk1 * kBS);             // first key this item does not own
+        float sl2 = P.scale_log2;
+        {
+          // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
+          // order). tcgen05.st is warp-collective: a warp holding live rows
+          // stores all 32 (zeros for rows past R); warps with none skip it
+          // (their rows of S, P and O are never read). The previous item's
+          // Q K^T have all run: its epilogue waited for its last P V.
+          if (warp_live) {
+            const uint4 *src = nullptr;
+            if (live) {
+              const int j = row / P.G, hh = row % P.G;
+              src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                    (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
             }
-          }
-          float mx = -INFINITY;
+            if constexpr (FP8) {
+              // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
+              // in [2^14, 2^15): the f16 range then holds the whole row with no
+              // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
+              // exact, and 2^-s, k_scale and the softmax scale fold into the
+              // row's scale (values below 2^-31 of the maximum lose bits in the
+              // f16 subnormals; their products are far below the fp32 sum's
+              // rounding). Two passes over the row (the second from L1) keep
+              // few registers live.
+              float amax = 0.f;
+              if (live) {
+#pragma unroll 4
+                for (int k = 0; k < 16; ++k) {
+                  const uint4 v = __ldg(src + k);
+                  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
-          // rows past R hold whatever Q's unused rows produce: they must not
-          // vote for a rescale of the warp
-          if (!live) mx = -INFINITY;
-          // the reference moves only when a tile exceeds it by more than 8
-          const bool up = mx > m_ref + 8.f;
-          float a = 1.f;
-          if (up) {
-            a = m_ref == -INFINITY ? 0.f : ex2f(m_ref - mx);
-            m_ref = mx;
-          }
-          if (t > 0 && __any_sync(0xffffffffu, up)) {
-            // rescale O: the previous P V must have landed first
-            const int pb = (t - 1) % kT5SBuf;
-            ok = __all_sync(0xffffffffu, t5_wait(&o_done[pb], ((t - 1) / kT5SBuf) & 1, abf, P.wait_ns));
-            t5_fence_after();
+                  for (int e = 0; e < 4; ++e)
+                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
+                }
+              }
+              const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
+              const float up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);     // 2^s, s = 14 - ex
+              const float down = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);   // 2^-s
+              sl2 *= P.k_scale[g] * down;
+              auto widen = [up](uint32_t w) {
+                return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
+              };
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 16) {
-              uint32_t r[16];
-              t5_ld16(lane_base + kT5OCol + c0, r);
-              t5_wait_ld();
+              for (int c0 = 0; c0 < 4; ++c0) {
+                uint32_t w[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
-              t5_st16(lane_base + kT5OCol + c0, r);
+                for (int k = 0; k < 4; ++k) {
+                  const uint4 v = live ? __ldg(src + 4 * c0 + k) : make_uint4(0u, 0u, 0u, 0u);
+                  w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
+                  w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
+                }
+                t5_st16(lane_base + kT5QCol + 16 * c0, w);
+              }
+            } else {
+              uint4 qv[16];
+              if (live) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
+              } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
+              }
+#pragma unroll
+              for (int c0 = 0; c0 < 4; ++c0) {
+                uint32_t w[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
+                  w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
+                }
+                t5_st16(lane_base + kT5QCol + 16 * c0, w);
+              }
             }
             t5_wait_st();
           }
-          l *= a;
-          const float base = m_ref == -INFINITY ? 0.f : m_ref;
-          float ps = 0.f;
+          t5_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&q_full);
+        }
+        float m_ref = -INFINITY, l = 0.f;
+        for (int t = 0; t < n_tiles && ok; ++t, ++u) {
+          const int sb = u % kT5SBuf, vs = u % VS;
+          ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (u / kT5SBuf) & 1, abf, P.wait_ns));
+          if (!ok) break;
+          t5_fence_after();
+          const int key0 = (it.blk0 + t * kT5Blk) * kBS;
+          if (warp_live) {
+            float x[kT5N];
+            {
+              uint32_t r[kT5N];
 #pragma unroll
-          for (int c0 = 0; c0 < kT5N; c0 += 32) {
-            uint32_t w[16];
+              for (int c0 = 0; c0 < kT5N; c0 += 16)
+                t5_ld16(lane_base + sb * kT5N + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+              t5_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
-              ps += p0 + p1;
-              w[k] = pack2<FP8>(p0, p1);
+              for (int k = 0; k < kT5N; ++k) x[k] = __uint_as_float(r[k]) * sl2;
             }
-            t5_st16(lane_base + sb * kT5N + c0 / 2, w);
-          }
-          t5_wait_st();
-          l += ps;
-        }
-        if (!FP8 && key0 + kT5N > end_key && warp == 0) {
-          // keys past the split or the sequence (not loaded, or stale): V rows
-          // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
-          // (FP8: the converter writes those rows as zeros)
-          if (!t5_wait(&v_full[vs], (t / VS) & 1, abf, P.wait_ns)) ok = false;
-          const uint32_t vb = v_ring + vs * kT5TileBytes;
-          for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
-            const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
+            if (key0 + kT5N > end_key || key0 + kT5N - 1 > L - P.n_new) {   // reaches the diagonal or the end
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+              for (int k = 0; k < kT5N; ++k)
+                if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
+              if (P.anc) {   // draft tree: new keys off the row's ancestor path go too
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + h * kT5HalfBytes + off + c * 16),
-                             "r"(0u)
-                             : "memory");
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-        t5_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[sb]);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      // ---- epilogue: O of this row -------------------------------------------
-      const int lb = (n_tiles - 1) % kT5SBuf;
-      const bool have = __all_sync(0xffffffffu, ok && t5_wait(&o_done[lb], ((n_tiles - 1) / kT5SBuf) & 1, abf, P.wait_ns));
-      t5_fence_after();
-      if (have && warp_live) {
-        const int nsplit = (nblk + P.bps - 1) / P.bps;
-        const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
-        __nv_bfloat16 *out = nullptr;
-        float *acc = nullptr;
-        if (live) {
-          const int j = row / P.G, hh = row % P.G;
-          out = static_cast<__nv_bfloat16 *>(P.out) + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
-          acc = P.ws_acc + (ent * P.R + row) * kD;
-        }
-        // FP8: the values are codes; v_scale makes them values again
-        const float vsc = FP8 ? P.v_scale[g] : 1.f;
-        const float il = (l > 0.f ? 1.f / l : 0.f) * vsc;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 64) {
-          uint32_t r[64];
-#pragma unroll
-          for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + kT5OCol + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
-          t5_wait_ld();
-          if (live) {
-            if (nsplit == 1) {
-#pragma unroll
-              for (int c = 0; c < 64; c += 8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  w[k] = pack2<false>(__uint_as_float(r[c + 2 * k]) * il, __uint_as_float(r[c + 2 * k + 1]) * il);
-                *reinterpret_cast<uint4 *>(out + c0 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int k = 0; k < kT5N; ++k) {
+                  const int rel = key0 + k - (L - P.n_new);
+                  if (rel >= 0 && !((anc >> (rel & 63)) & 1ull)) x[k] = -INFINITY;
+                }
               }
-            } else {
+            }
+            float mx = -INFINITY;
 #pragma unroll
-              for (int c = 0; c < 64; c += 4)
-                *reinterpret_cast<float4 *>(acc + c0 + c) =
-                    make_float4(__uint_as_float(r[c]) * vsc, __uint_as_float(r[c + 1]) * vsc,
-                                __uint_as_float(r[c + 2]) * vsc, __uint_as_float(r[c + 3]) * vsc);
+            for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
+            // rows past R hold whatever Q's unused rows produce: they must not
+            // vote for a rescale of the warp
+            if (!live) mx = -INFINITY;
+            // the reference moves only when a tile exceeds it by more than 8
+            const bool upd = mx > m_ref + 8.f;
+            float a = 1.f;
+            if (upd) {
+              a = m_ref == -INFINITY ? 0.f : ex2f(m_ref - mx);
+              m_ref = mx;
+            }
+            if (t > 0 && __any_sync(0xffffffffu, upd)) {
+              // rescale O: the previous P V must have landed first
+              const int pb = (u - 1) % kT5SBuf;
+              ok = __all_sync(0xffffffffu, t5_wait(&o_done[pb], ((u - 1) / kT5SBuf) & 1, abf, P.wait_ns));
+              t5_fence_after();
+#pragma unroll 1
+              for (int c0 = 0; c0 < 128; c0 += 16) {
+                uint32_t r[16];
+                t5_ld16(lane_base + kT5OCol + c0, r);
+                t5_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
+                t5_st16(lane_base + kT5OCol + c0, r);
+              }
+              t5_wait_st();
+            }
+            l *= a;
+            const float base = m_ref == -INFINITY ? 0.f : m_ref;
+            float ps = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < kT5N; c0 += 32) {
+              uint32_t w[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
+                ps += p0 + p1;
+                w[k] = pack2<FP8>(p0, p1);
+              }
+              t5_st16(lane_base + sb * kT5N + c0 / 2, w);
+            }
+            t5_wait_st();
+            l += ps;
+          }
+          if (!FP8 && key0 + kT5N > end_key && warp == 0) {
+            // keys past the item or the sequence (not loaded, or stale): V rows
+            // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
+            // (FP8: the converter writes those rows as zeros)
+            if (!t5_wait(&v_full[vs], (u / VS) & 1, abf, P.wait_ns)) ok = false;
+            const uint32_t vb = v_ring + vs * kT5TileBytes;
+            for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
+              const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + h * kT5HalfBytes + off + c * 16),
+                               "r"(0u)
+                               : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          t5_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[sb]);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) break;
+        // ---- epilogue: O of this row ------------------------------------------
+        const int lu = u - 1;   // the item's last tile
+        const bool have = __all_sync(0xffffffffu, t5_wait(&o_done[lu % kT5SBuf], (lu / kT5SBuf) & 1, abf, P.wait_ns));
+        t5_fence_after();
+        if (!have) {
+          ok = false;
+          break;
+        }
+        if (warp_live) {
+          __nv_bfloat16 *out = nullptr;
+          float *acc = nullptr;
+          if (live) {
+            const int j = row / P.G, hh = row % P.G;
+            out = static_cast<__nv_bfloat16 *>(P.out) + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
+            acc = P.ws_acc + (it.ent * P.R + row) * kD;
+          }
+          // FP8: the values are codes; v_scale makes them values again
+          const float vsc = FP8 ? P.v_scale[g] : 1.f;
+          const float il = (l > 0.f ? 1.f / l : 0.f) * vsc;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 64) {
+            uint32_t r[64];
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + kT5OCol + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+            t5_wait_ld();
+            if (live) {
+              if (it.whole) {
+#pragma unroll
+                for (int c = 0; c < 64; c += 8) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int k = 0; k < 4; ++k)
+                    w[k] = pack2<false>(__uint_as_float(r[c + 2 * k]) * il, __uint_as_float(r[c + 2 * k + 1]) * il);
+                  *reinterpret_cast<uint4 *>(out + c0 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < 64; c += 4)
+                  *reinterpret_cast<float4 *>(acc + c0 + c) =
+                      make_float4(__uint_as_float(r[c]) * vsc, __uint_as_float(r[c + 1]) * vsc,
+                                  __uint_as_float(r[c + 2]) * vsc, __uint_as_float(r[c + 3]) * vsc);
+              }
             }
           }
+          if (live && !it.whole) {
+            P.ws_ml[(it.ent * P.R + row) * 2] = m_ref;
+            P.ws_ml[(it.ent * P.R + row) * 2 + 1] = l;
+          }
         }
-        if (live && nsplit > 1) {
-          P.ws_ml[(ent * P.R + row) * 2] = m_ref;
-          P.ws_ml[(ent * P.R + row) * 2 + 1] = l;
-        }
+        // the epilogue's TMEM loads finish before the next item's first P V
+        // (which waits for this warp's arrival on its P buffer) may overwrite O
       }
     }
   }
@@ -766,7 +976,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
     // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
     // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
-    // keys past the split or the sequence are written as zeros.
+    // keys past the item or the sequence are written as zeros.
     const bool isv = warp == 8;
     const int NS = isv ? VS : KS;
     uint64_t *rfull = isv ? v_full : k_full;
@@ -775,49 +985,56 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     uint64_t *cempty = isv ? vc_empty : kc_empty;
     const uint32_t rring = isv ? v_ring : k_ring;
     const uint32_t cring = isv ? vc_ring : kc_ring;
-    const int end_key = min(L, blk1 * kBS);
-    for (int t = 0; t < n_tiles; ++t) {
-      const int rs = t % NS, cs = t % CS;
-      bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf, P.wait_ns));
-      if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf, P.wait_ns));
-      if (!ok) break;
-      const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
-      const int key0 = (blk0 + t * kT5Blk) * kBS;
+    T5Walk wk = {};
+    T5Item it;
+    int u = 0;
+    bool ok = true;
+    while (ok && t5_item(P, wk, it)) {
+      const int end_key = min(it.L, it.blk1 * kBS);
+      const int n_tiles = (it.blk1 - it.blk0 + kT5Blk - 1) / kT5Blk;
+      for (int t = 0; t < n_tiles; ++t, ++u) {
+        const int rs = u % NS, cs = u % CS;
+        ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (u / NS) & 1, abf, P.wait_ns));
+        if (ok && u >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((u / CS) - 1) & 1, abf, P.wait_ns));
+        if (!ok) break;
+        const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
+        const int key0 = (it.blk0 + t * kT5Blk) * kBS;
 #pragma unroll 2
-      for (int j = 0; j < 8; ++j) {
-        const int q = lane + 32 * j;
-        const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
-        uint32_t v0, v1, v2, v3;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                     : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
-        uint32_t h[8];
-        if (key0 + row < end_key) {
-          const uint32_t w[4] = {v0, v1, v2, v3};
+        for (int j = 0; j < 8; ++j) {
+          const int q = lane + 32 * j;
+          const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
+          uint32_t v0, v1, v2, v3;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                       : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
+          uint32_t h[8];
+          if (key0 + row < end_key) {
+            const uint32_t w[4] = {v0, v1, v2, v3};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffffu));
-            h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+            for (int k = 0; k < 4; ++k) {
+              h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffffu));
+              h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[k] = 0u;
           }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) h[k] = 0u;
+          const uint32_t rowb = dst + (ch >> 2) * kT5HalfBytes + blk * 2048 + r16 * 128;
+          const int c8 = 2 * (ch & 3);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
+                       "r"(h[1]), "r"(h[2]), "r"(h[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
+                       "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                       : "memory");
         }
-        const uint32_t rowb = dst + (ch >> 2) * kT5HalfBytes + blk * 2048 + r16 * 128;
-        const int c8 = 2 * (ch & 3);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
-                     "r"(h[1]), "r"(h[2]), "r"(h[3])
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
-                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                     : "memory");
-      }
-      // the tensor cores read the widened tile through the async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
-        mbar_arrive(&cfull[cs]);    // the widened stage may be read
+        // the tensor cores read the widened tile through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
+          mbar_arrive(&cfull[cs]);    // the widened stage may be read
+        }
       }
     }
   }
@@ -984,12 +1201,15 @@ struct MergeParams {
   const float *ws_acc;
   const float *ws_ml;
   const int32_t *seq_lens;
+  const int32_t *seq_pre;   // balanced mode: first tile of each sequence, then T
+  const int4 *split;        // balanced mode: (count, T), then (b, A, nt, r0) of each split sequence
   void *out;
   int B, n_new, H_q, H_kv, G, R, d, bs, max_blocks, bps, S, per_split;
+  int C;                    // balanced mode: CTAs of the tcgen05 kernel (0: split mode)
 };
 
 // Split merge: WPR warps per output row (sequence, kv head, packed query row),
-// each taking every WPR-th split in one pass with a running maximum (lanes
+// each taking every WPR-th piece in one pass with a running maximum (lanes
 // own float4 column chunks); the warps' states are then combined through
 // shared memory by the row's first warp.
 template <typename TO, int WPR>
@@ -1165,8 +1385,136 @@ __global__ void __launch_bounds__(1024) attn_merge_pair_kernel(const __grid_cons
   }
 }
 
+// Balanced-mode merge: only the sequences the partition listed as split
+// (split[1..n] = (b, A, nt, r0)); row u of the work is (listed sequence
+// u / (H_kv R), kv head, query row), WPR warps per row, rows taken
+// grid-stride so that the launch does not depend on n. The pieces of (b, g)
+// come from the ranges r0..r1 that meet b's tiles [A, A + nt) (range r holds
+// [r T / NR, (r + 1) T / NR)), skipping empty ranges, each run for head g by
+// CTA c = r H_kv + g; r0's piece is its CTA's last item (entry 2c + 1) unless
+// r0 starts at A, every other one is its CTA's first (entry 2c). Warp wr of a
+// row takes pieces wr, wr + WPR, ..., loading up to kMB of them at once (one
+// round trip), and the WPR warps' states are combined through shared
+// memory. d = 128 (the tcgen05 path): lane l owns float4 chunk l.
+template <typename TO, int WPR>
+__global__ void __launch_bounds__(256) attn_merge_bal_kernel(const __grid_constant__ MergeParams P) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kRows = 8 / WPR;  // rows per CTA and round
+  constexpr int kMB = 8;          // pieces a warp loads at once
+  __shared__ float4 xs_acc[8][32];
+  __shared__ float xs_ml[8][2];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wr = warp % WPR;
+  const int R = P.R;
+  const int4 hdr = P.split[0];
+  const int64_t NR = P.C / P.H_kv, T = hdr.y;
+  const int64_t nrows = (int64_t)hdr.x * P.H_kv * R;
+  for (int64_t base = (int64_t)blockIdx.x * kRows; base < nrows; base += (int64_t)gridDim.x * kRows) {
+    const int64_t u = base + warp / WPR;
+    const bool live = u < nrows;
+    int r = 0, g = 0, b = 0, npiece = 0;
+    int64_t A = 0, r0 = 0;
+    if (live) {
+      r = (int)(u % R);
+      g = (int)((u / R) % P.H_kv);
+      const int4 sp = P.split[1 + (int)(u / ((int64_t)R * P.H_kv))];
+      b = sp.x;
+      A = sp.y;
+      r0 = sp.w;
+      npiece = (int)(((A + sp.z) * NR - 1) / T - r0) + 1;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float m = -INFINITY, l = 0.f;
+    for (int e0 = wr; e0 < npiece; e0 += kMB * WPR) {
+      float me[kMB], le[kMB];
+      float4 va[kMB];
+#pragma unroll
+      for (int k = 0; k < kMB; ++k) {
+        const int e = e0 + k * WPR;
+        const int64_t rg = r0 + e, t0 = rg * T / NR;
+        me[k] = -INFINITY;
+        le[k] = 0.f;
+        va[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < npiece && (rg + 1) * T / NR > t0) {   // an empty range wrote nothing
+          const int64_t row = (2 * (rg * P.H_kv + g) + ((e == 0 && t0 < A) ? 1 : 0)) * R + r;
+          me[k] = P.ws_ml[row * 2];
+          le[k] = P.ws_ml[row * 2 + 1];
+          va[k] = reinterpret_cast<const float4 *>(P.ws_acc + row * P.d)[lane];
+        }
+      }
+      float mn = m;
+#pragma unroll
+      for (int k = 0; k < kMB; ++k) mn = fmaxf(mn, me[k]);
+      const float base_m = mn == -INFINITY ? 0.f : mn;
+      const float a = exp2f(m - base_m);
+      l *= a;
+      acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+#pragma unroll
+      for (int k = 0; k < kMB; ++k) {
+        const float w = exp2f(me[k] - base_m);
+        l += le[k] * w;
+        acc.x += va[k].x * w; acc.y += va[k].y * w; acc.z += va[k].z * w; acc.w += va[k].w * w;
+      }
+      m = mn;
+    }
+    if constexpr (WPR > 1) {
+      xs_acc[warp][lane] = acc;
+      if (lane == 0) { xs_ml[warp][0] = m; xs_ml[warp][1] = l; }
+      __syncthreads();
+      if (wr == 0) {
+        for (int w2 = 1; w2 < WPR; ++w2) {
+          const float me = xs_ml[warp + w2][0], le = xs_ml[warp + w2][1];
+          const float mn = fmaxf(m, me);
+          const float base_m = mn == -INFINITY ? 0.f : mn;
+          const float a = exp2f(m - base_m), w = exp2f(me - base_m);
+          l = l * a + le * w;
+          m = mn;
+          const float4 v = xs_acc[warp + w2][lane];
+          acc.x = acc.x * a + v.x * w;
+          acc.y = acc.y * a + v.y * w;
+          acc.z = acc.z * a + v.z * w;
+          acc.w = acc.w * a + v.w * w;
+        }
+      }
+      __syncthreads();   // xs_* are free for the next round
+    }
+    if (!live || wr != 0) continue;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int j = r / P.G, hh = r % P.G;
+    const int64_t out_off = (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * P.d;
+    if constexpr (std::is_same<TO, float>::value) {
+      reinterpret_cast<float4 *>(static_cast<float *>(P.out) + out_off)[lane] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(P.out) + out_off + 4 * lane;
+      *reinterpret_cast<__nv_bfloat162 *>(o) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      *reinterpret_cast<__nv_bfloat162 *>(o + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+  }
+}
+
+int num_sms();
+
 template <typename TO>
 void launch_merge(const MergeParams &M, int64_t rows, cudaStream_t st) {
+  if (M.C > 0) {
+    // a split sequence spans about NR / B + 2 ranges when the lengths are
+    // equal; the grid covers every row that could need a merge (at most
+    // NR - 1 split sequences) up to four CTAs per SM
+    const int64_t NR = M.C / M.H_kv;
+    const int64_t est = NR / std::max<int64_t>(1, M.B) + 2;
+    const int wpr = est >= 48 ? 8 : (est >= 24 ? 4 : (est >= 12 ? 2 : 1));
+    const int64_t maxrows = std::max<int64_t>(1, (NR - 1) * M.H_kv * M.R);
+    const unsigned nb = (unsigned)std::max<int64_t>(1, std::min<int64_t>(4 * num_sms(), (maxrows * wpr + 7) / 8));
+    switch (wpr) {
+      case 8: launch_k(attn_merge_bal_kernel<TO, 8>, dim3(nb), dim3(256), 0, st, 1, M); break;
+      case 4: launch_k(attn_merge_bal_kernel<TO, 4>, dim3(nb), dim3(256), 0, st, 1, M); break;
+      case 2: launch_k(attn_merge_bal_kernel<TO, 2>, dim3(nb), dim3(256), 0, st, 1, M); break;
+      default: launch_k(attn_merge_bal_kernel<TO, 1>, dim3(nb), dim3(256), 0, st, 1, M); break;
+    }
+    return;
+  }
   if (M.S <= 4) {
     launch_k(attn_merge_pair_kernel<TO>, dim3((unsigned)(M.B * M.H_kv)), dim3(32 * std::min(32, M.R)), 0, st, 1, M);
     return;
@@ -1201,6 +1549,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 struct Plan {
   bool tc;
   int R, S, bps, per_split, d;
+  int C;   // balanced mode (tcgen05 kernel, no explicit split size): CTAs; 0 otherwise
 };
 
 int num_sms() {
@@ -1235,13 +1584,27 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
                  (lay->slot_stride * es) % 16 == 0;
   p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS && p.R <= kT5MaxR &&
          strides_ok;
+  p.C = 0;
   if (bps_req > 0) {
     p.bps = bps_req;
+  } else if (p.tc && (int64_t)B * H_kv < 2 * num_sms() &&
+             (int64_t)std::max(B, 1) * ((max_blocks + kT5Blk - 1) / kT5Blk) < (1ll << 30)) {
+    // balanced mode, when there are fewer (sequence, kv head) pairs than
+    // CTA slots (two per SM): a small batch or long contexts: ranges of tiles for all kv heads side by side, about
+    // two CTAs per SM (what the shared memory and TMEM of one CTA leave room
+    // for), each taking an equal share of all tiles
+    const int64_t tiles = (int64_t)std::max(B, 1) * ((max_blocks + kT5Blk - 1) / kT5Blk);
+    const int64_t nr = std::max<int64_t>(1, std::min<int64_t>(2 * num_sms() / H_kv, tiles));
+    p.C = (int)(nr * H_kv);
+    p.bps = 0;
+    p.S = 1;
+    p.per_split = 1;
+    return p;
   } else if (p.tc) {
-    // tcgen05 kernel: long splits amortise its per-CTA setup (TMEM, Q,
-    // pipeline fill) and the merge; at least one split per SM when the batch
-    // is small. The longest-first order keeps the last wave short, so
-    // splits of up to 256 blocks pay off.
+    // split mode for larger batches: long splits amortise the tcgen05
+    // kernel's per-CTA setup (TMEM, Q, pipeline fill) and the merge; the
+    // longest-first order keeps the last wave short, so splits of up to 256
+    // blocks pay off
     p.bps = std::min(256, std::max(16, pow2_floor((int64_t)max_blocks * B * H_kv / num_sms())));
   } else {
     // fp32 caches are planned like bf16 ones so every dtype fits the same
@@ -1257,11 +1620,19 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
   return p;
 }
 
-// split partials (acc, then m and l), then the tcgen05 kernel's work order
+// Partial entries: split mode one per split, balanced mode two per CTA.
+size_t ws_entries(const Plan &p, int B, int H_kv) {
+  return p.C > 0 ? (size_t)2 * p.C : (size_t)B * H_kv * p.S * p.per_split;
+}
+
+// partials (acc, then m and l), then the work order (split mode) or the
+// per-CTA work and sequence prefixes (balanced mode)
 size_t ws_bytes(const Plan &p, int B, int H_kv) {
-  const size_t ent = (size_t)B * H_kv * p.S * p.per_split * p.R;
-  return align_up(ent * p.d * sizeof(float), 256) + align_up(ent * 2 * sizeof(float), 256) +
-         align_up((size_t)B * H_kv * p.S * sizeof(int32_t), 256);
+  const size_t ent = ws_entries(p, B, H_kv) * p.R;
+  const size_t tail = p.C > 0 ? align_up((size_t)p.C * sizeof(int4), 256) + align_up((size_t)(B + 1) * sizeof(int32_t), 256) +
+                                   align_up((size_t)(p.C / H_kv + 1) * sizeof(int4), 256)
+                              : align_up((size_t)B * H_kv * p.S * sizeof(int32_t), 256);
+  return align_up(ent * p.d * sizeof(float), 256) + align_up(ent * 2 * sizeof(float), 256) + tail;
 }
 
 // Ancestor masks of the draft trees: bit i of anc[b][j] is set iff node i is
@@ -1302,11 +1673,19 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  launch_k(attn_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, 1, P.seq_lens, P.B, P.S, P.H_kv, P.bps, P.n_new,
-           P.max_blocks, const_cast<int32_t *>(P.order));
+  unsigned grid;
+  if (P.balanced) {
+    launch_k(attn_part_kernel, dim3(1), dim3(kPartThreads), 0, st, 1, P.seq_lens, P.B, P.n_new, P.max_blocks,
+             P.ncta / P.H_kv, const_cast<int4 *>(P.work), P.seq_pre_w, P.split_w, P.status);
+    grid = (unsigned)P.ncta;
+  } else {
+    launch_k(attn_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, 1, P.seq_lens, P.B, P.S, P.H_kv, P.bps, P.n_new,
+             P.max_blocks, const_cast<int32_t *>(P.order));
+    grid = (unsigned)(P.S * P.H_kv * P.B);
+  }
   sv_status rc = check_launch("spec_verify_attn order launch");
   if (rc != SV_OK) return rc;
-  launch_k(attn_tc5_kernel<QR, FP8>, dim3(P.S * P.H_kv * P.B), dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
+  launch_k(attn_tc5_kernel<QR, FP8>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
   return check_launch("spec_verify_attn tcgen05 launch");
 }
 
@@ -1366,7 +1745,7 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
   if (!aligned(workspace, 256)) return fail(SV_ERR_WORKSPACE, "spec_verify_attn: workspace not 256-byte aligned");
   if (B == 0) return ok();
 
-  const size_t ent = (size_t)B * H_kv * plan.S * plan.per_split * plan.R;
+  const size_t ent = ws_entries(plan, B, H_kv) * plan.R;
   float *ws_acc = static_cast<float *>(workspace);
   float *ws_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                            align_up(ent * d_head * sizeof(float), 256));
@@ -1436,8 +1815,16 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     }
     P.q = q; P.out = out; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
     P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status; P.anc = anc;
-    P.order = reinterpret_cast<const int32_t *>(reinterpret_cast<uint8_t *>(ws_ml) +
-                                                align_up(ent * 2 * sizeof(float), 256));
+    uint8_t *tail = reinterpret_cast<uint8_t *>(ws_ml) + align_up(ent * 2 * sizeof(float), 256);
+    P.order = reinterpret_cast<const int32_t *>(tail);
+    if (plan.C > 0) {
+      P.balanced = 1;
+      P.ncta = plan.C;
+      P.work = reinterpret_cast<const int4 *>(tail);
+      P.seq_pre_w = reinterpret_cast<int32_t *>(tail + align_up((size_t)plan.C * sizeof(int4), 256));
+      P.split_w = reinterpret_cast<int4 *>(reinterpret_cast<uint8_t *>(P.seq_pre_w) +
+                                           align_up((size_t)(B + 1) * sizeof(int32_t), 256));
+    }
     P.B = B; P.n_new = n_new; P.H_q = H_q; P.H_kv = H_kv; P.G = G; P.R = plan.R;
     P.max_blocks = max_blocks_per_seq; P.num_blocks = num_blocks; P.bps = plan.bps; P.S = plan.S;
     P.scale_log2 = scale_log2;
@@ -1459,8 +1846,18 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
     else rc = launch_gen<uint8_t, __nv_bfloat16>(P, st);
   }
   if (rc != SV_OK) return rc;
-  if (plan.S == 1) return ok();   // every sequence was written directly
+  // every sequence was written directly: one range, or one split
+  if ((plan.C > 0 && plan.C / H_kv == 1) || (plan.C == 0 && plan.S == 1)) return ok();
   MergeParams M;
+  memset(&M, 0, sizeof(M));
+  if (plan.C > 0) {
+    M.C = plan.C;
+    M.seq_pre = reinterpret_cast<const int32_t *>(reinterpret_cast<uint8_t *>(ws_ml) +
+                                                  align_up(ent * 2 * sizeof(float), 256) +
+                                                  align_up((size_t)plan.C * sizeof(int4), 256));
+    M.split = reinterpret_cast<const int4 *>(reinterpret_cast<const uint8_t *>(M.seq_pre) +
+                                             align_up((size_t)(B + 1) * sizeof(int32_t), 256));
+  }
   M.ws_acc = ws_acc; M.ws_ml = ws_ml; M.seq_lens = seq_lens; M.out = out;
   M.B = B; M.n_new = n_new; M.H_q = H_q; M.H_kv = H_kv; M.G = G; M.R = plan.R; M.d = d_head; M.bs = block_size;
   M.max_blocks = max_blocks_per_seq; M.bps = plan.bps; M.S = plan.S; M.per_split = plan.per_split;
