@@ -210,9 +210,14 @@ sv_status spec_verify_attn(const void *q, sv_dtype q_dtype,
 
 /* Same as spec_verify_attn with an explicit split size: the keys of each
  * sequence are cut into chunks of blocks_per_split blocks that run in
- * parallel and are merged by log-sum-exp. The result does not depend on the
- * split size up to rounding; the workspace must hold
- * spec_verify_attn_workspace_size_ex(..., blocks_per_split) bytes. */
+ * parallel and are merged by log-sum-exp. blocks_per_split = 0 asks for
+ * balanced ranges instead (tensor-core path; other paths take their default
+ * split): the 32-key tiles of all sequences, end to end, are cut into equal
+ * ranges, one per CTA slot (two per SM) and kv head, whatever the lengths;
+ * this suits small batches of very uneven lengths. The result does not
+ * depend on the split size up to rounding; the workspace must hold
+ * spec_verify_attn_workspace_size_ex(..., blocks_per_split) bytes
+ * (SV_ERR_INVALID_ARG for blocks_per_split < 0; the size query returns 0). */
 size_t spec_verify_attn_workspace_size_ex(int B, int n_new, int H_q, int H_kv, int d_head,
                                           int max_blocks_per_seq, int block_size,
                                           int blocks_per_split);

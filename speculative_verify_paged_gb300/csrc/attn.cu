@@ -6,13 +6,13 @@
 // t <= L_b - n_new + j, K_t / V_t read through the block table.
 //
 // Design (flash-decoding style split-KV, CS336 lecture 10 section 9.2):
-//   * work items are pieces of (sequence, kv head) pairs. With at least as
-//     many pairs as CTA slots (two per SM), attn_order_kernel sorts splits
-//     of a fixed size longest first and each CTA takes one. With fewer pairs
-//     (a small batch, long contexts) attn_part_kernel cuts the tiles of all
-//     sequences into equal ranges, one per CTA slot and kv head, and a CTA
-//     walks its range through one or more pairs, so every CTA streams the
-//     same number of tiles;
+//   * work items are pieces of (sequence, kv head) pairs. By default
+//     attn_order_kernel sorts splits of a fixed size longest first and each
+//     CTA of attn_tc5_kernel takes one. On request (blocks_per_split = 0),
+//     attn_part_kernel cuts the tiles of all sequences into equal ranges, one
+//     per CTA slot and kv head, and each CTA of attn_tc5_bal_kernel walks its
+//     range through one or more pairs, so every CTA streams the same number
+//     of tiles whatever the lengths;
 //   * attn_tc5_kernel on the fifth-generation tensor
 //     cores: all (K+1)*G query rows of the GQA group share one M = 128 MMA
 //     tile, so every K/V byte is read from HBM once per step; two producer
@@ -249,13 +249,11 @@ __device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile 
   return false;
 }
 
-// The work items of a CTA of the tcgen05 kernel: blocks [blk0, blk1) of kv
-// head g of sequence b. Split mode: one item, split s of (b, g) in the order
-// the order kernel wrote; its partial goes to entry (b H_kv + g) S + s.
-// Balanced mode: the sequence of 32-key tiles of all sequences in order is
-// cut into NR equal ranges, and CTA c runs range c / H_kv for kv head
-// c % H_kv, so every CTA streams the same number of tiles; a range may end
-// inside one sequence and go on through whole sequences into the next. A
+// The work items of a CTA of the balanced-mode kernel: blocks [blk0, blk1)
+// of kv head g of sequence b. The sequence of 32-key tiles of all sequences
+// in order is cut into NR equal ranges, and CTA c runs range c / H_kv for kv
+// head c % H_kv, so every CTA streams the same number of tiles; a range may
+// end inside one sequence and go on through whole sequences into the next. A
 // piece of a (b, g) pair that another CTA shares writes a partial: entry 2c
 // for the CTA's first item, 2c + 1 for its last. Every role of the CTA walks
 // the same items in the same order.
@@ -268,31 +266,7 @@ struct T5Walk {
   int b, g, off, left, idx;
 };
 
-__device__ __forceinline__ bool t5_len_ok(const TcParams &P, int L) {
-  return L >= P.n_new && L <= P.max_blocks * kBS;
-}
-
 __device__ __forceinline__ bool t5_item(const TcParams &P, T5Walk &w, T5Item &it) {
-  if (!P.balanced) {
-    if (w.idx > 0) return false;
-    w.idx = 1;
-    const int item = __ldg(P.order + blockIdx.x);
-    const int s = item % P.S;
-    it.g = (item / P.S) % P.H_kv;
-    it.b = item / (P.S * P.H_kv);
-    it.L = P.seq_lens[it.b];
-    if (!t5_len_ok(P, it.L)) {
-      if (threadIdx.x == 0 && it.g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
-      return false;
-    }
-    it.nblk = (it.L + kBS - 1) / kBS;
-    it.blk0 = s * P.bps;
-    if (it.blk0 >= it.nblk) return false;   // the merge never reads this split
-    it.blk1 = min(it.nblk, it.blk0 + P.bps);
-    it.whole = it.nblk <= P.bps;
-    it.ent = ((int64_t)it.b * P.H_kv + it.g) * P.S + s;
-    return true;
-  }
   if (w.idx == 0) {
     const int4 wk = __ldg(P.work + blockIdx.x / P.H_kv);
     w.b = wk.x; w.g = (int)(blockIdx.x % P.H_kv); w.off = wk.z; w.left = wk.w;
@@ -302,7 +276,7 @@ __device__ __forceinline__ bool t5_item(const TcParams &P, T5Walk &w, T5Item &it
   for (;;) {   // sequences with invalid lengths hold no tiles
     if (w.b >= P.B) return false;
     L = P.seq_lens[w.b];
-    nt = t5_len_ok(P, L) ? ((L + kBS - 1) / kBS + kT5Blk - 1) / kT5Blk : 0;
+    nt = (L >= P.n_new && L <= P.max_blocks * kBS) ? ((L + kBS - 1) / kBS + kT5Blk - 1) / kT5Blk : 0;
     if (nt > 0) break;
     ++w.b;
   }
@@ -494,6 +468,528 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *
 
 template <int QR, bool FP8>
 __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
+  pdl_wait();
+  pdl_trigger();
+  using Cfg = T5Cfg<QR, FP8>;
+  constexpr int KS = Cfg::kKS, VS = Cfg::kVS, CS = Cfg::kCS > 0 ? Cfg::kCS : 1;
+  constexpr int RAW = Cfg::kRawBytes;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+  // FP8: widened stages, filled by the converter warps, freed by the MMAs
+  __shared__ __align__(8) uint64_t kc_full[CS], kc_empty[CS], vc_full[CS], vc_empty[CS];
+  __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  // the work item: split s of kv head g of sequence b, in the longest-first
+  // order the order kernel wrote (the CTAs launched first take the longest
+  // splits, so the last wave is made of the shortest ones)
+  const int item = __ldg(P.order + blockIdx.x);
+  const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t k_ring = smem_u32(smem);
+  const uint32_t v_ring = k_ring + KS * RAW;
+  // the rings the MMAs read: the widened ones for FP8, else the TMA rings
+  const uint32_t kc_ring = FP8 ? v_ring + VS * RAW : k_ring;
+  const uint32_t vc_ring = FP8 ? kc_ring + CS * kT5TileBytes : v_ring;
+
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * kBS) {
+    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int nblk = (L + kBS - 1) / kBS;
+  const int blk0 = s * P.bps;
+  if (blk0 >= nblk) return;   // the merge never reads this split
+  const int blk1 = min(nblk, blk0 + P.bps);
+  const int nblocks = blk1 - blk0;
+  const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+  const int R = P.R;
+
+  if (tid == 0) {
+    for (int k = 0; k < KS; ++k) {
+      mbar_init(&k_full[k], 1);
+      mbar_init(&k_empty[k], 1);
+    }
+    for (int k = 0; k < VS; ++k) {
+      mbar_init(&v_full[k], 1);
+      mbar_init(&v_empty[k], 1);
+    }
+    if (FP8)
+      for (int k = 0; k < CS; ++k) {
+        mbar_init(&kc_full[k], 1);
+        mbar_init(&kc_empty[k], 1);
+        mbar_init(&vc_full[k], 1);
+        mbar_init(&vc_empty[k], 1);
+      }
+    for (int k = 0; k < kT5SBuf; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&p_full[k], 4);
+      mbar_init(&o_done[k], 1);
+    }
+    mbar_init(&mma_drain, 1);
+    mbar_init(&q_full, 4);   // the four softmax warps wrote their Q rows
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  volatile int *abf = &abort_flag;
+
+  if (warp == 4 || warp == 5) {
+    // ------------------------------------------------------------ producers --
+    // warp 4 streams K, warp 5 streams V
+    {
+      // the whole warp walks the block table 32 entries at a time (the next
+      // 32 prefetched); lane 0 waits for free stages and issues the copies
+      const bool isv = warp == 5;
+      const int NS = isv ? VS : KS;
+      uint64_t *fullb = isv ? v_full : k_full;
+      uint64_t *emptyb = isv ? v_empty : k_empty;
+      const uint32_t ring = isv ? v_ring : k_ring;
+      const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
+      const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
+      int cur = lane < nblocks ? table[lane] : 0;
+      int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
+      int chunk = 0;
+      int issued = 0;
+      // (test hook: with the copies withheld every wait on them runs out,
+      // with nothing in flight)
+      const int n_issue = (P.withhold & SV_TEST_WITHHOLD_COPIES) ? 0 : n_tiles;
+      for (int t = 0; t < n_issue; ++t) {
+        const int first = t * kT5Blk;
+        if ((first >> 5) != chunk) {
+          chunk = first >> 5;
+          cur = nxt;
+          const int rel = (chunk + 1) * 32 + lane;
+          nxt = rel < nblocks ? table[rel] : 0;
+        }
+        int phys[kT5Blk];
+#pragma unroll
+        for (int kk = 0; kk < kT5Blk; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
+        const int st = t % NS;
+        bool go = true;
+        if (lane == 0) {
+          if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf, P.wait_ns)) {
+            go = false;
+          } else {
+            const int nvalid = min(kT5Blk, nblocks - first);
+            // a block is 2 KB of e4m3 (one 128-byte box row per slot) or two
+            // 2 KB head-dim halves of bf16
+            mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * (FP8 ? 2048 : 2 * 2048)));
+            const uint32_t base = ring + st * RAW;
+            for (int kk = 0; kk < nvalid; ++kk) {
+              int ph = phys[kk];
+              if (ph < 0 || ph >= P.num_blocks) {
+                if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+                ph = 0;   // stay in bounds; the output of this sequence is flagged
+              }
+              int c[3];
+              tile_coords(P, g, ph, c);
+              tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
+              if (!FP8) tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
+            }
+            issued = t + 1;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, (int)go, 0)) break;
+      }
+      // the copies in flight land before the CTA may exit
+      if (lane == 0) {
+        for (int t = max(0, issued - NS); t < issued; ++t)
+          if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      }
+    }
+  } else if (warp < 4 || warp == kT5MmaWarp) {
+    if (warp == kT5MmaWarp) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                   "r"(kT5Cols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    t5_fence_before();
+    named_bar_sync(1, 160);   // TMEM allocated
+    t5_fence_after();
+    const uint32_t tb = tmem_base;
+
+    if (warp == kT5MmaWarp) {
+      // ---------------------------------------------------------- MMA issuer --
+      if (lane == 0) {
+        // f32 accumulators; A and B bf16 (formats 1), or f16 for FP8 (0)
+        constexpr uint32_t ab = FP8 ? 0u : (1u << 7) | (1u << 10);
+        const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
+        const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
+        static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
+        int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
+        bool q_ready = false;
+        uint64_t t_last = global_ns();
+        while (tp < n_tiles) {
+          bool progressed = false;
+          if (!q_ready) q_ready = t5_test(&q_full, 0);
+          if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
+            // K stage: the TMA ring (bf16) or the widened ring (FP8)
+            const int KR = FP8 ? CS : KS;
+            const int ks = tq % KR, sb = tq % kT5SBuf;
+            uint64_t *kf = FP8 ? kc_full : k_full;
+            // S buffer sb is free once the P V of tile tq - kT5SBuf has run
+            const bool sfree = tq < kT5SBuf || t5_test(&o_done[sb], ((tq / kT5SBuf) - 1) & 1);
+            if (sfree && t5_test(&kf[ks], (tq / KR) & 1)) {
+              t5_fence_after();
+              const uint32_t kb = kc_ring + ks * kT5TileBytes;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
+                t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
+                          t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
+                          kk > 0 ? 1u : 0u);
+              t5_commit(&s_full[sb]);
+              t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
+              ++tq;
+              progressed = true;
+            }
+          }
+          if (tp < tq) {
+            const int VR = FP8 ? CS : VS;
+            const int vs = tp % VR, sb = tp % kT5SBuf;
+            uint64_t *vf = FP8 ? vc_full : v_full;
+            if (t5_test(&p_full[sb], (tp / kT5SBuf) & 1) && t5_test(&vf[vs], (tp / VR) & 1)) {
+              t5_fence_after();
+              const uint32_t vb = vc_ring + vs * kT5TileBytes;
+#pragma unroll
+              for (int j = 0; j < kT5Blk; ++j)
+                t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
+                          idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
+              t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
+              t5_commit(&o_done[sb]);
+              ++tp;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            t_last = global_ns();
+          } else if (*abf || global_ns() - t_last > P.wait_ns) {
+            *abf = 1;
+            break;
+          } else {
+            __nanosleep(64);   // leave issue slots to the other warps of this scheduler
+          }
+        }
+        // every MMA issued has completed before TMEM can be released
+        t5_commit(&mma_drain);
+        if (!mbar_wait(&mma_drain, 0)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ softmax ----
+      const int row = tid;   // warps 0-3
+      const bool warp_live = warp * 32 < R;
+      const bool live = row < R;
+      const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
+      const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
+      // draft tree: of the new keys, only the row's ancestors are visible
+      const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
+      const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
+      float sl2 = P.scale_log2;
+      {
+        // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
+        // order). tcgen05.st is warp-collective: a warp holding live rows
+        // stores all 32 (zeros for rows past R); warps with none skip it
+        // (their rows of S, P and O are never read).
+        if (warp_live) {
+          const uint4 *src = nullptr;
+          if (live) {
+            const int j = row / P.G, hh = row % P.G;
+            src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                  (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
+          }
+          if constexpr (FP8) {
+            // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
+            // in [2^14, 2^15): the f16 range then holds the whole row with no
+            // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
+            // exact, and 2^-s, k_scale and the softmax scale fold into the
+            // row's scale (values below 2^-31 of the maximum lose bits in the
+            // f16 subnormals; their products are far below the fp32 sum's
+            // rounding). Two passes over the row (the second from L1) keep
+            // few registers live.
+            float amax = 0.f;
+            if (live) {
+#pragma unroll 4
+              for (int k = 0; k < 16; ++k) {
+                const uint4 v = __ldg(src + k);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
+              }
+            }
+            const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
+            const float up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);     // 2^s, s = 14 - ex
+            const float down = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);   // 2^-s
+            sl2 *= P.k_scale[g] * down;
+            auto widen = [up](uint32_t w) {
+              return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
+            };
+#pragma unroll 1
+            for (int c0 = 0; c0 < 4; ++c0) {
+              uint32_t w[16];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint4 v = live ? __ldg(src + 4 * c0 + k) : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
+                w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
+              }
+              t5_st16(lane_base + kT5QCol + 16 * c0, w);
+            }
+          } else {
+            uint4 qv[16];
+            if (live) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < 4; ++c0) {
+              uint32_t w[16];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
+                w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
+              }
+              t5_st16(lane_base + kT5QCol + 16 * c0, w);
+            }
+          }
+          t5_wait_st();
+        }
+        t5_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
+      }
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int sb = t % kT5SBuf, vs = t % VS;
+        ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (t / kT5SBuf) & 1, abf, P.wait_ns));
+        if (!ok) break;
+        t5_fence_after();
+        const int key0 = (blk0 + t * kT5Blk) * kBS;
+        if (warp_live) {
+          float x[kT5N];
+          {
+            uint32_t r[kT5N];
+#pragma unroll
+            for (int c0 = 0; c0 < kT5N; c0 += 16)
+              t5_ld16(lane_base + sb * kT5N + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+            t5_wait_ld();
+#pragma unroll
+            for (int k = 0; k < kT5N; ++k) x[k] = __uint_as_float(r[k]) * sl2;
+          }
+          if (key0 + kT5N > end_key || key0 + kT5N - 1 > L - P.n_new) {   // reaches the diagonal or the end
+#pragma unroll
+            for (int k = 0; k < kT5N; ++k)
+              if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
+            if (P.anc) {   // draft tree: new keys off the row's ancestor path go too
+#pragma unroll
+              for (int k = 0; k < kT5N; ++k) {
+                const int rel = key0 + k - (L - P.n_new);
+                if (rel >= 0 && !((anc >> (rel & 63)) & 1ull)) x[k] = -INFINITY;
+              }
+            }
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
+          // rows past R hold whatever Q's unused rows produce: they must not
+          // vote for a rescale of the warp
+          if (!live) mx = -INFINITY;
+          // the reference moves only when a tile exceeds it by more than 8
+          const bool up = mx > m_ref + 8.f;
+          float a = 1.f;
+          if (up) {
+            a = m_ref == -INFINITY ? 0.f : ex2f(m_ref - mx);
+            m_ref = mx;
+          }
+          if (t > 0 && __any_sync(0xffffffffu, up)) {
+            // rescale O: the previous P V must have landed first
+            const int pb = (t - 1) % kT5SBuf;
+            ok = __all_sync(0xffffffffu, t5_wait(&o_done[pb], ((t - 1) / kT5SBuf) & 1, abf, P.wait_ns));
+            t5_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+              uint32_t r[16];
+              t5_ld16(lane_base + kT5OCol + c0, r);
+              t5_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
+              t5_st16(lane_base + kT5OCol + c0, r);
+            }
+            t5_wait_st();
+          }
+          l *= a;
+          const float base = m_ref == -INFINITY ? 0.f : m_ref;
+          float ps = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kT5N; c0 += 32) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
+              ps += p0 + p1;
+              w[k] = pack2<FP8>(p0, p1);
+            }
+            t5_st16(lane_base + sb * kT5N + c0 / 2, w);
+          }
+          t5_wait_st();
+          l += ps;
+        }
+        if (!FP8 && key0 + kT5N > end_key && warp == 0) {
+          // keys past the split or the sequence (not loaded, or stale): V rows
+          // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
+          // (FP8: the converter writes those rows as zeros)
+          if (!t5_wait(&v_full[vs], (t / VS) & 1, abf, P.wait_ns)) ok = false;
+          const uint32_t vb = v_ring + vs * kT5TileBytes;
+          for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
+            const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + h * kT5HalfBytes + off + c * 16),
+                             "r"(0u)
+                             : "memory");
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        t5_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      // ---- epilogue: O of this row -------------------------------------------
+      const int lb = (n_tiles - 1) % kT5SBuf;
+      const bool have = __all_sync(0xffffffffu, ok && t5_wait(&o_done[lb], ((n_tiles - 1) / kT5SBuf) & 1, abf, P.wait_ns));
+      t5_fence_after();
+      if (have && warp_live) {
+        const int nsplit = (nblk + P.bps - 1) / P.bps;
+        const int64_t ent = ((int64_t)b * P.H_kv + g) * P.S + s;
+        __nv_bfloat16 *out = nullptr;
+        float *acc = nullptr;
+        if (live) {
+          const int j = row / P.G, hh = row % P.G;
+          out = static_cast<__nv_bfloat16 *>(P.out) + (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD;
+          acc = P.ws_acc + (ent * P.R + row) * kD;
+        }
+        // FP8: the values are codes; v_scale makes them values again
+        const float vsc = FP8 ? P.v_scale[g] : 1.f;
+        const float il = (l > 0.f ? 1.f / l : 0.f) * vsc;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          uint32_t r[64];
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + kT5OCol + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+          t5_wait_ld();
+          if (live) {
+            if (nsplit == 1) {
+#pragma unroll
+              for (int c = 0; c < 64; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  w[k] = pack2<false>(__uint_as_float(r[c + 2 * k]) * il, __uint_as_float(r[c + 2 * k + 1]) * il);
+                *reinterpret_cast<uint4 *>(out + c0 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; c += 4)
+                *reinterpret_cast<float4 *>(acc + c0 + c) =
+                    make_float4(__uint_as_float(r[c]) * vsc, __uint_as_float(r[c + 1]) * vsc,
+                                __uint_as_float(r[c + 2]) * vsc, __uint_as_float(r[c + 3]) * vsc);
+            }
+          }
+        }
+        if (live && nsplit > 1) {
+          P.ws_ml[(ent * P.R + row) * 2] = m_ref;
+          P.ws_ml[(ent * P.R + row) * 2 + 1] = l;
+        }
+      }
+    }
+  }
+  if (FP8 && (warp == 7 || warp == 8)) {
+    // ----------------------------------------------------- e4m3 -> f16 ---
+    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is kT5Blk blocks of
+    // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
+    // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
+    // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
+    // keys past the split or the sequence are written as zeros.
+    const bool isv = warp == 8;
+    const int NS = isv ? VS : KS;
+    uint64_t *rfull = isv ? v_full : k_full;
+    uint64_t *rempty = isv ? v_empty : k_empty;
+    uint64_t *cfull = isv ? vc_full : kc_full;
+    uint64_t *cempty = isv ? vc_empty : kc_empty;
+    const uint32_t rring = isv ? v_ring : k_ring;
+    const uint32_t cring = isv ? vc_ring : kc_ring;
+    const int end_key = min(L, blk1 * kBS);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int rs = t % NS, cs = t % CS;
+      bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf, P.wait_ns));
+      if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf, P.wait_ns));
+      if (!ok) break;
+      const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
+      const int key0 = (blk0 + t * kT5Blk) * kBS;
+#pragma unroll 2
+      for (int j = 0; j < 8; ++j) {
+        const int q = lane + 32 * j;
+        const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
+        uint32_t v0, v1, v2, v3;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                     : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
+        uint32_t h[8];
+        if (key0 + row < end_key) {
+          const uint32_t w[4] = {v0, v1, v2, v3};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffffu));
+            h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) h[k] = 0u;
+        }
+        const uint32_t rowb = dst + (ch >> 2) * kT5HalfBytes + blk * 2048 + r16 * 128;
+        const int c8 = 2 * (ch & 3);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
+                     "r"(h[1]), "r"(h[2]), "r"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
+                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                     : "memory");
+      }
+      // the tensor cores read the widened tile through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
+        mbar_arrive(&cfull[cs]);    // the widened stage may be read
+      }
+    }
+  }
+  if (tid == 0 && *abf) atomic_or_status(P.status, SV_DEV_TIMEOUT);
+  t5_fence_before();
+  __syncthreads();
+  t5_fence_after();
+  if (warp == kT5MmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kT5Cols));
+}
+
+// The balanced-mode kernel: the same roles, pipelines and per-tile work as
+// attn_tc5_kernel, but a CTA runs a list of work items (see T5Walk): every
+// role walks the same items, and ring stages, S buffers and barrier phases
+// follow the CTA's running tile count, so the pipelines flow from one item
+// into the next. (A single kernel for both modes measured 7 % slower in split
+// mode: 6 % more instructions on the per-tile paths.)
+template <int QR, bool FP8>
+__global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kernel(const __grid_constant__ TcParams P) {
   pdl_wait();
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
@@ -1585,27 +2081,35 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
   p.tc = (kv == SV_BF16 || kv == SV_FP8_E4M3) && qd == SV_BF16 && d == kD && bs == kBS && p.R <= kT5MaxR &&
          strides_ok;
   p.C = 0;
+  const int64_t pairs = (int64_t)B * H_kv, slots = 2 * num_sms();
   if (bps_req > 0) {
     p.bps = bps_req;
-  } else if (p.tc && (int64_t)B * H_kv < 2 * num_sms() &&
-             (int64_t)std::max(B, 1) * ((max_blocks + kT5Blk - 1) / kT5Blk) < (1ll << 30)) {
-    // balanced mode, when there are fewer (sequence, kv head) pairs than
-    // CTA slots (two per SM): a small batch or long contexts: ranges of tiles for all kv heads side by side, about
-    // two CTAs per SM (what the shared memory and TMEM of one CTA leave room
-    // for), each taking an equal share of all tiles
+  } else if (bps_req < 0 && p.tc && (int64_t)std::max(B, 1) * ((max_blocks + kT5Blk - 1) / kT5Blk) < (1ll << 30)) {
+    // balanced mode (asked for): ranges of tiles for all kv heads side by
+    // side, about two CTAs per SM (what the shared memory and TMEM of one CTA
+    // leave room for), each taking an equal share of all tiles
     const int64_t tiles = (int64_t)std::max(B, 1) * ((max_blocks + kT5Blk - 1) / kT5Blk);
-    const int64_t nr = std::max<int64_t>(1, std::min<int64_t>(2 * num_sms() / H_kv, tiles));
+    const int64_t nr = std::max<int64_t>(1, std::min<int64_t>(slots / H_kv, tiles));
     p.C = (int)(nr * H_kv);
     p.bps = 0;
     p.S = 1;
     p.per_split = 1;
     return p;
   } else if (p.tc) {
-    // split mode for larger batches: long splits amortise the tcgen05
-    // kernel's per-CTA setup (TMEM, Q, pipeline fill) and the merge; the
-    // longest-first order keeps the last wave short, so splits of up to 256
-    // blocks pay off
-    p.bps = std::min(256, std::max(16, pow2_floor((int64_t)max_blocks * B * H_kv / num_sms())));
+    // split mode on the tensor cores. With at least as many (sequence, kv
+    // head) pairs as CTA slots (two per SM), one split per pair up to 512
+    // blocks: the longest-first order balances the slots and no merge runs.
+    // With fewer pairs, floor(slots / pairs) splits per pair, so the CTAs of
+    // equal-length sequences fill the slots once (an even block count keeps
+    // the 32-key tiles whole).
+    if (pairs >= slots) {
+      p.bps = std::min(max_blocks, 512);
+    } else {
+      const int64_t per = std::max<int64_t>(1, slots / std::max<int64_t>(1, pairs));
+      int bps = (int)((max_blocks + per - 1) / per);
+      bps = std::min(512, (bps + kT5Blk - 1) / kT5Blk * kT5Blk);
+      p.bps = std::max(kT5Blk, bps);
+    }
   } else {
     // fp32 caches are planned like bf16 ones so every dtype fits the same
     // workspace
@@ -1670,6 +2174,9 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(attn_tc5_kernel<QR, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(attn_tc5_bal_kernel<QR, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg::kSmem);
   });
   if (attr_err != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_verify_attn: cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
@@ -1685,7 +2192,8 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
   }
   sv_status rc = check_launch("spec_verify_attn order launch");
   if (rc != SV_OK) return rc;
-  launch_k(attn_tc5_kernel<QR, FP8>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
+  if (P.balanced) launch_k(attn_tc5_bal_kernel<QR, FP8>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
+  else launch_k(attn_tc5_kernel<QR, FP8>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmem, st, 1, P);
   return check_launch("spec_verify_attn tcgen05 launch");
 }
 
@@ -1892,7 +2400,9 @@ extern "C" size_t spec_verify_attn_workspace_size_ex(int B, int n_new, int H_q, 
                                                      int blocks_per_split) {
   if (B < 0 || n_new < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv || d_head < 1 || max_blocks_per_seq < 1)
     return 0;
-  return ws_bytes_any(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size, blocks_per_split);
+  if (blocks_per_split < 0) return 0;
+  return ws_bytes_any(B, n_new, H_q, H_kv, d_head, max_blocks_per_seq, block_size,
+                      blocks_per_split == 0 ? -1 : blocks_per_split);
 }
 
 extern "C" sv_status spec_verify_attn(const void *q, sv_dtype q_dtype, const void *k_cache, const void *v_cache,
@@ -1915,11 +2425,11 @@ extern "C" sv_status spec_verify_attn_ex(const void *q, sv_dtype q_dtype, const 
                                          float softmax_scale, void *out, sv_dtype out_dtype, void *workspace,
                                          size_t workspace_bytes, int32_t *dev_status, int blocks_per_split,
                                          sv_stream_t stream) {
-  if (blocks_per_split < 1) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn_ex: blocks_per_split < 1");
+  if (blocks_per_split < 0) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn_ex: blocks_per_split < 0");
   return attn_impl(q, q_dtype, k_cache, v_cache, kv_dtype, layout, k_scale, v_scale, block_table,
                    max_blocks_per_seq, seq_lens, B, n_new, H_q, H_kv, d_head, block_size, num_blocks,
-                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status, blocks_per_split,
-                   nullptr, stream);
+                   softmax_scale, out, out_dtype, workspace, workspace_bytes, dev_status,
+                   blocks_per_split == 0 ? -1 : blocks_per_split, nullptr, stream);
 }
 
 extern "C" size_t spec_verify_attn_tree_workspace_size(int B, int n_new, int H_q, int H_kv, int d_head,

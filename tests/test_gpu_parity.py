@@ -185,30 +185,44 @@ def test_attention_four_splits_repeated_calls(lib):
         assert torch.equal(out, outs[0])
 
 
+@pytest.mark.parametrize("bps", [None, 0])
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
-def test_attention_one_long_sequence_in_many_pieces(lib, kv):
-    # the default launch cuts the global tile sequence into two equal ranges
-    # per SM: with one 20000-token sequence every (b, g) pair is split into
-    # tens of pieces computed by different CTAs and merged by log-sum-exp
+def test_attention_one_long_sequence_in_many_pieces(lib, kv, bps):
+    # one 20000-token sequence: the default plan cuts each (b, g) pair into
+    # as many splits as there are CTA slots per pair, and the balanced ranges
+    # (blocks_per_split = 0) into tens of pieces computed by different CTAs;
+    # both are merged by log-sum-exp
     cfg = workloads.CONFIGS["tiny"].with_(kv_dtype=kv, q_dtype="bf16", d_head=128, H_q=16, H_kv=2, K=4, B=1,
                                           ctx=("fixed", (20000,)))
     a = to_dev(workloads.make_attention_inputs(cfg, seed=21))
-    out = run_attention(lib, cfg, a)
+    out = run_attention(lib, cfg, a, blocks_per_split=bps)
     check_attention(out, oracle_attention(cfg, a), cfg)
 
 
-def test_attention_invalid_length_leaves_the_other_sequences(lib):
-    # an invalid length holds no tiles in the balanced partition: it is
-    # flagged, and every other sequence (before and after it, some split
-    # across CTAs) still gets its own result
+def test_attention_balanced_ranges_uneven_lengths(lib):
+    # balanced ranges over very uneven lengths: ranges run through several
+    # short sequences and cut the long one into many pieces
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128, H_q=8, H_kv=2, B=7,
+                                          ctx=("fixed", (9000, 5, 40, 700, 33, 1500, 64)))
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=8))
+    out = run_attention(lib, cfg, a, blocks_per_split=0)
+    check_attention(out, oracle_attention(cfg, a), cfg)
+
+
+@pytest.mark.parametrize("bps", [None, 0])
+def test_attention_invalid_length_leaves_the_other_sequences(lib, bps):
+    # an invalid length is flagged and holds no tiles (of the balanced
+    # ranges too): every other sequence, before and after it, some split
+    # across CTAs, still gets its own result
     cfg = workloads.CONFIGS["tiny"].with_(kv_dtype="bf16", q_dtype="bf16", d_head=128, H_q=8, H_kv=2, B=6,
                                           ctx=("fixed", (300, 5000, 17, 2000, 45, 1000)))
     a = to_dev(workloads.make_attention_inputs(cfg, seed=4))
     lens = a["seq_lens"].clone()
     lens[2] = 10_000
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw = {} if bps is None else {"blocks_per_split": bps}
     out = lib.spec_verify_attn(a["q"], a["k_cache"], a["v_cache"], a["block_table"], lens,
-                               1 / math.sqrt(cfg.d_head), block_size=cfg.block_size, status=status)
+                               1 / math.sqrt(cfg.d_head), block_size=cfg.block_size, status=status, **kw)
     torch.cuda.synchronize()
     assert int(status.item()) & 1
     keep = [0, 1, 3, 4, 5]
