@@ -1138,78 +1138,74 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
         const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
         static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
-        // Q K^T and P V each walk the items on their own: (item index, tiles
-        // of the item, next tile in it) and the running tile count
-        T5Walk wq = {}, wp = {};
-        T5Item iq, ip;
-        bool hq = t5_item(P, wq, iq), hp = t5_item(P, wp, ip);
-        int nq = hq ? (iq.blk1 - iq.blk0 + kT5Blk - 1) / kT5Blk : 0;
-        int np = hp ? (ip.blk1 - ip.blk0 + kT5Blk - 1) / kT5Blk : 0;
-        int xq = 0, tq_l = 0, tp_l = 0;   // item of Q K^T; tiles done in the current items
-        int uq = 0, up = 0;               // running tile counts
-        bool q_ready = false;
-        uint64_t t_last = global_ns();
-        while (hp) {
-          bool progressed = false;
-          if (hq && !q_ready) q_ready = t5_test(&q_full, xq & 1);
-          if (hq && q_ready && uq - up < kT5SBuf) {
-            // K stage: the TMA ring (bf16) or the widened ring (FP8)
-            const int KR = FP8 ? CS : KS;
-            const int ks = uq % KR, sb = uq % kT5SBuf;
-            uint64_t *kf = FP8 ? kc_full : k_full;
-            // S buffer sb is free once the P V of tile uq - kT5SBuf has run
-            const bool sfree = uq < kT5SBuf || t5_test(&o_done[sb], ((uq / kT5SBuf) - 1) & 1);
-            if (sfree && t5_test(&kf[ks], (uq / KR) & 1)) {
-              t5_fence_after();
-              const uint32_t kb = kc_ring + ks * kT5TileBytes;
+        // the items in order, each with the split kernel's loop; u0 is the
+        // CTA's running tile count at the item's start. The next item's
+        // Q K^T could not start earlier anyway: its Q is written after this
+        // item's epilogue, which waits for the last P V.
+        T5Walk wk = {};
+        T5Item it;
+        int u0 = 0, xq = 0;
+        bool okm = true;
+        while (okm && t5_item(P, wk, it)) {
+          const int n_tiles = (it.blk1 - it.blk0 + kT5Blk - 1) / kT5Blk;
+          int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
+          bool q_ready = false;
+          uint64_t t_last = global_ns();
+          while (tp < n_tiles) {
+            bool progressed = false;
+            if (!q_ready) q_ready = t5_test(&q_full, xq & 1);
+            if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
+              // K stage: the TMA ring (bf16) or the widened ring (FP8)
+              const int KR = FP8 ? CS : KS;
+              const int uq = u0 + tq;
+              const int ks = uq % KR, sb = uq % kT5SBuf;
+              uint64_t *kf = FP8 ? kc_full : k_full;
+              // S buffer sb is free once the P V of tile uq - kT5SBuf has run
+              const bool sfree = uq < kT5SBuf || t5_test(&o_done[sb], ((uq / kT5SBuf) - 1) & 1);
+              if (sfree && t5_test(&kf[ks], (uq / KR) & 1)) {
+                t5_fence_after();
+                const uint32_t kb = kc_ring + ks * kT5TileBytes;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
-                t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
-                          t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
-                          kk > 0 ? 1u : 0u);
-              t5_commit(&s_full[sb]);
-              t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
-              ++uq;
-              if (++tq_l == nq) {   // next item: its Q is written after this item's epilogue
-                hq = t5_item(P, wq, iq);
-                nq = hq ? (iq.blk1 - iq.blk0 + kT5Blk - 1) / kT5Blk : 0;
-                tq_l = 0;
-                ++xq;
-                q_ready = false;
+                for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
+                  t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
+                            t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
+                            kk > 0 ? 1u : 0u);
+                t5_commit(&s_full[sb]);
+                t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
+                ++tq;
+                progressed = true;
               }
-              progressed = true;
+            }
+            if (tp < tq) {
+              const int VR = FP8 ? CS : VS;
+              const int up = u0 + tp;
+              const int vs = up % VR, sb = up % kT5SBuf;
+              uint64_t *vf = FP8 ? vc_full : v_full;
+              if (t5_test(&p_full[sb], (up / kT5SBuf) & 1) && t5_test(&vf[vs], (up / VR) & 1)) {
+                t5_fence_after();
+                const uint32_t vb = vc_ring + vs * kT5TileBytes;
+#pragma unroll
+                for (int j = 0; j < kT5Blk; ++j)   // an item's first P V starts O afresh
+                  t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
+                            idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
+                t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
+                t5_commit(&o_done[sb]);
+                ++tp;
+                progressed = true;
+              }
+            }
+            if (progressed) {
+              t_last = global_ns();
+            } else if (*abf || global_ns() - t_last > P.wait_ns) {
+              *abf = 1;
+              okm = false;
+              break;
+            } else {
+              __nanosleep(64);   // leave issue slots to the other warps of this scheduler
             }
           }
-          if (up < uq) {
-            const int VR = FP8 ? CS : VS;
-            const int vs = up % VR, sb = up % kT5SBuf;
-            uint64_t *vf = FP8 ? vc_full : v_full;
-            if (t5_test(&p_full[sb], (up / kT5SBuf) & 1) && t5_test(&vf[vs], (up / VR) & 1)) {
-              t5_fence_after();
-              const uint32_t vb = vc_ring + vs * kT5TileBytes;
-#pragma unroll
-              for (int j = 0; j < kT5Blk; ++j)   // an item's first P V starts O afresh
-                t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
-                          idesc_pv, (tp_l > 0 || j > 0) ? 1u : 0u);
-              t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
-              t5_commit(&o_done[sb]);
-              ++up;
-              if (++tp_l == np) {
-                hp = t5_item(P, wp, ip);
-                np = hp ? (ip.blk1 - ip.blk0 + kT5Blk - 1) / kT5Blk : 0;
-                tp_l = 0;
-              }
-              progressed = true;
-            }
-          }
-          if (progressed) {
-            t_last = global_ns();
-          } else if (*abf || global_ns() - t_last > P.wait_ns) {
-            *abf = 1;
-            break;
-          } else {
-            __nanosleep(64);   // leave issue slots to the other warps of this scheduler
-          }
+          u0 += n_tiles;
+          ++xq;
         }
         // every MMA issued has completed before TMEM can be released
         t5_commit(&mma_drain);
