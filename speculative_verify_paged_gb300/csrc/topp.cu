@@ -41,6 +41,13 @@
 // A logit's bin is round(32 (m - x) c) from the same roundings in every pass,
 // so it is non-increasing in x and a bin boundary never separates equal
 // logits; NaN and -inf fall in the last bin, which takes no mass.
+//
+// That is the general kernel, topp_row_kernel. Rows of at most 188000 logits
+// (every vocabulary the workloads use) run topp_bin_kernel instead, which
+// keeps exact per-bin masses in pass 2 (a count and quantised offsets from
+// each bin's nominal weight, two 32-bit atomics per logit), so that Z, the
+// window and the mass above it are exact sums and the write pass only
+// compares logits with two thresholds.
 
 #include <cmath>
 #include <mutex>
@@ -74,6 +81,7 @@ struct TpParams {
   int qbits;          // s: pass 2 scales bin f's weights by 2^(f/32 + s)
   double win_eps;     // relative error bound of pass 2's cumulative masses
   int32_t *status;
+  unsigned long long base[128];   // topp_bin_kernel: 2^(-j/128) in 2^-62 fixed point
 };
 
 // Per logit type: the element at position k of a 16-byte group, its value,
@@ -640,6 +648,422 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_row_kernel(const __grid_co
   }
 }
 
+// ---------------------------------------------------------------------------
+// topp_bin_kernel: rows of at most kTbMaxV logits. The same set with exact
+// per-bin masses, so that the write pass needs no weights.
+//
+// Pass 2 puts every logit in one of 8192 bins of 1/128 of a binade of weight
+// (bin f: weights within 2^(+-1/256) of 2^(-f/128)) and adds, with two 32-bit
+// shared atomics, 1 to the bin's count and q = round(2^22 v) - 2^22 to its
+// offset sum, where v = w 2^(f/128) is the weight relative to the bin's
+// nominal one (|q| <= 11373, so V <= kTbMaxV keeps the sum inside int32).
+// v comes from one SFU exp2 of h + f/128, an exact difference of at most
+// 1/256, with the first-order correction for the rounding of the exponent.
+// A bin's mass is then 2^(-f/128) (n_f + R_f 2^-22): each weight within
+// 2^-23 of its quantised value and about 2e-7 of its exact one. The masses
+// go to 2^-40 fixed point with a 64 x 64-bit product (2^(-j/128) in 2^-62
+// fixed point from the host, an exact shift for the binade), so Z, the
+// cumulative sums and the mass above the window are exact 64-bit integers
+// and the kernel is deterministic. A block scan gives the window of bins
+// where the running mass reaches ceil(top_p Z) (with a 1e-6 Z margin: one
+// bin in nearly every row), and bisection over the logits' ordered bits
+// gives the two logit thresholds of its edges (bins are non-increasing in the
+// logit). Pass 3 then keeps x >= x_keep, with packed two-lane compares for
+// 16-bit logits, and gathers the window's tokens (x_keep <= x < x_above) for
+// the ranking, as the general kernel does.
+constexpr int kTbBins = 8192;
+constexpr int kTbPer = kTbBins / kTpThreads;     // bins per thread in the scan
+constexpr int kTbMaxV = 188000;                  // 188000 * 11373 < 2^31
+constexpr size_t kTbSmem = (size_t)kTbBins * 8 + (size_t)kTpCap * (8 + 8 + 4) + 256 * 8;
+static_assert(kTbPer * kTpThreads == kTbBins, "bins per thread");
+
+// (hi:lo) = a * b, then >> s (44 <= s < 128)
+__device__ __forceinline__ u64 tb_mulshift(u64 a, u64 b, int s) {
+  const u64 lo = a * b, hi = __umul64hi(a, b);
+  if (s >= 64) return s >= 128 ? 0ull : hi >> (s - 64);
+  return (hi << (64 - s)) | (lo >> s);
+}
+
+// value bits of a 16- or 32-bit logit from its ordered key (the inverse of
+// the key map of tp_composite)
+template <typename T>
+__device__ __forceinline__ uint32_t tb_from_key(uint32_t k) {
+  using TT = TpType<T>;
+  return (k & TT::kSign) ? (k & ~TT::kSign) : (~k & TT::kKeyMask);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t tb_key(uint32_t b) {
+  using TT = TpType<T>;
+  return (b & TT::kSign) ? (~b & TT::kKeyMask) : (b | TT::kSign);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_constant__ TpParams P) {
+  using TT = TpType<T>;
+  constexpr int G = TT::G;
+  extern __shared__ __align__(16) uint8_t tb_smem[];
+  unsigned *cnt = reinterpret_cast<unsigned *>(tb_smem);                 // [kTbBins]
+  int *dsum = reinterpret_cast<int *>(tb_smem + (size_t)kTbBins * 4);    // [kTbBins]
+  u64 *c_comp = reinterpret_cast<u64 *>(tb_smem + (size_t)kTbBins * 8);  // [kTpCap]
+  u64 *c_q = c_comp + kTpCap;                                           // [kTpCap]
+  u64 *rhist = c_q + kTpCap;                                            // [256]
+  int *c_pos = reinterpret_cast<int *>(rhist + 256);                    // [kTpCap]
+  __shared__ u64 s_warp64[kTpWarps];
+  __shared__ float s_wmax[kTpWarps];
+  __shared__ int s_wflag[kTpWarps];
+  __shared__ int s_flo, s_fhi, s_sel;
+  __shared__ u64 s_above, s_above_q, s_cut, s_cmax, s_cmin;
+  __shared__ uint32_t s_xkeep, s_xabove;
+  __shared__ unsigned s_count;
+
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x;
+  const void *in;
+  void *out;
+  if (row < P.rows0) {
+    in = static_cast<const T *>(P.in0) + (int64_t)row * P.V;
+    out = static_cast<T *>(P.out0) + (int64_t)row * P.V;
+  } else {
+    in = static_cast<const T *>(P.in1) + (int64_t)(row - P.rows0) * P.V;
+    out = static_cast<T *>(P.out1) + (int64_t)(row - P.rows0) * P.V;
+  }
+  const int V = P.V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // ---- 1. row maximum (max ignores NaN; max.NaN propagates it, for the flag) ----
+  uint32_t wmax = TT::kNegInfWord, wnan = TT::kNegInfWord;
+  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      wmax = TT::pmax(wmax, (&r.x)[j]);
+      wnan = TT::pmax_nan(wnan, (&r.x)[j]);
+    }
+  });
+  for (int i = threadIdx.x; i < kTbBins; i += kTpThreads) {
+    cnt[i] = 0u;
+    dsum[i] = 0;
+  }
+  if (threadIdx.x == 0) {
+    s_count = 0u; s_sel = -1; s_flo = 0; s_fhi = kTbBins - 2;
+    s_above = 0ull; s_above_q = 0ull; s_cut = 0ull; s_cmax = 0ull; s_cmin = ~0ull;
+  }
+  {
+    float mx = warp_max(TT::word_max(wmax));
+    int flag = TT::word_nan(wnan) ? 1 : 0;
+    flag = (int)__reduce_or_sync(0xffffffffu, (unsigned)flag);
+    if (lane == 0) { s_wmax[warp] = mx; s_wflag[warp] = flag; }
+  }
+  __syncthreads();
+  float m = -INFINITY;
+  int flag = 0;
+#pragma unroll
+  for (int w = 0; w < kTpWarps; ++w) { m = fmaxf(m, s_wmax[w]); flag |= s_wflag[w]; }
+  if ((flag || m == INFINITY) && threadIdx.x == 0) atomic_or_status(P.status, SV_DEV_NONFINITE);
+
+  if (!(m > -INFINITY) || m == INFINITY) {
+    // nothing to rank (no finite logit, or a +inf one): the row is passed
+    // through unchanged and the sampling flags it
+    if (out != in)
+      tp_row_groups<T>(in, V, 0, [&](int e0, const uint4 &r, int nv) {
+#pragma unroll
+        for (int k = 0; k < G; ++k)
+          if (k < nv) TT::st1(out, e0 + k, TT::get(r, k));
+      });
+    return;
+  }
+
+  // bin = round(-128 h), h = (x - m) c_hi, from one fma onto the integer grid
+  // of [2^23, 2^24), capped at the last bin (which also takes -inf and NaN)
+  const float c_hi = P.c_hi, c_lo = P.c_lo;
+  const float top = 8388608.f + (float)(kTbBins - 1);
+  auto bin_of = [&](float x, float &d, float &h, float &y) {
+    d = __fsub_rn(x, m);
+    h = __fmul_rn(d, c_hi);
+    y = fminf(fmaf(h, -128.f, 8388608.f), top);
+    return __float_as_int(y) - 0x4B000000;
+  };
+  // lo: the rounding of the exponent d c (fma for the product, two-sum for
+  // x - m where it is not exact)
+  auto lo_of = [&](float x, float d, float h) {
+    float l = fmaf(d, c_hi, -h);
+    l = fmaf(d, c_lo, l);
+    if (!TT::kExactDiff) {
+      const float bb = d - x;
+      const float d_lo = (x - (d - bb)) + (-m - bb);
+      l = fmaf(d_lo, c_hi, l);
+    }
+    return l;
+  };
+  auto weight_of = [&](float x, float d, float h) -> float {
+    const float t = tp_ex2(h);
+    return fmaf(t, lo_of(x, d, h) * 0.693147180559945309f, t);
+  };
+
+  // ---- 2. counts and quantised offsets per bin ----
+  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const float x = TT::val(TT::get(r, k));
+      float d, h, y;
+      const int fb = bin_of(x, d, h, y);
+      if (fb < kTbBins - 1) {
+        const float rr = fmaf(y - 8388608.f, 0.0078125f, h);   // h + fb / 128, exact
+        const float t = tp_ex2(rr);
+        const float v = fmaf(t, lo_of(x, d, h) * 0.693147180559945309f, t);
+        const int q = (int)__float_as_uint(fmaf(v, 4194304.f, 8388608.f)) - 0x4B400000;
+        atomicAdd(&cnt[fb], 1u);
+        atomicAdd(&dsum[fb], q);
+      }
+    }
+  });
+  __syncthreads();
+  u64 thr;
+  {
+    // bin masses in 2^-40 fixed point, their exact scan, Z, and the window
+    u64 a[kTbPer];
+    u64 part = 0;
+#pragma unroll
+    for (int j = 0; j < kTbPer; ++j) {
+      const int f = threadIdx.x * kTbPer + j;
+      const u64 N = (u64)((int64_t)cnt[f] * 4194304 + (int64_t)dsum[f]);
+      a[j] = tb_mulshift(P.base[f & 127], N, 44 + (f >> 7));
+      part += a[j];
+    }
+    u64 Z;
+    u64 cum = tp_block_excl_scan(part, s_warp64, &Z);
+    const double td = ceil(P.top_p * (double)Z);
+    thr = td < 1.0 ? 1ull : (td >= (double)Z ? Z : (u64)td);
+    const u64 marg = (u64)(1e-6 * (double)Z) + 1;
+    const u64 lo_u = thr > marg ? thr - marg : 1ull, hi_u = thr + marg;
+#pragma unroll
+    for (int j = 0; j < kTbPer; ++j) {
+      const int f = threadIdx.x * kTbPer + j;
+      if (cum < lo_u && lo_u <= cum + a[j]) { s_flo = f; s_above = cum; }
+      if (cum < hi_u && hi_u <= cum + a[j]) s_fhi = f;
+      cum += a[j];
+    }
+  }
+  __syncthreads();
+  const int f_lo = s_flo, f_hi = max(s_flo, min(s_fhi, kTbBins - 2));
+  const u64 above = s_above;   // exact mass of the bins above the window
+  if (threadIdx.x < 2) {
+    // bisection over the ordered keys between -inf (last bin) and m (bin 0):
+    // the smallest key whose bin is at most F. x_keep: F = f_hi (x >= x_keep
+    // <=> bin <= f_hi); x_above: F = f_lo - 1 (none when f_lo = 0)
+    const int F = threadIdx.x == 0 ? f_hi : f_lo - 1;
+    uint32_t res;
+    if (F < 0) {
+      res = TT::kInf;   // +inf: no logit lies above a window at the top
+    } else {
+      // m is one of the row's logits: its bits in the logit type
+      uint32_t mb;
+      if constexpr (sizeof(T) == 4) mb = __float_as_uint(m);
+      else if constexpr (std::is_same<T, __nv_bfloat16>::value) mb = __float_as_uint(m) >> 16;
+      else mb = (uint32_t)__half_as_ushort(__float2half(m));
+      // invariant: bin(value of lo) > F (lo starts at -inf, the last bin),
+      // bin(value of hi) <= F (hi starts at m, bin 0)
+      uint32_t lo = tb_key<T>(TT::kNegInf), hi = tb_key<T>(mb);
+      while (hi - lo > 1) {
+        const uint32_t mid = lo + (hi - lo) / 2;
+        float d, h, y;
+        if (bin_of(TT::val(tb_from_key<T>(mid)), d, h, y) <= F) hi = mid;
+        else lo = mid;
+      }
+      res = tb_from_key<T>(hi);
+    }
+    if (threadIdx.x == 0) s_xkeep = res;
+    else s_xabove = res;
+  }
+  __syncthreads();
+  const uint32_t xk_b = s_xkeep, xa_b = s_xabove;
+  const float x_keep = TT::val(xk_b), x_above = TT::val(xa_b);
+
+  // ---- 3. write the row: x >= x_keep stays, the window's tokens
+  // (x_keep <= x < x_above) are gathered ----
+  auto gather_one = [&](int e, uint32_t b, unsigned slot) {
+    const float x = TT::val(b);
+    float d, h, y;
+    bin_of(x, d, h, y);
+    c_comp[slot] = tp_composite<T>(b, e);
+    c_q[slot] = __float2ull_rn(weight_of(x, d, h) * kTpQuant);
+    c_pos[slot] = e;
+  };
+  tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+    uint32_t ow[4];
+    unsigned cm = 0;
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x = __uint_as_float((&r.x)[k]);
+        const bool keep = x >= x_keep;
+        ow[k] = keep ? (&r.x)[k] : TT::kNegInf;
+        cm |= (keep && !(x >= x_above) && k < nv) ? 1u << k : 0u;
+      }
+    } else {
+      const uint32_t k2 = xk_b | (xk_b << 16), a2 = xa_b | (xa_b << 16);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = (&r.x)[j];
+        uint32_t km, am;
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+          km = __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w), *reinterpret_cast<const __nv_bfloat162 *>(&k2));
+          am = __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w), *reinterpret_cast<const __nv_bfloat162 *>(&a2));
+        } else {
+          km = __hge2_mask(*reinterpret_cast<const __half2 *>(&w), *reinterpret_cast<const __half2 *>(&k2));
+          am = __hge2_mask(*reinterpret_cast<const __half2 *>(&w), *reinterpret_cast<const __half2 *>(&a2));
+        }
+        ow[j] = (w & km) | (TT::kNegInfWord & ~km);
+        const unsigned c2 = km & ~am;
+        cm |= ((c2 & 0xffffu) ? 1u : 0u) << (2 * j);
+        cm |= ((c2 >> 16) ? 1u : 0u) << (2 * j + 1);
+      }
+      cm &= (nv >= G) ? 0xffu : ((1u << nv) - 1u);
+    }
+    if (P.vec && nv == G) {
+      *reinterpret_cast<uint4 *>(static_cast<T *>(out) + e0) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < G; ++k)
+        if (k < nv) TT::st1(out, e0 + k, sizeof(T) == 4 ? ow[k % 4] : ((ow[k >> 1] >> ((k & 1) * 16)) & 0xffffu));
+    }
+    if (cm) {
+      unsigned slot = atomicAdd(&s_count, (unsigned)__popc(cm));
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (((cm >> k) & 1u) && slot < (unsigned)kTpCap) gather_one(e0 + k, TT::get(r, k), slot);
+        slot += (cm >> k) & 1u;
+      }
+    }
+  });
+  __syncthreads();
+
+  // ---- the rare split: more than kTpCap tokens in the window. Histogram
+  // them by the next 8 bits of the composite, keep the digit where the
+  // running mass reaches thr, and gather again. Logits outside the window
+  // were final after pass 3 and the window's are unchanged in `in` (also when
+  // out == in), so the passes read `in`. ----
+  int sh = 64;        // the composite's bits at and above sh equal pfx
+  u64 pfx = 0ull;
+  u64 above_q = 0ull; // exact mass of the window's tokens above the prefix
+  int n_all = (int)s_count;
+  auto in_window = [&](uint32_t b, int e, u64 &comp) {
+    const float x = TT::val(b);
+    if (!(x >= x_keep) || x >= x_above) return false;
+    comp = tp_composite<T>(b, e);
+    return sh >= 64 || (comp >> sh) == pfx;
+  };
+  while (n_all > kTpCap && sh > 0) {
+    const int nsh = sh > 8 ? sh - 8 : 0;
+    const int width = sh - nsh;
+    __syncthreads();   // every thread has read s_count and s_sel before they are reset
+    for (int i = threadIdx.x; i < 256; i += kTpThreads) rhist[i] = 0ull;
+    if (threadIdx.x == 0) { s_count = 0u; s_sel = -1; }
+    __syncthreads();
+    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const uint32_t b = TT::get(r, k);
+        u64 comp;
+        if (k < nv && in_window(b, e0 + k, comp)) {
+          const float x = TT::val(b);
+          float d, h, y;
+          bin_of(x, d, h, y);
+          atomicAdd(&rhist[(int)((comp >> nsh) & ((1ull << width) - 1ull))],
+                    __float2ull_rn(weight_of(x, d, h) * kTpQuant));
+        }
+      }
+    });
+    __syncthreads();
+    {
+      // digits in descending order: entry i is digit 255 - i
+      const int i = threadIdx.x;
+      const u64 mine = i < 256 ? rhist[255 - i] : 0ull;
+      u64 tot;
+      const u64 cum = above + above_q + tp_block_excl_scan(mine, s_warp64, &tot);
+      if (i < 256 && mine > 0ull && cum < thr && thr <= cum + mine) {
+        s_sel = 255 - i;
+        s_above_q = cum - above;
+      }
+      __syncthreads();
+      const int sel0 = s_sel;
+      __syncthreads();   // read by every thread before thread 0 may write it
+      if (sel0 < 0) {
+        if (threadIdx.x == 0) {
+          // rounding left no digit that crosses: the first nonempty digit when
+          // the mass above already reaches thr, else the last
+          const bool before_all = above + above_q >= thr;
+          u64 c = above_q;
+          for (int dgt = 255; dgt >= 0; --dgt) {
+            if (rhist[dgt] == 0ull) continue;
+            if (before_all) { s_sel = dgt; s_above_q = c; break; }
+            s_sel = dgt; s_above_q = c;
+            c += rhist[dgt];
+          }
+        }
+        __syncthreads();
+      }
+    }
+    above_q = s_above_q;
+    pfx = (sh >= 64 ? 0ull : (pfx << width)) | (u64)(s_sel < 0 ? 0 : s_sel);
+    sh = nsh;
+    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+      unsigned cm = 0;
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        u64 comp;
+        if (k < nv && in_window(TT::get(r, k), e0 + k, comp)) cm |= 1u << k;
+      }
+      if (cm) {
+        unsigned slot = atomicAdd(&s_count, (unsigned)__popc(cm));
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+          if (((cm >> k) & 1u) && slot < (unsigned)kTpCap) gather_one(e0 + k, TT::get(r, k), slot);
+          slot += (cm >> k) & 1u;
+        }
+      }
+    });
+    __syncthreads();
+    n_all = (int)s_count;
+  }
+
+  // ---- the cut: candidate i is the cut iff the mass before it (everything
+  // above the window and the prefix, plus every candidate with a larger
+  // composite) is below thr and reaches thr with it ----
+  if (n_all <= kTpCap) {
+    for (int i = threadIdx.x; i < n_all; i += kTpThreads) {
+      const u64 ci = c_comp[i], qi = c_q[i];
+      u64 before = above + above_q;
+      for (int j = 0; j < n_all; ++j) before += (c_comp[j] > ci) ? c_q[j] : 0ull;
+      if (before < thr && thr <= before + qi) s_cut = ci;
+      atomicMax(&s_cmax, ci);
+      atomicMin(&s_cmin, ci);
+    }
+  }
+  __syncthreads();
+  u64 cut = s_cut;
+  if (cut == 0ull && n_all > 0 && n_all <= kTpCap) {
+    // rounding at the window's edge left no candidate that crosses thr: the
+    // first candidate when the mass above already reaches thr, else the last
+    cut = above + above_q >= thr ? s_cmax : s_cmin;
+  }
+  if (cut == 0ull) return;   // not reached: the window is kept whole
+  if (sh == 64) {
+    for (int i = threadIdx.x; i < n_all; i += kTpThreads)
+      if (c_comp[i] < cut) TT::st1(out, c_pos[i], TT::kNegInf);
+  } else {
+    sh = 64;
+    tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const uint32_t b = TT::get(r, k);
+        u64 comp;
+        if (k < nv && in_window(b, e0 + k, comp) && comp < cut) TT::st1(out, e0 + k, TT::kNegInf);
+      }
+    });
+  }
+}
+
 }  // namespace
 
 // Launches the filter over rows0 rows of in0 -> out0 followed by rows1 rows of
@@ -672,11 +1096,31 @@ sv_status launch_topp_filter(sv_dtype dtype, const void *in0, void *out0, int ro
   P.status = status;
   cudaError_t e = cudaSuccess;
   const dim3 grid(rows0 + rows1);
-  switch (dtype) {
-    case SV_F32: e = launch_k(topp_row_kernel<float>, grid, dim3(kTpThreads), 0, s, 1, P); break;
-    case SV_BF16: e = launch_k(topp_row_kernel<__nv_bfloat16>, grid, dim3(kTpThreads), 0, s, 1, P); break;
-    case SV_F16: e = launch_k(topp_row_kernel<__half>, grid, dim3(kTpThreads), 0, s, 1, P); break;
-    default: return fail(SV_ERR_UNSUPPORTED, "top-p filter: logits must be f32, bf16 or f16");
+  if (V <= kTbMaxV) {
+    // exact per-bin masses: rows up to kTbMaxV logits
+    for (int j = 0; j < 128; ++j) P.base[j] = (unsigned long long)std::llround(std::ldexp(std::exp2(-j / 128.0), 62));
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+      const cudaError_t e1 = cudaFuncSetAttribute(topp_bin_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTbSmem);
+      const cudaError_t e2 = cudaFuncSetAttribute(topp_bin_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTbSmem);
+      const cudaError_t e3 = cudaFuncSetAttribute(topp_bin_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTbSmem);
+      attr = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+    });
+    if (attr != cudaSuccess) return fail(SV_ERR_CUDA, "top-p filter: cudaFuncSetAttribute: %s", cudaGetErrorString(attr));
+    switch (dtype) {
+      case SV_F32: e = launch_k(topp_bin_kernel<float>, grid, dim3(kTpThreads), kTbSmem, s, 1, P); break;
+      case SV_BF16: e = launch_k(topp_bin_kernel<__nv_bfloat16>, grid, dim3(kTpThreads), kTbSmem, s, 1, P); break;
+      case SV_F16: e = launch_k(topp_bin_kernel<__half>, grid, dim3(kTpThreads), kTbSmem, s, 1, P); break;
+      default: return fail(SV_ERR_UNSUPPORTED, "top-p filter: logits must be f32, bf16 or f16");
+    }
+  } else {
+    switch (dtype) {
+      case SV_F32: e = launch_k(topp_row_kernel<float>, grid, dim3(kTpThreads), 0, s, 1, P); break;
+      case SV_BF16: e = launch_k(topp_row_kernel<__nv_bfloat16>, grid, dim3(kTpThreads), 0, s, 1, P); break;
+      case SV_F16: e = launch_k(topp_row_kernel<__half>, grid, dim3(kTpThreads), 0, s, 1, P); break;
+      default: return fail(SV_ERR_UNSUPPORTED, "top-p filter: logits must be f32, bf16 or f16");
+    }
   }
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "top-p filter launch: %s", cudaGetErrorString(e));
   return ok();

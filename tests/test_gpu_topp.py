@@ -9,11 +9,11 @@ oracle's sets for top_p - TOPP_TOL and top_p + TOPP_TOL; when no cumulative
 mass lies in that band the set is the oracle's exactly. Kept logits must be
 bit-identical to the input; every other entry is -inf.
 
-Rows are built to reach every path of the kernel: ordinary rows, rows with
+Rows are built to reach every path of the kernels: ordinary rows, rows with
 many equal logits, rows whose crossing bin holds more than the 512 tokens
 ranked directly (all logits equal; a dense f32 cluster), NaN and -inf
-entries, logits around 3e5, a vocabulary of one, and the full 128256-token
-vocabulary.
+entries, logits around 3e5, a vocabulary of one, the full 128256-token
+vocabulary, and rows above 188000 logits (the general kernel).
 """
 import numpy as np
 import pytest
@@ -85,7 +85,10 @@ def rows_for(kind, rows, V, dt, seed):
 CASES = [("normal", "bf16", 1000), ("normal", "f32", 1000), ("normal", "f16", 4099), ("ties", "bf16", 5000),
          ("equal", "bf16", 4096), ("equal", "f32", 3000), ("dense", "f32", 50000), ("neginf", "bf16", 777),
          ("sharp", "bf16", 32000), ("normal", "bf16", 1), ("normal", "bf16", 17), ("normal", "bf16", 128256),
-         ("normal", "f32", 128256), ("huge", "f32", 5000)]
+         ("normal", "f32", 128256), ("huge", "f32", 5000),
+         # rows above 188000 logits take the general kernel (approximate bin
+         # sums to find the window, compensated sums for the cut)
+         ("normal", "bf16", 200003), ("ties", "f32", 190001)]
 
 
 @pytest.mark.parametrize("kind,dt,V", CASES, ids=["%s-%s-%d" % c for c in CASES])
