@@ -221,21 +221,23 @@ __device__ __forceinline__ u64 tp_composite(uint32_t b, int id) {
 // round-robin over the threads, kTpUnroll loads in flight per thread; the
 // ragged end (and the whole row when it is not 16-byte aligned) is loaded one
 // element at a time.
-template <typename T, typename F>
+template <typename T, bool LAST = false, typename F>
 __device__ __forceinline__ void tp_row_groups(const void *row, int V, int vec, F f) {
   using TT = TpType<T>;
   constexpr int G = TT::G;
   const int ng = vec ? V / G : 0;
   const uint4 *rv = static_cast<const uint4 *>(row);
+  // LAST: the pass that reads the row for the last time loads it evict-first
+  auto ld = [](const uint4 *p) { return LAST ? __ldcs(p) : __ldg(p); };
   int g = threadIdx.x;
   for (; g + (kTpUnroll - 1) * kTpThreads < ng; g += kTpUnroll * kTpThreads) {
     uint4 r[kTpUnroll];
 #pragma unroll
-    for (int u = 0; u < kTpUnroll; ++u) r[u] = __ldg(rv + g + u * kTpThreads);
+    for (int u = 0; u < kTpUnroll; ++u) r[u] = ld(rv + g + u * kTpThreads);
 #pragma unroll
     for (int u = 0; u < kTpUnroll; ++u) f((g + u * kTpThreads) * G, r[u], G);
   }
-  for (; g < ng; g += kTpThreads) f(g * G, __ldg(rv + g), G);
+  for (; g < ng; g += kTpThreads) f(g * G, ld(rv + g), G);
   for (int h = ng + (int)threadIdx.x; h * G < V; h += kTpThreads) {
     const int nv = min(G, V - h * G);
     uint4 r = make_uint4(TT::kNegInfWord, TT::kNegInfWord, TT::kNegInfWord, TT::kNegInfWord);
@@ -889,7 +891,9 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
     c_q[slot] = __float2ull_rn(weight_of(x, d, h) * kTpQuant);
     c_pos[slot] = e;
   };
-  tp_row_groups<T>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
+  // (the output is written with streaming stores and the row read evict-
+  // first, so that neither displaces the rows other CTAs still re-read from L2)
+  tp_row_groups<T, true>(in, V, P.vec, [&](int e0, const uint4 &r, int nv) {
     uint32_t ow[4];
     unsigned cm = 0;
     if constexpr (sizeof(T) == 4) {
@@ -921,7 +925,7 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
       cm &= (nv >= G) ? 0xffu : ((1u << nv) - 1u);
     }
     if (P.vec && nv == G) {
-      *reinterpret_cast<uint4 *>(static_cast<T *>(out) + e0) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      __stcs(reinterpret_cast<uint4 *>(static_cast<T *>(out) + e0), make_uint4(ow[0], ow[1], ow[2], ow[3]));
     } else {
 #pragma unroll
       for (int k = 0; k < G; ++k)
