@@ -88,7 +88,9 @@ CASES = [("normal", "bf16", 1000), ("normal", "f32", 1000), ("normal", "f16", 40
          ("normal", "f32", 128256), ("huge", "f32", 5000),
          # rows above 188000 logits take the general kernel (approximate bin
          # sums to find the window, compensated sums for the cut)
-         ("normal", "bf16", 200003), ("ties", "f32", 190001)]
+         ("normal", "bf16", 200003), ("ties", "f32", 190001),
+         # the largest row of the exact-bin kernel, and the first of the general one
+         ("dense", "f16", 188000), ("equal", "bf16", 188001)]
 
 
 @pytest.mark.parametrize("kind,dt,V", CASES, ids=["%s-%s-%d" % c for c in CASES])
