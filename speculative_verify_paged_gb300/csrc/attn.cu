@@ -62,6 +62,21 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// maximum of a tile's N scores per row as a tree of depth log2 N (a chain
+// of N - 1 dependent maxima otherwise sits on every tile's critical path)
+template <int N>
+__device__ __forceinline__ float t5_tile_max(const float (&x)[N]) {
+  static_assert(N >= 2 && (N & (N - 1)) == 0, "power of two");
+  float m[N / 2];
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) m[k] = fmaxf(x[k], x[k + N / 2]);
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) m[k] = fmaxf(m[k], m[k + w]);
+  return m[0];
+}
+
 // 2^x on the SFU (results below 2^-126 flush to zero)
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -113,6 +128,7 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   const uint64_t *anc;    // [B][n_new] ancestor masks of a draft tree (NULL: a chain)
   int32_t *status;
   int B, n_new, H_q, H_kv, G, R, max_blocks, num_blocks, bps, S;
+  int tblk;           // paged blocks per tile of the kernel launched (balanced work counts)
   int role[3];        // tensor-map dims 1..3 hold (0 = slot, 1 = kv head, 2 = block)
   float scale_log2;   // softmax_scale * log2(e)
   uint64_t wait_ns;   // limit of each wait on another warp's signal
@@ -135,10 +151,11 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 // threads (288 for fp8 caches):
 //   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
 //              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
-//              and first writes that row of Q into TMEM
+//              and first writes that row of Q (into shared memory for bf16
+//              caches, into TMEM for fp8 ones)
 //   warps 4, 5 TMA producers (one lane each, in separate warps so that neither
 //              waits behind the other's barrier): warp 4 streams K tiles,
-//              warp 5 V tiles, each into its own shared-memory ring (a K
+//              warp 5 V stages, each into its own shared-memory ring (a K
 //              stage is free again as soon as its Q K^T has run, a V stage
 //              after its P V)
 //   warp 6     TMEM owner; lane 0 issues the MMAs from a polling loop, so
@@ -146,44 +163,56 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 //              It sits on the third scheduler (warp id % 4 = 2), away from
 //              the softmax warps that own rows 0-63.
 //   warp 7     idle (fp8 caches: widens K tiles to f16; warp 8 widens V)
-// A tile is kT5Blk paged blocks (N = 16 kT5Blk keys). Per tile t, with
+// A tile is Cfg::kBlk paged blocks (N = 16 kBlk keys). Per tile t, with
 // buffer u = t % kT5SBuf:
 //   S[u] = Q K^T           (M=128 padded query rows, N keys, K=128)
 //   P[u] = 2^(S c - m)      bf16, written over the first N/2 columns of S[u]
 //   O   += P V              (M=128, N=128 head dims, K=16 keys per MMA)
 // Each buffer has its own "P V done" barrier, so every wait is at most one
 // phase behind its barrier.
-// Q is the TMEM A operand of Q K^T (bf16 pairs along the head dim, one
-// query row per lane, written by the softmax warps). Shared-memory operands
-// use the 128-byte swizzle: K is K-major (head dim contiguous), V is MN-major
-// (head dim contiguous along N).
-constexpr int kT5Blk = 2;                      // blocks per tile
-constexpr int kT5N = 16 * kT5Blk;              // keys per tile
+// Shared-memory operands use the 128-byte swizzle: Q and K are K-major (head
+// dim contiguous), V is MN-major (head dim contiguous along N).
+constexpr int kT5Blk = 2;                      // blocks of a 32-key unit (V stages, fp8 tiles, work counts)
 constexpr int kT5SBuf = 2;                     // S / P buffers in TMEM
 constexpr int kT5MmaWarp = 6;
 constexpr int kT5MaxR = 128;
-constexpr int kT5HalfBytes = kT5Blk * 2048;    // one head-dim half of K (or V) for a tile
-constexpr int kT5TileBytes = 2 * kT5HalfBytes; // K (or V) of one tile
-// Q lives in TMEM (the A operand of Q K^T, like P for P V), so the rings take
-// all the shared memory two CTAs per SM leave. QR is the number of query rows
-// the softmax warps write (64 when R <= 64: rows 64-127 of S, P and O are
-// never used).
-// FP8: e4m3 caches. TMA lands each block's raw 16 x 128-byte tile in a ring
-// of its own; warps 7 (K) and 8 (V) widen them exactly to f16 (every e4m3
-// value is an f16 value) into a second ring laid out as the bf16 tiles are,
-// and the MMAs run on f16 operands (Q and P in f16 too).
+// bf16 caches: 64-key tiles. The tile loop's rate is set by the number of
+// Q K^T MMAs per key (an MMA of N = 64 keys costs about what one of N = 32
+// does), so a tile takes 64 keys; two 64-column S buffers and O then fill
+// the CTA's 256 TMEM columns and Q is the shared-memory A operand (QR rows:
+// for QR = 64 the MMA's rows 64-127 read the shared memory after Q, and
+// their rows of S, P and O are never used). K stages hold a tile, V streams
+// in 32-key stages, two per tile.
+// FP8: e4m3 caches, 32-key tiles. TMA lands each block's raw 16 x 128-byte
+// tile in a ring of its own; warps 7 (K) and 8 (V) widen them exactly to f16
+// (every e4m3 value is an f16 value) into a second ring laid out as the
+// 16-bit tiles are, and the MMAs run on f16 operands (Q, in TMEM, and P in
+// f16 too). Their rate is set by the widening.
+// The rings take what two CTAs per SM leave.
 template <int QR, bool FP8> struct T5Cfg {
-  static constexpr int kKS = 7;                                  // K stages (raw for FP8)
-  static constexpr int kVS = FP8 ? 7 : 6;                        // V stages
-  static constexpr int kCS = FP8 ? 3 : 0;                        // widened f16 stages, each of K and V
-  static constexpr int kRawBytes = FP8 ? kT5Blk * 2048 : kT5TileBytes;
+  static constexpr int kBlk = FP8 ? 2 : 4;                  // paged blocks per tile
+  static constexpr int kN = 16 * kBlk;                       // keys per tile
+  static constexpr int kVPT = kBlk / kT5Blk;                 // 32-key V stages per tile
+  static constexpr bool kQSmem = !FP8;                       // Q K^T reads A from shared memory
+  static constexpr int kQBytes = kQSmem ? QR * 256 : 0;      // two head-dim halves of QR rows
+  static constexpr int kKHalf = kBlk * 2048;                 // a head-dim half of a 16-bit K tile
+  static constexpr int kKTile = 2 * kKHalf;
+  static constexpr int kVHalf = kT5Blk * 2048;               // a head-dim half of a 16-bit V stage
+  static constexpr int kVTile = 2 * kVHalf;
+  static constexpr int kKS = FP8 ? 7 : 3;                    // K stages (raw for FP8)
+  static constexpr int kVS = FP8 ? 7 : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
+  static constexpr int kCS = FP8 ? 3 : 0;                    // widened f16 stages, each of K and V
+  static constexpr int kKRaw = FP8 ? kBlk * 2048 : kKTile;   // bytes of a K ring stage
+  static constexpr int kVRaw = FP8 ? kT5Blk * 2048 : kVTile; // bytes of a V ring stage
   static constexpr int kThreads = FP8 ? 288 : 256;
-  static constexpr int kSmem = 1024 + (kKS + kVS) * kRawBytes + 2 * kCS * kT5TileBytes;
+  static constexpr int kSmem = 1024 + kQBytes + kKS * kKRaw + kVS * kVRaw + kCS * (kKTile + kVTile);
+  static constexpr uint32_t kOCol = kT5SBuf * kN;             // O after the S buffers
+  static constexpr uint32_t kQCol = kOCol + 128;              // FP8: Q, 64 columns of f16 pairs
+  static_assert(kOCol + 128 + (kQSmem ? 0 : 64) <= 256, "TMEM budget");
+  static_assert(FP8 ? kVPT == 1 : kVPT == 2, "V stages per tile");
+  static_assert(!FP8 || (kKRaw == kVRaw && kKTile == kVTile && kKHalf == kVHalf), "fp8: K and V stages alike");
 };
-constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O, Q
-constexpr uint32_t kT5OCol = kT5SBuf * kT5N;
-constexpr uint32_t kT5QCol = kT5OCol + 128;    // Q: 64 columns of bf16 pairs (d 2c, 2c+1)
-static_assert(kT5QCol + 64 <= kT5Cols, "TMEM budget");
+constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O (and Q for fp8)
 
 __device__ __forceinline__ uint64_t t5_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -199,6 +228,13 @@ __device__ __forceinline__ void t5_mma_ts(uint32_t d, uint32_t a, uint64_t b, ui
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
                "r"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// A from shared memory (descriptor)
+__device__ __forceinline__ void t5_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void t5_commit(uint64_t *bar) {
@@ -250,8 +286,8 @@ __device__ __forceinline__ bool t5_wait(uint64_t *bar, uint32_t phase, volatile 
 }
 
 // The work items of a CTA of the balanced-mode kernel: blocks [blk0, blk1)
-// of kv head g of sequence b. The sequence of 32-key tiles of all sequences
-// in order is cut into NR equal ranges, and CTA c runs range c / H_kv for kv
+// of kv head g of sequence b. The sequence of tiles (P.tblk blocks each) of
+// all sequences in order is cut into NR equal ranges, and CTA c runs range c / H_kv for kv
 // head c % H_kv, so every CTA streams the same number of tiles; a range may
 // end inside one sequence and go on through whole sequences into the next. A
 // piece of a (b, g) pair that another CTA shares writes a partial: entry 2c
@@ -276,15 +312,15 @@ __device__ __forceinline__ bool t5_item(const TcParams &P, T5Walk &w, T5Item &it
   for (;;) {   // sequences with invalid lengths hold no tiles
     if (w.b >= P.B) return false;
     L = P.seq_lens[w.b];
-    nt = (L >= P.n_new && L <= P.max_blocks * kBS) ? ((L + kBS - 1) / kBS + kT5Blk - 1) / kT5Blk : 0;
+    nt = (L >= P.n_new && L <= P.max_blocks * kBS) ? ((L + kBS - 1) / kBS + P.tblk - 1) / P.tblk : 0;
     if (nt > 0) break;
     ++w.b;
   }
   const int take = min(nt - w.off, w.left);
   it.b = w.b; it.g = w.g; it.L = L;
   it.nblk = (L + kBS - 1) / kBS;
-  it.blk0 = w.off * kT5Blk;
-  it.blk1 = min(it.nblk, (w.off + take) * kT5Blk);
+  it.blk0 = w.off * P.tblk;
+  it.blk1 = min(it.nblk, (w.off + take) * P.tblk);
   it.whole = w.off == 0 && take == nt;
   it.ent = 2 * (int64_t)blockIdx.x + (w.idx > 0 ? 1 : 0);
   w.left -= take;
@@ -371,8 +407,9 @@ __global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *
 }
 
 // Balanced partition for the tcgen05 kernel: one CTA. The global tile
-// sequence holds, for every sequence b in order, the ceil(ceil(L_b / 16) / 2)
-// 32-key tiles of b (none for an invalid length, which it flags). It is cut
+// sequence holds, for every sequence b in order, the ceil(ceil(L_b / 16) /
+// tblk) tiles of b (tblk blocks each, the tile of the kernel launched after
+// it; none for an invalid length, which it flags). It is cut
 // into NR equal ranges, range r = [r T / NR, (r + 1) T / NR), and CTAs
 // r H_kv .. r H_kv + H_kv - 1 run range r for kv heads 0 .. H_kv - 1: the
 // CTAs reading the heads of one block run side by side, as the heads of a
@@ -385,8 +422,8 @@ __global__ void __launch_bounds__(kOrdThreads) attn_order_kernel(const int32_t *
 constexpr int kPartThreads = 1024;
 constexpr int kPartSmemB = 4096;   // prefixes kept in shared memory up to this batch
 __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *seq_lens, int B, int n_new,
-                                                                 int max_blocks, int NR, int4 *work, int32_t *seq_pre,
-                                                                 int4 *split, int32_t *status) {
+                                                                 int max_blocks, int tblk, int NR, int4 *work,
+                                                                 int32_t *seq_pre, int4 *split, int32_t *status) {
   pdl_trigger();
   __shared__ int s_pre[kPartSmemB + 1];
   __shared__ int s_warp[kPartThreads / 32];
@@ -399,7 +436,7 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *
     int v = 0;
     if (b < B) {
       const int L = seq_lens[b];
-      if (L >= n_new && L <= max_blocks * kBS) v = ((L + kBS - 1) / kBS + kT5Blk - 1) / kT5Blk;
+      if (L >= n_new && L <= max_blocks * kBS) v = ((L + kBS - 1) / kBS + tblk - 1) / tblk;
       else atomic_or_status(status, SV_DEV_BAD_SEQ_LEN);
     }
     int incl = v;
@@ -472,7 +509,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS, CS = Cfg::kCS > 0 ? Cfg::kCS : 1;
-  constexpr int RAW = Cfg::kRawBytes;
+  constexpr int TB = Cfg::kBlk, TN = Cfg::kN, VPT = Cfg::kVPT;
+  constexpr uint32_t OC = Cfg::kOCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   // FP8: widened stages, filled by the converter warps, freed by the MMAs
@@ -488,11 +526,12 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t k_ring = smem_u32(smem);
-  const uint32_t v_ring = k_ring + KS * RAW;
+  const uint32_t q_smem = smem_u32(smem);   // bf16: Q, the A operand of Q K^T
+  const uint32_t k_ring = q_smem + Cfg::kQBytes;
+  const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
   // the rings the MMAs read: the widened ones for FP8, else the TMA rings
-  const uint32_t kc_ring = FP8 ? v_ring + VS * RAW : k_ring;
-  const uint32_t vc_ring = FP8 ? kc_ring + CS * kT5TileBytes : v_ring;
+  const uint32_t kc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : k_ring;
+  const uint32_t vc_ring = FP8 ? kc_ring + CS * Cfg::kKTile : v_ring;
 
   const int L = P.seq_lens[b];
   if (L < P.n_new || L > P.max_blocks * kBS) {
@@ -504,7 +543,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   if (blk0 >= nblk) return;   // the merge never reads this split
   const int blk1 = min(nblk, blk0 + P.bps);
   const int nblocks = blk1 - blk0;
-  const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+  const int n_tiles = (nblocks + TB - 1) / TB;
   const int R = P.R;
 
   if (tid == 0) {
@@ -538,12 +577,17 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
 
   if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ producers --
-    // warp 4 streams K, warp 5 streams V
+    // warp 4 streams K tiles, warp 5 V stages (VPT of 32 keys per tile; a
+    // stage of a tile that ends before it completes with a plain arrival, so
+    // the ring's phases stay one per stage)
     {
       // the whole warp walks the block table 32 entries at a time (the next
       // 32 prefetched); lane 0 waits for free stages and issues the copies
       const bool isv = warp == 5;
       const int NS = isv ? VS : KS;
+      const int SB = isv ? kT5Blk : TB;                                // blocks per stage
+      const uint32_t sbytes = isv ? Cfg::kVRaw : Cfg::kKRaw;
+      const uint32_t half = isv ? Cfg::kVHalf : Cfg::kKHalf;           // 16-bit: second head-dim half
       uint64_t *fullb = isv ? v_full : k_full;
       uint64_t *emptyb = isv ? v_empty : k_empty;
       const uint32_t ring = isv ? v_ring : k_ring;
@@ -555,41 +599,45 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       int issued = 0;
       // (test hook: with the copies withheld every wait on them runs out,
       // with nothing in flight)
-      const int n_issue = (P.withhold & SV_TEST_WITHHOLD_COPIES) ? 0 : n_tiles;
-      for (int t = 0; t < n_issue; ++t) {
-        const int first = t * kT5Blk;
+      const int n_issue = (P.withhold & SV_TEST_WITHHOLD_COPIES) ? 0 : n_tiles * (isv ? VPT : 1);
+      for (int i = 0; i < n_issue; ++i) {
+        const int first = i * SB;   // stage i holds blocks first .. first + SB - 1
         if ((first >> 5) != chunk) {
           chunk = first >> 5;
           cur = nxt;
           const int rel = (chunk + 1) * 32 + lane;
           nxt = rel < nblocks ? table[rel] : 0;
         }
-        int phys[kT5Blk];
+        int phys[TB];
 #pragma unroll
-        for (int kk = 0; kk < kT5Blk; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
-        const int st = t % NS;
+        for (int kk = 0; kk < TB; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
+        const int st = i % NS;
         bool go = true;
         if (lane == 0) {
-          if (t >= NS && !t5_wait(&emptyb[st], ((t / NS) & 1) ^ 1, abf, P.wait_ns)) {
+          if (i >= NS && !t5_wait(&emptyb[st], ((i / NS) & 1) ^ 1, abf, P.wait_ns)) {
             go = false;
           } else {
-            const int nvalid = min(kT5Blk, nblocks - first);
-            // a block is 2 KB of e4m3 (one 128-byte box row per slot) or two
-            // 2 KB head-dim halves of bf16
-            mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * (FP8 ? 2048 : 2 * 2048)));
-            const uint32_t base = ring + st * RAW;
-            for (int kk = 0; kk < nvalid; ++kk) {
-              int ph = phys[kk];
-              if (ph < 0 || ph >= P.num_blocks) {
-                if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
-                ph = 0;   // stay in bounds; the output of this sequence is flagged
+            const int nvalid = max(0, min(SB, nblocks - first));
+            if (nvalid == 0) {
+              mbar_arrive(&fullb[st]);   // past the end of the split: nothing to copy
+            } else {
+              // a block is 2 KB of e4m3 (one 128-byte box row per slot) or two
+              // 2 KB head-dim halves of bf16
+              mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * (FP8 ? 2048 : 2 * 2048)));
+              const uint32_t base = ring + st * sbytes;
+              for (int kk = 0; kk < nvalid; ++kk) {
+                int ph = phys[kk];
+                if (ph < 0 || ph >= P.num_blocks) {
+                  if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+                  ph = 0;   // stay in bounds; the output of this sequence is flagged
+                }
+                int c[3];
+                tile_coords(P, g, ph, c);
+                tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
+                if (!FP8) tma_load_4d(base + half + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
               }
-              int c[3];
-              tile_coords(P, g, ph, c);
-              tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
-              if (!FP8) tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
             }
-            issued = t + 1;
+            issued = i + 1;
           }
         }
         if (!__shfl_sync(0xffffffffu, (int)go, 0)) break;
@@ -616,9 +664,9 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       if (lane == 0) {
         // f32 accumulators; A and B bf16 (formats 1), or f16 for FP8 (0)
         constexpr uint32_t ab = FP8 ? 0u : (1u << 7) | (1u << 10);
-        const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
+        const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(TN >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
-        static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
+        static_assert(TN % 16 == 0 && TN <= 256, "MMA N");
         int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
         bool q_ready = false;
         uint64_t t_last = global_ns();
@@ -634,12 +682,16 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
             const bool sfree = tq < kT5SBuf || t5_test(&o_done[sb], ((tq / kT5SBuf) - 1) & 1);
             if (sfree && t5_test(&kf[ks], (tq / KR) & 1)) {
               t5_fence_after();
-              const uint32_t kb = kc_ring + ks * kT5TileBytes;
+              const uint32_t kb = kc_ring + ks * Cfg::kKTile;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
-                t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
-                          t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
-                          kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk) {   // 16 head dims per step
+                const uint64_t bd = t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024);
+                if constexpr (Cfg::kQSmem)   // A = Q from shared memory
+                  t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024), bd,
+                            idesc_qk, kk > 0 ? 1u : 0u);
+                else   // A = Q from TMEM: 8 columns per step
+                  t5_mma_ts(tb + sb * TN, tb + Cfg::kQCol + 8 * kk, bd, idesc_qk, kk > 0 ? 1u : 0u);
+              }
               t5_commit(&s_full[sb]);
               t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
               ++tq;
@@ -647,17 +699,32 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
             }
           }
           if (tp < tq) {
+            // the tile's V stages: the TMA ring (bf16) or the widened ring (FP8)
             const int VR = FP8 ? CS : VS;
-            const int vs = tp % VR, sb = tp % kT5SBuf;
+            const int sb = tp % kT5SBuf;
             uint64_t *vf = FP8 ? vc_full : v_full;
-            if (t5_test(&p_full[sb], (tp / kT5SBuf) & 1) && t5_test(&vf[vs], (tp / VR) & 1)) {
-              t5_fence_after();
-              const uint32_t vb = vc_ring + vs * kT5TileBytes;
+            bool ready = t5_test(&p_full[sb], (tp / kT5SBuf) & 1);
 #pragma unroll
-              for (int j = 0; j < kT5Blk; ++j)
-                t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
-                          idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
-              t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
+            for (int h = 0; h < VPT; ++h) ready = ready && t5_test(&vf[(tp * VPT + h) % VR], ((tp * VPT + h) / VR) & 1);
+            if (ready) {
+              t5_fence_after();
+              // stages past the end of the split hold nothing to multiply
+              const int nvs = min(VPT, (min(TB, nblocks - tp * TB) + kT5Blk - 1) / kT5Blk);
+#pragma unroll
+              for (int h = 0; h < VPT; ++h) {
+                if (h < nvs) {
+                  const uint32_t vb = vc_ring + ((tp * VPT + h) % VR) * Cfg::kVTile;
+#pragma unroll
+                  for (int j = 0; j < kT5Blk; ++j)   // 16 keys per MMA
+                    t5_mma_ts(tb + OC, tb + sb * TN + 8 * (kT5Blk * h + j), t5_desc(vb + j * 2048, Cfg::kVHalf, 1024),
+                              idesc_pv, (tp > 0 || h > 0 || j > 0) ? 1u : 0u);
+                }
+              }
+#pragma unroll
+              for (int h = 0; h < VPT; ++h) {
+                const int vs = (tp * VPT + h) % VR;
+                t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
+              }
               t5_commit(&o_done[sb]);
               ++tp;
               progressed = true;
@@ -689,18 +756,33 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
       float sl2 = P.scale_log2;
       {
-        // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
-        // order). tcgen05.st is warp-collective: a warp holding live rows
-        // stores all 32 (zeros for rows past R); warps with none skip it
-        // (their rows of S, P and O are never read).
-        if (warp_live) {
-          const uint4 *src = nullptr;
-          if (live) {
-            const int j = row / P.G, hh = row % P.G;
-            src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
-                                                  (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
+        const uint4 *src = nullptr;
+        if (live) {
+          const int j = row / P.G, hh = row % P.G;
+          src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
+        }
+        if constexpr (Cfg::kQSmem) {
+          // this row of Q into shared memory: head-dim halves of QR rows of
+          // 128 bytes, the 16-byte chunks of row r at chunk index ^ (r % 8)
+          // (the 128-byte swizzle of the MMA operand); rows past R are zeros
+          if (row < QR) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+              const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
+            }
+            // the tensor cores read it through the async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           }
-          if constexpr (FP8) {
+        } else if (warp_live) {
+          // this row of Q into TMEM (columns kQCol.., f16 pairs in memory
+          // order). tcgen05.st is warp-collective: a warp holding live rows
+          // stores all 32 (zeros for rows past R); warps with none skip it
+          // (their rows of S, P and O are never read).
+          {
             // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
             // in [2^14, 2^15): the f16 range then holds the whole row with no
             // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
@@ -736,26 +818,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
                 w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
                 w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
               }
-              t5_st16(lane_base + kT5QCol + 16 * c0, w);
-            }
-          } else {
-            uint4 qv[16];
-            if (live) {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int c0 = 0; c0 < 4; ++c0) {
-              uint32_t w[16];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
-                w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
-              }
-              t5_st16(lane_base + kT5QCol + 16 * c0, w);
+              t5_st16(lane_base + Cfg::kQCol + 16 * c0, w);
             }
           }
           t5_wait_st();
@@ -767,37 +830,37 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
-        const int sb = t % kT5SBuf, vs = t % VS;
+        const int sb = t % kT5SBuf;
         ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (t / kT5SBuf) & 1, abf, P.wait_ns));
         if (!ok) break;
         t5_fence_after();
-        const int key0 = (blk0 + t * kT5Blk) * kBS;
+        const int key0 = (blk0 + t * TB) * kBS;
         if (warp_live) {
-          float x[kT5N];
+          float x[TN];
           {
-            uint32_t r[kT5N];
+            uint32_t r[TN];
 #pragma unroll
-            for (int c0 = 0; c0 < kT5N; c0 += 16)
-              t5_ld16(lane_base + sb * kT5N + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+            for (int c0 = 0; c0 < TN; c0 += 16)
+              t5_ld16(lane_base + sb * TN + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
             t5_wait_ld();
 #pragma unroll
-            for (int k = 0; k < kT5N; ++k) x[k] = __uint_as_float(r[k]) * sl2;
+            for (int k = 0; k < TN; ++k) x[k] = __uint_as_float(r[k]);   // unscaled scores
           }
-          if (key0 + kT5N > end_key || key0 + kT5N - 1 > L - P.n_new) {   // reaches the diagonal or the end
+          if (key0 + TN > end_key || key0 + TN - 1 > L - P.n_new) {   // reaches the diagonal or the end
 #pragma unroll
-            for (int k = 0; k < kT5N; ++k)
+            for (int k = 0; k < TN; ++k)
               if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
             if (P.anc) {   // draft tree: new keys off the row's ancestor path go too
 #pragma unroll
-              for (int k = 0; k < kT5N; ++k) {
+              for (int k = 0; k < TN; ++k) {
                 const int rel = key0 + k - (L - P.n_new);
                 if (rel >= 0 && !((anc >> (rel & 63)) & 1ull)) x[k] = -INFINITY;
               }
             }
           }
-          float mx = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
+          // maximum as a tree; the scale is positive, so scaling the maximum
+          // gives the maximum of the scaled scores (rounding is monotone)
+          float mx = t5_tile_max(x) * sl2;
           // rows past R hold whatever Q's unused rows produce: they must not
           // vote for a rescale of the warp
           if (!live) mx = -INFINITY;
@@ -816,46 +879,57 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
 #pragma unroll 1
             for (int c0 = 0; c0 < 128; c0 += 16) {
               uint32_t r[16];
-              t5_ld16(lane_base + kT5OCol + c0, r);
+              t5_ld16(lane_base + OC + c0, r);
               t5_wait_ld();
 #pragma unroll
               for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
-              t5_st16(lane_base + kT5OCol + c0, r);
+              t5_st16(lane_base + OC + c0, r);
             }
             t5_wait_st();
           }
           l *= a;
           const float base = m_ref == -INFINITY ? 0.f : m_ref;
-          float ps = 0.f;
+          // exponent arguments x c - base two at a time (packed fma), sums
+          // in four packed chains
+          const float2 c2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
+          float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int c0 = 0; c0 < kT5N; c0 += 32) {
+          for (int c0 = 0; c0 < TN; c0 += 32) {
             uint32_t w[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
-              ps += p0 + p1;
-              w[k] = pack2<FP8>(p0, p1);
+              const float2 y = __ffma2_rn(make_float2(x[c0 + 2 * k], x[c0 + 2 * k + 1]), c2, nb2);
+              const float2 pp = make_float2(ex2f(y.x), ex2f(y.y));
+              ps2[k & 1] = __fadd2_rn(ps2[k & 1], pp);
+              w[k] = pack2<FP8>(pp.x, pp.y);
             }
-            t5_st16(lane_base + sb * kT5N + c0 / 2, w);
+            t5_st16(lane_base + sb * TN + c0 / 2, w);
           }
           t5_wait_st();
-          l += ps;
+          const float2 pst = __fadd2_rn(ps2[0], ps2[1]);
+          l += pst.x + pst.y;
         }
-        if (!FP8 && key0 + kT5N > end_key && warp == 0) {
+        if (!FP8 && key0 + TN > end_key && warp == 0) {
           // keys past the split or the sequence (not loaded, or stale): V rows
-          // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
-          // (FP8: the converter writes those rows as zeros)
-          if (!t5_wait(&v_full[vs], (t / VS) & 1, abf, P.wait_ns)) ok = false;
-          const uint32_t vb = v_ring + vs * kT5TileBytes;
-          for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
-            const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
+          // zeroed, once the V stage holding them has landed, so that
+          // 0 * (anything) = 0 (stages wholly past the end are not multiplied;
+          // FP8: the converter writes those rows as zeros)
+          for (int h = 0; h < VPT; ++h) {
+            const int k0 = key0 + 16 * kT5Blk * h;   // first key of the stage
+            if (k0 >= end_key || k0 + 16 * kT5Blk <= end_key) continue;
+            const int vi = t * VPT + h;
+            if (!t5_wait(&v_full[vi % VS], (vi / VS) & 1, abf, P.wait_ns)) ok = false;
+            const uint32_t vb = v_ring + (vi % VS) * Cfg::kVRaw;
+            for (int k = end_key - k0 + lane; k < 16 * kT5Blk; k += 32) {
+              const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+              for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + h * kT5HalfBytes + off + c * 16),
-                             "r"(0u)
-                             : "memory");
+                for (int c = 0; c < 8; ++c)
+                  asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + hh * Cfg::kVHalf + off + c * 16),
+                               "r"(0u)
+                               : "memory");
+            }
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
@@ -885,7 +959,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
         for (int c0 = 0; c0 < 128; c0 += 64) {
           uint32_t r[64];
 #pragma unroll
-          for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + kT5OCol + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+          for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + OC + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
           t5_wait_ld();
           if (live) {
             if (nsplit == 1) {
@@ -915,7 +989,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   }
   if (FP8 && (warp == 7 || warp == 8)) {
     // ----------------------------------------------------- e4m3 -> f16 ---
-    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is kT5Blk blocks of
+    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is TB blocks of
     // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
     // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
     // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
@@ -934,8 +1008,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf, P.wait_ns));
       if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf, P.wait_ns));
       if (!ok) break;
-      const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
-      const int key0 = (blk0 + t * kT5Blk) * kBS;
+      const uint32_t src = rring + rs * Cfg::kKRaw, dst = cring + cs * Cfg::kKTile;   // K and V alike for FP8
+      const int key0 = (blk0 + t * TB) * kBS;
 #pragma unroll 2
       for (int j = 0; j < 8; ++j) {
         const int q = lane + 32 * j;
@@ -956,7 +1030,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
 #pragma unroll
           for (int k = 0; k < 8; ++k) h[k] = 0u;
         }
-        const uint32_t rowb = dst + (ch >> 2) * kT5HalfBytes + blk * 2048 + r16 * 128;
+        const uint32_t rowb = dst + (ch >> 2) * Cfg::kKHalf + blk * 2048 + r16 * 128;
         const int c8 = 2 * (ch & 3);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
                      "r"(h[1]), "r"(h[2]), "r"(h[3])
@@ -994,7 +1068,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS, CS = Cfg::kCS > 0 ? Cfg::kCS : 1;
-  constexpr int RAW = Cfg::kRawBytes;
+  constexpr int TB = Cfg::kBlk, TN = Cfg::kN, VPT = Cfg::kVPT;
+  constexpr uint32_t OC = Cfg::kOCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   // FP8: widened stages, filled by the converter warps, freed by the MMAs
@@ -1011,11 +1086,12 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
     if (!t5_item(P, w0, it0)) return;
   }
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t k_ring = smem_u32(smem);
-  const uint32_t v_ring = k_ring + KS * RAW;
+  const uint32_t q_smem = smem_u32(smem);   // bf16: Q, the A operand of Q K^T
+  const uint32_t k_ring = q_smem + Cfg::kQBytes;
+  const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
   // the rings the MMAs read: the widened ones for FP8, else the TMA rings
-  const uint32_t kc_ring = FP8 ? v_ring + VS * RAW : k_ring;
-  const uint32_t vc_ring = FP8 ? kc_ring + CS * kT5TileBytes : v_ring;
+  const uint32_t kc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : k_ring;
+  const uint32_t vc_ring = FP8 ? kc_ring + CS * Cfg::kKTile : v_ring;
   const int R = P.R;
 
   if (tid == 0) {
@@ -1052,62 +1128,71 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
 
   if (warp == 4 || warp == 5) {
     // ------------------------------------------------------------ producers --
-    // warp 4 streams K, warp 5 streams V; the whole warp walks the block
-    // table 32 entries at a time (the next 32 prefetched); lane 0 waits for
-    // free stages and issues the copies
+    // warp 4 streams K tiles, warp 5 V stages (VPT of 32 keys per tile; a
+    // stage of a tile that ends before it completes with a plain arrival);
+    // the whole warp walks the block table 32 entries at a time (the next 32
+    // prefetched); lane 0 waits for free stages and issues the copies
     const bool isv = warp == 5;
     const int NS = isv ? VS : KS;
+    const int SPT = isv ? VPT : 1;                                   // stages per tile
+    const int SB = isv ? kT5Blk : TB;                                // blocks per stage
+    const uint32_t sbytes = isv ? Cfg::kVRaw : Cfg::kKRaw;
+    const uint32_t half = isv ? Cfg::kVHalf : Cfg::kKHalf;           // 16-bit: second head-dim half
     uint64_t *fullb = isv ? v_full : k_full;
     uint64_t *emptyb = isv ? v_empty : k_empty;
     const uint32_t ring = isv ? v_ring : k_ring;
     const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
     T5Walk wk = {};
     T5Item it;
-    int u = 0, issued = 0;
+    int i = 0, issued = 0;   // the CTA's running stage count
     bool go = true;
     // (test hook: with the copies withheld every wait on them runs out,
     // with nothing in flight)
     const bool withhold = (P.withhold & SV_TEST_WITHHOLD_COPIES) != 0;
     while (go && !withhold && t5_item(P, wk, it)) {
       const int nblocks = it.blk1 - it.blk0;
-      const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+      const int n_st = (nblocks + TB - 1) / TB * SPT;
       const int32_t *table = P.block_table + (int64_t)it.b * P.max_blocks + it.blk0;
       int cur = lane < nblocks ? table[lane] : 0;
       int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
       int chunk = 0;
-      for (int t = 0; t < n_tiles; ++t, ++u) {
-        const int first = t * kT5Blk;
+      for (int q = 0; q < n_st; ++q, ++i) {
+        const int first = q * SB;   // the item's stage q holds blocks first .. first + SB - 1
         if ((first >> 5) != chunk) {
           chunk = first >> 5;
           cur = nxt;
           const int rel = (chunk + 1) * 32 + lane;
           nxt = rel < nblocks ? table[rel] : 0;
         }
-        int phys[kT5Blk];
+        int phys[TB];
 #pragma unroll
-        for (int kk = 0; kk < kT5Blk; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
-        const int st = u % NS;
+        for (int kk = 0; kk < TB; ++kk) phys[kk] = __shfl_sync(0xffffffffu, cur, (first + kk) & 31);
+        const int st = i % NS;
         if (lane == 0) {
-          if (u >= NS && !t5_wait(&emptyb[st], ((u / NS) & 1) ^ 1, abf, P.wait_ns)) {
+          if (i >= NS && !t5_wait(&emptyb[st], ((i / NS) & 1) ^ 1, abf, P.wait_ns)) {
             go = false;
           } else {
-            const int nvalid = min(kT5Blk, nblocks - first);
-            // a block is 2 KB of e4m3 (one 128-byte box row per slot) or two
-            // 2 KB head-dim halves of bf16
-            mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * (FP8 ? 2048 : 2 * 2048)));
-            const uint32_t base = ring + st * RAW;
-            for (int kk = 0; kk < nvalid; ++kk) {
-              int ph = phys[kk];
-              if (ph < 0 || ph >= P.num_blocks) {
-                if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
-                ph = 0;   // stay in bounds; the output of this sequence is flagged
+            const int nvalid = max(0, min(SB, nblocks - first));
+            if (nvalid == 0) {
+              mbar_arrive(&fullb[st]);   // past the end of the item: nothing to copy
+            } else {
+              // a block is 2 KB of e4m3 (one 128-byte box row per slot) or two
+              // 2 KB head-dim halves of bf16
+              mbar_arrive_expect_tx(&fullb[st], (uint32_t)(nvalid * (FP8 ? 2048 : 2 * 2048)));
+              const uint32_t base = ring + st * sbytes;
+              for (int kk = 0; kk < nvalid; ++kk) {
+                int ph = phys[kk];
+                if (ph < 0 || ph >= P.num_blocks) {
+                  if (!isv) atomic_or_status(P.status, SV_DEV_BAD_BLOCK);
+                  ph = 0;   // stay in bounds; the output of this sequence is flagged
+                }
+                int c[3];
+                tile_coords(P, it.g, ph, c);
+                tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
+                if (!FP8) tma_load_4d(base + half + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
               }
-              int c[3];
-              tile_coords(P, it.g, ph, c);
-              tma_load_4d(base + kk * 2048, map, 0, c[0], c[1], c[2], &fullb[st]);
-              if (!FP8) tma_load_4d(base + kT5HalfBytes + kk * 2048, map, 64, c[0], c[1], c[2], &fullb[st]);
             }
-            issued = u + 1;
+            issued = i + 1;
           }
         }
         go = __shfl_sync(0xffffffffu, (int)go, 0) != 0;
@@ -1135,9 +1220,9 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
       if (lane == 0) {
         // f32 accumulators; A and B bf16 (formats 1), or f16 for FP8 (0)
         constexpr uint32_t ab = FP8 ? 0u : (1u << 7) | (1u << 10);
-        const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(kT5N >> 3) << 17) | (8u << 24);
+        const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(TN >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
-        static_assert(kT5N % 16 == 0 && kT5N <= 256, "MMA N");
+        static_assert(TN % 16 == 0 && TN <= 256, "MMA N");
         // the items in order, each with the split kernel's loop; u0 is the
         // CTA's running tile count at the item's start. The next item's
         // Q K^T could not start earlier anyway: its Q is written after this
@@ -1147,7 +1232,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
         int u0 = 0, xq = 0;
         bool okm = true;
         while (okm && t5_item(P, wk, it)) {
-          const int n_tiles = (it.blk1 - it.blk0 + kT5Blk - 1) / kT5Blk;
+          const int nblocks = it.blk1 - it.blk0;
+          const int n_tiles = (nblocks + TB - 1) / TB;
           int tq = 0, tp = 0;   // next tiles for Q K^T and for P V
           bool q_ready = false;
           uint64_t t_last = global_ns();
@@ -1164,12 +1250,16 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
               const bool sfree = uq < kT5SBuf || t5_test(&o_done[sb], ((uq / kT5SBuf) - 1) & 1);
               if (sfree && t5_test(&kf[ks], (uq / KR) & 1)) {
                 t5_fence_after();
-                const uint32_t kb = kc_ring + ks * kT5TileBytes;
+                const uint32_t kb = kc_ring + ks * Cfg::kKTile;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)   // A = Q from TMEM: 16 head dims = 8 columns per step
-                  t5_mma_ts(tb + sb * kT5N, tb + kT5QCol + 8 * kk,
-                            t5_desc(kb + (kk >> 2) * kT5HalfBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
-                            kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {   // 16 head dims per step
+                  const uint64_t bd = t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024);
+                  if constexpr (Cfg::kQSmem)   // A = Q from shared memory
+                    t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024), bd,
+                              idesc_qk, kk > 0 ? 1u : 0u);
+                  else   // A = Q from TMEM: 8 columns per step
+                    t5_mma_ts(tb + sb * TN, tb + Cfg::kQCol + 8 * kk, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                }
                 t5_commit(&s_full[sb]);
                 t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
                 ++tq;
@@ -1177,18 +1267,34 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
               }
             }
             if (tp < tq) {
+              // the tile's V stages: the TMA ring (bf16) or the widened ring (FP8)
               const int VR = FP8 ? CS : VS;
               const int up = u0 + tp;
-              const int vs = up % VR, sb = up % kT5SBuf;
+              const int sb = up % kT5SBuf;
               uint64_t *vf = FP8 ? vc_full : v_full;
-              if (t5_test(&p_full[sb], (up / kT5SBuf) & 1) && t5_test(&vf[vs], (up / VR) & 1)) {
-                t5_fence_after();
-                const uint32_t vb = vc_ring + vs * kT5TileBytes;
+              bool ready = t5_test(&p_full[sb], (up / kT5SBuf) & 1);
 #pragma unroll
-                for (int j = 0; j < kT5Blk; ++j)   // an item's first P V starts O afresh
-                  t5_mma_ts(tb + kT5OCol, tb + sb * kT5N + 8 * j, t5_desc(vb + j * 2048, kT5HalfBytes, 1024),
-                            idesc_pv, (tp > 0 || j > 0) ? 1u : 0u);
-                t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
+              for (int h = 0; h < VPT; ++h) ready = ready && t5_test(&vf[(up * VPT + h) % VR], ((up * VPT + h) / VR) & 1);
+              if (ready) {
+                t5_fence_after();
+                // stages past the end of the item hold nothing to multiply
+                const int nvs = min(VPT, (min(TB, nblocks - tp * TB) + kT5Blk - 1) / kT5Blk);
+#pragma unroll
+                for (int h = 0; h < VPT; ++h) {
+                  if (h < nvs) {
+                    const uint32_t vb = vc_ring + ((up * VPT + h) % VR) * Cfg::kVTile;
+#pragma unroll
+                    for (int j = 0; j < kT5Blk; ++j)   // an item's first P V starts O afresh
+                      t5_mma_ts(tb + OC, tb + sb * TN + 8 * (kT5Blk * h + j),
+                                t5_desc(vb + j * 2048, Cfg::kVHalf, 1024), idesc_pv,
+                                (tp > 0 || h > 0 || j > 0) ? 1u : 0u);
+                  }
+                }
+#pragma unroll
+                for (int h = 0; h < VPT; ++h) {
+                  const int vs = (up * VPT + h) % VR;
+                  t5_commit(FP8 ? &vc_empty[vs] : &v_empty[vs]);
+                }
                 t5_commit(&o_done[sb]);
                 ++tp;
                 progressed = true;
@@ -1225,26 +1331,43 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
       while (ok && t5_item(P, wk, it)) {
         const int b = it.b, g = it.g, L = it.L;
         const int nblocks = it.blk1 - it.blk0;
-        const int n_tiles = (nblocks + kT5Blk - 1) / kT5Blk;
+        const int n_tiles = (nblocks + TB - 1) / TB;
         const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
         // draft tree: of the new keys, only the row's ancestors are visible
         const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
         const int end_key = min(L, it.blk1 * kBS);             // first key this item does not own
         float sl2 = P.scale_log2;
         {
-          // this row of Q into TMEM (columns kT5QCol.., bf16 pairs in memory
-          // order). tcgen05.st is warp-collective: a warp holding live rows
-          // stores all 32 (zeros for rows past R); warps with none skip it
-          // (their rows of S, P and O are never read). The previous item's
-          // Q K^T have all run: its epilogue waited for its last P V.
-          if (warp_live) {
-            const uint4 *src = nullptr;
-            if (live) {
-              const int j = row / P.G, hh = row % P.G;
-              src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
-                                                    (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
+          // The previous item's Q K^T have all run: its epilogue waited for
+          // its last P V.
+          const uint4 *src = nullptr;
+          if (live) {
+            const int j = row / P.G, hh = row % P.G;
+            src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                                  (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
+          }
+          if constexpr (Cfg::kQSmem) {
+            // this row of Q into shared memory: head-dim halves of QR rows of
+            // 128 bytes, the 16-byte chunks of row r at chunk index ^ (r % 8)
+            // (the 128-byte swizzle of the MMA operand); rows past R are zeros
+            if (row < QR) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z),
+                             "r"(v.w)
+                             : "memory");
+              }
+              // the tensor cores read it through the async proxy
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            if constexpr (FP8) {
+          } else if (warp_live) {
+            // this row of Q into TMEM (columns kQCol.., f16 pairs in memory
+            // order). tcgen05.st is warp-collective: a warp holding live rows
+            // stores all 32 (zeros for rows past R); warps with none skip it
+            // (their rows of S, P and O are never read).
+            {
               // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
               // in [2^14, 2^15): the f16 range then holds the whole row with no
               // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
@@ -1280,26 +1403,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
                   w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
                   w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
                 }
-                t5_st16(lane_base + kT5QCol + 16 * c0, w);
-              }
-            } else {
-              uint4 qv[16];
-              if (live) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
-              } else {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
-              }
-#pragma unroll
-              for (int c0 = 0; c0 < 4; ++c0) {
-                uint32_t w[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  w[4 * k] = qv[4 * c0 + k].x; w[4 * k + 1] = qv[4 * c0 + k].y;
-                  w[4 * k + 2] = qv[4 * c0 + k].z; w[4 * k + 3] = qv[4 * c0 + k].w;
-                }
-                t5_st16(lane_base + kT5QCol + 16 * c0, w);
+                t5_st16(lane_base + Cfg::kQCol + 16 * c0, w);
               }
             }
             t5_wait_st();
@@ -1310,37 +1414,35 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
         }
         float m_ref = -INFINITY, l = 0.f;
         for (int t = 0; t < n_tiles && ok; ++t, ++u) {
-          const int sb = u % kT5SBuf, vs = u % VS;
+          const int sb = u % kT5SBuf;
           ok = __all_sync(0xffffffffu, t5_wait(&s_full[sb], (u / kT5SBuf) & 1, abf, P.wait_ns));
           if (!ok) break;
           t5_fence_after();
-          const int key0 = (it.blk0 + t * kT5Blk) * kBS;
+          const int key0 = (it.blk0 + t * TB) * kBS;
           if (warp_live) {
-            float x[kT5N];
+            float x[TN];
             {
-              uint32_t r[kT5N];
+              uint32_t r[TN];
 #pragma unroll
-              for (int c0 = 0; c0 < kT5N; c0 += 16)
-                t5_ld16(lane_base + sb * kT5N + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+              for (int c0 = 0; c0 < TN; c0 += 16)
+                t5_ld16(lane_base + sb * TN + c0, *reinterpret_cast<uint32_t(*)[16]>(r + c0));
               t5_wait_ld();
 #pragma unroll
-              for (int k = 0; k < kT5N; ++k) x[k] = __uint_as_float(r[k]) * sl2;
+              for (int k = 0; k < TN; ++k) x[k] = __uint_as_float(r[k]);   // unscaled scores
             }
-            if (key0 + kT5N > end_key || key0 + kT5N - 1 > L - P.n_new) {   // reaches the diagonal or the end
+            if (key0 + TN > end_key || key0 + TN - 1 > L - P.n_new) {   // reaches the diagonal or the end
 #pragma unroll
-              for (int k = 0; k < kT5N; ++k)
+              for (int k = 0; k < TN; ++k)
                 if (key0 + k > lim || key0 + k >= end_key) x[k] = -INFINITY;
               if (P.anc) {   // draft tree: new keys off the row's ancestor path go too
 #pragma unroll
-                for (int k = 0; k < kT5N; ++k) {
+                for (int k = 0; k < TN; ++k) {
                   const int rel = key0 + k - (L - P.n_new);
                   if (rel >= 0 && !((anc >> (rel & 63)) & 1ull)) x[k] = -INFINITY;
                 }
               }
             }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < kT5N; ++k) mx = fmaxf(mx, x[k]);
+            float mx = t5_tile_max(x) * sl2;   // the scale is positive
             // rows past R hold whatever Q's unused rows produce: they must not
             // vote for a rescale of the warp
             if (!live) mx = -INFINITY;
@@ -1359,46 +1461,55 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
 #pragma unroll 1
               for (int c0 = 0; c0 < 128; c0 += 16) {
                 uint32_t r[16];
-                t5_ld16(lane_base + kT5OCol + c0, r);
+                t5_ld16(lane_base + OC + c0, r);
                 t5_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * a);
-                t5_st16(lane_base + kT5OCol + c0, r);
+                t5_st16(lane_base + OC + c0, r);
               }
               t5_wait_st();
             }
             l *= a;
             const float base = m_ref == -INFINITY ? 0.f : m_ref;
-            float ps = 0.f;
+            const float2 c2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
+            float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int c0 = 0; c0 < kT5N; c0 += 32) {
+            for (int c0 = 0; c0 < TN; c0 += 32) {
               uint32_t w[16];
 #pragma unroll
               for (int k = 0; k < 16; ++k) {
-                const float p0 = ex2f(x[c0 + 2 * k] - base), p1 = ex2f(x[c0 + 2 * k + 1] - base);
-                ps += p0 + p1;
-                w[k] = pack2<FP8>(p0, p1);
+                const float2 y = __ffma2_rn(make_float2(x[c0 + 2 * k], x[c0 + 2 * k + 1]), c2, nb2);
+                const float2 pp = make_float2(ex2f(y.x), ex2f(y.y));
+                ps2[k & 1] = __fadd2_rn(ps2[k & 1], pp);
+                w[k] = pack2<FP8>(pp.x, pp.y);
               }
-              t5_st16(lane_base + sb * kT5N + c0 / 2, w);
+              t5_st16(lane_base + sb * TN + c0 / 2, w);
             }
             t5_wait_st();
-            l += ps;
+            const float2 pst = __fadd2_rn(ps2[0], ps2[1]);
+            l += pst.x + pst.y;
           }
-          if (!FP8 && key0 + kT5N > end_key && warp == 0) {
+          if (!FP8 && key0 + TN > end_key && warp == 0) {
             // keys past the item or the sequence (not loaded, or stale): V rows
-            // zeroed, once this tile's V copy has landed, so 0 * (anything) = 0
-            // (FP8: the converter writes those rows as zeros)
-            if (!t5_wait(&v_full[vs], (u / VS) & 1, abf, P.wait_ns)) ok = false;
-            const uint32_t vb = v_ring + vs * kT5TileBytes;
-            for (int k = max(0, end_key - key0) + lane; k < kT5N; k += 32) {
-              const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
+            // zeroed, once the V stage holding them has landed, so that
+            // 0 * (anything) = 0 (stages wholly past the end are not
+            // multiplied; FP8: the converter writes those rows as zeros)
+            for (int h = 0; h < VPT; ++h) {
+              const int k0 = key0 + 16 * kT5Blk * h;   // first key of the stage
+              if (k0 >= end_key || k0 + 16 * kT5Blk <= end_key) continue;
+              const int vi = u * VPT + h;
+              if (!t5_wait(&v_full[vi % VS], (vi / VS) & 1, abf, P.wait_ns)) ok = false;
+              const uint32_t vb = v_ring + (vi % VS) * Cfg::kVRaw;
+              for (int k = end_key - k0 + lane; k < 16 * kT5Blk; k += 32) {
+                const uint32_t off = (uint32_t)((k >> 4) * 2048 + (k & 15) * 128);
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
+                for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + h * kT5HalfBytes + off + c * 16),
-                               "r"(0u)
-                               : "memory");
+                  for (int c = 0; c < 8; ++c)
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vb + hh * Cfg::kVHalf + off + c * 16),
+                                 "r"(0u)
+                                 : "memory");
+              }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           }
@@ -1431,7 +1542,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
           for (int c0 = 0; c0 < 128; c0 += 64) {
             uint32_t r[64];
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + kT5OCol + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+            for (int c = 0; c < 64; c += 16) t5_ld16(lane_base + OC + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
             t5_wait_ld();
             if (live) {
               if (it.whole) {
@@ -1464,7 +1575,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
   }
   if (FP8 && (warp == 7 || warp == 8)) {
     // ----------------------------------------------------- e4m3 -> f16 ---
-    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is kT5Blk blocks of
+    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is TB blocks of
     // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
     // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
     // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
@@ -1483,14 +1594,14 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
     bool ok = true;
     while (ok && t5_item(P, wk, it)) {
       const int end_key = min(it.L, it.blk1 * kBS);
-      const int n_tiles = (it.blk1 - it.blk0 + kT5Blk - 1) / kT5Blk;
+      const int n_tiles = (it.blk1 - it.blk0 + TB - 1) / TB;
       for (int t = 0; t < n_tiles; ++t, ++u) {
         const int rs = u % NS, cs = u % CS;
         ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (u / NS) & 1, abf, P.wait_ns));
         if (ok && u >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((u / CS) - 1) & 1, abf, P.wait_ns));
         if (!ok) break;
-        const uint32_t src = rring + rs * RAW, dst = cring + cs * kT5TileBytes;
-        const int key0 = (it.blk0 + t * kT5Blk) * kBS;
+        const uint32_t src = rring + rs * Cfg::kKRaw, dst = cring + cs * Cfg::kKTile;   // K and V alike for FP8
+        const int key0 = (it.blk0 + t * TB) * kBS;
 #pragma unroll 2
         for (int j = 0; j < 8; ++j) {
           const int q = lane + 32 * j;
@@ -1511,7 +1622,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
 #pragma unroll
             for (int k = 0; k < 8; ++k) h[k] = 0u;
           }
-          const uint32_t rowb = dst + (ch >> 2) * kT5HalfBytes + blk * 2048 + r16 * 128;
+          const uint32_t rowb = dst + (ch >> 2) * Cfg::kKHalf + blk * 2048 + r16 * 128;
           const int c8 = 2 * (ch & 3);
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
                        "r"(h[1]), "r"(h[2]), "r"(h[3])
@@ -2096,15 +2207,15 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
     // head) pairs as CTA slots (two per SM), one split per pair up to 512
     // blocks: the longest-first order balances the slots and no merge runs.
     // With fewer pairs, floor(slots / pairs) splits per pair, so the CTAs of
-    // equal-length sequences fill the slots once (an even block count keeps
-    // the 32-key tiles whole).
+    // equal-length sequences fill the slots once (a block count that is a
+    // multiple of 4 keeps the 64-key and 32-key tiles whole).
     if (pairs >= slots) {
       p.bps = std::min(max_blocks, 512);
     } else {
       const int64_t per = std::max<int64_t>(1, slots / std::max<int64_t>(1, pairs));
       int bps = (int)((max_blocks + per - 1) / per);
-      bps = std::min(512, (bps + kT5Blk - 1) / kT5Blk * kT5Blk);
-      p.bps = std::max(kT5Blk, bps);
+      bps = std::min(512, (bps + 3) / 4 * 4);
+      p.bps = std::max(4, bps);
     }
   } else {
     // fp32 caches are planned like bf16 ones so every dtype fits the same
@@ -2164,8 +2275,10 @@ __global__ void __launch_bounds__(64) attn_tree_kernel(const int32_t *parent, in
 }
 
 template <int QR, bool FP8>
-sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
+sv_status launch_tc5(const TcParams &P0, cudaStream_t st) {
   using Cfg = T5Cfg<QR, FP8>;
+  TcParams P = P0;
+  P.tblk = Cfg::kBlk;   // the partition counts this kernel's tiles
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -2179,7 +2292,7 @@ sv_status launch_tc5(const TcParams &P, cudaStream_t st) {
   unsigned grid;
   if (P.balanced) {
     launch_k(attn_part_kernel, dim3(1), dim3(kPartThreads), 0, st, 1, P.seq_lens, P.B, P.n_new, P.max_blocks,
-             P.ncta / P.H_kv, const_cast<int4 *>(P.work), P.seq_pre_w, P.split_w, P.status);
+             P.tblk, P.ncta / P.H_kv, const_cast<int4 *>(P.work), P.seq_pre_w, P.split_w, P.status);
     grid = (unsigned)P.ncta;
   } else {
     launch_k(attn_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, 1, P.seq_lens, P.B, P.S, P.H_kv, P.bps, P.n_new,
