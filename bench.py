@@ -652,7 +652,9 @@ def measure_next_rows(sv, cfg, a, s, dev, stream, status, reps=20):
                                      "bytes": tsamp_bytes}},
         "top_p": {"top_p": 0.9, "draft_top_p": True, "sample_topp_us": samp_us,
                   "filter_us": filt_us, "filter_rows": rows.shape[0],
-                  "roofline": {"bound": "hbm", "kernel": "topp_row_kernel", "achieved": filt_bytes / (filt_us * 1e-6) / 1e9,
+                  "roofline": {"bound": "hbm",
+                               "kernel": "topp_bin_kernel" if rows.shape[1] <= 188000 else "topp_row_kernel",
+                               "achieved": filt_bytes / (filt_us * 1e-6) / 1e9,
                                "peak": peak, "unit": "GB/s",
                                "frac": filt_bytes / (filt_us * 1e-6) / 1e9 / peak, "bytes": filt_bytes}},
         "cow_copy": {"pairs": len(pages), "pools": 2, "page_bytes": page_bytes, "us": cow_us,
