@@ -176,43 +176,45 @@ constexpr int kT5Blk = 2;                      // blocks of a 32-key unit (V sta
 constexpr int kT5SBuf = 2;                     // S / P buffers in TMEM
 constexpr int kT5MmaWarp = 6;
 constexpr int kT5MaxR = 128;
-// bf16 caches: 64-key tiles. The tile loop's rate is set by the number of
-// Q K^T MMAs per key (an MMA of N = 64 keys costs about what one of N = 32
-// does), so a tile takes 64 keys; two 64-column S buffers and O then fill
-// the CTA's 256 TMEM columns and Q is the shared-memory A operand (QR rows:
-// for QR = 64 the MMA's rows 64-127 read the shared memory after Q, and
-// their rows of S, P and O are never used). K stages hold a tile, V streams
-// in 32-key stages, two per tile.
-// FP8: e4m3 caches, 32-key tiles. TMA lands each block's raw 16 x 128-byte
-// tile in a ring of its own; warps 7 (K) and 8 (V) widen them exactly to f16
-// (every e4m3 value is an f16 value) into a second ring laid out as the
-// 16-bit tiles are, and the MMAs run on f16 operands (Q, in TMEM, and P in
-// f16 too). Their rate is set by the widening.
+// Tiles of 64 keys. The tile loop's rate is set by the number of Q K^T
+// MMAs per key (an MMA of N = 64 keys costs about what one of N = 32 does),
+// so a tile takes 64 keys; two 64-column S buffers and O then fill the CTA's
+// 256 TMEM columns and Q is the shared-memory A operand (QR rows: for QR = 64
+// the MMA's rows 64-127 read the shared memory after Q, and their rows of S,
+// P and O are never used). K stages hold a tile, V streams in 32-key stages,
+// two per tile.
+// FP8: e4m3 caches. TMA lands the raw 16 x 128-byte tile of each block in
+// rings of their own; converter warps widen them exactly to f16 (every e4m3
+// value is an f16 value) into second rings laid out as the 16-bit tiles are,
+// and the MMAs run on f16 operands (Q and P in f16 too). K and V each have
+// two converter warps when the group has at most 64 query rows (softmax
+// warps 2 and 3 have no rows then and widen instead), else one.
 // The rings take what two CTAs per SM leave.
 template <int QR, bool FP8> struct T5Cfg {
-  static constexpr int kBlk = FP8 ? 2 : 4;                  // paged blocks per tile
+  static constexpr int kBlk = 4;                             // paged blocks per tile
   static constexpr int kN = 16 * kBlk;                       // keys per tile
   static constexpr int kVPT = kBlk / kT5Blk;                 // 32-key V stages per tile
-  static constexpr bool kQSmem = !FP8;                       // Q K^T reads A from shared memory
-  static constexpr int kQBytes = kQSmem ? QR * 256 : 0;      // two head-dim halves of QR rows
+  static constexpr int kQBytes = QR * 256;                   // two head-dim halves of QR rows
   static constexpr int kKHalf = kBlk * 2048;                 // a head-dim half of a 16-bit K tile
   static constexpr int kKTile = 2 * kKHalf;
   static constexpr int kVHalf = kT5Blk * 2048;               // a head-dim half of a 16-bit V stage
   static constexpr int kVTile = 2 * kVHalf;
-  static constexpr int kKS = FP8 ? 7 : 3;                    // K stages (raw for FP8)
-  static constexpr int kVS = FP8 ? 7 : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
-  static constexpr int kCS = FP8 ? 3 : 0;                    // widened f16 stages, each of K and V
+  static constexpr int kKS = FP8 ? 2 : 3;                    // K stages (raw for FP8)
+  static constexpr int kVS = FP8 ? (QR == 64 ? 4 : 2) : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
+  static constexpr int kCKS = FP8 ? 2 : 0;                   // widened K stages
+  static constexpr int kCVS = FP8 ? (QR == 64 ? 3 : 2) : 0;  // widened V stages
+  static constexpr int kConvW = FP8 ? (QR == 64 ? 2 : 1) : 0;   // converter warps each of K and V
+  static constexpr int kSoftW = 4 - (kConvW == 2 ? 2 : 0);   // warps in the softmax role
   static constexpr int kKRaw = FP8 ? kBlk * 2048 : kKTile;   // bytes of a K ring stage
   static constexpr int kVRaw = FP8 ? kT5Blk * 2048 : kVTile; // bytes of a V ring stage
   static constexpr int kThreads = FP8 ? 288 : 256;
-  static constexpr int kSmem = 1024 + kQBytes + kKS * kKRaw + kVS * kVRaw + kCS * (kKTile + kVTile);
+  static constexpr int kSmem = 1024 + kQBytes + kKS * kKRaw + kVS * kVRaw + kCKS * kKTile + kCVS * kVTile;
   static constexpr uint32_t kOCol = kT5SBuf * kN;             // O after the S buffers
-  static constexpr uint32_t kQCol = kOCol + 128;              // FP8: Q, 64 columns of f16 pairs
-  static_assert(kOCol + 128 + (kQSmem ? 0 : 64) <= 256, "TMEM budget");
-  static_assert(FP8 ? kVPT == 1 : kVPT == 2, "V stages per tile");
-  static_assert(!FP8 || (kKRaw == kVRaw && kKTile == kVTile && kKHalf == kVHalf), "fp8: K and V stages alike");
+  static_assert(kOCol + 128 <= 256, "TMEM budget");
+  static_assert(kVPT == 2, "V stages per tile");
+  static_assert(kSmem <= 1024 + 106496, "two CTAs per SM");
 };
-constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O (and Q for fp8)
+constexpr uint32_t kT5Cols = 256;              // TMEM columns: S/P buffers, O
 
 __device__ __forceinline__ uint64_t t5_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -503,18 +505,66 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *
   if (tid == 0) split[0] = make_int4(s_n, T, 0, 0);
 }
 
+// One query row into shared memory as the K-major, 128-byte-swizzled A
+// operand of Q K^T: two head-dim halves of QR rows of 128 bytes, the 16-byte
+// chunks of row r at chunk index ^ (r % 8); a row past R (src null) is zeros.
+// FP8: f16 pairs of q 2^s, s chosen so that the row's largest |q| lies in
+// [2^14, 2^15): the f16 range then holds the whole row with no overflow (a
+// bf16 |q| may exceed f16's 65504), every bf16 value is exact, and 2^-s and
+// k_scale fold into the row's score scale, which is returned (values below
+// 2^-31 of the maximum lose bits in the f16 subnormals; their products are
+// far below the fp32 sum's rounding). Two passes over the row (the second
+// from L1) keep few registers live.
+template <int QR, bool FP8>
+__device__ __forceinline__ float t5_store_q(uint32_t q_smem, int row, const uint4 *src, float k_scale) {
+  float fold = 1.f, up = 1.f;
+  if constexpr (FP8) {
+    float amax = 0.f;
+    if (src) {
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const uint4 v = __ldg(src + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
+      }
+    }
+    const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
+    up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);                  // 2^s, s = 14 - ex
+    fold = k_scale * __uint_as_float((uint32_t)(127 - 14 + ex) << 23);      // k_scale 2^-s
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    uint4 v = src ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (FP8) {
+      auto widen = [up](uint32_t w) {
+        return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
+      };
+      v = make_uint4(widen(v.x), widen(v.y), widen(v.z), widen(v.w));
+    }
+    const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+  }
+  // the tensor cores read it through the async proxy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  return fold;
+}
+
 template <int QR, bool FP8>
 __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
   pdl_wait();
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
-  constexpr int KS = Cfg::kKS, VS = Cfg::kVS, CS = Cfg::kCS > 0 ? Cfg::kCS : 1;
+  constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
+  constexpr int CKS = Cfg::kCKS > 0 ? Cfg::kCKS : 1, CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
+  constexpr int SW = Cfg::kSoftW, CW = Cfg::kConvW;
   constexpr int TB = Cfg::kBlk, TN = Cfg::kN, VPT = Cfg::kVPT;
   constexpr uint32_t OC = Cfg::kOCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   // FP8: widened stages, filled by the converter warps, freed by the MMAs
-  __shared__ __align__(8) uint64_t kc_full[CS], kc_empty[CS], vc_full[CS], vc_empty[CS];
+  __shared__ __align__(8) uint64_t kc_full[CKS], kc_empty[CKS], vc_full[CVS], vc_empty[CVS];
   __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -526,12 +576,12 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t q_smem = smem_u32(smem);   // bf16: Q, the A operand of Q K^T
+  const uint32_t q_smem = smem_u32(smem);   // Q, the A operand of Q K^T
   const uint32_t k_ring = q_smem + Cfg::kQBytes;
   const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
   // the rings the MMAs read: the widened ones for FP8, else the TMA rings
   const uint32_t kc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : k_ring;
-  const uint32_t vc_ring = FP8 ? kc_ring + CS * Cfg::kKTile : v_ring;
+  const uint32_t vc_ring = FP8 ? kc_ring + CKS * Cfg::kKTile : v_ring;
 
   const int L = P.seq_lens[b];
   if (L < P.n_new || L > P.max_blocks * kBS) {
@@ -547,28 +597,33 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   const int R = P.R;
 
   if (tid == 0) {
+    // raw stages are freed by the MMAs (bf16) or by the CW converter warps
+    // (FP8); widened stages are filled by the converter warps
     for (int k = 0; k < KS; ++k) {
       mbar_init(&k_full[k], 1);
-      mbar_init(&k_empty[k], 1);
+      mbar_init(&k_empty[k], FP8 ? CW : 1);
     }
     for (int k = 0; k < VS; ++k) {
       mbar_init(&v_full[k], 1);
-      mbar_init(&v_empty[k], 1);
+      mbar_init(&v_empty[k], FP8 ? CW : 1);
     }
-    if (FP8)
-      for (int k = 0; k < CS; ++k) {
-        mbar_init(&kc_full[k], 1);
+    if (FP8) {
+      for (int k = 0; k < CKS; ++k) {
+        mbar_init(&kc_full[k], CW);
         mbar_init(&kc_empty[k], 1);
-        mbar_init(&vc_full[k], 1);
+      }
+      for (int k = 0; k < CVS; ++k) {
+        mbar_init(&vc_full[k], CW);
         mbar_init(&vc_empty[k], 1);
       }
+    }
     for (int k = 0; k < kT5SBuf; ++k) {
       mbar_init(&s_full[k], 1);
-      mbar_init(&p_full[k], 4);
+      mbar_init(&p_full[k], SW);
       mbar_init(&o_done[k], 1);
     }
     mbar_init(&mma_drain, 1);
-    mbar_init(&q_full, 4);   // the four softmax warps wrote their Q rows
+    mbar_init(&q_full, SW);   // the softmax warps wrote their Q rows
     abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -648,14 +703,14 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
       }
     }
-  } else if (warp < 4 || warp == kT5MmaWarp) {
+  } else if (warp < SW || warp == kT5MmaWarp) {
     if (warp == kT5MmaWarp) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                    "r"(kT5Cols));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     t5_fence_before();
-    named_bar_sync(1, 160);   // TMEM allocated
+    named_bar_sync(1, 32 * (SW + 1));   // TMEM allocated
     t5_fence_after();
     const uint32_t tb = tmem_base;
 
@@ -675,7 +730,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           if (!q_ready) q_ready = t5_test(&q_full, 0);
           if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
             // K stage: the TMA ring (bf16) or the widened ring (FP8)
-            const int KR = FP8 ? CS : KS;
+            const int KR = FP8 ? CKS : KS;
             const int ks = tq % KR, sb = tq % kT5SBuf;
             uint64_t *kf = FP8 ? kc_full : k_full;
             // S buffer sb is free once the P V of tile tq - kT5SBuf has run
@@ -685,12 +740,10 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
               const uint32_t kb = kc_ring + ks * Cfg::kKTile;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {   // 16 head dims per step
-                const uint64_t bd = t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024);
-                if constexpr (Cfg::kQSmem)   // A = Q from shared memory
-                  t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024), bd,
-                            idesc_qk, kk > 0 ? 1u : 0u);
-                else   // A = Q from TMEM: 8 columns per step
-                  t5_mma_ts(tb + sb * TN, tb + Cfg::kQCol + 8 * kk, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                // A = Q and B = K from shared memory
+                t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024),
+                          t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024), idesc_qk,
+                          kk > 0 ? 1u : 0u);
               }
               t5_commit(&s_full[sb]);
               t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
@@ -700,7 +753,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           }
           if (tp < tq) {
             // the tile's V stages: the TMA ring (bf16) or the widened ring (FP8)
-            const int VR = FP8 ? CS : VS;
+            const int VR = FP8 ? CVS : VS;
             const int sb = tp % kT5SBuf;
             uint64_t *vf = FP8 ? vc_full : v_full;
             bool ready = t5_test(&p_full[sb], (tp / kT5SBuf) & 1);
@@ -746,7 +799,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       __syncwarp();
     } else {
       // ------------------------------------------------------------ softmax ----
-      const int row = tid;   // warps 0-3
+      const int row = tid;   // the softmax warps
       const bool warp_live = warp * 32 < R;
       const bool live = row < R;
       const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
@@ -762,67 +815,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
                                                 (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
         }
-        if constexpr (Cfg::kQSmem) {
-          // this row of Q into shared memory: head-dim halves of QR rows of
-          // 128 bytes, the 16-byte chunks of row r at chunk index ^ (r % 8)
-          // (the 128-byte swizzle of the MMA operand); rows past R are zeros
-          if (row < QR) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-              const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                           : "memory");
-            }
-            // the tensor cores read it through the async proxy
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          }
-        } else if (warp_live) {
-          // this row of Q into TMEM (columns kQCol.., f16 pairs in memory
-          // order). tcgen05.st is warp-collective: a warp holding live rows
-          // stores all 32 (zeros for rows past R); warps with none skip it
-          // (their rows of S, P and O are never read).
-          {
-            // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
-            // in [2^14, 2^15): the f16 range then holds the whole row with no
-            // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
-            // exact, and 2^-s, k_scale and the softmax scale fold into the
-            // row's scale (values below 2^-31 of the maximum lose bits in the
-            // f16 subnormals; their products are far below the fp32 sum's
-            // rounding). Two passes over the row (the second from L1) keep
-            // few registers live.
-            float amax = 0.f;
-            if (live) {
-#pragma unroll 4
-              for (int k = 0; k < 16; ++k) {
-                const uint4 v = __ldg(src + k);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
-              }
-            }
-            const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
-            const float up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);     // 2^s, s = 14 - ex
-            const float down = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);   // 2^-s
-            sl2 *= P.k_scale[g] * down;
-            auto widen = [up](uint32_t w) {
-              return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
-            };
-#pragma unroll 1
-            for (int c0 = 0; c0 < 4; ++c0) {
-              uint32_t w[16];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint4 v = live ? __ldg(src + 4 * c0 + k) : make_uint4(0u, 0u, 0u, 0u);
-                w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
-                w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
-              }
-              t5_st16(lane_base + Cfg::kQCol + 16 * c0, w);
-            }
-          }
-          t5_wait_st();
-        }
+        if (row < QR) sl2 *= t5_store_q<QR, FP8>(q_smem, row, src, FP8 ? P.k_scale[g] : 1.f);
         t5_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full);
@@ -987,64 +980,73 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       }
     }
   }
-  if (FP8 && (warp == 7 || warp == 8)) {
+  if constexpr (FP8) {
     // ----------------------------------------------------- e4m3 -> f16 ---
-    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is TB blocks of
-    // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
-    // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
-    // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
-    // keys past the split or the sequence are written as zeros.
-    const bool isv = warp == 8;
-    const int NS = isv ? VS : KS;
-    uint64_t *rfull = isv ? v_full : k_full;
-    uint64_t *rempty = isv ? v_empty : k_empty;
-    uint64_t *cfull = isv ? vc_full : kc_full;
-    uint64_t *cempty = isv ? vc_empty : kc_empty;
-    const uint32_t rring = isv ? v_ring : k_ring;
-    const uint32_t cring = isv ? vc_ring : kc_ring;
-    const int end_key = min(L, blk1 * kBS);
-    for (int t = 0; t < n_tiles; ++t) {
-      const int rs = t % NS, cs = t % CS;
-      bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (t / NS) & 1, abf, P.wait_ns));
-      if (ok && t >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((t / CS) - 1) & 1, abf, P.wait_ns));
-      if (!ok) break;
-      const uint32_t src = rring + rs * Cfg::kKRaw, dst = cring + cs * Cfg::kKTile;   // K and V alike for FP8
-      const int key0 = (blk0 + t * TB) * kBS;
+    // K stages: warp 7 (and warp 2), V stages: warp 8 (and warp 3). A raw
+    // stage is blocks of 16 slots x 128 codes (128-byte swizzle); the CW
+    // warps of a direction share its 16-byte chunks: chunk q = 32 cw + lane
+    // + 32 CW j is key row q / 8, head dims 16 (q % 8) .. + 15, and lands as
+    // two 16-byte chunks of one head-dim half of the f16 stage. Rows of keys
+    // past the split or the sequence are written as zeros.
+    const bool isk = warp == 7 || (CW == 2 && warp == 2);
+    const bool isv = warp == 8 || (CW == 2 && warp == 3);
+    if (isk || isv) {
+      const int cw = (warp == 7 || warp == 8) ? 0 : 1;
+      const int NS = isv ? VS : KS, NC = isv ? CVS : CKS;
+      const int sblk = isv ? kT5Blk : TB;   // blocks per stage
+      const uint32_t rbytes = isv ? Cfg::kVRaw : Cfg::kKRaw, cbytes = isv ? Cfg::kVTile : Cfg::kKTile;
+      const uint32_t chalf = isv ? Cfg::kVHalf : Cfg::kKHalf;
+      uint64_t *rfull = isv ? v_full : k_full;
+      uint64_t *rempty = isv ? v_empty : k_empty;
+      uint64_t *cfull = isv ? vc_full : kc_full;
+      uint64_t *cempty = isv ? vc_empty : kc_empty;
+      const uint32_t rring = isv ? v_ring : k_ring;
+      const uint32_t cring = isv ? vc_ring : kc_ring;
+      const int end_key = min(L, blk1 * kBS);
+      const int n_st = n_tiles * (isv ? VPT : 1);
+      const int nch = sblk * 128;   // 16-byte chunks of a raw stage
+      for (int i = 0; i < n_st; ++i) {
+        const int rs = i % NS, cs = i % NC;
+        bool ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (i / NS) & 1, abf, P.wait_ns));
+        if (ok && i >= NC) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((i / NC) - 1) & 1, abf, P.wait_ns));
+        if (!ok) break;
+        const uint32_t src = rring + rs * rbytes, dst = cring + cs * cbytes;
+        const int key0 = (blk0 + i * sblk) * kBS;
 #pragma unroll 2
-      for (int j = 0; j < 8; ++j) {
-        const int q = lane + 32 * j;
-        const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
-        uint32_t v0, v1, v2, v3;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                     : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
-        uint32_t h[8];
-        if (key0 + row < end_key) {
-          const uint32_t w[4] = {v0, v1, v2, v3};
+        for (int q = 32 * cw + lane; q < nch; q += 32 * CW) {
+          const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
+          uint32_t v0, v1, v2, v3;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                       : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
+          uint32_t h[8];
+          if (key0 + row < end_key) {
+            const uint32_t w[4] = {v0, v1, v2, v3};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffffu));
-            h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+            for (int e = 0; e < 4; ++e) {
+              h[2 * e] = e4m3x2_to_f16x2((uint16_t)(w[e] & 0xffffu));
+              h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(w[e] >> 16));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[e] = 0u;
           }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) h[k] = 0u;
+          const uint32_t rowb = dst + (ch >> 2) * chalf + row * 128;
+          const int c8 = 2 * (ch & 3);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
+                       "r"(h[1]), "r"(h[2]), "r"(h[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
+                       "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                       : "memory");
         }
-        const uint32_t rowb = dst + (ch >> 2) * Cfg::kKHalf + blk * 2048 + r16 * 128;
-        const int c8 = 2 * (ch & 3);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
-                     "r"(h[1]), "r"(h[2]), "r"(h[3])
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
-                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                     : "memory");
-      }
-      // the tensor cores read the widened tile through the async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
-        mbar_arrive(&cfull[cs]);    // the widened stage may be read
+        // the tensor cores read the widened stage through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
+          mbar_arrive(&cfull[cs]);    // the widened stage may be read
+        }
       }
     }
   }
@@ -1067,13 +1069,15 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
   pdl_wait();
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
-  constexpr int KS = Cfg::kKS, VS = Cfg::kVS, CS = Cfg::kCS > 0 ? Cfg::kCS : 1;
+  constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
+  constexpr int CKS = Cfg::kCKS > 0 ? Cfg::kCKS : 1, CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
+  constexpr int SW = Cfg::kSoftW, CW = Cfg::kConvW;
   constexpr int TB = Cfg::kBlk, TN = Cfg::kN, VPT = Cfg::kVPT;
   constexpr uint32_t OC = Cfg::kOCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   // FP8: widened stages, filled by the converter warps, freed by the MMAs
-  __shared__ __align__(8) uint64_t kc_full[CS], kc_empty[CS], vc_full[CS], vc_empty[CS];
+  __shared__ __align__(8) uint64_t kc_full[CKS], kc_empty[CKS], vc_full[CVS], vc_empty[CVS];
   __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -1086,37 +1090,42 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
     if (!t5_item(P, w0, it0)) return;
   }
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t q_smem = smem_u32(smem);   // bf16: Q, the A operand of Q K^T
+  const uint32_t q_smem = smem_u32(smem);   // Q, the A operand of Q K^T
   const uint32_t k_ring = q_smem + Cfg::kQBytes;
   const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
   // the rings the MMAs read: the widened ones for FP8, else the TMA rings
   const uint32_t kc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : k_ring;
-  const uint32_t vc_ring = FP8 ? kc_ring + CS * Cfg::kKTile : v_ring;
+  const uint32_t vc_ring = FP8 ? kc_ring + CKS * Cfg::kKTile : v_ring;
   const int R = P.R;
 
   if (tid == 0) {
+    // raw stages are freed by the MMAs (bf16) or by the CW converter warps
+    // (FP8); widened stages are filled by the converter warps
     for (int k = 0; k < KS; ++k) {
       mbar_init(&k_full[k], 1);
-      mbar_init(&k_empty[k], 1);
+      mbar_init(&k_empty[k], FP8 ? CW : 1);
     }
     for (int k = 0; k < VS; ++k) {
       mbar_init(&v_full[k], 1);
-      mbar_init(&v_empty[k], 1);
+      mbar_init(&v_empty[k], FP8 ? CW : 1);
     }
-    if (FP8)
-      for (int k = 0; k < CS; ++k) {
-        mbar_init(&kc_full[k], 1);
+    if (FP8) {
+      for (int k = 0; k < CKS; ++k) {
+        mbar_init(&kc_full[k], CW);
         mbar_init(&kc_empty[k], 1);
-        mbar_init(&vc_full[k], 1);
+      }
+      for (int k = 0; k < CVS; ++k) {
+        mbar_init(&vc_full[k], CW);
         mbar_init(&vc_empty[k], 1);
       }
+    }
     for (int k = 0; k < kT5SBuf; ++k) {
       mbar_init(&s_full[k], 1);
-      mbar_init(&p_full[k], 4);
+      mbar_init(&p_full[k], SW);
       mbar_init(&o_done[k], 1);
     }
     mbar_init(&mma_drain, 1);
-    mbar_init(&q_full, 4);   // the four softmax warps wrote their Q rows (one phase per item)
+    mbar_init(&q_full, SW);   // the softmax warps wrote their Q rows (one phase per item)
     abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -1204,14 +1213,14 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
       for (int t = max(0, issued - NS); t < issued; ++t)
         if (!mbar_wait(&fullb[t % NS], (t / NS) & 1)) atomic_or_status(P.status, SV_DEV_TIMEOUT);
     }
-  } else if (warp < 4 || warp == kT5MmaWarp) {
+  } else if (warp < SW || warp == kT5MmaWarp) {
     if (warp == kT5MmaWarp) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                    "r"(kT5Cols));
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     t5_fence_before();
-    named_bar_sync(1, 160);   // TMEM allocated
+    named_bar_sync(1, 32 * (SW + 1));   // TMEM allocated
     t5_fence_after();
     const uint32_t tb = tmem_base;
 
@@ -1242,7 +1251,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
             if (!q_ready) q_ready = t5_test(&q_full, xq & 1);
             if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
               // K stage: the TMA ring (bf16) or the widened ring (FP8)
-              const int KR = FP8 ? CS : KS;
+              const int KR = FP8 ? CKS : KS;
               const int uq = u0 + tq;
               const int ks = uq % KR, sb = uq % kT5SBuf;
               uint64_t *kf = FP8 ? kc_full : k_full;
@@ -1253,12 +1262,10 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
                 const uint32_t kb = kc_ring + ks * Cfg::kKTile;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {   // 16 head dims per step
-                  const uint64_t bd = t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024);
-                  if constexpr (Cfg::kQSmem)   // A = Q from shared memory
-                    t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024), bd,
-                              idesc_qk, kk > 0 ? 1u : 0u);
-                  else   // A = Q from TMEM: 8 columns per step
-                    t5_mma_ts(tb + sb * TN, tb + Cfg::kQCol + 8 * kk, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                  // A = Q and B = K from shared memory
+                  t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024),
+                            t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024), idesc_qk,
+                            kk > 0 ? 1u : 0u);
                 }
                 t5_commit(&s_full[sb]);
                 t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
@@ -1268,7 +1275,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
             }
             if (tp < tq) {
               // the tile's V stages: the TMA ring (bf16) or the widened ring (FP8)
-              const int VR = FP8 ? CS : VS;
+              const int VR = FP8 ? CVS : VS;
               const int up = u0 + tp;
               const int sb = up % kT5SBuf;
               uint64_t *vf = FP8 ? vc_full : v_full;
@@ -1320,7 +1327,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
       __syncwarp();
     } else {
       // ------------------------------------------------------------ softmax ----
-      const int row = tid;   // warps 0-3
+      const int row = tid;   // the softmax warps
       const bool warp_live = warp * 32 < R;
       const bool live = row < R;
       const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
@@ -1346,68 +1353,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
             src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
                                                   (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
           }
-          if constexpr (Cfg::kQSmem) {
-            // this row of Q into shared memory: head-dim halves of QR rows of
-            // 128 bytes, the 16-byte chunks of row r at chunk index ^ (r % 8)
-            // (the 128-byte swizzle of the MMA operand); rows past R are zeros
-            if (row < QR) {
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z),
-                             "r"(v.w)
-                             : "memory");
-              }
-              // the tensor cores read it through the async proxy
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-          } else if (warp_live) {
-            // this row of Q into TMEM (columns kQCol.., f16 pairs in memory
-            // order). tcgen05.st is warp-collective: a warp holding live rows
-            // stores all 32 (zeros for rows past R); warps with none skip it
-            // (their rows of S, P and O are never read).
-            {
-              // f16 pairs of q 2^s, s chosen so that the row's largest |q| lies
-              // in [2^14, 2^15): the f16 range then holds the whole row with no
-              // overflow (a bf16 |q| may exceed f16's 65504), every bf16 value is
-              // exact, and 2^-s, k_scale and the softmax scale fold into the
-              // row's scale (values below 2^-31 of the maximum lose bits in the
-              // f16 subnormals; their products are far below the fp32 sum's
-              // rounding). Two passes over the row (the second from L1) keep
-              // few registers live.
-              float amax = 0.f;
-              if (live) {
-#pragma unroll 4
-                for (int k = 0; k < 16; ++k) {
-                  const uint4 v = __ldg(src + k);
-                  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                  for (int e = 0; e < 4; ++e)
-                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
-                }
-              }
-              const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
-              const float up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);     // 2^s, s = 14 - ex
-              const float down = __uint_as_float((uint32_t)(127 - 14 + ex) << 23);   // 2^-s
-              sl2 *= P.k_scale[g] * down;
-              auto widen = [up](uint32_t w) {
-                return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
-              };
-#pragma unroll 1
-              for (int c0 = 0; c0 < 4; ++c0) {
-                uint32_t w[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const uint4 v = live ? __ldg(src + 4 * c0 + k) : make_uint4(0u, 0u, 0u, 0u);
-                  w[4 * k] = widen(v.x); w[4 * k + 1] = widen(v.y);
-                  w[4 * k + 2] = widen(v.z); w[4 * k + 3] = widen(v.w);
-                }
-                t5_st16(lane_base + Cfg::kQCol + 16 * c0, w);
-              }
-            }
-            t5_wait_st();
-          }
+          if (row < QR) sl2 *= t5_store_q<QR, FP8>(q_smem, row, src, FP8 ? P.k_scale[g] : 1.f);
           t5_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&q_full);
@@ -1573,70 +1519,75 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
       }
     }
   }
-  if (FP8 && (warp == 7 || warp == 8)) {
+  if constexpr (FP8) {
     // ----------------------------------------------------- e4m3 -> f16 ---
-    // warp 7 widens K tiles, warp 8 V tiles. A raw tile is TB blocks of
-    // 16 slots x 128 codes (128-byte swizzle); lane l takes 16-byte chunks
-    // q = l + 32 j: key row q / 8, head dims 16 (q % 8) .. + 15, which land
-    // as two 16-byte chunks of one head-dim half of the f16 tile. Rows of
-    // keys past the item or the sequence are written as zeros.
-    const bool isv = warp == 8;
-    const int NS = isv ? VS : KS;
-    uint64_t *rfull = isv ? v_full : k_full;
-    uint64_t *rempty = isv ? v_empty : k_empty;
-    uint64_t *cfull = isv ? vc_full : kc_full;
-    uint64_t *cempty = isv ? vc_empty : kc_empty;
-    const uint32_t rring = isv ? v_ring : k_ring;
-    const uint32_t cring = isv ? vc_ring : kc_ring;
-    T5Walk wk = {};
-    T5Item it;
-    int u = 0;
-    bool ok = true;
-    while (ok && t5_item(P, wk, it)) {
-      const int end_key = min(it.L, it.blk1 * kBS);
-      const int n_tiles = (it.blk1 - it.blk0 + TB - 1) / TB;
-      for (int t = 0; t < n_tiles; ++t, ++u) {
-        const int rs = u % NS, cs = u % CS;
-        ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (u / NS) & 1, abf, P.wait_ns));
-        if (ok && u >= CS) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((u / CS) - 1) & 1, abf, P.wait_ns));
-        if (!ok) break;
-        const uint32_t src = rring + rs * Cfg::kKRaw, dst = cring + cs * Cfg::kKTile;   // K and V alike for FP8
-        const int key0 = (it.blk0 + t * TB) * kBS;
+    // as in attn_tc5_kernel, over the CTA's items: the running stage count
+    // indexes the rings, and rows of keys past the item or the sequence are
+    // written as zeros
+    const bool isk = warp == 7 || (CW == 2 && warp == 2);
+    const bool isv = warp == 8 || (CW == 2 && warp == 3);
+    if (isk || isv) {
+      const int cw = (warp == 7 || warp == 8) ? 0 : 1;
+      const int NS = isv ? VS : KS, NC = isv ? CVS : CKS;
+      const int sblk = isv ? kT5Blk : TB;   // blocks per stage
+      const uint32_t rbytes = isv ? Cfg::kVRaw : Cfg::kKRaw, cbytes = isv ? Cfg::kVTile : Cfg::kKTile;
+      const uint32_t chalf = isv ? Cfg::kVHalf : Cfg::kKHalf;
+      uint64_t *rfull = isv ? v_full : k_full;
+      uint64_t *rempty = isv ? v_empty : k_empty;
+      uint64_t *cfull = isv ? vc_full : kc_full;
+      uint64_t *cempty = isv ? vc_empty : kc_empty;
+      const uint32_t rring = isv ? v_ring : k_ring;
+      const uint32_t cring = isv ? vc_ring : kc_ring;
+      const int nch = sblk * 128;   // 16-byte chunks of a raw stage
+      T5Walk wk = {};
+      T5Item it;
+      int i = 0;   // the CTA's running stage count
+      bool ok = true;
+      while (ok && t5_item(P, wk, it)) {
+        const int end_key = min(it.L, it.blk1 * kBS);
+        const int n_st = (it.blk1 - it.blk0 + TB - 1) / TB * (isv ? VPT : 1);
+        for (int q0 = 0; q0 < n_st; ++q0, ++i) {
+          const int rs = i % NS, cs = i % NC;
+          ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (i / NS) & 1, abf, P.wait_ns));
+          if (ok && i >= NC) ok = __all_sync(0xffffffffu, t5_wait(&cempty[cs], ((i / NC) - 1) & 1, abf, P.wait_ns));
+          if (!ok) break;
+          const uint32_t src = rring + rs * rbytes, dst = cring + cs * cbytes;
+          const int key0 = (it.blk0 + q0 * sblk) * kBS;
 #pragma unroll 2
-        for (int j = 0; j < 8; ++j) {
-          const int q = lane + 32 * j;
-          const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
-          uint32_t v0, v1, v2, v3;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                       : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
-          uint32_t h[8];
-          if (key0 + row < end_key) {
-            const uint32_t w[4] = {v0, v1, v2, v3};
+          for (int q = 32 * cw + lane; q < nch; q += 32 * CW) {
+            const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
+            uint32_t v0, v1, v2, v3;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                         : "r"(src + blk * 2048 + r16 * 128 + ((ch ^ (r16 & 7)) << 4)));
+            uint32_t h[8];
+            if (key0 + row < end_key) {
+              const uint32_t w[4] = {v0, v1, v2, v3};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              h[2 * k] = e4m3x2_to_f16x2((uint16_t)(w[k] & 0xffffu));
-              h[2 * k + 1] = e4m3x2_to_f16x2((uint16_t)(w[k] >> 16));
+              for (int e = 0; e < 4; ++e) {
+                h[2 * e] = e4m3x2_to_f16x2((uint16_t)(w[e] & 0xffffu));
+                h[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(w[e] >> 16));
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) h[e] = 0u;
             }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] = 0u;
+            const uint32_t rowb = dst + (ch >> 2) * chalf + row * 128;
+            const int c8 = 2 * (ch & 3);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
+                         "r"(h[1]), "r"(h[2]), "r"(h[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
+                         "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                         : "memory");
           }
-          const uint32_t rowb = dst + (ch >> 2) * Cfg::kKHalf + blk * 2048 + r16 * 128;
-          const int c8 = 2 * (ch & 3);
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + ((c8 ^ (r16 & 7)) << 4)), "r"(h[0]),
-                       "r"(h[1]), "r"(h[2]), "r"(h[3])
-                       : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rowb + (((c8 + 1) ^ (r16 & 7)) << 4)),
-                       "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                       : "memory");
-        }
-        // the tensor cores read the widened tile through the async proxy
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
-          mbar_arrive(&cfull[cs]);    // the widened stage may be read
+          // the tensor cores read the widened stage through the async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
+            mbar_arrive(&cfull[cs]);    // the widened stage may be read
+          }
         }
       }
     }

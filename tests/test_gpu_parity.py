@@ -169,6 +169,21 @@ def test_attention_split_count_invariance(lib, bps, kv):
     assert ((out.float() - base.float()).abs() <= tol + ulp * base.float().abs()).all()
 
 
+@pytest.mark.parametrize("bps", [None, 0, 5])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_attention_ragged_last_tiles(lib, bps, kv):
+    # lengths whose last tile (64 keys for bf16 caches, 32 for fp8) holds 1
+    # to 4 blocks, the last block 1 to 16 keys: the tile's second V stage is
+    # absent, partial or whole; also with 5-block splits (tiles cut at every
+    # split edge) and balanced ranges
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype=kv, q_dtype="bf16", d_head=128, B=6, H_q=8, H_kv=2, K=3,
+                                          ctx=("fixed", (129, 145, 161, 177, 190, 200)))
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=11))
+    kw = {} if bps is None else {"blocks_per_split": bps}
+    out = run_attention(lib, cfg, a, **kw)
+    check_attention(out, oracle_attention(cfg, a), cfg)
+
+
 def test_attention_four_splits_repeated_calls(lib):
     # four splits per sequence (partials merged by the merge kernel) and the
     # longest-first work order, with one workspace reused across calls: every
