@@ -1012,7 +1012,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
         if (!ok) break;
         const uint32_t src = rring + rs * rbytes, dst = cring + cs * cbytes;
         const int key0 = (blk0 + i * sblk) * kBS;
-#pragma unroll 2
+#pragma unroll 4
         for (int q = 32 * cw + lane; q < nch; q += 32 * CW) {
           const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
           uint32_t v0, v1, v2, v3;
@@ -1553,7 +1553,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
           if (!ok) break;
           const uint32_t src = rring + rs * rbytes, dst = cring + cs * cbytes;
           const int key0 = (it.blk0 + q0 * sblk) * kBS;
-#pragma unroll 2
+#pragma unroll 4
           for (int q = 32 * cw + lane; q < nch; q += 32 * CW) {
             const int row = q >> 3, ch = q & 7, blk = row >> 4, r16 = row & 15;
             uint32_t v0, v1, v2, v3;
