@@ -184,6 +184,20 @@ def test_attention_ragged_last_tiles(lib, bps, kv):
     check_attention(out, oracle_attention(cfg, a), cfg)
 
 
+@pytest.mark.parametrize("bps", [1, 2])
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_attention_many_splits_merge(lib, bps, kv):
+    # a sequence of 69 blocks cut into 69 or 35 splits: the merge takes more
+    # pieces per row than one round trip of its warps loads (8 warps x 8
+    # pieces), beside a short sequence with a single split
+    q = "f32" if kv == "f32" else "bf16"
+    d = 64 if kv == "f32" else 128
+    cfg = workloads.CONFIGS["tiny"].with_(kv_dtype=kv, q_dtype=q, d_head=d, ctx=("fixed", (1100, 40)))
+    a = to_dev(workloads.make_attention_inputs(cfg, seed=13))
+    out = run_attention(lib, cfg, a, blocks_per_split=bps)
+    check_attention(out, oracle_attention(cfg, a), cfg)
+
+
 def test_attention_four_splits_repeated_calls(lib):
     # four splits per sequence (partials merged by the merge kernel) and the
     # longest-first work order, with one workspace reused across calls: every
