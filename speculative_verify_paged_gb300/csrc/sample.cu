@@ -607,10 +607,10 @@ __device__ __forceinline__ void draw_weights8(const Raw8<TT> &rt, const Raw8<TD>
 }
 
 constexpr int kMaxDrawBlocks = 64;   // blocks of 32 groups per CTA slice (2048 groups)
+constexpr int kDrawRowCache = 64;    // rows whose statistics the draw kernel keeps from its accept tests
 
 struct DrawShared {
   int stop;               // 2 * position + (0: not certified, 1: certified rejection)
-  float row_m_p, row_s_p, row_m_q, row_s_q;
   float pub_tot;          // this CTA's draw mass
   float wsum[kRowWarps];  // per warp
   float btot[kMaxDrawBlocks];   // per block of 32 groups
@@ -658,10 +658,9 @@ __device__ __forceinline__ void row_stats(const SampleParams &P, int b, int i, b
 
 template <typename TT, int DK>
 __global__ void __launch_bounds__(kRowThreads, 4) sample_draw_kernel(const __grid_constant__ SampleParams P) {
-  pdl_wait();
-  pdl_trigger();
   using TD = typename std::conditional<DK == 0, TT, float>::type;
   __shared__ DrawShared sh;
+  __shared__ float4 s_rs[kDrawRowCache];   // (m_p, S_p, m_q, S_q) of the first rows
 
   const int cs = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
   const int b = blockIdx.y;
@@ -669,23 +668,63 @@ __global__ void __launch_bounds__(kRowThreads, 4) sample_draw_kernel(const __gri
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float c = P.c;
   const bool force = (P.flags & SV_SAMPLE_FORCE_EXACT) != 0;
+  // The inputs of this warp's first accept test are loaded before the wait
+  // on the statistics pass: the caller's arrays, or rows the top-p filter
+  // wrote, which had finished before any CTA of the statistics pass let
+  // this grid start.
+  int x0 = 0;
+  bool bad0 = false;
+  float lp0 = 0.f, lq0 = 0.f, u0 = 0.f;
+  if (warp < K) {
+    x0 = P.tokens[(int64_t)b * K + warp];
+    bad0 = x0 < 0 || x0 >= V;
+    x0 = min(max(x0, 0), V - 1);
+    lp0 = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + warp) * V + x0]);
+    lq0 = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + warp) * V + x0]);
+    u0 = P.uniforms[((int64_t)b * (K + 1) + warp) * 2];
+  }
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) sh.stop = 2 * K + 1;
   if (tid == 0 && blockIdx.x == 0 && b == 0) P.fin_sync[0] = 0u;   // the finish grid barrier starts empty
   __syncthreads();
 
-  // ---- accept tests of every draft position --------------------------------
-  for (int i = warp; i < K; i += kRowWarps) {
+  // ---- accept tests of every draft position, and the bonus row's record ---
+  // (each row's statistics are kept for the draw that follows)
+  for (int i = warp; i <= K; i += kRowWarps) {
     float m_p, S_p, m_q, S_q;
+    if (i == K) {   // the bonus row: the finish kernel may walk to it
+      row_stats(P, b, K, false, m_p, S_p, m_q, S_q);
+      if (lane == 0) {
+        if (K < kDrawRowCache) s_rs[K] = make_float4(m_p, S_p, 0.f, 1.f);
+        if (rank == 0) {
+          RowRec *rec = P.recs + (int64_t)b * (K + 1) + K;
+          rec->m_p = m_p; rec->s_p = S_p; rec->m_q = 0.f; rec->s_q = 1.f;
+          rec->p_x = 0.f; rec->q_x = 0.f;
+          rec->y = -1; rec->y_exact = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
+          rec->flags = 0u;
+          if (!(fabsf(m_p) <= 3.0e38f && S_p > 0.f)) atomic_or_status(P.status, SV_DEV_NONFINITE);
+        }
+      }
+      continue;
+    }
     row_stats(P, b, i, DK == 0, m_p, S_p, m_q, S_q);
     if (DK != 0) { m_q = 0.f; S_q = 1.f; }
-    int x = P.tokens[(int64_t)b * K + i];
-    if (x < 0 || x >= V) {
-      if (rank == 0 && lane == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+    int x;
+    float lp_x, lq_x, u;
+    bool bad;
+    if (i == warp) {
+      x = x0; bad = bad0; lp_x = lp0; lq_x = lq0; u = u0;
+    } else {
+      x = P.tokens[(int64_t)b * K + i];
+      bad = x < 0 || x >= V;
       x = min(max(x, 0), V - 1);
+      lp_x = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + i) * V + x]);
+      lq_x = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + i) * V + x]);
+      u = P.uniforms[((int64_t)b * (K + 1) + i) * 2];
     }
-    const float lp_x = to_f32(static_cast<const TT *>(P.target)[((int64_t)b * (K + 1) + i) * V + x]);
-    const float lq_x = to_f32(static_cast<const TD *>(P.draft)[((int64_t)b * K + i) * V + x]);
-    const float u = P.uniforms[((int64_t)b * (K + 1) + i) * 2];
+    if (bad && rank == 0 && lane == 0) atomic_or_status(P.status, SV_DEV_BAD_TOKEN);
+    if (i < kDrawRowCache && lane == 0) s_rs[i] = make_float4(m_p, S_p, m_q, S_q);
     const bool finite = fabsf(m_p) <= 3.0e38f && (DK != 0 || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
     const float mcp = __fmul_rn(m_p, c), mcq = __fmul_rn(m_q, c);
     const float p_x = ex2(fmaf(lp_x, c, -mcp)) / S_p;
@@ -717,33 +756,23 @@ __global__ void __launch_bounds__(kRowThreads, 4) sample_draw_kernel(const __gri
   const int n = stop >> 1;
   const bool has_draft = n < K;
   const bool q_logits = has_draft && DK == 0;
-  if (warp == 0 && certain) {   // statistics of the row drawn from
-    float m_p, S_p, m_q, S_q;
-    row_stats(P, b, n, q_logits, m_p, S_p, m_q, S_q);
-    if (!q_logits) { m_q = 0.f; S_q = 1.f; }
-    if (lane == 0) { sh.row_m_p = m_p; sh.row_s_p = S_p; sh.row_m_q = m_q; sh.row_s_q = S_q; }
-  }
-  if (warp == 1 && rank == 0) {
-    // the bonus row's record (the finish kernel may walk to it)
-    float m_p, S_p, m_q, S_q;
-    row_stats(P, b, K, false, m_p, S_p, m_q, S_q);
-    if (lane == 0) {
-      RowRec *rec = P.recs + (int64_t)b * (K + 1) + K;
-      rec->m_p = m_p; rec->s_p = S_p; rec->m_q = 0.f; rec->s_q = 1.f;
-      rec->p_x = 0.f; rec->q_x = 0.f;
-      rec->y = -1; rec->y_exact = -1; rec->gap = 0.f; rec->z = 0.f; rec->e_abs = 0.f;
-      rec->flags = 0u;
-      if (!(fabsf(m_p) <= 3.0e38f && S_p > 0.f)) atomic_or_status(P.status, SV_DEV_NONFINITE);
-    }
-  }
-  __syncthreads();
   // identical in every CTA of the cluster: no shared memory of a peer is
   // read on this path
   if (!certain || force) {   // the first uncertified accept test (or all, forced)
     if (rank == 0 && tid == 0) push_pending(P, b, force ? 0 : n);
     return;
   }
-  const float m_p = sh.row_m_p, S_p = sh.row_s_p, m_q = sh.row_m_q, S_q = sh.row_s_q;
+  if (n >= kDrawRowCache) {   // statistics of the row drawn from, when not kept
+    if (warp == 0) {
+      float a0, a1, a2, a3;
+      row_stats(P, b, n, q_logits, a0, a1, a2, a3);
+      if (!q_logits) { a2 = 0.f; a3 = 1.f; }
+      if (lane == 0) s_rs[0] = make_float4(a0, a1, a2, a3);
+    }
+    __syncthreads();
+  }
+  const float4 rs = s_rs[n < kDrawRowCache ? n : 0];
+  const float m_p = rs.x, S_p = rs.y, m_q = rs.z, S_q = rs.w;
   const bool finite = fabsf(m_p) <= 3.0e38f && (!q_logits || fabsf(m_q) <= 3.0e38f) && S_p > 0.f;
 
   // ---- the draw: this CTA's slice of row n, straight into registers -------
