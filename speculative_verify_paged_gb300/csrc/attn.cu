@@ -84,6 +84,14 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
+// two fp32 values -> two e4m3 codes (x0 in the low byte), rounded to
+// nearest even, saturating at +-448
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float x0, float x1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+
 // two e4m3 codes (low byte first) -> f16x2
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t out;
@@ -184,31 +192,33 @@ constexpr int kT5MaxR = 128;
 // P and O are never used). K stages hold a tile, V streams in 32-key stages,
 // two per tile.
 // FP8: e4m3 caches. TMA lands the raw 16 x 128-byte tile of each block in
-// rings of their own; converter warps widen them exactly to f16 (every e4m3
-// value is an f16 value) into second rings laid out as the 16-bit tiles are,
-// and the MMAs run on f16 operands (Q and P in f16 too). K and V each have
-// two converter warps when the group has at most 64 query rows (softmax
-// warps 2 and 3 have no rows then and widen instead), else one.
+// rings of their own. Q K^T reads the raw K tiles directly (kind::f8f6f4):
+// each query row, scaled by a power of two, is split into two e4m3 terms
+// (hi + lo, about the precision of its bf16 values), and the two partial
+// products accumulate in the S buffer. V is widened exactly to f16 (every
+// e4m3 value is an f16 value) by converter warps into a second ring laid
+// out as the 16-bit stages are, and P V runs on f16 operands. Four warps
+// widen V when the group has at most 64 query rows (softmax warps 2 and 3
+// hold no rows then), else two.
 // The rings take what two CTAs per SM leave.
 template <int QR, bool FP8> struct T5Cfg {
   static constexpr int kBlk = 4;                             // paged blocks per tile
   static constexpr int kN = 16 * kBlk;                       // keys per tile
   static constexpr int kVPT = kBlk / kT5Blk;                 // 32-key V stages per tile
-  static constexpr int kQBytes = QR * 256;                   // two head-dim halves of QR rows
+  static constexpr int kQBytes = QR * 256;                   // bf16: two head-dim halves; fp8: hi and lo terms
   static constexpr int kKHalf = kBlk * 2048;                 // a head-dim half of a 16-bit K tile
   static constexpr int kKTile = 2 * kKHalf;
   static constexpr int kVHalf = kT5Blk * 2048;               // a head-dim half of a 16-bit V stage
   static constexpr int kVTile = 2 * kVHalf;
-  static constexpr int kKS = FP8 ? 2 : 3;                    // K stages (raw for FP8)
-  static constexpr int kVS = FP8 ? (QR == 64 ? 4 : 2) : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
-  static constexpr int kCKS = FP8 ? 2 : 0;                   // widened K stages
-  static constexpr int kCVS = FP8 ? (QR == 64 ? 3 : 2) : 0;  // widened V stages
-  static constexpr int kConvW = FP8 ? (QR == 64 ? 2 : 1) : 0;   // converter warps each of K and V
-  static constexpr int kSoftW = 4 - (kConvW == 2 ? 2 : 0);   // warps in the softmax role
+  static constexpr int kKS = FP8 ? (QR == 64 ? 4 : 3) : 3;   // K stages (raw for FP8)
+  static constexpr int kVS = FP8 ? (QR == 64 ? 6 : 4) : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
+  static constexpr int kCVS = FP8 ? 4 : 0;                   // widened V stages
+  static constexpr int kConvW = FP8 ? (QR == 64 ? 4 : 2) : 0;   // V converter warps
+  static constexpr int kSoftW = FP8 && QR == 64 ? 2 : 4;     // warps in the softmax role
   static constexpr int kKRaw = FP8 ? kBlk * 2048 : kKTile;   // bytes of a K ring stage
   static constexpr int kVRaw = FP8 ? kT5Blk * 2048 : kVTile; // bytes of a V ring stage
   static constexpr int kThreads = FP8 ? 288 : 256;
-  static constexpr int kSmem = 1024 + kQBytes + kKS * kKRaw + kVS * kVRaw + kCKS * kKTile + kCVS * kVTile;
+  static constexpr int kSmem = 1024 + kQBytes + kKS * kKRaw + kVS * kVRaw + kCVS * kVTile;
   static constexpr uint32_t kOCol = kT5SBuf * kN;             // O after the S buffers
   static_assert(kOCol + 128 <= 256, "TMEM budget");
   static_assert(kVPT == 2, "V stages per tile");
@@ -236,6 +246,13 @@ __device__ __forceinline__ void t5_mma_ts(uint32_t d, uint32_t a, uint64_t b, ui
 __device__ __forceinline__ void t5_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// kind::f8f6f4 (e4m3 A and B, 32 elements of K per MMA), A from shared memory
+__device__ __forceinline__ void t5_mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
                "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
@@ -506,18 +523,19 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *
 }
 
 // One query row into shared memory as the K-major, 128-byte-swizzled A
-// operand of Q K^T: two head-dim halves of QR rows of 128 bytes, the 16-byte
-// chunks of row r at chunk index ^ (r % 8); a row past R (src null) is zeros.
-// FP8: f16 pairs of q 2^s, s chosen so that the row's largest |q| lies in
-// [2^14, 2^15): the f16 range then holds the whole row with no overflow (a
-// bf16 |q| may exceed f16's 65504), every bf16 value is exact, and 2^-s and
-// k_scale fold into the row's score scale, which is returned (values below
-// 2^-31 of the maximum lose bits in the f16 subnormals; their products are
-// far below the fp32 sum's rounding). Two passes over the row (the second
-// from L1) keep few registers live.
+// operand of Q K^T; a row past R (src null) is zeros.
+// bf16: two head-dim halves of QR rows of 128 bytes, the 16-byte chunks of
+// row r at chunk index ^ (r % 8).
+// FP8: the row times 2^s, s chosen so that its largest |q| lies in
+// [2^7, 2^8) (inside e4m3's range), as two e4m3 terms: hi = e4m3(y) and
+// lo = e4m3(y - hi), each QR rows of 128 bytes (all 128 head dims), so that
+// hi + lo carries the 8 significant bits of a bf16 value (elements below
+// 2^-11 of the row's largest lose bits in e4m3's subnormals; their products
+// are far below the fp32 sum's rounding). k_scale 2^-s folds into the
+// row's score scale, which is returned. Two passes over the row (the second
+// from L1).
 template <int QR, bool FP8>
 __device__ __forceinline__ float t5_store_q(uint32_t q_smem, int row, const uint4 *src, float k_scale) {
-  float fold = 1.f, up = 1.f;
   if constexpr (FP8) {
     float amax = 0.f;
     if (src) {
@@ -530,25 +548,53 @@ __device__ __forceinline__ float t5_store_q(uint32_t q_smem, int row, const uint
           amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xffff0000u))));
       }
     }
-    const int ex = amax > 0.f ? max(-112, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
-    up = __uint_as_float((uint32_t)(127 + 14 - ex) << 23);                  // 2^s, s = 14 - ex
-    fold = k_scale * __uint_as_float((uint32_t)(127 - 14 + ex) << 23);      // k_scale 2^-s
-  }
+    const int ex = amax > 0.f ? max(-100, (int)((__float_as_uint(amax) >> 23) & 0xff) - 127) : 0;
+    const float up = __uint_as_float((uint32_t)(127 + 7 - ex) << 23);   // 2^s, s = 7 - ex
+    const float fold = k_scale * __uint_as_float((uint32_t)(127 - 7 + ex) << 23);
+#pragma unroll 2
+    for (int j = 0; j < 8; ++j) {   // 16 head dims: one 16-byte chunk of each term
+      const uint4 v0 = src ? __ldg(src + 2 * j) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 v1 = src ? __ldg(src + 2 * j + 1) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t hi[4], lo[4];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    uint4 v = src ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (FP8) {
-      auto widen = [up](uint32_t w) {
-        return pack2<true>(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
-      };
-      v = make_uint4(widen(v.x), widen(v.y), widen(v.z), widen(v.w));
+      for (int e = 0; e < 4; ++e) {
+        uint32_t hp[2], lp[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ww = w[2 * e + h];
+          const float y0 = __uint_as_float(ww << 16) * up, y1 = __uint_as_float(ww & 0xffff0000u) * up;
+          const uint32_t c = f32x2_to_e4m3x2(y0, y1);
+          const uint32_t f = e4m3x2_to_f16x2((uint16_t)c);
+          const float2 hv = __half22float2(*reinterpret_cast<const __half2 *>(&f));
+          hp[h] = c;
+          lp[h] = f32x2_to_e4m3x2(y0 - hv.x, y1 - hv.y);
+        }
+        hi[e] = hp[0] | (hp[1] << 16);
+        lo[e] = lp[0] | (lp[1] << 16);
+      }
+      const uint32_t off = row * 128 + ((j ^ (row & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(q_smem + off), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]),
+                   "r"(hi[3])
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(q_smem + QR * 128 + off), "r"(lo[0]), "r"(lo[1]),
+                   "r"(lo[2]), "r"(lo[3])
+                   : "memory");
     }
-    const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    // the tensor cores read it through the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    return fold;
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = src ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t qa = q_smem + (c >> 3) * (QR * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qa), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+    }
+    // the tensor cores read it through the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    return 1.f;
   }
-  // the tensor cores read it through the async proxy
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  return fold;
 }
 
 template <int QR, bool FP8>
@@ -557,14 +603,14 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
-  constexpr int CKS = Cfg::kCKS > 0 ? Cfg::kCKS : 1, CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
+  constexpr int CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
   constexpr int SW = Cfg::kSoftW, CW = Cfg::kConvW;
   constexpr int TB = Cfg::kBlk, TN = Cfg::kN, VPT = Cfg::kVPT;
   constexpr uint32_t OC = Cfg::kOCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
-  // FP8: widened stages, filled by the converter warps, freed by the MMAs
-  __shared__ __align__(8) uint64_t kc_full[CKS], kc_empty[CKS], vc_full[CVS], vc_empty[CVS];
+  // FP8: widened V stages, filled by the converter warps, freed by the MMAs
+  __shared__ __align__(8) uint64_t vc_full[CVS], vc_empty[CVS];
   __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -579,9 +625,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   const uint32_t q_smem = smem_u32(smem);   // Q, the A operand of Q K^T
   const uint32_t k_ring = q_smem + Cfg::kQBytes;
   const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
-  // the rings the MMAs read: the widened ones for FP8, else the TMA rings
-  const uint32_t kc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : k_ring;
-  const uint32_t vc_ring = FP8 ? kc_ring + CKS * Cfg::kKTile : v_ring;
+  // the V ring the MMAs read: the widened one for FP8, else the TMA ring
+  const uint32_t vc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : v_ring;
 
   const int L = P.seq_lens[b];
   if (L < P.n_new || L > P.max_blocks * kBS) {
@@ -597,21 +642,17 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   const int R = P.R;
 
   if (tid == 0) {
-    // raw stages are freed by the MMAs (bf16) or by the CW converter warps
-    // (FP8); widened stages are filled by the converter warps
+    // K stages are freed by the MMAs; raw V stages by the MMAs (bf16) or by
+    // the CW converter warps (FP8), whose widened stages the MMAs free
     for (int k = 0; k < KS; ++k) {
       mbar_init(&k_full[k], 1);
-      mbar_init(&k_empty[k], FP8 ? CW : 1);
+      mbar_init(&k_empty[k], 1);
     }
     for (int k = 0; k < VS; ++k) {
       mbar_init(&v_full[k], 1);
       mbar_init(&v_empty[k], FP8 ? CW : 1);
     }
     if (FP8) {
-      for (int k = 0; k < CKS; ++k) {
-        mbar_init(&kc_full[k], CW);
-        mbar_init(&kc_empty[k], 1);
-      }
       for (int k = 0; k < CVS; ++k) {
         mbar_init(&vc_full[k], CW);
         mbar_init(&vc_empty[k], 1);
@@ -717,7 +758,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     if (warp == kT5MmaWarp) {
       // ---------------------------------------------------------- MMA issuer --
       if (lane == 0) {
-        // f32 accumulators; A and B bf16 (formats 1), or f16 for FP8 (0)
+        // f32 accumulators; A and B bf16 (formats 1), or for FP8 e4m3 in Q K^T
+        // (kind::f8f6f4, format 0) and f16 in P V (format 0)
         constexpr uint32_t ab = FP8 ? 0u : (1u << 7) | (1u << 10);
         const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(TN >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
@@ -729,24 +771,29 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
           bool progressed = false;
           if (!q_ready) q_ready = t5_test(&q_full, 0);
           if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
-            // K stage: the TMA ring (bf16) or the widened ring (FP8)
-            const int KR = FP8 ? CKS : KS;
+            // K stage: the TMA ring (raw e4m3 codes for FP8)
+            const int KR = KS;
             const int ks = tq % KR, sb = tq % kT5SBuf;
-            uint64_t *kf = FP8 ? kc_full : k_full;
+            uint64_t *kf = k_full;
             // S buffer sb is free once the P V of tile tq - kT5SBuf has run
             const bool sfree = tq < kT5SBuf || t5_test(&o_done[sb], ((tq / kT5SBuf) - 1) & 1);
             if (sfree && t5_test(&kf[ks], (tq / KR) & 1)) {
               t5_fence_after();
-              const uint32_t kb = kc_ring + ks * Cfg::kKTile;
+              const uint32_t kb = k_ring + ks * Cfg::kKRaw;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {   // 16 head dims per step
-                // A = Q and B = K from shared memory
-                t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024),
-                          t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024), idesc_qk,
-                          kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk) {
+                // A = Q and B = K from shared memory. bf16: 16 head dims per step over
+                // the two head-dim halves; FP8: 32 head dims per step, the hi term of Q
+                // (kk < 4) then the lo term, against the raw codes
+                const uint64_t ad = t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024);
+                if constexpr (FP8)
+                  t5_mma_ss_f8(tb + sb * TN, ad, t5_desc(kb + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                else
+                  t5_mma_ss(tb + sb * TN, ad, t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024), idesc_qk,
+                            kk > 0 ? 1u : 0u);
               }
               t5_commit(&s_full[sb]);
-              t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
+              t5_commit(&k_empty[ks]);
               ++tq;
               progressed = true;
             }
@@ -988,20 +1035,20 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     // + 32 CW j is key row q / 8, head dims 16 (q % 8) .. + 15, and lands as
     // two 16-byte chunks of one head-dim half of the f16 stage. Rows of keys
     // past the split or the sequence are written as zeros.
-    const bool isk = warp == 7 || (CW == 2 && warp == 2);
-    const bool isv = warp == 8 || (CW == 2 && warp == 3);
-    if (isk || isv) {
-      const int cw = (warp == 7 || warp == 8) ? 0 : 1;
-      const int NS = isv ? VS : KS, NC = isv ? CVS : CKS;
-      const int sblk = isv ? kT5Blk : TB;   // blocks per stage
-      const uint32_t rbytes = isv ? Cfg::kVRaw : Cfg::kKRaw, cbytes = isv ? Cfg::kVTile : Cfg::kKTile;
-      const uint32_t chalf = isv ? Cfg::kVHalf : Cfg::kKHalf;
-      uint64_t *rfull = isv ? v_full : k_full;
-      uint64_t *rempty = isv ? v_empty : k_empty;
-      uint64_t *cfull = isv ? vc_full : kc_full;
-      uint64_t *cempty = isv ? vc_empty : kc_empty;
-      const uint32_t rring = isv ? v_ring : k_ring;
-      const uint32_t cring = isv ? vc_ring : kc_ring;
+    // converter index: warps 8, 7 (and 3, 2 when the softmax needs two warps)
+    const int cw = warp == 8 ? 0 : (warp == 7 ? 1 : (warp == 3 ? 2 : (warp == 2 ? 3 : CW)));
+    if (cw < CW) {
+      const bool isv = true;   // only V is widened
+      const int NS = VS, NC = CVS;
+      const int sblk = kT5Blk;   // blocks per stage
+      const uint32_t rbytes = Cfg::kVRaw, cbytes = Cfg::kVTile;
+      const uint32_t chalf = Cfg::kVHalf;
+      uint64_t *rfull = v_full;
+      uint64_t *rempty = v_empty;
+      uint64_t *cfull = vc_full;
+      uint64_t *cempty = vc_empty;
+      const uint32_t rring = v_ring;
+      const uint32_t cring = vc_ring;
       const int end_key = min(L, blk1 * kBS);
       const int n_st = n_tiles * (isv ? VPT : 1);
       const int nch = sblk * 128;   // 16-byte chunks of a raw stage
@@ -1070,14 +1117,14 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
   pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
-  constexpr int CKS = Cfg::kCKS > 0 ? Cfg::kCKS : 1, CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
+  constexpr int CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
   constexpr int SW = Cfg::kSoftW, CW = Cfg::kConvW;
   constexpr int TB = Cfg::kBlk, TN = Cfg::kN, VPT = Cfg::kVPT;
   constexpr uint32_t OC = Cfg::kOCol;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
-  // FP8: widened stages, filled by the converter warps, freed by the MMAs
-  __shared__ __align__(8) uint64_t kc_full[CKS], kc_empty[CKS], vc_full[CVS], vc_empty[CVS];
+  // FP8: widened V stages, filled by the converter warps, freed by the MMAs
+  __shared__ __align__(8) uint64_t vc_full[CVS], vc_empty[CVS];
   __shared__ __align__(8) uint64_t s_full[kT5SBuf], p_full[kT5SBuf], o_done[kT5SBuf], mma_drain, q_full;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -1093,27 +1140,22 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
   const uint32_t q_smem = smem_u32(smem);   // Q, the A operand of Q K^T
   const uint32_t k_ring = q_smem + Cfg::kQBytes;
   const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
-  // the rings the MMAs read: the widened ones for FP8, else the TMA rings
-  const uint32_t kc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : k_ring;
-  const uint32_t vc_ring = FP8 ? kc_ring + CKS * Cfg::kKTile : v_ring;
+  // the V ring the MMAs read: the widened one for FP8, else the TMA ring
+  const uint32_t vc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : v_ring;
   const int R = P.R;
 
   if (tid == 0) {
-    // raw stages are freed by the MMAs (bf16) or by the CW converter warps
-    // (FP8); widened stages are filled by the converter warps
+    // K stages are freed by the MMAs; raw V stages by the MMAs (bf16) or by
+    // the CW converter warps (FP8), whose widened stages the MMAs free
     for (int k = 0; k < KS; ++k) {
       mbar_init(&k_full[k], 1);
-      mbar_init(&k_empty[k], FP8 ? CW : 1);
+      mbar_init(&k_empty[k], 1);
     }
     for (int k = 0; k < VS; ++k) {
       mbar_init(&v_full[k], 1);
       mbar_init(&v_empty[k], FP8 ? CW : 1);
     }
     if (FP8) {
-      for (int k = 0; k < CKS; ++k) {
-        mbar_init(&kc_full[k], CW);
-        mbar_init(&kc_empty[k], 1);
-      }
       for (int k = 0; k < CVS; ++k) {
         mbar_init(&vc_full[k], CW);
         mbar_init(&vc_empty[k], 1);
@@ -1227,7 +1269,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
     if (warp == kT5MmaWarp) {
       // ---------------------------------------------------------- MMA issuer --
       if (lane == 0) {
-        // f32 accumulators; A and B bf16 (formats 1), or f16 for FP8 (0)
+        // f32 accumulators; A and B bf16 (formats 1), or for FP8 e4m3 in Q K^T
+        // (kind::f8f6f4, format 0) and f16 in P V (format 0)
         constexpr uint32_t ab = FP8 ? 0u : (1u << 7) | (1u << 10);
         const uint32_t idesc_qk = (1u << 4) | ab | ((uint32_t)(TN >> 3) << 17) | (8u << 24);
         const uint32_t idesc_pv = (1u << 4) | ab | (1u << 16) | (16u << 17) | (8u << 24);
@@ -1250,25 +1293,30 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
             bool progressed = false;
             if (!q_ready) q_ready = t5_test(&q_full, xq & 1);
             if (q_ready && tq < n_tiles && tq - tp < kT5SBuf) {
-              // K stage: the TMA ring (bf16) or the widened ring (FP8)
-              const int KR = FP8 ? CKS : KS;
+              // K stage: the TMA ring (raw e4m3 codes for FP8)
+              const int KR = KS;
               const int uq = u0 + tq;
               const int ks = uq % KR, sb = uq % kT5SBuf;
-              uint64_t *kf = FP8 ? kc_full : k_full;
+              uint64_t *kf = k_full;
               // S buffer sb is free once the P V of tile uq - kT5SBuf has run
               const bool sfree = uq < kT5SBuf || t5_test(&o_done[sb], ((uq / kT5SBuf) - 1) & 1);
               if (sfree && t5_test(&kf[ks], (uq / KR) & 1)) {
                 t5_fence_after();
-                const uint32_t kb = kc_ring + ks * Cfg::kKTile;
+                const uint32_t kb = k_ring + ks * Cfg::kKRaw;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {   // 16 head dims per step
-                  // A = Q and B = K from shared memory
-                  t5_mma_ss(tb + sb * TN, t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024),
-                            t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024), idesc_qk,
-                            kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                  // A = Q and B = K from shared memory. bf16: 16 head dims per step over
+                  // the two head-dim halves; FP8: 32 head dims per step, the hi term of Q
+                  // (kk < 4) then the lo term, against the raw codes
+                  const uint64_t ad = t5_desc(q_smem + (kk >> 2) * (QR * 128) + (kk & 3) * 32, 16, 1024);
+                  if constexpr (FP8)
+                    t5_mma_ss_f8(tb + sb * TN, ad, t5_desc(kb + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                  else
+                    t5_mma_ss(tb + sb * TN, ad, t5_desc(kb + (kk >> 2) * Cfg::kKHalf + (kk & 3) * 32, 16, 1024), idesc_qk,
+                              kk > 0 ? 1u : 0u);
                 }
                 t5_commit(&s_full[sb]);
-                t5_commit(FP8 ? &kc_empty[ks] : &k_empty[ks]);
+                t5_commit(&k_empty[ks]);
                 ++tq;
                 progressed = true;
               }
@@ -1524,20 +1572,20 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
     // as in attn_tc5_kernel, over the CTA's items: the running stage count
     // indexes the rings, and rows of keys past the item or the sequence are
     // written as zeros
-    const bool isk = warp == 7 || (CW == 2 && warp == 2);
-    const bool isv = warp == 8 || (CW == 2 && warp == 3);
-    if (isk || isv) {
-      const int cw = (warp == 7 || warp == 8) ? 0 : 1;
-      const int NS = isv ? VS : KS, NC = isv ? CVS : CKS;
-      const int sblk = isv ? kT5Blk : TB;   // blocks per stage
-      const uint32_t rbytes = isv ? Cfg::kVRaw : Cfg::kKRaw, cbytes = isv ? Cfg::kVTile : Cfg::kKTile;
-      const uint32_t chalf = isv ? Cfg::kVHalf : Cfg::kKHalf;
-      uint64_t *rfull = isv ? v_full : k_full;
-      uint64_t *rempty = isv ? v_empty : k_empty;
-      uint64_t *cfull = isv ? vc_full : kc_full;
-      uint64_t *cempty = isv ? vc_empty : kc_empty;
-      const uint32_t rring = isv ? v_ring : k_ring;
-      const uint32_t cring = isv ? vc_ring : kc_ring;
+    // converter index: warps 8, 7 (and 3, 2 when the softmax needs two warps)
+    const int cw = warp == 8 ? 0 : (warp == 7 ? 1 : (warp == 3 ? 2 : (warp == 2 ? 3 : CW)));
+    if (cw < CW) {
+      const bool isv = true;   // only V is widened
+      const int NS = VS, NC = CVS;
+      const int sblk = kT5Blk;   // blocks per stage
+      const uint32_t rbytes = Cfg::kVRaw, cbytes = Cfg::kVTile;
+      const uint32_t chalf = Cfg::kVHalf;
+      uint64_t *rfull = v_full;
+      uint64_t *rempty = v_empty;
+      uint64_t *cfull = vc_full;
+      uint64_t *cempty = vc_empty;
+      const uint32_t rring = v_ring;
+      const uint32_t cring = vc_ring;
       const int nch = sblk * 128;   // 16-byte chunks of a raw stage
       T5Walk wk = {};
       T5Item it;
