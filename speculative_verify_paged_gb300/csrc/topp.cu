@@ -809,13 +809,15 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
       const float x = TT::val(TT::get(r, k));
       float d, h, y;
       const int fb = bin_of(x, d, h, y);
-      if (fb < kTbBins - 1) {
+      {
+        // branch-free: the last bin (which also takes -inf and NaN) adds zeros
+        const bool in = fb < kTbBins - 1;
         const float rr = fmaf(y - 8388608.f, 0.0078125f, h);   // h + fb / 128, exact
         const float t = tp_ex2(rr);
         const float v = fmaf(t, lo_of(x, d, h) * 0.693147180559945309f, t);
         const int q = (int)__float_as_uint(fmaf(v, 4194304.f, 8388608.f)) - 0x4B400000;
-        atomicAdd(&cnt[fb], 1u);
-        atomicAdd(&dsum[fb], q);
+        atomicAdd(&cnt[fb], in ? 1u : 0u);
+        atomicAdd(&dsum[fb], in ? q : 0);
       }
     }
   });
