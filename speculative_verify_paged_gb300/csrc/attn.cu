@@ -529,9 +529,9 @@ __global__ void __launch_bounds__(kPartThreads) attn_part_kernel(const int32_t *
 // FP8: the row times 2^s, s chosen so that its largest |q| lies in
 // [2^7, 2^8) (inside e4m3's range), as two e4m3 terms: hi = e4m3(y) and
 // lo = e4m3(y - hi), each QR rows of 128 bytes (all 128 head dims), so that
-// hi + lo carries the 8 significant bits of a bf16 value (elements below
-// 2^-11 of the row's largest lose bits in e4m3's subnormals; their products
-// are far below the fp32 sum's rounding). k_scale 2^-s folds into the
+// hi + lo carries the 8 significant bits of a bf16 value exactly for
+// |y| >= 2^-2, i.e. down to 2^-9 of the row's largest element (smaller ones
+// lose bits in e4m3's subnormals, an error below 2^-17 of the largest). k_scale 2^-s folds into the
 // row's score scale, which is returned. Two passes over the row (the second
 // from L1).
 template <int QR, bool FP8>
