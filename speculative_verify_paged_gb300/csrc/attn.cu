@@ -159,8 +159,8 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 // threads (288 for fp8 caches):
 //   warps 0-3  softmax warpgroup; thread w*32+l owns query row w*32+l
 //              (TMEM lane w*32+l: warp w may only touch lanes 32w..32w+31)
-//              and first writes that row of Q (into shared memory for bf16
-//              caches, into TMEM for fp8 ones)
+//              and first writes that row of Q into shared memory (fp8
+//              caches with at most 64 rows: warps 0-1; warps 2-3 widen V)
 //   warps 4, 5 TMA producers (one lane each, in separate warps so that neither
 //              waits behind the other's barrier): warp 4 streams K tiles,
 //              warp 5 V stages, each into its own shared-memory ring (a K
@@ -170,7 +170,7 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 //              Q K^T runs ahead whenever K data and an S buffer are ready.
 //              It sits on the third scheduler (warp id % 4 = 2), away from
 //              the softmax warps that own rows 0-63.
-//   warp 7     idle (fp8 caches: widens K tiles to f16; warp 8 widens V)
+//   warp 7     idle (fp8 caches: it and warp 8 widen V stages to f16)
 // A tile is Cfg::kBlk paged blocks (N = 16 kBlk keys). Per tile t, with
 // buffer u = t % kT5SBuf:
 //   S[u] = Q K^T           (M=128 padded query rows, N keys, K=128)
@@ -1028,17 +1028,16 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     }
   }
   if constexpr (FP8) {
-    // ----------------------------------------------------- e4m3 -> f16 ---
-    // K stages: warp 7 (and warp 2), V stages: warp 8 (and warp 3). A raw
-    // stage is blocks of 16 slots x 128 codes (128-byte swizzle); the CW
-    // warps of a direction share its 16-byte chunks: chunk q = 32 cw + lane
-    // + 32 CW j is key row q / 8, head dims 16 (q % 8) .. + 15, and lands as
-    // two 16-byte chunks of one head-dim half of the f16 stage. Rows of keys
-    // past the split or the sequence are written as zeros.
-    // converter index: warps 8, 7 (and 3, 2 when the softmax needs two warps)
+    // -------------------------------------------------- V: e4m3 -> f16 ---
+    // Converter warps 8 and 7 (and 3 and 2 when the softmax needs two warps)
+    // widen the V stages. A raw stage is two blocks of 16 slots x 128 codes
+    // (128-byte swizzle); the CW warps share its 16-byte chunks: chunk
+    // q = 32 cw + lane + 32 CW j is key row q / 8, head dims 16 (q % 8) ..
+    // + 15, and lands as two 16-byte chunks of one head-dim half of the f16
+    // stage. Rows of keys past the split or the sequence are written as
+    // zeros.
     const int cw = warp == 8 ? 0 : (warp == 7 ? 1 : (warp == 3 ? 2 : (warp == 2 ? 3 : CW)));
     if (cw < CW) {
-      const bool isv = true;   // only V is widened
       const int NS = VS, NC = CVS;
       const int sblk = kT5Blk;   // blocks per stage
       const uint32_t rbytes = Cfg::kVRaw, cbytes = Cfg::kVTile;
@@ -1050,7 +1049,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       const uint32_t rring = v_ring;
       const uint32_t cring = vc_ring;
       const int end_key = min(L, blk1 * kBS);
-      const int n_st = n_tiles * (isv ? VPT : 1);
+      const int n_st = n_tiles * VPT;
       const int nch = sblk * 128;   // 16-byte chunks of a raw stage
       for (int i = 0; i < n_st; ++i) {
         const int rs = i % NS, cs = i % NC;
@@ -1568,14 +1567,12 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
     }
   }
   if constexpr (FP8) {
-    // ----------------------------------------------------- e4m3 -> f16 ---
+    // -------------------------------------------------- V: e4m3 -> f16 ---
     // as in attn_tc5_kernel, over the CTA's items: the running stage count
     // indexes the rings, and rows of keys past the item or the sequence are
     // written as zeros
-    // converter index: warps 8, 7 (and 3, 2 when the softmax needs two warps)
     const int cw = warp == 8 ? 0 : (warp == 7 ? 1 : (warp == 3 ? 2 : (warp == 2 ? 3 : CW)));
     if (cw < CW) {
-      const bool isv = true;   // only V is widened
       const int NS = VS, NC = CVS;
       const int sblk = kT5Blk;   // blocks per stage
       const uint32_t rbytes = Cfg::kVRaw, cbytes = Cfg::kVTile;
@@ -1593,7 +1590,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
       bool ok = true;
       while (ok && t5_item(P, wk, it)) {
         const int end_key = min(it.L, it.blk1 * kBS);
-        const int n_st = (it.blk1 - it.blk0 + TB - 1) / TB * (isv ? VPT : 1);
+        const int n_st = (it.blk1 - it.blk0 + TB - 1) / TB * VPT;
         for (int q0 = 0; q0 < n_st; ++q0, ++i) {
           const int rs = i % NS, cs = i % NC;
           ok = __all_sync(0xffffffffu, t5_wait(&rfull[rs], (i / NS) & 1, abf, P.wait_ns));
