@@ -212,7 +212,7 @@ sv_status spec_verify_attn(const void *q, sv_dtype q_dtype,
  * sequence are cut into chunks of blocks_per_split blocks that run in
  * parallel and are merged by log-sum-exp. blocks_per_split = 0 asks for
  * balanced ranges instead (tensor-core path; other paths take their default
- * split): the 32-key tiles of all sequences, end to end, are cut into equal
+ * split): the 64-key tiles of all sequences, end to end, are cut into equal
  * ranges, one per CTA slot (two per SM) and kv head, whatever the lengths;
  * this suits small batches of very uneven lengths. The result does not
  * depend on the split size up to rounding; the workspace must hold
