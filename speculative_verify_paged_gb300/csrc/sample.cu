@@ -453,11 +453,12 @@ __device__ __forceinline__ float max8(const Raw8<T> &r) {
   }
 }
 
-// 16-bit logits with draft logits: five CTAs per SM (8B shape 23.2 -> 22.2 us, 70B 71.4 ->
-// 70.8 us per call); the others keep the compiler's register budget (five
-// CTAs spill fp32 rows: 277 -> 373 us on the fp8 workload)
+// Resident CTAs per SM: five for 16-bit logits with draft logits (8B shape
+// 23.2 -> 22.2 us per sampling call, 70B 71.4 -> 70.8 us), three for the
+// others (fp32 rows spill at five: 277 -> 373 us on the fp8 workload, and
+// reach 88 registers, two CTAs, with no bound: 300 us)
 template <typename TT, int DK>
-__global__ void __launch_bounds__(kStatThreads, sizeof(TT) == 2 && DK == 0 ? 5 : 1)
+__global__ void __launch_bounds__(kStatThreads, sizeof(TT) == 2 && DK == 0 ? 5 : 3)
     sample_stats_kernel(const __grid_constant__ SampleParams P) {
   pdl_wait();
   pdl_trigger();
