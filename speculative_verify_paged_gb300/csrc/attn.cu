@@ -358,9 +358,11 @@ __device__ __forceinline__ bool t5_item(const TcParams &P, T5Walk &w, T5Item &it
 // It reads only seq_lens and writes only its own part of the workspace, so
 // it runs while the previous kernel of the stream is still running (that
 // kernel passed its own wait, so everything before it has completed; the
-// library's kernels never write seq_lens). It waits for that kernel at its
-// end, so the attention kernel's wait on this one still covers, for
-// example, the K/V rows the append kernel writes.
+// library's kernels never write seq_lens; an attention kernel of the
+// previous call lets the next kernel start only once each of its CTAs has
+// read its item from this order). It waits for that kernel at its end, so
+// the attention kernel's wait on this one still covers, for example, the
+// K/V rows the append kernel writes.
 constexpr int kOrdThreads = 1024;
 constexpr int kOrdMaxTiles = 1023;   // buckets 0..kOrdMaxTiles
 constexpr int kOrdPairs = 4;         // (s, b) pairs a thread keeps in registers
@@ -600,7 +602,6 @@ __device__ __forceinline__ float t5_store_q(uint32_t q_smem, int row, const uint
 template <int QR, bool FP8>
 __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
   pdl_wait();
-  pdl_trigger();
   using Cfg = T5Cfg<QR, FP8>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
   constexpr int CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
@@ -619,6 +620,9 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   // order the order kernel wrote (the CTAs launched first take the longest
   // splits, so the last wave is made of the shortest ones)
   const int item = __ldg(P.order + blockIdx.x);
+  // the next kernel of the stream may start (and the next call's order
+  // kernel overwrite the order) only once every CTA has read its item
+  pdl_trigger();
   const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -151,9 +151,11 @@ def test_attention_fp8_queries_outside_the_f16_range(lib, shift):
     check_attention(out, ref, cfg)
 
 
-@pytest.mark.parametrize("bps", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("bps", [1, 2, 3, 7, 8, 64])
 @pytest.mark.parametrize("kv", ["f32", "bf16", "fp8_e4m3"])
 def test_attention_split_count_invariance(lib, bps, kv):
+    # (bps 8: two splits of the 250-token sequence, merged by the attention
+    # kernel's last split on the tensor-core path)
     q = "f32" if kv == "f32" else "bf16"
     d = 64 if kv == "f32" else 128
     cfg = workloads.CONFIGS["tiny"].with_(kv_dtype=kv, q_dtype=q, d_head=d, ctx=("fixed", (77, 250)))
@@ -169,7 +171,7 @@ def test_attention_split_count_invariance(lib, bps, kv):
     assert ((out.float() - base.float()).abs() <= tol + ulp * base.float().abs()).all()
 
 
-@pytest.mark.parametrize("bps", [None, 0, 5])
+@pytest.mark.parametrize("bps", [None, 0, 5, 8])
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
 def test_attention_ragged_last_tiles(lib, bps, kv):
     # lengths whose last tile (64 keys for bf16 caches, 32 for fp8) holds 1
