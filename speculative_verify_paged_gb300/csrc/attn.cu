@@ -118,7 +118,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 struct TcParams {   // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmk;
   CUtensorMap tmv;
-  CUtensorMap tmq;   // q [B][n_new][H_q][d]: a box is one head-dim half of a GQA group's rows
   const void *q;
   void *out;       // [B][n_new][H_q][kD] bf16, written directly when a sequence has one split
   const float *k_scale;
@@ -2440,20 +2439,8 @@ static sv_status attn_impl(const void *q, sv_dtype q_dtype, const void *k_cache,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
-    if (!fp8) {
-      // q [B][n_new][H_q][d]: box = 64 dims x G heads x n_new positions of one
-      // batch entry, i.e. one head-dim half of the group's (K+1) G rows
-      if (!aligned(q, 16)) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: q must be 16-byte aligned");
-      cuuint64_t qd[4] = {(cuuint64_t)d_head, (cuuint64_t)H_q, (cuuint64_t)n_new, (cuuint64_t)B};
-      cuuint64_t qs[3] = {(cuuint64_t)d_head * 2, (cuuint64_t)H_q * d_head * 2, (cuuint64_t)n_new * H_q * d_head * 2};
-      cuuint32_t qb[4] = {64, (cuuint32_t)G, (cuuint32_t)n_new, 1};
-      if (G > 256 || n_new > 256)
-        return fail(SV_ERR_UNSUPPORTED, "spec_verify_attn: query group too large for the tensor-core path");
-      CUresult r = enc(&P.tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), qd, qs, qb, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (r != CUDA_SUCCESS) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
-    }
+    // the softmax warps read their Q rows with 16-byte loads
+    if (!aligned(q, 16)) return fail(SV_ERR_INVALID_ARG, "spec_verify_attn: q must be 16-byte aligned");
     P.q = q; P.out = out; P.k_scale = k_scale; P.v_scale = v_scale; P.block_table = block_table; P.seq_lens = seq_lens;
     P.ws_acc = ws_acc; P.ws_ml = ws_ml; P.status = dev_status; P.anc = anc;
     uint8_t *tail = reinterpret_cast<uint8_t *>(ws_ml) + align_up(ent * 2 * sizeof(float), 256);
