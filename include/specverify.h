@@ -185,9 +185,10 @@ sv_status kv_tree_commit(void *k_cache, void *v_cache, sv_dtype kv_dtype, const 
  *   Supported: kv_dtype SV_F32 with q/out SV_F32, or kv_dtype SV_BF16 /
  *   SV_FP8_E4M3 with q/out SV_BF16; d_head a multiple of 4 and <= 256; any
  *   block_size. The tensor-core kernel takes bf16 / fp8 caches with
- *   d_head 128, block_size 16, (H_q/H_kv) * n_new <= 64 and pool strides
- *   that are multiples of 16 bytes; every other supported shape runs on a
- *   CUDA-core kernel with fp32 arithmetic.
+ *   d_head 128, block_size 16, (H_q/H_kv) * n_new <= 128 and pool strides
+ *   that are multiples of 16 bytes (q must then be 16-byte aligned, else
+ *   SV_ERR_INVALID_ARG); every other supported shape runs on a CUDA-core
+ *   kernel with fp32 arithmetic.
  *   fp8 pools hold e4m3 codes; the key / value is code * k_scale[g] /
  *   code * v_scale[g] (k_scale, v_scale: float [H_kv] on the device).
  *   workspace: at least spec_verify_attn_workspace_size(...) bytes of device
