@@ -179,7 +179,7 @@ __device__ __forceinline__ void tile_coords(const TcParams &P, int g, int phys, 
 // phase behind its barrier.
 // Shared-memory operands use the 128-byte swizzle: Q and K are K-major (head
 // dim contiguous), V is MN-major (head dim contiguous along N).
-constexpr int kT5Blk = 2;                      // blocks of a 32-key unit (V stages, fp8 tiles, work counts)
+constexpr int kT5Blk = 2;                      // blocks of a 32-key unit (V stages, the order's work counts)
 constexpr int kT5SBuf = 2;                     // S / P buffers in TMEM
 constexpr int kT5MmaWarp = 6;
 constexpr int kT5MaxR = 128;
@@ -2231,7 +2231,7 @@ Plan make_plan(int B, int n_new, int H_q, int H_kv, int d, int max_blocks, int b
     // blocks: the longest-first order balances the slots and no merge runs.
     // With fewer pairs, floor(slots / pairs) splits per pair, so the CTAs of
     // equal-length sequences fill the slots once (a block count that is a
-    // multiple of 4 keeps the 64-key and 32-key tiles whole).
+    // multiple of 4 keeps the 64-key tiles whole).
     if (pairs >= slots) {
       p.bps = std::min(max_blocks, 512);
     } else {
