@@ -94,7 +94,8 @@ enum {
   SV_DEV_BAD_TOKEN = 4,     /* draft token outside [0, V)                             */
   SV_DEV_TIMEOUT = 8,       /* a bounded wait on an asynchronous copy ran out        */
   SV_DEV_NONFINITE = 16,    /* a logit row's maximum is not finite                   */
-  SV_DEV_BAD_TREE = 32      /* a draft-tree parent index is not a valid BFS parent   */
+  SV_DEV_BAD_TREE = 32,     /* a draft-tree parent index is not a valid BFS parent   */
+  SV_DEV_BAD_WORK = 64      /* a work-list entry the library wrote is out of range   */
 };
 
 /* Strides of the paged pools in elements (d_head is contiguous). Each must be

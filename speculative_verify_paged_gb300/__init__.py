@@ -32,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SV_F32, SV_BF16, SV_F16, SV_FP8_E4M3 = 0, 1, 2, 3
 SV_SAMPLE_FORCE_EXACT = 1
 DEV_STATUS_BITS = {1: "BAD_SEQ_LEN", 2: "BAD_BLOCK", 4: "BAD_TOKEN", 8: "TIMEOUT", 16: "NONFINITE",
-                   32: "BAD_TREE"}
+                   32: "BAD_TREE", 64: "BAD_WORK"}
 _STATUS = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_WORKSPACE",
            4: "SV_ERR_CUDA", 5: "SV_ERR_TIMEOUT", 6: "SV_ERR_OUT_OF_BLOCKS"}
 SV_ERR_OUT_OF_BLOCKS = 6

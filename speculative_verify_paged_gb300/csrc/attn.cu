@@ -322,7 +322,7 @@ struct T5Walk {
 
 __device__ __forceinline__ bool t5_item(const TcParams &P, T5Walk &w, T5Item &it) {
   if (w.idx == 0) {
-    const int4 wk = __ldg(P.work + blockIdx.x / P.H_kv);
+    const int4 wk = P.work[blockIdx.x / P.H_kv];   // written by the partition kernel
     w.b = wk.x; w.g = (int)(blockIdx.x % P.H_kv); w.off = wk.z; w.left = wk.w;
   }
   if (w.left <= 0) return false;
@@ -600,7 +600,6 @@ __device__ __forceinline__ float t5_store_q(uint32_t q_smem, int row, const uint
 
 template <int QR, bool FP8>
 __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(const __grid_constant__ TcParams P) {
-  pdl_wait();
   using Cfg = T5Cfg<QR, FP8>;
   constexpr int KS = Cfg::kKS, VS = Cfg::kVS;
   constexpr int CVS = Cfg::kCVS > 0 ? Cfg::kCVS : 1;
@@ -615,35 +614,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  // the work item: split s of kv head g of sequence b, in the longest-first
-  // order the order kernel wrote (the CTAs launched first take the longest
-  // splits, so the last wave is made of the shortest ones)
-  const int item = __ldg(P.order + blockIdx.x);
-  // the next kernel of the stream may start (and the next call's order
-  // kernel overwrite the order) only once every CTA has read its item
-  pdl_trigger();
-  const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t q_smem = smem_u32(smem);   // Q, the A operand of Q K^T
-  const uint32_t k_ring = q_smem + Cfg::kQBytes;
-  const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
-  // the V ring the MMAs read: the widened one for FP8, else the TMA ring
-  const uint32_t vc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : v_ring;
-
-  const int L = P.seq_lens[b];
-  if (L < P.n_new || L > P.max_blocks * kBS) {
-    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
-    return;
-  }
-  const int nblk = (L + kBS - 1) / kBS;
-  const int blk0 = s * P.bps;
-  if (blk0 >= nblk) return;   // the merge never reads this split
-  const int blk1 = min(nblk, blk0 + P.bps);
-  const int nblocks = blk1 - blk0;
-  const int n_tiles = (nblocks + TB - 1) / TB;
-  const int R = P.R;
-
   if (tid == 0) {
     // K stages are freed by the MMAs; raw V stages by the MMAs (bf16) or by
     // the CW converter warps (FP8), whose widened stages the MMAs free
@@ -671,6 +642,53 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
     abort_flag = 0;
     fence_mbarrier_init();
   }
+  // (the barriers live in shared memory: set up while the previous kernel
+  // of the stream finishes)
+  pdl_wait();
+  // the work item: split s of kv head g of sequence b, in the longest-first
+  // order the order kernel wrote (the CTAs launched first take the longest
+  // splits, so the last wave is made of the shortest ones)
+  // (a plain load: the order kernel may still have been writing the order
+  // when this CTA started, so it is not read-only data for this kernel)
+  const int item = P.order[blockIdx.x];
+  // the next kernel of the stream may start (and the next call's order
+  // kernel overwrite the order) only once every CTA has read its item
+  pdl_trigger();
+  if (item < 0 || item >= (int)gridDim.x) {
+    if (threadIdx.x == 0) atomic_or_status(P.status, SV_DEV_BAD_WORK);
+    return;
+  }
+  const int s = item % P.S, g = (item / P.S) % P.H_kv, b = item / (P.S * P.H_kv);
+  // the producers read the split's first 64 block-table entries alongside
+  // the sequence length (the row is max_blocks entries long; entries past
+  // the sequence are read but never used)
+  int tab_cur = 0, tab_nxt = 0;
+  if (warp == 4 || warp == 5) {
+    const int avail = P.max_blocks - s * P.bps;
+    const int32_t *row0 = P.block_table + (int64_t)b * P.max_blocks + (int64_t)s * P.bps;
+    tab_cur = lane < avail ? __ldg(row0 + lane) : 0;
+    tab_nxt = 32 + lane < avail ? __ldg(row0 + 32 + lane) : 0;
+  }
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t q_smem = smem_u32(smem);   // Q, the A operand of Q K^T
+  const uint32_t k_ring = q_smem + Cfg::kQBytes;
+  const uint32_t v_ring = k_ring + KS * Cfg::kKRaw;
+  // the V ring the MMAs read: the widened one for FP8, else the TMA ring
+  const uint32_t vc_ring = FP8 ? v_ring + VS * Cfg::kVRaw : v_ring;
+
+  const int L = P.seq_lens[b];
+  if (L < P.n_new || L > P.max_blocks * kBS) {
+    if (tid == 0 && g == 0 && s == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int nblk = (L + kBS - 1) / kBS;
+  const int blk0 = s * P.bps;
+  if (blk0 >= nblk) return;   // the merge never reads this split
+  const int blk1 = min(nblk, blk0 + P.bps);
+  const int nblocks = blk1 - blk0;
+  const int n_tiles = (nblocks + TB - 1) / TB;
+  const int R = P.R;
+
   __syncthreads();
   volatile int *abf = &abort_flag;
 
@@ -692,8 +710,8 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       const uint32_t ring = isv ? v_ring : k_ring;
       const CUtensorMap *map = isv ? &P.tmv : &P.tmk;
       const int32_t *table = P.block_table + (int64_t)b * P.max_blocks + blk0;
-      int cur = lane < nblocks ? table[lane] : 0;
-      int nxt = 32 + lane < nblocks ? table[32 + lane] : 0;
+      int cur = tab_cur;
+      int nxt = tab_nxt;
       int chunk = 0;
       int issued = 0;
       // (test hook: with the copies withheld every wait on them runs out,
@@ -748,6 +766,20 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       }
     }
   } else if (warp < SW || warp == kT5MmaWarp) {
+    // the softmax warps store Q (their rows) while the MMA warp allocates TMEM
+    float q_fold = 1.f;
+    if (warp < SW) {
+      const int row = tid;
+      const uint4 *src = nullptr;
+      if (row < R) {
+        const int j = row / P.G, hh = row % P.G;
+        src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
+                                              (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
+      }
+      if (row < QR) q_fold = t5_store_q<QR, FP8>(q_smem, row, src, FP8 ? P.k_scale[g] : 1.f);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full);
+    }
     if (warp == kT5MmaWarp) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                    "r"(kT5Cols));
@@ -855,21 +887,9 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
       const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
       const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
       // draft tree: of the new keys, only the row's ancestors are visible
-      const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
+      const uint64_t anc = (P.anc && live) ? P.anc[(int64_t)b * P.n_new + row / P.G] : ~0ull;
       const int end_key = min(L, blk1 * kBS);                 // first key this split does not own
-      float sl2 = P.scale_log2;
-      {
-        const uint4 *src = nullptr;
-        if (live) {
-          const int j = row / P.G, hh = row % P.G;
-          src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.q) +
-                                                (((int64_t)b * P.n_new + j) * P.H_q + (int64_t)g * P.G + hh) * kD);
-        }
-        if (row < QR) sl2 *= t5_store_q<QR, FP8>(q_smem, row, src, FP8 ? P.k_scale[g] : 1.f);
-        t5_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full);
-      }
+      const float sl2 = P.scale_log2 * q_fold;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int t = 0; t < n_tiles && ok; ++t) {
@@ -1391,7 +1411,7 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_bal_kern
         const int n_tiles = (nblocks + TB - 1) / TB;
         const int lim = live ? L - P.n_new + row / P.G : -1;   // last visible key of this row
         // draft tree: of the new keys, only the row's ancestors are visible
-        const uint64_t anc = (P.anc && live) ? __ldg(P.anc + (int64_t)b * P.n_new + row / P.G) : ~0ull;
+        const uint64_t anc = (P.anc && live) ? P.anc[(int64_t)b * P.n_new + row / P.G] : ~0ull;
         const int end_key = min(L, it.blk1 * kBS);             // first key this item does not own
         float sl2 = P.scale_log2;
         {
@@ -1748,7 +1768,7 @@ __global__ void __launch_bounds__(kGenThreads) attn_generic_kernel(const __grid_
       const int t = t0 + lane;
       const int lim = L - P.n_new + r / P.G;
       const int rel = t - (L - P.n_new);
-      const bool in_tree = !P.anc || rel < 0 || ((__ldg(P.anc + (int64_t)b * P.n_new + r / P.G) >> (rel & 63)) & 1ull);
+      const bool in_tree = !P.anc || rel < 0 || ((P.anc[(int64_t)b * P.n_new + r / P.G] >> (rel & 63)) & 1ull);
       float sc = -INFINITY;
       if (t < t_end && t <= lim && in_tree) {
         float acc = 0.f;

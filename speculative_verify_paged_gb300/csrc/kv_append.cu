@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kCmThreads) kv_tree_commit_kernel(const __grid
   const int b = blockIdx.x, tid = threadIdx.x;
   uint8_t *cache = a.cache[blockIdx.y];
   const int L = __ldg(a.seq_lens + b);
-  const int nacc = __ldg(a.nacc + b);
+  const int nacc = a.nacc[b];   // may come from the sampling kernel just before
   if (L < a.n_new || L > a.max_blocks * a.bs || nacc < 0 || nacc > a.n_new - 1) {
     if (tid == 0 && blockIdx.y == 0) atomic_or_status(a.status, SV_DEV_BAD_SEQ_LEN);
     return;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kCmThreads) kv_tree_commit_kernel(const __grid
   __syncthreads();
   const int base = L - a.n_new;
   for (int i = tid; i < nacc; i += kCmThreads) {
-    const int node = __ldg(a.path + (int64_t)b * a.n_new + i);
+    const int node = a.path[(int64_t)b * a.n_new + i];
     const int s = base + node, d = base + 1 + i;
     bool ok = node >= 1 && node < a.n_new;
     int sb = 0, db = 0;

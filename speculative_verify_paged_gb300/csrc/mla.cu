@@ -197,12 +197,16 @@ __global__ void __launch_bounds__(kLThreads, 1) attn_mla_kernel(const __grid_con
   const int hv = blockIdx.x & 1;
   const int mt = (blockIdx.x >> 1) % P.n_mt;
   const int s = (blockIdx.x >> 1) / P.n_mt;
-  const int b = P.order ? __ldg(P.order + blockIdx.y) : (int)blockIdx.y;
+  const int b = P.order ? P.order[blockIdx.y] : (int)blockIdx.y;   // written by the order kernel
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t q_smem = smem_u32(smem);
   const uint32_t ring = q_smem + kLQSm * kLQChunkBytes;
 
+  if (b < 0 || b >= (int)gridDim.y) {   // (both CTAs of a pair share blockIdx.y)
+    if (tid == 0) atomic_or_status(P.status, SV_DEV_BAD_WORK);
+    return;
+  }
   const int L = P.seq_lens[b];
   if (L < P.n_new || L > P.max_blocks * kLBS) {
     if (tid == 0 && blockIdx.x == 0) atomic_or_status(P.status, SV_DEV_BAD_SEQ_LEN);

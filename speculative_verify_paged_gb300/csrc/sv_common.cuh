@@ -208,7 +208,11 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
 // be scheduled while this grid drains. Kernels call both first, except where
 // a kernel reads only inputs no kernel of the library writes (lengths, block
 // table, new K/V rows, logits): those loads may come before the wait, and
-// every write still comes after it.
+// every write still comes after it. Data that the previous kernel writes
+// (a work order, a partition, ancestor masks, accepted counts) is read after
+// the wait with plain loads, never __ldg: that kernel may still have been
+// writing it when this grid started, so it is not read-only data for this
+// grid, and a read-only load may be scheduled as if it were.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
