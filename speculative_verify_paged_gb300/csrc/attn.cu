@@ -126,7 +126,7 @@ struct TcParams {   // 64-byte aligned through its CUtensorMap members
   const int32_t *seq_lens;
   float *ws_acc;   // [B][H_kv][S][R][kD]
   float *ws_ml;    // [B][H_kv][S][R][2]
-  const int32_t *order;   // split mode: work items s + S (g + H_kv b), longest first
+  const int32_t *order;   // split mode: work items s + S (g + H_kv b), longest first (NULL: blockIdx.x)
   const int4 *work;       // balanced mode: per CTA (b, g, first tile, tiles) of its tile range
   int32_t *seq_pre_w;     // balanced mode: first tile of each sequence (written by the partition)
   int4 *split_w;          // balanced mode: (count, T), then the sequences split across CTAs
@@ -647,10 +647,11 @@ __global__ void __launch_bounds__(T5Cfg<QR, FP8>::kThreads, 2) attn_tc5_kernel(c
   pdl_wait();
   // the work item: split s of kv head g of sequence b, in the longest-first
   // order the order kernel wrote (the CTAs launched first take the longest
-  // splits, so the last wave is made of the shortest ones)
+  // splits, so the last wave is made of the shortest ones), or with no
+  // order (a grid that fits the CTA slots at once) item = blockIdx.x
   // (a plain load: the order kernel may still have been writing the order
   // when this CTA started, so it is not read-only data for this kernel)
-  const int item = P.order[blockIdx.x];
+  const int item = P.order ? P.order[blockIdx.x] : (int)blockIdx.x;
   // the next kernel of the stream may start (and the next call's order
   // kernel overwrite the order) only once every CTA has read its item
   pdl_trigger();
@@ -2338,9 +2339,17 @@ sv_status launch_tc5(const TcParams &P0, cudaStream_t st) {
              P.tblk, P.ncta / P.H_kv, const_cast<int4 *>(P.work), P.seq_pre_w, P.split_w, P.status);
     grid = (unsigned)P.ncta;
   } else {
-    launch_k(attn_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, 1, P.seq_lens, P.B, P.S, P.H_kv, P.bps, P.n_new,
-             P.max_blocks, const_cast<int32_t *>(P.order));
     grid = (unsigned)(P.S * P.H_kv * P.B);
+    // Longest-first dispatch matters only when the CTAs take more than one
+    // wave of the slots (two per SM); a grid that fits runs all its CTAs at
+    // once, so it takes item = blockIdx.x and the order kernel (and its
+    // latency before the first tile) is left out.
+    if ((int64_t)grid <= 2 * (int64_t)num_sms()) {
+      P.order = nullptr;
+    } else {
+      launch_k(attn_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, 1, P.seq_lens, P.B, P.S, P.H_kv, P.bps, P.n_new,
+               P.max_blocks, const_cast<int32_t *>(P.order));
+    }
   }
   sv_status rc = check_launch("spec_verify_attn order launch");
   if (rc != SV_OK) return rc;
