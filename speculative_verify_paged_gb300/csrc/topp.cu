@@ -659,8 +659,10 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_row_kernel(const __grid_co
 // shared atomics, 1 to the bin's count and q = round(2^22 v) - 2^22 to its
 // offset sum, where v = w 2^(f/128) is the weight relative to the bin's
 // nominal one (|q| <= 11373, so V <= kTbMaxV keeps the sum inside int32).
-// v comes from one SFU exp2 of h + f/128, an exact difference of at most
-// 1/256, with the first-order correction for the rounding of the exponent.
+// v comes from one SFU exp2 of (x - m) c + f/128, at most 1/256 in
+// magnitude and formed with fmas that round only that small sum (the
+// product (x - m) c_hi is never rounded on its own), so the exponent's own
+// error is below 2^-31 and v's is the SFU's.
 // A bin's mass is then 2^(-f/128) (n_f + R_f 2^-22): each weight within
 // 2^-23 of its quantised value and about 2e-7 of its exact one. The masses
 // go to 2^-40 fixed point with a 64 x 64-bit product (2^(-j/128) in 2^-62
@@ -775,14 +777,17 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
     return;
   }
 
-  // bin = round(-128 h), h = (x - m) c_hi, from one fma onto the integer grid
-  // of [2^23, 2^24), capped at the last bin (which also takes -inf and NaN)
+  // bin = round(-128 d c_hi), d = x - m, from one fma onto the integer grid
+  // of [2^23, 2^24) (-128 c_hi is exact), capped at the last bin (which also
+  // takes -inf and NaN); h = d c_hi rounded, for the weights of the window's
+  // tokens
   const float c_hi = P.c_hi, c_lo = P.c_lo;
+  const float nc128 = -128.f * c_hi;
   const float top = 8388608.f + (float)(kTbBins - 1);
   auto bin_of = [&](float x, float &d, float &h, float &y) {
     d = __fsub_rn(x, m);
     h = __fmul_rn(d, c_hi);
-    y = fminf(fmaf(h, -128.f, 8388608.f), top);
+    y = fminf(fmaf(d, nc128, 8388608.f), top);
     return __float_as_int(y) - 0x4B000000;
   };
   // lo: the rounding of the exponent d c (fma for the product, two-sum for
@@ -809,16 +814,24 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
       const float x = TT::val(TT::get(r, k));
       float d, h, y;
       const int fb = bin_of(x, d, h, y);
-      {
-        // branch-free: the last bin (which also takes -inf and NaN) adds zeros
-        const bool in = fb < kTbBins - 1;
-        const float rr = fmaf(y - 8388608.f, 0.0078125f, h);   // h + fb / 128, exact
-        const float t = tp_ex2(rr);
-        const float v = fmaf(t, lo_of(x, d, h) * 0.693147180559945309f, t);
-        const int q = (int)__float_as_uint(fmaf(v, 4194304.f, 8388608.f)) - 0x4B400000;
-        atomicAdd(&cnt[fb], in ? 1u : 0u);
-        atomicAdd(&dsum[fb], in ? q : 0);
+      // the exponent against bin fb's nominal weight, (x - m) c + fb / 128,
+      // in [-1/256, 1/256]: d c_hi + fb / 128 from one fma (the exact sum
+      // rounded once, an error below 2^-32), then d c_lo and, where x - m
+      // is not exact in fp32, the part of it that d dropped
+      const float sf = fmaf(y, 0.0078125f, -65536.f);   // fb / 128, exact
+      float rr = fmaf(d, c_hi, sf);
+      rr = fmaf(d, c_lo, rr);
+      if (!TT::kExactDiff) {
+        const float bb = d - x;
+        const float d_lo = (x - (d - bb)) + (-m - bb);
+        rr = fmaf(d_lo, c_hi, rr);
       }
+      const float v = tp_ex2(rr);
+      const int q = (int)__float_as_uint(fmaf(v, 4194304.f, 8388608.f)) - 0x4B400000;
+      // the last bin (which also takes -inf and NaN) collects whatever its
+      // logits give, modulo 2^32; the scan counts it as empty
+      atomicAdd(&cnt[fb], 1u);
+      atomicAdd(reinterpret_cast<unsigned *>(&dsum[fb]), (unsigned)q);
     }
   });
   __syncthreads();
@@ -830,7 +843,7 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
 #pragma unroll
     for (int j = 0; j < kTbPer; ++j) {
       const int f = threadIdx.x * kTbPer + j;
-      const u64 N = (u64)((int64_t)cnt[f] * 4194304 + (int64_t)dsum[f]);
+      const u64 N = f == kTbBins - 1 ? 0ull : (u64)((int64_t)cnt[f] * 4194304 + (int64_t)dsum[f]);
       a[j] = tb_mulshift(P.base[f & 127], N, 44 + (f >> 7));
       part += a[j];
     }
