@@ -827,11 +827,13 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
         rr = fmaf(d_lo, c_hi, rr);
       }
       const float v = tp_ex2(rr);
-      const int q = (int)__float_as_uint(fmaf(v, 4194304.f, 8388608.f)) - 0x4B400000;
-      // the last bin (which also takes -inf and NaN) collects whatever its
-      // logits give, modulo 2^32; the scan counts it as empty
+      // 2^22 v + 2^23 rounded to an integer in [2^23, 2^24) has the bits
+      // 0x4B400000 + q: the bin sums those bits modulo 2^32, and the scan
+      // takes n_f 0x4B400000 back off. The last bin (which also takes -inf
+      // and NaN) collects whatever its logits give; the scan counts it as
+      // empty
       atomicAdd(&cnt[fb], 1u);
-      atomicAdd(reinterpret_cast<unsigned *>(&dsum[fb]), (unsigned)q);
+      atomicAdd(reinterpret_cast<unsigned *>(&dsum[fb]), __float_as_uint(fmaf(v, 4194304.f, 8388608.f)));
     }
   });
   __syncthreads();
@@ -843,7 +845,8 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
 #pragma unroll
     for (int j = 0; j < kTbPer; ++j) {
       const int f = threadIdx.x * kTbPer + j;
-      const u64 N = f == kTbBins - 1 ? 0ull : (u64)((int64_t)cnt[f] * 4194304 + (int64_t)dsum[f]);
+      const int sq = (int)((unsigned)dsum[f] - cnt[f] * 0x4B400000u);   // the offsets' sum (|.| < 2^31)
+      const u64 N = f == kTbBins - 1 ? 0ull : (u64)((int64_t)cnt[f] * 4194304 + (int64_t)sq);
       a[j] = tb_mulshift(P.base[f & 127], N, 44 + (f >> 7));
       part += a[j];
     }
