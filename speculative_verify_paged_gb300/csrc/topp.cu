@@ -63,6 +63,7 @@ constexpr int kTpBins = 2048;         // 64 binades of weight in steps of 1/32
 constexpr int kTpBinsPer = kTpBins / kTpThreads;
 constexpr int kTpCap = 512;           // candidates ranked directly
 constexpr int kTpUnroll = 4;          // 16-byte loads in flight per thread
+constexpr int kTpUnroll1 = 8;         // the same in the maximum passes and topp_bin_kernel's binning pass
 constexpr float kTpQuant = 1099511627776.0f;  // 2^40
 static_assert(kTpBinsPer * kTpThreads == kTpBins, "bins per thread");
 
@@ -218,10 +219,10 @@ __device__ __forceinline__ u64 tp_composite(uint32_t b, int id) {
 // Calls f(e0, r, nv) for every group of a row of V elements: r holds the
 // elements e0 .. e0 + nv - 1 packed as in memory (nv = G except in the last
 // group); the lanes of a short group past nv hold -inf. Full 16-byte groups go
-// round-robin over the threads, kTpUnroll loads in flight per thread; the
-// ragged end (and the whole row when it is not 16-byte aligned) is loaded one
-// element at a time.
-template <typename T, bool LAST = false, typename F>
+// round-robin over the threads, U loads in flight per thread; the ragged end
+// (and the whole row when it is not 16-byte aligned) is loaded one element at
+// a time.
+template <typename T, bool LAST = false, int U = kTpUnroll, typename F>
 __device__ __forceinline__ void tp_row_groups(const void *row, int V, int vec, F f) {
   using TT = TpType<T>;
   constexpr int G = TT::G;
@@ -230,12 +231,12 @@ __device__ __forceinline__ void tp_row_groups(const void *row, int V, int vec, F
   // LAST: the pass that reads the row for the last time loads it evict-first
   auto ld = [](const uint4 *p) { return LAST ? __ldcs(p) : __ldg(p); };
   int g = threadIdx.x;
-  for (; g + (kTpUnroll - 1) * kTpThreads < ng; g += kTpUnroll * kTpThreads) {
-    uint4 r[kTpUnroll];
+  for (; g + (U - 1) * kTpThreads < ng; g += U * kTpThreads) {
+    uint4 r[U];
 #pragma unroll
-    for (int u = 0; u < kTpUnroll; ++u) r[u] = ld(rv + g + u * kTpThreads);
+    for (int u = 0; u < U; ++u) r[u] = ld(rv + g + u * kTpThreads);
 #pragma unroll
-    for (int u = 0; u < kTpUnroll; ++u) f((g + u * kTpThreads) * G, r[u], G);
+    for (int u = 0; u < U; ++u) f((g + u * kTpThreads) * G, r[u], G);
   }
   for (; g < ng; g += kTpThreads) f(g * G, ld(rv + g), G);
   for (int h = ng + (int)threadIdx.x; h * G < V; h += kTpThreads) {
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_row_kernel(const __grid_co
 
   // ---- 1. row maximum (max ignores NaN; max.NaN propagates it, for the flag) ----
   uint32_t wmax = TT::kNegInfWord, wnan = TT::kNegInfWord;
-  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
+  tp_row_groups<T, false, kTpUnroll1>(in, V, P.vec, [&](int, const uint4 &r, int) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       wmax = TT::pmax(wmax, (&r.x)[j]);
@@ -737,7 +738,7 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
 
   // ---- 1. row maximum (max ignores NaN; max.NaN propagates it, for the flag) ----
   uint32_t wmax = TT::kNegInfWord, wnan = TT::kNegInfWord;
-  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
+  tp_row_groups<T, false, kTpUnroll1>(in, V, P.vec, [&](int, const uint4 &r, int) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       wmax = TT::pmax(wmax, (&r.x)[j]);
@@ -808,7 +809,7 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_bin_kernel(const __grid_co
   };
 
   // ---- 2. counts and quantised offsets per bin ----
-  tp_row_groups<T>(in, V, P.vec, [&](int, const uint4 &r, int) {
+  tp_row_groups<T, false, kTpUnroll1>(in, V, P.vec, [&](int, const uint4 &r, int) {
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       const float x = TT::val(TT::get(r, k));
