@@ -209,9 +209,9 @@ template <int QR, bool FP8> struct T5Cfg {
   static constexpr int kKTile = 2 * kKHalf;
   static constexpr int kVHalf = kT5Blk * 2048;               // a head-dim half of a 16-bit V stage
   static constexpr int kVTile = 2 * kVHalf;
-  static constexpr int kKS = FP8 ? (QR == 64 ? 4 : 3) : 3;   // K stages (raw for FP8)
-  static constexpr int kVS = FP8 ? (QR == 64 ? 6 : 4) : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
-  static constexpr int kCVS = FP8 ? 4 : 0;                   // widened V stages
+  static constexpr int kKS = 3;                              // K stages (raw for FP8)
+  static constexpr int kVS = FP8 ? 4 : (QR == 64 ? 5 : 3);   // V stages (raw for FP8)
+  static constexpr int kCVS = FP8 ? (QR == 64 ? 6 : 4) : 0;  // widened V stages
   static constexpr int kConvW = FP8 ? (QR == 64 ? 4 : 2) : 0;   // V converter warps
   static constexpr int kSoftW = FP8 && QR == 64 ? 2 : 4;     // warps in the softmax role
   static constexpr int kKRaw = FP8 ? kBlk * 2048 : kKTile;   // bytes of a K ring stage
